@@ -1,0 +1,203 @@
+"""Pins for the oracle's routing, dispatch, forward layer and combine (no GPU).
+
+Checks against closed forms, brute force over subsets, invariants and an
+independent dense formulation of the layer.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import inputs
+from oracle import formats as F
+from oracle import moe as M
+
+
+def _sig(v):
+    return 1.0 / (1.0 + math.exp(-v))
+
+
+# ---- SwiGLU closed forms --------------------------------------------------
+def test_swiglu_closed_forms():
+    assert M.act_fwd(0.0, 3.0) == 0.0
+    assert M.act_fwd(2.0, 0.0) == 0.0
+    assert M.act_fwd(1.0, 1.0) == pytest.approx(0.7310585786300049, abs=1e-15)   # sigmoid(1)
+    assert M.act_fwd(-1.0, 1.0) == pytest.approx(-0.2689414213699951, abs=1e-15)
+    assert M.act_fwd(2.0, 3.0) == pytest.approx(6.0 * _sig(2.0), rel=1e-15)
+    assert M.act_fwd(40.0, 0.5) == pytest.approx(20.0, rel=1e-15)                 # -> g*u
+    assert M.act_fwd(-40.0, 0.5) == pytest.approx(0.0, abs=1e-15)
+
+
+def test_swiglu_clamp_closed_forms():
+    kw = dict(act="swiglu_clamp", alpha=1.702, limit=7.0)
+    assert M.act_fwd(10.0, 10.0, **kw) == pytest.approx(49.0 * _sig(1.702 * 7.0), rel=1e-15)
+    assert M.act_fwd(-10.0, -10.0, **kw) == pytest.approx(-7.0 * _sig(-1.702 * 7.0) * -7.0, rel=1e-15)
+    assert M.act_fwd(1.0, 2.0, **kw) == pytest.approx(2.0 * _sig(1.702), rel=1e-15)
+    # gradient is zero beyond the clamp, nonzero inside
+    dg, du = M.act_bwd(np.array([8.0, 1.0]), np.array([1.0, -9.0]), 1.0, **kw)
+    assert dg[0] == 0.0 and du[1] == 0.0 and dg[1] != 0.0 and du[0] != 0.0
+
+
+def test_swiglu_derivative_closed_form():
+    # d/dg [g s(g) u] = u (s + g s (1 - s)); d/du = g s(g)
+    g, u = 0.7, -1.3
+    s = _sig(g)
+    dg, du = M.act_bwd(g, u, 1.0)
+    assert dg == pytest.approx(u * (s + g * s * (1 - s)), rel=1e-14)
+    assert du == pytest.approx(g * s, rel=1e-14)
+
+
+# ---- routing ---------------------------------------------------------------
+def test_topk_k1_is_argmax():
+    rng = np.random.default_rng(0)
+    lg = rng.normal(0, 1, (50, 16))
+    ids, w = M.topk_route(lg, 1, 2.5)
+    assert (ids[:, 0] == lg.argmax(1)).all()
+    assert (w == 2.5).all()
+
+
+def test_topk_kE_is_full_softmax():
+    rng = np.random.default_rng(1)
+    lg = rng.normal(0, 3, (20, 6))
+    ids, w = M.topk_route(lg, 6)
+    for t in range(20):
+        ex = [math.exp(v) for v in lg[t]]
+        tot = sum(ex)
+        for j in range(6):
+            assert w[t, j] == pytest.approx(ex[ids[t, j]] / tot, rel=1e-13)
+        assert list(ids[t]) == sorted(range(6), key=lambda e: -lg[t, e])
+
+
+def test_topk_brute_force_subsets_and_ties():
+    rng = np.random.default_rng(2)
+    for trial in range(200):
+        E, k = rng.integers(2, 7), None
+        k = int(rng.integers(1, E + 1))
+        lg = rng.integers(-3, 3, size=(1, E)).astype(np.float64)   # many ties
+        ids, _ = M.topk_route(lg, k)
+        best = None
+        for sub in itertools.combinations(range(E), k):
+            key = sorted(((-lg[0, e], e) for e in sub))
+            if best is None or key < best:
+                best = key
+        # the chosen set is the lexicographically best (value desc, id asc) subset, in order
+        assert [e for _, e in best] == list(ids[0])
+
+
+# ---- dispatch --------------------------------------------------------------
+@pytest.mark.parametrize("T,E,k,S", [(0, 4, 2, 0), (1, 8, 2, 0), (37, 8, 3, 0), (64, 33, 8, 1), (200, 5, 5, 0)])
+def test_dispatch_invariants(T, E, k, S):
+    rng = np.random.default_rng(T + E)
+    lg = rng.normal(0, 1, (T, E))
+    ids, w = M.topk_route(lg, k)
+    d = M.dispatch(ids, w, E, S)
+    kp, G = k + S, E + S
+    assert d.counts.sum() == T * kp
+    assert (np.diff(d.offsets) == d.counts).all() and d.offsets[0] == 0
+    assert sorted(d.perm_src.tolist()) == list(range(T * kp))          # bijection
+    assert (d.inv[d.perm_src] == np.arange(T * kp)).all()               # inv o perm = id
+    for e in range(G):
+        seg = d.perm_src[d.offsets[e]:d.offsets[e + 1]]
+        assert (np.diff(seg) > 0).all()                                 # token-major order
+        assert (d.expert[seg] == e).all()
+    if S:
+        assert d.counts[E] == T
+    for r in range(T * kp):
+        a = d.perm_src[r]
+        t, j = divmod(a, kp)
+        assert d.w_row[r] == (w[t, j] if j < k else 1.0)
+
+
+def test_combine_identity_experts():
+    """Identity experts: dispatch rows are the weighted token copies; combine
+    returns x * sum_j w_j exactly."""
+    rng = np.random.default_rng(7)
+    T, E, k, H = 40, 6, 3, 16
+    x = rng.normal(0, 1, (T, H))
+    ids, w = M.topk_route(rng.normal(0, 1, (T, E)), k)
+    d = M.dispatch(ids, w, E, 1)
+    kp = k + 1
+    z = np.stack([x[d.perm_src[r] // kp] * d.w_row[r] for r in range(T * kp)])
+    out = M.combine(z, d.inv, T, kp)
+    expect = x * (w.sum(1) + 1.0)[:, None]
+    assert np.allclose(out, expect, rtol=1e-15, atol=1e-15)
+
+
+# ---- forward layer ---------------------------------------------------------
+def _tiny_case(act="swiglu", wfmt="nvfp4", S=0, rs=1.0, T=16):
+    s = inputs.workload("tiny", T=T, n_shared=S, routed_scale=rs, act=act,
+                        alpha=1.702 if act != "swiglu" else 1.0,
+                        limit=7.0 if act != "swiglu" else 0.0, wfmt=wfmt)
+    x = inputs.gen_x(s, 0)
+    Wr = inputs.gen_router(s, 0)
+    wts = {k: v.numpy() for k, v in inputs.gen_expert_weights(s, 0).items()}
+    logits = (x.float() @ Wr).numpy()          # fp32 logits as the routing input
+    return s, inputs.bf16_bits(x).numpy(), logits, wts
+
+
+@pytest.mark.parametrize("act,wfmt,S,rs", [("swiglu", "nvfp4", 0, 1.0), ("swiglu", "nvfp4", 1, 2.5),
+                                          ("swiglu_clamp", "mxfp8", 0, 1.0)])
+def test_routed_equals_dense_formulation(act, wfmt, S, rs):
+    s, xb, lg, wts = _tiny_case(act, wfmt, S, rs)
+    kw = dict(E=s.E, k=s.k, n_shared=S, routed_scale=rs, act=s.act, alpha=s.alpha, limit=s.limit, wfmt=wfmt)
+    f = M.layer_forward(xb, lg, wts, **kw)
+    dense = M.dense_forward(xb, lg, wts, **kw)
+    assert np.allclose(f.out, dense, rtol=1e-12, atol=1e-12)
+    assert np.isfinite(f.out).all()
+
+
+def test_gemm_brute_force_triple_loop():
+    s, xb, lg, wts = _tiny_case(T=3)
+    f = M.layer_forward(xb, lg, wts, E=s.E, k=s.k, wfmt="nvfp4")
+    a = F.mx_dequantize(f.xq, f.xs)
+    kp = s.kp
+    for r in range(0, s.T * kp, 2):
+        e = f.disp.expert[f.disp.perm_src[r]]
+        t = f.disp.perm_src[r] // kp
+        W1 = M.expert_w1(wts, e, "nvfp4")
+        for n in (0, 5, s.I, 2 * s.I - 1):
+            acc = 0.0
+            for h in range(s.H):
+                acc += a[t, h] * W1[n, h]
+            assert f.h[r, n] == pytest.approx(acc, rel=1e-12, abs=1e-14)
+
+
+def test_one_hot_weights_are_exact():
+    """W1 rows that pick single inputs with power-of-two values reproduce the
+    dequantised activations exactly."""
+    s, xb, lg, wts = _tiny_case(T=8)
+    G, I, H = s.groups, s.I, s.H
+    w1 = np.zeros((G, 2 * I, H))
+    for n in range(2 * I):
+        w1[:, n, (3 * n) % H] = 2.0 ** ((n % 5) - 2)
+    wts2 = dict(wts, w1_f64=w1)
+    f = M.layer_forward(xb, lg, wts2, E=s.E, k=s.k)
+    a = F.mx_dequantize(f.xq, f.xs)
+    t = f.disp.perm_src // s.kp
+    for n in range(2 * I):
+        assert (f.h[:, n] == a[t, (3 * n) % H] * 2.0 ** ((n % 5) - 2)).all()
+
+
+def test_unrouted_expert_has_no_effect():
+    s, xb, lg, wts = _tiny_case(T=4)
+    f = M.layer_forward(xb, lg, wts, E=s.E, k=s.k)
+    empty = [e for e in range(s.E) if f.disp.counts[e] == 0]
+    assert empty, "tiny case should leave some expert empty at T=4"
+    wts2 = {k: v.copy() for k, v in wts.items()}
+    for e in empty:
+        wts2["w1_q"][e] ^= 0x77
+        wts2["w2_q"][e] ^= 0x11
+    f2 = M.layer_forward(xb, lg, wts2, E=s.E, k=s.k)
+    assert (f2.out == f.out).all()
+
+
+def test_row_subset_matches_full():
+    s, xb, lg, wts = _tiny_case()
+    kw = dict(E=s.E, k=s.k, wfmt="nvfp4")
+    full = M.layer_forward(xb, lg, wts, **kw)
+    rows = full.disp.inv[3 * s.kp:5 * s.kp]
+    part = M.layer_forward(xb, lg, wts, rows=rows, **kw)
+    assert (part.out[3:5] == full.out[3:5]).all()
+    assert np.isnan(part.out[0]).all()
