@@ -1,0 +1,279 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) routed Mixture-of-Experts layer.
+ *
+ * The layer (one GPU) runs, in order:
+ *   S1 router logits        logits = x . W_r (fp32)
+ *   S2 top-k routing        k experts per token, softmax over the selected
+ *                           logits, times routed_scale
+ *   S3/S4 dispatch          per-expert counts, exclusive offsets and a stable
+ *                           token-major permutation, all on the device; x is
+ *                           quantised to MXFP8 once per token
+ *   S5 grouped GEMM W1      h = a . W1_e, epilogue: SwiGLU, routing weight,
+ *                           MXFP8 requantisation of the result y1
+ *   S7 grouped GEMM W2      z = y1 . W2_e, bf16
+ *   S8 combine              out[t] = sum over the token's k' rows of z
+ *   S9 backward             dgrad with a fused dSwiGLU + quantise/transpose
+ *                           epilogue, wgrads, router gradient
+ * Sources: GC-MoE summary ("GC-MoE: Overlapping Expert-Parallel Token
+ * Dispatch with FP8/FP4 Grouped GEMM via CUDA Green Contexts"), Approach:
+ * role1 routing-count aggregation and token dispatch in BM blocks, role2
+ * W1 with SwiGLU / routing weight / requantisation fused in the epilogue then
+ * W2 emitting BF16 fragments, role3 combine; Developer notes: weights are
+ * prepacked once by the caller, one workspace instance serialises its calls
+ * (Limitations). NVIDIA blog "Boosting MoE training throughput with advanced
+ * fusion kernels": SwiGLU formula and the gate/up column repack (section on
+ * GLU epilogue fusion), per-group token counts kept in device memory so no
+ * host sync is needed (section on removing host-device sync), MXFP8
+ * quantisation with a transposed copy fused into the GEMM (section on
+ * MXFP8/NVFP4 quantisation fusion), GroupGemm + dActivation +
+ * Quantize/Transpose for the backward.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers marked "device" must point to device memory of the current
+ *   device; "host" pointers to host memory. Every device buffer is allocated
+ *   and owned by the caller. The library never allocates, frees or
+ *   synchronises inside the compute calls below (moe_read_status excepted),
+ *   so every compute call can be captured into a CUDA graph.
+ * - `stream` is a cudaStream_t passed as void*. All device work is enqueued on
+ *   it, in order; NULL means the legacy default stream.
+ * - Device pointers must be 16-byte aligned.
+ * - bf16 values are passed as their raw 16-bit patterns (uint16_t).
+ * - Matrices are row-major. "[R, C]" means R rows of C contiguous elements.
+ * - MXFP8 data: E4M3 element codes plus one E8M0 scale code per 32
+ *   consecutive elements along the contiguous axis: a matrix [R, C] has scales
+ *   [R, C/32]. The block exponent e is the smallest integer with
+ *   max|v| <= 448 * 2^e (clamped to [-127, 127]); elements are
+ *   round-to-nearest-even E4M3 of v / 2^e.
+ * - Notation: T tokens, H hidden, I expert FFN width, E routed experts,
+ *   k top-k, S = n_shared shared experts (width I, always on, weight 1),
+ *   k' = k + S slots per token, G = E + S expert groups, R = T * k' rows.
+ *   Row r of the grouped GEMMs belongs to group e when
+ *   offsets[e] <= r < offsets[e+1]; within a group rows keep increasing flat
+ *   assignment index a = t * k' + j (slot j < k: the j-th routed expert,
+ *   slots k..k'-1: the shared experts).
+ * - Errors found on the host (NULL pointers, bad shapes, T > T_max,
+ *   misalignment, workspace too small) return a status and enqueue nothing.
+ *   Errors only visible on the device (an expert id outside [0, E), a NaN
+ *   logit) set bits of a sticky status word inside the workspace and skip the
+ *   offending writes; read it with moe_read_status. No kernel traps.
+ * - One workspace must not be used by two calls that may run concurrently.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1, /* NULL pointer, bad shape or alignment        */
+    MOE_ERR_UNSUPPORTED = 2, /* valid request this build does not implement */
+    MOE_ERR_WORKSPACE = 3,   /* workspace or output buffer too small         */
+    MOE_ERR_CUDA = 4,        /* a CUDA runtime call failed                   */
+    MOE_ERR_DEVICE = 5       /* the device status word reports an error      */
+} moe_status_t;
+
+/* bits of the device status word */
+#define MOE_DEV_BAD_EXPERT_ID 0x1 /* routing id outside [0, E)              */
+#define MOE_DEV_NAN_LOGIT 0x2     /* NaN among a token's logits              */
+#define MOE_DEV_BAD_PACK 0x4      /* packed weight blob header mismatch      */
+
+enum { MOE_ACT_SWIGLU = 0, MOE_ACT_SWIGLU_CLAMP = 1 };
+enum { MOE_WFMT_NVFP4 = 0, MOE_WFMT_MXFP8 = 1 };
+enum { MOE_PACK_FORWARD = 0, MOE_PACK_DGRAD = 1 };
+
+/* Layer configuration (plain data, validated by moe_config_validate).
+ * act = MOE_ACT_SWIGLU:        act(g, u) = g * sigmoid(g) * u
+ * act = MOE_ACT_SWIGLU_CLAMP:  g' = clamp(g, -act_limit, act_limit),
+ *                              u' = clamp(u, -act_limit, act_limit),
+ *                              act = g' * sigmoid(act_alpha * g') * u'
+ * weight_fmt = MOE_WFMT_NVFP4: E2M1 elements, E4M3 scale per 16 along K,
+ *                              fp32 scale per (group, matrix)
+ * weight_fmt = MOE_WFMT_MXFP8: E4M3 elements, E8M0 scale per 32 along K */
+typedef struct moe_config {
+    int32_t H, I, E, k;
+    int32_t n_shared;     /* 0 or 1                                          */
+    int32_t T_max;        /* largest T any call with this config may pass    */
+    int32_t act;
+    float act_alpha;
+    float act_limit;
+    float routed_scale;   /* multiplies the renormalised routing weights     */
+    int32_t weight_fmt;
+    int32_t max_sms;      /* 0: use every SM; else cap the GEMM grids        */
+} moe_config_t;
+
+/* Unpacked expert weights (device pointers), one entry per group e < G, in
+ * the layout "one row per output feature, reduction axis contiguous":
+ *   which = MOE_PACK_FORWARD: W1 rows n < 2I (gate features then up
+ *     features), K = H; W2 rows n < H, K = I.
+ *   which = MOE_PACK_DGRAD (MXFP8 only, training): W1 copy with rows h < H,
+ *     K = 2I; W2 copy with rows i < I, K = H (quantised along that K).
+ * NVFP4: w*_q [G, N, K/2] bytes, element 2i in the low nibble of byte i;
+ *        w*_s [G, N, K/16] E4M3 codes; w*_gs [G] fp32.
+ * MXFP8: w*_q [G, N, K] E4M3 codes; w*_s [G, N, K/32] E8M0 codes;
+ *        w*_gs ignored (may be NULL). */
+typedef struct moe_weights_view {
+    const uint8_t* w1_q;
+    const uint8_t* w1_s;
+    const float* w1_gs;
+    const uint8_t* w2_q;
+    const uint8_t* w2_s;
+    const float* w2_gs;
+} moe_weights_view_t;
+
+/* Dispatch results (device pointers, caller-owned; see moe_workspace_view
+ * for a ready-made set inside a workspace). */
+typedef struct moe_dispatch {
+    int32_t* topk_ids;  /* [T, k]   expert ids, best first                    */
+    float* topk_w;      /* [T, k]   routing weights                           */
+    int32_t* counts;    /* [G]      rows per group                            */
+    int32_t* offsets;   /* [G + 1]  exclusive prefix sum of counts            */
+    int32_t* perm_src;  /* [R]      row r <- flat assignment t*k' + j         */
+    int32_t* inv;       /* [R]      flat assignment -> row                    */
+    float* w_row;       /* [R]      routing weight of row r (1 for shared)    */
+    uint8_t* xq;        /* [T, H]   MXFP8 codes of x (one copy per token)     */
+    uint8_t* xs;        /* [T, H/32] E8M0 scales of x                         */
+} moe_dispatch_t;
+
+/* Tensors the training forward saves for moe_layer_backward (device,
+ * caller-owned; sizes from moe_train_sizes). Pad rows: every group's rows are
+ * padded with zero rows to a multiple of 32; poff[e] is the padded offset. */
+typedef struct moe_train_save {
+    uint16_t* h;        /* [R, 2I] bf16 W1 output before the activation       */
+    uint8_t* y1t_q;     /* [I, R_pad] MXFP8 of y (activation x routing weight)
+                           quantised along the padded row axis               */
+    uint8_t* y1t_s;     /* [I, R_pad/32]                                      */
+    uint8_t* at_q;      /* [H, R_pad] MXFP8 of the gathered x rows, quantised
+                           along the padded row axis                          */
+    uint8_t* at_s;      /* [H, R_pad/32]                                      */
+    int32_t* poff;      /* [G + 1] padded row offsets                         */
+} moe_train_save_t;
+
+/* Pointers into a workspace (all device). */
+typedef struct moe_ws_view {
+    float* logits;      /* [T_max, E]                                         */
+    moe_dispatch_t d;   /* dispatch results                                   */
+    uint8_t* y1_q;      /* [R_max, I] MXFP8 codes of y1                       */
+    uint8_t* y1_s;      /* [R_max, I/32]                                      */
+    uint16_t* z;        /* [R_max, H] bf16 W2 output                          */
+    int32_t* status;    /* sticky device status word                          */
+} moe_ws_view_t;
+
+/* ---- configuration, sizes ---------------------------------------------- */
+
+/* Host only. MOE_OK if the config is supported: H, I multiples of 64,
+ * 1 <= k <= E, k' <= 32, G <= 2048, n_shared in {0, 1}, T_max >= 0. */
+moe_status_t moe_config_validate(const moe_config_t* cfg);
+
+/* Host only. Bytes of workspace for calls with T <= T_max (cfg->T_max). */
+moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
+
+/* Host only. Carves the named buffers out of a workspace of at least
+ * moe_workspace_size bytes at device address ws (no device access). */
+moe_status_t moe_workspace_view(const moe_config_t* cfg, void* ws, moe_ws_view_t* view);
+
+/* Host only. Bytes of the packed weight blob for `which`. */
+moe_status_t moe_packed_weights_size(const moe_config_t* cfg, int which, size_t* bytes);
+
+/* Host only. Sizes of the training save buffers for T tokens: R_pad upper
+ * bound (rows of the padded transposed copies). */
+moe_status_t moe_train_sizes(const moe_config_t* cfg, int T, int64_t* r_pad_max);
+
+/* ---- S0 weight prepack (once, at load time) ------------------------------ */
+
+/* Rearranges the unpacked weights `src` into the opaque blob `dst` (device,
+ * dst_bytes >= moe_packed_weights_size) used by the grouped GEMMs: per group,
+ * tiles of 128 output features (W1 tiles hold 64 gate and the matching 64 up
+ * features, so SwiGLU completes inside one tile), each tile stored as
+ * contiguous 64-wide K chunks carrying their scales. Source: GC-MoE summary,
+ * Developer notes (K128 prepacked FP4 weights, converted once by the caller)
+ * and the NVIDIA blog's gate/up column repack done at checkpoint load. */
+moe_status_t moe_prepack_weights(const moe_config_t* cfg, const moe_weights_view_t* src, int which,
+                                 void* dst, size_t dst_bytes, void* stream);
+
+/* ---- forward steps ------------------------------------------------------ */
+
+/* S1. logits [T, E] fp32 (device) = x [T, H] bf16 (device) . W_r [H, E] fp32
+ * (device), fp32 accumulation. ws: the workspace (holds split partials). */
+moe_status_t moe_router_logits(const moe_config_t* cfg, const uint16_t* x, const float* W_r, int T,
+                               float* logits, void* ws, void* stream);
+
+/* S2-S4. From logits [T, E] fp32 (device): top-k ids and weights, counts,
+ * offsets, permutation, inverse, row weights, and the MXFP8 copy of x
+ * [T, H] bf16 (device). Outputs in *d (device buffers). Bit-exact and
+ * deterministic: ties in the logits go to the lower expert id; rows of a
+ * group keep increasing t*k' + j. T = 0 writes zero counts and offsets. */
+moe_status_t moe_route_dispatch(const moe_config_t* cfg, const float* logits, const uint16_t* x, int T,
+                                const moe_dispatch_t* d, void* ws, void* stream);
+
+/* S2 alone: top-k ids [T, k] and weights [T, k] from logits (device). */
+moe_status_t moe_route_topk(const moe_config_t* cfg, const float* logits, int T, int32_t* topk_ids,
+                            float* topk_w, void* ws, void* stream);
+
+/* S3-S4 alone: dispatch from given top-k ids/weights (device) and x.
+ * d->topk_ids / d->topk_w are read, the other fields of *d written. */
+moe_status_t moe_dispatch(const moe_config_t* cfg, const uint16_t* x, int T, const moe_dispatch_t* d,
+                          void* ws, void* stream);
+
+/* S5-S6. Grouped W1 over the dispatched rows with the fused epilogue
+ * y1 = MXFP8(w_row * act(h[:, :I], h[:, I:])); y1_q [R, I], y1_s [R, I/32]
+ * (device). save (nullable): training tensors h, y1t, at, poff. */
+moe_status_t moe_grouped_gemm_w1_swiglu_quant(const moe_config_t* cfg, const moe_dispatch_t* d, int T,
+                                              const void* packed_w, uint8_t* y1_q, uint8_t* y1_s,
+                                              const moe_train_save_t* save, void* ws, void* stream);
+
+/* S7. Grouped W2: z [R, H] bf16 (device) = y1 . W2_e, fp32 accumulation. */
+moe_status_t moe_grouped_gemm_w2(const moe_config_t* cfg, const moe_dispatch_t* d, int T,
+                                 const uint8_t* y1_q, const uint8_t* y1_s, const void* packed_w,
+                                 uint16_t* z, void* ws, void* stream);
+
+/* S8. out [T, H] bf16 (device): out[t] = bf16(sum_j c_j * z[inv[t*k'+j]])
+ * summed in fp32 in slot order j = 0..k'-1, c_j = topk_w[t, j] for routed
+ * slots and 1 for shared slots when topk_w is non-NULL, else c_j = 1 (the
+ * routing weight was applied in the W1 epilogue). */
+moe_status_t moe_combine(const moe_config_t* cfg, const uint16_t* z, const int32_t* inv, const float* topk_w,
+                         int T, uint16_t* out, void* stream);
+
+/* Whole forward. Exactly one of W_r (router weights [H, E] fp32) and
+ * logits_in ([T, E] fp32) is non-NULL. out [T, H] bf16. save nullable
+ * (training). Intermediates live in ws (see moe_workspace_view). */
+moe_status_t moe_layer_forward(const moe_config_t* cfg, const uint16_t* x, const float* W_r,
+                               const float* logits_in, int T, const void* packed_w, uint16_t* out,
+                               const moe_train_save_t* save, void* ws, void* stream);
+
+/* ---- backward (MXFP8 weights, n_shared = 0) ------------------------------ */
+
+/* Gradients of L = sum(dout * out) for the forward that filled ws and save
+ * with the same T: dx [T, H] bf16 (expert path only), dW1 [E, H, 2I] bf16 in
+ * the logical W1 layout (gate columns then up columns), dW2 [E, I, H] bf16,
+ * dlogits [T, E] fp32. packed_w_dgrad: moe_prepack_weights(..., DGRAD, ...).
+ * The router's own dense GEMM gradients (dlogits . W_r^T, x^T . dlogits) are
+ * left to the caller. */
+moe_status_t moe_layer_backward(const moe_config_t* cfg, const uint16_t* dout, const uint16_t* x, int T,
+                                const moe_train_save_t* save, const void* packed_w_dgrad, uint16_t* dx,
+                                uint16_t* dW1, uint16_t* dW2, float* dlogits, void* ws, void* stream);
+
+/* ---- status --------------------------------------------------------------- */
+
+/* Synchronises `stream`, copies the workspace status word to *out (host) and
+ * clears it. Not for use inside graph capture. */
+moe_status_t moe_read_status(const moe_config_t* cfg, void* ws, int32_t* out, void* stream);
+
+/* Clears the workspace status word (enqueued on stream; capturable). */
+moe_status_t moe_clear_status(const moe_config_t* cfg, void* ws, void* stream);
+
+/* Static description of a status code. */
+const char* moe_status_string(moe_status_t s);
+
+/* Number of kernels the last host call enqueued (for launch accounting). */
+int moe_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_GB300_H */

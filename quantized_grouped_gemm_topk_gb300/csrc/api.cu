@@ -1,0 +1,650 @@
+// C ABI of the routed-MoE layer: argument checks, workspace carving, and the
+// launch sequence of each step. No allocation, no host sync (except
+// moe_read_status): every call only enqueues kernels / async copies on the
+// caller's stream.
+#include <cstring>
+
+#include "internal.cuh"
+
+namespace moe {
+
+static thread_local int g_launches = 0;
+void note_launch() { ++g_launches; }
+void reset_launch_count() { g_launches = 0; }
+int launch_count() { return g_launches; }
+
+static inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Dims {
+  int H, I, E, k, S, kp, G, Tmax;
+  int64_t Rmax, RpMax;
+};
+
+static Dims dims_of(const moe_config_t& c) {
+  Dims d;
+  d.H = c.H; d.I = c.I; d.E = c.E; d.k = c.k; d.S = c.n_shared;
+  d.kp = c.k + c.n_shared; d.G = c.E + c.n_shared; d.Tmax = c.T_max;
+  d.Rmax = (int64_t)c.T_max * d.kp;
+  d.RpMax = (int64_t)align_up((size_t)(d.Rmax + 31LL * d.G), 32);
+  return d;
+}
+
+static int64_t r_pad_for(const Dims& d, int T) {
+  return (int64_t)align_up((size_t)((int64_t)T * d.kp + 31LL * d.G), 32);
+}
+
+static bool backward_capable(const moe_config_t& c) {
+  return c.weight_fmt == MOE_WFMT_MXFP8 && c.n_shared == 0;
+}
+
+// ---- workspace layout -------------------------------------------------------
+struct WsLayout {
+  size_t status, logits, rpart, ids, wts, counts, offsets, touched, ntouch, poff, hist, base;
+  size_t perm, inv, wrow, xq, xs, y1q, y1s, z, P;
+  size_t ysave, dzq, dzs, dztq, dzts, dwrow, dhq, dhs, dh, dhtq, dhts;
+  size_t total;
+};
+
+static WsLayout ws_layout(const moe_config_t& c) {
+  const Dims d = dims_of(c);
+  WsLayout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + std::max<size_t>(bytes, 1), 256); return at; };
+  const int64_t T = d.Tmax, R = d.Rmax;
+  const int NB = (int)((T + kTokBlk - 1) / kTokBlk);
+  const int64_t rpart_rows = std::max<int64_t>(4096, T);     // KS * T <= max(4096, T)
+  L.status = take(256);
+  L.logits = take((size_t)T * d.E * 4);
+  L.rpart = take((size_t)rpart_rows * d.E * 4);
+  L.ids = take((size_t)T * d.k * 4);
+  L.wts = take((size_t)T * d.k * 4);
+  L.counts = take((size_t)d.G * 4);
+  L.offsets = take((size_t)(d.G + 1) * 4);
+  L.touched = take((size_t)d.G * 4);
+  L.ntouch = take(4);
+  L.poff = take((size_t)(d.G + 1) * 4);
+  L.hist = take((size_t)NB * d.G * 4);
+  L.base = take((size_t)NB * d.G * 4);
+  L.perm = take((size_t)R * 4);
+  L.inv = take((size_t)R * 4);
+  L.wrow = take((size_t)R * 4);
+  L.xq = take((size_t)T * d.H);
+  L.xs = take((size_t)T * d.H / 32);
+  L.y1q = take((size_t)R * d.I);
+  L.y1s = take((size_t)R * d.I / 32);
+  L.z = take((size_t)R * d.H * 2);
+  L.P = take((size_t)R * std::max(2 * d.I, d.H) * 4);
+  if (backward_capable(c)) {
+    L.ysave = take((size_t)R * d.I * 4);
+    L.dzq = take((size_t)T * d.H);
+    L.dzs = take((size_t)T * d.H / 32);
+    L.dztq = take((size_t)d.H * d.RpMax);
+    L.dzts = take((size_t)d.H * d.RpMax / 32);
+    L.dwrow = take((size_t)R * 4);
+    L.dhq = take((size_t)R * 2 * d.I);
+    L.dhs = take((size_t)R * 2 * d.I / 32);
+    L.dh = take((size_t)R * 2 * d.I * 4);
+    L.dhtq = take((size_t)2 * d.I * d.RpMax);
+    L.dhts = take((size_t)2 * d.I * d.RpMax / 32);
+  } else {
+    L.ysave = L.dzq = L.dzs = L.dztq = L.dzts = L.dwrow = L.dhq = L.dhs = L.dh = L.dhtq = L.dhts = 0;
+  }
+  L.total = o;
+  return L;
+}
+
+template <typename Tp>
+static Tp* at(void* ws, size_t off) { return reinterpret_cast<Tp*>(reinterpret_cast<uint8_t*>(ws) + off); }
+
+// ---- packed weights layout ------------------------------------------------------
+struct PackLayout {
+  int fmt, G;
+  int N1, K1, N2, K2, il1;
+  int tiles1, tiles2;
+  int64_t tile_bytes1, tile_bytes2;
+  size_t off_gs1, off_gs2, off_w1, off_w2, total;
+};
+
+static PackLayout pack_layout(const moe_config_t& c, int which) {
+  PackLayout P;
+  P.fmt = c.weight_fmt;
+  P.G = c.E + c.n_shared;
+  if (which == MOE_PACK_FORWARD) {
+    P.N1 = 2 * c.I; P.K1 = c.H; P.il1 = c.I;
+    P.N2 = c.H; P.K2 = c.I;
+  } else {
+    P.N1 = c.H; P.K1 = 2 * c.I; P.il1 = 0;
+    P.N2 = c.I; P.K2 = c.H;
+  }
+  const int CB = chunk_bytes(P.fmt);
+  P.tiles1 = (P.N1 + kTileN - 1) / kTileN;
+  P.tiles2 = (P.N2 + kTileN - 1) / kTileN;
+  P.tile_bytes1 = (int64_t)(P.K1 / kChunkK) * CB;
+  P.tile_bytes2 = (int64_t)(P.K2 / kChunkK) * CB;
+  size_t o = 256;
+  P.off_gs1 = o; o = align_up(o + (size_t)P.G * 4, 256);
+  P.off_gs2 = o; o = align_up(o + (size_t)P.G * 4, 256);
+  P.off_w1 = o; o = align_up(o + (size_t)P.G * P.tiles1 * P.tile_bytes1, 256);
+  P.off_w2 = o; o = align_up(o + (size_t)P.G * P.tiles2 * P.tile_bytes2, 256);
+  P.total = o;
+  return P;
+}
+
+__global__ void k_write_header(PackHeader h, uint8_t* dst) { *reinterpret_cast<PackHeader*>(dst) = h; }
+
+__global__ void k_fill_f32(float* p, int n, float v) {
+  int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n) p[i] = v;
+}
+
+__global__ void k_reduce_partials(const float* part, int KS, int64_t n, float* out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    float v = part[i];
+    for (int ks = 1; ks < KS; ++ks) v += part[(int64_t)ks * n + i];
+    out[i] = v;
+  }
+}
+
+static int num_sms() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+  }
+  return n;
+}
+
+static int gemm_ctas(const moe_config_t& c) {
+  int sms = num_sms();
+  if (c.max_sms > 0) sms = std::min(sms, c.max_sms);
+  return sms * 8;
+}
+
+// K slices for a grouped GEMM: enough units for ~2 waves, limited by the
+// partial buffer (S * R <= Rmax) and by the number of K chunks.
+static int gemm_splits(const moe_config_t& c, int T, int tiles, int K) {
+  const Dims d = dims_of(c);
+  const double touched = c.E * (1.0 - std::pow(1.0 - (double)c.k / c.E, (double)T)) + c.n_shared;
+  const double units = std::max(1.0, touched) * tiles;
+  int S = (int)std::ceil(2.0 * gemm_ctas(c) / units);
+  const int64_t R = (int64_t)T * d.kp;
+  S = std::min<int64_t>(S, std::max<int64_t>(1, d.Rmax / std::max<int64_t>(R, 1)));
+  S = std::max(1, std::min(S, K / kChunkK));
+  return S;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+#define MOE_CHECK_CUDA(x)                        \
+  do {                                           \
+    cudaError_t _e = (x);                        \
+    if (_e != cudaSuccess) return MOE_ERR_CUDA;  \
+  } while (0)
+
+static inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+#define REQ(p) do { if (!(p) || !aligned16(p)) return MOE_ERR_INVALID_ARG; } while (0)
+#define OPT(p) do { if ((p) && !aligned16(p)) return MOE_ERR_INVALID_ARG; } while (0)
+// buffers whose size scales with T may be NULL when T == 0
+#define REQ_T(p) do { if (T > 0) REQ(p); else OPT(p); } while (0)
+
+extern "C" {
+
+moe_status_t moe_config_validate(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->H <= 0 || c->I <= 0 || c->H % 64 || c->I % 64) return MOE_ERR_INVALID_ARG;
+  if (c->E <= 0 || c->k < 1 || c->k > c->E) return MOE_ERR_INVALID_ARG;
+  if (c->n_shared < 0 || c->n_shared > 1) return MOE_ERR_INVALID_ARG;
+  if (c->k + c->n_shared > 32 || c->E + c->n_shared > 2048) return MOE_ERR_INVALID_ARG;
+  if (c->T_max < 0) return MOE_ERR_INVALID_ARG;
+  if (c->act != MOE_ACT_SWIGLU && c->act != MOE_ACT_SWIGLU_CLAMP) return MOE_ERR_INVALID_ARG;
+  if (c->act == MOE_ACT_SWIGLU_CLAMP && !(c->act_limit > 0.f)) return MOE_ERR_INVALID_ARG;
+  if (c->weight_fmt != MOE_WFMT_NVFP4 && c->weight_fmt != MOE_WFMT_MXFP8) return MOE_ERR_INVALID_ARG;
+  if (!(c->routed_scale > 0.f)) return MOE_ERR_INVALID_ARG;
+  if (c->max_sms < 0) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_size(const moe_config_t* c, size_t* bytes) {
+  moe_status_t s = moe_config_validate(c);
+  if (s != MOE_OK) return s;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = ws_layout(*c).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_view(const moe_config_t* c, void* ws, moe_ws_view_t* v) {
+  moe_status_t s = moe_config_validate(c);
+  if (s != MOE_OK) return s;
+  if (!v) return MOE_ERR_INVALID_ARG;
+  REQ(ws);
+  const WsLayout L = ws_layout(*c);
+  v->logits = at<float>(ws, L.logits);
+  v->d.topk_ids = at<int32_t>(ws, L.ids);
+  v->d.topk_w = at<float>(ws, L.wts);
+  v->d.counts = at<int32_t>(ws, L.counts);
+  v->d.offsets = at<int32_t>(ws, L.offsets);
+  v->d.perm_src = at<int32_t>(ws, L.perm);
+  v->d.inv = at<int32_t>(ws, L.inv);
+  v->d.w_row = at<float>(ws, L.wrow);
+  v->d.xq = at<uint8_t>(ws, L.xq);
+  v->d.xs = at<uint8_t>(ws, L.xs);
+  v->y1_q = at<uint8_t>(ws, L.y1q);
+  v->y1_s = at<uint8_t>(ws, L.y1s);
+  v->z = at<uint16_t>(ws, L.z);
+  v->status = at<int32_t>(ws, L.status);
+  return MOE_OK;
+}
+
+moe_status_t moe_packed_weights_size(const moe_config_t* c, int which, size_t* bytes) {
+  moe_status_t s = moe_config_validate(c);
+  if (s != MOE_OK) return s;
+  if (!bytes || (which != MOE_PACK_FORWARD && which != MOE_PACK_DGRAD)) return MOE_ERR_INVALID_ARG;
+  if (which == MOE_PACK_DGRAD && c->weight_fmt != MOE_WFMT_MXFP8) return MOE_ERR_UNSUPPORTED;
+  *bytes = pack_layout(*c, which).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_train_sizes(const moe_config_t* c, int T, int64_t* r_pad_max) {
+  moe_status_t s = moe_config_validate(c);
+  if (s != MOE_OK) return s;
+  if (!r_pad_max || T < 0 || T > c->T_max) return MOE_ERR_INVALID_ARG;
+  *r_pad_max = r_pad_for(dims_of(*c), T);
+  return MOE_OK;
+}
+
+moe_status_t moe_prepack_weights(const moe_config_t* c, const moe_weights_view_t* src, int which, void* dst,
+                                 size_t dst_bytes, void* stream) {
+  moe_status_t s = moe_config_validate(c);
+  if (s != MOE_OK) return s;
+  if (!src || (which != MOE_PACK_FORWARD && which != MOE_PACK_DGRAD)) return MOE_ERR_INVALID_ARG;
+  if (which == MOE_PACK_DGRAD && c->weight_fmt != MOE_WFMT_MXFP8) return MOE_ERR_UNSUPPORTED;
+  REQ(dst); REQ(src->w1_q); REQ(src->w1_s); REQ(src->w2_q); REQ(src->w2_s);
+  if (c->weight_fmt == MOE_WFMT_NVFP4) { REQ(src->w1_gs); REQ(src->w2_gs); }
+  const PackLayout P = pack_layout(*c, which);
+  if (dst_bytes < P.total) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = (cudaStream_t)stream;
+  reset_launch_count();
+  uint8_t* d8 = reinterpret_cast<uint8_t*>(dst);
+  PackHeader h;
+  std::memset(&h, 0, sizeof(h));
+  h.magic = kPackMagic; h.version = kPackVersion; h.fmt = P.fmt; h.which = which; h.G = P.G;
+  h.N1 = P.N1; h.K1 = P.K1; h.N2 = P.N2; h.K2 = P.K2; h.interleave1 = P.il1 > 0;
+  h.off_gs1 = P.off_gs1; h.off_gs2 = P.off_gs2; h.off_w1 = P.off_w1; h.off_w2 = P.off_w2;
+  h.tile_bytes1 = P.tile_bytes1; h.tile_bytes2 = P.tile_bytes2; h.tiles1 = P.tiles1; h.tiles2 = P.tiles2;
+  k_write_header<<<1, 1, 0, st>>>(h, d8);
+  note_launch();
+  if (c->weight_fmt == MOE_WFMT_NVFP4) {
+    MOE_CHECK_CUDA(cudaMemcpyAsync(d8 + P.off_gs1, src->w1_gs, (size_t)P.G * 4, cudaMemcpyDeviceToDevice, st));
+    MOE_CHECK_CUDA(cudaMemcpyAsync(d8 + P.off_gs2, src->w2_gs, (size_t)P.G * 4, cudaMemcpyDeviceToDevice, st));
+  } else {
+    k_fill_f32<<<(P.G + 255) / 256, 256, 0, st>>>(reinterpret_cast<float*>(d8 + P.off_gs1), P.G, 1.0f);
+    k_fill_f32<<<(P.G + 255) / 256, 256, 0, st>>>(reinterpret_cast<float*>(d8 + P.off_gs2), P.G, 1.0f);
+    note_launch(); note_launch();
+  }
+  MOE_CHECK_CUDA(launch_prepack(src->w1_q, src->w1_s, P.G, P.N1, P.K1, P.fmt, P.il1, P.tiles1, P.tile_bytes1,
+                                d8 + P.off_w1, st));
+  MOE_CHECK_CUDA(launch_prepack(src->w2_q, src->w2_s, P.G, P.N2, P.K2, P.fmt, 0, P.tiles2, P.tile_bytes2,
+                                d8 + P.off_w2, st));
+  return MOE_OK;
+}
+
+static moe_status_t check_T(const moe_config_t* c, int T) {
+  moe_status_t s = moe_config_validate(c);
+  if (s != MOE_OK) return s;
+  if (T < 0 || T > c->T_max) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status_t moe_router_logits(const moe_config_t* c, const uint16_t* x, const float* W_r, int T, float* logits,
+                               void* ws, void* stream) {
+  moe_status_t s = check_T(c, T);
+  if (s != MOE_OK) return s;
+  REQ_T(x); REQ(W_r); REQ_T(logits); REQ(ws);
+  cudaStream_t st = (cudaStream_t)stream;
+  reset_launch_count();
+  const WsLayout L = ws_layout(*c);
+  const int KS = router_splits(T, c->H);
+  if (KS == 1) {
+    MOE_CHECK_CUDA(launch_router(x, W_r, T, c->H, c->E, 1, logits, st));
+    return MOE_OK;
+  }
+  float* part = at<float>(ws, L.rpart);
+  MOE_CHECK_CUDA(launch_router(x, W_r, T, c->H, c->E, KS, part, st));
+  if (T > 0) {
+    const int64_t n = (int64_t)T * c->E;
+    k_reduce_partials<<<(int)std::min<int64_t>((n + 255) / 256, 4096), 256, 0, st>>>(part, KS, n, logits);
+    note_launch();
+    MOE_CHECK_CUDA(cudaGetLastError());
+  }
+  return MOE_OK;
+}
+
+static RouteArgs route_args(const moe_config_t* c, int T, const moe_dispatch_t* d, void* ws, const WsLayout& L) {
+  RouteArgs a;
+  a.T = T; a.H = c->H; a.E = c->E; a.k = c->k; a.S = c->n_shared; a.rs = c->routed_scale;
+  a.route = true; a.part = nullptr; a.KS = 1; a.logits = nullptr;
+  a.ids = d->topk_ids; a.wts = d->topk_w; a.counts = d->counts; a.offsets = d->offsets;
+  a.touched = at<int32_t>(ws, L.touched); a.n_touched = at<int32_t>(ws, L.ntouch); a.poff = at<int32_t>(ws, L.poff);
+  a.hist = at<int32_t>(ws, L.hist); a.base = at<int32_t>(ws, L.base);
+  a.perm = d->perm_src; a.inv = d->inv; a.w_row = d->w_row;
+  a.x = nullptr; a.xq = d->xq; a.xs = d->xs;
+  a.status = at<int32_t>(ws, L.status);
+  return a;
+}
+
+static moe_status_t check_dispatch(const moe_dispatch_t* d, bool need_x, int T) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  REQ_T(d->topk_ids); REQ_T(d->topk_w); REQ(d->counts); REQ(d->offsets); REQ_T(d->perm_src); REQ_T(d->inv);
+  REQ_T(d->w_row);
+  if (need_x) { REQ_T(d->xq); REQ_T(d->xs); }
+  return MOE_OK;
+}
+
+moe_status_t moe_route_topk(const moe_config_t* c, const float* logits, int T, int32_t* ids, float* w, void* ws,
+                            void* stream) {
+  moe_status_t s = check_T(c, T);
+  if (s != MOE_OK) return s;
+  REQ_T(logits); REQ_T(ids); REQ_T(w); REQ(ws);
+  reset_launch_count();
+  const WsLayout L = ws_layout(*c);
+  MOE_CHECK_CUDA(launch_topk_only(logits, T, c->E, c->k, c->routed_scale, ids, w, at<int32_t>(ws, L.status),
+                                  (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_route_dispatch(const moe_config_t* c, const float* logits, const uint16_t* x, int T,
+                                const moe_dispatch_t* d, void* ws, void* stream) {
+  moe_status_t s = check_T(c, T);
+  if (s != MOE_OK) return s;
+  REQ_T(logits); REQ_T(x); REQ(ws);
+  if ((s = check_dispatch(d, true, T)) != MOE_OK) return s;
+  reset_launch_count();
+  const WsLayout L = ws_layout(*c);
+  RouteArgs a = route_args(c, T, d, ws, L);
+  a.part = logits; a.KS = 1; a.logits = const_cast<float*>(logits); a.x = x;
+  MOE_CHECK_CUDA(launch_route_dispatch(a, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_dispatch(const moe_config_t* c, const uint16_t* x, int T, const moe_dispatch_t* d, void* ws,
+                          void* stream) {
+  moe_status_t s = check_T(c, T);
+  if (s != MOE_OK) return s;
+  REQ_T(x); REQ(ws);
+  if ((s = check_dispatch(d, true, T)) != MOE_OK) return s;
+  reset_launch_count();
+  const WsLayout L = ws_layout(*c);
+  RouteArgs a = route_args(c, T, d, ws, L);
+  a.route = false; a.x = x;
+  MOE_CHECK_CUDA(launch_route_dispatch(a, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+static GemmArgs gemm_args(const moe_config_t* c, const PackLayout& P, int which_mat, const void* packed, void* ws,
+                          const WsLayout& L, const int32_t* offsets, int T) {
+  GemmArgs g;
+  const uint8_t* b = reinterpret_cast<const uint8_t*>(packed);
+  if (which_mat == 1) {
+    g.w = b + P.off_w1; g.gs = reinterpret_cast<const float*>(b + P.off_gs1);
+    g.tile_bytes = P.tile_bytes1; g.tiles = P.tiles1; g.N = P.N1; g.K = P.K1; g.interleave_I = P.il1;
+  } else {
+    g.w = b + P.off_w2; g.gs = reinterpret_cast<const float*>(b + P.off_gs2);
+    g.tile_bytes = P.tile_bytes2; g.tiles = P.tiles2; g.N = P.N2; g.K = P.K2; g.interleave_I = 0;
+  }
+  g.fmt = P.fmt;
+  g.offsets = offsets;
+  g.touched = at<int32_t>(ws, L.touched);
+  g.n_touched = at<int32_t>(ws, L.ntouch);
+  g.aq = nullptr; g.as = nullptr; g.row_map = nullptr; g.row_div = 1;
+  g.out = at<float>(ws, L.P);
+  const int64_t R = (int64_t)T * (c->k + c->n_shared);
+  g.split_stride = R * g.N;
+  g.S = gemm_splits(*c, T, g.tiles, g.K);
+  g.max_ctas = gemm_ctas(*c);
+  return g;
+}
+
+static ActParams act_params(const moe_config_t* c) {
+  ActParams p;
+  p.act = c->act;
+  p.alpha = c->act == MOE_ACT_SWIGLU ? 1.f : c->act_alpha;
+  p.limit = c->act_limit;
+  return p;
+}
+
+static moe_status_t w1_impl(const moe_config_t* c, const moe_dispatch_t* d, int T, const void* packed, uint8_t* y1q,
+                            uint8_t* y1s, const moe_train_save_t* save, void* ws, cudaStream_t st,
+                            float* y_save_override) {
+  const WsLayout L = ws_layout(*c);
+  const PackLayout P = pack_layout(*c, MOE_PACK_FORWARD);
+  const int kp = c->k + c->n_shared, G = c->E + c->n_shared;
+  const int R = T * kp;
+  if (T == 0) return MOE_OK;
+  GemmArgs g = gemm_args(c, P, 1, packed, ws, L, d->offsets, T);
+  g.aq = d->xq; g.as = d->xs; g.row_map = d->perm_src; g.row_div = kp;
+  MOE_CHECK_CUDA(launch_gemm_cc(g, st));
+  W1FinArgs f;
+  f.P = g.out; f.S = g.S; f.split_stride = g.split_stride; f.R = R; f.I = c->I;
+  f.offsets = d->offsets; f.G = G; f.w_row = d->w_row; f.act = act_params(c);
+  f.y1q = y1q; f.y1s = y1s;
+  f.h_save = save ? save->h : nullptr;
+  f.y_save = save ? (y_save_override ? y_save_override : at<float>(ws, L.ysave)) : nullptr;
+  MOE_CHECK_CUDA(launch_w1_finalize(f, st));
+  if (save) {
+    const Dims dm = dims_of(*c);
+    ColQuantArgs q;
+    q.src16 = nullptr; q.row_map = nullptr; q.row_div = 1; q.src32 = f.y_save;
+    q.C = c->I; q.offsets = d->offsets; q.poff = at<int32_t>(ws, L.poff); q.G = G;
+    q.r_pad_max = r_pad_for(dm, T); q.q = save->y1t_q; q.s = save->y1t_s;
+    MOE_CHECK_CUDA(launch_quant_cols(q, st));
+    MOE_CHECK_CUDA(cudaMemcpyAsync(save->poff, at<int32_t>(ws, L.poff), (size_t)(G + 1) * 4,
+                                   cudaMemcpyDeviceToDevice, st));
+  }
+  return MOE_OK;
+}
+
+static moe_status_t check_save(const moe_config_t* c, const moe_train_save_t* save) {
+  if (!save) return MOE_OK;
+  if (!backward_capable(*c)) return MOE_ERR_UNSUPPORTED;
+  REQ(save->h); REQ(save->y1t_q); REQ(save->y1t_s); REQ(save->at_q); REQ(save->at_s); REQ(save->poff);
+  return MOE_OK;
+}
+
+moe_status_t moe_grouped_gemm_w1_swiglu_quant(const moe_config_t* c, const moe_dispatch_t* d, int T,
+                                              const void* packed_w, uint8_t* y1_q, uint8_t* y1_s,
+                                              const moe_train_save_t* save, void* ws, void* stream) {
+  moe_status_t s = check_T(c, T);
+  if (s != MOE_OK) return s;
+  if ((s = check_dispatch(d, true, T)) != MOE_OK) return s;
+  REQ(packed_w); REQ_T(y1_q); REQ_T(y1_s); REQ(ws);
+  if ((s = check_save(c, save)) != MOE_OK) return s;
+  reset_launch_count();
+  return w1_impl(c, d, T, packed_w, y1_q, y1_s, save, ws, (cudaStream_t)stream, nullptr);
+}
+
+moe_status_t moe_grouped_gemm_w2(const moe_config_t* c, const moe_dispatch_t* d, int T, const uint8_t* y1_q,
+                                 const uint8_t* y1_s, const void* packed_w, uint16_t* z, void* ws, void* stream) {
+  moe_status_t s = check_T(c, T);
+  if (s != MOE_OK) return s;
+  if ((s = check_dispatch(d, false, T)) != MOE_OK) return s;
+  REQ_T(y1_q); REQ_T(y1_s); REQ(packed_w); REQ_T(z); REQ(ws);
+  reset_launch_count();
+  if (T == 0) return MOE_OK;
+  cudaStream_t st = (cudaStream_t)stream;
+  const WsLayout L = ws_layout(*c);
+  const PackLayout P = pack_layout(*c, MOE_PACK_FORWARD);
+  GemmArgs g = gemm_args(c, P, 2, packed_w, ws, L, d->offsets, T);
+  g.aq = y1_q; g.as = y1_s;
+  MOE_CHECK_CUDA(launch_gemm_cc(g, st));
+  MOE_CHECK_CUDA(launch_finalize_rows(g.out, g.S, g.split_stride, c->H, T * (c->k + c->n_shared), z, st));
+  return MOE_OK;
+}
+
+moe_status_t moe_combine(const moe_config_t* c, const uint16_t* z, const int32_t* inv, const float* topk_w, int T,
+                         uint16_t* out, void* stream) {
+  moe_status_t s = check_T(c, T);
+  if (s != MOE_OK) return s;
+  REQ_T(z); REQ_T(inv); OPT(topk_w); REQ_T(out);
+  reset_launch_count();
+  MOE_CHECK_CUDA(launch_combine(z, inv, topk_w, T, c->k, c->k + c->n_shared, c->H, out, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const float* W_r, const float* logits_in,
+                               int T, const void* packed_w, uint16_t* out, const moe_train_save_t* save, void* ws,
+                               void* stream) {
+  moe_status_t s = check_T(c, T);
+  if (s != MOE_OK) return s;
+  if (W_r && logits_in) return MOE_ERR_INVALID_ARG;
+  if (!W_r && !logits_in && T > 0) return MOE_ERR_INVALID_ARG;
+  REQ_T(x); OPT(W_r); OPT(logits_in); REQ(packed_w); REQ_T(out); REQ(ws);
+  if ((s = check_save(c, save)) != MOE_OK) return s;
+  reset_launch_count();
+  cudaStream_t st = (cudaStream_t)stream;
+  const WsLayout L = ws_layout(*c);
+  moe_ws_view_t v;
+  moe_workspace_view(c, ws, &v);
+  const int kp = c->k + c->n_shared, G = c->E + c->n_shared;
+  RouteArgs a = route_args(c, T, &v.d, ws, L);
+  a.x = x;
+  a.logits = v.logits;
+  if (W_r) {
+    const int KS = router_splits(T, c->H);
+    float* part = KS == 1 ? v.logits : at<float>(ws, L.rpart);
+    MOE_CHECK_CUDA(launch_router(x, W_r, T, c->H, c->E, KS, part, st));
+    a.part = part; a.KS = KS;
+  } else {
+    a.part = logits_in; a.KS = 1;
+  }
+  MOE_CHECK_CUDA(launch_route_dispatch(a, st));
+  if (T == 0) return MOE_OK;
+  if (save) {
+    // transposed MXFP8 copy of the gathered activations for the W1 wgrad
+    ColQuantArgs q;
+    q.src16 = x; q.row_map = v.d.perm_src; q.row_div = kp; q.src32 = nullptr;
+    q.C = c->H; q.offsets = v.d.offsets; q.poff = at<int32_t>(ws, L.poff); q.G = G;
+    q.r_pad_max = r_pad_for(dims_of(*c), T); q.q = save->at_q; q.s = save->at_s;
+    MOE_CHECK_CUDA(launch_quant_cols(q, st));
+  }
+  if ((s = w1_impl(c, &v.d, T, packed_w, v.y1_q, v.y1_s, save, ws, st, nullptr)) != MOE_OK) return s;
+  const PackLayout P = pack_layout(*c, MOE_PACK_FORWARD);
+  GemmArgs g = gemm_args(c, P, 2, packed_w, ws, L, v.d.offsets, T);
+  g.aq = v.y1_q; g.as = v.y1_s;
+  MOE_CHECK_CUDA(launch_gemm_cc(g, st));
+  MOE_CHECK_CUDA(launch_finalize_combine(g.out, g.S, g.split_stride, c->H, v.d.inv, T, kp, v.z, out, st));
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_backward(const moe_config_t* c, const uint16_t* dout, const uint16_t* x, int T,
+                                const moe_train_save_t* save, const void* packed_w_dgrad, uint16_t* dx, uint16_t* dW1,
+                                uint16_t* dW2, float* dlogits, void* ws, void* stream) {
+  moe_status_t s = check_T(c, T);
+  if (s != MOE_OK) return s;
+  if (!backward_capable(*c)) return MOE_ERR_UNSUPPORTED;
+  if (!save) return MOE_ERR_INVALID_ARG;
+  if ((s = check_save(c, save)) != MOE_OK) return s;
+  REQ_T(dout); REQ_T(x); REQ(packed_w_dgrad); REQ_T(dx); REQ(dW1); REQ(dW2); REQ_T(dlogits); REQ(ws);
+  reset_launch_count();
+  cudaStream_t st = (cudaStream_t)stream;
+  const WsLayout L = ws_layout(*c);
+  moe_ws_view_t v;
+  moe_workspace_view(c, ws, &v);
+  const Dims dm = dims_of(*c);
+  const int kp = dm.kp, G = dm.G, I = c->I, H = c->H;
+  const int R = T * kp;
+  const int64_t Rp = r_pad_for(dm, T);
+  const PackLayout P = pack_layout(*c, MOE_PACK_DGRAD);
+  uint8_t* dzq = at<uint8_t>(ws, L.dzq);
+  uint8_t* dzs = at<uint8_t>(ws, L.dzs);
+  uint8_t* dztq = at<uint8_t>(ws, L.dztq);
+  uint8_t* dzts = at<uint8_t>(ws, L.dzts);
+  float* dwrow = at<float>(ws, L.dwrow);
+  uint8_t* dhq = at<uint8_t>(ws, L.dhq);
+  uint8_t* dhs = at<uint8_t>(ws, L.dhs);
+  float* dh = at<float>(ws, L.dh);
+  uint8_t* dhtq = at<uint8_t>(ws, L.dhtq);
+  uint8_t* dhts = at<uint8_t>(ws, L.dhts);
+  const int32_t* poff = at<int32_t>(ws, L.poff);
+  // 1. dz rows: MXFP8 per token along H (rows gathered by the GEMM), and the
+  //    transposed copy along the padded row axis.
+  MOE_CHECK_CUDA(launch_quant_rows(dout, T, H, dzq, dzs, st));
+  ColQuantArgs q;
+  q.src16 = dout; q.row_map = v.d.perm_src; q.row_div = kp; q.src32 = nullptr;
+  q.C = H; q.offsets = v.d.offsets; q.poff = poff; q.G = G; q.r_pad_max = Rp; q.q = dztq; q.s = dzts;
+  MOE_CHECK_CUDA(launch_quant_cols(q, st));
+  // 2. dY1 = dz . W2^T (dgrad copy of W2: rows i < I, K = H)
+  GemmArgs g = gemm_args(c, P, 2, packed_w_dgrad, ws, L, v.d.offsets, T);
+  g.aq = dzq; g.as = dzs; g.row_map = v.d.perm_src; g.row_div = kp;
+  MOE_CHECK_CUDA(launch_gemm_cc(g, st));
+  // 3. dSwiGLU epilogue
+  DswigluArgs ds;
+  ds.P = g.out; ds.S = g.S; ds.split_stride = g.split_stride; ds.R = R; ds.I = I;
+  ds.offsets = v.d.offsets; ds.G = G; ds.h = save->h; ds.w_row = v.d.w_row; ds.act = act_params(c);
+  ds.dw_row = dwrow; ds.dhq = dhq; ds.dhs = dhs; ds.dh = dh;
+  MOE_CHECK_CUDA(launch_dswiglu(ds, st));
+  ColQuantArgs qh;
+  qh.src16 = nullptr; qh.row_map = nullptr; qh.row_div = 1; qh.src32 = dh;
+  qh.C = 2 * I; qh.offsets = v.d.offsets; qh.poff = poff; qh.G = G; qh.r_pad_max = Rp; qh.q = dhtq; qh.s = dhts;
+  MOE_CHECK_CUDA(launch_quant_cols(qh, st));
+  // 4. dXp = dh . W1^T (dgrad copy of W1: rows h < H, K = 2I), then the
+  //    slot-ordered combine backward into dx.
+  GemmArgs g2 = gemm_args(c, P, 1, packed_w_dgrad, ws, L, v.d.offsets, T);
+  g2.aq = dhq; g2.as = dhs;
+  MOE_CHECK_CUDA(launch_gemm_cc(g2, st));
+  MOE_CHECK_CUDA(launch_finalize_combine(g2.out, g2.S, g2.split_stride, H, v.d.inv, T, kp, nullptr, dx, st));
+  // 5. wgrads over each group's padded rows
+  WgradArgs w1;
+  w1.pq = save->at_q; w1.ps = save->at_s; w1.qq = dhtq; w1.qs = dhts; w1.Rp = Rp;
+  w1.M = H; w1.N = 2 * I; w1.G = c->E; w1.poff = poff; w1.out = dW1;
+  MOE_CHECK_CUDA(launch_wgrad(w1, st));
+  WgradArgs w2;
+  w2.pq = save->y1t_q; w2.ps = save->y1t_s; w2.qq = dztq; w2.qs = dzts; w2.Rp = Rp;
+  w2.M = I; w2.N = H; w2.G = c->E; w2.poff = poff; w2.out = dW2;
+  MOE_CHECK_CUDA(launch_wgrad(w2, st));
+  // 6. router
+  MOE_CHECK_CUDA(launch_router_bwd(v.d.topk_w, v.d.topk_ids, dwrow, v.d.inv, T, c->E, c->k, kp, c->routed_scale,
+                                   dlogits, st));
+  return MOE_OK;
+}
+
+moe_status_t moe_read_status(const moe_config_t* c, void* ws, int32_t* out, void* stream) {
+  moe_status_t s = moe_config_validate(c);
+  if (s != MOE_OK) return s;
+  REQ(ws);
+  if (!out) return MOE_ERR_INVALID_ARG;
+  const WsLayout L = ws_layout(*c);
+  cudaStream_t st = (cudaStream_t)stream;
+  MOE_CHECK_CUDA(cudaStreamSynchronize(st));
+  MOE_CHECK_CUDA(cudaMemcpy(out, at<int32_t>(ws, L.status), 4, cudaMemcpyDeviceToHost));
+  MOE_CHECK_CUDA(cudaMemsetAsync(at<int32_t>(ws, L.status), 0, 4, st));
+  MOE_CHECK_CUDA(cudaStreamSynchronize(st));
+  return *out ? MOE_ERR_DEVICE : MOE_OK;
+}
+
+moe_status_t moe_clear_status(const moe_config_t* c, void* ws, void* stream) {
+  moe_status_t s = moe_config_validate(c);
+  if (s != MOE_OK) return s;
+  REQ(ws);
+  const WsLayout L = ws_layout(*c);
+  MOE_CHECK_CUDA(cudaMemsetAsync(at<int32_t>(ws, L.status), 0, 4, (cudaStream_t)stream));
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument (null pointer, shape, alignment or T > T_max)";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_WORKSPACE: return "workspace or output buffer too small";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_DEVICE: return "device status word reports an error";
+  }
+  return "unknown status";
+}
+
+int moe_last_launch_count(void) { return launch_count(); }
+
+}  // extern "C"

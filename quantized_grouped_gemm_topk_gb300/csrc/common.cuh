@@ -1,0 +1,150 @@
+// Device helpers shared by the routed-MoE kernels (sm_103a).
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kWarp = 32;
+constexpr unsigned kFull = 0xffffffffu;
+
+// ---- packed weight blob ---------------------------------------------------
+// Tiles of 128 output features; each tile is a run of 64-wide K chunks.
+// NVFP4 chunk: [granule g < 2][row p < 128][16 B of 32 E2M1 codes] (4096 B)
+//              then [row p][4 E4M3 scale codes, one per 16 K] (512 B).
+// MXFP8 chunk: [granule g < 4][row p < 128][16 B of 16 E4M3 codes] (8192 B)
+//              then [row p][2 E8M0 scale codes, one per 32 K] (256 B).
+constexpr int kTileN = 128;
+constexpr int kChunkK = 64;
+constexpr uint32_t kPackMagic = 0x4d4f4557u;  // 'MOEW'
+constexpr int kPackVersion = 1;
+
+__host__ __device__ inline int chunk_bytes(int fmt) {
+  return fmt == MOE_WFMT_NVFP4 ? (4096 + 512) : (8192 + 256);
+}
+__host__ __device__ inline int chunk_data_bytes(int fmt) {
+  return fmt == MOE_WFMT_NVFP4 ? 4096 : 8192;
+}
+
+struct PackHeader {            // first 256 bytes of a packed blob
+  uint32_t magic;
+  int32_t version, fmt, which, G;
+  int32_t N1, K1, N2, K2;      // logical rows / K of the two matrices
+  int32_t interleave1;         // 1: W1 tiles hold 64 gate + 64 up features (I = N1/2)
+  int64_t off_gs1, off_gs2, off_w1, off_w2;   // byte offsets from the blob start
+  int64_t tile_bytes1, tile_bytes2;           // bytes of one 128-row tile
+  int32_t tiles1, tiles2;                     // tiles per group
+};
+
+// ---- conversions ------------------------------------------------------------
+__device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {
+  return __uint_as_float(((uint32_t)b) << 16);
+}
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// E4M3 decode of one code (exact).
+__device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)c, __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// Two E4M3 codes -> two floats (low byte first).
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint16_t c2) {
+  __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)c2, __NV_E4M3);
+  return __half22float2(__half2(h));
+}
+
+// Round-to-nearest-even E4M3 of two floats (saturating); a -> low byte.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float a, float b) {
+  return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+}
+
+// One byte holding two E2M1 codes -> two halfs (element 2i in the low nibble
+// lands in the low half).
+__device__ __forceinline__ uint32_t e2m1x2_to_f16x2(uint32_t byte) {
+  uint32_t r;
+  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(r) : "r"(byte));
+  return r;
+}
+
+__device__ __forceinline__ float2 h2_bits_to_f2(uint32_t h2) {
+  __half2 h = *reinterpret_cast<__half2*>(&h2);
+  return __half22float2(h);
+}
+
+// E8M0 code -> 2^(c - 127) for c in [1, 254] (exact, normal fp32).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t c) {
+  if (c == 0) return __uint_as_float(0x00400000u);   // 2^-127 (subnormal)
+  return __uint_as_float(c << 23);
+}
+
+// Smallest integer e with amax <= 448 * 2^e, clamped to [-127, 127];
+// -127 for amax == 0 (or any value below the normal range). Exact: 448 is
+// 1.75 * 2^8, so for amax = 1.m * 2^E the answer is E - 8, plus one when
+// 1.m > 1.75.
+__device__ __forceinline__ int mx_exponent(float amax) {
+  uint32_t b = __float_as_uint(amax) & 0x7fffffffu;
+  int ex = (int)(b >> 23);
+  if (ex == 0) return -127;
+  int e = ex - 127 - 8 + ((b & 0x7fffffu) > 0x600000u ? 1 : 0);
+  return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+
+// 2^-e as fp32 for e in [-127, 121] (all finite block maxima land there).
+__device__ __forceinline__ float pow2_neg(int e) {
+  return __uint_as_float((uint32_t)(127 - e) << 23);
+}
+
+// ---- warp helpers -----------------------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(kFull, v, o));
+  return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+
+// ---- activation ---------------------------------------------------------------
+struct ActParams {
+  int act;
+  float alpha, limit;
+};
+
+__device__ __forceinline__ float sigmoidf_(float v) { return 1.0f / (1.0f + expf(-v)); }
+
+__device__ __forceinline__ float act_fwd(float g, float u, const ActParams& p) {
+  if (p.act == MOE_ACT_SWIGLU) return g * sigmoidf_(g) * u;
+  float gc = fminf(fmaxf(g, -p.limit), p.limit);
+  float uc = fminf(fmaxf(u, -p.limit), p.limit);
+  return gc * sigmoidf_(p.alpha * gc) * uc;
+}
+
+// Gradients of d * act(g, u): returns (dg, du).
+__device__ __forceinline__ float2 act_bwd(float g, float u, float d, const ActParams& p) {
+  if (p.act == MOE_ACT_SWIGLU) {
+    float s = sigmoidf_(g);
+    return make_float2(d * (s + g * s * (1.0f - s)) * u, d * g * s);
+  }
+  float gc = fminf(fmaxf(g, -p.limit), p.limit);
+  float uc = fminf(fmaxf(u, -p.limit), p.limit);
+  float s = sigmoidf_(p.alpha * gc);
+  float dg = (g >= -p.limit && g <= p.limit) ? d * (s + p.alpha * gc * s * (1.0f - s)) * uc : 0.0f;
+  float du = (u >= -p.limit && u <= p.limit) ? d * gc * s : 0.0f;
+  return make_float2(dg, du);
+}
+
+__device__ __forceinline__ void set_status(int32_t* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+}  // namespace moe

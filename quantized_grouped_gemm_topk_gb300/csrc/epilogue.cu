@@ -1,0 +1,295 @@
+// Epilogues and the combine:
+//  * W1 epilogue: y = w_row * SwiGLU(g, u), MXFP8 requantisation along I,
+//    optional training saves (GC-MoE summary, Approach: SwiGLU, routing
+//    weight and requantisation fused after W1; NVIDIA blog "Boosting MoE
+//    training throughput with advanced fusion kernels", GLU epilogue fusion).
+//  * W2 epilogue fused with the combine: z = bf16(W2 output), out[t] = sum
+//    of the token's k' rows in slot order (GC-MoE summary, Approach: W2
+//    emits BF16 fragments that role3 combines).
+//  * transposed MXFP8 copies (same blog, MXFP8 quantisation with a
+//    transposed copy for the backward).
+//  * backward epilogue: dSwiGLU + routing-weight gradient + MXFP8 (same
+//    blog: GroupGemm + dActivation + Quantize/Transpose).
+#include "internal.cuh"
+
+namespace moe {
+
+static int grid_for(int64_t warps, int warps_per_block) {
+  int64_t b = (warps + warps_per_block - 1) / warps_per_block;
+  return (int)std::max<int64_t>(1, std::min<int64_t>(b, 152 * 32));
+}
+
+// ---- W1 epilogue --------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_w1_finalize(const W1FinArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int nb = a.I / 32;
+  const int Rv = a.offsets[a.G];
+  const int64_t total = (int64_t)min(a.R, Rv) * nb;
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); w < total; w += nw) {
+    const int64_t r = w / nb;
+    const int b = (int)(w % nb);
+    const int i = b * 32 + lane;
+    const float* P = a.P + r * 2 * a.I;
+    float g = 0.f, u = 0.f;
+    for (int s = 0; s < a.S; ++s) {
+      g += P[(int64_t)s * a.split_stride + i];
+      u += P[(int64_t)s * a.split_stride + a.I + i];
+    }
+    const float y = a.w_row[r] * act_fwd(g, u, a.act);
+    const int e = mx_exponent(warp_max(fabsf(y)));
+    const uint16_t c = f32x2_to_e4m3x2(y * pow2_neg(e), 0.f);
+    a.y1q[r * a.I + i] = (uint8_t)(c & 0xffu);
+    if (lane == 0) a.y1s[r * nb + b] = (uint8_t)(e + 127);
+    if (a.h_save) {
+      a.h_save[r * 2 * a.I + i] = f32_to_bf16_bits(g);
+      a.h_save[r * 2 * a.I + a.I + i] = f32_to_bf16_bits(u);
+    }
+    if (a.y_save) a.y_save[r * a.I + i] = y;
+  }
+}
+
+cudaError_t launch_w1_finalize(const W1FinArgs& a, cudaStream_t st) {
+  if (a.R == 0) return cudaSuccess;
+  k_w1_finalize<<<grid_for((int64_t)a.R * (a.I / 32), 8), 256, 0, st>>>(a);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// ---- W2 epilogue + combine --------------------------------------------------
+__device__ __forceinline__ float4 sum_splits4(const float* P, int S, int64_t ss, int64_t off) {
+  float4 v = *reinterpret_cast<const float4*>(P + off);
+  for (int s = 1; s < S; ++s) {
+    const float4 w = *reinterpret_cast<const float4*>(P + (int64_t)s * ss + off);
+    v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
+  }
+  return v;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  return (uint32_t)f32_to_bf16_bits(a) | ((uint32_t)f32_to_bf16_bits(b) << 16);
+}
+
+__global__ void __launch_bounds__(256) k_finalize_combine(const float* __restrict__ P, int S, int64_t ss, int N,
+                                                          const int32_t* __restrict__ inv, int T, int kp,
+                                                          uint16_t* __restrict__ z, uint16_t* __restrict__ out) {
+  const int nq = N / 4;
+  const int64_t total = (int64_t)T * nq;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = idx / nq;
+    const int n = (int)(idx % nq) * 4;
+    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+    for (int j = 0; j < kp; ++j) {
+      const int r = inv[t * kp + j];
+      if (r < 0) continue;
+      const float4 v = sum_splits4(P, S, ss, (int64_t)r * N + n);
+      const uint32_t lo = pack_bf16x2(v.x, v.y), hi = pack_bf16x2(v.z, v.w);
+      if (z) *reinterpret_cast<uint2*>(z + (int64_t)r * N + n) = make_uint2(lo, hi);
+      o0 += __uint_as_float(lo << 16);
+      o1 += __uint_as_float(lo & 0xffff0000u);
+      o2 += __uint_as_float(hi << 16);
+      o3 += __uint_as_float(hi & 0xffff0000u);
+    }
+    *reinterpret_cast<uint2*>(out + t * N + n) = make_uint2(pack_bf16x2(o0, o1), pack_bf16x2(o2, o3));
+  }
+}
+
+cudaError_t launch_finalize_combine(const float* P, int S, int64_t ss, int N, const int32_t* inv, int T, int kp,
+                                    uint16_t* z, uint16_t* out, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  int64_t threads = (int64_t)T * (N / 4);
+  int blocks = (int)std::min<int64_t>((threads + 255) / 256, 152 * 16);
+  k_finalize_combine<<<blocks, 256, 0, st>>>(P, S, ss, N, inv, T, kp, z, out);
+  note_launch();
+  return cudaGetLastError();
+}
+
+__global__ void __launch_bounds__(256) k_finalize_rows(const float* __restrict__ P, int S, int64_t ss, int N, int R,
+                                                       uint16_t* __restrict__ z) {
+  const int nq = N / 4;
+  const int64_t total = (int64_t)R * nq;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = idx / nq;
+    const int n = (int)(idx % nq) * 4;
+    const float4 v = sum_splits4(P, S, ss, r * N + n);
+    *reinterpret_cast<uint2*>(z + r * N + n) = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+  }
+}
+
+cudaError_t launch_finalize_rows(const float* P, int S, int64_t ss, int N, int R, uint16_t* z, cudaStream_t st) {
+  if (R == 0) return cudaSuccess;
+  int64_t threads = (int64_t)R * (N / 4);
+  int blocks = (int)std::min<int64_t>((threads + 255) / 256, 152 * 16);
+  k_finalize_rows<<<blocks, 256, 0, st>>>(P, S, ss, N, R, z);
+  note_launch();
+  return cudaGetLastError();
+}
+
+__global__ void __launch_bounds__(256) k_combine(const uint16_t* __restrict__ z, const int32_t* __restrict__ inv,
+                                                 const float* __restrict__ topk_w, int T, int k, int kp, int H,
+                                                 uint16_t* __restrict__ out) {
+  const int nq = H / 4;
+  const int64_t total = (int64_t)T * nq;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = idx / nq;
+    const int n = (int)(idx % nq) * 4;
+    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+    for (int j = 0; j < kp; ++j) {
+      const int r = inv[t * kp + j];
+      if (r < 0) continue;
+      const float c = (topk_w && j < k) ? topk_w[t * k + j] : 1.0f;
+      const uint2 v = *reinterpret_cast<const uint2*>(z + (int64_t)r * H + n);
+      o0 = fmaf(c, __uint_as_float(v.x << 16), o0);
+      o1 = fmaf(c, __uint_as_float(v.x & 0xffff0000u), o1);
+      o2 = fmaf(c, __uint_as_float(v.y << 16), o2);
+      o3 = fmaf(c, __uint_as_float(v.y & 0xffff0000u), o3);
+    }
+    *reinterpret_cast<uint2*>(out + t * H + n) = make_uint2(pack_bf16x2(o0, o1), pack_bf16x2(o2, o3));
+  }
+}
+
+cudaError_t launch_combine(const uint16_t* z, const int32_t* inv, const float* topk_w, int T, int k, int kp, int H,
+                           uint16_t* out, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  int64_t threads = (int64_t)T * (H / 4);
+  int blocks = (int)std::min<int64_t>((threads + 255) / 256, 152 * 16);
+  k_combine<<<blocks, 256, 0, st>>>(z, inv, topk_w, T, k, kp, H, out);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// ---- transposed MXFP8 copies ---------------------------------------------------
+// warp per (padded 32-row block, 32 columns); lane = column.
+__global__ void __launch_bounds__(256) k_quant_cols(const ColQuantArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int ncc = (a.C + 31) / 32;
+  const int64_t npb = a.r_pad_max / 32;
+  const int ptot = a.poff[a.G];
+  const int64_t total = npb * ncc;
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); w < total; w += nw) {
+    const int64_t pb = w / ncc;
+    const int cc = (int)(w % ncc);
+    const int prow = (int)(pb * 32);
+    if (prow >= ptot) continue;
+    int lo = 0, hi = a.G - 1;          // group with poff[e] <= prow < poff[e+1]
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.poff[mid] <= prow) lo = mid; else hi = mid - 1;
+    }
+    const int e = lo;
+    const int cnt = a.offsets[e + 1] - a.offsets[e];
+    const int p0 = prow - a.poff[e];
+    const int c = cc * 32 + lane;
+    const bool cok = c < a.C;
+    float v[32];
+    float am = 0.f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      float x = 0.f;
+      if (cok && p0 + i < cnt) {
+        const int64_t r = a.offsets[e] + p0 + i;
+        if (a.src16) x = bf16_bits_to_f32(a.src16[(int64_t)(a.row_map[r] / a.row_div) * a.C + c]);
+        else x = a.src32[r * a.C + c];
+      }
+      v[i] = x;
+      am = fmaxf(am, fabsf(x));
+    }
+    if (!cok) continue;
+    const int ex = mx_exponent(am);
+    const float sc = pow2_neg(ex);
+    uint32_t wds[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      wds[q] = (uint32_t)f32x2_to_e4m3x2(v[4 * q] * sc, v[4 * q + 1] * sc) |
+               ((uint32_t)f32x2_to_e4m3x2(v[4 * q + 2] * sc, v[4 * q + 3] * sc) << 16);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(a.q + (int64_t)c * a.r_pad_max + prow);
+    dst[0] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+    dst[1] = make_uint4(wds[4], wds[5], wds[6], wds[7]);
+    a.s[(int64_t)c * (a.r_pad_max / 32) + pb] = (uint8_t)(ex + 127);
+  }
+}
+
+cudaError_t launch_quant_cols(const ColQuantArgs& a, cudaStream_t st) {
+  if (a.r_pad_max == 0) return cudaSuccess;
+  k_quant_cols<<<grid_for((a.r_pad_max / 32) * ((a.C + 31) / 32), 8), 256, 0, st>>>(a);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// ---- backward epilogue: dSwiGLU + routing-weight gradient + MXFP8 -------------
+__global__ void __launch_bounds__(256) k_dswiglu(const DswigluArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int Rv = min(a.R, a.offsets[a.G]);
+  const int nb = a.I / 32;
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); r < Rv; r += nw) {
+    const float wr = a.w_row[r];
+    float dw = 0.f;
+    for (int b = 0; b < nb; ++b) {
+      const int i = b * 32 + lane;
+      float dy = 0.f;
+      for (int s = 0; s < a.S; ++s) dy += a.P[(int64_t)s * a.split_stride + r * a.I + i];
+      const float g = bf16_bits_to_f32(a.h[r * 2 * a.I + i]);
+      const float u = bf16_bits_to_f32(a.h[r * 2 * a.I + a.I + i]);
+      dw = fmaf(dy, act_fwd(g, u, a.act), dw);
+      const float2 d = act_bwd(g, u, wr * dy, a.act);
+      a.dh[r * 2 * a.I + i] = d.x;
+      a.dh[r * 2 * a.I + a.I + i] = d.y;
+      const int eg = mx_exponent(warp_max(fabsf(d.x)));
+      const int eu = mx_exponent(warp_max(fabsf(d.y)));
+      a.dhq[r * 2 * a.I + i] = (uint8_t)(f32x2_to_e4m3x2(d.x * pow2_neg(eg), 0.f) & 0xffu);
+      a.dhq[r * 2 * a.I + a.I + i] = (uint8_t)(f32x2_to_e4m3x2(d.y * pow2_neg(eu), 0.f) & 0xffu);
+      if (lane == 0) {
+        a.dhs[r * (2 * nb) + b] = (uint8_t)(eg + 127);
+        a.dhs[r * (2 * nb) + nb + b] = (uint8_t)(eu + 127);
+      }
+    }
+    dw = warp_sum(dw);
+    if (lane == 0) a.dw_row[r] = dw;
+  }
+}
+
+cudaError_t launch_dswiglu(const DswigluArgs& a, cudaStream_t st) {
+  if (a.R == 0) return cudaSuccess;
+  k_dswiglu<<<grid_for(a.R, 8), 256, 0, st>>>(a);
+  note_launch();
+  return cudaGetLastError();
+}
+
+// ---- router backward: softmax-over-selected Jacobian ---------------------------
+__global__ void __launch_bounds__(256) k_router_bwd(const float* __restrict__ topk_w, const int32_t* __restrict__ ids,
+                                                    const float* __restrict__ dw_row, const int32_t* __restrict__ inv,
+                                                    int T, int E, int k, int kp, float rs, float* dlogits) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (t >= T) return;
+  for (int e = lane; e < E; e += 32) dlogits[(int64_t)t * E + e] = 0.f;
+  float p = 0.f, dp = 0.f;
+  if (lane < k) {
+    p = topk_w[(int64_t)t * k + lane] / rs;
+    const int r = inv[(int64_t)t * kp + lane];
+    dp = r >= 0 ? rs * dw_row[r] : 0.f;
+  }
+  float sdot = 0.f;
+  for (int j = 0; j < k; ++j) sdot += __shfl_sync(kFull, p * dp, j);
+  __syncwarp();
+  if (lane < k) {
+    const int e = ids[(int64_t)t * k + lane];
+    if (e >= 0 && e < E) dlogits[(int64_t)t * E + e] = p * (dp - sdot);
+  }
+}
+
+cudaError_t launch_router_bwd(const float* topk_w, const int32_t* ids, const float* dw_row, const int32_t* inv,
+                              int T, int E, int k, int kp, float rs, float* dlogits, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  k_router_bwd<<<(T + 7) / 8, 256, 0, st>>>(topk_w, ids, dw_row, inv, T, E, k, kp, rs, dlogits);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

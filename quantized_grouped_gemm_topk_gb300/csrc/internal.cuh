@@ -1,0 +1,140 @@
+// Internal interfaces between the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+#include <algorithm>
+#include <cstddef>
+#include <cstdint>
+
+#include "common.cuh"
+
+namespace moe {
+
+constexpr int kTokBlk = 32;   // tokens per dispatch block (histogram / scatter)
+
+// launch accounting (host side, per calling thread)
+void note_launch();
+void reset_launch_count();
+int launch_count();
+
+struct RouteArgs {
+  int T, H, E, k, S;
+  float rs;
+  bool route;                 // false: ids/wts are inputs
+  const float* part;          // logits partials [KS][T][E] (or logits [T][E], KS = 1)
+  int KS;
+  float* logits;              // [T][E] summed logits out (may equal part when KS == 1)
+  int32_t *ids;
+  float* wts;
+  int32_t *counts, *offsets, *touched, *n_touched, *poff;
+  int32_t *hist, *base;       // [NB][G] each (multi-block path)
+  int32_t *perm, *inv;
+  float* w_row;
+  const uint16_t* x;          // nullable: skip quantisation
+  uint8_t *xq, *xs;
+  int32_t* status;
+};
+
+int router_splits(int T, int H);
+bool use_small_route(int T, int G, int kp);
+cudaError_t launch_router(const uint16_t* x, const float* Wr, int T, int H, int E, int KS, float* part,
+                          cudaStream_t st);
+cudaError_t launch_route_dispatch(const RouteArgs& a, cudaStream_t st);
+cudaError_t launch_topk_only(const float* logits, int T, int E, int k, float rs, int32_t* ids, float* w,
+                             int32_t* status, cudaStream_t st);
+cudaError_t launch_quant_rows(const uint16_t* src, int rows, int C, uint8_t* q, uint8_t* s, cudaStream_t st);
+
+// ---- grouped GEMM over packed weights ---------------------------------------
+// out[s][r][n] (fp32 partial over the s-th K slice, times the group's scale)
+//   = gs[e] * sum_k A[r][k] * W_e[n][k]
+// for every row r of every group e with rows; A row r is MXFP8 data at
+// source row  row_map ? row_map[r] / row_div : r  of (aq [*, K], as [*, K/32]).
+struct GemmArgs {
+  const uint8_t* w;           // packed matrix region (group 0, tile 0)
+  const float* gs;            // [G] or nullptr (scale 1)
+  int64_t tile_bytes;
+  int tiles;                  // 128-row tiles per group
+  int N, K, fmt;
+  int interleave_I;           // > 0: tile j holds gate rows 64j.. and up rows I+64j..
+  const int32_t* offsets;     // [G + 1]
+  const int32_t* touched;     // groups with rows
+  const int32_t* n_touched;
+  const uint8_t* aq;
+  const uint8_t* as;
+  const int32_t* row_map;
+  int row_div;
+  float* out;
+  int64_t split_stride;       // elements between K slices of out
+  int S;                      // K slices
+  int max_ctas;
+};
+cudaError_t launch_gemm_cc(const GemmArgs& g, cudaStream_t st);
+
+// W1 epilogue: sums the S partials, y = w_row * act(g, u), MXFP8 along I.
+struct W1FinArgs {
+  const float* P; int S; int64_t split_stride;
+  int R; int I;
+  const int32_t* offsets; int G;      // offsets[G] = rows present
+  const float* w_row;
+  ActParams act;
+  uint8_t* y1q; uint8_t* y1s;
+  uint16_t* h_save;                   // nullable [R][2I] bf16
+  float* y_save;                      // nullable [R][I] fp32
+};
+cudaError_t launch_w1_finalize(const W1FinArgs& a, cudaStream_t st);
+
+// out[t][n] = bf16(sum_j bf16(sum_s P[s][inv[t*kp+j]][n])); z (nullable) gets
+// the per-row bf16 values.
+cudaError_t launch_finalize_combine(const float* P, int S, int64_t split_stride, int N, const int32_t* inv, int T,
+                                    int kp, uint16_t* z, uint16_t* out, cudaStream_t st);
+// z [R][N] = bf16(sum_s P[s][r][n]) for r < R.
+cudaError_t launch_finalize_rows(const float* P, int S, int64_t split_stride, int N, int R, uint16_t* z,
+                                 cudaStream_t st);
+// out[t] = bf16(sum_j c_j z[inv[t*kp+j]]) with c_j from topk_w (nullable).
+cudaError_t launch_combine(const uint16_t* z, const int32_t* inv, const float* topk_w, int T, int k, int kp, int H,
+                           uint16_t* out, cudaStream_t st);
+
+// Transposed MXFP8 copy: for each group e and padded row p < pad(count_e),
+// dst[c][poff[e] + p] = MXFP8 along p (blocks of 32) of the value of row
+// offsets[e] + p (zero past count_e). Source rows: bf16 rows of src16 at
+// row_map[r] / row_div (gather), or fp32 rows src32[r].
+struct ColQuantArgs {
+  const uint16_t* src16; const int32_t* row_map; int row_div;
+  const float* src32;
+  int C;
+  const int32_t* offsets; const int32_t* poff; int G;
+  int64_t r_pad_max;                  // row length of dst
+  uint8_t* q; uint8_t* s;             // [C][r_pad_max], [C][r_pad_max/32]
+};
+cudaError_t launch_quant_cols(const ColQuantArgs& a, cudaStream_t st);
+
+// ---- backward pieces ----------------------------------------------------------
+struct DswigluArgs {
+  const float* P; int S; int64_t split_stride;   // dY1 partials [S][R][I]
+  int R, I;
+  const int32_t* offsets; int G;
+  const uint16_t* h;                  // saved bf16 [R][2I]
+  const float* w_row;
+  ActParams act;
+  float* dw_row;                      // [R]
+  uint8_t* dhq; uint8_t* dhs;         // [R][2I], [R][2I/32]
+  float* dh;                          // [R][2I] fp32 (for the transposed copy)
+};
+cudaError_t launch_dswiglu(const DswigluArgs& a, cudaStream_t st);
+
+struct WgradArgs {
+  const uint8_t* pq; const uint8_t* ps;   // [M][Rp], [M][Rp/32]
+  const uint8_t* qq; const uint8_t* qs;   // [N][Rp], [N][Rp/32]
+  int64_t Rp;
+  int M, N, G;
+  const int32_t* poff;
+  uint16_t* out;                          // [G][M][N] bf16
+};
+cudaError_t launch_wgrad(const WgradArgs& a, cudaStream_t st);
+
+cudaError_t launch_router_bwd(const float* topk_w, const int32_t* ids, const float* dw_row, const int32_t* inv,
+                              int T, int E, int k, int kp, float rs, float* dlogits, cudaStream_t st);
+
+// ---- prepack ----------------------------------------------------------------
+cudaError_t launch_prepack(const uint8_t* q, const uint8_t* s, int G, int N, int K, int fmt, int interleave_I,
+                           int tiles, int64_t tile_bytes, uint8_t* dst, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,467 @@
+// S1 router logits, S2 top-k routing, S3 counts/offsets, S4 permutation and
+// the MXFP8 quantisation of token rows.
+//
+// GC-MoE summary (arxiv-wiki "GC-MoE: Overlapping Expert-Parallel Token
+// Dispatch with FP8/FP4 Grouped GEMM via CUDA Green Contexts"), Approach:
+// role1 aggregates routing counts and places tokens into expert blocks.
+// NVIDIA blog "Boosting MoE training throughput with advanced fusion
+// kernels", section on removing host-device sync: per-group token counts stay
+// in GPU memory so nothing waits on the host. On one GPU the cross-rank token
+// pull becomes this local, deterministic permutation.
+//
+// Determinism: counts come from order-independent integer histograms; the
+// row order inside a group is fixed by a stable, warp-sequential scatter in
+// flat assignment order (t * k' + j); no float atomics anywhere.
+#include "internal.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// S1: logits partials. grid (ceil(T/16), ceil(E/256), KS), block 256.
+// part[ks][t][e] = sum over the ks-th slice of H of x[t][h] * W_r[h][e].
+// ---------------------------------------------------------------------------
+constexpr int kRtTok = 16;
+constexpr int kRtH = 64;
+
+__global__ void __launch_bounds__(256) k_router_partial(const uint16_t* __restrict__ x,
+                                                        const float* __restrict__ Wr, int T, int H, int E,
+                                                        int KS, float* __restrict__ part) {
+  __shared__ float xs[kRtTok][kRtH];
+  const int t0 = blockIdx.x * kRtTok;
+  const int e = blockIdx.y * 256 + threadIdx.x;
+  const int ks = blockIdx.z;
+  const int h0 = (int)((int64_t)ks * H / KS), h1 = (int)((int64_t)(ks + 1) * H / KS);
+  float acc[kRtTok];
+#pragma unroll
+  for (int i = 0; i < kRtTok; ++i) acc[i] = 0.f;
+  for (int hb = h0; hb < h1; hb += kRtH) {
+    const int hn = min(kRtH, h1 - hb);
+    for (int i = threadIdx.x; i < kRtTok * kRtH; i += 256) {
+      int tt = i / kRtH, hh = i % kRtH;
+      float v = 0.f;
+      if (t0 + tt < T && hh < hn) v = bf16_bits_to_f32(x[(int64_t)(t0 + tt) * H + hb + hh]);
+      xs[tt][hh] = v;
+    }
+    __syncthreads();
+    if (e < E) {
+      for (int hh = 0; hh < hn; ++hh) {
+        float w = __ldg(Wr + (int64_t)(hb + hh) * E + e);
+#pragma unroll
+        for (int i = 0; i < kRtTok; ++i) acc[i] = fmaf(xs[i][hh], w, acc[i]);
+      }
+    }
+    __syncthreads();
+  }
+  if (e < E) {
+    for (int i = 0; i < kRtTok && t0 + i < T; ++i) part[((int64_t)ks * T + t0 + i) * E + e] = acc[i];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// S2: one warp routes one token. Logits are first summed over the KS
+// partials in ks order and written out; then k rounds of a warp arg-max on
+// (value desc, id asc). NaN logits rank below every number and raise
+// MOE_DEV_NAN_LOGIT. Weights: softmax over the selected logits x scale.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
+  return va > vb || (va == vb && ia < ib);
+}
+
+__device__ void route_token(int t, int lane, const float* __restrict__ part, int KS, int T, int E, int k,
+                            float rs, float* __restrict__ logits, int32_t* __restrict__ ids,
+                            float* __restrict__ wts, int32_t* status) {
+  bool nan_seen = false;
+  const float* row_in = part + (int64_t)t * E;
+  float* row = logits + (int64_t)t * E;
+  for (int e = lane; e < E; e += kWarp) {
+    float v = row_in[e];
+    for (int ks = 1; ks < KS; ++ks) v += part[((int64_t)ks * T + t) * E + e];
+    if (v != v) nan_seen = true;
+    if (row != row_in) row[e] = v;
+  }
+  if (__any_sync(kFull, nan_seen) && lane == 0) set_status(status, MOE_DEV_NAN_LOGIT);
+  uint64_t taken = 0;
+  float sel_v = 0.f;    // lane j keeps the j-th selected logit
+  int sel_i = 0;
+  for (int j = 0; j < k; ++j) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    int slot = 0;
+    for (int e = lane; e < E; e += kWarp, ++slot) {
+      if (taken >> slot & 1ull) continue;
+      float v = row[e];
+      if (v != v) v = -INFINITY;
+      if (better(v, e, bv, bi)) { bv = v; bi = e; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      float ov = __shfl_xor_sync(kFull, bv, o);
+      int oi = __shfl_xor_sync(kFull, bi, o);
+      if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    if (bi < E && (bi & 31) == lane) taken |= 1ull << (bi >> 5);
+    if (lane == j) { sel_v = bv; sel_i = bi; }
+  }
+  // softmax over the selected logits (lane j holds selection j); the first
+  // selection is the maximum.
+  float m = __shfl_sync(kFull, sel_v, 0);
+  float p = lane < k ? expf(sel_v - m) : 0.f;
+  float sum = 0.f;
+  for (int j = 0; j < k; ++j) sum += __shfl_sync(kFull, p, j);   // slot order
+  if (lane < k) {
+    ids[(int64_t)t * k + lane] = sel_i;
+    wts[(int64_t)t * k + lane] = p / sum * rs;
+  }
+}
+
+// grid: ceil(T / 8), block 256 (warp per token).
+__global__ void __launch_bounds__(256) k_topk(const float* __restrict__ part, int KS, int T, int E, int k, float rs,
+                                              float* __restrict__ logits, int32_t* __restrict__ ids,
+                                              float* __restrict__ wts, int32_t* status) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t < T) route_token(t, lane, part, KS, T, E, k, rs, logits, ids, wts, status);
+}
+
+// ---------------------------------------------------------------------------
+// S3: per-block histograms of the assignments of kTokBlk tokens.
+// grid NB = ceil(T / kTokBlk), block 256. Invalid ids are skipped (and
+// flagged); shared slots count for every token.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int assignment_expert(const int32_t* ids, int t, int j, int k, int E) {
+  if (j >= k) return E + (j - k);
+  int e = ids[(int64_t)t * k + j];
+  return (e >= 0 && e < E) ? e : -1;
+}
+
+__global__ void __launch_bounds__(256) k_hist(const int32_t* __restrict__ ids, int T, int k, int kp, int E, int G,
+                                              int32_t* __restrict__ hist, int32_t* status) {
+  extern __shared__ int32_t sh[];
+  for (int e = threadIdx.x; e < G; e += blockDim.x) sh[e] = 0;
+  __syncthreads();
+  const int t0 = blockIdx.x * kTokBlk, t1 = min(T, t0 + kTokBlk);
+  bool bad = false;
+  for (int a = t0 * kp + threadIdx.x; a < t1 * kp; a += blockDim.x) {
+    int e = assignment_expert(ids, a / kp, a % kp, k, E);
+    if (e < 0) bad = true;
+    else atomicAdd(&sh[e], 1);
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(status, MOE_DEV_BAD_EXPERT_ID);
+  for (int e = threadIdx.x; e < G; e += blockDim.x) hist[(int64_t)blockIdx.x * G + e] = sh[e];
+}
+
+// ---------------------------------------------------------------------------
+// Block-wide exclusive scan of n ints held in shared memory (in place);
+// returns the total. blockDim.x must be a multiple of 32.
+// ---------------------------------------------------------------------------
+__device__ int block_excl_scan(int32_t* v, int n, int32_t* scratch /* >= 33 ints */) {
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int per = (n + nt - 1) / nt;
+  const int b = tid * per, e = min(n, b + per);
+  int s = 0;
+  for (int i = b; i < e; ++i) s += v[i];
+  // inclusive warp scan of s
+  const int lane = tid & 31, warp = tid >> 5;
+  int incl = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) scratch[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int nw = nt / 32;
+    int x = lane < nw ? scratch[lane] : 0;
+    int xi = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(kFull, xi, o);
+      if (lane >= o) xi += y;
+    }
+    if (lane < nw) scratch[lane] = xi - x;   // exclusive warp offsets
+    if (lane == 31) scratch[32] = xi;        // total
+  }
+  __syncthreads();
+  int run = scratch[warp] + incl - s;
+  for (int i = b; i < e; ++i) {
+    int c = v[i];
+    v[i] = run;
+    run += c;
+  }
+  int total = scratch[32];
+  __syncthreads();
+  return total;
+}
+
+// From per-block histograms: counts, offsets, per-block bases, the list of
+// groups with rows (increasing id), and 32-row padded offsets.
+// One block of 1024 threads; smem: 3 * (G + 1) + 33 ints.
+__device__ void scan_groups(const int32_t* hist, int NB, int G, int32_t* counts, int32_t* offsets,
+                            int32_t* base, int32_t* touched, int32_t* n_touched, int32_t* poff, int32_t* sm) {
+  int32_t* off = sm;               // [G + 1]
+  int32_t* flag = sm + (G + 1);    // [G + 1]
+  int32_t* pad = flag + (G + 1);   // [G + 1]
+  int32_t* scr = pad + (G + 1);    // [33]
+  for (int e = threadIdx.x; e < G; e += blockDim.x) {
+    int c = 0;
+    for (int b = 0; b < NB; ++b) c += hist[(int64_t)b * G + e];
+    counts[e] = c;
+    off[e] = c;
+    flag[e] = c > 0;
+    pad[e] = (c + 31) & ~31;
+  }
+  __syncthreads();
+  int tot = block_excl_scan(off, G, scr);
+  int ntouch = block_excl_scan(flag, G, scr);
+  int ptot = block_excl_scan(pad, G, scr);
+  for (int e = threadIdx.x; e < G; e += blockDim.x) {
+    offsets[e] = off[e];
+    if (poff) poff[e] = pad[e];
+    int c = counts[e];
+    if (c > 0) touched[flag[e]] = e;
+    if (base) {
+      int run = off[e];
+      for (int b = 0; b < NB; ++b) {
+        base[(int64_t)b * G + e] = run;
+        run += hist[(int64_t)b * G + e];
+      }
+    }
+  }
+  if (threadIdx.x == 0) {
+    offsets[G] = tot;
+    if (poff) poff[G] = ptot;
+    *n_touched = ntouch;
+  }
+}
+
+__global__ void __launch_bounds__(1024) k_scan(const int32_t* __restrict__ hist, int NB, int G,
+                                               int32_t* counts, int32_t* offsets, int32_t* base,
+                                               int32_t* touched, int32_t* n_touched, int32_t* poff) {
+  extern __shared__ int32_t sm[];
+  scan_groups(hist, NB, G, counts, offsets, base, touched, n_touched, poff, sm);
+}
+
+// ---------------------------------------------------------------------------
+// S4: stable scatter. One warp walks the assignments of a token block in
+// flat order, 32 at a time; equal experts inside a step are ranked with
+// __match_any_sync, and a per-group cursor (starting at the block's base)
+// advances after each step. Invalid ids leave inv = -1.
+// ---------------------------------------------------------------------------
+__device__ void scatter_warp(int a0, int a1, const int32_t* ids, const float* wts, int k, int kp, int E,
+                             int32_t* cursor, int32_t* perm, int32_t* inv, float* w_row) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int c = a0; c < a1; c += kWarp) {
+    const int a = c + lane;
+    int e = -1;
+    float wt = 0.f;
+    if (a < a1) {
+      int t = a / kp, j = a % kp;
+      e = assignment_expert(ids, t, j, k, E);
+      wt = j < k ? wts[(int64_t)t * k + j] : 1.0f;
+    }
+    const unsigned m = __match_any_sync(kFull, e);
+    const int rank = __popc(m & lt);
+    int basev = e >= 0 ? cursor[e] : 0;
+    __syncwarp();
+    if (e >= 0) {
+      int r = basev + rank;
+      perm[r] = a;
+      inv[a] = r;
+      w_row[r] = wt;
+      if (rank == 0) cursor[e] = basev + __popc(m);
+    } else if (a < a1) {
+      inv[a] = -1;
+    }
+    __syncwarp();
+  }
+}
+
+// grid NB, block 32; smem G ints.
+__global__ void __launch_bounds__(32) k_scatter(const int32_t* __restrict__ ids, const float* __restrict__ wts, int T,
+                                                int k, int kp, int E, int G, const int32_t* __restrict__ base,
+                                                int32_t* perm, int32_t* inv, float* w_row) {
+  extern __shared__ int32_t cursor[];
+  for (int e = threadIdx.x; e < G; e += kWarp) cursor[e] = base[(int64_t)blockIdx.x * G + e];
+  __syncwarp();
+  const int t0 = blockIdx.x * kTokBlk, t1 = min(T, t0 + kTokBlk);
+  scatter_warp(t0 * kp, t1 * kp, ids, wts, k, kp, E, cursor, perm, inv, w_row);
+}
+
+// ---------------------------------------------------------------------------
+// MXFP8 quantisation of bf16 rows [rows, C] (C % 32 == 0) into codes
+// [rows, C] and scales [rows, C/32]. Each lane takes 8 elements, four lanes a
+// 32-element block. Grid-stride over (row, 256-element group).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void quant_group_bf16(const uint16_t* __restrict__ src, int64_t row, int C, int grp,
+                                                 uint8_t* __restrict__ q, uint8_t* __restrict__ s, int lane) {
+  const int c0 = grp * 256 + lane * 8;
+  const bool ok = c0 < C;
+  float v[8];
+  if (ok) {
+    uint4 raw = *reinterpret_cast<const uint4*>(src + row * C + c0);
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      v[2 * i] = __uint_as_float(w[i] << 16);
+      v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = 0.f;
+  }
+  float am = 0.f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(v[i]));
+  am = fmaxf(am, __shfl_xor_sync(kFull, am, 1));
+  am = fmaxf(am, __shfl_xor_sync(kFull, am, 2));
+  const int e = mx_exponent(am);
+  const float sc = pow2_neg(e);
+  if (ok) {
+    uint32_t lo = (uint32_t)f32x2_to_e4m3x2(v[0] * sc, v[1] * sc) | ((uint32_t)f32x2_to_e4m3x2(v[2] * sc, v[3] * sc) << 16);
+    uint32_t hi = (uint32_t)f32x2_to_e4m3x2(v[4] * sc, v[5] * sc) | ((uint32_t)f32x2_to_e4m3x2(v[6] * sc, v[7] * sc) << 16);
+    *reinterpret_cast<uint2*>(q + row * C + c0) = make_uint2(lo, hi);
+    if ((lane & 3) == 0) s[row * (C / 32) + c0 / 32] = (uint8_t)(e + 127);
+  }
+}
+
+__global__ void __launch_bounds__(256) k_quant_rows_bf16(const uint16_t* __restrict__ src, int rows, int C,
+                                                         uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
+  const int lane = threadIdx.x & 31;
+  const int groups = (C + 255) / 256;
+  const int64_t total = (int64_t)rows * groups;
+  const int64_t wid = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t i = wid; i < total; i += nw) quant_group_bf16(src, i / groups, C, (int)(i % groups), q, s, lane);
+}
+
+// ---------------------------------------------------------------------------
+// Small-T fused path: block 0 routes every token, histograms, scans and
+// scatters inside shared memory; blocks 1.. quantise x meanwhile. One launch
+// for all of S2-S4. block 1024; smem: G ints of histogram/cursor + scan
+// scratch (3 (G + 1) + 33) + T*k ids + T*k weights.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) k_route_small(const float* __restrict__ part, int KS, int T, int E, int k,
+                                                      int kp, int G, float rs, int route, float* __restrict__ logits,
+                                                      int32_t* ids, float* wts, int32_t* counts, int32_t* offsets,
+                                                      int32_t* touched, int32_t* n_touched, int32_t* poff,
+                                                      int32_t* perm, int32_t* inv, float* w_row,
+                                                      const uint16_t* __restrict__ x, int H, uint8_t* xq,
+                                                      uint8_t* xs, int32_t* status) {
+  extern __shared__ int32_t sm[];
+  if (blockIdx.x > 0) {
+    const int lane = threadIdx.x & 31;
+    const int groups = (H + 255) / 256;
+    const int64_t total = (int64_t)T * groups;
+    const int64_t wid = (int64_t)(blockIdx.x - 1) * 32 + (threadIdx.x >> 5);
+    const int64_t nw = (int64_t)(gridDim.x - 1) * 32;
+    for (int64_t i = wid; i < total; i += nw) quant_group_bf16(x, i / groups, H, (int)(i % groups), xq, xs, lane);
+    return;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int32_t* hist = sm;                    // [G]
+  int32_t* scan_sm = sm + G;             // 3 (G + 1) + 33
+  if (route) {
+    for (int t = warp; t < T; t += 32) route_token(t, lane, part, KS, T, E, k, rs, logits, ids, wts, status);
+  }
+  for (int e = threadIdx.x; e < G; e += blockDim.x) hist[e] = 0;
+  __syncthreads();   // ids / wts written by this block are visible block-wide
+  bool bad = false;
+  for (int a = threadIdx.x; a < T * kp; a += blockDim.x) {
+    int e = assignment_expert(ids, a / kp, a % kp, k, E);
+    if (e < 0) bad = true;
+    else atomicAdd(&hist[e], 1);
+  }
+  if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(status, MOE_DEV_BAD_EXPERT_ID);
+  scan_groups(hist, 1, G, counts, offsets, nullptr, touched, n_touched, poff, scan_sm);
+  __syncthreads();
+  // cursor = offsets (reuse hist)
+  for (int e = threadIdx.x; e < G; e += blockDim.x) hist[e] = scan_sm[e];
+  __syncthreads();
+  if (warp == 0) scatter_warp(0, T * kp, ids, wts, k, kp, E, hist, perm, inv, w_row);
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+int router_splits(int T, int H) {
+  int ks = T > 0 ? 4096 / T : 1;
+  ks = std::max(1, std::min(ks, H / 32));
+  return ks;
+}
+
+cudaError_t launch_router(const uint16_t* x, const float* Wr, int T, int H, int E, int KS, float* part,
+                          cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  dim3 grid((T + kRtTok - 1) / kRtTok, (E + 255) / 256, KS);
+  k_router_partial<<<grid, 256, 0, st>>>(x, Wr, T, H, E, KS, part);
+  note_launch();
+  return cudaGetLastError();
+}
+
+static size_t small_smem(int G, int T, int k) {
+  return (size_t)(G + 3 * (G + 1) + 33) * 4;
+  (void)T; (void)k;
+}
+
+bool use_small_route(int T, int G, int kp) { return T <= 256 && T * kp <= 4096 && G <= 2048; }
+
+cudaError_t launch_route_dispatch(const RouteArgs& a, cudaStream_t st) {
+  const int kp = a.k + a.S, G = a.E + a.S;
+  const int T = a.T;
+  if (use_small_route(T, G, kp)) {
+    int nq = T == 0 ? 0 : std::min(64, std::max(1, (T * ((a.H + 255) / 256) + 31) / 32));
+    if (!a.x) nq = 0;
+    size_t smem = small_smem(G, T, a.k);
+    if (smem > 48 * 1024) {
+      cudaFuncSetAttribute(k_route_small, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    }
+    k_route_small<<<1 + nq, 1024, smem, st>>>(a.part, a.KS, T, a.E, a.k, kp, G, a.rs, a.route ? 1 : 0, a.logits,
+                                              a.ids, a.wts, a.counts, a.offsets, a.touched, a.n_touched, a.poff,
+                                              a.perm, a.inv, a.w_row, a.x, a.H, a.xq, a.xs, a.status);
+    note_launch();
+    return cudaGetLastError();
+  }
+  const int NB = (T + kTokBlk - 1) / kTokBlk;
+  if (a.route) {
+    k_topk<<<(T + 7) / 8, 256, 0, st>>>(a.part, a.KS, T, a.E, a.k, a.rs, a.logits, a.ids, a.wts, a.status);
+    note_launch();
+  }
+  k_hist<<<NB, 256, G * 4, st>>>(a.ids, T, a.k, kp, a.E, G, a.hist, a.status);
+  note_launch();
+  size_t smem = (size_t)(3 * (G + 1) + 33) * 4;
+  if (smem > 48 * 1024) cudaFuncSetAttribute(k_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  k_scan<<<1, 1024, smem, st>>>(a.hist, NB, G, a.counts, a.offsets, a.base, a.touched, a.n_touched, a.poff);
+  note_launch();
+  k_scatter<<<NB, 32, G * 4, st>>>(a.ids, a.wts, T, a.k, kp, a.E, G, a.base, a.perm, a.inv, a.w_row);
+  note_launch();
+  if (a.x) {
+    int groups = (a.H + 255) / 256;
+    int64_t warps = (int64_t)T * groups;
+    int blocks = (int)std::min<int64_t>((warps + 7) / 8, 152 * 16);
+    k_quant_rows_bf16<<<blocks, 256, 0, st>>>(a.x, T, a.H, a.xq, a.xs);
+    note_launch();
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_only(const float* logits, int T, int E, int k, float rs, int32_t* ids, float* w,
+                             int32_t* status, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  k_topk<<<(T + 7) / 8, 256, 0, st>>>(logits, 1, T, E, k, rs, const_cast<float*>(logits), ids, w, status);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_rows(const uint16_t* src, int rows, int C, uint8_t* q, uint8_t* s, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  int groups = (C + 255) / 256;
+  int64_t warps = (int64_t)rows * groups;
+  int blocks = (int)std::min<int64_t>((warps + 7) / 8, 152 * 16);
+  k_quant_rows_bf16<<<blocks, 256, 0, st>>>(src, rows, C, q, s);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,85 @@
+"""The C-ABI library builds, loads, exports every symbol include/moe.h declares,
+and rejects bad arguments on the host (no GPU needed: every checked call
+returns before touching the device)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from quantized_grouped_gemm_topk_gb300 import build as b
+    b.build()
+    from quantized_grouped_gemm_topk_gb300 import binding
+    return binding.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    from quantized_grouped_gemm_topk_gb300 import binding
+    names = _declared()
+    assert len(names) >= 19
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(binding.EXPORTS) == names
+
+
+def _cfg(**kw):
+    from quantized_grouped_gemm_topk_gb300 import binding as m
+    base = dict(H=256, I=128, E=8, k=2, T_max=16)
+    base.update(kw)
+    return m.make_config(**base)
+
+
+def test_config_validation(lib):
+    from quantized_grouped_gemm_topk_gb300 import binding as m
+    assert m.moe_config_validate(_cfg()) == 0
+    bad = [dict(H=200), dict(I=96), dict(k=0), dict(k=9), dict(n_shared=2), dict(E=2048, n_shared=1),
+           dict(k=32, E=64, n_shared=1), dict(T_max=-1), dict(act="swiglu_clamp", limit=0.0),
+           dict(routed_scale=0.0), dict(max_sms=-1)]
+    for b in bad:
+        assert m.moe_config_validate(_cfg(**b)) == 1, b
+    assert m.moe_config_validate(_cfg(act="swiglu_clamp", limit=7.0, alpha=1.702)) == 0
+
+
+def test_sizes(lib):
+    from quantized_grouped_gemm_topk_gb300 import binding as m
+    c = _cfg()
+    assert m.moe_workspace_size(c) > 0
+    nv = m.moe_packed_weights_size(c)
+    # 2 matrices x 8 groups x tiles x chunks x 4608 B, plus header/scales
+    assert nv >= 8 * (2 * (256 // 64) + 2 * (128 // 64)) * 4608
+    with pytest.raises(m.MoEError):
+        m.moe_packed_weights_size(c, m.MOE_PACK_DGRAD)       # NVFP4 has no dgrad copy
+    c8 = _cfg(wfmt="mxfp8")
+    assert m.moe_packed_weights_size(c8, m.MOE_PACK_DGRAD) > 0
+    assert m.moe_train_sizes(c8, 16) % 32 == 0
+    with pytest.raises(m.MoEError):
+        m.moe_train_sizes(c8, 17)                            # T > T_max
+
+
+def test_host_errors_enqueue_nothing(lib):
+    from quantized_grouped_gemm_topk_gb300 import binding as m
+    c = _cfg()
+    P = ctypes.c_void_p
+    # NULL / misaligned pointers and bad T are rejected before any device work
+    assert lib.moe_layer_forward(ctypes.byref(c), None, None, None, 4, None, None, None, None, None) == 1
+    assert lib.moe_layer_forward(ctypes.byref(c), 0x1000, 0x1000, 0x2000, 4, 0x3000, 0x4000, None, 0x5000,
+                                 None) == 1               # both W_r and logits given
+    assert lib.moe_layer_forward(ctypes.byref(c), 0x1001, 0x1000, None, 4, 0x3000, 0x4000, None, 0x5000,
+                                 None) == 1               # misaligned x
+    assert lib.moe_layer_forward(ctypes.byref(c), 0x1000, 0x1000, None, 17, 0x3000, 0x4000, None, 0x5000,
+                                 None) == 1               # T > T_max
+    assert lib.moe_combine(ctypes.byref(c), None, P(0x1000), None, 4, P(0x2000), None) == 1
+    assert lib.moe_layer_backward(ctypes.byref(c), 0x10, 0x10, 4, None, 0x10, 0x10, 0x10, 0x10, 0x10, 0x10,
+                                  None) == 2              # NVFP4 config: backward unsupported
+    assert m.moe_status_string(0) == "ok"
