@@ -230,65 +230,54 @@ def encode_mxfp8(w: torch.Tensor):
     return q.contiguous(), (e + 127).to(torch.uint8).contiguous()
 
 
+def gen_one_expert(s: MoEShape, seed: int, e: int, device="cpu", dgrad_copies: bool = False) -> dict:
+    """Weights of expert group e, drawn and encoded exactly as in
+    gen_expert_weights (per-expert generators, so any expert can be drawn
+    alone)."""
+    H, I = s.H, s.I
+    w1 = torch.randn(2 * I, H, generator=_gen((seed + 2) * 65536 + e, device), device=device,
+                     dtype=torch.float32) * 0.02
+    w2 = torch.randn(H, I, generator=_gen((seed + 3) * 65536 + e, device), device=device,
+                     dtype=torch.float32) * 0.02
+    out = {}
+    if s.wfmt == "nvfp4":
+        out["w1_q"], out["w1_s"], out["w1_gs"] = encode_nvfp4(w1)
+        out["w2_q"], out["w2_s"], out["w2_gs"] = encode_nvfp4(w2)
+    elif s.wfmt == "mxfp8":
+        w1 = w1.to(torch.bfloat16).to(torch.float32)      # bf16 master weights
+        w2 = w2.to(torch.bfloat16).to(torch.float32)
+        out["w1_q"], out["w1_s"] = encode_mxfp8(w1)
+        out["w2_q"], out["w2_s"] = encode_mxfp8(w2)
+        out["w1_gs"] = torch.ones((), dtype=torch.float32, device=device)
+        out["w2_gs"] = torch.ones((), dtype=torch.float32, device=device)
+        if dgrad_copies:
+            out["w1t_q"], out["w1t_s"] = encode_mxfp8(w1.t().contiguous())
+            out["w2t_q"], out["w2t_s"] = encode_mxfp8(w2.t().contiguous())
+    else:
+        raise ValueError(s.wfmt)
+    return out
+
+
 def gen_expert_weights(s: MoEShape, seed: int = 0, device="cpu", dgrad_copies: bool | None = None):
     """Expert weights for every group (routed experts then shared experts).
 
     W1_e is logically [H, 2I] (gate columns then up columns) and W2_e is
     [I, H]; both are drawn ~N(0, 0.02) and stored transposed, one row per
     output feature with the reduction axis contiguous: W1 as [2I, H], W2 as
-    [H, I]. For MXFP8 training weights the dgrad copies are quantised along
-    the other axis from the same draws: W1 as [H, 2I] and W2 as [I, H].
+    [H, I]. NVFP4: w*_q packed nibbles [N, K/2], w*_s E4M3 scales [N, K/16],
+    w*_gs fp32 per (group, matrix). MXFP8 (bf16 master weights): w*_q E4M3
+    [N, K], w*_s E8M0 [N, K/32], w*_gs = 1; the dgrad copies w1t_* [H, 2I] and
+    w2t_* [I, H] are quantised along the other axis from the same draws.
     """
-    G, H, I = s.groups, s.H, s.I
+    G = s.groups
     if dgrad_copies is None:
         dgrad_copies = s.wfmt == "mxfp8"
     out = {}
-    if s.wfmt == "nvfp4":
-        q1 = torch.empty(G, 2 * I, H // 2, dtype=torch.uint8, device=device)
-        s1 = torch.empty(G, 2 * I, H // 16, dtype=torch.uint8, device=device)
-        g1 = torch.empty(G, dtype=torch.float32, device=device)
-        q2 = torch.empty(G, H, I // 2, dtype=torch.uint8, device=device)
-        s2 = torch.empty(G, H, I // 16, dtype=torch.uint8, device=device)
-        g2 = torch.empty(G, dtype=torch.float32, device=device)
-        for e in range(G):
-            w1 = torch.randn(2 * I, H, generator=_gen((seed + 2) * 65536 + e, device),
-                             device=device, dtype=torch.float32) * 0.02
-            q1[e], s1[e], g1[e] = encode_nvfp4(w1)
-            del w1
-            w2 = torch.randn(H, I, generator=_gen((seed + 3) * 65536 + e, device),
-                             device=device, dtype=torch.float32) * 0.02
-            q2[e], s2[e], g2[e] = encode_nvfp4(w2)
-            del w2
-        out.update(w1_q=q1, w1_s=s1, w1_gs=g1, w2_q=q2, w2_s=s2, w2_gs=g2)
-    elif s.wfmt == "mxfp8":
-        q1 = torch.empty(G, 2 * I, H, dtype=torch.uint8, device=device)
-        s1 = torch.empty(G, 2 * I, H // 32, dtype=torch.uint8, device=device)
-        q2 = torch.empty(G, H, I, dtype=torch.uint8, device=device)
-        s2 = torch.empty(G, H, I // 32, dtype=torch.uint8, device=device)
-        if dgrad_copies:
-            q1t = torch.empty(G, H, 2 * I, dtype=torch.uint8, device=device)
-            s1t = torch.empty(G, H, 2 * I // 32, dtype=torch.uint8, device=device)
-            q2t = torch.empty(G, I, H, dtype=torch.uint8, device=device)
-            s2t = torch.empty(G, I, H // 32, dtype=torch.uint8, device=device)
-        for e in range(G):
-            w1 = torch.randn(2 * I, H, generator=_gen((seed + 2) * 65536 + e, device),
-                             device=device, dtype=torch.float32) * 0.02
-            w1 = w1.to(torch.bfloat16).to(torch.float32)      # bf16 master weights
-            q1[e], s1[e] = encode_mxfp8(w1)
-            if dgrad_copies:
-                q1t[e], s1t[e] = encode_mxfp8(w1.t().contiguous())
-            del w1
-            w2 = torch.randn(H, I, generator=_gen((seed + 3) * 65536 + e, device),
-                             device=device, dtype=torch.float32) * 0.02
-            w2 = w2.to(torch.bfloat16).to(torch.float32)
-            q2[e], s2[e] = encode_mxfp8(w2)
-            if dgrad_copies:
-                q2t[e], s2t[e] = encode_mxfp8(w2.t().contiguous())
-            del w2
-        ones = torch.ones(G, dtype=torch.float32, device=device)
-        out.update(w1_q=q1, w1_s=s1, w1_gs=ones, w2_q=q2, w2_s=s2, w2_gs=ones.clone())
-        if dgrad_copies:
-            out.update(w1t_q=q1t, w1t_s=s1t, w2t_q=q2t, w2t_s=s2t)
-    else:
-        raise ValueError(s.wfmt)
+    for e in range(G):
+        one = gen_one_expert(s, seed, e, device, dgrad_copies)
+        for name, t in one.items():
+            if name not in out:
+                out[name] = torch.empty((G,) + tuple(t.shape), dtype=t.dtype, device=device)
+            out[name][e] = t
+        del one
     return out

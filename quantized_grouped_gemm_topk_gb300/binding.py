@@ -31,8 +31,9 @@ EXPORTS = (
     "moe_train_sizes", "moe_prepack_weights", "moe_router_logits", "moe_route_dispatch", "moe_route_topk",
     "moe_dispatch", "moe_grouped_gemm_w1_swiglu_quant", "moe_grouped_gemm_w2", "moe_combine",
     "moe_layer_forward", "moe_layer_backward", "moe_read_status", "moe_clear_status", "moe_status_string",
-    "moe_last_launch_count",
+    "moe_last_launch_count", "moe_set_phase_events",
 )
+MOE_N_PHASE_EVENTS = 6
 
 
 class MoEError(RuntimeError):
@@ -104,6 +105,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "moe_clear_status": [cfgp, P, P],
         "moe_status_string": [ctypes.c_int],
         "moe_last_launch_count": [],
+        "moe_set_phase_events": [ctypes.POINTER(ctypes.c_void_p)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -186,6 +188,17 @@ def moe_status_string(code) -> str:
 
 def moe_last_launch_count() -> int:
     return load().moe_last_launch_count()
+
+
+def moe_set_phase_events(events):
+    """events: MOE_N_PHASE_EVENTS torch.cuda.Event(enable_timing=True) (each
+    recorded once beforehand so its handle exists), or None to switch off."""
+    if events is None:
+        _check("moe_set_phase_events", load().moe_set_phase_events(None))
+        return
+    arr = (ctypes.c_void_p * MOE_N_PHASE_EVENTS)(*[e.cuda_event for e in events])
+    moe_set_phase_events._keep = arr
+    _check("moe_set_phase_events", load().moe_set_phase_events(arr))
 
 
 # ---- device calls ----------------------------------------------------------------

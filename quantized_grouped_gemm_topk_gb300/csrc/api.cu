@@ -9,6 +9,11 @@
 namespace moe {
 
 static thread_local int g_launches = 0;
+static thread_local cudaEvent_t g_phase[MOE_N_PHASE_EVENTS] = {};
+static thread_local bool g_phase_on = false;
+static inline void phase(int i, cudaStream_t st) {
+  if (g_phase_on && g_phase[i]) cudaEventRecord(g_phase[i], st);
+}
 void note_launch() { ++g_launches; }
 void reset_launch_count() { g_launches = 0; }
 int launch_count() { return g_launches; }
@@ -426,6 +431,7 @@ static moe_status_t w1_impl(const moe_config_t* c, const moe_dispatch_t* d, int 
   GemmArgs g = gemm_args(c, P, 1, packed, ws, L, d->offsets, T);
   g.aq = d->xq; g.as = d->xs; g.row_map = d->perm_src; g.row_div = kp;
   MOE_CHECK_CUDA(launch_gemm_cc(g, st));
+  phase(2, st);
   W1FinArgs f;
   f.P = g.out; f.S = g.S; f.split_stride = g.split_stride; f.R = R; f.I = c->I;
   f.offsets = d->offsets; f.G = G; f.w_row = d->w_row; f.act = act_params(c);
@@ -433,6 +439,7 @@ static moe_status_t w1_impl(const moe_config_t* c, const moe_dispatch_t* d, int 
   f.h_save = save ? save->h : nullptr;
   f.y_save = save ? (y_save_override ? y_save_override : at<float>(ws, L.ysave)) : nullptr;
   MOE_CHECK_CUDA(launch_w1_finalize(f, st));
+  phase(3, st);
   if (save) {
     const Dims dm = dims_of(*c);
     ColQuantArgs q;
@@ -511,6 +518,7 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
   RouteArgs a = route_args(c, T, &v.d, ws, L);
   a.x = x;
   a.logits = v.logits;
+  phase(0, st);
   if (W_r) {
     const int KS = router_splits(T, c->H);
     float* part = KS == 1 ? v.logits : at<float>(ws, L.rpart);
@@ -520,7 +528,11 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
     a.part = logits_in; a.KS = 1;
   }
   MOE_CHECK_CUDA(launch_route_dispatch(a, st));
-  if (T == 0) return MOE_OK;
+  phase(1, st);
+  if (T == 0) {
+    for (int i = 2; i < MOE_N_PHASE_EVENTS; ++i) phase(i, st);
+    return MOE_OK;
+  }
   if (save) {
     // transposed MXFP8 copy of the gathered activations for the W1 wgrad
     ColQuantArgs q;
@@ -534,7 +546,9 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
   GemmArgs g = gemm_args(c, P, 2, packed_w, ws, L, v.d.offsets, T);
   g.aq = v.y1_q; g.as = v.y1_s;
   MOE_CHECK_CUDA(launch_gemm_cc(g, st));
+  phase(4, st);
   MOE_CHECK_CUDA(launch_finalize_combine(g.out, g.S, g.split_stride, c->H, v.d.inv, T, kp, v.z, out, st));
+  phase(5, st);
   return MOE_OK;
 }
 
@@ -646,5 +660,15 @@ const char* moe_status_string(moe_status_t s) {
 }
 
 int moe_last_launch_count(void) { return launch_count(); }
+
+moe_status_t moe_set_phase_events(void* const* events) {
+  if (!events) {
+    g_phase_on = false;
+    return MOE_OK;
+  }
+  for (int i = 0; i < MOE_N_PHASE_EVENTS; ++i) g_phase[i] = (cudaEvent_t)events[i];
+  g_phase_on = true;
+  return MOE_OK;
+}
 
 }  // extern "C"
