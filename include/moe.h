@@ -82,6 +82,7 @@ typedef enum moe_status {
 #define MOE_DEV_BAD_EXPERT_ID 0x1 /* routing id outside [0, E)              */
 #define MOE_DEV_NAN_LOGIT 0x2     /* NaN among a token's logits              */
 #define MOE_DEV_BAD_PACK 0x4      /* packed weight blob header mismatch      */
+#define MOE_DEV_TIMEOUT 0x8       /* a kernel gave up waiting on itself      */
 
 enum { MOE_ACT_SWIGLU = 0, MOE_ACT_SWIGLU_CLAMP = 1 };
 enum { MOE_WFMT_NVFP4 = 0, MOE_WFMT_MXFP8 = 1 };

@@ -45,7 +45,7 @@ static bool backward_capable(const moe_config_t& c) {
 // ---- workspace layout -------------------------------------------------------
 struct WsLayout {
   size_t status, logits, rpart, ids, wts, counts, offsets, touched, ntouch, poff, hist, base;
-  size_t perm, inv, wrow, xq, xs, y1q, y1s, z, P;
+  size_t perm, inv, wrow, xq, xs, y1q, y1s, z, P, a16, y16, rexp1, rexp2;
   size_t ysave, dzq, dzs, dztq, dzts, dwrow, dhq, dhs, dh, dhtq, dhts;
   size_t total;
 };
@@ -79,6 +79,10 @@ static WsLayout ws_layout(const moe_config_t& c) {
   L.y1s = take((size_t)R * d.I / 32);
   L.z = take((size_t)R * d.H * 2);
   L.P = take((size_t)R * std::max(2 * d.I, d.H) * 4);
+  L.a16 = take((size_t)R * std::max(2 * d.I, d.H) * 2);
+  L.y16 = take((size_t)R * d.I * 2);
+  L.rexp1 = take((size_t)R * 4);
+  L.rexp2 = take((size_t)R * 4);
   if (backward_capable(c)) {
     L.ysave = take((size_t)R * d.I * 4);
     L.dzq = take((size_t)T * d.H);
@@ -107,7 +111,7 @@ struct PackLayout {
   int N1, K1, N2, K2, il1;
   int tiles1, tiles2;
   int64_t tile_bytes1, tile_bytes2;
-  size_t off_gs1, off_gs2, off_w1, off_w2, total;
+  size_t off_gs1, off_gs2, off_w1, off_w2, off_rx1, off_rx2, total;
 };
 
 static PackLayout pack_layout(const moe_config_t& c, int which) {
@@ -131,6 +135,8 @@ static PackLayout pack_layout(const moe_config_t& c, int which) {
   P.off_gs2 = o; o = align_up(o + (size_t)P.G * 4, 256);
   P.off_w1 = o; o = align_up(o + (size_t)P.G * P.tiles1 * P.tile_bytes1, 256);
   P.off_w2 = o; o = align_up(o + (size_t)P.G * P.tiles2 * P.tile_bytes2, 256);
+  P.off_rx1 = o; o = align_up(o + (size_t)P.G * P.tiles1 * kTileN, 256);
+  P.off_rx2 = o; o = align_up(o + (size_t)P.G * P.tiles2 * kTileN, 256);
   P.total = o;
   return P;
 }
@@ -158,25 +164,6 @@ static int num_sms() {
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
   }
   return n;
-}
-
-static int gemm_ctas(const moe_config_t& c) {
-  int sms = num_sms();
-  if (c.max_sms > 0) sms = std::min(sms, c.max_sms);
-  return sms * 8;
-}
-
-// K slices for a grouped GEMM: enough units for ~2 waves, limited by the
-// partial buffer (S * R <= Rmax) and by the number of K chunks.
-static int gemm_splits(const moe_config_t& c, int T, int tiles, int K) {
-  const Dims d = dims_of(c);
-  const double touched = c.E * (1.0 - std::pow(1.0 - (double)c.k / c.E, (double)T)) + c.n_shared;
-  const double units = std::max(1.0, touched) * tiles;
-  int S = (int)std::ceil(2.0 * gemm_ctas(c) / units);
-  const int64_t R = (int64_t)T * d.kp;
-  S = std::min<int64_t>(S, std::max<int64_t>(1, d.Rmax / std::max<int64_t>(R, 1)));
-  S = std::max(1, std::min(S, K / kChunkK));
-  return S;
 }
 
 }  // namespace moe
@@ -293,6 +280,12 @@ moe_status_t moe_prepack_weights(const moe_config_t* c, const moe_weights_view_t
                                 d8 + P.off_w1, st));
   MOE_CHECK_CUDA(launch_prepack(src->w2_q, src->w2_s, P.G, P.N2, P.K2, P.fmt, 0, P.tiles2, P.tile_bytes2,
                                 d8 + P.off_w2, st));
+  if (c->weight_fmt == MOE_WFMT_MXFP8) {
+    MOE_CHECK_CUDA(launch_prepack_rowexp(src->w1_s, P.G, P.N1, P.K1, P.il1, P.tiles1,
+                                         reinterpret_cast<int8_t*>(d8 + P.off_rx1), st));
+    MOE_CHECK_CUDA(launch_prepack_rowexp(src->w2_s, P.G, P.N2, P.K2, 0, P.tiles2,
+                                         reinterpret_cast<int8_t*>(d8 + P.off_rx2), st));
+  }
   return MOE_OK;
 }
 
@@ -388,28 +381,65 @@ moe_status_t moe_dispatch(const moe_config_t* c, const uint16_t* x, int T, const
   return MOE_OK;
 }
 
-static GemmArgs gemm_args(const moe_config_t* c, const PackLayout& P, int which_mat, const void* packed, void* ws,
-                          const WsLayout& L, const int32_t* offsets, int T) {
-  GemmArgs g;
+// K slices for the tcgen05 GEMM (one CTA per SM): about eight units per CTA
+// for load balance, each unit at least eight 64-wide K chunks long, and
+// S * R within the partial buffer.
+static int tc_splits(const moe_config_t& c, int T, int tiles, int K, int grid) {
+  const Dims d = dims_of(c);
+  const double touched = c.E * (1.0 - std::pow(1.0 - (double)c.k / c.E, (double)T)) + c.n_shared;
+  const double units = std::max(1.0, touched) * tiles;
+  int S = (int)std::lround(8.0 * grid / units);
+  S = std::min(S, std::max(1, K / kChunkK / 8));
+  const int64_t R = std::max<int64_t>(1, (int64_t)T * d.kp);
+  S = (int)std::min<int64_t>(S, std::max<int64_t>(1, d.Rmax / R));
+  return std::max(1, S);
+}
+
+struct TcRun {
+  float* out;
+  int64_t split_stride;
+  int S;
+};
+
+// One grouped GEMM over packed matrix `mat` (1 or 2) of `packed`, B operand
+// the f16 rows a16 [T*k', K] with exponents rexp; fp32 K-slice partials into
+// the workspace buffer P.
+static moe_status_t tc_gemm(const moe_config_t* c, const PackLayout& P, int mat, const void* packed, void* ws,
+                            const WsLayout& L, const int32_t* offsets, int T, const uint16_t* a16,
+                            const int32_t* rexp, cudaStream_t st, TcRun* run) {
+  TcArgs g;
   const uint8_t* b = reinterpret_cast<const uint8_t*>(packed);
-  if (which_mat == 1) {
+  if (mat == 1) {
     g.w = b + P.off_w1; g.gs = reinterpret_cast<const float*>(b + P.off_gs1);
+    g.wrowexp = reinterpret_cast<const int8_t*>(b + P.off_rx1);
     g.tile_bytes = P.tile_bytes1; g.tiles = P.tiles1; g.N = P.N1; g.K = P.K1; g.interleave_I = P.il1;
   } else {
     g.w = b + P.off_w2; g.gs = reinterpret_cast<const float*>(b + P.off_gs2);
+    g.wrowexp = reinterpret_cast<const int8_t*>(b + P.off_rx2);
     g.tile_bytes = P.tile_bytes2; g.tiles = P.tiles2; g.N = P.N2; g.K = P.K2; g.interleave_I = 0;
   }
+  if (P.fmt == MOE_WFMT_NVFP4) g.wrowexp = nullptr;
+  else g.gs = nullptr;
   g.fmt = P.fmt;
   g.offsets = offsets;
   g.touched = at<int32_t>(ws, L.touched);
   g.n_touched = at<int32_t>(ws, L.ntouch);
-  g.aq = nullptr; g.as = nullptr; g.row_map = nullptr; g.row_div = 1;
+  g.act_rowexp = rexp;
   g.out = at<float>(ws, L.P);
   const int64_t R = (int64_t)T * (c->k + c->n_shared);
   g.split_stride = R * g.N;
-  g.S = gemm_splits(*c, T, g.tiles, g.K);
-  g.max_ctas = gemm_ctas(*c);
-  return g;
+  int sms = num_sms();
+  if (c->max_sms > 0) sms = std::min(sms, c->max_sms);
+  g.max_ctas = sms;
+  g.S = tc_splits(*c, T, g.tiles, g.K, sms);
+  g.status = at<int32_t>(ws, L.status);
+  CUtensorMap map;
+  if (!make_tmap_f16(&map, a16, R, g.K)) return MOE_ERR_CUDA;
+  MOE_CHECK_CUDA(launch_gemm_tc(g, map, st));
+  run->out = g.out;
+  run->split_stride = g.split_stride;
+  run->S = g.S;
+  return MOE_OK;
 }
 
 static ActParams act_params(const moe_config_t* c) {
@@ -428,16 +458,21 @@ static moe_status_t w1_impl(const moe_config_t* c, const moe_dispatch_t* d, int 
   const int kp = c->k + c->n_shared, G = c->E + c->n_shared;
   const int R = T * kp;
   if (T == 0) return MOE_OK;
-  GemmArgs g = gemm_args(c, P, 1, packed, ws, L, d->offsets, T);
-  g.aq = d->xq; g.as = d->xs; g.row_map = d->perm_src; g.row_div = kp;
-  MOE_CHECK_CUDA(launch_gemm_cc(g, st));
+  uint16_t* a16 = at<uint16_t>(ws, L.a16);
+  int32_t* rexp1 = at<int32_t>(ws, L.rexp1);
+  MOE_CHECK_CUDA(launch_act_f16(d->xq, d->xs, c->H, d->perm_src, kp, R, d->offsets, G, a16, rexp1, st));
+  TcRun run;
+  moe_status_t s = tc_gemm(c, P, 1, packed, ws, L, d->offsets, T, a16, rexp1, st, &run);
+  if (s != MOE_OK) return s;
   phase(2, st);
   W1FinArgs f;
-  f.P = g.out; f.S = g.S; f.split_stride = g.split_stride; f.R = R; f.I = c->I;
+  f.P = run.out; f.S = run.S; f.split_stride = run.split_stride; f.R = R; f.I = c->I;
   f.offsets = d->offsets; f.G = G; f.w_row = d->w_row; f.act = act_params(c);
   f.y1q = y1q; f.y1s = y1s;
   f.h_save = save ? save->h : nullptr;
   f.y_save = save ? (y_save_override ? y_save_override : at<float>(ws, L.ysave)) : nullptr;
+  f.y16 = at<uint16_t>(ws, L.y16);
+  f.y_rowexp = at<int32_t>(ws, L.rexp2);
   MOE_CHECK_CUDA(launch_w1_finalize(f, st));
   phase(3, st);
   if (save) {
@@ -483,10 +518,14 @@ moe_status_t moe_grouped_gemm_w2(const moe_config_t* c, const moe_dispatch_t* d,
   cudaStream_t st = (cudaStream_t)stream;
   const WsLayout L = ws_layout(*c);
   const PackLayout P = pack_layout(*c, MOE_PACK_FORWARD);
-  GemmArgs g = gemm_args(c, P, 2, packed_w, ws, L, d->offsets, T);
-  g.aq = y1_q; g.as = y1_s;
-  MOE_CHECK_CUDA(launch_gemm_cc(g, st));
-  MOE_CHECK_CUDA(launch_finalize_rows(g.out, g.S, g.split_stride, c->H, T * (c->k + c->n_shared), z, st));
+  const int R = T * (c->k + c->n_shared);
+  uint16_t* y16 = at<uint16_t>(ws, L.y16);
+  int32_t* rexp2 = at<int32_t>(ws, L.rexp2);
+  MOE_CHECK_CUDA(launch_act_f16(y1_q, y1_s, c->I, nullptr, 1, R, d->offsets, c->E + c->n_shared, y16, rexp2, st));
+  TcRun run;
+  s = tc_gemm(c, P, 2, packed_w, ws, L, d->offsets, T, y16, rexp2, st, &run);
+  if (s != MOE_OK) return s;
+  MOE_CHECK_CUDA(launch_finalize_rows(run.out, run.S, run.split_stride, c->H, R, z, st));
   return MOE_OK;
 }
 
@@ -543,11 +582,12 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
   }
   if ((s = w1_impl(c, &v.d, T, packed_w, v.y1_q, v.y1_s, save, ws, st, nullptr)) != MOE_OK) return s;
   const PackLayout P = pack_layout(*c, MOE_PACK_FORWARD);
-  GemmArgs g = gemm_args(c, P, 2, packed_w, ws, L, v.d.offsets, T);
-  g.aq = v.y1_q; g.as = v.y1_s;
-  MOE_CHECK_CUDA(launch_gemm_cc(g, st));
+  TcRun run;
+  s = tc_gemm(c, P, 2, packed_w, ws, L, v.d.offsets, T, at<uint16_t>(ws, L.y16), at<int32_t>(ws, L.rexp2), st,
+              &run);
+  if (s != MOE_OK) return s;
   phase(4, st);
-  MOE_CHECK_CUDA(launch_finalize_combine(g.out, g.S, g.split_stride, c->H, v.d.inv, T, kp, v.z, out, st));
+  MOE_CHECK_CUDA(launch_finalize_combine(run.out, run.S, run.split_stride, c->H, v.d.inv, T, kp, v.z, out, st));
   phase(5, st);
   return MOE_OK;
 }
@@ -590,9 +630,12 @@ moe_status_t moe_layer_backward(const moe_config_t* c, const uint16_t* dout, con
   q.C = H; q.offsets = v.d.offsets; q.poff = poff; q.G = G; q.r_pad_max = Rp; q.q = dztq; q.s = dzts;
   MOE_CHECK_CUDA(launch_quant_cols(q, st));
   // 2. dY1 = dz . W2^T (dgrad copy of W2: rows i < I, K = H)
-  GemmArgs g = gemm_args(c, P, 2, packed_w_dgrad, ws, L, v.d.offsets, T);
-  g.aq = dzq; g.as = dzs; g.row_map = v.d.perm_src; g.row_div = kp;
-  MOE_CHECK_CUDA(launch_gemm_cc(g, st));
+  uint16_t* a16 = at<uint16_t>(ws, L.a16);
+  int32_t* rexp1 = at<int32_t>(ws, L.rexp1);
+  MOE_CHECK_CUDA(launch_act_f16(dzq, dzs, H, v.d.perm_src, kp, R, v.d.offsets, G, a16, rexp1, st));
+  TcRun g;
+  s = tc_gemm(c, P, 2, packed_w_dgrad, ws, L, v.d.offsets, T, a16, rexp1, st, &g);
+  if (s != MOE_OK) return s;
   // 3. dSwiGLU epilogue
   DswigluArgs ds;
   ds.P = g.out; ds.S = g.S; ds.split_stride = g.split_stride; ds.R = R; ds.I = I;
@@ -605,9 +648,10 @@ moe_status_t moe_layer_backward(const moe_config_t* c, const uint16_t* dout, con
   MOE_CHECK_CUDA(launch_quant_cols(qh, st));
   // 4. dXp = dh . W1^T (dgrad copy of W1: rows h < H, K = 2I), then the
   //    slot-ordered combine backward into dx.
-  GemmArgs g2 = gemm_args(c, P, 1, packed_w_dgrad, ws, L, v.d.offsets, T);
-  g2.aq = dhq; g2.as = dhs;
-  MOE_CHECK_CUDA(launch_gemm_cc(g2, st));
+  MOE_CHECK_CUDA(launch_act_f16(dhq, dhs, 2 * I, nullptr, 1, R, v.d.offsets, G, a16, rexp1, st));
+  TcRun g2;
+  s = tc_gemm(c, P, 1, packed_w_dgrad, ws, L, v.d.offsets, T, a16, rexp1, st, &g2);
+  if (s != MOE_OK) return s;
   MOE_CHECK_CUDA(launch_finalize_combine(g2.out, g2.S, g2.split_stride, H, v.d.inv, T, kp, nullptr, dx, st));
   // 5. wgrads over each group's padded rows
   WgradArgs w1;

@@ -1,0 +1,445 @@
+// Grouped GEMM on the 5th-generation tensor cores (tcgen05), operand-swapped:
+// the MMA's M side is 128 output features of one expert tile, its N side the
+// expert's tokens (16..64 per MMA), so a decode step with a handful of tokens
+// per expert still streams every weight byte exactly once.
+//
+// GC-MoE summary (arxiv-wiki "GC-MoE: Overlapping Expert-Parallel Token
+// Dispatch with FP8/FP4 Grouped GEMM via CUDA Green Contexts"), key
+// contributions: operand-swapped tcgen05 block-scaled MMA over K-prepacked FP4
+// weights streamed in large bursts. That design pairs FP8 activations with
+// per-32 power-of-two weight scales; NVFP4 weights carry E4M3 scales per 16
+// elements, which no block-scaled tcgen05 kind accepts next to FP8
+// activations. Here every weight element is decoded once, exactly, to f16
+// (E2M1 value x E4M3 scale has at most 6 significant bits), written by a
+// decoder warpgroup straight into tensor memory as the MMA's A operand, and
+// multiplied with f16 activations (the E4M3 activation codes times
+// 2^(block exponent - row exponent)) by tcgen05.mma kind::f16 with fp32
+// accumulation in tensor memory.
+//
+// Roles (one CTA per SM, persistent over work units):
+//   warp 0      producer: one bulk copy per 64-wide K chunk of the weight tile
+//               (codes + scales, contiguous), plus TMA loads of the f16
+//               activation rows of the chunk (16-row boxes, 128-byte swizzle)
+//   warp 1      MMA issuer: 4 MMAs (K = 16 each) per chunk, A from tensor
+//               memory, B from shared memory; commits free the A buffer and
+//               the shared-memory stage
+//   warps 2-5   decoders: thread = weight row = tensor-memory lane
+//   warps 6-9   epilogue: tensor memory -> fp32 partials in global memory,
+//               scaled by the per-row weight factor and the per-token
+//               activation exponent
+// Work unit = (expert with rows, 128-feature tile, K slice, 64-token tile).
+// Every wait is bounded in time; on a timeout the CTA sets a status bit,
+// drains its own copies and MMAs, frees tensor memory and returns.
+#include "internal.cuh"
+#include "tc.cuh"
+
+namespace moe {
+
+constexpr int kTcStages = 12;
+constexpr int kTcNA = 4;          // tensor-memory A buffers (32 columns each)
+constexpr int kTcNT = 64;         // tokens per MMA tile (columns of one D buffer)
+constexpr int kTcThreads = 320;
+constexpr int kTcBSlot = kTcNT * 128;   // 64 rows x 128 bytes of f16
+constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kDCol0 = kTcNA * 32;
+
+template <int FMT>
+struct TcCfg {
+  static constexpr int CB = FMT == MOE_WFMT_NVFP4 ? 4608 : 8448;     // chunk bytes
+  static constexpr int ASlot = FMT == MOE_WFMT_NVFP4 ? 5120 : 9216;  // 1024-aligned
+  static constexpr int StageBytes = ASlot + kTcBSlot;
+  static constexpr int Stages = FMT == MOE_WFMT_NVFP4 ? kTcStages : 9;
+  static constexpr int SmemBytes = Stages * StageBytes + 1024 /*align*/ + 1024 /*barriers*/;
+};
+
+struct TcUnit {
+  int e, j, s, c0, c1, r0, r1;
+};
+
+__device__ __forceinline__ bool tc_unit(const TcArgs& g, int64_t u, int nchunks, TcUnit& w) {
+  const int per_group = g.tiles * g.S;
+  const int ti = (int)(u / per_group), rem = (int)(u % per_group);
+  w.j = rem / g.S;
+  w.s = rem % g.S;
+  w.e = g.touched[ti];
+  w.r0 = g.offsets[w.e];
+  w.r1 = g.offsets[w.e + 1];
+  w.c0 = (int)((int64_t)w.s * nchunks / g.S);
+  w.c1 = (int)((int64_t)(w.s + 1) * nchunks / g.S);
+  return w.c1 > w.c0 && w.r1 > w.r0;
+}
+
+__device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two) {
+  uint32_t r;
+  asm("{ .reg .b16 t; cvt.u16.u32 t, %1; cvt.rn.f16x2.e4m3x2 %0, t; }" : "=r"(r) : "r"(two));
+  return r;
+}
+__device__ __forceinline__ void e2m1x8_f16x2(uint32_t w, uint32_t& o0, uint32_t& o1, uint32_t& o2, uint32_t& o3) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
+      : "r"(w));
+}
+// f16 bits of 2^d (0 below the subnormal range), duplicated into both halves.
+__device__ __forceinline__ uint32_t f16x2_pow2(int d) {
+  uint32_t h;
+  if (d >= -14) h = (uint32_t)(d + 15) << 10;
+  else if (d >= -24) h = 1u << (d + 24);
+  else h = 0;
+  return h | (h << 16);
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant__ TcArgs g,
+                                                           const __grid_constant__ CUtensorMap tmap_b) {
+  using C = TcCfg<FMT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* stages = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::Stages * C::StageBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = full + C::Stages;
+  uint64_t* afull = empty + C::Stages;
+  uint64_t* afree = afull + kTcNA;
+  uint64_t* dfull = afree + kTcNA;
+  uint64_t* dfree = dfull + 2;
+  uint64_t* drain = dfree + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::Stages; ++i) {
+      tc::mbar_init(&full[i], 1);
+      tc::mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < kTcNA; ++i) {
+      tc::mbar_init(&afull[i], 128);
+      tc::mbar_init(&afree[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&dfull[i], 1);
+      tc::mbar_init(&dfree[i], 128);
+    }
+    tc::mbar_init(drain, 1);
+    *abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == 1) tc::tmem_alloc(tmem_slot, kTmemCols);
+  tc::fence_before_sync();
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  const int nchunks = g.K / kChunkK;
+  const int64_t units = (int64_t)(*g.n_touched) * g.tiles * g.S;
+
+  if (warp == 0) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      tc::prefetch_tmap(&tmap_b);
+      const uint64_t pol_w = tc::policy_evict_first(), pol_a = tc::policy_evict_last();
+      uint32_t it = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        TcUnit w;
+        if (!tc_unit(g, u, nchunks, w)) continue;
+        const uint8_t* tile = g.w + ((int64_t)w.e * g.tiles + w.j) * g.tile_bytes;
+        for (int t0 = w.r0; ok && t0 < w.r1; t0 += kTcNT) {
+          const int nb16 = (min(kTcNT, w.r1 - t0) + 15) >> 4;
+          for (int c = w.c0; c < w.c1; ++c, ++it) {
+            const int st = it % C::Stages;
+            const uint32_t ph = (it / C::Stages) & 1;
+            if (!tc::mbar_wait(&empty[st], ph ^ 1, abort)) { ok = false; break; }
+            uint8_t* sa = stages + st * C::StageBytes;
+            uint8_t* sb = sa + C::ASlot;
+            tc::mbar_arrive_expect_tx(&full[st], C::CB + nb16 * 2048);
+            tc::bulk_g2s(sa, tile + (int64_t)c * C::CB, C::CB, &full[st], pol_w);
+            for (int b = 0; b < nb16; ++b) tc::tma_load_2d(sb + b * 2048, &tmap_b, c * kChunkK, t0 + b * 16,
+                                                           &full[st], pol_a);
+          }
+        }
+      }
+      if (!ok || *abort) {
+        // wind-down: wait (bounded, ignoring the abort flag) until every copy
+        // still in flight into this CTA's shared memory has landed
+        volatile int never = 0;
+        const uint32_t n = it < (uint32_t)C::Stages ? it : (uint32_t)C::Stages;
+        for (uint32_t k = 0; k < n; ++k) {
+          const uint32_t i2 = it - 1 - k;
+          tc::mbar_wait(&full[i2 % C::Stages], (i2 / C::Stages) & 1, &never, 200000000ull);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------- MMA issuer ----------------
+    if (lane == 0) {
+      uint32_t it = 0, ait = 0, dit = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        TcUnit w;
+        if (!tc_unit(g, u, nchunks, w)) continue;
+        for (int t0 = w.r0; ok && t0 < w.r1; t0 += kTcNT) {
+          const int nmma = ((min(kTcNT, w.r1 - t0) + 15) >> 4) << 4;
+          const uint32_t idesc = tc::idesc_f16_f32(128, nmma);
+          const int d = dit & 1;
+          if (!tc::mbar_wait(&dfree[d], ((dit >> 1) & 1) ^ 1, abort)) { ok = false; break; }
+          tc::fence_after_sync();
+          const uint32_t dt = tmem + kDCol0 + d * kTcNT;
+          for (int c = w.c0; c < w.c1; ++c, ++it, ++ait) {
+            const int st = it % C::Stages;
+            const int a = ait % kTcNA;
+            if (!tc::mbar_wait(&full[st], (it / C::Stages) & 1, abort)) { ok = false; break; }
+            if (!tc::mbar_wait(&afull[a], (ait / kTcNA) & 1, abort)) { ok = false; break; }
+            tc::fence_after_sync();
+            const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(stages + st * C::StageBytes + C::ASlot));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              tc::mma_f16_ts(dt, tmem + a * 32 + kk * 8, bd + (uint64_t)(kk * 2), idesc, (c > w.c0 || kk > 0) ? 1u : 0u);
+            tc::mma_commit(&afree[a]);
+            tc::mma_commit(&empty[st]);
+          }
+          if (!ok) break;
+          tc::mma_commit(&dfull[d]);
+          ++dit;
+        }
+      }
+      // every MMA of this thread has completed once `drain` fires
+      tc::mma_commit(drain);
+      volatile int zero = 0;
+      tc::mbar_wait(drain, 0, &zero, 200000000ull);
+    }
+  } else if (warp < 6) {
+    // ---------------- decoders ----------------
+    const int q = warp & 3;
+    const int p = q * 32 + lane;                  // weight row = TMEM lane
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    uint32_t it = 0, ait = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      TcUnit w;
+      if (!tc_unit(g, u, nchunks, w)) continue;
+      int rexp = 0;
+      if (FMT == MOE_WFMT_MXFP8) rexp = g.wrowexp[((int64_t)w.e * g.tiles + w.j) * kTileN + p];
+      for (int t0 = w.r0; ok && t0 < w.r1; t0 += kTcNT) {
+        for (int c = w.c0; c < w.c1; ++c, ++it, ++ait) {
+          const int st = it % C::Stages;
+          if (!tc::mbar_wait(&full[st], (it / C::Stages) & 1, abort)) { ok = false; break; }
+          const uint8_t* sa = stages + st * C::StageBytes;
+          uint32_t v[32];
+          if (FMT == MOE_WFMT_NVFP4) {
+            const uint4 g0 = *reinterpret_cast<const uint4*>(sa + p * 16);
+            const uint4 g1 = *reinterpret_cast<const uint4*>(sa + 2048 + p * 16);
+            const uint32_t sc = *reinterpret_cast<const uint32_t*>(sa + 4096 + p * 4);
+            const uint32_t s01 = e4m3x2_f16x2(sc & 0xffffu), s23 = e4m3x2_f16x2(sc >> 16);
+            const uint32_t ss[4] = {(s01 & 0xffffu) * 0x10001u, (s01 >> 16) * 0x10001u, (s23 & 0xffffu) * 0x10001u,
+                                    (s23 >> 16) * 0x10001u};
+            const uint32_t wd[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              uint32_t o0, o1, o2, o3;
+              e2m1x8_f16x2(wd[i], o0, o1, o2, o3);
+              const uint32_t s = ss[i >> 1];
+              v[4 * i + 0] = hmul2_bits(o0, s);
+              v[4 * i + 1] = hmul2_bits(o1, s);
+              v[4 * i + 2] = hmul2_bits(o2, s);
+              v[4 * i + 3] = hmul2_bits(o3, s);
+            }
+          } else {
+            const uint32_t sc = *reinterpret_cast<const uint16_t*>(sa + 8192 + p * 2);
+            const uint32_t f0 = f16x2_pow2((int)(sc & 0xffu) - 127 - rexp);
+            const uint32_t f1 = f16x2_pow2((int)(sc >> 8) - 127 - rexp);
+#pragma unroll
+            for (int gi = 0; gi < 4; ++gi) {
+              const uint4 gr = *reinterpret_cast<const uint4*>(sa + gi * 2048 + p * 16);
+              const uint32_t wd[4] = {gr.x, gr.y, gr.z, gr.w};
+              const uint32_t f = gi < 2 ? f0 : f1;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                v[gi * 8 + 2 * i] = hmul2_bits(e4m3x2_f16x2(wd[i] & 0xffffu), f);
+                v[gi * 8 + 2 * i + 1] = hmul2_bits(e4m3x2_f16x2(wd[i] >> 16), f);
+              }
+            }
+          }
+          const int a = ait % kTcNA;
+          if (!tc::mbar_wait(&afree[a], ((ait / kTcNA) & 1) ^ 1, abort)) { ok = false; break; }
+          tc::fence_after_sync();
+          tc::tmem_st32(lane_base + a * 32, v);
+          tc::tmem_wait_st();
+          tc::fence_before_sync();
+          tc::mbar_arrive(&afull[a]);
+        }
+      }
+    }
+  } else {
+    // ---------------- epilogue ----------------
+    const int q = warp & 3;
+    const int p = q * 32 + lane;
+    const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    uint32_t dit = 0;
+    bool ok = true;
+    for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      TcUnit w;
+      if (!tc_unit(g, u, nchunks, w)) continue;
+      int n;
+      if (g.interleave_I > 0) n = p < 64 ? 64 * w.j + p : g.interleave_I + 64 * w.j + (p - 64);
+      else n = kTileN * w.j + p;
+      const bool nvalid = n < g.N;
+      float rowf;
+      if (FMT == MOE_WFMT_NVFP4) rowf = g.gs ? g.gs[w.e] : 1.0f;
+      else rowf = ldexpf(1.0f, g.wrowexp[((int64_t)w.e * g.tiles + w.j) * kTileN + p]);
+      float* outp = g.out + (int64_t)w.s * g.split_stride + n;
+      for (int t0 = w.r0; t0 < w.r1; t0 += kTcNT) {
+        const int nt = min(kTcNT, w.r1 - t0);
+        const int d = dit & 1;
+        if (!tc::mbar_wait(&dfull[d], (dit >> 1) & 1, abort)) { ok = false; break; }
+        tc::fence_after_sync();
+        for (int cb = 0; cb < nt; cb += 16) {
+          uint32_t v[16];
+          tc::tmem_ld16(lane_base + kDCol0 + d * kTcNT + cb, v);
+          tc::tmem_wait_ld();
+          if (nvalid) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int t = t0 + cb + i;
+              if (cb + i < nt) outp[(int64_t)t * g.N] = __uint_as_float(v[i]) * rowf * ldexpf(1.0f, g.act_rowexp[t]);
+            }
+          }
+        }
+        tc::fence_before_sync();
+        tc::mbar_arrive(&dfree[d]);
+        ++dit;
+      }
+    }
+  }
+
+  tc::fence_before_sync();
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort) set_status(g.status, MOE_DEV_TIMEOUT);
+  if (warp == 1) {
+    tc::fence_after_sync();
+    tc::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D f16 matrix [rows][cols] (row stride cols * 2 bytes), 64 x 16 boxes,
+// 128-byte swizzle; rows past the end read as zero.
+bool make_tmap_f16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)std::max<int64_t>(rows, 1)};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {64, 16};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+cudaError_t launch_gemm_tc(const TcArgs& g, const CUtensorMap& tmap_b, cudaStream_t st) {
+  const int grid = std::max(1, g.max_ctas);
+  if (g.fmt == MOE_WFMT_NVFP4) {
+    static bool attr = false;
+    if (!attr) {
+      cudaFuncSetAttribute(k_gemm_tc<MOE_WFMT_NVFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           TcCfg<MOE_WFMT_NVFP4>::SmemBytes);
+      attr = true;
+    }
+    k_gemm_tc<MOE_WFMT_NVFP4><<<grid, kTcThreads, TcCfg<MOE_WFMT_NVFP4>::SmemBytes, st>>>(g, tmap_b);
+  } else {
+    static bool attr = false;
+    if (!attr) {
+      cudaFuncSetAttribute(k_gemm_tc<MOE_WFMT_MXFP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           TcCfg<MOE_WFMT_MXFP8>::SmemBytes);
+      attr = true;
+    }
+    k_gemm_tc<MOE_WFMT_MXFP8><<<grid, kTcThreads, TcCfg<MOE_WFMT_MXFP8>::SmemBytes, st>>>(g, tmap_b);
+  }
+  note_launch();
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// f16 activation rows for the B operand.
+// a16[r][k] = E4M3 value * 2^(block exponent - row exponent), rowexp[r] =
+// the largest block exponent of the row (unbiased), so the product of the
+// two is the MXFP8 value exactly unless a block sits more than 15 binades
+// below the row's largest block (then bits below 2^-24 of the row scale are
+// rounded away).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void f16_row_from_mx(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int C,
+                                                uint16_t* __restrict__ dst, int32_t* rowexp_out, int lane) {
+  const int nb = C / 32;
+  int mx = 0;
+  for (int b = lane; b < nb; b += 32) mx = max(mx, (int)s[b]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(kFull, mx, o));
+  if (lane == 0) *rowexp_out = mx - 127;
+  for (int c0 = lane * 8; c0 < C; c0 += 256) {
+    const uint2 codes = *reinterpret_cast<const uint2*>(q + c0);
+    const float f = ldexpf(1.0f, (int)s[c0 / 32] - mx);
+    uint32_t outw[4];
+    const uint32_t cw[2] = {codes.x, codes.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float2 lo = e4m3x2_to_f32x2((uint16_t)(cw[i] & 0xffffu));
+      const float2 hi = e4m3x2_to_f32x2((uint16_t)(cw[i] >> 16));
+      const __half2 h0 = __floats2half2_rn(lo.x * f, lo.y * f);
+      const __half2 h1 = __floats2half2_rn(hi.x * f, hi.y * f);
+      outw[2 * i] = *reinterpret_cast<const uint32_t*>(&h0);
+      outw[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&h1);
+    }
+    *reinterpret_cast<uint4*>(dst + c0) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+  }
+}
+
+// warp per row r < min(R, offsets[G]); source row row_map[r] / row_div.
+__global__ void __launch_bounds__(256) k_act_f16(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int C,
+                                                 const int32_t* __restrict__ row_map, int row_div, int R,
+                                                 const int32_t* __restrict__ offsets, int G, uint16_t* __restrict__ a16,
+                                                 int32_t* __restrict__ rowexp) {
+  const int lane = threadIdx.x & 31;
+  const int Rv = min(R, offsets[G]);
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); r < Rv; r += nw) {
+    const int64_t src = row_map ? (int64_t)(row_map[r] / row_div) : r;
+    f16_row_from_mx(q + src * C, s + src * (C / 32), C, a16 + r * C, rowexp + r, lane);
+  }
+}
+
+cudaError_t launch_act_f16(const uint8_t* q, const uint8_t* s, int C, const int32_t* row_map, int row_div, int R,
+                           const int32_t* offsets, int G, uint16_t* a16, int32_t* rowexp, cudaStream_t st) {
+  if (R == 0) return cudaSuccess;
+  const int blocks = (int)std::min<int64_t>((R + 7) / 8, 152 * 16);
+  k_act_f16<<<blocks, 256, 0, st>>>(q, s, C, row_map, row_div, R, offsets, G, a16, rowexp);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

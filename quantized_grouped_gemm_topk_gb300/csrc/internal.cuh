@@ -1,5 +1,7 @@
 // Internal interfaces between the C-ABI layer (api.cu) and the kernel files.
 #pragma once
+#include <cuda.h>
+
 #include <algorithm>
 #include <cstddef>
 #include <cstdint>
@@ -42,31 +44,34 @@ cudaError_t launch_topk_only(const float* logits, int T, int E, int k, float rs,
                              int32_t* status, cudaStream_t st);
 cudaError_t launch_quant_rows(const uint16_t* src, int rows, int C, uint8_t* q, uint8_t* s, cudaStream_t st);
 
-// ---- grouped GEMM over packed weights ---------------------------------------
-// out[s][r][n] (fp32 partial over the s-th K slice, times the group's scale)
-//   = gs[e] * sum_k A[r][k] * W_e[n][k]
-// for every row r of every group e with rows; A row r is MXFP8 data at
-// source row  row_map ? row_map[r] / row_div : r  of (aq [*, K], as [*, K/32]).
-struct GemmArgs {
-  const uint8_t* w;           // packed matrix region (group 0, tile 0)
-  const float* gs;            // [G] or nullptr (scale 1)
+// ---- grouped GEMM on tcgen05 (gemm_tc.cu) -------------------------------------
+// Same result layout as GemmArgs: out[s][r][n] = rowf(n) * 2^act_rowexp[r] *
+// sum_k W_e[n][k] * a16[r][k], with rowf = gs[e] (NVFP4) or 2^wrowexp (MXFP8);
+// the f16 activation rows a16 [R][K] come in through a TMA descriptor.
+struct TcArgs {
+  const uint8_t* w;
+  const float* gs;            // [G] (NVFP4) or nullptr
+  const int8_t* wrowexp;      // [G][tiles][128] (MXFP8) or nullptr
   int64_t tile_bytes;
-  int tiles;                  // 128-row tiles per group
+  int tiles;
   int N, K, fmt;
-  int interleave_I;           // > 0: tile j holds gate rows 64j.. and up rows I+64j..
-  const int32_t* offsets;     // [G + 1]
-  const int32_t* touched;     // groups with rows
+  int interleave_I;
+  const int32_t* offsets;
+  const int32_t* touched;
   const int32_t* n_touched;
-  const uint8_t* aq;
-  const uint8_t* as;
-  const int32_t* row_map;
-  int row_div;
+  const int32_t* act_rowexp;  // [R]
   float* out;
-  int64_t split_stride;       // elements between K slices of out
-  int S;                      // K slices
+  int64_t split_stride;
+  int S;
   int max_ctas;
+  int32_t* status;
 };
-cudaError_t launch_gemm_cc(const GemmArgs& g, cudaStream_t st);
+bool make_tmap_f16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols);
+cudaError_t launch_gemm_tc(const TcArgs& g, const CUtensorMap& tmap_b, cudaStream_t st);
+// a16[r] = f16 rows of the MXFP8 rows q/s [*, C] at row_map[r] / row_div
+// (or r), rowexp[r] = the row's largest block exponent.
+cudaError_t launch_act_f16(const uint8_t* q, const uint8_t* s, int C, const int32_t* row_map, int row_div, int R,
+                           const int32_t* offsets, int G, uint16_t* a16, int32_t* rowexp, cudaStream_t st);
 
 // W1 epilogue: sums the S partials, y = w_row * act(g, u), MXFP8 along I.
 struct W1FinArgs {
@@ -78,6 +83,8 @@ struct W1FinArgs {
   uint8_t* y1q; uint8_t* y1s;
   uint16_t* h_save;                   // nullable [R][2I] bf16
   float* y_save;                      // nullable [R][I] fp32
+  uint16_t* y16;                      // nullable [R][I] f16 rows for the W2 B operand
+  int32_t* y_rowexp;                  // [R] row exponent of y16
 };
 cudaError_t launch_w1_finalize(const W1FinArgs& a, cudaStream_t st);
 
@@ -136,5 +143,9 @@ cudaError_t launch_router_bwd(const float* topk_w, const int32_t* ids, const flo
 // ---- prepack ----------------------------------------------------------------
 cudaError_t launch_prepack(const uint8_t* q, const uint8_t* s, int G, int N, int K, int fmt, int interleave_I,
                            int tiles, int64_t tile_bytes, uint8_t* dst, cudaStream_t st);
+// MXFP8: per packed row, the largest E8M0 scale exponent (unbiased) of the
+// logical row, int8 [G][tiles][128] (0 for padding rows).
+cudaError_t launch_prepack_rowexp(const uint8_t* s, int G, int N, int K, int interleave_I, int tiles, int8_t* dst,
+                                  cudaStream_t st);
 
 }  // namespace moe

@@ -125,6 +125,37 @@ __global__ void __launch_bounds__(256) k_prepack(const uint8_t* __restrict__ q, 
   }
 }
 
+__global__ void __launch_bounds__(256) k_prepack_rowexp(const uint8_t* __restrict__ s, int G, int N, int K,
+                                                        int interleave_I, int tiles, int8_t* __restrict__ dst) {
+  const int64_t total = (int64_t)G * tiles * kTileN;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int p = (int)(idx % kTileN);
+    const int j = (int)((idx / kTileN) % tiles);
+    const int g = (int)(idx / ((int64_t)kTileN * tiles));
+    int n;
+    if (interleave_I > 0) n = p < 64 ? 64 * j + p : interleave_I + 64 * j + (p - 64);
+    else n = kTileN * j + p;
+    int mx = 127;
+    if (n < N) {
+      mx = 0;
+      const uint8_t* row = s + ((int64_t)g * N + n) * (K / 32);
+      for (int b = 0; b < K / 32; ++b) mx = max(mx, (int)row[b]);
+    }
+    dst[idx] = (int8_t)(mx - 127);
+  }
+}
+
+cudaError_t launch_prepack_rowexp(const uint8_t* s, int G, int N, int K, int interleave_I, int tiles, int8_t* dst,
+                                  cudaStream_t st) {
+  const int64_t total = (int64_t)G * tiles * kTileN;
+  if (total == 0) return cudaSuccess;
+  int blocks = (int)std::min<int64_t>((total + 255) / 256, 152 * 32);
+  k_prepack_rowexp<<<blocks, 256, 0, st>>>(s, G, N, K, interleave_I, tiles, dst);
+  note_launch();
+  return cudaGetLastError();
+}
+
 cudaError_t launch_prepack(const uint8_t* q, const uint8_t* s, int G, int N, int K, int fmt, int interleave_I,
                            int tiles, int64_t tile_bytes, uint8_t* dst, cudaStream_t st) {
   const int64_t total = (int64_t)G * tiles * (K / kChunkK) * kTileN;

@@ -1,0 +1,169 @@
+"""The step-wise C-ABI entry points, CUDA-graph replay, the identity-expert
+combine invariant, and the device status word."""
+import numpy as np
+import pytest
+import torch
+
+import inputs
+import quantized_grouped_gemm_topk_gb300 as m
+
+from gpu_harness import oracle_forward, run_forward, weights_for
+from util import assert_close_layer, cuda_device, np_
+
+pytestmark = pytest.mark.gpu
+
+
+def _alloc_dispatch(s, T, dev):
+    R = T * s.kp
+    G = s.groups
+    t = {
+        "topk_ids": torch.empty(T, s.k, dtype=torch.int32, device=dev),
+        "topk_w": torch.empty(T, s.k, dtype=torch.float32, device=dev),
+        "counts": torch.empty(G, dtype=torch.int32, device=dev),
+        "offsets": torch.empty(G + 1 + 3, dtype=torch.int32, device=dev),
+        "perm_src": torch.empty(R, dtype=torch.int32, device=dev),
+        "inv": torch.empty(R, dtype=torch.int32, device=dev),
+        "w_row": torch.empty(R, dtype=torch.float32, device=dev),
+        "xq": torch.empty(T, s.H, dtype=torch.uint8, device=dev),
+        "xs": torch.empty(T, s.H // 32, dtype=torch.uint8, device=dev),
+    }
+    return t, m.dispatch_struct(t)
+
+
+@pytest.mark.parametrize("name,S", [("tiny", 0), ("tiny", 1)])
+def test_stepwise_equals_layer_forward(name, S):
+    dev = cuda_device()
+    s = inputs.workload(name, n_shared=S, routed_scale=2.5 if S else 1.0)
+    T = s.T
+    r = run_forward(s, T, dev=dev)
+    cfg, ws = r["cfg"], r["ws"]
+    logits = torch.empty(T, s.E, dtype=torch.float32, device=dev)
+    m.moe_router_logits(cfg, r["x"], r["Wr"], T, logits, ws)
+    np.testing.assert_allclose(np_(logits), np_(r["views"]["logits"]), rtol=1e-5, atol=1e-6)
+    t, d = _alloc_dispatch(s, T, dev)
+    m.moe_route_dispatch(cfg, r["views"]["logits"], r["x"], T, d, ws)
+    for k in ("topk_ids", "counts", "perm_src", "inv", "xq", "xs"):
+        ref = r["views"][k]
+        assert torch.equal(t[k][: ref.numel()].view(ref.shape) if k != "counts" else t[k], ref), k
+    ids2 = torch.empty_like(t["topk_ids"])
+    w2 = torch.empty_like(t["topk_w"])
+    m.moe_route_topk(cfg, r["views"]["logits"], T, ids2, w2, ws)
+    assert torch.equal(ids2, t["topk_ids"]) and torch.equal(w2, t["topk_w"])
+    # dispatch from given ids
+    t2, d2 = _alloc_dispatch(s, T, dev)
+    t2["topk_ids"].copy_(t["topk_ids"])
+    t2["topk_w"].copy_(t["topk_w"])
+    m.moe_dispatch(cfg, r["x"], T, d2, ws)
+    assert torch.equal(t2["perm_src"], t["perm_src"]) and torch.equal(t2["inv"], t["inv"])
+    R = T * s.kp
+    y1q = torch.empty(R, s.I, dtype=torch.uint8, device=dev)
+    y1s = torch.empty(R, s.I // 32, dtype=torch.uint8, device=dev)
+    m.moe_grouped_gemm_w1_swiglu_quant(cfg, d, T, r["packed"], y1q, y1s, None, ws)
+    assert torch.equal(y1q, r["views"]["y1_q"]) and torch.equal(y1s, r["views"]["y1_s"])
+    z = torch.empty(R, s.H, dtype=torch.bfloat16, device=dev)
+    m.moe_grouped_gemm_w2(cfg, d, T, y1q, y1s, r["packed"], z, ws)
+    assert torch.equal(z.view(torch.int16), r["views"]["z"])
+    out = torch.empty(T, s.H, dtype=torch.bfloat16, device=dev)
+    m.moe_combine(cfg, z, t["inv"], None, T, out)
+    assert torch.equal(out, r["out"])
+
+
+def test_identity_experts_combine():
+    """Rows copied straight from their tokens and combined with the routing
+    weights give x * sum_j w_j."""
+    dev = cuda_device()
+    s = inputs.workload("tiny", n_shared=1, routed_scale=2.5)
+    T = 40
+    r = run_forward(s, T, dev=dev)
+    v = r["views"]
+    tok = (v["perm_src"].long() // s.kp)
+    z = r["x"][tok].contiguous()
+    out = torch.empty(T, s.H, dtype=torch.bfloat16, device=dev)
+    m.moe_combine(r["cfg"], z, v["inv"], v["topk_w"], T, out)
+    wsum = v["topk_w"].double().sum(1) + 1.0
+    ref = r["x"].double() * wsum[:, None]
+    assert_close_layer(np_(out.double()), np_(ref), "identity combine")
+    assert (out.double() - ref).abs().max() <= ref.abs().max() * 2 ** -7
+
+
+def test_cuda_graph_replay_matches_eager():
+    dev = cuda_device()
+    s = inputs.workload("dsv3", T=8, E=32)
+    T = s.T
+    r = run_forward(s, T, dev=dev)
+    cfg, ws, packed, Wr = r["cfg"], r["ws"], r["packed"], r["Wr"]
+    x_static = torch.empty_like(r["x"])
+    out_static = torch.empty_like(r["out"])
+    xs = [inputs.gen_x(s, 100 + i, device=dev, T=T) for i in range(3)]
+    eager = []
+    for x in xs:
+        o = torch.empty_like(out_static)
+        m.moe_layer_forward(cfg, x, Wr, None, T, packed, o, None, ws)
+        eager.append(o)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    x_static.copy_(xs[0])
+    with torch.cuda.graph(g):
+        m.moe_layer_forward(cfg, x_static, Wr, None, T, packed, out_static, None, ws)
+    for x, ref in zip(xs, eager):
+        x_static.copy_(x)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out_static, ref)
+
+
+def test_bad_expert_ids_flag_status():
+    dev = cuda_device()
+    s = inputs.workload("tiny")
+    T = 8
+    cfg = m.config_from_shape(s, T_max=T)
+    ws = torch.zeros(m.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    x = inputs.gen_x(s, 0, device=dev, T=T)
+    t, d = _alloc_dispatch(s, T, dev)
+    t["topk_ids"].copy_(torch.tensor([[0, 1]] * T, dtype=torch.int32))
+    t["topk_ids"][3, 1] = s.E + 5            # out of range
+    t["topk_ids"][5, 0] = -1
+    t["topk_w"].fill_(0.5)
+    t["perm_src"].fill_(-7)
+    m.moe_dispatch(cfg, x, T, d, ws)
+    st = m.moe_read_status(cfg, ws)
+    assert st & m.MOE_DEV_BAD_EXPERT_ID
+    counts = np_(t["counts"])
+    assert counts.sum() == T * s.k - 2                     # the bad slots are skipped
+    inv = np_(t["inv"])
+    assert inv[3 * s.k + 1] == -1 and inv[5 * s.k + 0] == -1
+    assert (np_(t["perm_src"])[: counts.sum()] >= 0).all()
+    assert m.moe_read_status(cfg, ws) == 0                 # reading clears it
+
+
+def test_nan_logit_flags_status():
+    dev = cuda_device()
+    s = inputs.workload("tiny")
+    T = 4
+    cfg = m.config_from_shape(s, T_max=T)
+    ws = torch.zeros(m.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    logits = torch.randn(T, s.E, device=dev)
+    logits[2, 3] = float("nan")
+    ids = torch.empty(T, s.k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, s.k, dtype=torch.float32, device=dev)
+    m.moe_route_topk(cfg, logits, T, ids, w, ws)
+    assert m.moe_read_status(cfg, ws) & m.MOE_DEV_NAN_LOGIT
+    assert ((ids >= 0) & (ids < s.E)).all()
+    assert 3 not in ids[2].tolist()                         # NaN ranks last
+
+
+def test_launch_accounting_and_phases():
+    dev = cuda_device()
+    s = inputs.workload("tiny")
+    r = run_forward(s, s.T, dev=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_N_PHASE_EVENTS)]
+    for e in ev:
+        e.record()
+    m.moe_set_phase_events(ev)
+    m.moe_layer_forward(r["cfg"], r["x"], r["Wr"], None, s.T, r["packed"], r["out"], None, r["ws"])
+    m.moe_set_phase_events(None)
+    torch.cuda.synchronize()
+    n = m.moe_last_launch_count()
+    assert 5 <= n <= 12
+    ts = [ev[0].elapsed_time(e) for e in ev]
+    assert all(b >= a for a, b in zip(ts, ts[1:]))

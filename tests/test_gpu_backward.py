@@ -1,0 +1,103 @@
+"""Training forward + backward parity (MXFP8 weights, clamped SwiGLU).
+
+A reduced case is checked in full (every gradient entry); the full-size
+training workload is checked on the experts of one sampled token (their
+complete weight gradients) and on that token's dx and router gradient.
+"""
+import numpy as np
+import pytest
+import torch
+
+import inputs
+import quantized_grouped_gemm_topk_gb300 as m
+from oracle import backward as B
+from oracle import moe as M
+
+from gpu_harness import LazyExperts, oracle_forward, oracle_weights, run_forward
+from util import assert_close_layer, assert_mx_close, cuda_device, np_
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_backward(s, r, T, seed=0):
+    dev = r["x"].device
+    cfg = r["cfg"]
+    dout = inputs.gen_dout(s, seed, device=dev, T=T)
+    packed_d = m.moe_prepack_weights(cfg, r["wts"], m.MOE_PACK_DGRAD)
+    dx = torch.empty(T, s.H, dtype=torch.bfloat16, device=dev)
+    dW1 = torch.empty(s.E, s.H, 2 * s.I, dtype=torch.bfloat16, device=dev)
+    dW2 = torch.empty(s.E, s.I, s.H, dtype=torch.bfloat16, device=dev)
+    dlog = torch.empty(T, s.E, dtype=torch.float32, device=dev)
+    m.moe_layer_backward(cfg, dout, r["x"], T, r["save"], packed_d, dx, dW1, dW2, dlog, r["ws"])
+    torch.cuda.synchronize()
+    assert m.moe_read_status(cfg, r["ws"]) == 0
+    return dout, dx, dW1, dW2, dlog
+
+
+def _oracle_backward(s, r, f, dout, experts=None):
+    wts = oracle_weights(r["wts"])
+
+    def w1t(e):
+        from oracle import formats as F
+        return F.mx_dequantize(wts["w1t_q"][e], wts["w1t_s"][e])
+
+    def w2t(e):
+        from oracle import formats as F
+        return F.mx_dequantize(wts["w2t_q"][e], wts["w2t_s"][e])
+
+    return B.layer_backward(f, inputs.bf16_bits(r["x"]).cpu().numpy(), inputs.bf16_bits(dout).cpu().numpy(), wts,
+                            E=s.E, k=s.k, routed_scale=s.routed_scale, act=s.act, alpha=s.alpha, limit=s.limit,
+                            quant=True, experts=experts, w1t=w1t, w2t=w2t)
+
+
+def test_train_reduced_full_check():
+    dev = cuda_device()
+    s = inputs.workload("train", T=48, E=8)
+    r = run_forward(s, s.T, dev=dev, save=True)
+    f = oracle_forward(s, r)
+    assert (np_(r["views"]["topk_ids"]) == f.ids).all()
+    assert_mx_close(np_(r["views"]["y1_q"]), np_(r["views"]["y1_s"]), f.y1q, f.y1s, "y1")
+    assert_close_layer(np_(r["out"].float()), f.out, "out")
+    # saved pre-activation h (bf16) against the oracle's h
+    h = np_(r["save_bufs"]["h"].view(torch.bfloat16).float())[: s.T * s.kp]
+    assert_close_layer(h, f.h, "h")
+    dout, dx, dW1, dW2, dlog = _run_backward(s, r, s.T)
+    b = _oracle_backward(s, r, f, dout)
+    assert_close_layer(np_(dx.float()), b.dx, "dx")
+    assert_close_layer(np_(dW1.float()), b.dW1, "dW1")
+    assert_close_layer(np_(dW2.float()), b.dW2, "dW2")
+    assert_close_layer(np_(dlog), b.dlogits, "dlogits")
+
+
+def test_train_empty_expert_grads_are_zero():
+    dev = cuda_device()
+    s = inputs.workload("train", T=4, E=16)
+    r = run_forward(s, s.T, dev=dev, save=True)
+    counts = np_(r["views"]["counts"])
+    assert (counts == 0).any()
+    _, _, dW1, dW2, _ = _run_backward(s, r, s.T)
+    for e in np.nonzero(counts == 0)[0]:
+        assert (dW1[e] == 0).all() and (dW2[e] == 0).all()
+
+
+@pytest.mark.slow
+def test_train_full_size_sampled():
+    dev = cuda_device()
+    s = inputs.workload("train")
+    T = s.T
+    r = run_forward(s, T, dev=dev, save=True)
+    ids = np_(r["views"]["topk_ids"])
+    t0 = 0
+    experts = sorted(set(int(e) for e in ids[t0]))
+    offs = np_(r["views"]["offsets"])
+    rows = [rr for e in experts for rr in range(offs[e], offs[e + 1])]
+    f = oracle_forward(s, r, rows=rows)
+    assert (ids == f.ids).all()
+    assert_close_layer(np_(r["out"].float())[t0], f.out[t0], "out[t0]")
+    dout, dx, dW1, dW2, dlog = _run_backward(s, r, T)
+    b = _oracle_backward(s, r, f, dout, experts=experts)
+    assert_close_layer(np_(dx.float())[t0], b.dx[t0], "dx[t0]")
+    assert_close_layer(np_(dlog)[t0], b.dlogits[t0], "dlogits[t0]")
+    for e in experts:
+        assert_close_layer(np_(dW1[e].float()), b.dW1[e], f"dW1[{e}]")
+        assert_close_layer(np_(dW2[e].float()), b.dW2[e], f"dW2[{e}]")
