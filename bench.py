@@ -66,7 +66,7 @@ def peaks():
 
 def kernel_source_sha():
     h = hashlib.sha256()
-    for f in ("gemm_cc.cu", "common.cuh", "internal.cuh"):
+    for f in ("gemm_tc.cu", "tc.cuh", "common.cuh", "internal.cuh"):
         h.update(open(os.path.join(ROOT, "quantized_grouped_gemm_topk_gb300", "csrc", f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -332,7 +332,7 @@ def run_ours(args, s, rank, world, local):
     sha = kernel_source_sha()
     tr = traffic_per_launch(sha)
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-            "traffic": None, "kernel": "W1 grouped GEMM (k_gemm_cc)", "peak_source": f"{peak_kind} hbm_gbs",
+            "traffic": None, "kernel": "W1 grouped GEMM (k_gemm_tc)", "peak_source": f"{peak_kind} hbm_gbs",
             "algorithmic_bytes": "touched experts x NVFP4 W1 bytes (2I*H/2 + 2I*H/16) + MXFP8 rows in and out",
             "kernel_us_per_step": w1_us / K}
     if tr is not None:

@@ -304,7 +304,7 @@ moe_status_t moe_router_logits(const moe_config_t* c, const uint16_t* x, const f
   cudaStream_t st = (cudaStream_t)stream;
   reset_launch_count();
   const WsLayout L = ws_layout(*c);
-  const int KS = router_splits(T, c->H);
+  const int KS = router_splits(T, c->H, c->E);
   if (KS == 1) {
     MOE_CHECK_CUDA(launch_router(x, W_r, T, c->H, c->E, 1, logits, st));
     return MOE_OK;
@@ -435,7 +435,7 @@ static moe_status_t tc_gemm(const moe_config_t* c, const PackLayout& P, int mat,
   g.status = at<int32_t>(ws, L.status);
   CUtensorMap map;
   if (!make_tmap_f16(&map, a16, R, g.K)) return MOE_ERR_CUDA;
-  MOE_CHECK_CUDA(launch_gemm_tc(g, map, st));
+  MOE_CHECK_CUDA(launch_gemm_tc(g, map, tc_token_tile(T, c->k + c->n_shared, c->E + c->n_shared), st));
   run->out = g.out;
   run->split_stride = g.split_stride;
   run->S = g.S;
@@ -559,7 +559,7 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
   a.logits = v.logits;
   phase(0, st);
   if (W_r) {
-    const int KS = router_splits(T, c->H);
+    const int KS = router_splits(T, c->H, c->E);
     float* part = KS == 1 ? v.logits : at<float>(ws, L.rpart);
     MOE_CHECK_CUDA(launch_router(x, W_r, T, c->H, c->E, KS, part, st));
     a.part = part; a.KS = KS;

@@ -20,55 +20,46 @@ static int grid_for(int64_t warps, int warps_per_block) {
 }
 
 // ---- W1 epilogue --------------------------------------------------------------
-// Warp per row: pass 1 sums the K-slice partials, forms
-// y = w_row * act(g, u) and quantises each 32-block of y to MXFP8; pass 2
-// (when y16 is requested) re-expresses the row's MXFP8 values as f16 relative
-// to the row's largest block exponent, the B operand of the W2 GEMM.
+// Warp per (row, 32-block of I): sums the K-slice partials, forms
+// y = w_row * act(g, u) and quantises the block of y to MXFP8.
 __global__ void __launch_bounds__(256) k_w1_finalize(const W1FinArgs a) {
   const int lane = threadIdx.x & 31;
   const int nb = a.I / 32;
   const int Rv = min(a.R, a.offsets[a.G]);
+  const int64_t total = (int64_t)Rv * nb;
   const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); r < Rv; r += nw) {
+  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); w < total; w += nw) {
+    const int64_t r = w / nb;
+    const int b = (int)(w % nb);
+    const int i = b * 32 + lane;
     const float* P = a.P + r * 2 * a.I;
-    const float wr = a.w_row[r];
-    int emax = 0;
-    for (int b = 0; b < nb; ++b) {
-      const int i = b * 32 + lane;
-      float g = 0.f, u = 0.f;
-      for (int s = 0; s < a.S; ++s) {
-        g += P[(int64_t)s * a.split_stride + i];
-        u += P[(int64_t)s * a.split_stride + a.I + i];
-      }
-      const float y = wr * act_fwd(g, u, a.act);
-      const int e = mx_exponent(warp_max(fabsf(y)));
-      emax = max(emax, e + 127);
-      const uint16_t c = f32x2_to_e4m3x2(y * pow2_neg(e), 0.f);
-      a.y1q[r * a.I + i] = (uint8_t)(c & 0xffu);
-      if (lane == 0) a.y1s[r * nb + b] = (uint8_t)(e + 127);
-      if (a.h_save) {
-        a.h_save[r * 2 * a.I + i] = f32_to_bf16_bits(g);
-        a.h_save[r * 2 * a.I + a.I + i] = f32_to_bf16_bits(u);
-      }
-      if (a.y_save) a.y_save[r * a.I + i] = y;
+    float g = 0.f, u = 0.f;
+    for (int s = 0; s < a.S; ++s) {
+      g += P[(int64_t)s * a.split_stride + i];
+      u += P[(int64_t)s * a.split_stride + a.I + i];
     }
-    if (a.y16) {
-      __syncwarp();
-      for (int b = 0; b < nb; ++b) {
-        const int i = b * 32 + lane;
-        const float f = ldexpf(1.0f, (int)a.y1s[r * nb + b] - emax);
-        const float v = e4m3_to_f32(a.y1q[r * a.I + i]) * f;
-        a.y16[r * a.I + i] = __half_as_ushort(__float2half_rn(v));
-      }
-      if (lane == 0) a.y_rowexp[r] = emax - 127;
+    const float y = a.w_row[r] * act_fwd(g, u, a.act);
+    const int e = mx_exponent(warp_max(fabsf(y)));
+    const uint16_t c = f32x2_to_e4m3x2(y * pow2_neg(e), 0.f);
+    a.y1q[r * a.I + i] = (uint8_t)(c & 0xffu);
+    if (lane == 0) a.y1s[r * nb + b] = (uint8_t)(e + 127);
+    if (a.h_save) {
+      a.h_save[r * 2 * a.I + i] = f32_to_bf16_bits(g);
+      a.h_save[r * 2 * a.I + a.I + i] = f32_to_bf16_bits(u);
     }
+    if (a.y_save) a.y_save[r * a.I + i] = y;
   }
 }
 
 cudaError_t launch_w1_finalize(const W1FinArgs& a, cudaStream_t st) {
   if (a.R == 0) return cudaSuccess;
-  k_w1_finalize<<<grid_for(a.R, 8), 256, 0, st>>>(a);
+  k_w1_finalize<<<grid_for((int64_t)a.R * (a.I / 32), 8), 256, 0, st>>>(a);
   note_launch();
+  if (a.y16) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_act_f16(a.y1q, a.y1s, a.I, nullptr, 1, a.R, a.offsets, a.G, a.y16, a.y_rowexp, st);
+  }
   return cudaGetLastError();
 }
 

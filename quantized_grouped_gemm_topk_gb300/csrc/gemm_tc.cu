@@ -1,6 +1,6 @@
 // Grouped GEMM on the 5th-generation tensor cores (tcgen05), operand-swapped:
 // the MMA's M side is 128 output features of one expert tile, its N side the
-// expert's tokens (16..64 per MMA), so a decode step with a handful of tokens
+// expert's tokens (16..NT per MMA), so a decode step with a handful of tokens
 // per expert still streams every weight byte exactly once.
 //
 // GC-MoE summary (arxiv-wiki "GC-MoE: Overlapping Expert-Parallel Token
@@ -17,17 +17,24 @@
 // accumulation in tensor memory.
 //
 // Roles (one CTA per SM, persistent over work units):
-//   warp 0      producer: one bulk copy per 64-wide K chunk of the weight tile
-//               (codes + scales, contiguous), plus TMA loads of the f16
-//               activation rows of the chunk (16-row boxes, 128-byte swizzle)
-//   warp 1      MMA issuer: 4 MMAs (K = 16 each) per chunk, A from tensor
-//               memory, B from shared memory; commits free the A buffer and
-//               the shared-memory stage
-//   warps 2-5   decoders: thread = weight row = tensor-memory lane
-//   warps 6-9   epilogue: tensor memory -> fp32 partials in global memory,
+//   warp 0      producer: per pipeline stage one bulk copy of CG consecutive
+//               64-wide K chunks of the weight tile (codes + scales), plus TMA
+//               loads of the f16 activation rows of those chunks (16-row
+//               boxes, 128-byte swizzle)
+//   warps 1,14.. MMA issuers (P of them), taking A buffers round-robin:
+//               4 MMAs (K = 16 each) per chunk, A from tensor memory, B from
+//               shared memory, each issuer into its own accumulator; commits
+//               free the A buffer and, per stage, the shared-memory slot. An
+//               issuing thread stalls ~90 cycles on every small-N MMA it
+//               queues, so P issuers keep the tensor pipe fed.
+//   warps 2-9   decoders, two groups of four taking alternate A buffers:
+//               thread = weight row = tensor-memory lane
+//   warps 10-13 epilogue: tensor memory -> fp32 partials in global memory,
 //               scaled by the per-row weight factor and the per-token
 //               activation exponent
-// Work unit = (expert with rows, 128-feature tile, K slice, 64-token tile).
+// Work unit = (expert with rows, 128-feature tile, K slice, NT-token tile).
+// The stage ring keeps ~130 KB of weights in flight per SM, which HBM latency
+// needs at full bandwidth.
 // Every wait is bounded in time; on a timeout the CTA sets a status bit,
 // drains its own copies and MMAs, frees tensor memory and returns.
 #include "internal.cuh"
@@ -35,20 +42,24 @@
 
 namespace moe {
 
-constexpr int kTcStages = 12;
-constexpr int kTcNA = 4;          // tensor-memory A buffers (32 columns each)
-constexpr int kTcNT = 64;         // tokens per MMA tile (columns of one D buffer)
-constexpr int kTcThreads = 320;
-constexpr int kTcBSlot = kTcNT * 128;   // 64 rows x 128 bytes of f16
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kDCol0 = kTcNA * 32;
+constexpr int kTcNA = 4;          // tensor-memory A buffers, two 64-K chunks (64 columns) each
+constexpr int kTcThreads = 544;   // 17 warps: producer, 4 issuers, 8 decoders, 4 epilogue
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kDCol0 = kTcNA * 64;
+constexpr int kSmemBudget = 212 * 1024;
 
-template <int FMT>
+template <int FMT, int NT>
 struct TcCfg {
+  // Each MMA issuer accumulates into its own NT-column tile; a D buffer
+  // holds all of them and the epilogue adds them.
+  static constexpr int P = NT <= 32 ? 4 : 2;                         // MMA issuers
+  static constexpr int DStride = P * NT;                             // TMEM columns per D buffer
   static constexpr int CB = FMT == MOE_WFMT_NVFP4 ? 4608 : 8448;     // chunk bytes
-  static constexpr int ASlot = FMT == MOE_WFMT_NVFP4 ? 5120 : 9216;  // 1024-aligned
-  static constexpr int StageBytes = ASlot + kTcBSlot;
-  static constexpr int Stages = FMT == MOE_WFMT_NVFP4 ? kTcStages : 9;
+  static constexpr int CG = FMT == MOE_WFMT_NVFP4 ? 4 : 2;           // chunks per stage
+  static constexpr int ASlot = (CG * CB + 1023) / 1024 * 1024;
+  static constexpr int BChunk = NT * 128;                             // NT rows x 64 f16
+  static constexpr int StageBytes = ASlot + CG * BChunk;
+  static constexpr int Stages = kSmemBudget / StageBytes > 16 ? 16 : kSmemBudget / StageBytes;
   static constexpr int SmemBytes = Stages * StageBytes + 1024 /*align*/ + 1024 /*barriers*/;
 };
 
@@ -95,10 +106,50 @@ __device__ __forceinline__ uint32_t f16x2_pow2(int d) {
   return h | (h << 16);
 }
 
+// Decodes one 64-wide K chunk of packed weight row p into 32 f16x2 words
+// (element pairs in K order).
 template <int FMT>
+__device__ __forceinline__ void decode_chunk(const uint8_t* sa, int p, int rexp, uint32_t (&v)[32]) {
+  if (FMT == MOE_WFMT_NVFP4) {
+    const uint4 g0 = *reinterpret_cast<const uint4*>(sa + p * 16);
+    const uint4 g1 = *reinterpret_cast<const uint4*>(sa + 2048 + p * 16);
+    const uint32_t sc = *reinterpret_cast<const uint32_t*>(sa + 4096 + p * 4);
+    const uint32_t s01 = e4m3x2_f16x2(sc & 0xffffu), s23 = e4m3x2_f16x2(sc >> 16);
+    const uint32_t ss[4] = {(s01 & 0xffffu) * 0x10001u, (s01 >> 16) * 0x10001u, (s23 & 0xffffu) * 0x10001u,
+                            (s23 >> 16) * 0x10001u};
+    const uint32_t wd[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      uint32_t o0, o1, o2, o3;
+      e2m1x8_f16x2(wd[i], o0, o1, o2, o3);
+      const uint32_t s = ss[i >> 1];
+      v[4 * i + 0] = hmul2_bits(o0, s);
+      v[4 * i + 1] = hmul2_bits(o1, s);
+      v[4 * i + 2] = hmul2_bits(o2, s);
+      v[4 * i + 3] = hmul2_bits(o3, s);
+    }
+  } else {
+    const uint32_t sc = *reinterpret_cast<const uint16_t*>(sa + 8192 + p * 2);
+    const uint32_t f0 = f16x2_pow2((int)(sc & 0xffu) - 127 - rexp);
+    const uint32_t f1 = f16x2_pow2((int)(sc >> 8) - 127 - rexp);
+#pragma unroll
+    for (int gi = 0; gi < 4; ++gi) {
+      const uint4 gr = *reinterpret_cast<const uint4*>(sa + gi * 2048 + p * 16);
+      const uint32_t wd[4] = {gr.x, gr.y, gr.z, gr.w};
+      const uint32_t f = gi < 2 ? f0 : f1;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[gi * 8 + 2 * i] = hmul2_bits(e4m3x2_f16x2(wd[i] & 0xffffu), f);
+        v[gi * 8 + 2 * i + 1] = hmul2_bits(e4m3x2_f16x2(wd[i] >> 16), f);
+      }
+    }
+  }
+}
+
+template <int FMT, int NT>
 __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant__ TcArgs g,
                                                            const __grid_constant__ CUtensorMap tmap_b) {
-  using C = TcCfg<FMT>;
+  using C = TcCfg<FMT, NT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* stages = smem;
@@ -117,17 +168,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::Stages; ++i) {
       tc::mbar_init(&full[i], 1);
-      tc::mbar_init(&empty[i], 1);
+      tc::mbar_init(&empty[i], C::P);
     }
     for (int i = 0; i < kTcNA; ++i) {
       tc::mbar_init(&afull[i], 128);
       tc::mbar_init(&afree[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
-      tc::mbar_init(&dfull[i], 1);
+      tc::mbar_init(&dfull[i], C::P);
       tc::mbar_init(&dfree[i], 128);
     }
-    tc::mbar_init(drain, 1);
+    tc::mbar_init(drain, C::P);     // one commit from each MMA issuer
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -151,18 +202,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
         TcUnit w;
         if (!tc_unit(g, u, nchunks, w)) continue;
         const uint8_t* tile = g.w + ((int64_t)w.e * g.tiles + w.j) * g.tile_bytes;
-        for (int t0 = w.r0; ok && t0 < w.r1; t0 += kTcNT) {
-          const int nb16 = (min(kTcNT, w.r1 - t0) + 15) >> 4;
-          for (int c = w.c0; c < w.c1; ++c, ++it) {
+        for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT) {
+          const int nb16 = (min(NT, w.r1 - t0) + 15) >> 4;
+          for (int c = w.c0; c < w.c1; c += C::CG, ++it) {
+            const int nc = min(C::CG, w.c1 - c);
             const int st = it % C::Stages;
             const uint32_t ph = (it / C::Stages) & 1;
             if (!tc::mbar_wait(&empty[st], ph ^ 1, abort)) { ok = false; break; }
             uint8_t* sa = stages + st * C::StageBytes;
             uint8_t* sb = sa + C::ASlot;
-            tc::mbar_arrive_expect_tx(&full[st], C::CB + nb16 * 2048);
-            tc::bulk_g2s(sa, tile + (int64_t)c * C::CB, C::CB, &full[st], pol_w);
-            for (int b = 0; b < nb16; ++b) tc::tma_load_2d(sb + b * 2048, &tmap_b, c * kChunkK, t0 + b * 16,
-                                                           &full[st], pol_a);
+            tc::mbar_arrive_expect_tx(&full[st], nc * (C::CB + nb16 * 2048));
+            tc::bulk_g2s(sa, tile + (int64_t)c * C::CB, nc * C::CB, &full[st], pol_w);
+            for (int ci = 0; ci < nc; ++ci)
+              for (int b = 0; b < nb16; ++b)
+                tc::tma_load_2d(sb + ci * C::BChunk + b * 2048, &tmap_b, (c + ci) * kChunkK, t0 + b * 16, &full[st],
+                                pol_a);
           }
         }
       }
@@ -177,32 +231,45 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
         }
       }
     }
-  } else if (warp == 1) {
-    // ---------------- MMA issuer ----------------
-    if (lane == 0) {
+  } else if (warp == 1 || warp >= 14) {
+    // ---------------- MMA issuers ----------------
+    const uint32_t mine = warp == 1 ? 0u : (uint32_t)(warp - 13);   // A buffers with (index % P) == mine
+    if (lane == 0 && mine < (uint32_t)C::P) {
       uint32_t it = 0, ait = 0, dit = 0;
       bool ok = true;
       for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
         TcUnit w;
         if (!tc_unit(g, u, nchunks, w)) continue;
-        for (int t0 = w.r0; ok && t0 < w.r1; t0 += kTcNT) {
-          const int nmma = ((min(kTcNT, w.r1 - t0) + 15) >> 4) << 4;
+        for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT) {
+          const int nmma = ((min(NT, w.r1 - t0) + 15) >> 4) << 4;
           const uint32_t idesc = tc::idesc_f16_f32(128, nmma);
           const int d = dit & 1;
           if (!tc::mbar_wait(&dfree[d], ((dit >> 1) & 1) ^ 1, abort)) { ok = false; break; }
           tc::fence_after_sync();
-          const uint32_t dt = tmem + kDCol0 + d * kTcNT;
-          for (int c = w.c0; c < w.c1; ++c, ++it, ++ait) {
+          const uint32_t dt = tmem + kDCol0 + d * C::DStride + mine * NT;
+          bool started = false;
+          for (int c = w.c0; ok && c < w.c1; c += C::CG, ++it) {
+            const int nc = min(C::CG, w.c1 - c);
             const int st = it % C::Stages;
-            const int a = ait % kTcNA;
             if (!tc::mbar_wait(&full[st], (it / C::Stages) & 1, abort)) { ok = false; break; }
-            if (!tc::mbar_wait(&afull[a], (ait / kTcNA) & 1, abort)) { ok = false; break; }
-            tc::fence_after_sync();
-            const uint64_t bd = tc::smem_desc_sw128(tc::smem_u32(stages + st * C::StageBytes + C::ASlot));
+            const uint32_t sb = tc::smem_u32(stages + st * C::StageBytes + C::ASlot);
+            for (int cp = 0; cp < nc; cp += 2, ++ait) {
+              if (ait % C::P != mine) continue;
+              const int a = ait % kTcNA;
+              if (!tc::mbar_wait(&afull[a], (ait / kTcNA) & 1, abort)) { ok = false; break; }
+              tc::fence_after_sync();
+              const int np = min(2, nc - cp);
+              for (int h = 0; h < np; ++h) {
+                const uint64_t bd = tc::smem_desc_sw128(sb + (cp + h) * C::BChunk);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              tc::mma_f16_ts(dt, tmem + a * 32 + kk * 8, bd + (uint64_t)(kk * 2), idesc, (c > w.c0 || kk > 0) ? 1u : 0u);
-            tc::mma_commit(&afree[a]);
+                for (int kk = 0; kk < 4; ++kk)
+                  tc::mma_f16_ts(dt, tmem + a * 64 + h * 32 + kk * 8, bd + (uint64_t)(kk * 2), idesc,
+                                 (started || h > 0 || kk > 0) ? 1u : 0u);
+              }
+              started = true;
+              tc::mma_commit(&afree[a]);
+            }
+            if (!ok) break;
             tc::mma_commit(&empty[st]);
           }
           if (!ok) break;
@@ -212,11 +279,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       }
       // every MMA of this thread has completed once `drain` fires
       tc::mma_commit(drain);
-      volatile int zero = 0;
-      tc::mbar_wait(drain, 0, &zero, 200000000ull);
+      volatile int never = 0;
+      tc::mbar_wait(drain, 0, &never, 200000000ull);
     }
-  } else if (warp < 6) {
+  } else if (warp < 10) {
     // ---------------- decoders ----------------
+    const uint32_t grp = (uint32_t)(warp - 2) >> 2;   // A buffers with (index % 2) == grp
     const int q = warp & 3;
     const int p = q * 32 + lane;                  // weight row = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
@@ -227,53 +295,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       if (!tc_unit(g, u, nchunks, w)) continue;
       int rexp = 0;
       if (FMT == MOE_WFMT_MXFP8) rexp = g.wrowexp[((int64_t)w.e * g.tiles + w.j) * kTileN + p];
-      for (int t0 = w.r0; ok && t0 < w.r1; t0 += kTcNT) {
-        for (int c = w.c0; c < w.c1; ++c, ++it, ++ait) {
+      for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT) {
+        for (int c = w.c0; ok && c < w.c1; c += C::CG, ++it) {
+          const int nc = min(C::CG, w.c1 - c);
           const int st = it % C::Stages;
-          if (!tc::mbar_wait(&full[st], (it / C::Stages) & 1, abort)) { ok = false; break; }
+          // Wait only on stages holding one of this group's pairs: a stage
+          // without one can be consumed and refilled (two phase flips) before
+          // this group gets to it.
+          const bool has_pair = ((nc + 1) >> 1) >= 2 || (ait & 1u) == grp;
+          if (has_pair && !tc::mbar_wait(&full[st], (it / C::Stages) & 1, abort)) { ok = false; break; }
           const uint8_t* sa = stages + st * C::StageBytes;
-          uint32_t v[32];
-          if (FMT == MOE_WFMT_NVFP4) {
-            const uint4 g0 = *reinterpret_cast<const uint4*>(sa + p * 16);
-            const uint4 g1 = *reinterpret_cast<const uint4*>(sa + 2048 + p * 16);
-            const uint32_t sc = *reinterpret_cast<const uint32_t*>(sa + 4096 + p * 4);
-            const uint32_t s01 = e4m3x2_f16x2(sc & 0xffffu), s23 = e4m3x2_f16x2(sc >> 16);
-            const uint32_t ss[4] = {(s01 & 0xffffu) * 0x10001u, (s01 >> 16) * 0x10001u, (s23 & 0xffffu) * 0x10001u,
-                                    (s23 >> 16) * 0x10001u};
-            const uint32_t wd[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              uint32_t o0, o1, o2, o3;
-              e2m1x8_f16x2(wd[i], o0, o1, o2, o3);
-              const uint32_t s = ss[i >> 1];
-              v[4 * i + 0] = hmul2_bits(o0, s);
-              v[4 * i + 1] = hmul2_bits(o1, s);
-              v[4 * i + 2] = hmul2_bits(o2, s);
-              v[4 * i + 3] = hmul2_bits(o3, s);
+          for (int cp = 0; cp < nc; cp += 2, ++ait) {
+            if ((ait & 1u) != grp) continue;
+            uint32_t v[32];
+            decode_chunk<FMT>(sa + cp * C::CB, p, rexp, v);
+            const int a = ait % kTcNA;
+            if (!tc::mbar_wait(&afree[a], ((ait / kTcNA) & 1) ^ 1, abort)) { ok = false; break; }
+            tc::fence_after_sync();
+            tc::tmem_st32(lane_base + a * 64, v);
+            if (cp + 1 < nc) {
+              decode_chunk<FMT>(sa + (cp + 1) * C::CB, p, rexp, v);
+              tc::tmem_st32(lane_base + a * 64 + 32, v);
             }
-          } else {
-            const uint32_t sc = *reinterpret_cast<const uint16_t*>(sa + 8192 + p * 2);
-            const uint32_t f0 = f16x2_pow2((int)(sc & 0xffu) - 127 - rexp);
-            const uint32_t f1 = f16x2_pow2((int)(sc >> 8) - 127 - rexp);
-#pragma unroll
-            for (int gi = 0; gi < 4; ++gi) {
-              const uint4 gr = *reinterpret_cast<const uint4*>(sa + gi * 2048 + p * 16);
-              const uint32_t wd[4] = {gr.x, gr.y, gr.z, gr.w};
-              const uint32_t f = gi < 2 ? f0 : f1;
-#pragma unroll
-              for (int i = 0; i < 4; ++i) {
-                v[gi * 8 + 2 * i] = hmul2_bits(e4m3x2_f16x2(wd[i] & 0xffffu), f);
-                v[gi * 8 + 2 * i + 1] = hmul2_bits(e4m3x2_f16x2(wd[i] >> 16), f);
-              }
-            }
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            tc::mbar_arrive(&afull[a]);
           }
-          const int a = ait % kTcNA;
-          if (!tc::mbar_wait(&afree[a], ((ait / kTcNA) & 1) ^ 1, abort)) { ok = false; break; }
-          tc::fence_after_sync();
-          tc::tmem_st32(lane_base + a * 32, v);
-          tc::tmem_wait_st();
-          tc::fence_before_sync();
-          tc::mbar_arrive(&afull[a]);
         }
       }
     }
@@ -282,11 +329,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
     const int q = warp & 3;
     const int p = q * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-    uint32_t dit = 0;
+    uint32_t dit = 0, ait = 0;
     bool ok = true;
     for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
       TcUnit w;
       if (!tc_unit(g, u, nchunks, w)) continue;
+      // A-buffer pairs per token tile (same count the issuers walk)
+      int pairs = 0;
+      for (int c = w.c0; c < w.c1; c += C::CG) pairs += (min(C::CG, w.c1 - c) + 1) >> 1;
       int n;
       if (g.interleave_I > 0) n = p < 64 ? 64 * w.j + p : g.interleave_I + 64 * w.j + (p - 64);
       else n = kTileN * w.j + p;
@@ -295,20 +345,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       if (FMT == MOE_WFMT_NVFP4) rowf = g.gs ? g.gs[w.e] : 1.0f;
       else rowf = ldexpf(1.0f, g.wrowexp[((int64_t)w.e * g.tiles + w.j) * kTileN + p]);
       float* outp = g.out + (int64_t)w.s * g.split_stride + n;
-      for (int t0 = w.r0; t0 < w.r1; t0 += kTcNT) {
-        const int nt = min(kTcNT, w.r1 - t0);
+      for (int t0 = w.r0; t0 < w.r1; t0 += NT) {
+        const int nt = min(NT, w.r1 - t0);
+        // issuer m wrote its tile iff one of this tile's pairs had index = m (mod P)
+        const uint32_t a_first = ait;
+        ait += pairs;
         const int d = dit & 1;
         if (!tc::mbar_wait(&dfull[d], (dit >> 1) & 1, abort)) { ok = false; break; }
         tc::fence_after_sync();
         for (int cb = 0; cb < nt; cb += 16) {
-          uint32_t v[16];
-          tc::tmem_ld16(lane_base + kDCol0 + d * kTcNT + cb, v);
-          tc::tmem_wait_ld();
+          float acc[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+#pragma unroll
+          for (int ac = 0; ac < C::P; ++ac) {
+            if (pairs < C::P && (uint32_t)((ac - (int)(a_first % C::P) + C::P) % C::P) >= (uint32_t)pairs) continue;
+            uint32_t v[16];
+            tc::tmem_ld16(lane_base + kDCol0 + d * C::DStride + ac * NT + cb, v);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(v[i]);
+          }
           if (nvalid) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
               const int t = t0 + cb + i;
-              if (cb + i < nt) outp[(int64_t)t * g.N] = __uint_as_float(v[i]) * rowf * ldexpf(1.0f, g.act_rowexp[t]);
+              if (cb + i < nt) outp[(int64_t)t * g.N] = acc[i] * rowf * ldexpf(1.0f, g.act_rowexp[t]);
             }
           }
         }
@@ -362,27 +424,40 @@ bool make_tmap_f16(CUtensorMap* map, const void* base, int64_t rows, int64_t col
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t launch_gemm_tc(const TcArgs& g, const CUtensorMap& tmap_b, cudaStream_t st) {
+template <int FMT, int NT>
+static cudaError_t launch_tc_t(const TcArgs& g, const CUtensorMap& tmap_b, int grid, cudaStream_t st) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<FMT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         TcCfg<FMT, NT>::SmemBytes);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  k_gemm_tc<FMT, NT><<<grid, kTcThreads, TcCfg<FMT, NT>::SmemBytes, st>>>(g, tmap_b);
+  return cudaGetLastError();
+}
+
+int tc_token_tile(int T, int kp, int G) {
+  const double avg = (double)T * kp / std::max(G, 1);
+  if (avg <= 12.0) return 16;
+  if (avg <= 24.0) return 32;
+  return 64;
+}
+
+cudaError_t launch_gemm_tc(const TcArgs& g, const CUtensorMap& tmap_b, int nt, cudaStream_t st) {
   const int grid = std::max(1, g.max_ctas);
+  cudaError_t e;
   if (g.fmt == MOE_WFMT_NVFP4) {
-    static bool attr = false;
-    if (!attr) {
-      cudaFuncSetAttribute(k_gemm_tc<MOE_WFMT_NVFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           TcCfg<MOE_WFMT_NVFP4>::SmemBytes);
-      attr = true;
-    }
-    k_gemm_tc<MOE_WFMT_NVFP4><<<grid, kTcThreads, TcCfg<MOE_WFMT_NVFP4>::SmemBytes, st>>>(g, tmap_b);
+    e = nt <= 16 ? launch_tc_t<MOE_WFMT_NVFP4, 16>(g, tmap_b, grid, st)
+        : nt <= 32 ? launch_tc_t<MOE_WFMT_NVFP4, 32>(g, tmap_b, grid, st)
+                   : launch_tc_t<MOE_WFMT_NVFP4, 64>(g, tmap_b, grid, st);
   } else {
-    static bool attr = false;
-    if (!attr) {
-      cudaFuncSetAttribute(k_gemm_tc<MOE_WFMT_MXFP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           TcCfg<MOE_WFMT_MXFP8>::SmemBytes);
-      attr = true;
-    }
-    k_gemm_tc<MOE_WFMT_MXFP8><<<grid, kTcThreads, TcCfg<MOE_WFMT_MXFP8>::SmemBytes, st>>>(g, tmap_b);
+    e = nt <= 16 ? launch_tc_t<MOE_WFMT_MXFP8, 16>(g, tmap_b, grid, st)
+        : nt <= 32 ? launch_tc_t<MOE_WFMT_MXFP8, 32>(g, tmap_b, grid, st)
+                   : launch_tc_t<MOE_WFMT_MXFP8, 64>(g, tmap_b, grid, st);
   }
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 // ---------------------------------------------------------------------------
@@ -391,52 +466,54 @@ cudaError_t launch_gemm_tc(const TcArgs& g, const CUtensorMap& tmap_b, cudaStrea
 // the largest block exponent of the row (unbiased), so the product of the
 // two is the MXFP8 value exactly unless a block sits more than 15 binades
 // below the row's largest block (then bits below 2^-24 of the row scale are
-// rounded away).
+// rounded away). One warp per (row, 256-column slice); every warp derives the
+// row exponent from the row's scale bytes itself.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void f16_row_from_mx(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int C,
-                                                uint16_t* __restrict__ dst, int32_t* rowexp_out, int lane) {
-  const int nb = C / 32;
-  int mx = 0;
-  for (int b = lane; b < nb; b += 32) mx = max(mx, (int)s[b]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(kFull, mx, o));
-  if (lane == 0) *rowexp_out = mx - 127;
-  for (int c0 = lane * 8; c0 < C; c0 += 256) {
-    const uint2 codes = *reinterpret_cast<const uint2*>(q + c0);
-    const float f = ldexpf(1.0f, (int)s[c0 / 32] - mx);
-    uint32_t outw[4];
-    const uint32_t cw[2] = {codes.x, codes.y};
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const float2 lo = e4m3x2_to_f32x2((uint16_t)(cw[i] & 0xffffu));
-      const float2 hi = e4m3x2_to_f32x2((uint16_t)(cw[i] >> 16));
-      const __half2 h0 = __floats2half2_rn(lo.x * f, lo.y * f);
-      const __half2 h1 = __floats2half2_rn(hi.x * f, hi.y * f);
-      outw[2 * i] = *reinterpret_cast<const uint32_t*>(&h0);
-      outw[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&h1);
-    }
-    *reinterpret_cast<uint4*>(dst + c0) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-  }
-}
-
-// warp per row r < min(R, offsets[G]); source row row_map[r] / row_div.
 __global__ void __launch_bounds__(256) k_act_f16(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int C,
                                                  const int32_t* __restrict__ row_map, int row_div, int R,
                                                  const int32_t* __restrict__ offsets, int G, uint16_t* __restrict__ a16,
                                                  int32_t* __restrict__ rowexp) {
   const int lane = threadIdx.x & 31;
   const int Rv = min(R, offsets[G]);
+  const int nsl = (C + 255) / 256;
+  const int nb = C / 32;
+  const int64_t total = (int64_t)Rv * nsl;
   const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); r < Rv; r += nw) {
+  for (int64_t wi = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); wi < total; wi += nw) {
+    const int64_t r = wi / nsl;
+    const int sl = (int)(wi % nsl);
     const int64_t src = row_map ? (int64_t)(row_map[r] / row_div) : r;
-    f16_row_from_mx(q + src * C, s + src * (C / 32), C, a16 + r * C, rowexp + r, lane);
+    const uint8_t* sr = s + src * nb;
+    int mx = 0;
+    for (int b = lane; b < nb; b += 32) mx = max(mx, (int)sr[b]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(kFull, mx, o));
+    if (sl == 0 && lane == 0) rowexp[r] = mx - 127;
+    const int c0 = sl * 256 + lane * 8;
+    if (c0 < C) {
+      const uint2 codes = *reinterpret_cast<const uint2*>(q + src * C + c0);
+      const float f = ldexpf(1.0f, (int)sr[c0 / 32] - mx);
+      uint32_t outw[4];
+      const uint32_t cw[2] = {codes.x, codes.y};
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        const float2 lo = e4m3x2_to_f32x2((uint16_t)(cw[i] & 0xffffu));
+        const float2 hi = e4m3x2_to_f32x2((uint16_t)(cw[i] >> 16));
+        const __half2 h0 = __floats2half2_rn(lo.x * f, lo.y * f);
+        const __half2 h1 = __floats2half2_rn(hi.x * f, hi.y * f);
+        outw[2 * i] = *reinterpret_cast<const uint32_t*>(&h0);
+        outw[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&h1);
+      }
+      *reinterpret_cast<uint4*>(a16 + r * C + c0) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+    }
   }
 }
 
 cudaError_t launch_act_f16(const uint8_t* q, const uint8_t* s, int C, const int32_t* row_map, int row_div, int R,
                            const int32_t* offsets, int G, uint16_t* a16, int32_t* rowexp, cudaStream_t st) {
   if (R == 0) return cudaSuccess;
-  const int blocks = (int)std::min<int64_t>((R + 7) / 8, 152 * 16);
+  const int64_t warps = (int64_t)R * ((C + 255) / 256);
+  const int blocks = (int)std::min<int64_t>((warps + 7) / 8, 152 * 16);
   k_act_f16<<<blocks, 256, 0, st>>>(q, s, C, row_map, row_div, R, offsets, G, a16, rowexp);
   note_launch();
   return cudaGetLastError();

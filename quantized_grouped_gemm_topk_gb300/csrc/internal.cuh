@@ -35,7 +35,7 @@ struct RouteArgs {
   int32_t* status;
 };
 
-int router_splits(int T, int H);
+int router_splits(int T, int H, int E);
 bool use_small_route(int T, int G, int kp);
 cudaError_t launch_router(const uint16_t* x, const float* Wr, int T, int H, int E, int KS, float* part,
                           cudaStream_t st);
@@ -67,7 +67,10 @@ struct TcArgs {
   int32_t* status;
 };
 bool make_tmap_f16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols);
-cudaError_t launch_gemm_tc(const TcArgs& g, const CUtensorMap& tmap_b, cudaStream_t st);
+// nt: tokens per MMA tile (16, 32 or 64); tc_token_tile picks it from the
+// average rows per group.
+int tc_token_tile(int T, int kp, int G);
+cudaError_t launch_gemm_tc(const TcArgs& g, const CUtensorMap& tmap_b, int nt, cudaStream_t st);
 // a16[r] = f16 rows of the MXFP8 rows q/s [*, C] at row_map[r] / row_div
 // (or r), rowexp[r] = the row's largest block exponent.
 cudaError_t launch_act_f16(const uint8_t* q, const uint8_t* s, int C, const int32_t* row_map, int row_div, int R,

@@ -17,43 +17,59 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// S1: logits partials. grid (ceil(T/16), ceil(E/256), KS), block 256.
+// S1: logits partials. grid (ceil(T/TT), ceil(E/32), KS), block 256: lane =
+// expert within a 32-expert block (one 128-byte row segment of W_r per warp
+// and h), warp = h residue mod 8. Each thread accumulates its h-subsequence
+// in fp32, the 8 warp partials are summed in fixed order in shared memory.
 // part[ks][t][e] = sum over the ks-th slice of H of x[t][h] * W_r[h][e].
 // ---------------------------------------------------------------------------
-constexpr int kRtTok = 16;
 constexpr int kRtH = 64;
 
+template <int TT>
 __global__ void __launch_bounds__(256) k_router_partial(const uint16_t* __restrict__ x,
                                                         const float* __restrict__ Wr, int T, int H, int E,
                                                         int KS, float* __restrict__ part) {
-  __shared__ float xs[kRtTok][kRtH];
-  const int t0 = blockIdx.x * kRtTok;
-  const int e = blockIdx.y * 256 + threadIdx.x;
+  __shared__ float xs[TT][kRtH];
+  __shared__ float red[8][TT][33];
+  const int el = threadIdx.x & 31, hl = threadIdx.x >> 5;
+  const int t0 = blockIdx.x * TT;
+  const int e = blockIdx.y * 32 + el;
   const int ks = blockIdx.z;
   const int h0 = (int)((int64_t)ks * H / KS), h1 = (int)((int64_t)(ks + 1) * H / KS);
-  float acc[kRtTok];
+  float acc[TT];
 #pragma unroll
-  for (int i = 0; i < kRtTok; ++i) acc[i] = 0.f;
+  for (int i = 0; i < TT; ++i) acc[i] = 0.f;
   for (int hb = h0; hb < h1; hb += kRtH) {
     const int hn = min(kRtH, h1 - hb);
-    for (int i = threadIdx.x; i < kRtTok * kRtH; i += 256) {
-      int tt = i / kRtH, hh = i % kRtH;
+    __syncthreads();
+    for (int i = threadIdx.x; i < TT * kRtH; i += 256) {
+      const int tt = i / kRtH, hh = i % kRtH;
       float v = 0.f;
       if (t0 + tt < T && hh < hn) v = bf16_bits_to_f32(x[(int64_t)(t0 + tt) * H + hb + hh]);
       xs[tt][hh] = v;
     }
     __syncthreads();
     if (e < E) {
-      for (int hh = 0; hh < hn; ++hh) {
-        float w = __ldg(Wr + (int64_t)(hb + hh) * E + e);
+#pragma unroll 4
+      for (int hh = hl; hh < hn; hh += 8) {
+        const float w = __ldg(Wr + (int64_t)(hb + hh) * E + e);
 #pragma unroll
-        for (int i = 0; i < kRtTok; ++i) acc[i] = fmaf(xs[i][hh], w, acc[i]);
+        for (int i = 0; i < TT; ++i) acc[i] = fmaf(xs[i][hh], w, acc[i]);
       }
     }
-    __syncthreads();
   }
-  if (e < E) {
-    for (int i = 0; i < kRtTok && t0 + i < T; ++i) part[((int64_t)ks * T + t0 + i) * E + e] = acc[i];
+#pragma unroll
+  for (int i = 0; i < TT; ++i) red[hl][i][el] = acc[i];
+  __syncthreads();
+  for (int i = threadIdx.x; i < TT * 32; i += 256) {
+    const int tt = i / 32, l = i % 32;
+    const int ee = blockIdx.y * 32 + l;
+    if (t0 + tt < T && ee < E) {
+      float v = red[0][tt][l];
+#pragma unroll
+      for (int w = 1; w < 8; ++w) v += red[w][tt][l];
+      part[((int64_t)ks * T + t0 + tt) * E + ee] = v;
+    }
   }
 }
 
@@ -67,17 +83,27 @@ __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
   return va > vb || (va == vb && ia < ib);
 }
 
+// VPL: logits per lane kept in registers (E <= 32 * VPL).
+template <int VPL>
 __device__ void route_token(int t, int lane, const float* __restrict__ part, int KS, int T, int E, int k,
                             float rs, float* __restrict__ logits, int32_t* __restrict__ ids,
                             float* __restrict__ wts, int32_t* status) {
   bool nan_seen = false;
   const float* row_in = part + (int64_t)t * E;
   float* row = logits + (int64_t)t * E;
-  for (int e = lane; e < E; e += kWarp) {
-    float v = row_in[e];
-    for (int ks = 1; ks < KS; ++ks) v += part[((int64_t)ks * T + t) * E + e];
-    if (v != v) nan_seen = true;
-    if (row != row_in) row[e] = v;
+  float vals[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    float v = -INFINITY;
+    if (e < E) {
+      v = row_in[e];
+      for (int ks = 1; ks < KS; ++ks) v += part[((int64_t)ks * T + t) * E + e];
+      if (v != v) nan_seen = true;
+      if (row != row_in) row[e] = v;
+      if (v != v) v = -INFINITY;
+    }
+    vals[i] = v;
   }
   if (__any_sync(kFull, nan_seen) && lane == 0) set_status(status, MOE_DEV_NAN_LOGIT);
   uint64_t taken = 0;
@@ -86,12 +112,11 @@ __device__ void route_token(int t, int lane, const float* __restrict__ part, int
   for (int j = 0; j < k; ++j) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-    int slot = 0;
-    for (int e = lane; e < E; e += kWarp, ++slot) {
-      if (taken >> slot & 1ull) continue;
-      float v = row[e];
-      if (v != v) v = -INFINITY;
-      if (better(v, e, bv, bi)) { bv = v; bi = e; }
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int e = lane + 32 * i;
+      if (e >= E || (taken >> i & 1ull)) continue;
+      if (better(vals[i], e, bv, bi)) { bv = vals[i]; bi = e; }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -115,12 +140,19 @@ __device__ void route_token(int t, int lane, const float* __restrict__ part, int
 }
 
 // grid: ceil(T / 8), block 256 (warp per token).
+template <int VPL>
 __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ part, int KS, int T, int E, int k, float rs,
                                               float* __restrict__ logits, int32_t* __restrict__ ids,
                                               float* __restrict__ wts, int32_t* status) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
-  if (t < T) route_token(t, lane, part, KS, T, E, k, rs, logits, ids, wts, status);
+  if (t < T) route_token<VPL>(t, lane, part, KS, T, E, k, rs, logits, ids, wts, status);
+}
+
+static void launch_topk(const float* part, int KS, int T, int E, int k, float rs, float* logits, int32_t* ids,
+                        float* wts, int32_t* status, cudaStream_t st) {
+  if (E <= 256) k_topk<8><<<(T + 7) / 8, 256, 0, st>>>(part, KS, T, E, k, rs, logits, ids, wts, status);
+  else k_topk<64><<<(T + 7) / 8, 256, 0, st>>>(part, KS, T, E, k, rs, logits, ids, wts, status);
 }
 
 // ---------------------------------------------------------------------------
@@ -337,11 +369,16 @@ __global__ void __launch_bounds__(256) k_quant_rows_bf16(const uint16_t* __restr
 }
 
 // ---------------------------------------------------------------------------
-// Small-T fused path: block 0 routes every token, histograms, scans and
-// scatters inside shared memory; blocks 1.. quantise x meanwhile. One launch
-// for all of S2-S4. block 1024; smem: G ints of histogram/cursor + scan
-// scratch (3 (G + 1) + 33) + T*k ids + T*k weights.
+// Small-T fused path: block 0 sums the router partials (all threads), routes
+// every token (warp per token), histograms, scans and scatters; blocks 1..
+// quantise x meanwhile. One launch for all of S2-S4.
+// The scatter splits the flat assignment list into one contiguous segment per
+// warp: each warp counts its segment per group, a per-group prefix over the
+// warps (in warp order) gives every warp its cursors, then each warp places its
+// segment exactly as a single sequential pass would (stable in flat order).
+// smem: G (histogram) + 3 (G + 1) + 33 (scan) + 32 G (per-warp cursors) ints.
 // ---------------------------------------------------------------------------
+template <int VPL>
 __global__ void __launch_bounds__(1024) k_route_small(const float* __restrict__ part, int KS, int T, int E, int k,
                                                       int kp, int G, float rs, int route, float* __restrict__ logits,
                                                       int32_t* ids, float* wts, int32_t* counts, int32_t* offsets,
@@ -362,13 +399,26 @@ __global__ void __launch_bounds__(1024) k_route_small(const float* __restrict__ 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int32_t* hist = sm;                    // [G]
   int32_t* scan_sm = sm + G;             // 3 (G + 1) + 33
+  int32_t* wc = scan_sm + 3 * (G + 1) + 33;   // [32][G]
   if (route) {
-    for (int t = warp; t < T; t += 32) route_token(t, lane, part, KS, T, E, k, rs, logits, ids, wts, status);
+    const float* src = part;
+    if (KS > 1) {
+      const int64_t n = (int64_t)T * E;
+      for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+        float v = part[i];
+        for (int ks = 1; ks < KS; ++ks) v += part[(int64_t)ks * n + i];
+        logits[i] = v;
+      }
+      __syncthreads();
+      src = logits;
+    }
+    for (int t = warp; t < T; t += 32) route_token<VPL>(t, lane, src, 1, T, E, k, rs, logits, ids, wts, status);
   }
   for (int e = threadIdx.x; e < G; e += blockDim.x) hist[e] = 0;
   __syncthreads();   // ids / wts written by this block are visible block-wide
   bool bad = false;
-  for (int a = threadIdx.x; a < T * kp; a += blockDim.x) {
+  const int n = T * kp;
+  for (int a = threadIdx.x; a < n; a += blockDim.x) {
     int e = assignment_expert(ids, a / kp, a % kp, k, E);
     if (e < 0) bad = true;
     else atomicAdd(&hist[e], 1);
@@ -376,36 +426,77 @@ __global__ void __launch_bounds__(1024) k_route_small(const float* __restrict__ 
   if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(status, MOE_DEV_BAD_EXPERT_ID);
   scan_groups(hist, 1, G, counts, offsets, nullptr, touched, n_touched, poff, scan_sm);
   __syncthreads();
-  // cursor = offsets (reuse hist)
-  for (int e = threadIdx.x; e < G; e += blockDim.x) hist[e] = scan_sm[e];
+  // per-warp segment counts
+  const int seg = ((n + 31) / 32 + 31) / 32 * 32;
+  const int a0 = min(n, warp * seg), a1 = min(n, a0 + seg);
+  int32_t* wcw = wc + warp * G;
+  for (int e = lane; e < G; e += 32) wcw[e] = 0;
+  __syncwarp();
+  const unsigned lt = (1u << lane) - 1u;
+  for (int c = a0; c < a1; c += 32) {
+    const int a = c + lane;
+    const int e = a < a1 ? assignment_expert(ids, a / kp, a % kp, k, E) : -1;
+    const unsigned m = __match_any_sync(kFull, e);
+    if (e >= 0 && (m & lt) == 0) wcw[e] += __popc(m);
+    __syncwarp();
+  }
   __syncthreads();
-  if (warp == 0) scatter_warp(0, T * kp, ids, wts, k, kp, E, hist, perm, inv, w_row);
+  // cursors: group offset plus the counts of the earlier warps
+  for (int e = threadIdx.x; e < G; e += blockDim.x) {
+    int run = scan_sm[e];
+    for (int w = 0; w < 32; ++w) {
+      const int c = wc[w * G + e];
+      wc[w * G + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  scatter_warp(a0, a1, ids, wts, k, kp, E, wcw, perm, inv, w_row);
 }
 
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
-int router_splits(int T, int H) {
-  int ks = T > 0 ? 4096 / T : 1;
-  ks = std::max(1, std::min(ks, H / 32));
+static int router_tile(int T) { return T <= 64 ? 16 : 32; }
+
+// H slices: enough CTAs to cover the GPU about twice, each slice >= 256 rows,
+// and at most 512 partial rows (KS * T) for the routing kernel to sum.
+int router_splits(int T, int H, int E) {
+  const int tiles = ((T + router_tile(T) - 1) / router_tile(T)) * ((E + 31) / 32);
+  int ks = (2 * 152 + tiles - 1) / std::max(tiles, 1);
+  ks = std::max(1, std::min(ks, std::max(1, H / 256)));
+  if ((int64_t)ks * T > 512) ks = std::max(1, 512 / std::max(T, 1));
   return ks;
 }
 
 cudaError_t launch_router(const uint16_t* x, const float* Wr, int T, int H, int E, int KS, float* part,
                           cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  dim3 grid((T + kRtTok - 1) / kRtTok, (E + 255) / 256, KS);
-  k_router_partial<<<grid, 256, 0, st>>>(x, Wr, T, H, E, KS, part);
+  const int tt = router_tile(T);
+  dim3 grid((T + tt - 1) / tt, (E + 31) / 32, KS);
+  if (tt == 16) k_router_partial<16><<<grid, 256, 0, st>>>(x, Wr, T, H, E, KS, part);
+  else k_router_partial<32><<<grid, 256, 0, st>>>(x, Wr, T, H, E, KS, part);
   note_launch();
   return cudaGetLastError();
 }
 
-static size_t small_smem(int G, int T, int k) {
-  return (size_t)(G + 3 * (G + 1) + 33) * 4;
-  (void)T; (void)k;
-}
+static size_t small_smem(int G) { return (size_t)(G + 3 * (G + 1) + 33 + 32 * G) * 4; }
 
-bool use_small_route(int T, int G, int kp) { return T <= 256 && T * kp <= 4096 && G <= 2048; }
+bool use_small_route(int T, int G, int kp) { return T <= 256 && T * kp <= 4096 && small_smem(G) <= 200 * 1024; }
+
+template <int VPL>
+static void launch_small(const RouteArgs& a, int kp, int G, int nq, cudaStream_t st) {
+  const size_t smem = small_smem(G);
+  static bool attr = false;
+  if (!attr) {
+    cudaFuncSetAttribute(k_route_small<VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    attr = true;
+  }
+  k_route_small<VPL><<<1 + nq, 1024, smem, st>>>(a.part, a.KS, a.T, a.E, a.k, kp, G, a.rs, a.route ? 1 : 0,
+                                                 a.logits, a.ids, a.wts, a.counts, a.offsets, a.touched,
+                                                 a.n_touched, a.poff, a.perm, a.inv, a.w_row, a.x, a.H, a.xq, a.xs,
+                                                 a.status);
+}
 
 cudaError_t launch_route_dispatch(const RouteArgs& a, cudaStream_t st) {
   const int kp = a.k + a.S, G = a.E + a.S;
@@ -413,19 +504,14 @@ cudaError_t launch_route_dispatch(const RouteArgs& a, cudaStream_t st) {
   if (use_small_route(T, G, kp)) {
     int nq = T == 0 ? 0 : std::min(64, std::max(1, (T * ((a.H + 255) / 256) + 31) / 32));
     if (!a.x) nq = 0;
-    size_t smem = small_smem(G, T, a.k);
-    if (smem > 48 * 1024) {
-      cudaFuncSetAttribute(k_route_small, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    }
-    k_route_small<<<1 + nq, 1024, smem, st>>>(a.part, a.KS, T, a.E, a.k, kp, G, a.rs, a.route ? 1 : 0, a.logits,
-                                              a.ids, a.wts, a.counts, a.offsets, a.touched, a.n_touched, a.poff,
-                                              a.perm, a.inv, a.w_row, a.x, a.H, a.xq, a.xs, a.status);
+    if (a.E <= 256) launch_small<8>(a, kp, G, nq, st);
+    else launch_small<64>(a, kp, G, nq, st);
     note_launch();
     return cudaGetLastError();
   }
   const int NB = (T + kTokBlk - 1) / kTokBlk;
   if (a.route) {
-    k_topk<<<(T + 7) / 8, 256, 0, st>>>(a.part, a.KS, T, a.E, a.k, a.rs, a.logits, a.ids, a.wts, a.status);
+    launch_topk(a.part, a.KS, T, a.E, a.k, a.rs, a.logits, a.ids, a.wts, a.status, st);
     note_launch();
   }
   k_hist<<<NB, 256, G * 4, st>>>(a.ids, T, a.k, kp, a.E, G, a.hist, a.status);
@@ -449,7 +535,7 @@ cudaError_t launch_route_dispatch(const RouteArgs& a, cudaStream_t st) {
 cudaError_t launch_topk_only(const float* logits, int T, int E, int k, float rs, int32_t* ids, float* w,
                              int32_t* status, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  k_topk<<<(T + 7) / 8, 256, 0, st>>>(logits, 1, T, E, k, rs, const_cast<float*>(logits), ids, w, status);
+  launch_topk(logits, 1, T, E, k, rs, const_cast<float*>(logits), ids, w, status, st);
   note_launch();
   return cudaGetLastError();
 }
