@@ -204,6 +204,24 @@ moe_status_t moe_prepack_weights(const moe_config_t* cfg, const moe_weights_view
 moe_status_t moe_router_logits(const moe_config_t* cfg, const uint16_t* x, const float* W_r, int T,
                                float* logits, void* ws, void* stream);
 
+/* S1 without a workspace, for callers that cannot allocate device memory
+ * where they need logits (an allocator-free region, a host that hands out no
+ * device buffers, a path where cudaMalloc's implicit synchronisation is not
+ * allowed). The pages have no counterpart: this is a convenience of this
+ * library. Same result as moe_router_logits, bit for bit; the split partial
+ * sums live in one static 4 MiB device array that every GPU loading the
+ * library holds until process exit. A call whose partials would exceed it
+ * (split count x T x E > 2^20 floats) returns MOE_ERR_WORKSPACE and enqueues
+ * nothing. Nothing is allocated or freed. All calls on a device share the
+ * array and leave their partials in it (each call overwrites what it reads,
+ * so nothing needs clearing); calls whose kernels may overlap on the GPU race
+ * on it and must be serialised. The first call made with a given device
+ * current looks up the array's device address; make it before any stream
+ * capture on that device. x [T, H] bf16, W_r [H, E] fp32, logits [T, E]
+ * fp32, all device. */
+moe_status_t moe_router_logits_noalloc(const moe_config_t* cfg, const uint16_t* x, const float* W_r, int T,
+                                       float* logits, void* stream);
+
 /* S2-S4. From logits [T, E] fp32 (device): top-k ids and weights, counts,
  * offsets, permutation, inverse, row weights, and the MXFP8 copy of x
  * [T, H] bf16 (device). Outputs in *d (device buffers). Bit-exact and

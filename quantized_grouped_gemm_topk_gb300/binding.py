@@ -31,7 +31,7 @@ EXPORTS = (
     "moe_train_sizes", "moe_prepack_weights", "moe_router_logits", "moe_route_dispatch", "moe_route_topk",
     "moe_dispatch", "moe_grouped_gemm_w1_swiglu_quant", "moe_grouped_gemm_w2", "moe_combine",
     "moe_layer_forward", "moe_layer_backward", "moe_read_status", "moe_clear_status", "moe_status_string",
-    "moe_last_launch_count", "moe_set_phase_events",
+    "moe_last_launch_count", "moe_set_phase_events", "moe_router_logits_noalloc",
 )
 MOE_N_PHASE_EVENTS = 6
 
@@ -106,6 +106,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "moe_status_string": [ctypes.c_int],
         "moe_last_launch_count": [],
         "moe_set_phase_events": [ctypes.POINTER(ctypes.c_void_p)],
+        "moe_router_logits_noalloc": [cfgp, P, P, ctypes.c_int, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -220,6 +221,14 @@ def moe_prepack_weights(cfg, wts: dict, which=MOE_PACK_FORWARD, dst=None, stream
 def moe_router_logits(cfg, x, W_r, T, logits, ws, stream=None):
     _check("moe_router_logits", load().moe_router_logits(ctypes.byref(cfg), _ptr(x), _ptr(W_r), T, _ptr(logits),
                                                          _ptr(ws), _stream(stream)))
+
+
+def moe_router_logits_noalloc(cfg, x, W_r, T, logits, stream=None):
+    """Router logits with no workspace: for callers that cannot allocate
+    device memory; the split partials live in the library's static device
+    scratch (see include/moe.h for its size limit and sharing rules)."""
+    _check("moe_router_logits_noalloc", load().moe_router_logits_noalloc(ctypes.byref(cfg), _ptr(x), _ptr(W_r), T,
+                                                                         _ptr(logits), _stream(stream)))
 
 
 def moe_route_topk(cfg, logits, T, ids, w, ws, stream=None):
