@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
         const uint32_t n = it < (uint32_t)C::Stages ? it : (uint32_t)C::Stages;
         for (uint32_t k = 0; k < n; ++k) {
           const uint32_t i2 = it - 1 - k;
-          tc::mbar_wait(&full[i2 % C::Stages], (i2 / C::Stages) & 1, &never, 200000000ull);
+          tc::mbar_wait(&full[i2 % C::Stages], (i2 / C::Stages) & 1, &never, 400000000ll);
         }
       }
     }
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       // every MMA of this thread has completed once `drain` fires
       tc::mma_commit(drain);
       volatile int never = 0;
-      tc::mbar_wait(drain, 0, &never, 200000000ull);
+      tc::mbar_wait(drain, 0, &never, 400000000ll);
     }
   } else if (warp < 10) {
     // ---------------- decoders ----------------

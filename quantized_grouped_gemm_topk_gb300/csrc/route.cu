@@ -17,60 +17,100 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// S1: logits partials. grid (ceil(T/TT), ceil(E/32), KS), block 256: lane =
-// expert within a 32-expert block (one 128-byte row segment of W_r per warp
-// and h), warp = h residue mod 8. Each thread accumulates its h-subsequence
-// in fp32, the 8 warp partials are summed in fixed order in shared memory.
-// part[ks][t][e] = sum over the ks-th slice of H of x[t][h] * W_r[h][e].
+// S1: logits partials, a register-tiled fp32 GEMM over one slice of H.
+// grid (ceil(T/TT), ceil(E/64), KS), block 256: thread (tx = tid % 16,
+// ty = tid / 16) owns experts 4tx..4tx+3 and tokens ty*TT/16.. of the
+// CTA's 64-expert x TT-token tile. Per 32-row step of H both operands are
+// staged in shared memory (x transposed to [h][token]), so each pair of
+// shared loads feeds 4 * TT/16 FMAs. Every thread accumulates its h in
+// increasing order. part[ks][t][e] = sum over the ks-th slice of H of
+// x[t][h] * W_r[h][e].
 // ---------------------------------------------------------------------------
-constexpr int kRtH = 64;
+constexpr int kRtKH = 32;
 
 template <int TT>
 __global__ void __launch_bounds__(256) k_router_partial(const uint16_t* __restrict__ x,
                                                         const float* __restrict__ Wr, int T, int H, int E,
                                                         int KS, float* __restrict__ part) {
-  __shared__ float xs[TT][kRtH];
-  __shared__ float red[8][TT][33];
-  const int el = threadIdx.x & 31, hl = threadIdx.x >> 5;
+  constexpr int TPT = TT / 16;                     // tokens per thread
+  __shared__ __align__(16) float ws_[kRtKH][64];
+  __shared__ __align__(16) float xs_[kRtKH][TT + 1];   // +1: conflict-free transposed stores
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int t0 = blockIdx.x * TT;
-  const int e = blockIdx.y * 32 + el;
+  const int e0 = blockIdx.y * 64;
   const int ks = blockIdx.z;
   const int h0 = (int)((int64_t)ks * H / KS), h1 = (int)((int64_t)(ks + 1) * H / KS);
-  float acc[TT];
+  float acc[TPT][4];
 #pragma unroll
-  for (int i = 0; i < TT; ++i) acc[i] = 0.f;
-  for (int hb = h0; hb < h1; hb += kRtH) {
-    const int hn = min(kRtH, h1 - hb);
+  for (int i = 0; i < TPT; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  for (int hb = h0; hb < h1; hb += kRtKH) {
+    const int hn = min(kRtKH, h1 - hb);
     __syncthreads();
-    for (int i = threadIdx.x; i < TT * kRtH; i += 256) {
-      const int tt = i / kRtH, hh = i % kRtH;
+    for (int i = threadIdx.x; i < kRtKH * 16; i += 256) {       // W tile: 32 rows x 64 experts
+      const int hh = i >> 4, c = (i & 15) * 4;
+      float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (hh < hn) {
+        const float* src = Wr + (int64_t)(hb + hh) * E + e0 + c;
+        if (e0 + c + 3 < E && (E & 3) == 0) {
+          w = __ldg(reinterpret_cast<const float4*>(src));
+        } else {
+          if (e0 + c + 0 < E) w.x = __ldg(src + 0);
+          if (e0 + c + 1 < E) w.y = __ldg(src + 1);
+          if (e0 + c + 2 < E) w.z = __ldg(src + 2);
+          if (e0 + c + 3 < E) w.w = __ldg(src + 3);
+        }
+      }
+      *reinterpret_cast<float4*>(&ws_[hh][c]) = w;
+    }
+    for (int i = threadIdx.x; i < TT * kRtKH; i += 256) {       // x tile, transposed
+      const int tt = i / kRtKH, hh = i % kRtKH;
       float v = 0.f;
       if (t0 + tt < T && hh < hn) v = bf16_bits_to_f32(x[(int64_t)(t0 + tt) * H + hb + hh]);
-      xs[tt][hh] = v;
+      xs_[hh][tt] = v;
     }
     __syncthreads();
-    if (e < E) {
-#pragma unroll 4
-      for (int hh = hl; hh < hn; hh += 8) {
-        const float w = __ldg(Wr + (int64_t)(hb + hh) * E + e);
+#pragma unroll 8
+    for (int hh = 0; hh < kRtKH; ++hh) {
+      const float4 w = *reinterpret_cast<const float4*>(&ws_[hh][tx * 4]);
+      float a[TPT];
 #pragma unroll
-        for (int i = 0; i < TT; ++i) acc[i] = fmaf(xs[i][hh], w, acc[i]);
+      for (int i = 0; i < TPT; ++i) a[i] = xs_[hh][ty * TPT + i];
+#pragma unroll
+      for (int i = 0; i < TPT; ++i) {
+        acc[i][0] = fmaf(a[i], w.x, acc[i][0]);
+        acc[i][1] = fmaf(a[i], w.y, acc[i][1]);
+        acc[i][2] = fmaf(a[i], w.z, acc[i][2]);
+        acc[i][3] = fmaf(a[i], w.w, acc[i][3]);
       }
     }
   }
 #pragma unroll
-  for (int i = 0; i < TT; ++i) red[hl][i][el] = acc[i];
-  __syncthreads();
-  for (int i = threadIdx.x; i < TT * 32; i += 256) {
-    const int tt = i / 32, l = i % 32;
-    const int ee = blockIdx.y * 32 + l;
-    if (t0 + tt < T && ee < E) {
-      float v = red[0][tt][l];
+  for (int i = 0; i < TPT; ++i) {
+    const int t = t0 + ty * TPT + i;
+    if (t >= T) continue;
 #pragma unroll
-      for (int w = 1; w < 8; ++w) v += red[w][tt][l];
-      part[((int64_t)ks * T + t0 + tt) * E + ee] = v;
+    for (int j = 0; j < 4; ++j) {
+      const int e = e0 + tx * 4 + j;
+      if (e < E) part[((int64_t)ks * T + t) * E + e] = acc[i][j];
     }
   }
+}
+
+// Sum over ks of part[ks * n + i], in ks order, with 8 loads in flight.
+__device__ __forceinline__ float sum_partials(const float* __restrict__ part, int KS, int64_t n, int64_t i) {
+  float v = 0.f;
+  int ks = 0;
+  for (; ks + 8 <= KS; ks += 8) {
+    float t[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t[j] = part[(int64_t)(ks + j) * n + i];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v += t[j];
+  }
+  for (; ks < KS; ++ks) v += part[(int64_t)ks * n + i];
+  return v;
 }
 
 // ---------------------------------------------------------------------------
@@ -97,8 +137,7 @@ __device__ void route_token(int t, int lane, const float* __restrict__ part, int
     const int e = lane + 32 * i;
     float v = -INFINITY;
     if (e < E) {
-      v = row_in[e];
-      for (int ks = 1; ks < KS; ++ks) v += part[((int64_t)ks * T + t) * E + e];
+      v = KS == 1 ? row_in[e] : sum_partials(part, KS, (int64_t)T * E, (int64_t)t * E + e);
       if (v != v) nan_seen = true;
       if (row != row_in) row[e] = v;
       if (v != v) v = -INFINITY;
@@ -405,9 +444,7 @@ __global__ void __launch_bounds__(1024) k_route_small(const float* __restrict__ 
     if (KS > 1) {
       const int64_t n = (int64_t)T * E;
       for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
-        float v = part[i];
-        for (int ks = 1; ks < KS; ++ks) v += part[(int64_t)ks * n + i];
-        logits[i] = v;
+        logits[i] = sum_partials(part, KS, n, i);
       }
       __syncthreads();
       src = logits;
@@ -457,15 +494,15 @@ __global__ void __launch_bounds__(1024) k_route_small(const float* __restrict__ 
 // ---------------------------------------------------------------------------
 // launchers
 // ---------------------------------------------------------------------------
-static int router_tile(int T) { return T <= 64 ? 16 : 32; }
+static int router_tile(int T) { return T <= 16 ? 16 : 32; }
 
-// H slices: enough CTAs to cover the GPU about twice, each slice >= 256 rows,
-// and at most 512 partial rows (KS * T) for the routing kernel to sum.
+// H slices: about two CTAs per SM, each slice >= 128 rows, and at most 4096
+// partial rows (KS * T) to sum afterwards.
 int router_splits(int T, int H, int E) {
-  const int tiles = ((T + router_tile(T) - 1) / router_tile(T)) * ((E + 31) / 32);
+  const int tiles = ((T + router_tile(T) - 1) / router_tile(T)) * ((E + 63) / 64);
   int ks = (2 * 152 + tiles - 1) / std::max(tiles, 1);
-  ks = std::max(1, std::min(ks, std::max(1, H / 256)));
-  if ((int64_t)ks * T > 512) ks = std::max(1, 512 / std::max(T, 1));
+  ks = std::max(1, std::min(ks, std::max(1, H / 128)));
+  if ((int64_t)ks * T > 4096) ks = std::max(1, 4096 / std::max(T, 1));
   return ks;
 }
 
@@ -473,7 +510,7 @@ cudaError_t launch_router(const uint16_t* x, const float* Wr, int T, int H, int 
                           cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   const int tt = router_tile(T);
-  dim3 grid((T + tt - 1) / tt, (E + 31) / 32, KS);
+  dim3 grid((T + tt - 1) / tt, (E + 63) / 64, KS);
   if (tt == 16) k_router_partial<16><<<grid, 256, 0, st>>>(x, Wr, T, H, E, KS, part);
   else k_router_partial<32><<<grid, 256, 0, st>>>(x, Wr, T, H, E, KS, part);
   note_launch();

@@ -40,18 +40,32 @@ __device__ __forceinline__ uint64_t globaltimer() {
   return t;
 }
 
-// Waits for the phase with the given parity to complete. Gives up after
-// `limit_ns` of wall time or as soon as *abort is set, returning false (the
-// caller then winds down); sets *abort on its own timeout.
+// Non-suspending probe of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete, spinning on the
+// non-suspending probe. Gives up after about `limit_cycles` SM clock cycles
+// (4e9: two seconds at the top clock, longer when the clock is lower) or as
+// soon as *abort is set, returning false (the caller then winds down); sets
+// *abort on its own timeout. The timer is the SM's own cycle counter, read
+// only on every 256th probe: these waits sit on the kernels' critical
+// handoffs and must cost no more than the probe when the phase is ready.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint64_t limit_ns = 2000000000ull) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63) == 0) {
+                                          long long limit_cycles = 4000000000ll) {
+  const long long t0 = clock64();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_test_wait(bar, parity)) return true;
+    if ((it & 255) == 255) {
       if (*abort) return false;
-      if (globaltimer() - t0 > limit_ns) {
+      if (clock64() - t0 > limit_cycles) {
         *abort = 1;
         return false;
       }
