@@ -5,8 +5,12 @@ NVFP4 weights, MXFP8 activations). One step = one layer forward at each of
 T = 1, 8, 32 and 128 tokens, every layer on a fresh batch of synthetic tokens
 (so routing touches a different set of experts), with the L2 cache flushed
 (512 MiB write) before each layer and the flush kept out of the timing.
-The metric is microseconds per step (lower is better); the per-T layer times
-are listed in ``config.per_T_us``.
+Each layer call replays a CUDA graph holding one captured moe_layer_forward
+(the decode layer is launch-bound without one). The metric is microseconds
+per step (lower is better), the sum of the layers' device times; the per-T
+layer times are listed in ``config.per_T_us``. The ``e2e`` figure calls the
+C ABI directly (no graph) with the tokens copied in from pinned host memory
+and the output copied back inside each timed interval.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -208,7 +212,8 @@ def config_block(s, per_T):
     c = {"workload": f"{s.name}_decode", "H": s.H, "I": s.I, "E": s.E, "k": s.k, "n_shared": s.n_shared,
          "T": list(DECODE_TS), "weights": s.wfmt, "activations": "mxfp8",
          "l2": "flushed by a 512 MiB write before every layer; flush not timed",
-         "inputs": "fresh seeded batch per layer call; weights resident in HBM", "parallelism": "replica per GPU"}
+         "inputs": "fresh seeded batch per layer call; weights resident in HBM", "parallelism": "replica per GPU",
+         "launch": "each layer call is a CUDA graph of one moe_layer_forward; e2e calls the C ABI directly"}
     if per_T is not None:
         c["per_T_us"] = per_T
     return c
@@ -256,50 +261,65 @@ def run_ours(args, s, rank, world, local):
         R = T * s.kp
         return n * w1_bytes_per_expert(s), R * (s.H + s.H // 32) + R * (s.I + s.I // 32)
 
+    # One CUDA graph per (T, batch): the whole layer forward captured once,
+    # with its phase events as event-record nodes, replayed in the timed loop.
+    graphs, gev, glaunch = {}, {}, {}
+    for T in DECODE_TS:
+        for i in range(nx):
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_N_PHASE_EVENTS)]
+            for e in evs:
+                e.record()      # creates the event's handle
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            m.moe_set_phase_events(evs)
+            with torch.cuda.graph(g):
+                m.moe_layer_forward(cfg, xs[T][i], Wr, None, T, packed, outs[T], None, ws)
+                glaunch[(T, i)] = m.moe_last_launch_count()
+            m.moe_set_phase_events(None)
+            graphs[(T, i)], gev[(T, i)] = g, evs
+    torch.cuda.synchronize()
+
     # warm-up
     for w in range(args.warmup):
         for T in DECODE_TS:
-            m.moe_layer_forward(cfg, xs[T][w % nx], Wr, None, T, packed, outs[T], None, ws)
+            flush.zero_()
+            graphs[(T, w % nx)].replay()
     torch.cuda.synchronize()
+    assert m.moe_read_status(cfg, ws) == 0
 
     K = args.steps
-    ncall = K * len(DECODE_TS)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_N_PHASE_EVENTS)] for _ in range(ncall)]
-    for row in ev:
-        for e in row:
-            e.record()
-    torch.cuda.synchronize()
     launches = 0
+    layer_us = []
+    w1_us, w1_bytes, w2_us = 0.0, 0, 0.0
+    per_T = {T: [] for T in DECODE_TS}
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    t_wall = time.perf_counter()
     with ClockSampler(local) as clk:
-        c = 0
         for step in range(K):
+            i = step % nx
             for T in DECODE_TS:
                 flush.zero_()
-                m.moe_set_phase_events(ev[c])
-                m.moe_layer_forward(cfg, xs[T][step % nx], Wr, None, T, packed, outs[T], None, ws)
-                launches += m.moe_last_launch_count()
-                c += 1
-        m.moe_set_phase_events(None)
-        torch.cuda.synchronize()
+                graphs[(T, i)].replay()
+                launches += glaunch[(T, i)]
+            # the graphs of this step are replayed again nx steps later: read
+            # their events now (host-side wait, outside every device interval)
+            torch.cuda.synchronize()
+            for T in DECODE_TS:
+                e = gev[(T, i)]
+                t = e[0].elapsed_time(e[5]) * 1e3
+                layer_us.append(t)
+                per_T[T].append(t)
+                w1_us += e[1].elapsed_time(e[2]) * 1e3
+                w2_us += e[3].elapsed_time(e[4]) * 1e3
+                wb, ab = layer_bytes(T, i)
+                w1_bytes += wb + ab
     if world > 1:
         torch.distributed.barrier()
-    layer_us = []
-    w1_us, w1_bytes = 0.0, 0
-    per_T = {T: [] for T in DECODE_TS}
-    c = 0
-    for step in range(K):
-        for T in DECODE_TS:
-            e = ev[c]
-            t = e[0].elapsed_time(e[5]) * 1e3
-            layer_us.append(t)
-            per_T[T].append(t)
-            w1_us += e[1].elapsed_time(e[2]) * 1e3
-            wb, ab = layer_bytes(T, step % nx)
-            w1_bytes += wb + ab
-            c += 1
+    torch.cuda.synchronize()
+    wall_ms = (time.perf_counter() - t_wall) * 1e3 / K
+    assert m.moe_read_status(cfg, ws) == 0
     us_step = sum(layer_us) / K
     if world > 1:
         tt = torch.tensor([us_step], device=dev)
@@ -310,6 +330,7 @@ def run_ours(args, s, rank, world, local):
     host_x = {T: [xs[T][i].cpu().pin_memory() for i in range(nx)] for T in DECODE_TS}
     host_out = {T: torch.empty(T, s.H, dtype=torch.bfloat16).pin_memory() for T in DECODE_TS}
     dev_x = {T: torch.empty(T, s.H, dtype=torch.bfloat16, device=dev) for T in DECODE_TS}
+    ncall = K * len(DECODE_TS)
     e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ncall)]
     torch.cuda.synchronize()
     c = 0
@@ -334,10 +355,14 @@ def run_ours(args, s, rank, world, local):
     roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
             "traffic": None, "kernel": "W1 grouped GEMM (k_gemm_tc)", "peak_source": f"{peak_kind} hbm_gbs",
             "algorithmic_bytes": "touched experts x NVFP4 W1 bytes (2I*H/2 + 2I*H/16) + MXFP8 rows in and out",
-            "kernel_us_per_step": w1_us / K}
+            "kernel_us_per_step": w1_us / K, "w2_gemm_us_per_step": w2_us / K}
     if tr is not None:
-        roof["traffic"] = tr.get("dram_bytes_per_launch")
-        roof["traffic_note"] = tr.get("note")
+        # DRAM bytes of one captured W1 launch over its algorithmic bytes,
+        # applied to this run's average algorithmic bytes per W1 launch
+        roof["traffic"] = tr["dram_over_algorithmic"] * w1_bytes / (K * len(DECODE_TS))
+        roof["traffic_note"] = (f"ncu dram__bytes_read+write of one W1 launch ({tr['captured']}) = "
+                                f"{tr['dram_over_algorithmic']:.4f} x its algorithmic bytes, scaled to this "
+                                f"run's average W1 launch")
     per_T_us = {str(T): statistics.median(v) for T, v in per_T.items()}
     clocks = clk.summary()
     line = {
@@ -348,6 +373,7 @@ def run_ours(args, s, rank, world, local):
         "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": h2d},
         "gpu_launches": launches,
         "clocks": clocks,
+        "wall_ms_per_step": wall_ms,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         x_bits, logits, wts_np, e = cpu_sample_inputs(s, dev)

@@ -295,10 +295,13 @@ int moe_last_launch_count(void);
 /* Optional phase timing for moe_layer_forward, per calling thread. With
  * `events` non-NULL (MOE_N_PHASE_EVENTS cudaEvent_t handles created by the
  * caller), each later moe_layer_forward on this thread records, on its
- * stream: [0] at entry, [1] after routing and dispatch, [2] after the W1
- * grouped-GEMM kernel, [3] after the W1 epilogue, [4] after the W2
- * grouped-GEMM kernel, [5] after the combine. NULL switches it off. Host only;
- * the events must outlive the calls that record them. */
+ * stream: [0] at entry, [1] after routing, dispatch and the gather of the
+ * W1 operand rows, [2] after the W1 grouped-GEMM kernel, [3] after the W1
+ * epilogue, [4] after the W2 grouped-GEMM kernel, [5] after the combine.
+ * NULL switches it off. Host only; the events must outlive the calls that
+ * record them. A call made while its stream is being captured into a CUDA
+ * graph records them as event-record nodes, so every replay of that graph
+ * records them again. */
 #define MOE_N_PHASE_EVENTS 6
 moe_status_t moe_set_phase_events(void* const* events);
 

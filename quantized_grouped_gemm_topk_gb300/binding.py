@@ -197,6 +197,8 @@ def moe_set_phase_events(events):
     if events is None:
         _check("moe_set_phase_events", load().moe_set_phase_events(None))
         return
+    if len(events) != MOE_N_PHASE_EVENTS or not all(e.cuda_event for e in events):
+        raise ValueError(f"moe_set_phase_events needs {MOE_N_PHASE_EVENTS} events, each recorded once")
     arr = (ctypes.c_void_p * MOE_N_PHASE_EVENTS)(*[e.cuda_event for e in events])
     moe_set_phase_events._keep = arr
     _check("moe_set_phase_events", load().moe_set_phase_events(arr))

@@ -11,8 +11,16 @@ namespace moe {
 static thread_local int g_launches = 0;
 static thread_local cudaEvent_t g_phase[MOE_N_PHASE_EVENTS] = {};
 static thread_local bool g_phase_on = false;
+// Records phase event i on st. Under stream capture the record becomes an
+// event-record node of the graph (a plain record there would only express a
+// dependency), so each replay of the graph re-records the event.
 static inline void phase(int i, cudaStream_t st) {
-  if (g_phase_on && g_phase[i]) cudaEventRecord(g_phase[i], st);
+  if (!g_phase_on || !g_phase[i]) return;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(g_phase[i], st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(g_phase[i], st);
 }
 void note_launch() { ++g_launches; }
 void reset_launch_count() { g_launches = 0; }
@@ -452,7 +460,7 @@ static ActParams act_params(const moe_config_t* c) {
 
 static moe_status_t w1_impl(const moe_config_t* c, const moe_dispatch_t* d, int T, const void* packed, uint8_t* y1q,
                             uint8_t* y1s, const moe_train_save_t* save, void* ws, cudaStream_t st,
-                            float* y_save_override) {
+                            float* y_save_override, bool a16_ready = false) {
   const WsLayout L = ws_layout(*c);
   const PackLayout P = pack_layout(*c, MOE_PACK_FORWARD);
   const int kp = c->k + c->n_shared, G = c->E + c->n_shared;
@@ -460,7 +468,8 @@ static moe_status_t w1_impl(const moe_config_t* c, const moe_dispatch_t* d, int 
   if (T == 0) return MOE_OK;
   uint16_t* a16 = at<uint16_t>(ws, L.a16);
   int32_t* rexp1 = at<int32_t>(ws, L.rexp1);
-  MOE_CHECK_CUDA(launch_act_f16(d->xq, d->xs, c->H, d->perm_src, kp, R, d->offsets, G, a16, rexp1, st));
+  if (!a16_ready)
+    MOE_CHECK_CUDA(launch_act_f16(d->xq, d->xs, c->H, d->perm_src, kp, R, d->offsets, G, a16, rexp1, st));
   TcRun run;
   moe_status_t s = tc_gemm(c, P, 1, packed, ws, L, d->offsets, T, a16, rexp1, st, &run);
   if (s != MOE_OK) return s;
@@ -567,6 +576,9 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
     a.part = logits_in; a.KS = 1;
   }
   MOE_CHECK_CUDA(launch_route_dispatch(a, st));
+  if (T > 0)   // gather the quantised rows into the GEMM's f16 operand (part of dispatch)
+    MOE_CHECK_CUDA(launch_act_f16(v.d.xq, v.d.xs, c->H, v.d.perm_src, kp, T * kp, v.d.offsets, G,
+                                  at<uint16_t>(ws, L.a16), at<int32_t>(ws, L.rexp1), st));
   phase(1, st);
   if (T == 0) {
     for (int i = 2; i < MOE_N_PHASE_EVENTS; ++i) phase(i, st);
@@ -580,7 +592,7 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
     q.r_pad_max = r_pad_for(dims_of(*c), T); q.q = save->at_q; q.s = save->at_s;
     MOE_CHECK_CUDA(launch_quant_cols(q, st));
   }
-  if ((s = w1_impl(c, &v.d, T, packed_w, v.y1_q, v.y1_s, save, ws, st, nullptr)) != MOE_OK) return s;
+  if ((s = w1_impl(c, &v.d, T, packed_w, v.y1_q, v.y1_s, save, ws, st, nullptr, true)) != MOE_OK) return s;
   const PackLayout P = pack_layout(*c, MOE_PACK_FORWARD);
   TcRun run;
   s = tc_gemm(c, P, 2, packed_w, ws, L, v.d.offsets, T, at<uint16_t>(ws, L.y16), at<int32_t>(ws, L.rexp2), st,
