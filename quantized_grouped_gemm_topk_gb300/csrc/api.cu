@@ -441,9 +441,9 @@ static moe_status_t tc_gemm(const moe_config_t* c, const PackLayout& P, int mat,
   g.max_ctas = sms;
   g.S = tc_splits(*c, T, g.tiles, g.K, sms);
   g.status = at<int32_t>(ws, L.status);
-  CUtensorMap map;
-  if (!make_tmap_f16(&map, a16, R, g.K)) return MOE_ERR_CUDA;
-  MOE_CHECK_CUDA(launch_gemm_tc(g, map, tc_token_tile(T, c->k + c->n_shared, c->E + c->n_shared), st));
+  TcMaps maps;
+  if (!make_tmaps_b(&maps, a16, R, g.K)) return MOE_ERR_CUDA;
+  MOE_CHECK_CUDA(launch_gemm_tc(g, maps, tc_token_tile(T, c->k + c->n_shared, c->E + c->n_shared), st));
   run->out = g.out;
   run->split_stride = g.split_stride;
   run->S = g.S;

@@ -17,24 +17,31 @@
 // accumulation in tensor memory.
 //
 // Roles (one CTA per SM, persistent over work units):
-//   warp 0      producer: per pipeline stage one bulk copy of CG consecutive
-//               64-wide K chunks of the weight tile (codes + scales), plus TMA
-//               loads of the f16 activation rows of those chunks (16-row
-//               boxes, 128-byte swizzle)
-//   warps 1,14.. MMA issuers (P of them), taking A buffers round-robin:
-//               4 MMAs (K = 16 each) per chunk, A from tensor memory, B from
-//               shared memory, each issuer into its own accumulator; commits
-//               free the A buffer and, per stage, the shared-memory slot. An
-//               issuing thread stalls ~90 cycles on every small-N MMA it
-//               queues, so P issuers keep the tensor pipe fed.
-//   warps 2-9   decoders, two groups of four taking alternate A buffers:
-//               thread = weight row = tensor-memory lane
-//   warps 10-13 epilogue: tensor memory -> fp32 partials in global memory,
+//   warp 0      weight producer: per stage one bulk copy of a pair of
+//               consecutive 64-wide K chunks of the weight tile (codes +
+//               scales) into the weight ring. A stage is released as soon as
+//               its decoders have read it, so the ring's bytes stay in flight
+//               instead of waiting for the MMAs.
+//   warp 25     activation producer: per pair of chunks one 3-D tensor copy
+//               of the f16 activation rows (128-byte swizzle) into the
+//               activation ring, released by the MMA commit. The row box is
+//               the smallest of 8/16/32/64 rows holding the tile's valid
+//               rows: at decode an expert often has 1-4 rows. Two producer
+//               threads, because each copy instruction costs its issuing
+//               thread a few hundred cycles.
+//   warps 1-4   MMA issuers (P of them), taking pairs round-robin: 4 MMAs
+//               (K = 16 each) per chunk, A from tensor memory, B from the
+//               activation ring, each issuer into its own accumulator; the
+//               commits free the A buffer and the activation slot.
+//   warps 5-20  decoders, four groups of four warps, group g filling the A
+//               buffer of every pair with index = g (mod 4): thread = weight
+//               row = tensor-memory lane. Decoding is latency-bound (a chain
+//               of loads, conversions and multiplies per row), so the SM
+//               runs four independent groups.
+//   warps 21-24 epilogue: tensor memory -> fp32 partials in global memory,
 //               scaled by the per-row weight factor and the per-token
 //               activation exponent
 // Work unit = (expert with rows, 128-feature tile, K slice, NT-token tile).
-// The stage ring keeps ~130 KB of weights in flight per SM, which HBM latency
-// needs at full bandwidth.
 // Every wait is bounded in time; on a timeout the CTA sets a status bit,
 // drains its own copies and MMAs, frees tensor memory and returns.
 #include "internal.cuh"
@@ -43,7 +50,13 @@
 namespace moe {
 
 constexpr int kTcNA = 4;          // tensor-memory A buffers, two 64-K chunks (64 columns) each
-constexpr int kTcThreads = 544;   // 17 warps: producer, 4 issuers, 8 decoders, 4 epilogue
+constexpr int kTcNG = 4;          // decoder groups (group g fills A buffer g)
+constexpr int kWIss = 1;          // first MMA-issuer warp
+constexpr int kWDec = 5;          // first decoder warp
+constexpr int kWEpi = kWDec + 4 * kTcNG;   // first epilogue warp
+constexpr int kWBProd = kWEpi + 4;         // activation producer warp
+constexpr int kTcThreads = 32 * (kWBProd + 1);   // 26 warps
+static_assert(kTcNA % kTcNG == 0, "each A buffer belongs to one decoder group");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol0 = kTcNA * 64;
 constexpr int kSmemBudget = 212 * 1024;
@@ -55,12 +68,18 @@ struct TcCfg {
   static constexpr int P = NT <= 32 ? 4 : 2;                         // MMA issuers
   static constexpr int DStride = P * NT;                             // TMEM columns per D buffer
   static constexpr int CB = FMT == MOE_WFMT_NVFP4 ? 4608 : 8448;     // chunk bytes
-  static constexpr int CG = FMT == MOE_WFMT_NVFP4 ? 4 : 2;           // chunks per stage
-  static constexpr int ASlot = (CG * CB + 1023) / 1024 * 1024;
-  static constexpr int BChunk = NT * 128;                             // NT rows x 64 f16
-  static constexpr int StageBytes = ASlot + CG * BChunk;
-  static constexpr int Stages = kSmemBudget / StageBytes > 16 ? 16 : kSmemBudget / StageBytes;
-  static constexpr int SmemBytes = Stages * StageBytes + 1024 /*align*/ + 1024 /*barriers*/;
+  // A stage is one pair of chunks, so every stage feeds exactly one decoder
+  // group and one MMA issuer: weight slot s always belongs to group
+  // s % kTcNG and activation slot s to issuer s % P, and each waiter sees
+  // every phase of its slots in order.
+  static constexpr int WSlot = (2 * CB + 1023) / 1024 * 1024;
+  static constexpr int BSlot = 2 * NT * 128;                         // two chunks x NT rows x 64 f16
+  static constexpr int BS = NT == 16 ? 16 : NT == 32 ? 8 : 4;        // activation slots
+  static constexpr int WSraw = (kSmemBudget - BS * BSlot) / WSlot / kTcNG * kTcNG;
+  static constexpr int WS = WSraw > 24 ? 24 : WSraw;                 // weight stages
+  static constexpr int SmemBytes = WS * WSlot + BS * BSlot + 1024 /*align*/ + 1024 /*barriers*/;
+  static_assert(WS >= 2 * kTcNG && WS % kTcNG == 0, "weight slots must map to decoder groups");
+  static_assert(BS % P == 0, "activation slots must map to MMA issuers");
 };
 
 struct TcUnit {
@@ -146,17 +165,26 @@ __device__ __forceinline__ void decode_chunk(const uint8_t* sa, int p, int rexp,
   }
 }
 
+// Index of the activation row box (8 << index rows) for a tile with nv valid
+// rows; the MMA still spans round_up(nv, 16) rows, and rows past the box
+// (other chunks' data or stale shared memory) only reach accumulator columns
+// of tokens past nv, which the epilogue never reads.
+__device__ __forceinline__ int box_index(int nv) { return nv <= 8 ? 0 : nv <= 16 ? 1 : nv <= 32 ? 2 : 3; }
+
 template <int FMT, int NT>
 __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant__ TcArgs g,
-                                                           const __grid_constant__ CUtensorMap tmap_b) {
+                                                           const __grid_constant__ TcMaps maps) {
   using C = TcCfg<FMT, NT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  uint8_t* stages = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::Stages * C::StageBytes);
-  uint64_t* full = bars;
-  uint64_t* empty = full + C::Stages;
-  uint64_t* afull = empty + C::Stages;
+  uint8_t* wring = smem;
+  uint8_t* bring = smem + C::WS * C::WSlot;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(bring + C::BS * C::BSlot);
+  uint64_t* wfull = bars;
+  uint64_t* wempty = wfull + C::WS;
+  uint64_t* bfull = wempty + C::WS;
+  uint64_t* bempty = bfull + C::BS;
+  uint64_t* afull = bempty + C::BS;
   uint64_t* afree = afull + kTcNA;
   uint64_t* dfull = afree + kTcNA;
   uint64_t* dfree = dfull + 2;
@@ -166,9 +194,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::Stages; ++i) {
-      tc::mbar_init(&full[i], 1);
-      tc::mbar_init(&empty[i], C::P);
+    for (int i = 0; i < C::WS; ++i) {
+      tc::mbar_init(&wfull[i], 1);
+      tc::mbar_init(&wempty[i], 4);   // the 4 warps of the slot's decoder group
+    }
+    for (int i = 0; i < C::BS; ++i) {
+      tc::mbar_init(&bfull[i], 1);
+      tc::mbar_init(&bempty[i], 1);
     }
     for (int i = 0; i < kTcNA; ++i) {
       tc::mbar_init(&afull[i], 128);
@@ -182,7 +214,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
     *abort = 0;
     tc::fence_mbar_init();
   }
-  if (warp == 1) tc::tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == kWIss) tc::tmem_alloc(tmem_slot, kTmemCols);
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
@@ -191,32 +223,25 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
   const int nchunks = g.K / kChunkK;
   const int64_t units = (int64_t)(*g.n_touched) * g.tiles * g.S;
 
+  // Every role walks the same sequence: units -> token tiles -> chunk pairs;
+  // `ait` counts pairs (= weight stages).
   if (warp == 0) {
-    // ---------------- producer ----------------
+    // ---------------- weight producer ----------------
     if (lane == 0) {
-      tc::prefetch_tmap(&tmap_b);
-      const uint64_t pol_w = tc::policy_evict_first(), pol_a = tc::policy_evict_last();
-      uint32_t it = 0;
+      const uint64_t pol_w = tc::policy_evict_first();
+      uint32_t wit = 0;
       bool ok = true;
       for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
         TcUnit w;
         if (!tc_unit(g, u, nchunks, w)) continue;
         const uint8_t* tile = g.w + ((int64_t)w.e * g.tiles + w.j) * g.tile_bytes;
         for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT) {
-          const int nb16 = (min(NT, w.r1 - t0) + 15) >> 4;
-          for (int c = w.c0; c < w.c1; c += C::CG, ++it) {
-            const int nc = min(C::CG, w.c1 - c);
-            const int st = it % C::Stages;
-            const uint32_t ph = (it / C::Stages) & 1;
-            if (!tc::mbar_wait(&empty[st], ph ^ 1, abort)) { ok = false; break; }
-            uint8_t* sa = stages + st * C::StageBytes;
-            uint8_t* sb = sa + C::ASlot;
-            tc::mbar_arrive_expect_tx(&full[st], nc * (C::CB + nb16 * 2048));
-            tc::bulk_g2s(sa, tile + (int64_t)c * C::CB, nc * C::CB, &full[st], pol_w);
-            for (int ci = 0; ci < nc; ++ci)
-              for (int b = 0; b < nb16; ++b)
-                tc::tma_load_2d(sb + ci * C::BChunk + b * 2048, &tmap_b, (c + ci) * kChunkK, t0 + b * 16, &full[st],
-                                pol_a);
+          for (int c = w.c0; c < w.c1; c += 2, ++wit) {
+            const int nc = min(2, w.c1 - c);
+            const int ws = wit % C::WS;
+            if (!tc::mbar_wait(&wempty[ws], ((wit / C::WS) & 1) ^ 1, abort)) { ok = false; break; }
+            tc::mbar_arrive_expect_tx(&wfull[ws], nc * C::CB);
+            tc::bulk_g2s(wring + ws * C::WSlot, tile + (int64_t)c * C::CB, nc * C::CB, &wfull[ws], pol_w);
           }
         }
       }
@@ -224,53 +249,81 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
         // wind-down: wait (bounded, ignoring the abort flag) until every copy
         // still in flight into this CTA's shared memory has landed
         volatile int never = 0;
-        const uint32_t n = it < (uint32_t)C::Stages ? it : (uint32_t)C::Stages;
+        const uint32_t n = wit < (uint32_t)C::WS ? wit : (uint32_t)C::WS;
         for (uint32_t k = 0; k < n; ++k) {
-          const uint32_t i2 = it - 1 - k;
-          tc::mbar_wait(&full[i2 % C::Stages], (i2 / C::Stages) & 1, &never, 400000000ll);
+          const uint32_t i2 = wit - 1 - k;
+          tc::mbar_wait(&wfull[i2 % C::WS], (i2 / C::WS) & 1, &never, 400000000ll);
         }
       }
     }
-  } else if (warp == 1 || warp >= 14) {
-    // ---------------- MMA issuers ----------------
-    const uint32_t mine = warp == 1 ? 0u : (uint32_t)(warp - 13);   // A buffers with (index % P) == mine
-    if (lane == 0 && mine < (uint32_t)C::P) {
-      uint32_t it = 0, ait = 0, dit = 0;
+  } else if (warp == kWBProd) {
+    // ---------------- activation producer ----------------
+    if (lane == 0) {
+      for (int i = 0; i < 4; ++i) tc::prefetch_tmap(&maps.m[i]);
+      const uint64_t pol_a = tc::policy_evict_last();
+      uint32_t ait = 0;
       bool ok = true;
       for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
         TcUnit w;
         if (!tc_unit(g, u, nchunks, w)) continue;
         for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT) {
-          const int nmma = ((min(NT, w.r1 - t0) + 15) >> 4) << 4;
+          const int bi = box_index(min(NT, w.r1 - t0));
+          const uint32_t b_bytes = 2u * (8u << bi) * 128u;
+          for (int c = w.c0; c < w.c1; c += 2, ++ait) {
+            const int bs = ait % C::BS;
+            if (!tc::mbar_wait(&bempty[bs], ((ait / C::BS) & 1) ^ 1, abort)) { ok = false; break; }
+            tc::mbar_arrive_expect_tx(&bfull[bs], b_bytes);
+            // 2 chunks x (8 << bi) rows; a chunk past K reads as zero
+            tc::tma_load_3d(bring + bs * C::BSlot, &maps.m[bi], 0, t0, c, &bfull[bs], pol_a);
+          }
+        }
+      }
+      if (!ok || *abort) {
+        volatile int never = 0;
+        const uint32_t n = ait < (uint32_t)C::BS ? ait : (uint32_t)C::BS;
+        for (uint32_t k = 0; k < n; ++k) {
+          const uint32_t i2 = ait - 1 - k;
+          tc::mbar_wait(&bfull[i2 % C::BS], (i2 / C::BS) & 1, &never, 400000000ll);
+        }
+      }
+    }
+  } else if (warp < kWDec) {
+    // ---------------- MMA issuers ----------------
+    const uint32_t mine = (uint32_t)(warp - kWIss);   // pairs with (index % P) == mine
+    if (lane == 0 && mine < (uint32_t)C::P) {
+      uint32_t ait = 0, dit = 0;
+      bool ok = true;
+      for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
+        TcUnit w;
+        if (!tc_unit(g, u, nchunks, w)) continue;
+        for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT) {
+          const int nv = min(NT, w.r1 - t0);
+          const int nmma = ((nv + 15) >> 4) << 4;
+          const uint32_t b_chunk = (8u << box_index(nv)) * 128u;   // bytes per chunk in an activation slot
           const uint32_t idesc = tc::idesc_f16_f32(128, nmma);
           const int d = dit & 1;
           if (!tc::mbar_wait(&dfree[d], ((dit >> 1) & 1) ^ 1, abort)) { ok = false; break; }
           tc::fence_after_sync();
           const uint32_t dt = tmem + kDCol0 + d * C::DStride + mine * NT;
           bool started = false;
-          for (int c = w.c0; ok && c < w.c1; c += C::CG, ++it) {
-            const int nc = min(C::CG, w.c1 - c);
-            const int st = it % C::Stages;
-            if (!tc::mbar_wait(&full[st], (it / C::Stages) & 1, abort)) { ok = false; break; }
-            const uint32_t sb = tc::smem_u32(stages + st * C::StageBytes + C::ASlot);
-            for (int cp = 0; cp < nc; cp += 2, ++ait) {
-              if (ait % C::P != mine) continue;
-              const int a = ait % kTcNA;
-              if (!tc::mbar_wait(&afull[a], (ait / kTcNA) & 1, abort)) { ok = false; break; }
-              tc::fence_after_sync();
-              const int np = min(2, nc - cp);
-              for (int h = 0; h < np; ++h) {
-                const uint64_t bd = tc::smem_desc_sw128(sb + (cp + h) * C::BChunk);
+          for (int c = w.c0; ok && c < w.c1; c += 2, ++ait) {
+            if (ait % C::P != mine) continue;
+            const int a = ait % kTcNA, bs = ait % C::BS;
+            if (!tc::mbar_wait(&bfull[bs], (ait / C::BS) & 1, abort)) { ok = false; break; }
+            if (!tc::mbar_wait(&afull[a], (ait / kTcNA) & 1, abort)) { ok = false; break; }
+            tc::fence_after_sync();
+            const uint32_t sb = tc::smem_u32(bring + bs * C::BSlot);
+            const int np = min(2, w.c1 - c);
+            for (int h = 0; h < np; ++h) {
+              const uint64_t bd = tc::smem_desc_sw128(sb + h * b_chunk);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                  tc::mma_f16_ts(dt, tmem + a * 64 + h * 32 + kk * 8, bd + (uint64_t)(kk * 2), idesc,
-                                 (started || h > 0 || kk > 0) ? 1u : 0u);
-              }
-              started = true;
-              tc::mma_commit(&afree[a]);
+              for (int kk = 0; kk < 4; ++kk)
+                tc::mma_f16_ts(dt, tmem + a * 64 + h * 32 + kk * 8, bd + (uint64_t)(kk * 2), idesc,
+                               (started || h > 0 || kk > 0) ? 1u : 0u);
             }
-            if (!ok) break;
-            tc::mma_commit(&empty[st]);
+            started = true;
+            tc::mma_commit(&afree[a]);
+            tc::mma_commit(&bempty[bs]);
           }
           if (!ok) break;
           tc::mma_commit(&dfull[d]);
@@ -282,13 +335,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       volatile int never = 0;
       tc::mbar_wait(drain, 0, &never, 400000000ll);
     }
-  } else if (warp < 10) {
+  } else if (warp < kWEpi) {
     // ---------------- decoders ----------------
-    const uint32_t grp = (uint32_t)(warp - 2) >> 2;   // A buffers with (index % 2) == grp
-    const int q = warp & 3;
-    const int p = q * 32 + lane;                  // weight row = TMEM lane
+    const uint32_t grp = (uint32_t)(warp - kWDec) >> 2;   // pairs with (index % kTcNG) == grp
+    const int q = warp & 3;                               // tensor-memory lane quarter of this warp
+    const int p = q * 32 + lane;                          // weight row = TMEM lane
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
-    uint32_t it = 0, ait = 0;
+    uint32_t ait = 0;
     bool ok = true;
     for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
       TcUnit w;
@@ -296,35 +349,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       int rexp = 0;
       if (FMT == MOE_WFMT_MXFP8) rexp = g.wrowexp[((int64_t)w.e * g.tiles + w.j) * kTileN + p];
       for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT) {
-        for (int c = w.c0; ok && c < w.c1; c += C::CG, ++it) {
-          const int nc = min(C::CG, w.c1 - c);
-          const int st = it % C::Stages;
-          // Wait only on stages holding one of this group's pairs: a stage
-          // without one can be consumed and refilled (two phase flips) before
-          // this group gets to it.
-          const bool has_pair = ((nc + 1) >> 1) >= 2 || (ait & 1u) == grp;
-          if (has_pair && !tc::mbar_wait(&full[st], (it / C::Stages) & 1, abort)) { ok = false; break; }
-          const uint8_t* sa = stages + st * C::StageBytes;
-          for (int cp = 0; cp < nc; cp += 2, ++ait) {
-            if ((ait & 1u) != grp) continue;
-            uint32_t v[32];
-            decode_chunk<FMT>(sa + cp * C::CB, p, rexp, v);
-            const int a = ait % kTcNA;
-            if (!tc::mbar_wait(&afree[a], ((ait / kTcNA) & 1) ^ 1, abort)) { ok = false; break; }
-            tc::fence_after_sync();
-            tc::tmem_st32(lane_base + a * 64, v);
-            if (cp + 1 < nc) {
-              decode_chunk<FMT>(sa + (cp + 1) * C::CB, p, rexp, v);
-              tc::tmem_st32(lane_base + a * 64 + 32, v);
-            }
-            tc::tmem_wait_st();
-            tc::fence_before_sync();
-            tc::mbar_arrive(&afull[a]);
+        for (int c = w.c0; ok && c < w.c1; c += 2, ++ait) {
+          if (ait % (uint32_t)kTcNG != grp) continue;   // another group's pair (and weight slot)
+          const int nc = min(2, w.c1 - c);
+          const int ws = ait % C::WS;
+          if (!tc::mbar_wait(&wfull[ws], (ait / C::WS) & 1, abort)) { ok = false; break; }
+          const uint8_t* sa = wring + ws * C::WSlot;
+          uint32_t v[32];
+          decode_chunk<FMT>(sa, p, rexp, v);
+          const int a = ait % kTcNA;
+          if (!tc::mbar_wait(&afree[a], ((ait / kTcNA) & 1) ^ 1, abort)) { ok = false; break; }
+          tc::fence_after_sync();
+          tc::tmem_st32(lane_base + a * 64, v);
+          if (nc > 1) {
+            decode_chunk<FMT>(sa + C::CB, p, rexp, v);
+            tc::tmem_st32(lane_base + a * 64 + 32, v);
           }
+          // this warp has read its rows of the pair: release them
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&wempty[ws]);
+          tc::tmem_wait_st();
+          tc::fence_before_sync();
+          tc::mbar_arrive(&afull[a]);
         }
       }
     }
-  } else {
+  } else if (warp < kWBProd) {
     // ---------------- epilogue ----------------
     const int q = warp & 3;
     const int p = q * 32 + lane;
@@ -334,9 +384,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
     for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
       TcUnit w;
       if (!tc_unit(g, u, nchunks, w)) continue;
-      // A-buffer pairs per token tile (same count the issuers walk)
-      int pairs = 0;
-      for (int c = w.c0; c < w.c1; c += C::CG) pairs += (min(C::CG, w.c1 - c) + 1) >> 1;
+      // chunk pairs per token tile (the sequence the issuers walk)
+      const int pairs = (w.c1 - w.c0 + 1) >> 1;
       int n;
       if (g.interleave_I > 0) n = p < 64 ? 64 * w.j + p : g.interleave_I + 64 * w.j + (p - 64);
       else n = kTileN * w.j + p;
@@ -384,7 +433,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
   tc::fence_before_sync();
   __syncthreads();
   if (threadIdx.x == 0 && *abort) set_status(g.status, MOE_DEV_TIMEOUT);
-  if (warp == 1) {
+  if (warp == kWIss) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, kTmemCols);
   }
@@ -410,22 +459,28 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// 2-D f16 matrix [rows][cols] (row stride cols * 2 bytes), 64 x 16 boxes,
-// 128-byte swizzle; rows past the end read as zero.
-bool make_tmap_f16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols) {
+
+// f16 matrix [rows][cols] viewed as (64 columns, rows, cols / 64 chunks),
+// strides (2 B, cols * 2 B, 128 B); boxes of 64 x (8 << i) x 2 chunks,
+// 128-byte swizzle; rows past the end and chunks past the last read as zero.
+bool make_tmaps_b(TcMaps* maps, const void* base, int64_t rows, int64_t cols) {
   EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)std::max<int64_t>(rows, 1)};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-  cuuint32_t box[2] = {64, 16};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  if (!fn || cols % kChunkK != 0) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)kChunkK, (cuuint64_t)std::max<int64_t>(rows, 1), (cuuint64_t)(cols / kChunkK)};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)kChunkK * 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  for (int i = 0; i < 4; ++i) {
+    cuuint32_t box[3] = {(cuuint32_t)kChunkK, 8u << i, 2u};
+    if (fn(&maps->m[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return false;
+  }
+  return true;
 }
 
 template <int FMT, int NT>
-static cudaError_t launch_tc_t(const TcArgs& g, const CUtensorMap& tmap_b, int grid, cudaStream_t st) {
+static cudaError_t launch_tc_t(const TcArgs& g, const TcMaps& maps, int grid, cudaStream_t st) {
   static bool attr = false;
   if (!attr) {
     cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<FMT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -433,7 +488,7 @@ static cudaError_t launch_tc_t(const TcArgs& g, const CUtensorMap& tmap_b, int g
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  k_gemm_tc<FMT, NT><<<grid, kTcThreads, TcCfg<FMT, NT>::SmemBytes, st>>>(g, tmap_b);
+  k_gemm_tc<FMT, NT><<<grid, kTcThreads, TcCfg<FMT, NT>::SmemBytes, st>>>(g, maps);
   return cudaGetLastError();
 }
 
@@ -444,17 +499,17 @@ int tc_token_tile(int T, int kp, int G) {
   return 64;
 }
 
-cudaError_t launch_gemm_tc(const TcArgs& g, const CUtensorMap& tmap_b, int nt, cudaStream_t st) {
+cudaError_t launch_gemm_tc(const TcArgs& g, const TcMaps& maps, int nt, cudaStream_t st) {
   const int grid = std::max(1, g.max_ctas);
   cudaError_t e;
   if (g.fmt == MOE_WFMT_NVFP4) {
-    e = nt <= 16 ? launch_tc_t<MOE_WFMT_NVFP4, 16>(g, tmap_b, grid, st)
-        : nt <= 32 ? launch_tc_t<MOE_WFMT_NVFP4, 32>(g, tmap_b, grid, st)
-                   : launch_tc_t<MOE_WFMT_NVFP4, 64>(g, tmap_b, grid, st);
+    e = nt <= 16 ? launch_tc_t<MOE_WFMT_NVFP4, 16>(g, maps, grid, st)
+        : nt <= 32 ? launch_tc_t<MOE_WFMT_NVFP4, 32>(g, maps, grid, st)
+                   : launch_tc_t<MOE_WFMT_NVFP4, 64>(g, maps, grid, st);
   } else {
-    e = nt <= 16 ? launch_tc_t<MOE_WFMT_MXFP8, 16>(g, tmap_b, grid, st)
-        : nt <= 32 ? launch_tc_t<MOE_WFMT_MXFP8, 32>(g, tmap_b, grid, st)
-                   : launch_tc_t<MOE_WFMT_MXFP8, 64>(g, tmap_b, grid, st);
+    e = nt <= 16 ? launch_tc_t<MOE_WFMT_MXFP8, 16>(g, maps, grid, st)
+        : nt <= 32 ? launch_tc_t<MOE_WFMT_MXFP8, 32>(g, maps, grid, st)
+                   : launch_tc_t<MOE_WFMT_MXFP8, 64>(g, maps, grid, st);
   }
   note_launch();
   return e;

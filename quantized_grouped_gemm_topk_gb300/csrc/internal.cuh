@@ -66,11 +66,18 @@ struct TcArgs {
   int max_ctas;
   int32_t* status;
 };
-bool make_tmap_f16(CUtensorMap* map, const void* base, int64_t rows, int64_t cols);
+// Tensor maps of the f16 operand rows a16 [rows, cols], viewed as
+// (64 columns, rows, cols / 64 chunks): m[i] loads a box of 8 << i rows of
+// two consecutive 64-column chunks in one copy (128-byte swizzle), stored
+// chunk after chunk.
+struct TcMaps {
+  CUtensorMap m[4];
+};
+bool make_tmaps_b(TcMaps* maps, const void* base, int64_t rows, int64_t cols);
 // nt: tokens per MMA tile (16, 32 or 64); tc_token_tile picks it from the
 // average rows per group.
 int tc_token_tile(int T, int kp, int G);
-cudaError_t launch_gemm_tc(const TcArgs& g, const CUtensorMap& tmap_b, int nt, cudaStream_t st);
+cudaError_t launch_gemm_tc(const TcArgs& g, const TcMaps& maps, int nt, cudaStream_t st);
 // a16[r] = f16 rows of the MXFP8 rows q/s [*, C] at row_map[r] / row_div
 // (or r), rowexp[r] = the row's largest block exponent.
 cudaError_t launch_act_f16(const uint8_t* q, const uint8_t* s, int C, const int32_t* row_map, int row_div, int R,

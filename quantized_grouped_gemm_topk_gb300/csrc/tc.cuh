@@ -21,6 +21,10 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// `count` arrivals at once.
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                : "memory");
@@ -51,19 +55,20 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete, spinning on the
-// non-suspending probe. Gives up after about `limit_cycles` SM clock cycles
-// (4e9: two seconds at the top clock, longer when the clock is lower) or as
-// soon as *abort is set, returning false (the caller then winds down); sets
-// *abort on its own timeout. The timer is the SM's own cycle counter, read
-// only on every 256th probe: these waits sit on the kernels' critical
-// handoffs and must cost no more than the probe when the phase is ready.
+// Waits for the phase with the given parity to complete. try_wait suspends
+// the waiting thread for a short hardware-chosen interval instead of
+// spinning, which leaves issue slots to the warps doing work. Gives up after
+// about `limit_cycles` SM clock cycles (4e9: two seconds at the top clock,
+// longer when the clock is lower) or as soon as *abort is set, returning
+// false (the caller then winds down); sets *abort on its own timeout. The
+// cycle counter is read only on every 64th probe.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           long long limit_cycles = 4000000000ll) {
+  if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  for (uint32_t it = 0;; ++it) {
-    if (mbar_test_wait(bar, parity)) return true;
-    if ((it & 255) == 255) {
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63) == 0) {
       if (*abort) return false;
       if (clock64() - t0 > limit_cycles) {
         *abort = 1;
@@ -103,6 +108,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
+// 3-D tiled tensor copy global -> shared; x is the innermost coordinate
+// (elements), must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar,
+                                            uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 
