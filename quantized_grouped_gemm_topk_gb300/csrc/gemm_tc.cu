@@ -17,11 +17,13 @@
 // accumulation in tensor memory.
 //
 // Roles (one CTA per SM, persistent over work units):
-//   warp 0      weight producer: per stage one bulk copy of a pair of
-//               consecutive 64-wide K chunks of the weight tile (codes +
-//               scales) into the weight ring. A stage is released as soon as
-//               its decoders have read it, so the ring's bytes stay in flight
-//               instead of waiting for the MMAs.
+//   warps 0, 26 weight producers (even / odd stages): per stage one bulk
+//               copy of a pair of consecutive 64-wide K chunks of the weight
+//               tile (codes + scales) into the weight ring. A stage is
+//               released as soon as its decoders have read it, so the ring's
+//               bytes stay in flight instead of waiting for the MMAs. Each
+//               bulk copy costs its issuing thread several hundred cycles,
+//               more than one thread can afford at full bandwidth.
 //   warp 25     activation producer: per pair of chunks one 3-D tensor copy
 //               of the f16 activation rows (128-byte swizzle) into the
 //               activation ring, released by the MMA commit. The row box is
@@ -55,7 +57,8 @@ constexpr int kWIss = 1;          // first MMA-issuer warp
 constexpr int kWDec = 5;          // first decoder warp
 constexpr int kWEpi = kWDec + 4 * kTcNG;   // first epilogue warp
 constexpr int kWBProd = kWEpi + 4;         // activation producer warp
-constexpr int kTcThreads = 32 * (kWBProd + 1);   // 26 warps
+constexpr int kWProd1 = kWBProd + 1;       // second weight producer warp
+constexpr int kTcThreads = 32 * (kWProd1 + 1);   // 27 warps
 static_assert(kTcNA % kTcNG == 0, "each A buffer belongs to one decoder group");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol0 = kTcNA * 64;
@@ -86,14 +89,29 @@ struct TcUnit {
   int e, j, s, c0, c1, r0, r1;
 };
 
-__device__ __forceinline__ bool tc_unit(const TcArgs& g, int64_t u, int nchunks, TcUnit& w) {
+// Groups with rows, staged in shared memory once per CTA: every role looks a
+// unit's group up at every unit boundary, and the dependent global loads
+// (touched list, then offsets) would stall the whole pipeline for ~2 us each
+// time. Groups past the table's end are read from global memory.
+constexpr int kUnitTab = 512;
+struct UnitTab {
+  int e[kUnitTab], r0[kUnitTab], r1[kUnitTab];
+};
+
+__device__ __forceinline__ bool tc_unit(const TcArgs& g, const UnitTab& tab, int64_t u, int nchunks, TcUnit& w) {
   const int per_group = g.tiles * g.S;
   const int ti = (int)(u / per_group), rem = (int)(u % per_group);
   w.j = rem / g.S;
   w.s = rem % g.S;
-  w.e = g.touched[ti];
-  w.r0 = g.offsets[w.e];
-  w.r1 = g.offsets[w.e + 1];
+  if (ti < kUnitTab) {
+    w.e = tab.e[ti];
+    w.r0 = tab.r0[ti];
+    w.r1 = tab.r1[ti];
+  } else {
+    w.e = g.touched[ti];
+    w.r0 = g.offsets[w.e];
+    w.r1 = g.offsets[w.e + 1];
+  }
   w.c0 = (int)((int64_t)w.s * nchunks / g.S);
   w.c1 = (int)((int64_t)(w.s + 1) * nchunks / g.S);
   return w.c1 > w.c0 && w.r1 > w.r0;
@@ -165,6 +183,13 @@ __device__ __forceinline__ void decode_chunk(const uint8_t* sa, int p, int rexp,
   }
 }
 
+// First index >= base that is congruent to r modulo m. Each role steps over
+// its own pairs directly: a single-thread loop that tested and skipped the
+// other roles' pairs spent most of its time resolving branches.
+__device__ __forceinline__ uint32_t first_own(uint32_t base, uint32_t r, uint32_t m) {
+  return base + (r + m - base % m) % m;
+}
+
 // Index of the activation row box (8 << index rows) for a tile with nv valid
 // rows; the MMA still spans round_up(nv, 16) rows, and rows past the box
 // (other chunks' data or stale shared memory) only reach accumulator columns
@@ -192,7 +217,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
+  __shared__ UnitTab tab;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  {
+    const int nt = min(*g.n_touched, kUnitTab);
+    for (int i = threadIdx.x; i < nt; i += blockDim.x) {
+      const int e = g.touched[i];
+      tab.e[i] = e;
+      tab.r0[i] = g.offsets[e];
+      tab.r1[i] = g.offsets[e + 1];
+    }
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::WS; ++i) {
       tc::mbar_init(&wfull[i], 1);
@@ -203,12 +238,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       tc::mbar_init(&bempty[i], 1);
     }
     for (int i = 0; i < kTcNA; ++i) {
-      tc::mbar_init(&afull[i], 128);
+      tc::mbar_init(&afull[i], 4);     // one elected arrive per decoder warp
       tc::mbar_init(&afree[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       tc::mbar_init(&dfull[i], C::P);
-      tc::mbar_init(&dfree[i], 128);
+      tc::mbar_init(&dfree[i], 4);     // one elected arrive per epilogue warp
     }
     tc::mbar_init(drain, C::P);     // one commit from each MMA issuer
     *abort = 0;
@@ -225,23 +260,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
 
   // Every role walks the same sequence: units -> token tiles -> chunk pairs;
   // `ait` counts pairs (= weight stages).
-  if (warp == 0) {
-    // ---------------- weight producer ----------------
+  if (warp == 0 || warp == kWProd1) {
+    // ---------------- weight producers ----------------
+    const uint32_t pid = warp == 0 ? 0u : 1u;   // stages with (index % 2) == pid; WS is even
     if (lane == 0) {
       const uint64_t pol_w = tc::policy_evict_first();
-      uint32_t wit = 0;
+      uint32_t wit = 0, issued = 0;   // issued: one past the last stage this thread issued
       bool ok = true;
       for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
         TcUnit w;
-        if (!tc_unit(g, u, nchunks, w)) continue;
+        if (!tc_unit(g, tab, u, nchunks, w)) continue;
         const uint8_t* tile = g.w + ((int64_t)w.e * g.tiles + w.j) * g.tile_bytes;
-        for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT) {
-          for (int c = w.c0; c < w.c1; c += 2, ++wit) {
+        const uint32_t npt = (uint32_t)(w.c1 - w.c0 + 1) >> 1;   // chunk pairs per token tile
+        for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT, wit += npt) {
+          for (uint32_t i = first_own(wit, pid, 2); i < wit + npt; i += 2) {
+            const int c = w.c0 + 2 * (int)(i - wit);
             const int nc = min(2, w.c1 - c);
-            const int ws = wit % C::WS;
-            if (!tc::mbar_wait(&wempty[ws], ((wit / C::WS) & 1) ^ 1, abort)) { ok = false; break; }
+            const int ws = i % C::WS;
+            if (!tc::mbar_wait(&wempty[ws], ((i / C::WS) & 1) ^ 1, abort)) { ok = false; break; }
             tc::mbar_arrive_expect_tx(&wfull[ws], nc * C::CB);
             tc::bulk_g2s(wring + ws * C::WSlot, tile + (int64_t)c * C::CB, nc * C::CB, &wfull[ws], pol_w);
+            issued = i + 1;
           }
         }
       }
@@ -249,10 +288,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
         // wind-down: wait (bounded, ignoring the abort flag) until every copy
         // still in flight into this CTA's shared memory has landed
         volatile int never = 0;
-        const uint32_t n = wit < (uint32_t)C::WS ? wit : (uint32_t)C::WS;
+        const uint32_t n = issued < (uint32_t)C::WS ? issued : (uint32_t)C::WS;
         for (uint32_t k = 0; k < n; ++k) {
-          const uint32_t i2 = wit - 1 - k;
-          tc::mbar_wait(&wfull[i2 % C::WS], (i2 / C::WS) & 1, &never, 400000000ll);
+          const uint32_t i2 = issued - 1 - k;
+          if ((i2 & 1u) == pid) tc::mbar_wait(&wfull[i2 % C::WS], (i2 / C::WS) & 1, &never, 400000000ll);
         }
       }
     }
@@ -265,7 +304,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       bool ok = true;
       for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
         TcUnit w;
-        if (!tc_unit(g, u, nchunks, w)) continue;
+        if (!tc_unit(g, tab, u, nchunks, w)) continue;
         for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT) {
           const int bi = box_index(min(NT, w.r1 - t0));
           const uint32_t b_bytes = 2u * (8u << bi) * 128u;
@@ -295,7 +334,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       bool ok = true;
       for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
         TcUnit w;
-        if (!tc_unit(g, u, nchunks, w)) continue;
+        if (!tc_unit(g, tab, u, nchunks, w)) continue;
         for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT) {
           const int nv = min(NT, w.r1 - t0);
           const int nmma = ((nv + 15) >> 4) << 4;
@@ -305,26 +344,31 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
           if (!tc::mbar_wait(&dfree[d], ((dit >> 1) & 1) ^ 1, abort)) { ok = false; break; }
           tc::fence_after_sync();
           const uint32_t dt = tmem + kDCol0 + d * C::DStride + mine * NT;
-          bool started = false;
-          for (int c = w.c0; ok && c < w.c1; c += 2, ++ait) {
-            if (ait % C::P != mine) continue;
-            const int a = ait % kTcNA, bs = ait % C::BS;
-            if (!tc::mbar_wait(&bfull[bs], (ait / C::BS) & 1, abort)) { ok = false; break; }
-            if (!tc::mbar_wait(&afull[a], (ait / kTcNA) & 1, abort)) { ok = false; break; }
+          const uint32_t npt = (uint32_t)(w.c1 - w.c0 + 1) >> 1;   // chunk pairs per token tile
+          uint32_t acc = 0;                                       // first MMA of the tile overwrites
+          for (uint32_t i = first_own(ait, mine, C::P); i < ait + npt; i += C::P) {
+            const int a = i % kTcNA, bs = i % C::BS;
+            if (!tc::mbar_wait(&bfull[bs], (i / C::BS) & 1, abort)) { ok = false; break; }
+            if (!tc::mbar_wait(&afull[a], (i / kTcNA) & 1, abort)) { ok = false; break; }
             tc::fence_after_sync();
-            const uint32_t sb = tc::smem_u32(bring + bs * C::BSlot);
-            const int np = min(2, w.c1 - c);
-            for (int h = 0; h < np; ++h) {
-              const uint64_t bd = tc::smem_desc_sw128(sb + h * b_chunk);
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                tc::mma_f16_ts(dt, tmem + a * 64 + h * 32 + kk * 8, bd + (uint64_t)(kk * 2), idesc,
-                               (started || h > 0 || kk > 0) ? 1u : 0u);
+            const uint32_t ta = tmem + a * 64;
+            const uint64_t bd0 = tc::smem_desc_sw128(tc::smem_u32(bring + bs * C::BSlot));
+            tc::mma_f16_ts(dt, ta, bd0, idesc, acc);
+            tc::mma_f16_ts(dt, ta + 8, bd0 + 2, idesc, 1u);
+            tc::mma_f16_ts(dt, ta + 16, bd0 + 4, idesc, 1u);
+            tc::mma_f16_ts(dt, ta + 24, bd0 + 6, idesc, 1u);
+            if (w.c0 + 2 * (int)(i - ait) + 1 < w.c1) {   // second chunk of the pair
+              const uint64_t bd1 = bd0 + (uint64_t)(b_chunk >> 4);
+              tc::mma_f16_ts(dt, ta + 32, bd1, idesc, 1u);
+              tc::mma_f16_ts(dt, ta + 40, bd1 + 2, idesc, 1u);
+              tc::mma_f16_ts(dt, ta + 48, bd1 + 4, idesc, 1u);
+              tc::mma_f16_ts(dt, ta + 56, bd1 + 6, idesc, 1u);
             }
-            started = true;
+            acc = 1u;
             tc::mma_commit(&afree[a]);
             tc::mma_commit(&bempty[bs]);
           }
+          ait += npt;
           if (!ok) break;
           tc::mma_commit(&dfull[d]);
           ++dit;
@@ -345,20 +389,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
     bool ok = true;
     for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
       TcUnit w;
-      if (!tc_unit(g, u, nchunks, w)) continue;
+      if (!tc_unit(g, tab, u, nchunks, w)) continue;
       int rexp = 0;
       if (FMT == MOE_WFMT_MXFP8) rexp = g.wrowexp[((int64_t)w.e * g.tiles + w.j) * kTileN + p];
-      for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT) {
-        for (int c = w.c0; ok && c < w.c1; c += 2, ++ait) {
-          if (ait % (uint32_t)kTcNG != grp) continue;   // another group's pair (and weight slot)
+      const uint32_t npt = (uint32_t)(w.c1 - w.c0 + 1) >> 1;   // chunk pairs per token tile
+      for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT, ait += npt) {
+        for (uint32_t i = first_own(ait, grp, kTcNG); i < ait + npt; i += kTcNG) {
+          const int c = w.c0 + 2 * (int)(i - ait);
           const int nc = min(2, w.c1 - c);
-          const int ws = ait % C::WS;
-          if (!tc::mbar_wait(&wfull[ws], (ait / C::WS) & 1, abort)) { ok = false; break; }
+          const int ws = i % C::WS;
+          if (!tc::mbar_wait(&wfull[ws], (i / C::WS) & 1, abort)) { ok = false; break; }
           const uint8_t* sa = wring + ws * C::WSlot;
           uint32_t v[32];
           decode_chunk<FMT>(sa, p, rexp, v);
-          const int a = ait % kTcNA;
-          if (!tc::mbar_wait(&afree[a], ((ait / kTcNA) & 1) ^ 1, abort)) { ok = false; break; }
+          const int a = i % kTcNA;
+          if (!tc::mbar_wait(&afree[a], ((i / kTcNA) & 1) ^ 1, abort)) { ok = false; break; }
           tc::fence_after_sync();
           tc::tmem_st32(lane_base + a * 64, v);
           if (nc > 1) {
@@ -370,7 +415,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
           if (lane == 0) tc::mbar_arrive(&wempty[ws]);
           tc::tmem_wait_st();
           tc::fence_before_sync();
-          tc::mbar_arrive(&afull[a]);
+          __syncwarp();
+          if (lane == 0) tc::mbar_arrive(&afull[a]);
         }
       }
     }
@@ -383,7 +429,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
     bool ok = true;
     for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
       TcUnit w;
-      if (!tc_unit(g, u, nchunks, w)) continue;
+      if (!tc_unit(g, tab, u, nchunks, w)) continue;
       // chunk pairs per token tile (the sequence the issuers walk)
       const int pairs = (w.c1 - w.c0 + 1) >> 1;
       int n;
@@ -424,7 +470,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
           }
         }
         tc::fence_before_sync();
-        tc::mbar_arrive(&dfree[d]);
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&dfree[d]);
         ++dit;
       }
     }
