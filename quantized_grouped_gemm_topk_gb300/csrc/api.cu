@@ -156,10 +156,20 @@ __global__ void k_fill_f32(float* p, int n, float v) {
   if (i < n) p[i] = v;
 }
 
+// out[i] = sum over ks of part[ks * n + i], added in ks order; 16 loads in
+// flight per thread.
 __global__ void k_reduce_partials(const float* part, int KS, int64_t n, float* out) {
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     float v = part[i];
-    for (int ks = 1; ks < KS; ++ks) v += part[(int64_t)ks * n + i];
+    int ks = 1;
+    for (; ks + 16 <= KS; ks += 16) {
+      float t[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) t[j] = part[(int64_t)(ks + j) * n + i];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v += t[j];
+    }
+    for (; ks < KS; ++ks) v += part[(int64_t)ks * n + i];
     out[i] = v;
   }
 }
@@ -572,6 +582,15 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
     float* part = KS == 1 ? v.logits : at<float>(ws, L.rpart);
     MOE_CHECK_CUDA(launch_router(x, W_r, T, c->H, c->E, KS, part, st));
     a.part = part; a.KS = KS;
+    const int64_t n = (int64_t)T * c->E;
+    if (KS > 1 && n * KS > kRouteStage) {
+      // too many partials for the routing kernel's single block to sum: a
+      // grid-wide pass (same ks order, same result) writes the logits first
+      k_reduce_partials<<<(int)std::min<int64_t>((n + 255) / 256, 4096), 256, 0, st>>>(part, KS, n, v.logits);
+      note_launch();
+      MOE_CHECK_CUDA(cudaGetLastError());
+      a.part = v.logits; a.KS = 1;
+    }
   } else {
     a.part = logits_in; a.KS = 1;
   }

@@ -36,6 +36,10 @@ struct RouteArgs {
 };
 
 int router_splits(int T, int H, int E);
+// Router partials (KS * T * E floats) up to this many are summed inside the
+// fused routing kernel, staged in its shared memory; larger sets are summed
+// by a grid-wide pass first.
+constexpr int64_t kRouteStage = 16 * 1024;
 bool use_small_route(int T, int G, int kp);
 cudaError_t launch_router(const uint16_t* x, const float* Wr, int T, int H, int E, int KS, float* part,
                           cudaStream_t st);

@@ -26,8 +26,36 @@ namespace moe {
 // increasing order. part[ks][t][e] = sum over the ks-th slice of H of
 // x[t][h] * W_r[h][e].
 // ---------------------------------------------------------------------------
-constexpr int kRtKH = 32;
+constexpr int kRtKH = 64;
 
+// Loads one 64-row x 64-expert W tile (4 float4 per thread) into registers;
+// rows past hn and experts past E read as zero.
+__device__ __forceinline__ void router_load_w(const float* __restrict__ Wr, int hb, int hn, int e0, int E,
+                                              float4 (&w)[4]) {
+#pragma unroll
+  for (int r = 0; r < 4; ++r) {
+    const int i = threadIdx.x + r * 256;
+    const int hh = i >> 4, c = (i & 15) * 4;
+    w[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (hh < hn) {
+      const float* src = Wr + (int64_t)(hb + hh) * E + e0 + c;
+      if (e0 + c + 3 < E && (E & 3) == 0) {
+        w[r] = __ldg(reinterpret_cast<const float4*>(src));
+      } else {
+        if (e0 + c + 0 < E) w[r].x = __ldg(src + 0);
+        if (e0 + c + 1 < E) w[r].y = __ldg(src + 1);
+        if (e0 + c + 2 < E) w[r].z = __ldg(src + 2);
+        if (e0 + c + 3 < E) w[r].w = __ldg(src + 3);
+      }
+    }
+  }
+}
+
+// One CTA: TT tokens x 64 experts over the H slice [h0, h1). The next 64-row
+// W tile is loaded into registers while the current one is multiplied, so a
+// CTA keeps its loads in flight instead of paying one DRAM round trip per
+// tile (W_r is streamed once; at decode the CTA count, not the FLOPs, sets
+// the time).
 template <int TT>
 __global__ void __launch_bounds__(256) k_router_partial(const uint16_t* __restrict__ x,
                                                         const float* __restrict__ Wr, int T, int H, int E,
@@ -45,24 +73,15 @@ __global__ void __launch_bounds__(256) k_router_partial(const uint16_t* __restri
   for (int i = 0; i < TPT; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  float4 wn[4];
+  router_load_w(Wr, h0, min(kRtKH, h1 - h0), e0, E, wn);
   for (int hb = h0; hb < h1; hb += kRtKH) {
     const int hn = min(kRtKH, h1 - hb);
     __syncthreads();
-    for (int i = threadIdx.x; i < kRtKH * 16; i += 256) {       // W tile: 32 rows x 64 experts
-      const int hh = i >> 4, c = (i & 15) * 4;
-      float4 w = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (hh < hn) {
-        const float* src = Wr + (int64_t)(hb + hh) * E + e0 + c;
-        if (e0 + c + 3 < E && (E & 3) == 0) {
-          w = __ldg(reinterpret_cast<const float4*>(src));
-        } else {
-          if (e0 + c + 0 < E) w.x = __ldg(src + 0);
-          if (e0 + c + 1 < E) w.y = __ldg(src + 1);
-          if (e0 + c + 2 < E) w.z = __ldg(src + 2);
-          if (e0 + c + 3 < E) w.w = __ldg(src + 3);
-        }
-      }
-      *reinterpret_cast<float4*>(&ws_[hh][c]) = w;
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = threadIdx.x + r * 256;
+      *reinterpret_cast<float4*>(&ws_[i >> 4][(i & 15) * 4]) = wn[r];
     }
     for (int i = threadIdx.x; i < TT * kRtKH; i += 256) {       // x tile, transposed
       const int tt = i / kRtKH, hh = i % kRtKH;
@@ -71,6 +90,7 @@ __global__ void __launch_bounds__(256) k_router_partial(const uint16_t* __restri
       xs_[hh][tt] = v;
     }
     __syncthreads();
+    if (hb + kRtKH < h1) router_load_w(Wr, hb + kRtKH, min(kRtKH, h1 - hb - kRtKH), e0, E, wn);
 #pragma unroll 8
     for (int hh = 0; hh < kRtKH; ++hh) {
       const float4 w = *reinterpret_cast<const float4*>(&ws_[hh][tx * 4]);
@@ -442,9 +462,17 @@ __global__ void __launch_bounds__(1024) k_route_small(const float* __restrict__ 
   if (route) {
     const float* src = part;
     if (KS > 1) {
-      const int64_t n = (int64_t)T * E;
-      for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
-        logits[i] = sum_partials(part, KS, n, i);
+      // stage every partial in shared memory with all loads in flight at
+      // once, then sum each logit in ks order (the launcher only sends
+      // KS * T * E <= kRouteStage floats here)
+      const int n = T * E;
+      float* stg = reinterpret_cast<float*>(wc + 32 * G);
+      for (int i = threadIdx.x; i < n * KS; i += blockDim.x) stg[i] = part[i];
+      __syncthreads();
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        float v = stg[i];
+        for (int ks = 1; ks < KS; ++ks) v += stg[ks * n + i];
+        logits[i] = v;
       }
       __syncthreads();
       src = logits;
@@ -496,8 +524,8 @@ __global__ void __launch_bounds__(1024) k_route_small(const float* __restrict__ 
 // ---------------------------------------------------------------------------
 static int router_tile(int T) { return T <= 16 ? 16 : 32; }
 
-// H slices: about two CTAs per SM, each slice >= 128 rows, and at most 4096
-// partial rows (KS * T) to sum afterwards.
+// H slices: about two CTAs per SM, each slice >= 128 rows (two W tiles), and
+// at most 4096 partial rows (KS * T) to sum afterwards.
 int router_splits(int T, int H, int E) {
   const int tiles = ((T + router_tile(T) - 1) / router_tile(T)) * ((E + 63) / 64);
   int ks = (2 * 152 + tiles - 1) / std::max(tiles, 1);
@@ -523,7 +551,8 @@ bool use_small_route(int T, int G, int kp) { return T <= 256 && T * kp <= 4096 &
 
 template <int VPL>
 static void launch_small(const RouteArgs& a, int kp, int G, int nq, cudaStream_t st) {
-  const size_t smem = small_smem(G);
+  size_t smem = small_smem(G);
+  if (a.route && a.KS > 1) smem += (size_t)a.KS * a.T * a.E * 4;   // staged partials
   static bool attr = false;
   if (!attr) {
     cudaFuncSetAttribute(k_route_small<VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
@@ -538,7 +567,7 @@ static void launch_small(const RouteArgs& a, int kp, int G, int nq, cudaStream_t
 cudaError_t launch_route_dispatch(const RouteArgs& a, cudaStream_t st) {
   const int kp = a.k + a.S, G = a.E + a.S;
   const int T = a.T;
-  if (use_small_route(T, G, kp)) {
+  if (use_small_route(T, G, kp) && (!a.route || a.KS == 1 || (int64_t)a.KS * T * a.E <= kRouteStage)) {
     int nq = T == 0 ? 0 : std::min(64, std::max(1, (T * ((a.H + 255) / 256) + 31) / 32));
     if (!a.x) nq = 0;
     if (a.E <= 256) launch_small<8>(a, kp, G, nq, st);
