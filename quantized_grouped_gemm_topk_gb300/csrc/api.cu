@@ -410,7 +410,7 @@ static int tc_splits(const moe_config_t& c, int T, int tiles, int K, int grid) {
   S = std::min(S, std::max(1, K / kChunkK / 8));
   const int64_t R = std::max<int64_t>(1, (int64_t)T * d.kp);
   S = (int)std::min<int64_t>(S, std::max<int64_t>(1, d.Rmax / R));
-  return std::max(1, S);
+  return std::max(1, std::min(S, 64));   // the GEMM stages at most 64 K-slice boundaries
 }
 
 struct TcRun {

@@ -89,31 +89,64 @@ struct TcUnit {
   int e, j, s, c0, c1, r0, r1;
 };
 
-// Groups with rows, staged in shared memory once per CTA: every role looks a
-// unit's group up at every unit boundary, and the dependent global loads
-// (touched list, then offsets) would stall the whole pipeline for ~2 us each
-// time. Groups past the table's end are read from global memory.
+// Groups with rows and the split boundaries, staged in shared memory once
+// per CTA: every role decodes a unit at every unit boundary, and dependent
+// global loads (touched list, then offsets) or divisions there would stall
+// the pipeline each time (the role threads are single lanes whose dependent
+// instructions issue slowly). Groups past the table's end are read from
+// global memory.
 constexpr int kUnitTab = 512;
+constexpr int kMaxSplits = 64;
 struct UnitTab {
   int e[kUnitTab], r0[kUnitTab], r1[kUnitTab];
+  int cb[kMaxSplits + 1];   // K-slice s covers chunks [cb[s], cb[s + 1])
 };
 
-__device__ __forceinline__ bool tc_unit(const TcArgs& g, const UnitTab& tab, int64_t u, int nchunks, TcUnit& w) {
-  const int per_group = g.tiles * g.S;
-  const int ti = (int)(u / per_group), rem = (int)(u % per_group);
-  w.j = rem / g.S;
-  w.s = rem % g.S;
-  if (ti < kUnitTab) {
-    w.e = tab.e[ti];
-    w.r0 = tab.r0[ti];
-    w.r1 = tab.r1[ti];
+// Work unit u = (ti * tiles + j) * S + s, visited as u = blockIdx.x,
+// blockIdx.x + gridDim.x, ...; the mixed-radix digits are advanced by the
+// precomputed digits of gridDim.x, with no division per step.
+struct UnitIt {
+  uint32_t ti, j, s;
+};
+struct UnitStep {
+  uint32_t dti, dj, ds, tiles, S;
+  __device__ UnitStep(const TcArgs& g) {
+    tiles = (uint32_t)g.tiles;
+    S = (uint32_t)g.S;
+    const uint32_t step = gridDim.x;
+    ds = step % S;
+    dj = (step / S) % tiles;
+    dti = step / (S * tiles);
+  }
+  __device__ UnitIt first() const {
+    const uint32_t b = blockIdx.x;
+    return UnitIt{b / (S * tiles), (b / S) % tiles, b % S};
+  }
+  __device__ void next(UnitIt& it) const {
+    it.s += ds;
+    uint32_t cj = 0;
+    if (it.s >= S) { it.s -= S; cj = 1; }
+    it.j += dj + cj;
+    uint32_t ct = 0;
+    if (it.j >= tiles) { it.j -= tiles; ct = 1; }
+    it.ti += dti + ct;
+  }
+};
+
+__device__ __forceinline__ bool tc_unit(const TcArgs& g, const UnitTab& tab, const UnitIt& it, TcUnit& w) {
+  w.j = (int)it.j;
+  w.s = (int)it.s;
+  if (it.ti < (uint32_t)kUnitTab) {
+    w.e = tab.e[it.ti];
+    w.r0 = tab.r0[it.ti];
+    w.r1 = tab.r1[it.ti];
   } else {
-    w.e = g.touched[ti];
+    w.e = g.touched[it.ti];
     w.r0 = g.offsets[w.e];
     w.r1 = g.offsets[w.e + 1];
   }
-  w.c0 = (int)((int64_t)w.s * nchunks / g.S);
-  w.c1 = (int)((int64_t)(w.s + 1) * nchunks / g.S);
+  w.c0 = tab.cb[it.s];
+  w.c1 = tab.cb[it.s + 1];
   return w.c1 > w.c0 && w.r1 > w.r0;
 }
 
@@ -227,6 +260,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       tab.r0[i] = g.offsets[e];
       tab.r1[i] = g.offsets[e + 1];
     }
+    const int nchunks = g.K / kChunkK;
+    for (int i = threadIdx.x; i <= g.S; i += blockDim.x) tab.cb[i] = (int)((int64_t)i * nchunks / g.S);
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::WS; ++i) {
@@ -255,8 +290,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  const int nchunks = g.K / kChunkK;
-  const int64_t units = (int64_t)(*g.n_touched) * g.tiles * g.S;
+  const uint32_t n_groups = (uint32_t)*g.n_touched;   // groups with rows
+  const UnitStep ustep(g);
 
   // Every role walks the same sequence: units -> token tiles -> chunk pairs;
   // `ait` counts pairs (= weight stages).
@@ -267,9 +302,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       const uint64_t pol_w = tc::policy_evict_first();
       uint32_t wit = 0, issued = 0;   // issued: one past the last stage this thread issued
       bool ok = true;
-      for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      for (UnitIt it = ustep.first(); ok && it.ti < n_groups; ustep.next(it)) {
         TcUnit w;
-        if (!tc_unit(g, tab, u, nchunks, w)) continue;
+        if (!tc_unit(g, tab, it, w)) continue;
         const uint8_t* tile = g.w + ((int64_t)w.e * g.tiles + w.j) * g.tile_bytes;
         const uint32_t npt = (uint32_t)(w.c1 - w.c0 + 1) >> 1;   // chunk pairs per token tile
         for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT, wit += npt) {
@@ -302,9 +337,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       const uint64_t pol_a = tc::policy_evict_last();
       uint32_t ait = 0;
       bool ok = true;
-      for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      for (UnitIt it = ustep.first(); ok && it.ti < n_groups; ustep.next(it)) {
         TcUnit w;
-        if (!tc_unit(g, tab, u, nchunks, w)) continue;
+        if (!tc_unit(g, tab, it, w)) continue;
         for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT) {
           const int bi = box_index(min(NT, w.r1 - t0));
           const uint32_t b_bytes = 2u * (8u << bi) * 128u;
@@ -332,9 +367,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
     if (lane == 0 && mine < (uint32_t)C::P) {
       uint32_t ait = 0, dit = 0;
       bool ok = true;
-      for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
+      for (UnitIt it = ustep.first(); ok && it.ti < n_groups; ustep.next(it)) {
         TcUnit w;
-        if (!tc_unit(g, tab, u, nchunks, w)) continue;
+        if (!tc_unit(g, tab, it, w)) continue;
         for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT) {
           const int nv = min(NT, w.r1 - t0);
           const int nmma = ((nv + 15) >> 4) << 4;
@@ -387,9 +422,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t ait = 0;
     bool ok = true;
-    for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
+    for (UnitIt it = ustep.first(); ok && it.ti < n_groups; ustep.next(it)) {
       TcUnit w;
-      if (!tc_unit(g, tab, u, nchunks, w)) continue;
+      if (!tc_unit(g, tab, it, w)) continue;
       int rexp = 0;
       if (FMT == MOE_WFMT_MXFP8) rexp = g.wrowexp[((int64_t)w.e * g.tiles + w.j) * kTileN + p];
       const uint32_t npt = (uint32_t)(w.c1 - w.c0 + 1) >> 1;   // chunk pairs per token tile
@@ -427,9 +462,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t dit = 0, ait = 0;
     bool ok = true;
-    for (int64_t u = blockIdx.x; ok && u < units; u += gridDim.x) {
+    for (UnitIt it = ustep.first(); ok && it.ti < n_groups; ustep.next(it)) {
       TcUnit w;
-      if (!tc_unit(g, tab, u, nchunks, w)) continue;
+      if (!tc_unit(g, tab, it, w)) continue;
       // chunk pairs per token tile (the sequence the issuers walk)
       const int pairs = (w.c1 - w.c0 + 1) >> 1;
       int n;
