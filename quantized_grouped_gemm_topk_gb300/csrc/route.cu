@@ -241,59 +241,60 @@ __global__ void __launch_bounds__(256) k_hist(const int32_t* __restrict__ ids, i
   for (int e = threadIdx.x; e < G; e += blockDim.x) hist[(int64_t)blockIdx.x * G + e] = sh[e];
 }
 
-// ---------------------------------------------------------------------------
-// Block-wide exclusive scan of n ints held in shared memory (in place);
-// returns the total. blockDim.x must be a multiple of 32.
-// ---------------------------------------------------------------------------
-__device__ int block_excl_scan(int32_t* v, int n, int32_t* scratch /* >= 33 ints */) {
+// Three block-wide exclusive scans in one pass (one set of barriers):
+// a, b, c each hold n ints in shared memory; totals returned in ta, tb, tc.
+// scratch >= 3 * 33 ints.
+__device__ void block_excl_scan3(int32_t* a, int32_t* b, int32_t* c, int n, int32_t* scratch, int& ta, int& tb,
+                                 int& tc) {
   const int tid = threadIdx.x, nt = blockDim.x;
   const int per = (n + nt - 1) / nt;
-  const int b = tid * per, e = min(n, b + per);
-  int s = 0;
-  for (int i = b; i < e; ++i) s += v[i];
-  // inclusive warp scan of s
+  const int lo = tid * per, hi = min(n, lo + per);
+  int sa = 0, sb = 0, sc = 0;
+  for (int i = lo; i < hi; ++i) { sa += a[i]; sb += b[i]; sc += c[i]; }
   const int lane = tid & 31, warp = tid >> 5;
-  int incl = s;
+  int ia = sa, ib = sb, ic = sc;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(kFull, incl, o);
-    if (lane >= o) incl += y;
+    const int ya = __shfl_up_sync(kFull, ia, o), yb = __shfl_up_sync(kFull, ib, o),
+              yc = __shfl_up_sync(kFull, ic, o);
+    if (lane >= o) { ia += ya; ib += yb; ic += yc; }
   }
-  if (lane == 31) scratch[warp] = incl;
+  if (lane == 31) { scratch[warp] = ia; scratch[33 + warp] = ib; scratch[66 + warp] = ic; }
   __syncthreads();
   if (warp == 0) {
-    int nw = nt / 32;
-    int x = lane < nw ? scratch[lane] : 0;
-    int xi = x;
+    const int nw = nt / 32;
+    const int xa = lane < nw ? scratch[lane] : 0, xb = lane < nw ? scratch[33 + lane] : 0,
+              xc = lane < nw ? scratch[66 + lane] : 0;
+    int pa = xa, pb = xb, pc = xc;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(kFull, xi, o);
-      if (lane >= o) xi += y;
+      const int ya = __shfl_up_sync(kFull, pa, o), yb = __shfl_up_sync(kFull, pb, o),
+                yc = __shfl_up_sync(kFull, pc, o);
+      if (lane >= o) { pa += ya; pb += yb; pc += yc; }
     }
-    if (lane < nw) scratch[lane] = xi - x;   // exclusive warp offsets
-    if (lane == 31) scratch[32] = xi;        // total
+    if (lane < nw) { scratch[lane] = pa - xa; scratch[33 + lane] = pb - xb; scratch[66 + lane] = pc - xc; }
+    if (lane == 31) { scratch[32] = pa; scratch[65] = pb; scratch[98] = pc; }
   }
   __syncthreads();
-  int run = scratch[warp] + incl - s;
-  for (int i = b; i < e; ++i) {
-    int c = v[i];
-    v[i] = run;
-    run += c;
+  int ra = scratch[warp] + ia - sa, rb = scratch[33 + warp] + ib - sb, rc = scratch[66 + warp] + ic - sc;
+  for (int i = lo; i < hi; ++i) {
+    const int va = a[i], vb = b[i], vc = c[i];
+    a[i] = ra; b[i] = rb; c[i] = rc;
+    ra += va; rb += vb; rc += vc;
   }
-  int total = scratch[32];
+  ta = scratch[32]; tb = scratch[65]; tc = scratch[98];
   __syncthreads();
-  return total;
 }
 
 // From per-block histograms: counts, offsets, per-block bases, the list of
 // groups with rows (increasing id), and 32-row padded offsets.
-// One block of 1024 threads; smem: 3 * (G + 1) + 33 ints.
+// One block of 1024 threads; smem: 3 * (G + 1) + 99 ints.
 __device__ void scan_groups(const int32_t* hist, int NB, int G, int32_t* counts, int32_t* offsets,
                             int32_t* base, int32_t* touched, int32_t* n_touched, int32_t* poff, int32_t* sm) {
   int32_t* off = sm;               // [G + 1]
   int32_t* flag = sm + (G + 1);    // [G + 1]
   int32_t* pad = flag + (G + 1);   // [G + 1]
-  int32_t* scr = pad + (G + 1);    // [33]
+  int32_t* scr = pad + (G + 1);    // [99]
   for (int e = threadIdx.x; e < G; e += blockDim.x) {
     int c = 0;
     for (int b = 0; b < NB; ++b) c += hist[(int64_t)b * G + e];
@@ -303,9 +304,8 @@ __device__ void scan_groups(const int32_t* hist, int NB, int G, int32_t* counts,
     pad[e] = (c + 31) & ~31;
   }
   __syncthreads();
-  int tot = block_excl_scan(off, G, scr);
-  int ntouch = block_excl_scan(flag, G, scr);
-  int ptot = block_excl_scan(pad, G, scr);
+  int tot, ntouch, ptot;
+  block_excl_scan3(off, flag, pad, G, scr, tot, ntouch, ptot);
   for (int e = threadIdx.x; e < G; e += blockDim.x) {
     offsets[e] = off[e];
     if (poff) poff[e] = pad[e];
@@ -435,7 +435,8 @@ __global__ void __launch_bounds__(256) k_quant_rows_bf16(const uint16_t* __restr
 // warp: each warp counts its segment per group, a per-group prefix over the
 // warps (in warp order) gives every warp its cursors, then each warp places its
 // segment exactly as a single sequential pass would (stable in flat order).
-// smem: G (histogram) + 3 (G + 1) + 33 (scan) + 32 G (per-warp cursors) ints.
+// smem: G (histogram) + 3 (G + 1) + 99 (scan) + 32 G (per-warp cursors) ints,
+// then the staged router partials when KS > 1.
 // ---------------------------------------------------------------------------
 template <int VPL>
 __global__ void __launch_bounds__(1024) k_route_small(const float* __restrict__ part, int KS, int T, int E, int k,
@@ -457,8 +458,8 @@ __global__ void __launch_bounds__(1024) k_route_small(const float* __restrict__ 
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   int32_t* hist = sm;                    // [G]
-  int32_t* scan_sm = sm + G;             // 3 (G + 1) + 33
-  int32_t* wc = scan_sm + 3 * (G + 1) + 33;   // [32][G]
+  int32_t* scan_sm = sm + G;             // 3 (G + 1) + 99
+  int32_t* wc = scan_sm + 3 * (G + 1) + 99;   // [32][G]
   if (route) {
     const float* src = part;
     if (KS > 1) {
@@ -467,7 +468,20 @@ __global__ void __launch_bounds__(1024) k_route_small(const float* __restrict__ 
       // KS * T * E <= kRouteStage floats here)
       const int n = T * E;
       float* stg = reinterpret_cast<float*>(wc + 32 * G);
-      for (int i = threadIdx.x; i < n * KS; i += blockDim.x) stg[i] = part[i];
+      const int tot = n * KS;
+      for (int i0 = 0; i0 < tot; i0 += 16 * 1024) {     // 16 loads in flight per thread
+        float t[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int i = i0 + j * 1024 + threadIdx.x;
+          t[j] = i < tot ? part[i] : 0.f;
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int i = i0 + j * 1024 + threadIdx.x;
+          if (i < tot) stg[i] = t[j];
+        }
+      }
       __syncthreads();
       for (int i = threadIdx.x; i < n; i += blockDim.x) {
         float v = stg[i];
@@ -545,7 +559,7 @@ cudaError_t launch_router(const uint16_t* x, const float* Wr, int T, int H, int 
   return cudaGetLastError();
 }
 
-static size_t small_smem(int G) { return (size_t)(G + 3 * (G + 1) + 33 + 32 * G) * 4; }
+static size_t small_smem(int G) { return (size_t)(G + 3 * (G + 1) + 99 + 32 * G) * 4; }
 
 bool use_small_route(int T, int G, int kp) { return T <= 256 && T * kp <= 4096 && small_smem(G) <= 200 * 1024; }
 
@@ -582,7 +596,7 @@ cudaError_t launch_route_dispatch(const RouteArgs& a, cudaStream_t st) {
   }
   k_hist<<<NB, 256, G * 4, st>>>(a.ids, T, a.k, kp, a.E, G, a.hist, a.status);
   note_launch();
-  size_t smem = (size_t)(3 * (G + 1) + 33) * 4;
+  size_t smem = (size_t)(3 * (G + 1) + 99) * 4;
   if (smem > 48 * 1024) cudaFuncSetAttribute(k_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   k_scan<<<1, 1024, smem, st>>>(a.hist, NB, G, a.counts, a.offsets, a.base, a.touched, a.n_touched, a.poff);
   note_launch();
