@@ -51,8 +51,87 @@ __global__ void __launch_bounds__(256) k_w1_finalize(const W1FinArgs a) {
   }
 }
 
+// The same epilogue for one row per CTA, which also writes the W2 GEMM's f16
+// operand row: y16[r][i] = E4M3 value * 2^(block exponent - row exponent)
+// and y_rowexp[r] = the row's largest block exponent, exactly as the
+// separate conversion pass (k_act_f16) computes them from y1q / y1s. The
+// row's codes and scales are staged in shared memory (I + I/32 bytes) until
+// the row exponent is known. Saves a launch and a pass over y1 per layer.
+__global__ void __launch_bounds__(1024) k_w1_finalize_rows(const W1FinArgs a) {
+  extern __shared__ __align__(16) uint8_t fsm[];
+  uint8_t* qs = fsm;            // [I] codes
+  uint8_t* ss = fsm + a.I;      // [I / 32] scale codes
+  __shared__ int wmax[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int nb = a.I / 32;
+  const int Rv = min(a.R, a.offsets[a.G]);
+  const int64_t r = blockIdx.x;
+  if (r >= Rv) return;
+  const float* P = a.P + r * 2 * a.I;
+  const float wr = a.w_row[r];
+  int mx = 0;
+  for (int b = warp; b < nb; b += nwarps) {
+    const int i = b * 32 + lane;
+    float g = 0.f, u = 0.f;
+#pragma unroll 4
+    for (int s = 0; s < a.S; ++s) {
+      g += P[(int64_t)s * a.split_stride + i];
+      u += P[(int64_t)s * a.split_stride + a.I + i];
+    }
+    const float y = wr * act_fwd(g, u, a.act);
+    const int e = mx_exponent(warp_max(fabsf(y)));
+    const uint8_t c = (uint8_t)(f32x2_to_e4m3x2(y * pow2_neg(e), 0.f) & 0xffu);
+    a.y1q[r * a.I + i] = c;
+    qs[i] = c;
+    if (lane == 0) {
+      a.y1s[r * nb + b] = (uint8_t)(e + 127);
+      ss[b] = (uint8_t)(e + 127);
+    }
+    mx = max(mx, e + 127);
+    if (a.h_save) {
+      a.h_save[r * 2 * a.I + i] = f32_to_bf16_bits(g);
+      a.h_save[r * 2 * a.I + a.I + i] = f32_to_bf16_bits(u);
+    }
+    if (a.y_save) a.y_save[r * a.I + i] = y;
+  }
+  if (lane == 0) wmax[warp] = mx;
+  __syncthreads();
+  mx = wmax[0];
+  for (int w = 1; w < nwarps; ++w) mx = max(mx, wmax[w]);
+  if (threadIdx.x == 0) a.y_rowexp[r] = mx - 127;
+  for (int c0 = threadIdx.x * 8; c0 < a.I; c0 += blockDim.x * 8) {
+    const float f = ldexpf(1.0f, (int)ss[c0 / 32] - mx);
+    const uint2 codes = *reinterpret_cast<const uint2*>(qs + c0);
+    uint32_t outw[4];
+    const uint32_t cw[2] = {codes.x, codes.y};
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float2 lo = e4m3x2_to_f32x2((uint16_t)(cw[h] & 0xffffu));
+      const float2 hi = e4m3x2_to_f32x2((uint16_t)(cw[h] >> 16));
+      const __half2 h0 = __floats2half2_rn(lo.x * f, lo.y * f);
+      const __half2 h1 = __floats2half2_rn(hi.x * f, hi.y * f);
+      outw[2 * h] = *reinterpret_cast<const uint32_t*>(&h0);
+      outw[2 * h + 1] = *reinterpret_cast<const uint32_t*>(&h1);
+    }
+    *reinterpret_cast<uint4*>(a.y16 + r * a.I + c0) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+  }
+}
+
 cudaError_t launch_w1_finalize(const W1FinArgs& a, cudaStream_t st) {
   if (a.R == 0) return cudaSuccess;
+  if (a.y16) {
+    const size_t smem = (size_t)a.I + a.I / 32;
+    if (smem > 48 * 1024) {
+      cudaError_t e = cudaFuncSetAttribute(k_w1_finalize_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)smem);
+      if (e != cudaSuccess) return e;
+    }
+    // few rows (decode): a 1024-thread CTA per row spreads a row's blocks
+    // over 32 warps; many rows: 256 threads per row
+    k_w1_finalize_rows<<<a.R, a.R < 4 * 152 ? 1024 : 256, smem, st>>>(a);
+    note_launch();
+    return cudaGetLastError();
+  }
   k_w1_finalize<<<grid_for((int64_t)a.R * (a.I / 32), 8), 256, 0, st>>>(a);
   note_launch();
   if (a.y16) {
