@@ -159,6 +159,7 @@ __global__ void k_fill_f32(float* p, int n, float v) {
 // out[i] = sum over ks of part[ks * n + i], added in ks order; 16 loads in
 // flight per thread.
 __global__ void k_reduce_partials(const float* part, int KS, int64_t n, float* out) {
+  pdl_enter();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     float v = part[i];
     int ks = 1;
@@ -406,6 +407,7 @@ static int tc_splits(const moe_config_t& c, int T, int tiles, int K, int grid) {
   const Dims d = dims_of(c);
   const double touched = c.E * (1.0 - std::pow(1.0 - (double)c.k / c.E, (double)T)) + c.n_shared;
   const double units = std::max(1.0, touched) * tiles;
+  // about 8 units per CTA, each K slice at least 8 chunks (4 pairs)
   int S = (int)std::lround(8.0 * grid / units);
   S = std::min(S, std::max(1, K / kChunkK / 8));
   const int64_t R = std::max<int64_t>(1, (int64_t)T * d.kp);
@@ -588,9 +590,9 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
       // grid-wide pass (same ks order, same result) writes the logits, then
       // the warp-per-token top-k kernel routes all tokens in parallel and
       // the dispatch kernel takes the ids as given
-      k_reduce_partials<<<(int)std::min<int64_t>((n + 255) / 256, 4096), 256, 0, st>>>(part, KS, n, v.logits);
+      MOE_CHECK_CUDA(launch_pdl(k_reduce_partials, dim3((unsigned)std::min<int64_t>((n + 255) / 256, 4096)), dim3(256),
+                                0, st, (const float*)part, KS, n, v.logits));
       note_launch();
-      MOE_CHECK_CUDA(cudaGetLastError());
       MOE_CHECK_CUDA(launch_topk_only(v.logits, T, c->E, c->k, c->routed_scale, v.d.topk_ids, v.d.topk_w,
                                       at<int32_t>(ws, L.status), st));
       a.part = v.logits; a.KS = 1; a.route = false;

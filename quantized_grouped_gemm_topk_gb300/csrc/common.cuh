@@ -143,6 +143,18 @@ __device__ __forceinline__ float2 act_bwd(float g, float u, float d, const ActPa
   return make_float2(dg, du);
 }
 
+// Programmatic dependent launch. Every kernel of the forward chain first
+// waits until the kernel before it on the stream has completed and its
+// memory is visible (a no-op when it was launched without the attribute),
+// then lets the next kernel of the chain be launched, so the next kernel's
+// launch and CTA setup overlap this kernel's run instead of following it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_enter() {
+  pdl_wait();
+  pdl_trigger();
+}
+
 __device__ __forceinline__ void set_status(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
 }

@@ -62,6 +62,7 @@ __global__ void __launch_bounds__(1024) k_w1_finalize_rows(const W1FinArgs a) {
   uint8_t* qs = fsm;            // [I] codes
   uint8_t* ss = fsm + a.I;      // [I / 32] scale codes
   __shared__ int wmax[32];
+  pdl_enter();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int nb = a.I / 32;
   const int Rv = min(a.R, a.offsets[a.G]);
@@ -128,9 +129,9 @@ cudaError_t launch_w1_finalize(const W1FinArgs& a, cudaStream_t st) {
     }
     // few rows (decode): a 1024-thread CTA per row spreads a row's blocks
     // over 32 warps; many rows: 256 threads per row
-    k_w1_finalize_rows<<<a.R, a.R < 4 * 152 ? 1024 : 256, smem, st>>>(a);
+    cudaError_t e = launch_pdl(k_w1_finalize_rows, dim3(a.R), dim3(a.R < 4 * 152 ? 1024 : 256), smem, st, a);
     note_launch();
-    return cudaGetLastError();
+    return e;
   }
   k_w1_finalize<<<grid_for((int64_t)a.R * (a.I / 32), 8), 256, 0, st>>>(a);
   note_launch();
@@ -159,6 +160,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 __global__ void __launch_bounds__(256) k_finalize_combine(const float* __restrict__ P, int S, int64_t ss, int N,
                                                           const int32_t* __restrict__ inv, int T, int kp,
                                                           uint16_t* __restrict__ z, uint16_t* __restrict__ out) {
+  pdl_enter();
   const int nq = N / 4;
   const int64_t total = (int64_t)T * nq;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
@@ -186,9 +188,9 @@ cudaError_t launch_finalize_combine(const float* P, int S, int64_t ss, int N, co
   if (T == 0) return cudaSuccess;
   int64_t threads = (int64_t)T * (N / 4);
   int blocks = (int)std::min<int64_t>((threads + 255) / 256, 152 * 16);
-  k_finalize_combine<<<blocks, 256, 0, st>>>(P, S, ss, N, inv, T, kp, z, out);
+  cudaError_t e = launch_pdl(k_finalize_combine, dim3(blocks), dim3(256), 0, st, P, S, ss, N, inv, T, kp, z, out);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 __global__ void __launch_bounds__(256) k_finalize_rows(const float* __restrict__ P, int S, int64_t ss, int N, int R,

@@ -252,6 +252,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
 
   __shared__ UnitTab tab;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_enter();
   {
     const int nt = min(*g.n_touched, kUnitTab);
     for (int i = threadIdx.x; i < nt; i += blockDim.x) {
@@ -570,8 +571,7 @@ static cudaError_t launch_tc_t(const TcArgs& g, const TcMaps& maps, int grid, cu
     if (e != cudaSuccess) return e;
     attr = true;
   }
-  k_gemm_tc<FMT, NT><<<grid, kTcThreads, TcCfg<FMT, NT>::SmemBytes, st>>>(g, maps);
-  return cudaGetLastError();
+  return launch_pdl(k_gemm_tc<FMT, NT>, dim3(grid), dim3(kTcThreads), (size_t)TcCfg<FMT, NT>::SmemBytes, st, g, maps);
 }
 
 int tc_token_tile(int T, int kp, int G) {
@@ -610,6 +610,7 @@ __global__ void __launch_bounds__(256) k_act_f16(const uint8_t* __restrict__ q, 
                                                  const int32_t* __restrict__ row_map, int row_div, int R,
                                                  const int32_t* __restrict__ offsets, int G, uint16_t* __restrict__ a16,
                                                  int32_t* __restrict__ rowexp) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
   const int Rv = min(R, offsets[G]);
   const int nsl = (C + 255) / 256;
@@ -651,9 +652,10 @@ cudaError_t launch_act_f16(const uint8_t* q, const uint8_t* s, int C, const int3
   if (R == 0) return cudaSuccess;
   const int64_t warps = (int64_t)R * ((C + 255) / 256);
   const int blocks = (int)std::min<int64_t>((warps + 7) / 8, 152 * 16);
-  k_act_f16<<<blocks, 256, 0, st>>>(q, s, C, row_map, row_div, R, offsets, G, a16, rowexp);
+  cudaError_t e = launch_pdl(k_act_f16, dim3(blocks), dim3(256), 0, st, q, s, C, row_map, row_div, R, offsets, G,
+                             a16, rowexp);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace moe

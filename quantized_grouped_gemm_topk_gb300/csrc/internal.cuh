@@ -1,5 +1,6 @@
 // Internal interfaces between the C-ABI layer (api.cu) and the kernel files.
 #pragma once
+#include <utility>
 #include <cuda.h>
 
 #include <algorithm>
@@ -9,6 +10,25 @@
 #include "common.cuh"
 
 namespace moe {
+
+// Launch with programmatic stream serialization (the kernel must start with
+// pdl_enter(), see common.cuh).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 
 constexpr int kTokBlk = 32;   // tokens per dispatch block (histogram / scatter)
 

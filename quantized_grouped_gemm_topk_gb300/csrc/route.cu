@@ -60,6 +60,7 @@ template <int TT>
 __global__ void __launch_bounds__(256) k_router_partial(const uint16_t* __restrict__ x,
                                                         const float* __restrict__ Wr, int T, int H, int E,
                                                         int KS, float* __restrict__ part) {
+  pdl_enter();
   constexpr int TPT = TT / 16;                     // tokens per thread
   __shared__ __align__(16) float ws_[kRtKH][64];
   __shared__ __align__(16) float xs_[kRtKH][TT + 1];   // +1: conflict-free transposed stores
@@ -203,6 +204,7 @@ template <int VPL>
 __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ part, int KS, int T, int E, int k, float rs,
                                               float* __restrict__ logits, int32_t* __restrict__ ids,
                                               float* __restrict__ wts, int32_t* status) {
+  pdl_enter();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + warp;
   if (t < T) route_token<VPL>(t, lane, part, KS, T, E, k, rs, logits, ids, wts, status);
@@ -210,8 +212,10 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ part, in
 
 static void launch_topk(const float* part, int KS, int T, int E, int k, float rs, float* logits, int32_t* ids,
                         float* wts, int32_t* status, cudaStream_t st) {
-  if (E <= 256) k_topk<8><<<(T + 7) / 8, 256, 0, st>>>(part, KS, T, E, k, rs, logits, ids, wts, status);
-  else k_topk<64><<<(T + 7) / 8, 256, 0, st>>>(part, KS, T, E, k, rs, logits, ids, wts, status);
+  if (E <= 256)
+    launch_pdl(k_topk<8>, dim3((T + 7) / 8), dim3(256), 0, st, part, KS, T, E, k, rs, logits, ids, wts, status);
+  else
+    launch_pdl(k_topk<64>, dim3((T + 7) / 8), dim3(256), 0, st, part, KS, T, E, k, rs, logits, ids, wts, status);
 }
 
 // ---------------------------------------------------------------------------
@@ -447,6 +451,7 @@ __global__ void __launch_bounds__(1024) k_route_small(const float* __restrict__ 
                                                       const uint16_t* __restrict__ x, int H, uint8_t* xq,
                                                       uint8_t* xs, int32_t* status) {
   extern __shared__ int32_t sm[];
+  pdl_enter();
   if (blockIdx.x > 0) {
     const int lane = threadIdx.x & 31;
     const int groups = (H + 255) / 256;
@@ -553,10 +558,10 @@ cudaError_t launch_router(const uint16_t* x, const float* Wr, int T, int H, int 
   if (T == 0) return cudaSuccess;
   const int tt = router_tile(T);
   dim3 grid((T + tt - 1) / tt, (E + 63) / 64, KS);
-  if (tt == 16) k_router_partial<16><<<grid, 256, 0, st>>>(x, Wr, T, H, E, KS, part);
-  else k_router_partial<32><<<grid, 256, 0, st>>>(x, Wr, T, H, E, KS, part);
+  cudaError_t e = tt == 16 ? launch_pdl(k_router_partial<16>, grid, dim3(256), 0, st, x, Wr, T, H, E, KS, part)
+                           : launch_pdl(k_router_partial<32>, grid, dim3(256), 0, st, x, Wr, T, H, E, KS, part);
   note_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 static size_t small_smem(int G) { return (size_t)(G + 3 * (G + 1) + 99 + 32 * G) * 4; }
@@ -572,10 +577,9 @@ static void launch_small(const RouteArgs& a, int kp, int G, int nq, cudaStream_t
     cudaFuncSetAttribute(k_route_small<VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     attr = true;
   }
-  k_route_small<VPL><<<1 + nq, 1024, smem, st>>>(a.part, a.KS, a.T, a.E, a.k, kp, G, a.rs, a.route ? 1 : 0,
-                                                 a.logits, a.ids, a.wts, a.counts, a.offsets, a.touched,
-                                                 a.n_touched, a.poff, a.perm, a.inv, a.w_row, a.x, a.H, a.xq, a.xs,
-                                                 a.status);
+  launch_pdl(k_route_small<VPL>, dim3(1 + nq), dim3(1024), smem, st, a.part, a.KS, a.T, a.E, a.k, kp, G, a.rs,
+             a.route ? 1 : 0, a.logits, a.ids, a.wts, a.counts, a.offsets, a.touched, a.n_touched, a.poff, a.perm,
+             a.inv, a.w_row, a.x, a.H, a.xq, a.xs, a.status);
 }
 
 cudaError_t launch_route_dispatch(const RouteArgs& a, cudaStream_t st) {
