@@ -58,6 +58,11 @@
  *   logit) set bits of a sticky status word inside the workspace and skip the
  *   offending writes; read it with moe_read_status. No kernel traps.
  * - One workspace must not be used by two calls that may run concurrently.
+ * - The forward chain's kernels are launched with programmatic dependent
+ *   launch: each waits for the kernel before it on the stream to complete
+ *   before touching memory, so the stream order the caller sees is the
+ *   plain one (a kernel of the caller's enqueued before a call completes
+ *   before the call's kernels read or write anything).
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H

@@ -20,43 +20,14 @@ static int grid_for(int64_t warps, int warps_per_block) {
 }
 
 // ---- W1 epilogue --------------------------------------------------------------
-// Warp per (row, 32-block of I): sums the K-slice partials, forms
-// y = w_row * act(g, u) and quantises the block of y to MXFP8.
-__global__ void __launch_bounds__(256) k_w1_finalize(const W1FinArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int nb = a.I / 32;
-  const int Rv = min(a.R, a.offsets[a.G]);
-  const int64_t total = (int64_t)Rv * nb;
-  const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
-  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); w < total; w += nw) {
-    const int64_t r = w / nb;
-    const int b = (int)(w % nb);
-    const int i = b * 32 + lane;
-    const float* P = a.P + r * 2 * a.I;
-    float g = 0.f, u = 0.f;
-    for (int s = 0; s < a.S; ++s) {
-      g += P[(int64_t)s * a.split_stride + i];
-      u += P[(int64_t)s * a.split_stride + a.I + i];
-    }
-    const float y = a.w_row[r] * act_fwd(g, u, a.act);
-    const int e = mx_exponent(warp_max(fabsf(y)));
-    const uint16_t c = f32x2_to_e4m3x2(y * pow2_neg(e), 0.f);
-    a.y1q[r * a.I + i] = (uint8_t)(c & 0xffu);
-    if (lane == 0) a.y1s[r * nb + b] = (uint8_t)(e + 127);
-    if (a.h_save) {
-      a.h_save[r * 2 * a.I + i] = f32_to_bf16_bits(g);
-      a.h_save[r * 2 * a.I + a.I + i] = f32_to_bf16_bits(u);
-    }
-    if (a.y_save) a.y_save[r * a.I + i] = y;
-  }
-}
-
-// The same epilogue for one row per CTA, which also writes the W2 GEMM's f16
-// operand row: y16[r][i] = E4M3 value * 2^(block exponent - row exponent)
-// and y_rowexp[r] = the row's largest block exponent, exactly as the
-// separate conversion pass (k_act_f16) computes them from y1q / y1s. The
-// row's codes and scales are staged in shared memory (I + I/32 bytes) until
-// the row exponent is known. Saves a launch and a pass over y1 per layer.
+// One CTA per row r: a warp per 32-block of I sums the K-slice partials,
+// forms y = w_row * act(g, u) and quantises the block to MXFP8 (y1q, y1s).
+// The CTA then writes the W2 GEMM's f16 operand row:
+// y16[r][i] = E4M3 value * 2^(block exponent - row exponent), with
+// y_rowexp[r] = the row's largest block exponent, exactly as the conversion
+// pass k_act_f16 computes them from y1q / y1s. The row's codes and scales
+// are staged in shared memory (I + I/32 bytes) until the row exponent is
+// known, so y1 is not read back from memory.
 __global__ void __launch_bounds__(1024) k_w1_finalize_rows(const W1FinArgs a) {
   extern __shared__ __align__(16) uint8_t fsm[];
   uint8_t* qs = fsm;            // [I] codes
@@ -120,27 +91,17 @@ __global__ void __launch_bounds__(1024) k_w1_finalize_rows(const W1FinArgs a) {
 
 cudaError_t launch_w1_finalize(const W1FinArgs& a, cudaStream_t st) {
   if (a.R == 0) return cudaSuccess;
-  if (a.y16) {
-    const size_t smem = (size_t)a.I + a.I / 32;
-    if (smem > 48 * 1024) {
-      cudaError_t e = cudaFuncSetAttribute(k_w1_finalize_rows, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           (int)smem);
-      if (e != cudaSuccess) return e;
-    }
-    // few rows (decode): a 1024-thread CTA per row spreads a row's blocks
-    // over 32 warps; many rows: 256 threads per row
-    cudaError_t e = launch_pdl(k_w1_finalize_rows, dim3(a.R), dim3(a.R < 4 * 152 ? 1024 : 256), smem, st, a);
-    note_launch();
-    return e;
-  }
-  k_w1_finalize<<<grid_for((int64_t)a.R * (a.I / 32), 8), 256, 0, st>>>(a);
-  note_launch();
-  if (a.y16) {
-    cudaError_t e = cudaGetLastError();
+  if (!a.y16 || !a.y_rowexp) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)a.I + a.I / 32;
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_w1_finalize_rows, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    return launch_act_f16(a.y1q, a.y1s, a.I, nullptr, 1, a.R, a.offsets, a.G, a.y16, a.y_rowexp, st);
   }
-  return cudaGetLastError();
+  // few rows (decode): a 1024-thread CTA per row spreads a row's blocks over
+  // 32 warps; many rows: 256 threads per row
+  cudaError_t e = launch_pdl(k_w1_finalize_rows, dim3(a.R), dim3(a.R < 4 * 152 ? 1024 : 256), smem, st, a);
+  note_launch();
+  return e;
 }
 
 // ---- W2 epilogue + combine --------------------------------------------------

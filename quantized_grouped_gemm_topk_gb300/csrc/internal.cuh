@@ -117,7 +117,7 @@ struct W1FinArgs {
   uint8_t* y1q; uint8_t* y1s;
   uint16_t* h_save;                   // nullable [R][2I] bf16
   float* y_save;                      // nullable [R][I] fp32
-  uint16_t* y16;                      // nullable [R][I] f16 rows for the W2 B operand
+  uint16_t* y16;                      // [R][I] f16 rows for the W2 B operand
   int32_t* y_rowexp;                  // [R] row exponent of y16
 };
 cudaError_t launch_w1_finalize(const W1FinArgs& a, cudaStream_t st);
