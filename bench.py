@@ -29,6 +29,7 @@ for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
 import argparse
 import hashlib
 import json
+import re
 import statistics
 import subprocess
 import sys
@@ -69,9 +70,15 @@ def peaks():
 
 
 def kernel_source_sha():
+    """Hash of the GEMM kernel's sources with comments and whitespace
+    removed, so a recorded ncu traffic figure stays tied to the code that was
+    captured and a comment edit does not void it."""
     h = hashlib.sha256()
     for f in ("gemm_tc.cu", "tc.cuh", "common.cuh", "internal.cuh"):
-        h.update(open(os.path.join(ROOT, "quantized_grouped_gemm_topk_gb300", "csrc", f), "rb").read())
+        src = open(os.path.join(ROOT, "quantized_grouped_gemm_topk_gb300", "csrc", f)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        h.update("".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 
