@@ -94,6 +94,17 @@ def traffic_per_launch(kernel_sha):
     return d
 
 
+def max_over_ranks(value, device):
+    """The largest of every rank's value (the job is as slow as its slowest
+    replica). Needs an initialised process group when the world has more than
+    one rank."""
+    if not (torch.distributed.is_available() and torch.distributed.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -329,9 +340,7 @@ def run_ours(args, s, rank, world, local):
     assert m.moe_read_status(cfg, ws) == 0
     us_step = sum(layer_us) / K
     if world > 1:
-        tt = torch.tensor([us_step], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        us_step = float(tt.item())
+        us_step = max_over_ranks(us_step, dev)
 
     # end to end through the public API with host buffers
     host_x = {T: [xs[T][i].cpu().pin_memory() for i in range(nx)] for T in DECODE_TS}
