@@ -85,7 +85,7 @@ typedef enum moe_status {
 
 /* bits of the device status word */
 #define MOE_DEV_BAD_EXPERT_ID 0x1 /* routing id outside [0, E)              */
-#define MOE_DEV_NAN_LOGIT 0x2     /* NaN among a token's logits              */
+#define MOE_DEV_NAN_LOGIT 0x2     /* NaN among a token's logits (ranked as -inf) */
 #define MOE_DEV_BAD_PACK 0x4      /* packed weight blob header mismatch      */
 #define MOE_DEV_TIMEOUT 0x8       /* a kernel gave up waiting on itself      */
 

@@ -201,3 +201,68 @@ def test_row_subset_matches_full():
     part = M.layer_forward(xb, lg, wts, rows=rows, **kw)
     assert (part.out[3:5] == full.out[3:5]).all()
     assert np.isnan(part.out[0]).all()
+
+
+# ---------------------------------------------------------------------------
+# Readings pinned one by one (each on the oracle alone).
+# ---------------------------------------------------------------------------
+def test_routed_scale_multiplies_renormalised_weights():
+    """Routing weights are the softmax over the k selected logits times
+    routed_scale: they sum to routed_scale, and scale linearly with it."""
+    rng = np.random.default_rng(11)
+    logits = rng.normal(size=(5, 16))
+    ids1, w1 = M.topk_route(logits, 4, 1.0)
+    ids2, w2 = M.topk_route(logits, 4, 2.5)
+    assert (ids1 == ids2).all()
+    np.testing.assert_allclose(w1.sum(axis=1), 1.0, rtol=0, atol=1e-15)
+    np.testing.assert_allclose(w2, 2.5 * w1, rtol=1e-15, atol=0)
+
+
+def test_shared_expert_slot_and_weight():
+    """A shared expert takes slot k (after the routed slots) of every token,
+    group E, weight 1.0 regardless of routed_scale, rows in token order."""
+    rng = np.random.default_rng(12)
+    T, E, k = 6, 8, 2
+    ids, w = M.topk_route(rng.normal(size=(T, E)), k, 2.5)
+    d = M.dispatch(ids, w, E, n_shared=1)
+    kp = k + 1
+    assert d.counts[E] == T
+    rows = range(d.offsets[E], d.offsets[E + 1])
+    assert [d.perm_src[r] for r in rows] == [t * kp + k for t in range(T)]
+    assert all(d.w_row[r] == 1.0 for r in rows)
+    assert all(d.expert[t * kp + k] == E for t in range(T))
+
+
+def test_nan_logit_ranks_below_finite():
+    """A NaN logit is never chosen while k finite logits remain; the weights
+    of the chosen experts stay finite."""
+    logits = np.array([[0.5, np.nan, 2.0, -1.0, 1.0]])
+    ids, w = M.topk_route(logits, 3)
+    assert 1 not in ids[0]
+    assert list(ids[0]) == [2, 4, 0]
+    assert np.isfinite(w).all()
+
+
+def test_dispatch_empty_batch():
+    """T = 0 is legal: zero counts, zero offsets, no rows."""
+    ids = np.zeros((0, 2), np.int32)
+    w = np.zeros((0, 2))
+    d = M.dispatch(ids, w, 8)
+    assert d.counts.shape == (8,) and (d.counts == 0).all()
+    assert (d.offsets == 0).all()
+    assert d.perm_src.size == 0 and d.inv.size == 0
+
+
+def test_clamp_gradient_is_inclusive_at_the_limit():
+    """The clamped SwiGLU passes gradient at |v| == limit and blocks it just
+    outside; inside, both partials match the unclamped form at alpha."""
+    lim, a = 7.0, 1.702
+    d = np.ones(4)
+    g = np.array([lim, -lim, lim * (1 + 1e-12), 0.3])
+    u = np.array([0.5, 0.5, 0.5, -lim])
+    dg, du = M.act_bwd(g, u, d, "swiglu_clamp", a, lim)
+    assert dg[0] != 0 and dg[1] != 0 and dg[2] == 0
+    assert du[3] != 0
+    s = 1.0 / (1.0 + np.exp(-a * 0.3))
+    np.testing.assert_allclose(dg[3], (s + a * 0.3 * s * (1 - s)) * (-lim), rtol=1e-13)
+    np.testing.assert_allclose(du[3], 0.3 * s, rtol=1e-13)
