@@ -83,3 +83,35 @@ def test_host_errors_enqueue_nothing(lib):
     assert lib.moe_layer_backward(ctypes.byref(c), 0x10, 0x10, 4, None, 0x10, 0x10, 0x10, 0x10, 0x10, 0x10,
                                   None) == 2              # NVFP4 config: backward unsupported
     assert m.moe_status_string(0) == "ok"
+
+
+def test_more_host_errors(lib):
+    """Further argument checks that return before any device work (on this
+    machine without a GPU, a call that reached the CUDA runtime would return
+    MOE_ERR_CUDA instead)."""
+    from quantized_grouped_gemm_topk_gb300 import binding as m
+    c = _cfg()
+    P = ctypes.c_void_p
+    by = ctypes.byref
+    # prepack: destination smaller than moe_packed_weights_size
+    src = m.moe_weights_view_t(0x1000, 0x1000, 0x1000, 0x1000, 0x1000, 0x1000)
+    assert lib.moe_prepack_weights(by(c), by(src), m.MOE_PACK_FORWARD, P(0x2000), 16, None) == 3
+    # prepack: NVFP4 needs the per-group fp32 scales; `which` out of range
+    src_nogs = m.moe_weights_view_t(0x1000, 0x1000, None, 0x1000, 0x1000, None)
+    assert lib.moe_prepack_weights(by(c), by(src_nogs), m.MOE_PACK_FORWARD, P(0x2000), 1 << 30, None) == 1
+    assert lib.moe_prepack_weights(by(c), by(src), 7, P(0x2000), 1 << 30, None) == 1
+    # top-k alone: T > T_max, misaligned output; T = 0 accepts NULL row buffers
+    assert lib.moe_route_topk(by(c), P(0x1000), 17, P(0x2000), P(0x3000), P(0x4000), None) == 1
+    assert lib.moe_route_topk(by(c), P(0x1000), 4, P(0x2004), P(0x3000), P(0x4000), None) == 1
+    assert lib.moe_route_topk(by(c), None, 0, None, None, P(0x4000), None) == 0
+    # workspace-free router: NULL W_r, T > T_max; T = 0 is a no-op
+    assert lib.moe_router_logits_noalloc(by(c), P(0x1000), None, 4, P(0x2000), None) == 1
+    assert lib.moe_router_logits_noalloc(by(c), P(0x1000), P(0x1000), 17, P(0x2000), None) == 1
+    assert lib.moe_router_logits_noalloc(by(c), None, P(0x1000), 0, None, None) == 0
+    # an invalid config is reported by every entry point
+    bad = _cfg(k=0)
+    assert lib.moe_layer_forward(by(bad), 0x1000, 0x1000, None, 4, 0x3000, 0x4000, None, 0x5000, None) == 1
+    assert lib.moe_route_topk(by(bad), P(0x1000), 4, P(0x2000), P(0x3000), P(0x4000), None) == 1
+    # status strings exist for every code
+    for code in range(6):
+        assert m.moe_status_string(code) not in ("", "unknown status")
