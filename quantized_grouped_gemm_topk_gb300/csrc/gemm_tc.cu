@@ -564,13 +564,9 @@ bool make_tmaps_b(TcMaps* maps, const void* base, int64_t rows, int64_t cols) {
 
 template <int FMT, int NT>
 static cudaError_t launch_tc_t(const TcArgs& g, const TcMaps& maps, int grid, cudaStream_t st) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<FMT, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         TcCfg<FMT, NT>::SmemBytes);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static bool done[kMaxDevices] = {};
+  cudaError_t e = set_smem_once((const void*)k_gemm_tc<FMT, NT>, TcCfg<FMT, NT>::SmemBytes, done);
+  if (e != cudaSuccess) return e;
   return launch_pdl(k_gemm_tc<FMT, NT>, dim3(grid), dim3(kTcThreads), (size_t)TcCfg<FMT, NT>::SmemBytes, st, g, maps);
 }
 

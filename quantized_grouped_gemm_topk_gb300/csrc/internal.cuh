@@ -11,6 +11,20 @@
 
 namespace moe {
 
+// Raises a kernel's dynamic shared-memory limit once per device (the
+// attribute is per device, and a process may drive several GPUs).
+// `done` is the caller's per-kernel table, indexed by device.
+constexpr int kMaxDevices = 64;
+inline cudaError_t set_smem_once(const void* kern, int bytes, bool (&done)[kMaxDevices]) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 0 && dev < kMaxDevices && done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) done[dev] = true;
+  return e;
+}
+
 // Launch with programmatic stream serialization (the kernel must start with
 // pdl_enter(), see common.cuh).
 template <typename... KArgs, typename... Args>

@@ -572,11 +572,8 @@ template <int VPL>
 static void launch_small(const RouteArgs& a, int kp, int G, int nq, cudaStream_t st) {
   size_t smem = small_smem(G);
   if (a.route && a.KS > 1) smem += (size_t)a.KS * a.T * a.E * 4;   // staged partials
-  static bool attr = false;
-  if (!attr) {
-    cudaFuncSetAttribute(k_route_small<VPL>, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
-    attr = true;
-  }
+  static bool done[kMaxDevices] = {};
+  set_smem_once((const void*)k_route_small<VPL>, 200 * 1024, done);
   launch_pdl(k_route_small<VPL>, dim3(1 + nq), dim3(1024), smem, st, a.part, a.KS, a.T, a.E, a.k, kp, G, a.rs,
              a.route ? 1 : 0, a.logits, a.ids, a.wts, a.counts, a.offsets, a.touched, a.n_touched, a.poff, a.perm,
              a.inv, a.w_row, a.x, a.H, a.xq, a.xs, a.status);
