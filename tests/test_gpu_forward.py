@@ -101,3 +101,39 @@ def test_dsv3_decode(T):
     v = r["views"]
     assert_mx_close(np_(v["y1_q"])[rows], np_(v["y1_s"])[rows], f.y1q[rows], f.y1s[rows], "y1")
     assert_close_layer(np_(r["out"].float())[toks], f.out[toks], "out")
+
+
+def _full_size_sampled(s, T, seed, toks):
+    """Dispatch checked in full; the expert path (y1, out) on the rows of the
+    sampled tokens `toks`."""
+    dev = cuda_device()
+    r = run_forward(s, T, dev=dev, seed=seed)
+    assert r["status"] == 0
+    kp = s.kp
+    inv = np_(r["views"]["inv"])
+    rows = [int(inv[t * kp + j]) for t in toks for j in range(kp)]
+    f = oracle_forward(s, r, rows=rows)
+    _check_dispatch(s, r, f)
+    v = r["views"]
+    assert_mx_close(np_(v["y1_q"])[rows], np_(v["y1_s"])[rows], f.y1q[rows], f.y1s[rows], "y1")
+    assert_close_layer(np_(r["out"].float())[toks], f.out[toks], "out")
+    return r
+
+
+@pytest.mark.parametrize("T", [1, 16, 64])
+def test_shared_expert_decode(T):
+    """Decode with one always-on shared expert at full size (H=6144, I=1536,
+    E=160 + 1 shared, top-8, routed weights x2.5)."""
+    s = inputs.workload("shared", T=T)
+    _full_size_sampled(s, T, 0, list(range(T)) if T <= 2 else [0, T - 1])
+
+
+def test_skewed_routing_full_size():
+    """Zipf-skewed routing at full size (T=4096, H=4096, I=1536, E=128,
+    top-8): 30% of the experts receive no rows, the rest are load-imbalanced;
+    multi-block dispatch and 64-token GEMM tiles."""
+    s = inputs.workload("skewed")
+    r = _full_size_sampled(s, s.T, 3, [0, s.T // 2, s.T - 1])
+    counts = np_(r["views"]["counts"])
+    assert (counts == 0).sum() >= int(0.3 * s.E)
+    assert counts.sum() == s.T * s.k
