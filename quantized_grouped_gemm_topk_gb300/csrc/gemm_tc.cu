@@ -28,8 +28,8 @@
 //               of the f16 activation rows (128-byte swizzle) into the
 //               activation ring, released by the MMA commit. The row box is
 //               the smallest of 8/16/32/64 rows holding the tile's valid
-//               rows: at decode an expert often has 1-4 rows. Two producer
-//               threads, because each copy instruction costs its issuing
+//               rows: at decode an expert often has 1-4 rows. A thread of
+//               its own, because each copy instruction costs its issuing
 //               thread a few hundred cycles.
 //   warps 1-4   MMA issuers (P of them), taking pairs round-robin: 4 MMAs
 //               (K = 16 each) per chunk, A from tensor memory, B from the
@@ -43,7 +43,8 @@
 //   warps 21-24 epilogue: tensor memory -> fp32 partials in global memory,
 //               scaled by the per-row weight factor and the per-token
 //               activation exponent
-// Work unit = (expert with rows, 128-feature tile, K slice, NT-token tile).
+// Work unit = (expert with rows, 128-feature tile, K slice); within a unit
+// the expert's rows are taken NT at a time.
 // Every wait is bounded in time; on a timeout the CTA sets a status bit,
 // drains its own copies and MMAs, frees tensor memory and returns.
 #include "internal.cuh"
