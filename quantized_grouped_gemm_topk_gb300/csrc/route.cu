@@ -20,7 +20,7 @@ namespace moe {
 // S1: logits partials, a register-tiled fp32 GEMM over one slice of H.
 // grid (ceil(T/TT), ceil(E/64), KS), block 256: thread (tx = tid % 16,
 // ty = tid / 16) owns experts 4tx..4tx+3 and tokens ty*TT/16.. of the
-// CTA's 64-expert x TT-token tile. Per 32-row step of H both operands are
+// CTA's 64-expert x TT-token tile. Per 64-row step of H both operands are
 // staged in shared memory (x transposed to [h][token]), so each pair of
 // shared loads feeds 4 * TT/16 FMAs. Every thread accumulates its h in
 // increasing order. part[ks][t][e] = sum over the ks-th slice of H of
