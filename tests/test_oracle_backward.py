@@ -10,6 +10,7 @@ import numpy as np
 import pytest
 
 from oracle import backward as B
+from oracle import formats as F
 from oracle import moe as M
 
 
@@ -91,3 +92,80 @@ def test_quantised_backward_close_to_unquantised():
         a, b = getattr(outs[0], name), getattr(outs[1], name)
         rel = np.linalg.norm(a - b) / np.linalg.norm(a)
         assert rel < 0.15, (name, rel)
+
+
+def test_q_cols_blocks_of_32_rows_with_trailing_zero_pad():
+    """The wgrad operands' quantiser: MXFP8 along the row axis in blocks of 32
+    rows, rows padded with zeros AFTER the data to a multiple of 32. A 33-row
+    input therefore puts row 32 alone in a second block (its 31 pad rows are
+    zero). Expected values worked out by hand from the scale rule (smallest e
+    with amax <= 448 * 2^e) and E4M3 round-to-nearest-even:
+
+      column 0, rows 0..31: 1.0 everywhere except row 5 = 448 * 2^10 and
+        row 7 = 1.1. amax = 448 * 2^10, so e = 10 and the step near zero is
+        the E4M3 subnormal 2^-9 * 2^10 = 2:
+          row 5 -> 448 * 2^10 exactly, row 7 -> 1.1 / 1024 = 0.55 steps -> 2.0,
+          1.0 -> exactly half a step -> ties to the even code 0 -> 0.0.
+      column 0, row 32 (alone): 3.3 -> e = -7 (448 * 2^-7 = 3.5), 3.3 * 128 =
+        422.4 -> nearest E4M3 416 -> 3.25.
+      column 1: zero except row 32 = -0.2 -> e = -11, -0.2 * 2048 = -409.6 ->
+        -416 -> -0.203125.
+    Quantising along the other axis (each row's 32 columns), or padding in
+    front of the data, gives different values (checked below)."""
+    v = np.zeros((33, 32))
+    v[:32, 0] = 1.0
+    v[5, 0] = 448.0 * 2 ** 10
+    v[7, 0] = 1.1
+    v[32, 0] = 3.3
+    v[32, 1] = -0.2
+    got = B._q_cols(v, True)
+    assert got.shape == (33, 32)
+    assert got[5, 0] == 448.0 * 2 ** 10
+    assert got[7, 0] == 2.0
+    for r in set(range(32)) - {5, 7}:
+        assert got[r, 0] == 0.0
+    assert got[32, 0] == 3.25
+    assert got[32, 1] == -0.203125
+    assert (got[:32, 1] == 0.0).all() and (got[:, 2:] == 0.0).all()
+    # the other axis: row 7 alone in its block would give 1.1 -> 1.125, and a
+    # row of 1.0 would stay 1.0
+    along_rows = B._q_rows(v, True)
+    assert along_rows[7, 0] == 1.125 and along_rows[0, 0] == 1.0
+    assert not np.array_equal(along_rows, got)
+    # padding in front of the data would put row 32 in row 5's block
+    front = np.zeros((64, 32))
+    front[31:] = v
+    q, s = F.mx_quantize(front.T)
+    assert F.mx_dequantize(q, s).T[63, 0] == 4.0 != got[32, 0]
+    assert np.array_equal(B._q_cols(v, False), v)
+
+
+def test_backward_reads_bf16_rounded_h():
+    """The backward evaluates SwiGLU and its derivative at the saved h rounded
+    to bf16, not at the exact h. With g = 1 + 2^-10 (rounds to 1.0 in bf16),
+    u = 1, a one-hot upstream gradient and a one-hot W2 copy, the routing-weight
+    gradient is act(1, 1) = sigmoid(1) and the gate gradient is the closed form
+    d/dg[g sigmoid(g)] at g = 1, sigmoid(1) * (2 - sigmoid(1)); the exact h
+    would give values about 1e-3 away."""
+    I = H = 32
+    ids = np.array([[0]], np.int32)
+    w = np.array([[1.0]])
+    disp = M.dispatch(ids, w, 1)
+    h = np.zeros((1, 2 * I))
+    h[0, 0] = 1.0 + 2.0 ** -10          # gate feature 0
+    h[0, I] = 1.0                       # up feature 0
+    fwd = M.Forward(ids, w, disp, None, None, h, np.zeros((1, I)), None, None, np.zeros((1, H)),
+                    np.zeros((1, H)))
+    dout = np.zeros((1, H))
+    dout[0, 0] = 1.0                    # exact in MXFP8
+    w2t = np.zeros((I, H))
+    w2t[0, 0] = 1.0                     # dY1 = e_0
+    bw = B.layer_backward(fwd, np.zeros((1, H)), dout, {}, E=1, k=1, quant=True,
+                          w1t=lambda e: np.zeros((H, 2 * I)), w2t=lambda e: w2t)
+    s1 = 0.7310585786300049             # sigmoid(1)
+    assert bw.dY1[0, 0] == 1.0
+    assert bw.dw_row[0] == pytest.approx(s1, abs=1e-15)
+    assert bw.dh[0, 0] == pytest.approx(s1 * (2.0 - s1), abs=1e-15)
+    assert bw.dh[0, I] == pytest.approx(s1, abs=1e-15)     # du = g * sigmoid(g) at g = 1
+    exact = (1.0 + 2.0 ** -10) / (1.0 + np.exp(-(1.0 + 2.0 ** -10)))
+    assert abs(bw.dw_row[0] - exact) > 5e-4

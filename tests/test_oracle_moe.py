@@ -266,3 +266,36 @@ def test_clamp_gradient_is_inclusive_at_the_limit():
     s = 1.0 / (1.0 + np.exp(-a * 0.3))
     np.testing.assert_allclose(dg[3], (s + a * 0.3 * s * (1 - s)) * (-lim), rtol=1e-13)
     np.testing.assert_allclose(du[3], 0.3 * s, rtol=1e-13)
+
+
+# ---- S1 router logits ---------------------------------------------------------
+def test_router_logits_one_hot_rows_pick_rows_of_w():
+    """x = e_h (a one-hot row) gives logits = W_r[h, :]: the contraction runs
+    over H and the result keeps W_r's expert axis. W_r is non-symmetric, so a
+    transposed operand or a reduction over the wrong axis changes the rows."""
+    W_r = np.array([[0.5, -1.0, 2.0, 0.0],
+                    [3.0, 0.25, -4.0, 1.5],
+                    [-0.75, 6.0, 1.0, -2.0]])          # H = 3, E = 4
+    x = np.zeros((5, 3))
+    hs = [2, 0, 1, 2, 0]
+    for t, h in enumerate(hs):
+        x[t, h] = 1.0
+    got = M.router_logits(x, W_r)
+    assert got.shape == (5, 4)
+    for t, h in enumerate(hs):
+        assert list(got[t]) == list(W_r[h])
+
+
+def test_router_logits_hand_computed_case():
+    """Two tokens, H = 4, E = 3, power-of-two entries (every product and sum
+    exact); expected values worked out by hand:
+      row 0: 1*(1, 0, 2) + 2*(0, 1/4, 1) + 0*(..) - 1*(1, 1, 1) = (0, -1/2, 3)
+      row 1: (1/2)*(1, 0, 2) + 4*(-2, 1, 0)                     = (-15/2, 4, 1)"""
+    x = np.array([[1.0, 2.0, 0.0, -1.0],
+                  [0.5, 0.0, 4.0, 0.0]])
+    W_r = np.array([[1.0, 0.0, 2.0],
+                    [0.0, 0.25, 1.0],
+                    [-2.0, 1.0, 0.0],
+                    [1.0, 1.0, 1.0]])
+    got = M.router_logits(x, W_r)
+    assert got.tolist() == [[0.0, -0.5, 3.0], [-7.5, 4.0, 1.0]]
