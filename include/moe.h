@@ -220,9 +220,13 @@ moe_status_t moe_router_logits(const moe_config_t* cfg, const uint16_t* x, const
  * nothing. Nothing is allocated or freed. All calls on a device share the
  * array and leave their partials in it (each call overwrites what it reads,
  * so nothing needs clearing); calls whose kernels may overlap on the GPU race
- * on it and must be serialised. The first call made with a given device
- * current looks up the array's device address; make it before any stream
- * capture on that device. x [T, H] bf16, W_r [H, E] fp32, logits [T, E]
+ * on it and must be serialised. The array's device address is looked up
+ * the first time a call is made in a given CUDA context (the primary
+ * context, a context the caller created, or one converted from a green
+ * context) and cached under that context's unique id, so each context, and
+ * the context that replaces the primary one after cudaDeviceReset, gets its
+ * own lookup; make the first call in each context before any stream capture
+ * in it. x [T, H] bf16, W_r [H, E] fp32, logits [T, E]
  * fp32, all device. */
 moe_status_t moe_router_logits_noalloc(const moe_config_t* cfg, const uint16_t* x, const float* W_r, int T,
                                        float* logits, void* stream);

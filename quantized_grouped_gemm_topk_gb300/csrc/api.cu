@@ -175,15 +175,6 @@ __global__ void k_reduce_partials(const float* part, int KS, int64_t n, float* o
   }
 }
 
-static int num_sms() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
-  }
-  return n;
-}
 
 }  // namespace moe
 
@@ -448,7 +439,7 @@ static moe_status_t tc_gemm(const moe_config_t* c, const PackLayout& P, int mat,
   g.out = at<float>(ws, L.P);
   const int64_t R = (int64_t)T * (c->k + c->n_shared);
   g.split_stride = R * g.N;
-  int sms = num_sms();
+  int sms = device_sms();
   if (c->max_sms > 0) sms = std::min(sms, c->max_sms);
   g.max_ctas = sms;
   g.S = tc_splits(*c, T, g.tiles, g.K, sms);

@@ -16,7 +16,7 @@ namespace moe {
 
 static int grid_for(int64_t warps, int warps_per_block) {
   int64_t b = (warps + warps_per_block - 1) / warps_per_block;
-  return (int)std::max<int64_t>(1, std::min<int64_t>(b, 152 * 32));
+  return (int)std::max<int64_t>(1, std::min<int64_t>(b, device_sms() * 32));
 }
 
 // ---- W1 epilogue --------------------------------------------------------------
@@ -99,7 +99,7 @@ cudaError_t launch_w1_finalize(const W1FinArgs& a, cudaStream_t st) {
   }
   // few rows (decode): a 1024-thread CTA per row spreads a row's blocks over
   // 32 warps; many rows: 256 threads per row
-  cudaError_t e = launch_pdl(k_w1_finalize_rows, dim3(a.R), dim3(a.R < 4 * 152 ? 1024 : 256), smem, st, a);
+  cudaError_t e = launch_pdl(k_w1_finalize_rows, dim3(a.R), dim3(a.R < 4 * device_sms() ? 1024 : 256), smem, st, a);
   note_launch();
   return e;
 }
@@ -148,7 +148,7 @@ cudaError_t launch_finalize_combine(const float* P, int S, int64_t ss, int N, co
                                     uint16_t* z, uint16_t* out, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   int64_t threads = (int64_t)T * (N / 4);
-  int blocks = (int)std::min<int64_t>((threads + 255) / 256, 152 * 16);
+  int blocks = (int)std::min<int64_t>((threads + 255) / 256, device_sms() * 16);
   cudaError_t e = launch_pdl(k_finalize_combine, dim3(blocks), dim3(256), 0, st, P, S, ss, N, inv, T, kp, z, out);
   note_launch();
   return e;
@@ -170,7 +170,7 @@ __global__ void __launch_bounds__(256) k_finalize_rows(const float* __restrict__
 cudaError_t launch_finalize_rows(const float* P, int S, int64_t ss, int N, int R, uint16_t* z, cudaStream_t st) {
   if (R == 0) return cudaSuccess;
   int64_t threads = (int64_t)R * (N / 4);
-  int blocks = (int)std::min<int64_t>((threads + 255) / 256, 152 * 16);
+  int blocks = (int)std::min<int64_t>((threads + 255) / 256, device_sms() * 16);
   k_finalize_rows<<<blocks, 256, 0, st>>>(P, S, ss, N, R, z);
   note_launch();
   return cudaGetLastError();
@@ -204,7 +204,7 @@ cudaError_t launch_combine(const uint16_t* z, const int32_t* inv, const float* t
                            uint16_t* out, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
   int64_t threads = (int64_t)T * (H / 4);
-  int blocks = (int)std::min<int64_t>((threads + 255) / 256, 152 * 16);
+  int blocks = (int)std::min<int64_t>((threads + 255) / 256, device_sms() * 16);
   k_combine<<<blocks, 256, 0, st>>>(z, inv, topk_w, T, k, kp, H, out);
   note_launch();
   return cudaGetLastError();

@@ -565,7 +565,7 @@ bool make_tmaps_b(TcMaps* maps, const void* base, int64_t rows, int64_t cols) {
 
 template <int FMT, int NT>
 static cudaError_t launch_tc_t(const TcArgs& g, const TcMaps& maps, int grid, cudaStream_t st) {
-  static bool done[kMaxDevices] = {};
+  static std::atomic<bool> done[kMaxDevices] = {};
   cudaError_t e = set_smem_once((const void*)k_gemm_tc<FMT, NT>, TcCfg<FMT, NT>::SmemBytes, done);
   if (e != cudaSuccess) return e;
   return launch_pdl(k_gemm_tc<FMT, NT>, dim3(grid), dim3(kTcThreads), (size_t)TcCfg<FMT, NT>::SmemBytes, st, g, maps);
@@ -648,7 +648,7 @@ cudaError_t launch_act_f16(const uint8_t* q, const uint8_t* s, int C, const int3
                            const int32_t* offsets, int G, uint16_t* a16, int32_t* rowexp, cudaStream_t st) {
   if (R == 0) return cudaSuccess;
   const int64_t warps = (int64_t)R * ((C + 255) / 256);
-  const int blocks = (int)std::min<int64_t>((warps + 7) / 8, 152 * 16);
+  const int blocks = (int)std::min<int64_t>((warps + 7) / 8, device_sms() * 16);
   cudaError_t e = launch_pdl(k_act_f16, dim3(blocks), dim3(256), 0, st, q, s, C, row_map, row_div, R, offsets, G,
                              a16, rowexp);
   note_launch();

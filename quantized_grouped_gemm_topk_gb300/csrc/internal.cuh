@@ -1,5 +1,6 @@
 // Internal interfaces between the C-ABI layer (api.cu) and the kernel files.
 #pragma once
+#include <atomic>
 #include <utility>
 #include <cuda.h>
 
@@ -13,16 +14,37 @@ namespace moe {
 
 // Raises a kernel's dynamic shared-memory limit once per device (the
 // attribute is per device, and a process may drive several GPUs).
-// `done` is the caller's per-kernel table, indexed by device.
+// `done` is the caller's per-kernel table, indexed by device; its flags are
+// atomic so host threads launching on one device concurrently are safe (at
+// worst both set the attribute).
 constexpr int kMaxDevices = 64;
-inline cudaError_t set_smem_once(const void* kern, int bytes, bool (&done)[kMaxDevices]) {
+inline cudaError_t set_smem_once(const void* kern, int bytes, std::atomic<bool> (&done)[kMaxDevices]) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev >= 0 && dev < kMaxDevices && done[dev]) return cudaSuccess;
+  const bool slot = dev >= 0 && dev < kMaxDevices;
+  if (slot && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-  if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices) done[dev] = true;
+  if (e == cudaSuccess && slot) done[dev].store(true, std::memory_order_release);
   return e;
+}
+
+// Number of SMs of the current device, queried once per device (atomic
+// cache, same thread-safety rule as set_smem_once). Grid sizes and split
+// counts follow it instead of assuming a particular part.
+inline int device_sms() {
+  static std::atomic<int> cache[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) dev = -1;
+  const bool slot = dev >= 0 && dev < kMaxDevices;
+  if (slot) {
+    const int n = cache[dev].load(std::memory_order_acquire);
+    if (n > 0) return n;
+  }
+  int n = 0;
+  if (dev < 0 || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 1;
+  if (slot) cache[dev].store(n, std::memory_order_release);
+  return n;
 }
 
 // Launch with programmatic stream serialization (the kernel must start with

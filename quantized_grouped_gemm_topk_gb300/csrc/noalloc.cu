@@ -19,9 +19,14 @@
 //   * two calls whose kernels may overlap on the GPU (different streams with
 //     no ordering between them, or several host threads) race on the array:
 //     serialise them;
-//   * the array's device address is looked up (cudaGetSymbolAddress) on the
-//     first call made while a given device is current; make that first call
-//     before any stream capture on that device.
+//   * the array's device address is looked up (cudaGetSymbolAddress) the
+//     first time a call is made in a given CUDA context and cached under
+//     that context's unique id (cuCtxGetId): the device's primary context,
+//     a context the caller created, or one converted from a green context
+//     each hold their own copy of the array and get their own lookup, and
+//     the context that replaces a primary context after cudaDeviceReset has
+//     a new id, so a stale address is never reused. Make the first call in
+//     each context before any stream capture in it.
 // The result is bit-identical to moe_router_logits: the same kernels, the
 // same split count and the same summation order.
 #include <mutex>
@@ -31,25 +36,75 @@
 namespace moe {
 
 constexpr size_t kNoAllocScratchFloats = size_t(1) << 20;   // 4 MiB
-constexpr int kNoAllocMaxDevices = 64;
+constexpr int kNoAllocCacheSlots = 64;
 
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
 
-static std::mutex g_noalloc_mu;
-static float* g_noalloc_ptr[kNoAllocMaxDevices] = {};
+// Driver entry points, resolved through the runtime so the library needs no
+// link against the driver library.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
-// Device address of g_noalloc_scratch on the current device (looked up once
-// per device); nullptr on failure.
-static float* noalloc_scratch() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
+struct CtxFns {
+  CtxGetCurrentFn get_current = nullptr;
+  CtxGetIdFn get_id = nullptr;
+};
+
+static const CtxFns& ctx_fns() {
+  static const CtxFns f = [] {
+    CtxFns r;
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
-    g_noalloc_ptr[dev] = reinterpret_cast<float*>(p);
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      r.get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      r.get_id = reinterpret_cast<CtxGetIdFn>(p);
+    return r;
+  }();
+  return f;
+}
+
+// Unique id of the calling thread's current context; false when there is
+// none yet (the runtime has not made its primary context current) or the
+// driver cannot say.
+static bool current_ctx_id(unsigned long long* id) {
+  const CtxFns& f = ctx_fns();
+  if (!f.get_current || !f.get_id) return false;
+  CUcontext c = nullptr;
+  if (f.get_current(&c) != CUDA_SUCCESS || !c) return false;
+  return f.get_id(c, id) == CUDA_SUCCESS;
+}
+
+static std::mutex g_noalloc_mu;
+static unsigned long long g_noalloc_ctx[kNoAllocCacheSlots] = {};
+static float* g_noalloc_ptr[kNoAllocCacheSlots] = {};
+static int g_noalloc_next = 0;
+
+// Device address of g_noalloc_scratch in the current context; nullptr on
+// failure.
+static float* noalloc_scratch() {
+  unsigned long long id = 0;
+  bool have = current_ctx_id(&id);
+  if (have) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    for (int i = 0; i < kNoAllocCacheSlots; ++i)
+      if (g_noalloc_ptr[i] && g_noalloc_ctx[i] == id) return g_noalloc_ptr[i];
   }
-  return g_noalloc_ptr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return nullptr;
+  // the lookup makes the runtime's context current if none was
+  if (!have) have = current_ctx_id(&id);
+  if (have) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    const int i = g_noalloc_next;
+    g_noalloc_next = (g_noalloc_next + 1) % kNoAllocCacheSlots;
+    g_noalloc_ctx[i] = id;
+    g_noalloc_ptr[i] = reinterpret_cast<float*>(p);
+  }
+  return reinterpret_cast<float*>(p);
 }
 
 __global__ void k_sum_partials_noalloc(const float* __restrict__ part, int KS, int64_t n, float* __restrict__ out) {

@@ -9,9 +9,10 @@
 // in GPU memory so nothing waits on the host. On one GPU the cross-rank token
 // pull becomes this local, deterministic permutation.
 //
-// Determinism: counts come from order-independent integer histograms; the
-// row order inside a group is fixed by a stable, warp-sequential scatter in
-// flat assignment order (t * k' + j); no float atomics anywhere.
+// Determinism: counts come from per-warp histograms built with warp match
+// (no atomics: each count is a fixed sequence of integer additions); the row
+// order inside a group is fixed by a stable, warp-sequential scatter in flat
+// assignment order (t * k' + j).
 #include "internal.cuh"
 
 namespace moe {
@@ -153,7 +154,7 @@ __device__ void route_token(int t, int lane, const float* __restrict__ part, int
   const float* row_in = part + (int64_t)t * E;
   float* row = logits + (int64_t)t * E;
   float vals[VPL];
-#pragma unroll
+#pragma unroll (VPL <= 8 ? VPL : 1)
   for (int i = 0; i < VPL; ++i) {
     const int e = lane + 32 * i;
     float v = -INFINITY;
@@ -172,7 +173,7 @@ __device__ void route_token(int t, int lane, const float* __restrict__ part, int
   for (int j = 0; j < k; ++j) {
     float bv = -INFINITY;
     int bi = 0x7fffffff;
-#pragma unroll
+#pragma unroll (VPL <= 8 ? VPL : 1)
     for (int i = 0; i < VPL; ++i) {
       const int e = lane + 32 * i;
       if (e >= E || (taken >> i & 1ull)) continue;
@@ -219,9 +220,14 @@ static void launch_topk(const float* part, int KS, int T, int E, int k, float rs
 }
 
 // ---------------------------------------------------------------------------
-// S3: per-block histograms of the assignments of kTokBlk tokens.
-// grid NB = ceil(T / kTokBlk), block 256. Invalid ids are skipped (and
-// flagged); shared slots count for every token.
+// S3: per-block histograms of the assignments of kTokBlk tokens, without
+// atomics. grid NB = ceil(T / kTokBlk), one warp per block. The warp walks
+// the block's assignments 32 at a time; lanes holding the same expert are
+// grouped with __match_any_sync and the group's lowest lane adds the group
+// size. Within one step the adding lanes hold distinct experts, and the
+// steps follow one another, so every count is a plain sequence of integer
+// additions. Invalid ids are skipped (and flagged); shared slots count for
+// every token.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ int assignment_expert(const int32_t* ids, int t, int j, int k, int E) {
   if (j >= k) return E + (j - k);
@@ -229,20 +235,33 @@ __device__ __forceinline__ int assignment_expert(const int32_t* ids, int t, int 
   return (e >= 0 && e < E) ? e : -1;
 }
 
-__global__ void __launch_bounds__(256) k_hist(const int32_t* __restrict__ ids, int T, int k, int kp, int E, int G,
-                                              int32_t* __restrict__ hist, int32_t* status) {
-  extern __shared__ int32_t sh[];
-  for (int e = threadIdx.x; e < G; e += blockDim.x) sh[e] = 0;
-  __syncthreads();
-  const int t0 = blockIdx.x * kTokBlk, t1 = min(T, t0 + kTokBlk);
+// Adds the experts of assignments [a0, a1) to cnt (one warp; cnt is private
+// to the warp). Returns true on any lane that met an invalid id.
+__device__ __forceinline__ bool warp_count(int a0, int a1, const int32_t* ids, int k, int kp, int E, int32_t* cnt) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
   bool bad = false;
-  for (int a = t0 * kp + threadIdx.x; a < t1 * kp; a += blockDim.x) {
-    int e = assignment_expert(ids, a / kp, a % kp, k, E);
-    if (e < 0) bad = true;
-    else atomicAdd(&sh[e], 1);
+  for (int c = a0; c < a1; c += kWarp) {
+    const int a = c + lane;
+    const int e = a < a1 ? assignment_expert(ids, a / kp, a % kp, k, E) : -2;
+    if (e == -1) bad = true;
+    const unsigned m = __match_any_sync(kFull, e);
+    if (e >= 0 && (m & lt) == 0) cnt[e] += __popc(m);
+    __syncwarp();
   }
-  if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(status, MOE_DEV_BAD_EXPERT_ID);
-  for (int e = threadIdx.x; e < G; e += blockDim.x) hist[(int64_t)blockIdx.x * G + e] = sh[e];
+  return bad;
+}
+
+__global__ void __launch_bounds__(32) k_hist(const int32_t* __restrict__ ids, int T, int k, int kp, int E, int G,
+                                             int32_t* __restrict__ hist, int32_t* status) {
+  extern __shared__ int32_t sh[];
+  for (int e = threadIdx.x; e < G; e += kWarp) sh[e] = 0;
+  __syncwarp();
+  const int t0 = blockIdx.x * kTokBlk, t1 = min(T, t0 + kTokBlk);
+  const bool bad = warp_count(t0 * kp, t1 * kp, ids, k, kp, E, sh);
+  if (__any_sync(kFull, bad) && threadIdx.x == 0) set_status(status, MOE_DEV_BAD_EXPERT_ID);
+  __syncwarp();
+  for (int e = threadIdx.x; e < G; e += kWarp) hist[(int64_t)blockIdx.x * G + e] = sh[e];
 }
 
 // Three block-wide exclusive scans in one pass (one set of barriers):
@@ -498,32 +517,24 @@ __global__ void __launch_bounds__(1024) k_route_small(const float* __restrict__ 
     }
     for (int t = warp; t < T; t += 32) route_token<VPL>(t, lane, src, 1, T, E, k, rs, logits, ids, wts, status);
   }
-  for (int e = threadIdx.x; e < G; e += blockDim.x) hist[e] = 0;
   __syncthreads();   // ids / wts written by this block are visible block-wide
-  bool bad = false;
+  // per-warp segment counts (atomic-free, see warp_count); the histogram is
+  // their sum in warp order
   const int n = T * kp;
-  for (int a = threadIdx.x; a < n; a += blockDim.x) {
-    int e = assignment_expert(ids, a / kp, a % kp, k, E);
-    if (e < 0) bad = true;
-    else atomicAdd(&hist[e], 1);
-  }
-  if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(status, MOE_DEV_BAD_EXPERT_ID);
-  scan_groups(hist, 1, G, counts, offsets, nullptr, touched, n_touched, poff, scan_sm);
-  __syncthreads();
-  // per-warp segment counts
   const int seg = ((n + 31) / 32 + 31) / 32 * 32;
   const int a0 = min(n, warp * seg), a1 = min(n, a0 + seg);
   int32_t* wcw = wc + warp * G;
   for (int e = lane; e < G; e += 32) wcw[e] = 0;
   __syncwarp();
-  const unsigned lt = (1u << lane) - 1u;
-  for (int c = a0; c < a1; c += 32) {
-    const int a = c + lane;
-    const int e = a < a1 ? assignment_expert(ids, a / kp, a % kp, k, E) : -1;
-    const unsigned m = __match_any_sync(kFull, e);
-    if (e >= 0 && (m & lt) == 0) wcw[e] += __popc(m);
-    __syncwarp();
+  const bool bad = warp_count(a0, a1, ids, k, kp, E, wcw);
+  if (__syncthreads_or(bad) && threadIdx.x == 0) set_status(status, MOE_DEV_BAD_EXPERT_ID);
+  for (int e = threadIdx.x; e < G; e += blockDim.x) {
+    int c = 0;
+    for (int w = 0; w < 32; ++w) c += wc[w * G + e];
+    hist[e] = c;
   }
+  __syncthreads();
+  scan_groups(hist, 1, G, counts, offsets, nullptr, touched, n_touched, poff, scan_sm);
   __syncthreads();
   // cursors: group offset plus the counts of the earlier warps
   for (int e = threadIdx.x; e < G; e += blockDim.x) {
@@ -547,7 +558,7 @@ static int router_tile(int T) { return T <= 16 ? 16 : 32; }
 // at most 4096 partial rows (KS * T) to sum afterwards.
 int router_splits(int T, int H, int E) {
   const int tiles = ((T + router_tile(T) - 1) / router_tile(T)) * ((E + 63) / 64);
-  int ks = (2 * 152 + tiles - 1) / std::max(tiles, 1);
+  int ks = (2 * device_sms() + tiles - 1) / std::max(tiles, 1);
   ks = std::max(1, std::min(ks, std::max(1, H / 128)));
   if ((int64_t)ks * T > 4096) ks = std::max(1, 4096 / std::max(T, 1));
   return ks;
@@ -572,7 +583,7 @@ template <int VPL>
 static void launch_small(const RouteArgs& a, int kp, int G, int nq, cudaStream_t st) {
   size_t smem = small_smem(G);
   if (a.route && a.KS > 1) smem += (size_t)a.KS * a.T * a.E * 4;   // staged partials
-  static bool done[kMaxDevices] = {};
+  static std::atomic<bool> done[kMaxDevices] = {};
   set_smem_once((const void*)k_route_small<VPL>, 200 * 1024, done);
   launch_pdl(k_route_small<VPL>, dim3(1 + nq), dim3(1024), smem, st, a.part, a.KS, a.T, a.E, a.k, kp, G, a.rs,
              a.route ? 1 : 0, a.logits, a.ids, a.wts, a.counts, a.offsets, a.touched, a.n_touched, a.poff, a.perm,
@@ -595,7 +606,7 @@ cudaError_t launch_route_dispatch(const RouteArgs& a, cudaStream_t st) {
     launch_topk(a.part, a.KS, T, a.E, a.k, a.rs, a.logits, a.ids, a.wts, a.status, st);
     note_launch();
   }
-  k_hist<<<NB, 256, G * 4, st>>>(a.ids, T, a.k, kp, a.E, G, a.hist, a.status);
+  k_hist<<<NB, 32, G * 4, st>>>(a.ids, T, a.k, kp, a.E, G, a.hist, a.status);
   note_launch();
   size_t smem = (size_t)(3 * (G + 1) + 99) * 4;
   if (smem > 48 * 1024) cudaFuncSetAttribute(k_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -606,7 +617,7 @@ cudaError_t launch_route_dispatch(const RouteArgs& a, cudaStream_t st) {
   if (a.x) {
     int groups = (a.H + 255) / 256;
     int64_t warps = (int64_t)T * groups;
-    int blocks = (int)std::min<int64_t>((warps + 7) / 8, 152 * 16);
+    int blocks = (int)std::min<int64_t>((warps + 7) / 8, device_sms() * 16);
     k_quant_rows_bf16<<<blocks, 256, 0, st>>>(a.x, T, a.H, a.xq, a.xs);
     note_launch();
   }
@@ -625,7 +636,7 @@ cudaError_t launch_quant_rows(const uint16_t* src, int rows, int C, uint8_t* q, 
   if (rows == 0) return cudaSuccess;
   int groups = (C + 255) / 256;
   int64_t warps = (int64_t)rows * groups;
-  int blocks = (int)std::min<int64_t>((warps + 7) / 8, 152 * 16);
+  int blocks = (int)std::min<int64_t>((warps + 7) / 8, device_sms() * 16);
   k_quant_rows_bf16<<<blocks, 256, 0, st>>>(src, rows, C, q, s);
   note_launch();
   return cudaGetLastError();

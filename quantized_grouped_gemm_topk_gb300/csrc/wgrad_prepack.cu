@@ -150,7 +150,7 @@ cudaError_t launch_prepack_rowexp(const uint8_t* s, int G, int N, int K, int int
                                   cudaStream_t st) {
   const int64_t total = (int64_t)G * tiles * kTileN;
   if (total == 0) return cudaSuccess;
-  int blocks = (int)std::min<int64_t>((total + 255) / 256, 152 * 32);
+  int blocks = (int)std::min<int64_t>((total + 255) / 256, device_sms() * 32);
   k_prepack_rowexp<<<blocks, 256, 0, st>>>(s, G, N, K, interleave_I, tiles, dst);
   note_launch();
   return cudaGetLastError();
@@ -160,7 +160,7 @@ cudaError_t launch_prepack(const uint8_t* q, const uint8_t* s, int G, int N, int
                            int tiles, int64_t tile_bytes, uint8_t* dst, cudaStream_t st) {
   const int64_t total = (int64_t)G * tiles * (K / kChunkK) * kTileN;
   if (total == 0) return cudaSuccess;
-  int blocks = (int)std::min<int64_t>((total + 255) / 256, 152 * 32);
+  int blocks = (int)std::min<int64_t>((total + 255) / 256, device_sms() * 32);
   k_prepack<<<blocks, 256, 0, st>>>(q, s, G, N, K, fmt, interleave_I, tiles, tile_bytes, dst);
   note_launch();
   return cudaGetLastError();

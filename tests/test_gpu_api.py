@@ -13,21 +13,52 @@ from util import assert_close_layer, cuda_device, np_
 pytestmark = pytest.mark.gpu
 
 
-def _alloc_dispatch(s, T, dev):
+GUARD = 64   # guard elements on each side of a guarded buffer (>= 64 bytes)
+
+
+def _guarded(n, dtype, dev, fill):
+    """A buffer of n elements with GUARD canary elements on both sides;
+    returns (whole, inner view). The inner view stays 64-byte aligned."""
+    whole = torch.full((n + 2 * GUARD,), fill, dtype=dtype, device=dev)
+    return whole, whole[GUARD:GUARD + n]
+
+
+def _guards_intact(whole, n, fill):
+    return bool((whole[:GUARD] == fill).all()) and bool((whole[GUARD + n:] == fill).all())
+
+
+def _alloc_dispatch(s, T, dev, guard=False):
+    """Caller-owned dispatch buffers; with guard=True each one sits between
+    canary bands (t["_guards"] lists (whole, n, fill) to check afterwards)."""
     R = T * s.kp
     G = s.groups
-    t = {
-        "topk_ids": torch.empty(T, s.k, dtype=torch.int32, device=dev),
-        "topk_w": torch.empty(T, s.k, dtype=torch.float32, device=dev),
-        "counts": torch.empty(G, dtype=torch.int32, device=dev),
-        "offsets": torch.empty(G + 1 + 3, dtype=torch.int32, device=dev),
-        "perm_src": torch.empty(R, dtype=torch.int32, device=dev),
-        "inv": torch.empty(R, dtype=torch.int32, device=dev),
-        "w_row": torch.empty(R, dtype=torch.float32, device=dev),
-        "xq": torch.empty(T, s.H, dtype=torch.uint8, device=dev),
-        "xs": torch.empty(T, s.H // 32, dtype=torch.uint8, device=dev),
+    spec = {
+        "topk_ids": ((T, s.k), torch.int32, 0x5a5a5a5a),
+        "topk_w": ((T, s.k), torch.float32, -123.25),
+        "counts": ((G,), torch.int32, 0x3c3c3c3c),
+        "offsets": ((G + 1 + 3,), torch.int32, 0x3c3c3c3c),
+        "perm_src": ((R,), torch.int32, 0x7e7e7e7e),
+        "inv": ((R,), torch.int32, 0x7e7e7e7e),
+        "w_row": ((R,), torch.float32, -77.5),
+        "xq": ((T, s.H), torch.uint8, 0xA5),
+        "xs": ((T, s.H // 32), torch.uint8, 0xA5),
     }
+    t, guards = {}, []
+    for name, (shape, dtype, fill) in spec.items():
+        n = int(np.prod(shape))
+        if guard:
+            whole, inner = _guarded(n, dtype, dev, fill)
+            t[name] = inner.view(shape)
+            guards.append((name, whole, n, fill))
+        else:
+            t[name] = torch.empty(shape, dtype=dtype, device=dev)
+    t["_guards"] = guards
     return t, m.dispatch_struct(t)
+
+
+def _check_guards(t):
+    for name, whole, n, fill in t["_guards"]:
+        assert _guards_intact(whole, n, fill), f"write outside {name}"
 
 
 @pytest.mark.parametrize("name,S", [("tiny", 0), ("tiny", 1)])
@@ -113,27 +144,69 @@ def test_cuda_graph_replay_matches_eager():
 
 
 def test_bad_expert_ids_flag_status():
+    """Out-of-range expert ids set MOE_DEV_BAD_EXPERT_ID, their slots are
+    skipped (inv = -1), nothing is written past the valid rows, and every
+    output buffer's canary bands are untouched."""
     dev = cuda_device()
     s = inputs.workload("tiny")
     T = 8
     cfg = m.config_from_shape(s, T_max=T)
     ws = torch.zeros(m.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
     x = inputs.gen_x(s, 0, device=dev, T=T)
-    t, d = _alloc_dispatch(s, T, dev)
+    t, d = _alloc_dispatch(s, T, dev, guard=True)
     t["topk_ids"].copy_(torch.tensor([[0, 1]] * T, dtype=torch.int32))
     t["topk_ids"][3, 1] = s.E + 5            # out of range
     t["topk_ids"][5, 0] = -1
     t["topk_w"].fill_(0.5)
     t["perm_src"].fill_(-7)
+    t["w_row"].fill_(-9.0)
     m.moe_dispatch(cfg, x, T, d, ws)
     st = m.moe_read_status(cfg, ws)
     assert st & m.MOE_DEV_BAD_EXPERT_ID
     counts = np_(t["counts"])
-    assert counts.sum() == T * s.k - 2                     # the bad slots are skipped
+    n = T * s.k - 2
+    assert counts.sum() == n                               # the bad slots are skipped
     inv = np_(t["inv"])
     assert inv[3 * s.k + 1] == -1 and inv[5 * s.k + 0] == -1
-    assert (np_(t["perm_src"])[: counts.sum()] >= 0).all()
+    perm = np_(t["perm_src"])
+    assert (perm[:n] >= 0).all() and (perm[n:] == -7).all()  # rows past the valid ones untouched
+    assert (np_(t["w_row"])[n:] == -9.0).all()
+    _check_guards(t)
     assert m.moe_read_status(cfg, ws) == 0                 # reading clears it
+
+
+def test_empty_experts_write_nothing_outside_their_rows():
+    """Zipf-skewed routing with many empty experts, run step by step into
+    caller buffers between canary bands: the dispatch, W1 (y1), W2 (z) and
+    combine outputs touch no byte outside their valid rows, and equal the
+    layer forward's."""
+    dev = cuda_device()
+    s = inputs.workload("tiny", E=32, k=4, logits="zipf")
+    T = 48
+    r = run_forward(s, T, dev=dev, seed=2)
+    cfg, ws = r["cfg"], r["ws"]
+    counts_ref = np_(r["views"]["counts"])
+    assert (counts_ref == 0).sum() >= 9
+    t, d = _alloc_dispatch(s, T, dev, guard=True)
+    m.moe_route_dispatch(cfg, r["logits_in"], r["x"], T, d, ws)
+    R = T * s.kp
+    y1q_w, y1q = _guarded(R * s.I, torch.uint8, dev, 0xC3)
+    y1s_w, y1s = _guarded(R * s.I // 32, torch.uint8, dev, 0xC3)
+    z_w, z = _guarded(R * s.H, torch.int16, dev, 0x1357)
+    out_w, out = _guarded(T * s.H, torch.int16, dev, 0x2468)
+    y1q, y1s = y1q.view(R, s.I), y1s.view(R, s.I // 32)
+    m.moe_grouped_gemm_w1_swiglu_quant(cfg, d, T, r["packed"], y1q, y1s, None, ws)
+    m.moe_grouped_gemm_w2(cfg, d, T, y1q, y1s, r["packed"], z.view(R, s.H), ws)
+    m.moe_combine(cfg, z.view(R, s.H), t["inv"], None, T, out.view(T, s.H))
+    torch.cuda.synchronize()
+    assert m.moe_read_status(cfg, ws) == 0
+    _check_guards(t)
+    assert _guards_intact(y1q_w, R * s.I, 0xC3) and _guards_intact(y1s_w, R * s.I // 32, 0xC3)
+    assert _guards_intact(z_w, R * s.H, 0x1357) and _guards_intact(out_w, T * s.H, 0x2468)
+    assert torch.equal(t["counts"], r["views"]["counts"])
+    assert torch.equal(y1q, r["views"]["y1_q"]) and torch.equal(y1s, r["views"]["y1_s"])
+    assert torch.equal(z.view(R, s.H), r["views"]["z"])
+    assert torch.equal(out.view(T, s.H), r["out"].view(torch.int16))
 
 
 def test_nan_logit_flags_status():

@@ -84,31 +84,32 @@ def test_empty_experts_and_skew():
     assert_close_layer(np_(r["out"].float()), f.out, "out")
 
 
-@pytest.mark.parametrize("T", [1, 8, 32, 128])
-def test_dsv3_decode(T):
-    """DeepSeek-V3-shaped decode at full size; dispatch checked in full, the
-    expert path on sampled tokens."""
-    dev = cuda_device()
-    s = inputs.workload("dsv3", T=T)
-    r = run_forward(s, T, dev=dev)
-    assert r["status"] == 0
-    toks = list(range(T)) if T <= 2 else [0, T - 1]
-    kp = s.kp
-    inv = np_(r["views"]["inv"])
-    rows = [int(inv[t * kp + j]) for t in toks for j in range(kp)]
-    f = oracle_forward(s, r, rows=rows)
-    _check_dispatch(s, r, f)
-    v = r["views"]
-    assert_mx_close(np_(v["y1_q"])[rows], np_(v["y1_s"])[rows], f.y1q[rows], f.y1s[rows], "y1")
-    assert_close_layer(np_(r["out"].float())[toks], f.out[toks], "out")
+def _sample_tokens(r, s, T, n=16):
+    """n tokens spread over the batch, plus the tokens whose rows sit at
+    positions 16, 64, 128 and last inside the most loaded expert group (so
+    the sample reaches interior and trailing token tiles of the grouped
+    GEMMs, whatever tile height they run with)."""
+    if T <= n:
+        return list(range(T))
+    toks = set(int(t) for t in np.linspace(0, T - 1, n - 4).round())
+    counts = np_(r["views"]["counts"])
+    offs = np_(r["views"]["offsets"])
+    perm = np_(r["views"]["perm_src"])
+    e = int(np.argmax(counts))
+    for pos in (16, 64, 128, int(counts[e]) - 1):
+        if 0 <= pos < counts[e]:
+            toks.add(int(perm[offs[e] + pos]) // s.kp)
+    return sorted(toks)
 
 
-def _full_size_sampled(s, T, seed, toks):
+def _full_size_sampled(s, T, seed, toks=None):
     """Dispatch checked in full; the expert path (y1, out) on the rows of the
-    sampled tokens `toks`."""
+    sampled tokens (default: _sample_tokens)."""
     dev = cuda_device()
     r = run_forward(s, T, dev=dev, seed=seed)
     assert r["status"] == 0
+    if toks is None:
+        toks = _sample_tokens(r, s, T)
     kp = s.kp
     inv = np_(r["views"]["inv"])
     rows = [int(inv[t * kp + j]) for t in toks for j in range(kp)]
@@ -120,20 +121,55 @@ def _full_size_sampled(s, T, seed, toks):
     return r
 
 
+@pytest.mark.parametrize("T", [1, 8, 32, 128])
+def test_dsv3_decode(T):
+    """DeepSeek-V3-shaped decode at full size; dispatch checked in full, the
+    expert path on up to 16 sampled tokens (all of them for T <= 16)."""
+    s = inputs.workload("dsv3", T=T)
+    _full_size_sampled(s, T, 0)
+
+
 @pytest.mark.parametrize("T", [1, 16, 64])
 def test_shared_expert_decode(T):
     """Decode with one always-on shared expert at full size (H=6144, I=1536,
     E=160 + 1 shared, top-8, routed weights x2.5)."""
     s = inputs.workload("shared", T=T)
-    _full_size_sampled(s, T, 0, list(range(T)) if T <= 2 else [0, T - 1])
+    _full_size_sampled(s, T, 0)
 
 
 def test_skewed_routing_full_size():
     """Zipf-skewed routing at full size (T=4096, H=4096, I=1536, E=128,
     top-8): 30% of the experts receive no rows, the rest are load-imbalanced;
-    multi-block dispatch and 64-token GEMM tiles."""
+    multi-block dispatch and 64-token GEMM tiles. The sample includes rows in
+    the second and third 64-row tiles of the hottest expert."""
     s = inputs.workload("skewed")
-    r = _full_size_sampled(s, s.T, 3, [0, s.T // 2, s.T - 1])
+    r = _full_size_sampled(s, s.T, 3)
     counts = np_(r["views"]["counts"])
     assert (counts == 0).sum() >= int(0.3 * s.E)
     assert counts.sum() == s.T * s.k
+    assert counts.max() > 192
+
+
+@pytest.mark.parametrize("T,E,k", [(64, 33, 8), (40, 8, 2)])
+def test_route_topk_exact_ties(T, E, k):
+    """Integer-valued logits force many exact ties; moe_route_topk must pick
+    the same ids as the oracle's rule (larger logit first, the lower expert id
+    on a tie) and the same weights."""
+    dev = cuda_device()
+    import quantized_grouped_gemm_topk_gb300 as m
+    s = inputs.workload("tiny", E=E, k=k)
+    cfg = m.config_from_shape(s, T_max=T)
+    ws = torch.zeros(m.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(17)
+    logits = torch.randint(-3, 4, (T, E), generator=g).to(torch.float32)
+    logits[0] = 1.0                      # a token whose logits all tie
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    m.moe_route_topk(cfg, logits.to(dev), T, ids, w, ws)
+    torch.cuda.synchronize()
+    ref_ids, ref_w = M.topk_route(logits.numpy().astype(np.float64), k, 1.0)
+    assert (np_(ids) == ref_ids).all()
+    assert list(np_(ids)[0]) == list(range(k))
+    np.testing.assert_allclose(np_(w), ref_w, rtol=1e-6, atol=0)
+    assert m.moe_read_status(cfg, ws) == 0
