@@ -202,6 +202,16 @@ moe_status_t moe_train_sizes(const moe_config_t* cfg, int T, int64_t* r_pad_max)
 moe_status_t moe_prepack_weights(const moe_config_t* cfg, const moe_weights_view_t* src, int which,
                                  void* dst, size_t dst_bytes, void* stream);
 
+/* Debug export of the packed layout (tests): writes matrix `mat` (1 = W1 or
+ * its dgrad copy, 2 = W2 or its dgrad copy) of every group of the blob
+ * `packed` (device, from moe_prepack_weights with the same cfg and `which`)
+ * back to the plain layout of moe_weights_view_t: NVFP4 q [G, N, K/2],
+ * s [G, N, K/16]; MXFP8 q [G, N, K], s [G, N, K/32] (device, caller-owned).
+ * Prepacking followed by this export returns the source bytes exactly.
+ * Not on the hot path; enqueued on stream like the compute calls. */
+moe_status_t moe_debug_unpack_weights(const moe_config_t* cfg, const void* packed, int which, int mat,
+                                      uint8_t* q, uint8_t* s, void* stream);
+
 /* ---- forward steps ------------------------------------------------------ */
 
 /* S1. logits [T, E] fp32 (device) = x [T, H] bf16 (device) . W_r [H, E] fp32

@@ -21,6 +21,8 @@ STATUS_NAMES = {0: "ok", 1: "invalid argument", 2: "unsupported", 3: "workspace 
                 4: "CUDA error", 5: "device status error"}
 MOE_DEV_BAD_EXPERT_ID = 0x1
 MOE_DEV_NAN_LOGIT = 0x2
+MOE_DEV_BAD_PACK = 0x4
+MOE_DEV_TIMEOUT = 0x8
 MOE_ACT_SWIGLU, MOE_ACT_SWIGLU_CLAMP = 0, 1
 MOE_WFMT_NVFP4, MOE_WFMT_MXFP8 = 0, 1
 MOE_PACK_FORWARD, MOE_PACK_DGRAD = 0, 1
@@ -31,7 +33,7 @@ EXPORTS = (
     "moe_train_sizes", "moe_prepack_weights", "moe_router_logits", "moe_route_dispatch", "moe_route_topk",
     "moe_dispatch", "moe_grouped_gemm_w1_swiglu_quant", "moe_grouped_gemm_w2", "moe_combine",
     "moe_layer_forward", "moe_layer_backward", "moe_read_status", "moe_clear_status", "moe_status_string",
-    "moe_last_launch_count", "moe_set_phase_events", "moe_router_logits_noalloc",
+    "moe_last_launch_count", "moe_set_phase_events", "moe_router_logits_noalloc", "moe_debug_unpack_weights",
 )
 MOE_N_PHASE_EVENTS = 6
 
@@ -107,6 +109,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "moe_last_launch_count": [],
         "moe_set_phase_events": [ctypes.POINTER(ctypes.c_void_p)],
         "moe_router_logits_noalloc": [cfgp, P, P, ctypes.c_int, P, P],
+        "moe_debug_unpack_weights": [cfgp, P, ctypes.c_int, ctypes.c_int, P, P, P],
     }
     for name, args in sig.items():
         f = getattr(lib, name)
@@ -218,6 +221,12 @@ def moe_prepack_weights(cfg, wts: dict, which=MOE_PACK_FORWARD, dst=None, stream
     _check("moe_prepack_weights", load().moe_prepack_weights(ctypes.byref(cfg), ctypes.byref(view), which,
                                                              _ptr(dst), dst.numel(), _stream(stream)))
     return dst
+
+
+def moe_debug_unpack_weights(cfg, packed, which, mat, q, s, stream=None):
+    """Plain-layout copy of matrix `mat` (1 or 2) of a packed blob (tests)."""
+    _check("moe_debug_unpack_weights", load().moe_debug_unpack_weights(ctypes.byref(cfg), _ptr(packed), which, mat,
+                                                                       _ptr(q), _ptr(s), _stream(stream)))
 
 
 def moe_router_logits(cfg, x, W_r, T, logits, ws, stream=None):

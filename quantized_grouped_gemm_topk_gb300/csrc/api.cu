@@ -50,17 +50,26 @@ static bool backward_capable(const moe_config_t& c) {
   return c.weight_fmt == MOE_WFMT_MXFP8 && c.n_shared == 0;
 }
 
+// MXFP8 weights run on the block-scaled tensor-core GEMM (gemm_mx.cu); NVFP4
+// weights on the decoding GEMM (gemm_tc.cu).
+static bool mx_path(const moe_config_t& c) { return c.weight_fmt == MOE_WFMT_MXFP8; }
+
+static int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
 // ---- workspace layout -------------------------------------------------------
 struct WsLayout {
   size_t status, logits, rpart, ids, wts, counts, offsets, touched, ntouch, poff, hist, base;
-  size_t perm, inv, wrow, xq, xs, y1q, y1s, z, P, a16, y16, rexp1, rexp2;
-  size_t ysave, dzq, dzs, dztq, dzts, dwrow, dhq, dhs, dh, dhtq, dhts;
+  size_t perm, inv, wrow, xq, xs, y1q, y1s, z;
+  size_t P, a16, y16, rexp1, rexp2;                       // NVFP4 path
+  size_t xg, xgs;                                         // MXFP8 path: gathered x rows
+  size_t dzq, dzs, dzg, dzgs, dztq, dzts, dhq, dhs, dhtq, dhts, dxp, dwpart;   // backward
   size_t total;
 };
 
 static WsLayout ws_layout(const moe_config_t& c) {
   const Dims d = dims_of(c);
   WsLayout L;
+  std::memset(&L, 0, sizeof(L));
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + std::max<size_t>(bytes, 1), 256); return at; };
   const int64_t T = d.Tmax, R = d.Rmax;
@@ -86,25 +95,29 @@ static WsLayout ws_layout(const moe_config_t& c) {
   L.y1q = take((size_t)R * d.I);
   L.y1s = take((size_t)R * d.I / 32);
   L.z = take((size_t)R * d.H * 2);
-  L.P = take((size_t)R * std::max(2 * d.I, d.H) * 4);
-  L.a16 = take((size_t)R * std::max(2 * d.I, d.H) * 2);
-  L.y16 = take((size_t)R * d.I * 2);
-  L.rexp1 = take((size_t)R * 4);
-  L.rexp2 = take((size_t)R * 4);
+  if (!mx_path(c)) {
+    L.P = take((size_t)R * std::max(2 * d.I, d.H) * 4);
+    L.a16 = take((size_t)R * std::max(2 * d.I, d.H) * 2);
+    L.y16 = take((size_t)R * d.I * 2);
+    L.rexp1 = take((size_t)R * 4);
+    L.rexp2 = take((size_t)R * 4);
+  } else {
+    L.xg = take((size_t)R * d.H);
+    L.xgs = take((size_t)R * d.H / 32);
+  }
   if (backward_capable(c)) {
-    L.ysave = take((size_t)R * d.I * 4);
     L.dzq = take((size_t)T * d.H);
     L.dzs = take((size_t)T * d.H / 32);
+    L.dzg = take((size_t)R * d.H);
+    L.dzgs = take((size_t)R * d.H / 32);
     L.dztq = take((size_t)d.H * d.RpMax);
     L.dzts = take((size_t)d.H * d.RpMax / 32);
-    L.dwrow = take((size_t)R * 4);
     L.dhq = take((size_t)R * 2 * d.I);
     L.dhs = take((size_t)R * 2 * d.I / 32);
-    L.dh = take((size_t)R * 2 * d.I * 4);
     L.dhtq = take((size_t)2 * d.I * d.RpMax);
     L.dhts = take((size_t)2 * d.I * d.RpMax / 32);
-  } else {
-    L.ysave = L.dzq = L.dzs = L.dztq = L.dzts = L.dwrow = L.dhq = L.dhs = L.dh = L.dhtq = L.dhts = 0;
+    L.dxp = take((size_t)R * d.H * 2);
+    L.dwpart = take((size_t)ceil_div(d.I, kMxTileN) * R * 4);
   }
   L.total = o;
   return L;
@@ -117,13 +130,19 @@ static Tp* at(void* ws, size_t off) { return reinterpret_cast<Tp*>(reinterpret_c
 struct PackLayout {
   int fmt, G;
   int N1, K1, N2, K2, il1;
+  // NVFP4: 128-row tiles of 64-wide K chunks
   int tiles1, tiles2;
   int64_t tile_bytes1, tile_bytes2;
-  size_t off_gs1, off_gs2, off_w1, off_w2, off_rx1, off_rx2, total;
+  size_t off_gs1, off_gs2;
+  // MXFP8: plain rows
+  int rows1, rows2;
+  size_t off_s1, off_s2;
+  size_t off_w1, off_w2, total;
 };
 
 static PackLayout pack_layout(const moe_config_t& c, int which) {
   PackLayout P;
+  std::memset(&P, 0, sizeof(P));
   P.fmt = c.weight_fmt;
   P.G = c.E + c.n_shared;
   if (which == MOE_PACK_FORWARD) {
@@ -133,28 +152,30 @@ static PackLayout pack_layout(const moe_config_t& c, int which) {
     P.N1 = c.H; P.K1 = 2 * c.I; P.il1 = 0;
     P.N2 = c.I; P.K2 = c.H;
   }
-  const int CB = chunk_bytes(P.fmt);
-  P.tiles1 = (P.N1 + kTileN - 1) / kTileN;
-  P.tiles2 = (P.N2 + kTileN - 1) / kTileN;
-  P.tile_bytes1 = (int64_t)(P.K1 / kChunkK) * CB;
-  P.tile_bytes2 = (int64_t)(P.K2 / kChunkK) * CB;
   size_t o = 256;
-  P.off_gs1 = o; o = align_up(o + (size_t)P.G * 4, 256);
-  P.off_gs2 = o; o = align_up(o + (size_t)P.G * 4, 256);
-  P.off_w1 = o; o = align_up(o + (size_t)P.G * P.tiles1 * P.tile_bytes1, 256);
-  P.off_w2 = o; o = align_up(o + (size_t)P.G * P.tiles2 * P.tile_bytes2, 256);
-  P.off_rx1 = o; o = align_up(o + (size_t)P.G * P.tiles1 * kTileN, 256);
-  P.off_rx2 = o; o = align_up(o + (size_t)P.G * P.tiles2 * kTileN, 256);
+  if (P.fmt == MOE_WFMT_NVFP4) {
+    const int CB = chunk_bytes(P.fmt);
+    P.tiles1 = (P.N1 + kTileN - 1) / kTileN;
+    P.tiles2 = (P.N2 + kTileN - 1) / kTileN;
+    P.tile_bytes1 = (int64_t)(P.K1 / kChunkK) * CB;
+    P.tile_bytes2 = (int64_t)(P.K2 / kChunkK) * CB;
+    P.off_gs1 = o; o = align_up(o + (size_t)P.G * 4, 256);
+    P.off_gs2 = o; o = align_up(o + (size_t)P.G * 4, 256);
+    P.off_w1 = o; o = align_up(o + (size_t)P.G * P.tiles1 * P.tile_bytes1, 256);
+    P.off_w2 = o; o = align_up(o + (size_t)P.G * P.tiles2 * P.tile_bytes2, 256);
+  } else {
+    P.rows1 = P.il1 > 0 ? ceil_div(P.il1, kMxTileN / 2) * kMxTileN : P.N1;
+    P.rows2 = P.N2;
+    P.off_w1 = o; o = align_up(o + (size_t)P.G * P.rows1 * P.K1, 256);
+    P.off_s1 = o; o = align_up(o + (size_t)P.G * P.rows1 * (P.K1 / 32), 256);
+    P.off_w2 = o; o = align_up(o + (size_t)P.G * P.rows2 * P.K2, 256);
+    P.off_s2 = o; o = align_up(o + (size_t)P.G * P.rows2 * (P.K2 / 32), 256);
+  }
   P.total = o;
   return P;
 }
 
 __global__ void k_write_header(PackHeader h, uint8_t* dst) { *reinterpret_cast<PackHeader*>(dst) = h; }
-
-__global__ void k_fill_f32(float* p, int n, float v) {
-  int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < n) p[i] = v;
-}
 
 // out[i] = sum over ks of part[ks * n + i], added in ks order; 16 loads in
 // flight per thread.
@@ -273,28 +294,48 @@ moe_status_t moe_prepack_weights(const moe_config_t* c, const moe_weights_view_t
   PackHeader h;
   std::memset(&h, 0, sizeof(h));
   h.magic = kPackMagic; h.version = kPackVersion; h.fmt = P.fmt; h.which = which; h.G = P.G;
-  h.N1 = P.N1; h.K1 = P.K1; h.N2 = P.N2; h.K2 = P.K2; h.interleave1 = P.il1 > 0;
+  h.N1 = P.N1; h.K1 = P.K1; h.N2 = P.N2; h.K2 = P.K2; h.interleave1 = P.il1;
   h.off_gs1 = P.off_gs1; h.off_gs2 = P.off_gs2; h.off_w1 = P.off_w1; h.off_w2 = P.off_w2;
   h.tile_bytes1 = P.tile_bytes1; h.tile_bytes2 = P.tile_bytes2; h.tiles1 = P.tiles1; h.tiles2 = P.tiles2;
+  h.off_s1 = P.off_s1; h.off_s2 = P.off_s2; h.rows1 = P.rows1; h.rows2 = P.rows2;
   k_write_header<<<1, 1, 0, st>>>(h, d8);
   note_launch();
+  MOE_CHECK_CUDA(cudaGetLastError());
   if (c->weight_fmt == MOE_WFMT_NVFP4) {
     MOE_CHECK_CUDA(cudaMemcpyAsync(d8 + P.off_gs1, src->w1_gs, (size_t)P.G * 4, cudaMemcpyDeviceToDevice, st));
     MOE_CHECK_CUDA(cudaMemcpyAsync(d8 + P.off_gs2, src->w2_gs, (size_t)P.G * 4, cudaMemcpyDeviceToDevice, st));
+    MOE_CHECK_CUDA(launch_prepack_nv(src->w1_q, src->w1_s, P.G, P.N1, P.K1, P.il1, P.tiles1, P.tile_bytes1,
+                                     d8 + P.off_w1, st));
+    MOE_CHECK_CUDA(launch_prepack_nv(src->w2_q, src->w2_s, P.G, P.N2, P.K2, 0, P.tiles2, P.tile_bytes2,
+                                     d8 + P.off_w2, st));
   } else {
-    k_fill_f32<<<(P.G + 255) / 256, 256, 0, st>>>(reinterpret_cast<float*>(d8 + P.off_gs1), P.G, 1.0f);
-    k_fill_f32<<<(P.G + 255) / 256, 256, 0, st>>>(reinterpret_cast<float*>(d8 + P.off_gs2), P.G, 1.0f);
-    note_launch(); note_launch();
+    MOE_CHECK_CUDA(launch_prepack_mx(src->w1_q, src->w1_s, P.G, P.N1, P.K1, P.il1, P.rows1, d8 + P.off_w1,
+                                     d8 + P.off_s1, st));
+    MOE_CHECK_CUDA(launch_prepack_mx(src->w2_q, src->w2_s, P.G, P.N2, P.K2, 0, P.rows2, d8 + P.off_w2,
+                                     d8 + P.off_s2, st));
   }
-  MOE_CHECK_CUDA(launch_prepack(src->w1_q, src->w1_s, P.G, P.N1, P.K1, P.fmt, P.il1, P.tiles1, P.tile_bytes1,
-                                d8 + P.off_w1, st));
-  MOE_CHECK_CUDA(launch_prepack(src->w2_q, src->w2_s, P.G, P.N2, P.K2, P.fmt, 0, P.tiles2, P.tile_bytes2,
-                                d8 + P.off_w2, st));
-  if (c->weight_fmt == MOE_WFMT_MXFP8) {
-    MOE_CHECK_CUDA(launch_prepack_rowexp(src->w1_s, P.G, P.N1, P.K1, P.il1, P.tiles1,
-                                         reinterpret_cast<int8_t*>(d8 + P.off_rx1), st));
-    MOE_CHECK_CUDA(launch_prepack_rowexp(src->w2_s, P.G, P.N2, P.K2, 0, P.tiles2,
-                                         reinterpret_cast<int8_t*>(d8 + P.off_rx2), st));
+  return MOE_OK;
+}
+
+moe_status_t moe_debug_unpack_weights(const moe_config_t* c, const void* packed, int which, int mat, uint8_t* q,
+                                      uint8_t* sc, void* stream) {
+  moe_status_t s = moe_config_validate(c);
+  if (s != MOE_OK) return s;
+  if ((which != MOE_PACK_FORWARD && which != MOE_PACK_DGRAD) || (mat != 1 && mat != 2)) return MOE_ERR_INVALID_ARG;
+  if (which == MOE_PACK_DGRAD && c->weight_fmt != MOE_WFMT_MXFP8) return MOE_ERR_UNSUPPORTED;
+  REQ(packed); REQ(q); REQ(sc);
+  const PackLayout P = pack_layout(*c, which);
+  cudaStream_t st = (cudaStream_t)stream;
+  reset_launch_count();
+  const uint8_t* b = reinterpret_cast<const uint8_t*>(packed);
+  const int N = mat == 1 ? P.N1 : P.N2, K = mat == 1 ? P.K1 : P.K2, il = mat == 1 ? P.il1 : 0;
+  if (c->weight_fmt == MOE_WFMT_NVFP4) {
+    MOE_CHECK_CUDA(launch_unpack_nv(b + (mat == 1 ? P.off_w1 : P.off_w2), P.G, N, K, il,
+                                    mat == 1 ? P.tiles1 : P.tiles2, mat == 1 ? P.tile_bytes1 : P.tile_bytes2, q, sc,
+                                    st));
+  } else {
+    MOE_CHECK_CUDA(launch_unpack_mx(b + (mat == 1 ? P.off_w1 : P.off_w2), b + (mat == 1 ? P.off_s1 : P.off_s2), P.G,
+                                    N, K, il, mat == 1 ? P.rows1 : P.rows2, q, sc, st));
   }
   return MOE_OK;
 }
@@ -420,18 +461,16 @@ static moe_status_t tc_gemm(const moe_config_t* c, const PackLayout& P, int mat,
                             const int32_t* rexp, cudaStream_t st, TcRun* run) {
   TcArgs g;
   const uint8_t* b = reinterpret_cast<const uint8_t*>(packed);
+  g.hdr = reinterpret_cast<const PackHeader*>(b);
+  g.which = MOE_PACK_FORWARD;
+  g.G = P.G;
   if (mat == 1) {
     g.w = b + P.off_w1; g.gs = reinterpret_cast<const float*>(b + P.off_gs1);
-    g.wrowexp = reinterpret_cast<const int8_t*>(b + P.off_rx1);
     g.tile_bytes = P.tile_bytes1; g.tiles = P.tiles1; g.N = P.N1; g.K = P.K1; g.interleave_I = P.il1;
   } else {
     g.w = b + P.off_w2; g.gs = reinterpret_cast<const float*>(b + P.off_gs2);
-    g.wrowexp = reinterpret_cast<const int8_t*>(b + P.off_rx2);
     g.tile_bytes = P.tile_bytes2; g.tiles = P.tiles2; g.N = P.N2; g.K = P.K2; g.interleave_I = 0;
   }
-  if (P.fmt == MOE_WFMT_NVFP4) g.wrowexp = nullptr;
-  else g.gs = nullptr;
-  g.fmt = P.fmt;
   g.offsets = offsets;
   g.touched = at<int32_t>(ws, L.touched);
   g.n_touched = at<int32_t>(ws, L.ntouch);
@@ -453,6 +492,48 @@ static moe_status_t tc_gemm(const moe_config_t* c, const PackLayout& P, int mat,
   return MOE_OK;
 }
 
+static int mx_grid(const moe_config_t& c) {
+  int s = device_sms();
+  if (c.max_sms > 0) s = std::min(s, c.max_sms);
+  return s;
+}
+
+// Token-side block-scaled GEMM (modes kMxW1, kMxPlain, kMxDswiglu): A = the
+// MXFP8 rows aq/as [R][K] in group order, B = matrix `mat` of the packed
+// MXFP8 blob; g carries the epilogue fields.
+static moe_status_t mx_token_gemm(const moe_config_t* c, MxArgs& g, int mode, const uint8_t* aq, const uint8_t* as,
+                                  int64_t R, const void* packed, int which, int mat, const int32_t* offsets,
+                                  const int32_t* poff, int32_t* status, cudaStream_t st) {
+  const PackLayout P = pack_layout(*c, which);
+  const uint8_t* b = reinterpret_cast<const uint8_t*>(packed);
+  const int K = mat == 1 ? P.K1 : P.K2;
+  const int rows = mat == 1 ? P.rows1 : P.rows2;
+  g.mode = mode;
+  g.hdr = reinterpret_cast<const PackHeader*>(b);
+  g.which = which;
+  g.G = P.G;
+  g.K = K;
+  g.b_rows_per_group = rows;
+  g.offsets = offsets;
+  g.poff = poff;
+  g.a_sf = as; g.a_sf_ld = K / 32; g.a_rows = R;
+  g.b_sf = b + (mat == 1 ? P.off_s1 : P.off_s2); g.b_sf_ld = K / 32; g.b_rows = (int64_t)P.G * rows;
+  g.R = R;
+  g.status = status;
+  MxMaps maps;
+  if (!make_tmap_mx(&maps.a, aq, R, K, mx_tile_m()) ||
+      !make_tmap_mx(&maps.b, b + (mat == 1 ? P.off_w1 : P.off_w2), (int64_t)P.G * rows, K, mx_tile_n()))
+    return MOE_ERR_CUDA;
+  MOE_CHECK_CUDA(launch_gemm_mx(g, maps, mx_grid(*c), st));
+  return MOE_OK;
+}
+
+static MxArgs mx_args0() {
+  MxArgs g;
+  std::memset(&g, 0, sizeof(g));
+  return g;
+}
+
 static ActParams act_params(const moe_config_t* c) {
   ActParams p;
   p.act = c->act;
@@ -461,17 +542,46 @@ static ActParams act_params(const moe_config_t* c) {
   return p;
 }
 
+// W1 with its fused epilogue. NVFP4: f16 operand rows (unless a_ready),
+// decoding tensor-core GEMM, then the SwiGLU / routing weight / MXFP8
+// epilogue kernel. MXFP8: gathered MXFP8 rows (unless a_ready), then the
+// block-scaled GEMM whose epilogue writes y1 (and, with save, h and the
+// transposed copy of y).
 static moe_status_t w1_impl(const moe_config_t* c, const moe_dispatch_t* d, int T, const void* packed, uint8_t* y1q,
                             uint8_t* y1s, const moe_train_save_t* save, void* ws, cudaStream_t st,
-                            float* y_save_override, bool a16_ready = false) {
+                            bool a_ready = false) {
   const WsLayout L = ws_layout(*c);
   const PackLayout P = pack_layout(*c, MOE_PACK_FORWARD);
   const int kp = c->k + c->n_shared, G = c->E + c->n_shared;
   const int R = T * kp;
   if (T == 0) return MOE_OK;
+  int32_t* status = at<int32_t>(ws, L.status);
+  if (mx_path(*c)) {
+    uint8_t* xg = at<uint8_t>(ws, L.xg);
+    uint8_t* xgs = at<uint8_t>(ws, L.xgs);
+    if (!a_ready) MOE_CHECK_CUDA(launch_gather_mx(d->xq, d->xs, c->H, d->perm_src, kp, R, d->offsets, G, xg, xgs, st));
+    MxArgs g = mx_args0();
+    g.n_tiles = P.rows1 / kMxTileN;
+    g.I = c->I;
+    g.w_row = d->w_row;
+    g.act = act_params(c);
+    g.yq = y1q; g.ys = y1s;
+    if (save) {
+      g.hsave = save->h; g.tq = save->y1t_q; g.ts = save->y1t_s; g.t_ld = r_pad_for(dims_of(*c), T);
+    }
+    moe_status_t s = mx_token_gemm(c, g, kMxW1, xg, xgs, R, packed, MOE_PACK_FORWARD, 1, d->offsets,
+                                   at<int32_t>(ws, L.poff), status, st);
+    if (s != MOE_OK) return s;
+    phase(2, st);
+    phase(3, st);
+    if (save)
+      MOE_CHECK_CUDA(cudaMemcpyAsync(save->poff, at<int32_t>(ws, L.poff), (size_t)(G + 1) * 4,
+                                     cudaMemcpyDeviceToDevice, st));
+    return MOE_OK;
+  }
   uint16_t* a16 = at<uint16_t>(ws, L.a16);
   int32_t* rexp1 = at<int32_t>(ws, L.rexp1);
-  if (!a16_ready)
+  if (!a_ready)
     MOE_CHECK_CUDA(launch_act_f16(d->xq, d->xs, c->H, d->perm_src, kp, R, d->offsets, G, a16, rexp1, st));
   TcRun run;
   moe_status_t s = tc_gemm(c, P, 1, packed, ws, L, d->offsets, T, a16, rexp1, st, &run);
@@ -481,23 +591,24 @@ static moe_status_t w1_impl(const moe_config_t* c, const moe_dispatch_t* d, int 
   f.P = run.out; f.S = run.S; f.split_stride = run.split_stride; f.R = R; f.I = c->I;
   f.offsets = d->offsets; f.G = G; f.w_row = d->w_row; f.act = act_params(c);
   f.y1q = y1q; f.y1s = y1s;
-  f.h_save = save ? save->h : nullptr;
-  f.y_save = save ? (y_save_override ? y_save_override : at<float>(ws, L.ysave)) : nullptr;
   f.y16 = at<uint16_t>(ws, L.y16);
   f.y_rowexp = at<int32_t>(ws, L.rexp2);
   MOE_CHECK_CUDA(launch_w1_finalize(f, st));
   phase(3, st);
-  if (save) {
-    const Dims dm = dims_of(*c);
-    ColQuantArgs q;
-    q.src16 = nullptr; q.row_map = nullptr; q.row_div = 1; q.src32 = f.y_save;
-    q.C = c->I; q.offsets = d->offsets; q.poff = at<int32_t>(ws, L.poff); q.G = G;
-    q.r_pad_max = r_pad_for(dm, T); q.q = save->y1t_q; q.s = save->y1t_s;
-    MOE_CHECK_CUDA(launch_quant_cols(q, st));
-    MOE_CHECK_CUDA(cudaMemcpyAsync(save->poff, at<int32_t>(ws, L.poff), (size_t)(G + 1) * 4,
-                                   cudaMemcpyDeviceToDevice, st));
-  }
   return MOE_OK;
+}
+
+// W2 on the MXFP8 path: z [R][H] bf16 straight from the block-scaled GEMM.
+static moe_status_t w2_mx(const moe_config_t* c, const int32_t* offsets, int T, const uint8_t* y1q,
+                          const uint8_t* y1s, const void* packed, uint16_t* z, void* ws, cudaStream_t st) {
+  const WsLayout L = ws_layout(*c);
+  const int64_t R = (int64_t)T * (c->k + c->n_shared);
+  MxArgs g = mx_args0();
+  g.n_tiles = ceil_div(c->H, kMxTileN);
+  g.N = c->H;
+  g.out = z; g.out_ld = c->H;
+  return mx_token_gemm(c, g, kMxPlain, y1q, y1s, R, packed, MOE_PACK_FORWARD, 2, offsets, at<int32_t>(ws, L.poff),
+                       at<int32_t>(ws, L.status), st);
 }
 
 static moe_status_t check_save(const moe_config_t* c, const moe_train_save_t* save) {
@@ -516,7 +627,7 @@ moe_status_t moe_grouped_gemm_w1_swiglu_quant(const moe_config_t* c, const moe_d
   REQ(packed_w); REQ_T(y1_q); REQ_T(y1_s); REQ(ws);
   if ((s = check_save(c, save)) != MOE_OK) return s;
   reset_launch_count();
-  return w1_impl(c, d, T, packed_w, y1_q, y1_s, save, ws, (cudaStream_t)stream, nullptr);
+  return w1_impl(c, d, T, packed_w, y1_q, y1_s, save, ws, (cudaStream_t)stream);
 }
 
 moe_status_t moe_grouped_gemm_w2(const moe_config_t* c, const moe_dispatch_t* d, int T, const uint8_t* y1_q,
@@ -528,6 +639,7 @@ moe_status_t moe_grouped_gemm_w2(const moe_config_t* c, const moe_dispatch_t* d,
   reset_launch_count();
   if (T == 0) return MOE_OK;
   cudaStream_t st = (cudaStream_t)stream;
+  if (mx_path(*c)) return w2_mx(c, d->offsets, T, y1_q, y1_s, packed_w, z, ws, st);
   const WsLayout L = ws_layout(*c);
   const PackLayout P = pack_layout(*c, MOE_PACK_FORWARD);
   const int R = T * (c->k + c->n_shared);
@@ -592,9 +704,15 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
     a.part = logits_in; a.KS = 1;
   }
   MOE_CHECK_CUDA(launch_route_dispatch(a, st));
-  if (T > 0)   // gather the quantised rows into the GEMM's f16 operand (part of dispatch)
-    MOE_CHECK_CUDA(launch_act_f16(v.d.xq, v.d.xs, c->H, v.d.perm_src, kp, T * kp, v.d.offsets, G,
-                                  at<uint16_t>(ws, L.a16), at<int32_t>(ws, L.rexp1), st));
+  if (T > 0) {
+    // gather the quantised rows into the W1 GEMM's operand (part of dispatch)
+    if (mx_path(*c))
+      MOE_CHECK_CUDA(launch_gather_mx(v.d.xq, v.d.xs, c->H, v.d.perm_src, kp, T * kp, v.d.offsets, G,
+                                      at<uint8_t>(ws, L.xg), at<uint8_t>(ws, L.xgs), st));
+    else
+      MOE_CHECK_CUDA(launch_act_f16(v.d.xq, v.d.xs, c->H, v.d.perm_src, kp, T * kp, v.d.offsets, G,
+                                    at<uint16_t>(ws, L.a16), at<int32_t>(ws, L.rexp1), st));
+  }
   phase(1, st);
   if (T == 0) {
     for (int i = 2; i < MOE_N_PHASE_EVENTS; ++i) phase(i, st);
@@ -603,12 +721,19 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
   if (save) {
     // transposed MXFP8 copy of the gathered activations for the W1 wgrad
     ColQuantArgs q;
-    q.src16 = x; q.row_map = v.d.perm_src; q.row_div = kp; q.src32 = nullptr;
+    q.src16 = x; q.row_map = v.d.perm_src; q.row_div = kp;
     q.C = c->H; q.offsets = v.d.offsets; q.poff = at<int32_t>(ws, L.poff); q.G = G;
     q.r_pad_max = r_pad_for(dims_of(*c), T); q.q = save->at_q; q.s = save->at_s;
     MOE_CHECK_CUDA(launch_quant_cols(q, st));
   }
-  if ((s = w1_impl(c, &v.d, T, packed_w, v.y1_q, v.y1_s, save, ws, st, nullptr, true)) != MOE_OK) return s;
+  if ((s = w1_impl(c, &v.d, T, packed_w, v.y1_q, v.y1_s, save, ws, st, true)) != MOE_OK) return s;
+  if (mx_path(*c)) {
+    if ((s = w2_mx(c, v.d.offsets, T, v.y1_q, v.y1_s, packed_w, v.z, ws, st)) != MOE_OK) return s;
+    phase(4, st);
+    MOE_CHECK_CUDA(launch_combine(v.z, v.d.inv, nullptr, T, c->k, kp, c->H, out, st));
+    phase(5, st);
+    return MOE_OK;
+  }
   const PackLayout P = pack_layout(*c, MOE_PACK_FORWARD);
   TcRun run;
   s = tc_gemm(c, P, 2, packed_w, ws, L, v.d.offsets, T, at<uint16_t>(ws, L.y16), at<int32_t>(ws, L.rexp2), st,
@@ -617,6 +742,30 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
   phase(4, st);
   MOE_CHECK_CUDA(launch_finalize_combine(run.out, run.S, run.split_stride, c->H, v.d.inv, T, kp, v.z, out, st));
   phase(5, st);
+  return MOE_OK;
+}
+
+// Weight gradient of one matrix on the block-scaled GEMM: out[e][m][n] =
+// sum over group e's padded token rows p of P[m][p] * Q[n][p] (both MXFP8
+// along p).
+static moe_status_t mx_wgrad(const moe_config_t* c, const uint8_t* pq, const uint8_t* ps, int M, const uint8_t* qq,
+                             const uint8_t* qs, int N, int64_t Rp, const int32_t* poff, uint16_t* out,
+                             int32_t* status, cudaStream_t st) {
+  MxArgs g = mx_args0();
+  g.mode = kMxWgrad;
+  g.hdr = nullptr;
+  g.G = c->E;
+  g.M = M; g.m_tiles = ceil_div(M, mx_tile_m());
+  g.N = N; g.n_tiles = ceil_div(N, mx_tile_n());
+  g.poff = poff;
+  g.a_sf = ps; g.a_sf_ld = Rp / 32; g.a_rows = M;
+  g.b_sf = qs; g.b_sf_ld = Rp / 32; g.b_rows = N;
+  g.out = out; g.out_ld = N;
+  g.status = status;
+  MxMaps maps;
+  if (!make_tmap_mx(&maps.a, pq, M, Rp, mx_tile_m()) || !make_tmap_mx(&maps.b, qq, N, Rp, mx_tile_n()))
+    return MOE_ERR_CUDA;
+  MOE_CHECK_CUDA(launch_gemm_mx(g, maps, mx_grid(*c), st));
   return MOE_OK;
 }
 
@@ -638,61 +787,60 @@ moe_status_t moe_layer_backward(const moe_config_t* c, const uint16_t* dout, con
   const int kp = dm.kp, G = dm.G, I = c->I, H = c->H;
   const int R = T * kp;
   const int64_t Rp = r_pad_for(dm, T);
-  const PackLayout P = pack_layout(*c, MOE_PACK_DGRAD);
+  int32_t* status = at<int32_t>(ws, L.status);
   uint8_t* dzq = at<uint8_t>(ws, L.dzq);
   uint8_t* dzs = at<uint8_t>(ws, L.dzs);
+  uint8_t* dzg = at<uint8_t>(ws, L.dzg);
+  uint8_t* dzgs = at<uint8_t>(ws, L.dzgs);
   uint8_t* dztq = at<uint8_t>(ws, L.dztq);
   uint8_t* dzts = at<uint8_t>(ws, L.dzts);
-  float* dwrow = at<float>(ws, L.dwrow);
   uint8_t* dhq = at<uint8_t>(ws, L.dhq);
   uint8_t* dhs = at<uint8_t>(ws, L.dhs);
-  float* dh = at<float>(ws, L.dh);
   uint8_t* dhtq = at<uint8_t>(ws, L.dhtq);
   uint8_t* dhts = at<uint8_t>(ws, L.dhts);
+  uint16_t* dxp = at<uint16_t>(ws, L.dxp);
+  float* dwpart = at<float>(ws, L.dwpart);
   const int32_t* poff = at<int32_t>(ws, L.poff);
-  // 1. dz rows: MXFP8 per token along H (rows gathered by the GEMM), and the
-  //    transposed copy along the padded row axis.
-  MOE_CHECK_CUDA(launch_quant_rows(dout, T, H, dzq, dzs, st));
-  ColQuantArgs q;
-  q.src16 = dout; q.row_map = v.d.perm_src; q.row_div = kp; q.src32 = nullptr;
-  q.C = H; q.offsets = v.d.offsets; q.poff = poff; q.G = G; q.r_pad_max = Rp; q.q = dztq; q.s = dzts;
-  MOE_CHECK_CUDA(launch_quant_cols(q, st));
-  // 2. dY1 = dz . W2^T (dgrad copy of W2: rows i < I, K = H)
-  uint16_t* a16 = at<uint16_t>(ws, L.a16);
-  int32_t* rexp1 = at<int32_t>(ws, L.rexp1);
-  MOE_CHECK_CUDA(launch_act_f16(dzq, dzs, H, v.d.perm_src, kp, R, v.d.offsets, G, a16, rexp1, st));
-  TcRun g;
-  s = tc_gemm(c, P, 2, packed_w_dgrad, ws, L, v.d.offsets, T, a16, rexp1, st, &g);
-  if (s != MOE_OK) return s;
-  // 3. dSwiGLU epilogue
-  DswigluArgs ds;
-  ds.P = g.out; ds.S = g.S; ds.split_stride = g.split_stride; ds.R = R; ds.I = I;
-  ds.offsets = v.d.offsets; ds.G = G; ds.h = save->h; ds.w_row = v.d.w_row; ds.act = act_params(c);
-  ds.dw_row = dwrow; ds.dhq = dhq; ds.dhs = dhs; ds.dh = dh;
-  MOE_CHECK_CUDA(launch_dswiglu(ds, st));
-  ColQuantArgs qh;
-  qh.src16 = nullptr; qh.row_map = nullptr; qh.row_div = 1; qh.src32 = dh;
-  qh.C = 2 * I; qh.offsets = v.d.offsets; qh.poff = poff; qh.G = G; qh.r_pad_max = Rp; qh.q = dhtq; qh.s = dhts;
-  MOE_CHECK_CUDA(launch_quant_cols(qh, st));
-  // 4. dXp = dh . W1^T (dgrad copy of W1: rows h < H, K = 2I), then the
-  //    slot-ordered combine backward into dx.
-  MOE_CHECK_CUDA(launch_act_f16(dhq, dhs, 2 * I, nullptr, 1, R, v.d.offsets, G, a16, rexp1, st));
-  TcRun g2;
-  s = tc_gemm(c, P, 1, packed_w_dgrad, ws, L, v.d.offsets, T, a16, rexp1, st, &g2);
-  if (s != MOE_OK) return s;
-  MOE_CHECK_CUDA(launch_finalize_combine(g2.out, g2.S, g2.split_stride, H, v.d.inv, T, kp, nullptr, dx, st));
-  // 5. wgrads over each group's padded rows
-  WgradArgs w1;
-  w1.pq = save->at_q; w1.ps = save->at_s; w1.qq = dhtq; w1.qs = dhts; w1.Rp = Rp;
-  w1.M = H; w1.N = 2 * I; w1.G = c->E; w1.poff = poff; w1.out = dW1;
-  MOE_CHECK_CUDA(launch_wgrad(w1, st));
-  WgradArgs w2;
-  w2.pq = save->y1t_q; w2.ps = save->y1t_s; w2.qq = dztq; w2.qs = dzts; w2.Rp = Rp;
-  w2.M = I; w2.N = H; w2.G = c->E; w2.poff = poff; w2.out = dW2;
-  MOE_CHECK_CUDA(launch_wgrad(w2, st));
-  // 6. router
-  MOE_CHECK_CUDA(launch_router_bwd(v.d.topk_w, v.d.topk_ids, dwrow, v.d.inv, T, c->E, c->k, kp, c->routed_scale,
-                                   dlogits, st));
+  const int nparts = ceil_div(I, mx_tile_n());
+  if (T > 0) {
+    // 1. dz rows: MXFP8 per token along H, gathered into group order, and the
+    //    transposed copy along the padded row axis (W2 wgrad operand)
+    MOE_CHECK_CUDA(launch_quant_rows(dout, T, H, dzq, dzs, st));
+    ColQuantArgs q;
+    q.src16 = dout; q.row_map = v.d.perm_src; q.row_div = kp;
+    q.C = H; q.offsets = v.d.offsets; q.poff = poff; q.G = G; q.r_pad_max = Rp; q.q = dztq; q.s = dzts;
+    MOE_CHECK_CUDA(launch_quant_cols(q, st));
+    MOE_CHECK_CUDA(launch_gather_mx(dzq, dzs, H, v.d.perm_src, kp, R, v.d.offsets, G, dzg, dzgs, st));
+    // 2. dY1 = dz . W2^T with the fused dSwiGLU + MXFP8 / transposed-copy
+    //    epilogue and the routing-weight gradient partials
+    MxArgs g = mx_args0();
+    g.n_tiles = nparts;
+    g.I = I;
+    g.w_row = v.d.w_row;
+    g.act = act_params(c);
+    g.hsave = save->h;
+    g.yq = dhq; g.ys = dhs;
+    g.tq = dhtq; g.ts = dhts; g.t_ld = Rp;
+    g.dwpart = dwpart;
+    if ((s = mx_token_gemm(c, g, kMxDswiglu, dzg, dzgs, R, packed_w_dgrad, MOE_PACK_DGRAD, 2, v.d.offsets, poff,
+                           status, st)) != MOE_OK)
+      return s;
+    // 3. dXp = dh . W1^T (bf16 rows), then the slot-ordered combine backward
+    MxArgs g2 = mx_args0();
+    g2.n_tiles = ceil_div(H, mx_tile_n());
+    g2.N = H;
+    g2.out = dxp; g2.out_ld = H;
+    if ((s = mx_token_gemm(c, g2, kMxPlain, dhq, dhs, R, packed_w_dgrad, MOE_PACK_DGRAD, 1, v.d.offsets, poff, status,
+                           st)) != MOE_OK)
+      return s;
+    MOE_CHECK_CUDA(launch_combine(dxp, v.d.inv, nullptr, T, c->k, kp, H, dx, st));
+  }
+  // 4. wgrads over each group's padded rows (groups without rows: zeros)
+  if ((s = mx_wgrad(c, save->at_q, save->at_s, H, dhtq, dhts, 2 * I, Rp, poff, dW1, status, st)) != MOE_OK) return s;
+  if ((s = mx_wgrad(c, save->y1t_q, save->y1t_s, I, dztq, dzts, H, Rp, poff, dW2, status, st)) != MOE_OK) return s;
+  // 5. router
+  MOE_CHECK_CUDA(launch_router_bwd(v.d.topk_w, v.d.topk_ids, dwpart, nparts, R, v.d.inv, T, c->E, c->k, kp,
+                                   c->routed_scale, dlogits, st));
   return MOE_OK;
 }
 

@@ -14,32 +14,51 @@ constexpr int kWarp = 32;
 constexpr unsigned kFull = 0xffffffffu;
 
 // ---- packed weight blob ---------------------------------------------------
-// Tiles of 128 output features; each tile is a run of 64-wide K chunks.
-// NVFP4 chunk: [granule g < 2][row p < 128][16 B of 32 E2M1 codes] (4096 B)
-//              then [row p][4 E4M3 scale codes, one per 16 K] (512 B).
-// MXFP8 chunk: [granule g < 4][row p < 128][16 B of 16 E4M3 codes] (8192 B)
-//              then [row p][2 E8M0 scale codes, one per 32 K] (256 B).
+// NVFP4: tiles of 128 output features; each tile is a run of 64-wide K
+// chunks.
+//   chunk: [granule g < 2][row p < 128][16 B of 32 E2M1 codes] (4096 B)
+//          then [row p][4 E4M3 scale codes, one per 16 K] (512 B).
+// MXFP8: plain K-major rows, codes [G][rows][K] and scales [G][rows][K/32];
+//   W1's forward rows come in tiles of 192: 96 gate features then the same
+//   96 up features (zero rows past I), every other matrix in its own row
+//   order.
 constexpr int kTileN = 128;
 constexpr int kChunkK = 64;
+constexpr int kMxTileN = 192;
 constexpr uint32_t kPackMagic = 0x4d4f4557u;  // 'MOEW'
-constexpr int kPackVersion = 1;
+constexpr int kPackVersion = 2;
 
 __host__ __device__ inline int chunk_bytes(int fmt) {
   return fmt == MOE_WFMT_NVFP4 ? (4096 + 512) : (8192 + 256);
 }
-__host__ __device__ inline int chunk_data_bytes(int fmt) {
-  return fmt == MOE_WFMT_NVFP4 ? 4096 : 8192;
+
+// MXFP8 packed row p of a matrix -> its logical row (-1: zero padding row).
+// il > 0: W1 forward (I = il), tiles of 96 gate + 96 up features.
+__host__ __device__ inline int mx_pack_src_row(int p, int N, int il) {
+  if (il <= 0) return p < N ? p : -1;
+  const int j = p / kMxTileN, pp = p % kMxTileN, h = kMxTileN / 2;
+  const int f = j * h + (pp < h ? pp : pp - h);
+  if (f >= il) return -1;
+  return pp < h ? f : il + f;
 }
 
 struct PackHeader {            // first 256 bytes of a packed blob
   uint32_t magic;
   int32_t version, fmt, which, G;
   int32_t N1, K1, N2, K2;      // logical rows / K of the two matrices
-  int32_t interleave1;         // 1: W1 tiles hold 64 gate + 64 up features (I = N1/2)
+  int32_t interleave1;         // W1 gate/up interleave (I), 0 for none
   int64_t off_gs1, off_gs2, off_w1, off_w2;   // byte offsets from the blob start
-  int64_t tile_bytes1, tile_bytes2;           // bytes of one 128-row tile
-  int32_t tiles1, tiles2;                     // tiles per group
+  int64_t tile_bytes1, tile_bytes2;           // NVFP4: bytes of one 128-row tile
+  int32_t tiles1, tiles2;                     // NVFP4: tiles per group
+  int64_t off_s1, off_s2;                     // MXFP8: scale arrays
+  int32_t rows1, rows2;                       // MXFP8: packed rows per group
 };
+static_assert(sizeof(PackHeader) <= 256, "pack header fits its 256 bytes");
+
+// True when the blob's header describes the packing a GEMM expects.
+__device__ __forceinline__ bool pack_header_ok(const PackHeader* h, int fmt, int which, int G) {
+  return h->magic == kPackMagic && h->version == kPackVersion && h->fmt == fmt && h->which == which && h->G == G;
+}
 
 // ---- conversions ------------------------------------------------------------
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t b) {

@@ -6,10 +6,9 @@
 //  * W2 epilogue fused with the combine: z = bf16(W2 output), out[t] = sum
 //    of the token's k' rows in slot order (GC-MoE summary, Approach: W2
 //    emits BF16 fragments that role3 combines).
-//  * transposed MXFP8 copies (same blog, MXFP8 quantisation with a
-//    transposed copy for the backward).
-//  * backward epilogue: dSwiGLU + routing-weight gradient + MXFP8 (same
-//    blog: GroupGemm + dActivation + Quantize/Transpose).
+//  * transposed MXFP8 copies of gathered bf16 rows (same blog, MXFP8
+//    quantisation with a transposed copy for the backward).
+//  * the router backward.
 #include "internal.cuh"
 
 namespace moe {
@@ -19,7 +18,7 @@ static int grid_for(int64_t warps, int warps_per_block) {
   return (int)std::max<int64_t>(1, std::min<int64_t>(b, device_sms() * 32));
 }
 
-// ---- W1 epilogue --------------------------------------------------------------
+// ---- W1 epilogue (NVFP4 path) --------------------------------------------------
 // One CTA per row r: a warp per 32-block of I sums the K-slice partials,
 // forms y = w_row * act(g, u) and quantises the block to MXFP8 (y1q, y1s).
 // The CTA then writes the W2 GEMM's f16 operand row:
@@ -60,11 +59,6 @@ __global__ void __launch_bounds__(1024) k_w1_finalize_rows(const W1FinArgs a) {
       ss[b] = (uint8_t)(e + 127);
     }
     mx = max(mx, e + 127);
-    if (a.h_save) {
-      a.h_save[r * 2 * a.I + i] = f32_to_bf16_bits(g);
-      a.h_save[r * 2 * a.I + a.I + i] = f32_to_bf16_bits(u);
-    }
-    if (a.y_save) a.y_save[r * a.I + i] = y;
   }
   if (lane == 0) wmax[warp] = mx;
   __syncthreads();
@@ -241,8 +235,7 @@ __global__ void __launch_bounds__(256) k_quant_cols(const ColQuantArgs a) {
       float x = 0.f;
       if (cok && p0 + i < cnt) {
         const int64_t r = a.offsets[e] + p0 + i;
-        if (a.src16) x = bf16_bits_to_f32(a.src16[(int64_t)(a.row_map[r] / a.row_div) * a.C + c]);
-        else x = a.src32[r * a.C + c];
+        x = bf16_bits_to_f32(a.src16[(int64_t)(a.row_map[r] / a.row_div) * a.C + c]);
       }
       v[i] = x;
       am = fmaxf(am, fabsf(x));
@@ -270,50 +263,11 @@ cudaError_t launch_quant_cols(const ColQuantArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// ---- backward epilogue: dSwiGLU + routing-weight gradient + MXFP8 -------------
-__global__ void __launch_bounds__(256) k_dswiglu(const DswigluArgs a) {
-  const int lane = threadIdx.x & 31;
-  const int Rv = min(a.R, a.offsets[a.G]);
-  const int nb = a.I / 32;
-  const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); r < Rv; r += nw) {
-    const float wr = a.w_row[r];
-    float dw = 0.f;
-    for (int b = 0; b < nb; ++b) {
-      const int i = b * 32 + lane;
-      float dy = 0.f;
-      for (int s = 0; s < a.S; ++s) dy += a.P[(int64_t)s * a.split_stride + r * a.I + i];
-      const float g = bf16_bits_to_f32(a.h[r * 2 * a.I + i]);
-      const float u = bf16_bits_to_f32(a.h[r * 2 * a.I + a.I + i]);
-      dw = fmaf(dy, act_fwd(g, u, a.act), dw);
-      const float2 d = act_bwd(g, u, wr * dy, a.act);
-      a.dh[r * 2 * a.I + i] = d.x;
-      a.dh[r * 2 * a.I + a.I + i] = d.y;
-      const int eg = mx_exponent(warp_max(fabsf(d.x)));
-      const int eu = mx_exponent(warp_max(fabsf(d.y)));
-      a.dhq[r * 2 * a.I + i] = (uint8_t)(f32x2_to_e4m3x2(d.x * pow2_neg(eg), 0.f) & 0xffu);
-      a.dhq[r * 2 * a.I + a.I + i] = (uint8_t)(f32x2_to_e4m3x2(d.y * pow2_neg(eu), 0.f) & 0xffu);
-      if (lane == 0) {
-        a.dhs[r * (2 * nb) + b] = (uint8_t)(eg + 127);
-        a.dhs[r * (2 * nb) + nb + b] = (uint8_t)(eu + 127);
-      }
-    }
-    dw = warp_sum(dw);
-    if (lane == 0) a.dw_row[r] = dw;
-  }
-}
-
-cudaError_t launch_dswiglu(const DswigluArgs& a, cudaStream_t st) {
-  if (a.R == 0) return cudaSuccess;
-  k_dswiglu<<<grid_for(a.R, 8), 256, 0, st>>>(a);
-  note_launch();
-  return cudaGetLastError();
-}
-
 // ---- router backward: softmax-over-selected Jacobian ---------------------------
 __global__ void __launch_bounds__(256) k_router_bwd(const float* __restrict__ topk_w, const int32_t* __restrict__ ids,
-                                                    const float* __restrict__ dw_row, const int32_t* __restrict__ inv,
-                                                    int T, int E, int k, int kp, float rs, float* dlogits) {
+                                                    const float* __restrict__ dwpart, int nparts, int64_t R,
+                                                    const int32_t* __restrict__ inv, int T, int E, int k, int kp,
+                                                    float rs, float* dlogits) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -322,7 +276,11 @@ __global__ void __launch_bounds__(256) k_router_bwd(const float* __restrict__ to
   if (lane < k) {
     p = topk_w[(int64_t)t * k + lane] / rs;
     const int r = inv[(int64_t)t * kp + lane];
-    dp = r >= 0 ? rs * dw_row[r] : 0.f;
+    if (r >= 0) {
+      float dw = 0.f;
+      for (int i = 0; i < nparts; ++i) dw += dwpart[(int64_t)i * R + r];
+      dp = rs * dw;
+    }
   }
   float sdot = 0.f;
   for (int j = 0; j < k; ++j) sdot += __shfl_sync(kFull, p * dp, j);
@@ -333,10 +291,11 @@ __global__ void __launch_bounds__(256) k_router_bwd(const float* __restrict__ to
   }
 }
 
-cudaError_t launch_router_bwd(const float* topk_w, const int32_t* ids, const float* dw_row, const int32_t* inv,
-                              int T, int E, int k, int kp, float rs, float* dlogits, cudaStream_t st) {
+cudaError_t launch_router_bwd(const float* topk_w, const int32_t* ids, const float* dwpart, int nparts, int64_t R,
+                              const int32_t* inv, int T, int E, int k, int kp, float rs, float* dlogits,
+                              cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  k_router_bwd<<<(T + 7) / 8, 256, 0, st>>>(topk_w, ids, dw_row, inv, T, E, k, kp, rs, dlogits);
+  k_router_bwd<<<(T + 7) / 8, 256, 0, st>>>(topk_w, ids, dwpart, nparts, R, inv, T, E, k, kp, rs, dlogits);
   note_launch();
   return cudaGetLastError();
 }

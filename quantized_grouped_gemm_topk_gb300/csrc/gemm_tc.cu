@@ -65,13 +65,13 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol0 = kTcNA * 64;
 constexpr int kSmemBudget = 212 * 1024;
 
-template <int FMT, int NT>
+template <int NT>
 struct TcCfg {
   // Each MMA issuer accumulates into its own NT-column tile; a D buffer
   // holds all of them and the epilogue adds them.
   static constexpr int P = NT <= 32 ? 4 : 2;                         // MMA issuers
   static constexpr int DStride = P * NT;                             // TMEM columns per D buffer
-  static constexpr int CB = FMT == MOE_WFMT_NVFP4 ? 4608 : 8448;     // chunk bytes
+  static constexpr int CB = 4608;                                    // NVFP4 chunk bytes
   // A stage is one pair of chunks, so every stage feeds exactly one decoder
   // group and one MMA issuer: weight slot s always belongs to group
   // s % kTcNG and activation slot s to issuer s % P, and each waiter sees
@@ -168,52 +168,26 @@ __device__ __forceinline__ void e2m1x8_f16x2(uint32_t w, uint32_t& o0, uint32_t&
       : "=r"(o0), "=r"(o1), "=r"(o2), "=r"(o3)
       : "r"(w));
 }
-// f16 bits of 2^d (0 below the subnormal range), duplicated into both halves.
-__device__ __forceinline__ uint32_t f16x2_pow2(int d) {
-  uint32_t h;
-  if (d >= -14) h = (uint32_t)(d + 15) << 10;
-  else if (d >= -24) h = 1u << (d + 24);
-  else h = 0;
-  return h | (h << 16);
-}
-
-// Decodes one 64-wide K chunk of packed weight row p into 32 f16x2 words
-// (element pairs in K order).
-template <int FMT>
-__device__ __forceinline__ void decode_chunk(const uint8_t* sa, int p, int rexp, uint32_t (&v)[32]) {
-  if (FMT == MOE_WFMT_NVFP4) {
-    const uint4 g0 = *reinterpret_cast<const uint4*>(sa + p * 16);
-    const uint4 g1 = *reinterpret_cast<const uint4*>(sa + 2048 + p * 16);
-    const uint32_t sc = *reinterpret_cast<const uint32_t*>(sa + 4096 + p * 4);
-    const uint32_t s01 = e4m3x2_f16x2(sc & 0xffffu), s23 = e4m3x2_f16x2(sc >> 16);
-    const uint32_t ss[4] = {(s01 & 0xffffu) * 0x10001u, (s01 >> 16) * 0x10001u, (s23 & 0xffffu) * 0x10001u,
-                            (s23 >> 16) * 0x10001u};
-    const uint32_t wd[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+// Decodes one 64-wide K chunk of packed NVFP4 weight row p into 32 f16x2
+// words (element pairs in K order): E2M1 value x E4M3 block scale, exact in
+// f16.
+__device__ __forceinline__ void decode_chunk(const uint8_t* sa, int p, uint32_t (&v)[32]) {
+  const uint4 g0 = *reinterpret_cast<const uint4*>(sa + p * 16);
+  const uint4 g1 = *reinterpret_cast<const uint4*>(sa + 2048 + p * 16);
+  const uint32_t sc = *reinterpret_cast<const uint32_t*>(sa + 4096 + p * 4);
+  const uint32_t s01 = e4m3x2_f16x2(sc & 0xffffu), s23 = e4m3x2_f16x2(sc >> 16);
+  const uint32_t ss[4] = {(s01 & 0xffffu) * 0x10001u, (s01 >> 16) * 0x10001u, (s23 & 0xffffu) * 0x10001u,
+                          (s23 >> 16) * 0x10001u};
+  const uint32_t wd[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      uint32_t o0, o1, o2, o3;
-      e2m1x8_f16x2(wd[i], o0, o1, o2, o3);
-      const uint32_t s = ss[i >> 1];
-      v[4 * i + 0] = hmul2_bits(o0, s);
-      v[4 * i + 1] = hmul2_bits(o1, s);
-      v[4 * i + 2] = hmul2_bits(o2, s);
-      v[4 * i + 3] = hmul2_bits(o3, s);
-    }
-  } else {
-    const uint32_t sc = *reinterpret_cast<const uint16_t*>(sa + 8192 + p * 2);
-    const uint32_t f0 = f16x2_pow2((int)(sc & 0xffu) - 127 - rexp);
-    const uint32_t f1 = f16x2_pow2((int)(sc >> 8) - 127 - rexp);
-#pragma unroll
-    for (int gi = 0; gi < 4; ++gi) {
-      const uint4 gr = *reinterpret_cast<const uint4*>(sa + gi * 2048 + p * 16);
-      const uint32_t wd[4] = {gr.x, gr.y, gr.z, gr.w};
-      const uint32_t f = gi < 2 ? f0 : f1;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[gi * 8 + 2 * i] = hmul2_bits(e4m3x2_f16x2(wd[i] & 0xffffu), f);
-        v[gi * 8 + 2 * i + 1] = hmul2_bits(e4m3x2_f16x2(wd[i] >> 16), f);
-      }
-    }
+  for (int i = 0; i < 8; ++i) {
+    uint32_t o0, o1, o2, o3;
+    e2m1x8_f16x2(wd[i], o0, o1, o2, o3);
+    const uint32_t s = ss[i >> 1];
+    v[4 * i + 0] = hmul2_bits(o0, s);
+    v[4 * i + 1] = hmul2_bits(o1, s);
+    v[4 * i + 2] = hmul2_bits(o2, s);
+    v[4 * i + 3] = hmul2_bits(o3, s);
   }
 }
 
@@ -230,10 +204,10 @@ __device__ __forceinline__ uint32_t first_own(uint32_t base, uint32_t r, uint32_
 // of tokens past nv, which the epilogue never reads.
 __device__ __forceinline__ int box_index(int nv) { return nv <= 8 ? 0 : nv <= 16 ? 1 : nv <= 32 ? 2 : 3; }
 
-template <int FMT, int NT>
+template <int NT>
 __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant__ TcArgs g,
                                                            const __grid_constant__ TcMaps maps) {
-  using C = TcCfg<FMT, NT>;
+  using C = TcCfg<NT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* wring = smem;
@@ -252,8 +226,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   __shared__ UnitTab tab;
+  __shared__ int bad_pack;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_enter();
+  if (threadIdx.x == 0) {
+    bad_pack = !pack_header_ok(g.hdr, MOE_WFMT_NVFP4, g.which, g.G);
+    if (bad_pack) set_status(g.status, MOE_DEV_BAD_PACK);
+  }
+  __syncthreads();
+  if (bad_pack) return;   // the blob is not the packing this GEMM reads: write nothing
   {
     const int nt = min(*g.n_touched, kUnitTab);
     for (int i = threadIdx.x; i < nt; i += blockDim.x) {
@@ -427,8 +408,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
     for (UnitIt it = ustep.first(); ok && it.ti < n_groups; ustep.next(it)) {
       TcUnit w;
       if (!tc_unit(g, tab, it, w)) continue;
-      int rexp = 0;
-      if (FMT == MOE_WFMT_MXFP8) rexp = g.wrowexp[((int64_t)w.e * g.tiles + w.j) * kTileN + p];
       const uint32_t npt = (uint32_t)(w.c1 - w.c0 + 1) >> 1;   // chunk pairs per token tile
       for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT, ait += npt) {
         for (uint32_t i = first_own(ait, grp, kTcNG); i < ait + npt; i += kTcNG) {
@@ -438,13 +417,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
           if (!tc::mbar_wait(&wfull[ws], (i / C::WS) & 1, abort)) { ok = false; break; }
           const uint8_t* sa = wring + ws * C::WSlot;
           uint32_t v[32];
-          decode_chunk<FMT>(sa, p, rexp, v);
+          decode_chunk(sa, p, v);
           const int a = i % kTcNA;
           if (!tc::mbar_wait(&afree[a], ((i / kTcNA) & 1) ^ 1, abort)) { ok = false; break; }
           tc::fence_after_sync();
           tc::tmem_st32(lane_base + a * 64, v);
           if (nc > 1) {
-            decode_chunk<FMT>(sa + C::CB, p, rexp, v);
+            decode_chunk(sa + C::CB, p, v);
             tc::tmem_st32(lane_base + a * 64 + 32, v);
           }
           // this warp has read its rows of the pair: release them
@@ -473,9 +452,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       if (g.interleave_I > 0) n = p < 64 ? 64 * w.j + p : g.interleave_I + 64 * w.j + (p - 64);
       else n = kTileN * w.j + p;
       const bool nvalid = n < g.N;
-      float rowf;
-      if (FMT == MOE_WFMT_NVFP4) rowf = g.gs ? g.gs[w.e] : 1.0f;
-      else rowf = ldexpf(1.0f, g.wrowexp[((int64_t)w.e * g.tiles + w.j) * kTileN + p]);
+      const float rowf = g.gs[w.e];
       float* outp = g.out + (int64_t)w.s * g.split_stride + n;
       for (int t0 = w.r0; t0 < w.r1; t0 += NT) {
         const int nt = min(NT, w.r1 - t0);
@@ -563,12 +540,12 @@ bool make_tmaps_b(TcMaps* maps, const void* base, int64_t rows, int64_t cols) {
   return true;
 }
 
-template <int FMT, int NT>
+template <int NT>
 static cudaError_t launch_tc_t(const TcArgs& g, const TcMaps& maps, int grid, cudaStream_t st) {
   static std::atomic<bool> done[kMaxDevices] = {};
-  cudaError_t e = set_smem_once((const void*)k_gemm_tc<FMT, NT>, TcCfg<FMT, NT>::SmemBytes, done);
+  cudaError_t e = set_smem_once((const void*)k_gemm_tc<NT>, TcCfg<NT>::SmemBytes, done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_gemm_tc<FMT, NT>, dim3(grid), dim3(kTcThreads), (size_t)TcCfg<FMT, NT>::SmemBytes, st, g, maps);
+  return launch_pdl(k_gemm_tc<NT>, dim3(grid), dim3(kTcThreads), (size_t)TcCfg<NT>::SmemBytes, st, g, maps);
 }
 
 int tc_token_tile(int T, int kp, int G) {
@@ -580,16 +557,9 @@ int tc_token_tile(int T, int kp, int G) {
 
 cudaError_t launch_gemm_tc(const TcArgs& g, const TcMaps& maps, int nt, cudaStream_t st) {
   const int grid = std::max(1, g.max_ctas);
-  cudaError_t e;
-  if (g.fmt == MOE_WFMT_NVFP4) {
-    e = nt <= 16 ? launch_tc_t<MOE_WFMT_NVFP4, 16>(g, maps, grid, st)
-        : nt <= 32 ? launch_tc_t<MOE_WFMT_NVFP4, 32>(g, maps, grid, st)
-                   : launch_tc_t<MOE_WFMT_NVFP4, 64>(g, maps, grid, st);
-  } else {
-    e = nt <= 16 ? launch_tc_t<MOE_WFMT_MXFP8, 16>(g, maps, grid, st)
-        : nt <= 32 ? launch_tc_t<MOE_WFMT_MXFP8, 32>(g, maps, grid, st)
-                   : launch_tc_t<MOE_WFMT_MXFP8, 64>(g, maps, grid, st);
-  }
+  const cudaError_t e = nt <= 16 ? launch_tc_t<16>(g, maps, grid, st)
+                        : nt <= 32 ? launch_tc_t<32>(g, maps, grid, st)
+                                   : launch_tc_t<64>(g, maps, grid, st);
   note_launch();
   return e;
 }
@@ -648,7 +618,7 @@ cudaError_t launch_act_f16(const uint8_t* q, const uint8_t* s, int C, const int3
                            const int32_t* offsets, int G, uint16_t* a16, int32_t* rowexp, cudaStream_t st) {
   if (R == 0) return cudaSuccess;
   const int64_t warps = (int64_t)R * ((C + 255) / 256);
-  const int blocks = (int)std::min<int64_t>((warps + 7) / 8, device_sms() * 16);
+  const int blocks = (int)std::min<int64_t>((warps + 7) / 8, (int64_t)device_sms() * 16);
   cudaError_t e = launch_pdl(k_act_f16, dim3(blocks), dim3(256), 0, st, q, s, C, row_map, row_div, R, offsets, G,
                              a16, rowexp);
   note_launch();

@@ -104,17 +104,19 @@ cudaError_t launch_topk_only(const float* logits, int T, int E, int k, float rs,
                              int32_t* status, cudaStream_t st);
 cudaError_t launch_quant_rows(const uint16_t* src, int rows, int C, uint8_t* q, uint8_t* s, cudaStream_t st);
 
-// ---- grouped GEMM on tcgen05 (gemm_tc.cu) -------------------------------------
-// Same result layout as GemmArgs: out[s][r][n] = rowf(n) * 2^act_rowexp[r] *
-// sum_k W_e[n][k] * a16[r][k], with rowf = gs[e] (NVFP4) or 2^wrowexp (MXFP8);
-// the f16 activation rows a16 [R][K] come in through a TMA descriptor.
+// ---- NVFP4 grouped GEMM on tcgen05 (gemm_tc.cu) ---------------------------------
+// out[s][r][n] = gs[e] * 2^act_rowexp[r] * sum_k W_e[n][k] * a16[r][k] over
+// K slice s; the f16 activation rows a16 [R][K] come in through a TMA
+// descriptor.
 struct TcArgs {
   const uint8_t* w;
-  const float* gs;            // [G] (NVFP4) or nullptr
-  const int8_t* wrowexp;      // [G][tiles][128] (MXFP8) or nullptr
+  const float* gs;            // [G]
+  const PackHeader* hdr;      // the packed blob's header (checked on entry)
+  int which;                  // MOE_PACK_FORWARD / MOE_PACK_DGRAD expected in hdr
+  int G;
   int64_t tile_bytes;
   int tiles;
-  int N, K, fmt;
+  int N, K;
   int interleave_I;
   const int32_t* offsets;
   const int32_t* touched;
@@ -143,7 +145,52 @@ cudaError_t launch_gemm_tc(const TcArgs& g, const TcMaps& maps, int nt, cudaStre
 cudaError_t launch_act_f16(const uint8_t* q, const uint8_t* s, int C, const int32_t* row_map, int row_div, int R,
                            const int32_t* offsets, int G, uint16_t* a16, int32_t* rowexp, cudaStream_t st);
 
-// W1 epilogue: sums the S partials, y = w_row * act(g, u), MXFP8 along I.
+// ---- block-scaled MXFP8 grouped GEMM (gemm_mx.cu) ----------------------------
+// D_e[m][n] = sum_k A[m][k] * B[n][k], both operands MXFP8 (E4M3 bytes,
+// K-major, one E8M0 scale byte per 32 K). Token-side modes (W1, Plain,
+// Dswiglu): group e's A rows are offsets[e] .. offsets[e+1] of the A buffer,
+// its B rows b_rows_per_group * e + n. Wgrad: A rows are the M gradient
+// rows, B rows the N gradient columns, and group e's K range is
+// poff[e] .. poff[e+1] (token axis, padded to 32 per group).
+enum { kMxW1 = 0, kMxPlain = 1, kMxDswiglu = 2, kMxWgrad = 3 };
+struct MxArgs {
+  int mode;
+  const PackHeader* hdr;        // token-side modes: the weight blob's header (checked on entry); Wgrad: nullptr
+  int which;                    // MOE_PACK_FORWARD / MOE_PACK_DGRAD expected in hdr
+  int G;
+  int K;                        // token-side modes: reduction length
+  int n_tiles;                  // 192-column tiles per group
+  int N;                        // valid output columns (W1: unused, see I)
+  int M, m_tiles;               // Wgrad: gradient rows and their 128-row tiles
+  int64_t b_rows_per_group;
+  const int32_t* offsets;       // [G + 1] token rows per group
+  const int32_t* poff;          // [G + 1] 32-padded token rows per group
+  const uint8_t* a_sf; int64_t a_sf_ld; int64_t a_rows;   // A scales [a_rows][a_sf_ld]
+  const uint8_t* b_sf; int64_t b_sf_ld; int64_t b_rows;   // B scales [b_rows][b_sf_ld]
+  int64_t R;                    // token rows (A rows of the token-side modes)
+  const float* w_row;           // [R] routing weight per row
+  ActParams act;
+  int I;
+  uint8_t* yq; uint8_t* ys;     // W1: y1 [R][I] (+[R][I/32]); Dswiglu: dh [R][2I] (+[R][2I/32])
+  uint16_t* hsave;              // W1: h bf16 [R][2I] out (nullable); Dswiglu: h in
+  uint8_t* tq; uint8_t* ts; int64_t t_ld;   // transposed MXFP8 copy [features][t_ld] (+ scales); W1: nullable
+  uint16_t* out; int64_t out_ld;            // Plain: [R][out_ld]; Wgrad: [G][M][out_ld]
+  float* dwpart;                // Dswiglu: [n_tiles][R]
+  int32_t* status;
+};
+struct MxMaps {
+  CUtensorMap a, b;             // boxes of 128 K-bytes x 128 (A) / 192 (B) rows
+};
+bool make_tmap_mx(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows);
+int mx_tile_n();
+int mx_tile_m();
+cudaError_t launch_gemm_mx(const MxArgs& g, const MxMaps& maps, int grid, cudaStream_t st);
+// dst rows r < min(R, offsets[G]) = MXFP8 rows src[row_map[r] / row_div].
+cudaError_t launch_gather_mx(const uint8_t* q, const uint8_t* s, int C, const int32_t* row_map, int row_div, int R,
+                             const int32_t* offsets, int G, uint8_t* dq, uint8_t* ds, cudaStream_t st);
+
+// W1 epilogue of the NVFP4 path: sums the S partials, y = w_row * act(g, u),
+// MXFP8 along I, and the f16 operand rows of W2.
 struct W1FinArgs {
   const float* P; int S; int64_t split_stride;
   int R; int I;
@@ -151,8 +198,6 @@ struct W1FinArgs {
   const float* w_row;
   ActParams act;
   uint8_t* y1q; uint8_t* y1s;
-  uint16_t* h_save;                   // nullable [R][2I] bf16
-  float* y_save;                      // nullable [R][I] fp32
   uint16_t* y16;                      // [R][I] f16 rows for the W2 B operand
   int32_t* y_rowexp;                  // [R] row exponent of y16
 };
@@ -172,10 +217,9 @@ cudaError_t launch_combine(const uint16_t* z, const int32_t* inv, const float* t
 // Transposed MXFP8 copy: for each group e and padded row p < pad(count_e),
 // dst[c][poff[e] + p] = MXFP8 along p (blocks of 32) of the value of row
 // offsets[e] + p (zero past count_e). Source rows: bf16 rows of src16 at
-// row_map[r] / row_div (gather), or fp32 rows src32[r].
+// row_map[r] / row_div.
 struct ColQuantArgs {
   const uint16_t* src16; const int32_t* row_map; int row_div;
-  const float* src32;
   int C;
   const int32_t* offsets; const int32_t* poff; int G;
   int64_t r_pad_max;                  // row length of dst
@@ -184,38 +228,20 @@ struct ColQuantArgs {
 cudaError_t launch_quant_cols(const ColQuantArgs& a, cudaStream_t st);
 
 // ---- backward pieces ----------------------------------------------------------
-struct DswigluArgs {
-  const float* P; int S; int64_t split_stride;   // dY1 partials [S][R][I]
-  int R, I;
-  const int32_t* offsets; int G;
-  const uint16_t* h;                  // saved bf16 [R][2I]
-  const float* w_row;
-  ActParams act;
-  float* dw_row;                      // [R]
-  uint8_t* dhq; uint8_t* dhs;         // [R][2I], [R][2I/32]
-  float* dh;                          // [R][2I] fp32 (for the transposed copy)
-};
-cudaError_t launch_dswiglu(const DswigluArgs& a, cudaStream_t st);
+// dlogits from the routing-weight gradients dw_row[r] = sum over p < nparts of
+// dwpart[p * R + r] (added in p order).
+cudaError_t launch_router_bwd(const float* topk_w, const int32_t* ids, const float* dwpart, int nparts, int64_t R,
+                              const int32_t* inv, int T, int E, int k, int kp, float rs, float* dlogits,
+                              cudaStream_t st);
 
-struct WgradArgs {
-  const uint8_t* pq; const uint8_t* ps;   // [M][Rp], [M][Rp/32]
-  const uint8_t* qq; const uint8_t* qs;   // [N][Rp], [N][Rp/32]
-  int64_t Rp;
-  int M, N, G;
-  const int32_t* poff;
-  uint16_t* out;                          // [G][M][N] bf16
-};
-cudaError_t launch_wgrad(const WgradArgs& a, cudaStream_t st);
-
-cudaError_t launch_router_bwd(const float* topk_w, const int32_t* ids, const float* dw_row, const int32_t* inv,
-                              int T, int E, int k, int kp, float rs, float* dlogits, cudaStream_t st);
-
-// ---- prepack ----------------------------------------------------------------
-cudaError_t launch_prepack(const uint8_t* q, const uint8_t* s, int G, int N, int K, int fmt, int interleave_I,
-                           int tiles, int64_t tile_bytes, uint8_t* dst, cudaStream_t st);
-// MXFP8: per packed row, the largest E8M0 scale exponent (unbiased) of the
-// logical row, int8 [G][tiles][128] (0 for padding rows).
-cudaError_t launch_prepack_rowexp(const uint8_t* s, int G, int N, int K, int interleave_I, int tiles, int8_t* dst,
-                                  cudaStream_t st);
+// ---- prepack (prepack.cu) ------------------------------------------------------
+cudaError_t launch_prepack_nv(const uint8_t* q, const uint8_t* s, int G, int N, int K, int interleave_I, int tiles,
+                              int64_t tile_bytes, uint8_t* dst, cudaStream_t st);
+cudaError_t launch_unpack_nv(const uint8_t* src, int G, int N, int K, int interleave_I, int tiles, int64_t tile_bytes,
+                             uint8_t* q, uint8_t* s, cudaStream_t st);
+cudaError_t launch_prepack_mx(const uint8_t* q, const uint8_t* s, int G, int N, int K, int interleave_I, int NR,
+                              uint8_t* dq, uint8_t* ds, cudaStream_t st);
+cudaError_t launch_unpack_mx(const uint8_t* dq, const uint8_t* ds, int G, int N, int K, int interleave_I, int NR,
+                             uint8_t* q, uint8_t* s, cudaStream_t st);
 
 }  // namespace moe

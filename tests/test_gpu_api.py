@@ -240,3 +240,46 @@ def test_launch_accounting_and_phases():
     assert 5 <= n <= 12
     ts = [ev[0].elapsed_time(e) for e in ev]
     assert all(b >= a for a, b in zip(ts, ts[1:]))
+
+
+@pytest.mark.parametrize("name,which", [("tiny", 0), ("train_small", 0), ("train_small", 1)])
+def test_packed_layout_round_trip(name, which):
+    """moe_prepack_weights followed by moe_debug_unpack_weights gives back the
+    source bytes of both matrices exactly (NVFP4 tiles with gate/up
+    interleave; MXFP8 rows with the 96 + 96 gate/up tiles, and the dgrad
+    copies)."""
+    dev = cuda_device()
+    if name == "tiny":
+        s = inputs.workload("tiny", n_shared=1)
+    else:
+        s = inputs.workload("train", T=8, E=3, H=320, I=128)
+    cfg = m.config_from_shape(s, T_max=8)
+    wts = inputs.gen_expert_weights(s, 0, device=dev)
+    packed = m.moe_prepack_weights(cfg, wts, which)
+    suffix = "" if which == m.MOE_PACK_FORWARD else "t"
+    for mat in (1, 2):
+        src_q, src_s = wts[f"w{mat}{suffix}_q"], wts[f"w{mat}{suffix}_s"]
+        q = torch.full_like(src_q, 0x5A)
+        sc = torch.full_like(src_s, 0x5A)
+        m.moe_debug_unpack_weights(cfg, packed, which, mat, q, sc)
+        torch.cuda.synchronize()
+        assert torch.equal(q, src_q), f"codes of matrix {mat}"
+        assert torch.equal(sc, src_s), f"scales of matrix {mat}"
+
+
+def test_wrong_pack_sets_status_and_writes_nothing():
+    """A blob packed for the dgrad copies handed to the forward sets
+    MOE_DEV_BAD_PACK; the GEMMs write nothing."""
+    dev = cuda_device()
+    s = inputs.workload("train", T=16, E=4, H=320, I=128)
+    r = run_forward(s, s.T, dev=dev)
+    cfg, ws = r["cfg"], r["ws"]
+    wrong = m.moe_prepack_weights(cfg, r["wts"], m.MOE_PACK_DGRAD)
+    out = torch.full_like(r["out"], 7.0)
+    v = r["views"]
+    v["y1_q"].fill_(0x33)
+    m.moe_layer_forward(cfg, r["x"], r["Wr"], None, s.T, wrong, out, None, ws)
+    torch.cuda.synchronize()
+    st = m.moe_read_status(cfg, ws)
+    assert st & m.MOE_DEV_BAD_PACK
+    assert (v["y1_q"] == 0x33).all()
