@@ -1,6 +1,6 @@
-"""Benchmark of the routed-MoE layer forward on GB300.
+"""Benchmark of the routed-MoE layer on GB300.
 
-Default workload: DeepSeek-V3-shaped decode (H=7168, I=2048, E=256, top-8,
+Headline workload: DeepSeek-V3-shaped decode (H=7168, I=2048, E=256, top-8,
 NVFP4 weights, MXFP8 activations). One step = one layer forward at each of
 T = 1, 8, 32 and 128 tokens, every layer on a fresh batch of synthetic tokens
 (so routing touches a different set of experts), with the L2 cache flushed
@@ -8,9 +8,21 @@ T = 1, 8, 32 and 128 tokens, every layer on a fresh batch of synthetic tokens
 Each layer call replays a CUDA graph holding one captured moe_layer_forward
 (the decode layer is launch-bound without one). The metric is microseconds
 per step (lower is better), the sum of the layers' device times; the per-T
-layer times are listed in ``config.per_T_us``. The ``e2e`` figure calls the
-C ABI directly (no graph) with the tokens copied in from pinned host memory
-and the output copied back inside each timed interval.
+layer times are listed in ``config.per_T_us``.
+
+``e2e`` is the same step measured on the host clock through the public C ABI
+(no graph): per layer, perf_counter around the copy of the tokens from
+pinned host memory, the moe_layer_forward call, the copy of the output back
+and a synchronize.
+
+``per_config`` adds the other workloads, each on its own inputs:
+  * shared_decode  H=6144, I=1536, E=160 + 1 shared expert, top-8, x2.5,
+                   T = 1, 16, 64 (graph-replayed layers, as the headline);
+  * skewed_prefill T=4096, H=4096, I=1536, E=128, top-8, Zipf(1.2) routing
+                   with 30% of the experts empty, NVFP4 weights;
+  * train          T=16384, H=I=2880, E=128, top-4, MXFP8 weights, clamped
+                   SwiGLU: forward and backward.
+with latency, tokens/s and the fraction of the HBM or tensor roofline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -22,13 +34,16 @@ from __future__ import annotations
 
 import os
 
-# the CPU oracle legs run single-threaded so their core count is exact
+# the CPU oracle legs run their numpy single-threaded; the all-cores column
+# uses one process per core instead
 for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
     os.environ.setdefault(_v, "1")
 
 import argparse
 import hashlib
 import json
+import multiprocessing as mp
+import platform
 import re
 import statistics
 import subprocess
@@ -46,6 +61,7 @@ import inputs  # noqa: E402
 METRIC = "MoE layer us/step (decode T=1-128)"
 UNIT = "us/step"
 DECODE_TS = (1, 8, 32, 128)
+SHARED_TS = (1, 16, 64)
 FLUSH_BYTES = 512 << 20
 
 
@@ -62,15 +78,31 @@ def w2_bytes_per_expert(s):
 
 
 def peaks():
+    """(HBM GB/s, bf16 TFLOP/s burst, bf16 TFLOP/s sustained, source)."""
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         d = json.load(open(p))
-        return float(d["hbm_gbs"]), "measured"
-    return 6800.0, "fallback"
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "measured")
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def host_cpu():
+    """Core count and CPU model of this host."""
+    model = platform.processor() or platform.machine()
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                model = ln.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return os.cpu_count() or 1, model
 
 
 def kernel_source_sha():
-    """Hash of the GEMM kernel's sources with comments and whitespace
+    """Hash of the decode GEMM kernel's sources with comments and whitespace
     removed, so a recorded ncu traffic figure stays tied to the code that was
     captured and a comment edit does not void it."""
     h = hashlib.sha256()
@@ -156,11 +188,12 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-# CPU oracle sample (the cpu_baseline field and the reference arm)
+# CPU oracle (the cpu_baseline field and the reference arm)
 # ---------------------------------------------------------------------------
-def oracle_expert_sample(s, x_bits, logits, wts_np, e):
-    """Time the oracle's forward of one token through one expert: decode W1/W2
-    (NVFP4 -> fp64), both GEMMs, SwiGLU, requantisation. Returns seconds."""
+def oracle_expert_pass(s, x_bits, logits, wts_np, e, slot):
+    """The oracle's forward of one token through one of its experts:
+    routing, MXFP8 of x, decode of W1/W2 (NVFP4 -> fp64), both GEMMs,
+    SwiGLU x routing weight, requantisation. Returns (z row, seconds)."""
     from oracle import formats as F
     from oracle import moe as M
     t0 = time.perf_counter()
@@ -169,57 +202,86 @@ def oracle_expert_sample(s, x_bits, logits, wts_np, e):
     a = F.mx_dequantize(xq, xs)
     W1 = M.expert_w1(wts_np, e, s.wfmt)
     h = a @ W1.T
-    y = w[0, 0] * M.act_fwd(h[:, :s.I], h[:, s.I:], s.act, s.alpha, s.limit)
+    y = w[0, slot] * M.act_fwd(h[:, :s.I], h[:, s.I:], s.act, s.alpha, s.limit)
     q, sc = F.mx_quantize(y)
     W2 = M.expert_w2(wts_np, e, s.wfmt)
     z = F.mx_dequantize(q, sc) @ W2.T
     assert np.isfinite(z).all()
-    return time.perf_counter() - t0
+    return z, time.perf_counter() - t0
 
 
-def cpu_sample_inputs(s, dev):
-    """One token of a T=1 batch, its fp32 logits, and its top expert's weights
-    on the host (drawn exactly as the GPU run draws that expert)."""
-    x = inputs.gen_x(s, 100, device=dev, T=1)
-    Wr = inputs.gen_router(s, 0, device=dev)
-    logits = (x.float() @ Wr).cpu().numpy().astype(np.float64)
-    e = int(np.argmax(logits[0]))
-    one = inputs.gen_one_expert(s, 0, e, device=dev)
-    wts = {}
-    for name, t in one.items():
-        t = t.cpu().numpy()
-        arr = np.zeros((e + 1,) + t.shape, t.dtype)
-        arr[e] = t
-        wts[name] = arr
-    return inputs.bf16_bits(x).cpu().numpy(), logits, wts, e
+def _expert_worker(args):
+    """Process-pool worker: one expert pass (weights arrive as numpy)."""
+    s, x_bits, logits, wts_np, e, slot = args
+    _, dt = oracle_expert_pass(s, x_bits, logits, wts_np, e, slot)
+    return dt
+
+
+def t1_layer_inputs(s):
+    """One token of a T=1 batch, its fp32 logits, its k experts and their
+    weights (drawn on the host exactly as the GPU run draws them)."""
+    x = inputs.gen_x(s, 100, device="cpu", T=1)
+    Wr = inputs.gen_router(s, 0, device="cpu")
+    logits = (x.float() @ Wr).numpy().astype(np.float64)
+    from oracle import moe as M
+    ids, _ = M.topk_route(logits, s.k, s.routed_scale)
+    experts = [int(e) for e in ids[0]]
+    per = []
+    for e in experts:
+        one = inputs.gen_one_expert(s, 0, e, device="cpu")
+        per.append({name: t.numpy()[None] if t.dim() == 0 else t.numpy()[None] for name, t in one.items()})
+    return inputs.bf16_bits(x).numpy(), logits, experts, per
+
+
+def oracle_t1_layer(s, pool_procs=0):
+    """A full T=1 decode layer in the oracle: the token through each of its k
+    experts. Returns (single-thread seconds, all-cores wall seconds or None,
+    per-expert seconds)."""
+    x_bits, logits, experts, per = t1_layer_inputs(s)
+    times = [oracle_expert_pass(s, x_bits, logits, per[j], 0, j)[1] for j in range(len(experts))]
+    wall = None
+    if pool_procs > 1:
+        ctx = mp.get_context("spawn")
+        with ctx.Pool(min(pool_procs, len(experts))) as pool:
+            pool.map(_expert_worker, [(s, x_bits, logits, per[0], 0, 0)] * min(pool_procs, len(experts)))  # warm
+            t0 = time.perf_counter()
+            pool.map(_expert_worker, [(s, x_bits, logits, per[j], 0, j) for j in range(len(experts))])
+            wall = time.perf_counter() - t0
+    return sum(times), wall, times
 
 
 def run_reference(args, s, rank, world):
-    """Reference arm: the CPU oracle, timed on the host cores, on a bounded
-    sample of every step (one token through one expert), scaled to the step's
-    (batch, expert) pairs."""
+    """Reference arm: the CPU oracle, timed on the host cores. Each step
+    times a bounded sample (one token through one expert, cycling over the
+    experts of a T=1 layer); the step value is that per-expert time scaled to
+    the (batch, expert) passes of a decode step (T = 1, 8, 32, 128), so it is
+    an extrapolation and says so. A full T=1 layer is also timed once."""
     if rank != 0:
         return
-    dev = torch.device("cuda:0") if torch.cuda.is_available() else torch.device("cpu")
-    x_bits, logits, wts, e = cpu_sample_inputs(s, dev)
-    pairs = float(sum(inputs.expected_touched(s, T) for T in DECODE_TS))
-    for _ in range(args.warmup):
-        oracle_expert_sample(s, x_bits, logits, wts, e)
+    cores, model = host_cpu()
+    x_bits, logits, experts, per = t1_layer_inputs(s)
+    passes = float(sum(inputs.expected_touched(s, T) for T in DECODE_TS))
+    for i in range(args.warmup):
+        oracle_expert_pass(s, x_bits, logits, per[i % len(per)], 0, i % len(per))
     t0 = time.perf_counter()
-    per = []
-    for _ in range(args.steps):
-        per.append(oracle_expert_sample(s, x_bits, logits, wts, e))
+    samples = []
+    for i in range(args.steps):
+        samples.append(oracle_expert_pass(s, x_bits, logits, per[i % len(per)], 0, i % len(per))[1])
     wall = time.perf_counter() - t0
-    us_step = statistics.mean(per) * pairs * 1e6
-    sample = (f"numpy fp64 oracle, 1 thread: one token through one expert (NVFP4 decode of W1 and W2, both "
-              f"GEMMs, SwiGLU, MXFP8 requant) per step, scaled by the expected {pairs:.0f} (batch, expert) "
-              f"pairs of a step (T=1,8,32,128)")
+    t1_single = sum(oracle_expert_pass(s, x_bits, logits, per[j], 0, j)[1] for j in range(len(per)))
+    us_step = statistics.mean(samples) * passes * 1e6
+    sample = (f"numpy fp64 oracle, 1 thread: per step one token through one expert (routing, NVFP4 decode of W1 "
+              f"and W2, both GEMMs, SwiGLU, MXFP8 requant), scaled by the {passes:.0f} expected (batch, expert) "
+              f"passes of a step (T=1,8,32,128); a full T=1 layer ({len(per)} experts) took {t1_single:.2f} s")
     line = {
         "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": us_step / 1e3, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
         "config": config_block(s, None),
-        "cpu_baseline": {"value": us_step, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "extrapolated": True,
+        "cpu_baseline": {"value": us_step, "unit": UNIT, "cores": 1, "host_cores": cores, "cpu_model": model,
+                         "kind": "oracle", "sample": sample, "extrapolated": True,
+                         "t1_layer_s_1thread": t1_single},
         "e2e": {"value": us_step, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "wall_s": wall,
     }
@@ -240,7 +302,7 @@ def config_block(s, per_T):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
-def run_ours(args, s, rank, world, local):
+def load_lib():
     import quantized_grouped_gemm_topk_gb300 as m
     try:
         m.binding.load()
@@ -248,158 +310,333 @@ def run_ours(args, s, rank, world, local):
         from quantized_grouped_gemm_topk_gb300 import build as b
         b.build()
         m.binding.load()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    Tmax = max(DECODE_TS)
-    cfg = m.config_from_shape(s, T_max=Tmax)
+    return m
+
+
+class DecodeBench:
+    """Graph-replayed decode layers of one workload at several T."""
+
+    def __init__(self, m, s, Ts, dev, rank, nx=16):
+        self.m, self.s, self.Ts, self.dev, self.nx = m, s, Ts, dev, nx
+        self.cfg = m.config_from_shape(s, T_max=max(Ts))
+        wts = inputs.gen_expert_weights(s, 0, device=dev)
+        self.packed = m.moe_prepack_weights(self.cfg, wts)
+        torch.cuda.synchronize()
+        del wts
+        torch.cuda.empty_cache()
+        self.ws = torch.zeros(m.moe_workspace_size(self.cfg), dtype=torch.uint8, device=dev)
+        self.Wr = inputs.gen_router(s, 0, device=dev)
+        self.xs = {T: [inputs.gen_x(s, 100 + 1000 * T + i + 7919 * rank, device=dev, T=T) for i in range(nx)]
+                   for T in Ts}
+        self.outs = {T: torch.empty(T, s.H, dtype=torch.bfloat16, device=dev) for T in Ts}
+        # routing is deterministic: learn each batch's touched-group count once
+        self.touched = {}
+        for T in Ts:
+            for i in range(nx):
+                m.moe_layer_forward(self.cfg, self.xs[T][i], self.Wr, None, T, self.packed, self.outs[T], None,
+                                    self.ws)
+                v = m.ws_tensor_views(self.cfg, self.ws, T)
+                self.touched[(T, i)] = int((v["counts"] > 0).sum())
+        torch.cuda.synchronize()
+        assert m.moe_read_status(self.cfg, self.ws) == 0
+        # one CUDA graph per (T, batch): the whole layer forward captured
+        # once, with its phase events as event-record nodes
+        self.graphs, self.gev, self.glaunch = {}, {}, {}
+        for T in Ts:
+            for i in range(nx):
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_N_PHASE_EVENTS)]
+                for e in evs:
+                    e.record()      # creates the event's handle
+                torch.cuda.synchronize()
+                g = torch.cuda.CUDAGraph()
+                m.moe_set_phase_events(evs)
+                with torch.cuda.graph(g):
+                    m.moe_layer_forward(self.cfg, self.xs[T][i], self.Wr, None, T, self.packed, self.outs[T], None,
+                                        self.ws)
+                    self.glaunch[(T, i)] = m.moe_last_launch_count()
+                m.moe_set_phase_events(None)
+                self.graphs[(T, i)], self.gev[(T, i)] = g, evs
+        torch.cuda.synchronize()
+
+    def weight_bytes(self, T, i):
+        """Algorithmic bytes of the layer: every touched group's W1 and W2
+        (NVFP4 with scales), the router weights, x in and out."""
+        s = self.s
+        return (self.touched[(T, i)] * (w1_bytes_per_expert(s) + w2_bytes_per_expert(s)) + s.H * s.E * 4
+                + 2 * T * s.H * 2)
+
+    def w1_bytes(self, T, i):
+        s = self.s
+        R = T * s.kp
+        return self.touched[(T, i)] * w1_bytes_per_expert(s) + R * (s.H + s.H // 32) + R * (s.I + s.I // 32)
+
+    def run(self, K, warmup, flush):
+        m = self.m
+        for w in range(warmup):
+            for T in self.Ts:
+                flush.zero_()
+                self.graphs[(T, w % self.nx)].replay()
+        torch.cuda.synchronize()
+        res = {"layer_us": {T: [] for T in self.Ts}, "w1_us": 0.0, "w1_bytes": 0, "w2_us": 0.0, "launches": 0,
+               "layer_bytes": {T: [] for T in self.Ts}}
+        for step in range(K):
+            i = step % self.nx
+            for T in self.Ts:
+                flush.zero_()
+                self.graphs[(T, i)].replay()
+                res["launches"] += self.glaunch[(T, i)]
+            # the graphs of this step are replayed again nx steps later: read
+            # their events now (host-side wait, outside every device interval)
+            torch.cuda.synchronize()
+            for T in self.Ts:
+                e = self.gev[(T, i)]
+                res["layer_us"][T].append(e[0].elapsed_time(e[5]) * 1e3)
+                res["layer_bytes"][T].append(self.weight_bytes(T, i))
+                res["w1_us"] += e[1].elapsed_time(e[2]) * 1e3
+                res["w2_us"] += e[3].elapsed_time(e[4]) * 1e3
+                res["w1_bytes"] += self.w1_bytes(T, i)
+        assert m.moe_read_status(self.cfg, self.ws) == 0
+        return res
+
+    def e2e(self, K, flush):
+        """Host wall clock per layer through the C ABI: pinned H2D copy of the
+        tokens, the forward, the D2H copy of the output, synchronize."""
+        m, s = self.m, self.s
+        host_x = {T: [self.xs[T][i].cpu().pin_memory() for i in range(self.nx)] for T in self.Ts}
+        host_out = {T: torch.empty(T, s.H, dtype=torch.bfloat16).pin_memory() for T in self.Ts}
+        dev_x = {T: torch.empty(T, s.H, dtype=torch.bfloat16, device=self.dev) for T in self.Ts}
+        total = 0.0
+        for step in range(K):
+            for T in self.Ts:
+                flush.zero_()
+                torch.cuda.synchronize()
+                t0 = time.perf_counter()
+                dev_x[T].copy_(host_x[T][step % self.nx], non_blocking=True)
+                m.moe_layer_forward(self.cfg, dev_x[T], self.Wr, None, T, self.packed, self.outs[T], None, self.ws)
+                host_out[T].copy_(self.outs[T], non_blocking=True)
+                torch.cuda.synchronize()
+                total += time.perf_counter() - t0
+        return total / K * 1e6, sum(T * s.H * 2 for T in self.Ts)
+
+    def free(self):
+        del self.graphs, self.packed, self.ws, self.xs
+        torch.cuda.empty_cache()
+
+
+def bench_shared_decode(m, dev, K, warmup, flush, hbm):
+    s = inputs.workload("shared")
+    b = DecodeBench(m, s, SHARED_TS, dev, 0)
+    r = b.run(K, warmup, flush)
+    out = {"workload": "shared_decode", "H": s.H, "I": s.I, "E": s.E, "n_shared": s.n_shared, "k": s.k,
+           "routed_scale": s.routed_scale, "weights": "nvfp4", "launch": "CUDA graph per layer", "per_T": {}}
+    for T in SHARED_TS:
+        us = statistics.median(r["layer_us"][T])
+        gb = statistics.mean(r["layer_bytes"][T])
+        out["per_T"][str(T)] = {"us_per_layer": us, "tokens_per_s": T / us * 1e6,
+                                "layer_bytes": gb, "hbm_frac_of_measured": gb / (us * 1e-6) / 1e9 / hbm}
+    out["w1_gemm_hbm_frac_of_measured"] = r["w1_bytes"] / (r["w1_us"] * 1e-6) / 1e9 / hbm
+    b.free()
+    return out
+
+
+def bench_skewed(m, dev, K, warmup, flush, hbm, bf16):
+    """Skewed-routing prefill (NVFP4 weights, exact f16 tensor-core path)."""
+    s = inputs.workload("skewed")
+    T = s.T
+    cfg = m.config_from_shape(s, T_max=T)
     wts = inputs.gen_expert_weights(s, 0, device=dev)
     packed = m.moe_prepack_weights(cfg, wts)
-    torch.cuda.synchronize()
     del wts
     torch.cuda.empty_cache()
     ws = torch.zeros(m.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    x = inputs.gen_x(s, 3, device=dev)
+    lg = inputs.gen_logits(s, 3, device=dev)
+    out = torch.empty(T, s.H, dtype=torch.bfloat16, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_N_PHASE_EVENTS)]
+    for e in ev:
+        e.record()
+    for _ in range(warmup):
+        m.moe_layer_forward(cfg, x, None, lg, T, packed, out, None, ws)
+    torch.cuda.synchronize()
+    v = m.ws_tensor_views(cfg, ws, T)
+    counts = v["counts"].cpu()
+    touched = int((counts > 0).sum())
+    m.moe_set_phase_events(ev)
+    lay, w1, w2 = [], [], []
+    for _ in range(K):
+        flush.zero_()
+        m.moe_layer_forward(cfg, x, None, lg, T, packed, out, None, ws)
+        torch.cuda.synchronize()
+        lay.append(ev[0].elapsed_time(ev[5]) * 1e3)
+        w1.append(ev[1].elapsed_time(ev[2]) * 1e3)
+        w2.append(ev[3].elapsed_time(ev[4]) * 1e3)
+    m.moe_set_phase_events(None)
+    assert m.moe_read_status(cfg, ws) == 0
+    R = T * s.k
+    flops = 2.0 * R * s.H * 2 * s.I + 2.0 * R * s.I * s.H
+    wbytes = touched * (w1_bytes_per_expert(s) + w2_bytes_per_expert(s)) + 2 * T * s.H * 2
+    us = statistics.median(lay)
+    res = {"workload": "skewed_prefill", "T": T, "H": s.H, "I": s.I, "E": s.E, "k": s.k, "weights": "nvfp4",
+           "routing": "Zipf(1.2), 30% of experts forced empty", "touched_experts": touched,
+           "max_share": float(counts.max()) / R, "us_per_layer": us, "tokens_per_s": T / us * 1e6,
+           "w1_us": statistics.median(w1), "w2_us": statistics.median(w2),
+           "tflops": flops / (us * 1e-6) / 1e12,
+           "tensor_frac_of_bf16_measured": flops / (us * 1e-6) / 1e12 / bf16,
+           "tensor_frac_of_fp8_derived": flops / (us * 1e-6) / 1e12 / (2 * bf16),
+           "hbm_floor_us": wbytes / (hbm * 1e9) * 1e6,
+           "note": "NVFP4 weights are decoded exactly to f16 for the MMA, so the dense-f16 (= bf16) rate is the "
+                   "ceiling; the FP8 fraction uses 2x the measured bf16 peak"}
+    del packed, ws
+    torch.cuda.empty_cache()
+    return res
+
+
+def bench_train(m, dev, K, warmup, bf16):
+    """Training forward + backward (MXFP8 x MXFP8 on the block-scaled tensor
+    cores). Weights (3.2 GB) and activations exceed L2, so no flush."""
+    s = inputs.workload("train")
+    T = s.T
+    cfg = m.config_from_shape(s, T_max=T)
+    wts = inputs.gen_expert_weights(s, 0, device=dev)
+    packed = m.moe_prepack_weights(cfg, wts)
+    packed_d = m.moe_prepack_weights(cfg, wts, m.MOE_PACK_DGRAD)
+    del wts
+    torch.cuda.empty_cache()
+    ws = torch.zeros(m.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    x = inputs.gen_x(s, 0, device=dev)
     Wr = inputs.gen_router(s, 0, device=dev)
+    out = torch.empty(T, s.H, dtype=torch.bfloat16, device=dev)
+    st, bufs = m.alloc_train_save(cfg, T, dev)
+    dout = inputs.gen_dout(s, 0, device=dev)
+    dx = torch.empty(T, s.H, dtype=torch.bfloat16, device=dev)
+    dW1 = torch.empty(s.E, s.H, 2 * s.I, dtype=torch.bfloat16, device=dev)
+    dW2 = torch.empty(s.E, s.I, s.H, dtype=torch.bfloat16, device=dev)
+    dlog = torch.empty(T, s.E, dtype=torch.float32, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_N_PHASE_EVENTS)]
+    for e in ev:
+        e.record()
+    for _ in range(warmup):
+        m.moe_layer_forward(cfg, x, Wr, None, T, packed, out, st, ws)
+        m.moe_layer_backward(cfg, dout, x, T, st, packed_d, dx, dW1, dW2, dlog, ws)
+    torch.cuda.synchronize()
+    a, b, c = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    fw, bw, w1, w2 = [], [], [], []
+    m.moe_set_phase_events(ev)
+    for _ in range(K):
+        a.record()
+        m.moe_layer_forward(cfg, x, Wr, None, T, packed, out, st, ws)
+        b.record()
+        m.moe_layer_backward(cfg, dout, x, T, st, packed_d, dx, dW1, dW2, dlog, ws)
+        c.record()
+        torch.cuda.synchronize()
+        fw.append(a.elapsed_time(b))
+        bw.append(b.elapsed_time(c))
+        w1.append(ev[1].elapsed_time(ev[2]))
+        w2.append(ev[3].elapsed_time(ev[4]))
+    m.moe_set_phase_events(None)
+    assert m.moe_read_status(cfg, ws) == 0
+    R = T * s.k
+    f1 = 2.0 * R * s.H * 2 * s.I
+    f2 = 2.0 * R * s.I * s.H
+    fms, bms, w1ms, w2ms = (statistics.median(v) for v in (fw, bw, w1, w2))
+    fp8 = 2 * bf16
+    res = {"workload": "train", "T": T, "H": s.H, "I": s.I, "E": s.E, "k": s.k, "weights": "mxfp8",
+           "activations": "mxfp8", "act": "swiglu clamp 7, alpha 1.702", "l2": "not flushed: inputs exceed L2",
+           "fwd_ms": fms, "bwd_ms": bms, "fwd_tokens_per_s": T / fms * 1e3, "fwd_bwd_tokens_per_s": T / (fms + bms) * 1e3,
+           "w1_gemm_ms": w1ms, "w2_gemm_ms": w2ms,
+           "w1_gemm_tflops": f1 / w1ms / 1e9, "w2_gemm_tflops": f2 / w2ms / 1e9,
+           "w1_gemm_frac_of_fp8": f1 / w1ms / 1e9 / fp8, "w2_gemm_frac_of_fp8": f2 / w2ms / 1e9 / fp8,
+           "fwd_tflops": (f1 + f2) / fms / 1e9, "bwd_tflops": 2 * (f1 + f2) / bms / 1e9,
+           "bwd_frac_of_fp8": 2 * (f1 + f2) / bms / 1e9 / fp8,
+           "fp8_peak_tflops": fp8,
+           "fp8_peak_source": "2 x the measured dense bf16 burst peak (the nominal FP8 : BF16 tensor ratio); no FP8 "
+                              "peak is measured on this pool",
+           "kernel": "k_gemm_mx (tcgen05.mma kind::mxf8f6f4, block-scaled)"}
+    del packed, packed_d, ws, bufs, dW1, dW2
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args, s, rank, world, local):
+    m = load_lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    hbm, bf16, bf16_sus, peak_kind = peaks()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    nx = 16
-    xs = {T: [inputs.gen_x(s, 100 + 1000 * T + i + 7919 * rank, device=dev, T=T) for i in range(nx)]
-          for T in DECODE_TS}
-    outs = {T: torch.empty(T, s.H, dtype=torch.bfloat16, device=dev) for T in DECODE_TS}
-    # routing is deterministic: learn each batch's touched-expert count once
-    touched = {}
-    for T in DECODE_TS:
-        for i in range(nx):
-            m.moe_layer_forward(cfg, xs[T][i], Wr, None, T, packed, outs[T], None, ws)
-            v = m.ws_tensor_views(cfg, ws, T)
-            touched[(T, i)] = int((v["counts"] > 0).sum())
-    torch.cuda.synchronize()
-    assert m.moe_read_status(cfg, ws) == 0
+    bench = DecodeBench(m, s, DECODE_TS, dev, rank)
 
-    def layer_bytes(T, i):
-        n = touched[(T, i)]
-        R = T * s.kp
-        return n * w1_bytes_per_expert(s), R * (s.H + s.H // 32) + R * (s.I + s.I // 32)
-
-    # One CUDA graph per (T, batch): the whole layer forward captured once,
-    # with its phase events as event-record nodes, replayed in the timed loop.
-    graphs, gev, glaunch = {}, {}, {}
-    for T in DECODE_TS:
-        for i in range(nx):
-            evs = [torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_N_PHASE_EVENTS)]
-            for e in evs:
-                e.record()      # creates the event's handle
-            torch.cuda.synchronize()
-            g = torch.cuda.CUDAGraph()
-            m.moe_set_phase_events(evs)
-            with torch.cuda.graph(g):
-                m.moe_layer_forward(cfg, xs[T][i], Wr, None, T, packed, outs[T], None, ws)
-                glaunch[(T, i)] = m.moe_last_launch_count()
-            m.moe_set_phase_events(None)
-            graphs[(T, i)], gev[(T, i)] = g, evs
-    torch.cuda.synchronize()
-
-    # warm-up
-    for w in range(args.warmup):
-        for T in DECODE_TS:
-            flush.zero_()
-            graphs[(T, w % nx)].replay()
-    torch.cuda.synchronize()
-    assert m.moe_read_status(cfg, ws) == 0
-
-    K = args.steps
-    launches = 0
-    layer_us = []
-    w1_us, w1_bytes, w2_us = 0.0, 0, 0.0
-    per_T = {T: [] for T in DECODE_TS}
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t_wall = time.perf_counter()
     with ClockSampler(local) as clk:
-        for step in range(K):
-            i = step % nx
-            for T in DECODE_TS:
-                flush.zero_()
-                graphs[(T, i)].replay()
-                launches += glaunch[(T, i)]
-            # the graphs of this step are replayed again nx steps later: read
-            # their events now (host-side wait, outside every device interval)
-            torch.cuda.synchronize()
-            for T in DECODE_TS:
-                e = gev[(T, i)]
-                t = e[0].elapsed_time(e[5]) * 1e3
-                layer_us.append(t)
-                per_T[T].append(t)
-                w1_us += e[1].elapsed_time(e[2]) * 1e3
-                w2_us += e[3].elapsed_time(e[4]) * 1e3
-                wb, ab = layer_bytes(T, i)
-                w1_bytes += wb + ab
+        r = bench.run(args.steps, args.warmup, flush)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    K = args.steps
     wall_ms = (time.perf_counter() - t_wall) * 1e3 / K
-    assert m.moe_read_status(cfg, ws) == 0
-    us_step = sum(layer_us) / K
+    us_step = sum(sum(v) for v in r["layer_us"].values()) / K
     if world > 1:
         us_step = max_over_ranks(us_step, dev)
+    e2e_us, h2d = bench.e2e(min(K, 50), flush)
+    if world > 1:
+        e2e_us = max_over_ranks(e2e_us, dev)
 
-    # end to end through the public API with host buffers
-    host_x = {T: [xs[T][i].cpu().pin_memory() for i in range(nx)] for T in DECODE_TS}
-    host_out = {T: torch.empty(T, s.H, dtype=torch.bfloat16).pin_memory() for T in DECODE_TS}
-    dev_x = {T: torch.empty(T, s.H, dtype=torch.bfloat16, device=dev) for T in DECODE_TS}
-    ncall = K * len(DECODE_TS)
-    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(ncall)]
-    torch.cuda.synchronize()
-    c = 0
-    for step in range(K):
-        for T in DECODE_TS:
-            flush.zero_()
-            a, b = e2e_ev[c]
-            a.record()
-            dev_x[T].copy_(host_x[T][step % nx], non_blocking=True)
-            m.moe_layer_forward(cfg, dev_x[T], Wr, None, T, packed, outs[T], None, ws)
-            host_out[T].copy_(outs[T], non_blocking=True)
-            b.record()
-            c += 1
-    torch.cuda.synchronize()
-    e2e_us = sum(a.elapsed_time(b) * 1e3 for a, b in e2e_ev) / K
-    h2d = sum(T * s.H * 2 for T in DECODE_TS)
-
-    peak, peak_kind = peaks()
-    achieved = w1_bytes / (w1_us * 1e-6) / 1e9
+    achieved = r["w1_bytes"] / (r["w1_us"] * 1e-6) / 1e9
     sha = kernel_source_sha()
     tr = traffic_per_launch(sha)
-    roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+    roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
             "traffic": None, "kernel": "W1 grouped GEMM (k_gemm_tc)", "peak_source": f"{peak_kind} hbm_gbs",
             "algorithmic_bytes": "touched experts x NVFP4 W1 bytes (2I*H/2 + 2I*H/16) + MXFP8 rows in and out",
-            "kernel_us_per_step": w1_us / K, "w2_gemm_us_per_step": w2_us / K}
+            "kernel_us_per_step": r["w1_us"] / K, "w2_gemm_us_per_step": r["w2_us"] / K}
     if tr is not None:
         # DRAM bytes of one captured W1 launch over its algorithmic bytes,
         # applied to this run's average algorithmic bytes per W1 launch
-        roof["traffic"] = tr["dram_over_algorithmic"] * w1_bytes / (K * len(DECODE_TS))
+        roof["traffic"] = tr["dram_over_algorithmic"] * r["w1_bytes"] / (K * len(DECODE_TS))
         roof["traffic_note"] = (f"ncu dram__bytes_read+write of one W1 launch ({tr['captured']}) = "
                                 f"{tr['dram_over_algorithmic']:.4f} x its algorithmic bytes, scaled to this "
                                 f"run's average W1 launch")
-    per_T_us = {str(T): statistics.median(v) for T, v in per_T.items()}
+    per_T_us = {str(T): statistics.median(v) for T, v in r["layer_us"].items()}
+    layer_frac = {str(T): statistics.mean(r["layer_bytes"][T]) / (statistics.median(r["layer_us"][T]) * 1e-6) / 1e9
+                  / hbm for T in DECODE_TS}
     clocks = clk.summary()
+    cfgb = config_block(s, per_T_us)
+    cfgb["per_T_layer_hbm_frac_of_measured"] = layer_frac
     line = {
         "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": us_step / 1e3, "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3 x e2m1, f32 accumulate", "data": "synthetic", "config": config_block(s, per_T_us),
+        "dtype": "e4m3 x e2m1, f32 accumulate", "data": "synthetic", "config": cfgb,
         "roofline": roof,
-        "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": h2d},
-        "gpu_launches": launches,
+        "e2e": {"value": e2e_us, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": h2d,
+                "clock": "host perf_counter per layer around H2D copy, moe_layer_forward (C ABI, no graph), D2H "
+                         "copy and synchronize; L2 flushed before each layer, outside the interval"},
+        "gpu_launches": r["launches"],
         "clocks": clocks,
         "wall_ms_per_step": wall_ms,
     }
+    bench.free()
+    del bench
+    if not args.no_per_config:
+        pc = {}
+        pc["shared_decode"] = bench_shared_decode(m, dev, min(K, 50), args.warmup, flush, hbm)
+        pc["skewed_prefill"] = bench_skewed(m, dev, min(K, 20), args.warmup, flush, hbm, bf16)
+        pc["train"] = bench_train(m, dev, min(K, 10), max(2, min(args.warmup, 3)), bf16)
+        pc["peaks"] = {"hbm_gbs": hbm, "bf16_tflops_burst": bf16, "bf16_tflops_sustained": bf16_sus,
+                       "fp8_tflops_derived": 2 * bf16, "source": peak_kind}
+        line["per_config"] = pc
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        x_bits, logits, wts_np, e = cpu_sample_inputs(s, dev)
-        reps = [oracle_expert_sample(s, x_bits, logits, wts_np, e) for _ in range(3)]
-        pairs = float(sum(touched[(T, 0)] for T in DECODE_TS))
+        cores, model = host_cpu()
+        single, allc, per = oracle_t1_layer(s, pool_procs=cores)
+        passes = float(sum(inputs.expected_touched(s, T) for T in DECODE_TS))
         line["cpu_baseline"] = {
-            "value": statistics.median(reps) * pairs * 1e6, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"numpy fp64 oracle, 1 thread: one token through one expert (W1/W2 NVFP4 decode, GEMMs, "
-                      f"SwiGLU, MXFP8 requant), median of 3, scaled by the {pairs:.0f} touched experts of "
-                      f"step 0 (T=1,8,32,128)"}
+            "value": single / len(per) * passes * 1e6, "unit": UNIT, "cores": 1, "host_cores": cores,
+            "cpu_model": model, "kind": "oracle", "extrapolated": True,
+            "value_all_cores": (allc / len(per) * passes * 1e6) if allc else None,
+            "t1_layer_s_1thread": single, "t1_layer_s_all_cores": allc,
+            "sample": f"numpy fp64 oracle: one full T=1 layer ({len(per)} experts) timed single-threaded and with "
+                      f"one process per expert on {cores} cores, scaled per expert pass to the {passes:.0f} "
+                      f"expected (batch, expert) passes of a step (T=1,8,32,128)"}
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -412,6 +649,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="dsv3", choices=["dsv3", "shared"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="headline workload only")
     ap.add_argument("--E", type=int, default=0, help="override the expert count (small profiling cases)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup

@@ -153,10 +153,12 @@ typedef struct moe_train_save {
     uint16_t* h;        /* [R, 2I] bf16 W1 output before the activation       */
     uint8_t* y1t_q;     /* [I, R_pad] MXFP8 of y (activation x routing weight)
                            quantised along the padded row axis               */
-    uint8_t* y1t_s;     /* [I, R_pad/32]                                      */
+    uint8_t* y1t_s;     /* [R_pad/32, I] its E8M0 scales, block-major: the
+                           scale of feature i, padded rows 32b..32b+31 at
+                           [b, i]                                             */
     uint8_t* at_q;      /* [H, R_pad] MXFP8 of the gathered x rows, quantised
                            along the padded row axis                          */
-    uint8_t* at_s;      /* [H, R_pad/32]                                      */
+    uint8_t* at_s;      /* [R_pad/32, H] its scales, block-major as y1t_s     */
     int32_t* poff;      /* [G + 1] padded row offsets                         */
 } moe_train_save_t;
 

@@ -61,7 +61,7 @@ struct WsLayout {
   size_t status, logits, rpart, ids, wts, counts, offsets, touched, ntouch, poff, hist, base;
   size_t perm, inv, wrow, xq, xs, y1q, y1s, z;
   size_t P, a16, y16, rexp1, rexp2;                       // NVFP4 path
-  size_t xg, xgs;                                         // MXFP8 path: gathered x rows
+  size_t xg, xgs, y1st;                                   // MXFP8 path: gathered x rows, y1 scales (SFT)
   size_t dzq, dzs, dzg, dzgs, dztq, dzts, dhq, dhs, dhtq, dhts, dxp, dwpart;   // backward
   size_t total;
 };
@@ -104,6 +104,7 @@ static WsLayout ws_layout(const moe_config_t& c) {
   } else {
     L.xg = take((size_t)R * d.H);
     L.xgs = take((size_t)R * d.H / 32);
+    L.y1st = take((size_t)R * d.I / 32);
   }
   if (backward_capable(c)) {
     L.dzq = take((size_t)T * d.H);
@@ -499,8 +500,8 @@ static int mx_grid(const moe_config_t& c) {
 }
 
 // Token-side block-scaled GEMM (modes kMxW1, kMxPlain, kMxDswiglu): A = the
-// MXFP8 rows aq/as [R][K] in group order, B = matrix `mat` of the packed
-// MXFP8 blob; g carries the epilogue fields.
+// MXFP8 rows aq [R][K] in group order with scales as (SFT [K/32][R]), B =
+// matrix `mat` of the packed MXFP8 blob; g carries the epilogue fields.
 static moe_status_t mx_token_gemm(const moe_config_t* c, MxArgs& g, int mode, const uint8_t* aq, const uint8_t* as,
                                   int64_t R, const void* packed, int which, int mat, const int32_t* offsets,
                                   const int32_t* poff, int32_t* status, cudaStream_t st) {
@@ -516,8 +517,8 @@ static moe_status_t mx_token_gemm(const moe_config_t* c, MxArgs& g, int mode, co
   g.b_rows_per_group = rows;
   g.offsets = offsets;
   g.poff = poff;
-  g.a_sf = as; g.a_sf_ld = K / 32; g.a_rows = R;
-  g.b_sf = b + (mat == 1 ? P.off_s1 : P.off_s2); g.b_sf_ld = K / 32; g.b_rows = (int64_t)P.G * rows;
+  g.a_sf = as; g.a_sf_ld = R; g.a_rows = R;
+  g.b_sf = b + (mat == 1 ? P.off_s1 : P.off_s2); g.b_sf_ld = (int64_t)P.G * rows; g.b_rows = (int64_t)P.G * rows;
   g.R = R;
   g.status = status;
   MxMaps maps;
@@ -566,8 +567,9 @@ static moe_status_t w1_impl(const moe_config_t* c, const moe_dispatch_t* d, int 
     g.w_row = d->w_row;
     g.act = act_params(c);
     g.yq = y1q; g.ys = y1s;
+    g.yst = at<uint8_t>(ws, L.y1st);
     if (save) {
-      g.hsave = save->h; g.tq = save->y1t_q; g.ts = save->y1t_s; g.t_ld = r_pad_for(dims_of(*c), T);
+      g.hsave = save->h; g.tq = save->y1t_q; g.ts = save->y1t_s; g.t_ld = r_pad_for(dims_of(*c), T); g.t_nf = c->I;
     }
     moe_status_t s = mx_token_gemm(c, g, kMxW1, xg, xgs, R, packed, MOE_PACK_FORWARD, 1, d->offsets,
                                    at<int32_t>(ws, L.poff), status, st);
@@ -599,15 +601,23 @@ static moe_status_t w1_impl(const moe_config_t* c, const moe_dispatch_t* d, int 
 }
 
 // W2 on the MXFP8 path: z [R][H] bf16 straight from the block-scaled GEMM.
+// y1st: y1's scales in SFT layout ([I/32][R]); nullptr converts y1s (the
+// row-major [R][I/32] layout) into the workspace first.
 static moe_status_t w2_mx(const moe_config_t* c, const int32_t* offsets, int T, const uint8_t* y1q,
-                          const uint8_t* y1s, const void* packed, uint16_t* z, void* ws, cudaStream_t st) {
+                          const uint8_t* y1s, const uint8_t* y1st, const void* packed, uint16_t* z, void* ws,
+                          cudaStream_t st) {
   const WsLayout L = ws_layout(*c);
   const int64_t R = (int64_t)T * (c->k + c->n_shared);
+  if (!y1st) {
+    uint8_t* t = at<uint8_t>(ws, L.y1st);
+    MOE_CHECK_CUDA(launch_sf_to_sft(y1s, c->I, R, t, st));
+    y1st = t;
+  }
   MxArgs g = mx_args0();
   g.n_tiles = ceil_div(c->H, kMxTileN);
   g.N = c->H;
   g.out = z; g.out_ld = c->H;
-  return mx_token_gemm(c, g, kMxPlain, y1q, y1s, R, packed, MOE_PACK_FORWARD, 2, offsets, at<int32_t>(ws, L.poff),
+  return mx_token_gemm(c, g, kMxPlain, y1q, y1st, R, packed, MOE_PACK_FORWARD, 2, offsets, at<int32_t>(ws, L.poff),
                        at<int32_t>(ws, L.status), st);
 }
 
@@ -639,7 +649,7 @@ moe_status_t moe_grouped_gemm_w2(const moe_config_t* c, const moe_dispatch_t* d,
   reset_launch_count();
   if (T == 0) return MOE_OK;
   cudaStream_t st = (cudaStream_t)stream;
-  if (mx_path(*c)) return w2_mx(c, d->offsets, T, y1_q, y1_s, packed_w, z, ws, st);
+  if (mx_path(*c)) return w2_mx(c, d->offsets, T, y1_q, y1_s, nullptr, packed_w, z, ws, st);
   const WsLayout L = ws_layout(*c);
   const PackLayout P = pack_layout(*c, MOE_PACK_FORWARD);
   const int R = T * (c->k + c->n_shared);
@@ -728,7 +738,8 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
   }
   if ((s = w1_impl(c, &v.d, T, packed_w, v.y1_q, v.y1_s, save, ws, st, true)) != MOE_OK) return s;
   if (mx_path(*c)) {
-    if ((s = w2_mx(c, v.d.offsets, T, v.y1_q, v.y1_s, packed_w, v.z, ws, st)) != MOE_OK) return s;
+    if ((s = w2_mx(c, v.d.offsets, T, v.y1_q, v.y1_s, at<uint8_t>(ws, L.y1st), packed_w, v.z, ws, st)) != MOE_OK)
+      return s;
     phase(4, st);
     MOE_CHECK_CUDA(launch_combine(v.z, v.d.inv, nullptr, T, c->k, kp, c->H, out, st));
     phase(5, st);
@@ -758,8 +769,8 @@ static moe_status_t mx_wgrad(const moe_config_t* c, const uint8_t* pq, const uin
   g.M = M; g.m_tiles = ceil_div(M, mx_tile_m());
   g.N = N; g.n_tiles = ceil_div(N, mx_tile_n());
   g.poff = poff;
-  g.a_sf = ps; g.a_sf_ld = Rp / 32; g.a_rows = M;
-  g.b_sf = qs; g.b_sf_ld = Rp / 32; g.b_rows = N;
+  g.a_sf = ps; g.a_sf_ld = M; g.a_rows = M;
+  g.b_sf = qs; g.b_sf_ld = N; g.b_rows = N;
   g.out = out; g.out_ld = N;
   g.status = status;
   MxMaps maps;
@@ -819,8 +830,8 @@ moe_status_t moe_layer_backward(const moe_config_t* c, const uint16_t* dout, con
     g.w_row = v.d.w_row;
     g.act = act_params(c);
     g.hsave = save->h;
-    g.yq = dhq; g.ys = dhs;
-    g.tq = dhtq; g.ts = dhts; g.t_ld = Rp;
+    g.yq = dhq; g.yst = dhs;
+    g.tq = dhtq; g.ts = dhts; g.t_ld = Rp; g.t_nf = 2 * I;
     g.dwpart = dwpart;
     if ((s = mx_token_gemm(c, g, kMxDswiglu, dzg, dzgs, R, packed_w_dgrad, MOE_PACK_DGRAD, 2, v.d.offsets, poff,
                            status, st)) != MOE_OK)

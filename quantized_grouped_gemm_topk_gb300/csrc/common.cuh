@@ -18,7 +18,8 @@ constexpr unsigned kFull = 0xffffffffu;
 // chunks.
 //   chunk: [granule g < 2][row p < 128][16 B of 32 E2M1 codes] (4096 B)
 //          then [row p][4 E4M3 scale codes, one per 16 K] (512 B).
-// MXFP8: plain K-major rows, codes [G][rows][K] and scales [G][rows][K/32];
+// MXFP8: plain K-major rows, codes [G][rows][K] and scales block-major
+//   [K/32][G * rows];
 //   W1's forward rows come in tiles of 192: 96 gate features then the same
 //   96 up features (zero rows past I), every other matrix in its own row
 //   order.

@@ -118,13 +118,15 @@ __device__ __forceinline__ void mx_unit(const MxArgs& g, const int32_t* uoff, in
 
 __device__ __forceinline__ int mx_stages(int klen) { return (klen + kMxBK - 1) / kMxBK; }
 
-// The scale bytes of K blocks kb .. kb+kv-1 of one row, packed little-endian
-// (block kb in the low byte); 0 past kv.
-__device__ __forceinline__ uint32_t load_sf4(const uint8_t* row, int kb, int kv) {
+// The scale bytes of K blocks kb .. kb+kv-1 of one row of an SFT array
+// (col = the row's first byte, ld = the array's row count), packed
+// little-endian (block kb in the low byte); 0 past kv. Lanes holding
+// consecutive rows read consecutive bytes.
+__device__ __forceinline__ uint32_t load_sft4(const uint8_t* col, int64_t ld, int kb, int kv) {
   uint32_t v = 0;
 #pragma unroll
   for (int j = 0; j < 4; ++j)
-    if (j < kv) v |= (uint32_t)__ldg(row + kb + j) << (8 * j);
+    if (j < kv) v |= (uint32_t)__ldg(col + (int64_t)(kb + j) * ld) << (8 * j);
   return v;
 }
 
@@ -153,12 +155,13 @@ __device__ __forceinline__ uint8_t quant_block32_store(const float (&v)[32], uin
 
 // Column quantiser of the transposed copies: the warp's 32 lanes are 32
 // consecutive padded rows (one MX block along the token axis) of feature f;
-// lane l writes the code of its row, lane 0 the block's scale.
-__device__ __forceinline__ void quant_col_store(float v, uint8_t* tq, uint8_t* ts, int64_t f, int64_t ld, int64_t p,
-                                                int lane) {
+// lane l writes the code of its row, lane 0 the block's scale (SFT: blocks
+// of the token axis major, nf features).
+__device__ __forceinline__ void quant_col_store(float v, uint8_t* tq, uint8_t* ts, int64_t f, int64_t ld, int nf,
+                                                int64_t p, int lane) {
   const int e = mx_exponent(warp_max(fabsf(v)));
   tq[f * ld + p] = (uint8_t)(f32x2_to_e4m3x2(v * pow2_neg(e), 0.f) & 0xffu);
-  if (lane == 0) ts[f * (ld / 32) + p / 32] = (uint8_t)(e + 127);
+  if (lane == 0) ts[(p / 32) * nf + f] = (uint8_t)(e + 127);
 }
 
 template <int MODE>
@@ -212,7 +215,9 @@ __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, ui
 #pragma unroll
       for (int i = 0; i < 32; ++i) y[i] = wr * act_fwd(__uint_as_float(gv[i]), __uint_as_float(uv[i]), g.act);
       if (rvalid) {
-        g.ys[row * (g.I / 32) + f / 32] = quant_block32_store(y, g.yq + row * g.I + f);
+        const uint8_t sb = quant_block32_store(y, g.yq + row * g.I + f);
+        g.ys[row * (g.I / 32) + f / 32] = sb;
+        if (g.yst) g.yst[(int64_t)(f / 32) * g.R + row] = sb;
         if (g.hsave) {
           uint32_t hg[16], hu[16];
 #pragma unroll
@@ -232,7 +237,8 @@ __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, ui
       if (tblk) {
         const bool live = rel < w.cnt;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) quant_col_store(live ? y[i] : 0.f, g.tq, g.ts, f + i, g.t_ld, p, lane);
+        for (int i = 0; i < 32; ++i)
+          quant_col_store(live ? y[i] : 0.f, g.tq, g.ts, f + i, g.t_ld, g.t_nf, p, lane);
       }
     }
   } else {   // kMxDswiglu: columns = dY1 for features f0 + c
@@ -272,8 +278,8 @@ __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, ui
           dg[i] = d.x;
           du[i] = d.y;
         }
-        g.ys[row * (2 * I / 32) + f / 32] = quant_block32_store(dg, g.yq + row * 2 * I + f);
-        g.ys[row * (2 * I / 32) + (I + f) / 32] = quant_block32_store(du, g.yq + row * 2 * I + I + f);
+        g.yst[(int64_t)(f / 32) * g.R + row] = quant_block32_store(dg, g.yq + row * 2 * I + f);
+        g.yst[(int64_t)((I + f) / 32) * g.R + row] = quant_block32_store(du, g.yq + row * 2 * I + I + f);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) dg[i] = du[i] = 0.f;
@@ -281,8 +287,8 @@ __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, ui
       if (tblk) {
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          quant_col_store(live ? dg[i] : 0.f, g.tq, g.ts, f + i, g.t_ld, p, lane);
-          quant_col_store(live ? du[i] : 0.f, g.tq, g.ts, (int64_t)I + f + i, g.t_ld, p, lane);
+          quant_col_store(live ? dg[i] : 0.f, g.tq, g.ts, f + i, g.t_ld, g.t_nf, p, lane);
+          quant_col_store(live ? du[i] : 0.f, g.tq, g.ts, (int64_t)I + f + i, g.t_ld, g.t_nf, p, lane);
         }
       }
     }
@@ -451,17 +457,18 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
       MxUnit w;
       mx_unit(g, uoff, u, w);
       const int nk = mx_stages(w.klen);
+      // first byte of each row's SFT column (nullptr: no such row)
       const uint8_t* pa[4];
       const uint8_t* pb[4 + kNB1];
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int64_t ra = (int64_t)w.a_row0 + 32 * c + lane;
-        pa[c] = ra < g.a_rows ? g.a_sf + ra * g.a_sf_ld : nullptr;
+        pa[c] = ra < g.a_rows ? g.a_sf + ra : nullptr;
       }
 #pragma unroll
       for (int c = 0; c < 4 + kNB1; ++c) {
         const int64_t rb = (int64_t)w.b_row0 + 32 * c + lane;
-        pb[c] = rb < g.b_rows ? g.b_sf + rb * g.b_sf_ld : nullptr;
+        pb[c] = rb < g.b_rows ? g.b_sf + rb : nullptr;
       }
       const int kb0 = w.k0 / 32;
       // four stages of scale words in flight in registers
@@ -470,9 +477,10 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
       for (int j = 0; j < 4; ++j) {
         const int kv = j < nk ? min(4, (w.klen - j * kMxBK) / 32) : 0;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) va[j][c] = (pa[c] && kv) ? load_sf4(pa[c], kb0 + 4 * j, kv) : 0u;
+        for (int c = 0; c < 4; ++c) va[j][c] = (pa[c] && kv) ? load_sft4(pa[c], g.a_sf_ld, kb0 + 4 * j, kv) : 0u;
 #pragma unroll
-        for (int c = 0; c < 4 + kNB1; ++c) vb[j][c] = (pb[c] && kv) ? load_sf4(pb[c], kb0 + 4 * j, kv) : 0u;
+        for (int c = 0; c < 4 + kNB1; ++c)
+          vb[j][c] = (pb[c] && kv) ? load_sft4(pb[c], g.b_sf_ld, kb0 + 4 * j, kv) : 0u;
       }
       for (int s0 = 0; s0 < nk; s0 += 4) {
 #pragma unroll
@@ -499,10 +507,11 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
               const int s4 = s + 4;
               const int kv = s4 < nk ? min(4, (w.klen - s4 * kMxBK) / 32) : 0;
 #pragma unroll
-              for (int c = 0; c < 4; ++c) va[j][c] = (pa[c] && kv) ? load_sf4(pa[c], kb0 + 4 * s4, kv) : 0u;
+              for (int c = 0; c < 4; ++c)
+                va[j][c] = (pa[c] && kv) ? load_sft4(pa[c], g.a_sf_ld, kb0 + 4 * s4, kv) : 0u;
 #pragma unroll
               for (int c = 0; c < 4 + kNB1; ++c)
-                vb[j][c] = (pb[c] && kv) ? load_sf4(pb[c], kb0 + 4 * s4, kv) : 0u;
+                vb[j][c] = (pb[c] && kv) ? load_sft4(pb[c], g.b_sf_ld, kb0 + 4 * s4, kv) : 0u;
             }
           }
         }
@@ -601,7 +610,8 @@ int mx_tile_m() { return kMxBM; }
 
 // ---------------------------------------------------------------------------
 // Row gather of MXFP8 rows: dst[r] = src[row_map[r] / row_div] (codes and
-// scales), r < min(R, offsets[G]). One warp per row, 16-byte copies.
+// scales), r < min(R, offsets[G]). One warp per row, 16-byte copies; the
+// scales land block-major (SFT, ld R) for the GEMM's scale loaders.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_gather_mx(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int C,
                                                    const int32_t* __restrict__ row_map, int row_div, int R,
@@ -616,7 +626,7 @@ __global__ void __launch_bounds__(256) k_gather_mx(const uint8_t* __restrict__ q
     const uint4* sq = reinterpret_cast<const uint4*>(q + src * C);
     uint4* d = reinterpret_cast<uint4*>(dq + (int64_t)r * C);
     for (int i = lane; i < C / 16; i += 32) d[i] = sq[i];
-    for (int i = lane; i < C / 32; i += 32) ds[(int64_t)r * (C / 32) + i] = s[src * (C / 32) + i];
+    for (int i = lane; i < C / 32; i += 32) ds[(int64_t)i * R + r] = s[src * (C / 32) + i];
   }
 }
 
@@ -628,6 +638,27 @@ cudaError_t launch_gather_mx(const uint8_t* q, const uint8_t* s, int C, const in
                              dq, ds);
   note_launch();
   return e;
+}
+
+// Row-major scales [R][C/32] -> SFT [C/32][R]: thread per (row, block),
+// rows fastest so the stores are coalesced.
+__global__ void __launch_bounds__(256) k_sf_to_sft(const uint8_t* __restrict__ s, int nb, int64_t R,
+                                                   uint8_t* __restrict__ d) {
+  const int64_t total = R * nb;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i % R;
+    const int b = (int)(i / R);
+    d[(int64_t)b * R + r] = s[r * nb + b];
+  }
+}
+
+cudaError_t launch_sf_to_sft(const uint8_t* s, int C, int64_t R, uint8_t* d, cudaStream_t st) {
+  if (R == 0) return cudaSuccess;
+  const int64_t total = R * (C / 32);
+  const int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)device_sms() * 16);
+  k_sf_to_sft<<<blocks, 256, 0, st>>>(s, C / 32, R, d);
+  note_launch();
+  return cudaGetLastError();
 }
 
 }  // namespace moe

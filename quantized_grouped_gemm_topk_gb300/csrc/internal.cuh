@@ -152,6 +152,9 @@ cudaError_t launch_act_f16(const uint8_t* q, const uint8_t* s, int C, const int3
 // its B rows b_rows_per_group * e + n. Wgrad: A rows are the M gradient
 // rows, B rows the N gradient columns, and group e's K range is
 // poff[e] .. poff[e+1] (token axis, padded to 32 per group).
+// Every scale array the kernel reads or writes for another GEMM is stored
+// block-major ("SFT"): the scale of row r, K block b at [b * ld + r], so the
+// scales of consecutive rows are consecutive bytes.
 enum { kMxW1 = 0, kMxPlain = 1, kMxDswiglu = 2, kMxWgrad = 3 };
 struct MxArgs {
   int mode;
@@ -165,15 +168,18 @@ struct MxArgs {
   int64_t b_rows_per_group;
   const int32_t* offsets;       // [G + 1] token rows per group
   const int32_t* poff;          // [G + 1] 32-padded token rows per group
-  const uint8_t* a_sf; int64_t a_sf_ld; int64_t a_rows;   // A scales [a_rows][a_sf_ld]
-  const uint8_t* b_sf; int64_t b_sf_ld; int64_t b_rows;   // B scales [b_rows][b_sf_ld]
+  const uint8_t* a_sf; int64_t a_sf_ld; int64_t a_rows;   // A scales, SFT with ld = a_sf_ld; rows < a_rows exist
+  const uint8_t* b_sf; int64_t b_sf_ld; int64_t b_rows;   // B scales, SFT
   int64_t R;                    // token rows (A rows of the token-side modes)
   const float* w_row;           // [R] routing weight per row
   ActParams act;
   int I;
-  uint8_t* yq; uint8_t* ys;     // W1: y1 [R][I] (+[R][I/32]); Dswiglu: dh [R][2I] (+[R][2I/32])
+  uint8_t* yq;                  // W1: y1 codes [R][I]; Dswiglu: dh codes [R][2I]
+  uint8_t* ys;                  // W1: y1 scales [R][I/32] (row-major)
+  uint8_t* yst;                 // W1 (nullable): y1 scales again, SFT, ld R; Dswiglu: dh scales, SFT, ld R
   uint16_t* hsave;              // W1: h bf16 [R][2I] out (nullable); Dswiglu: h in
-  uint8_t* tq; uint8_t* ts; int64_t t_ld;   // transposed MXFP8 copy [features][t_ld] (+ scales); W1: nullable
+  uint8_t* tq; uint8_t* ts; int64_t t_ld; int t_nf;   // transposed MXFP8 copy: codes [t_nf][t_ld], scales SFT
+                                                       // [t_ld/32][t_nf]; W1: nullable
   uint16_t* out; int64_t out_ld;            // Plain: [R][out_ld]; Wgrad: [G][M][out_ld]
   float* dwpart;                // Dswiglu: [n_tiles][R]
   int32_t* status;
@@ -185,9 +191,13 @@ bool make_tmap_mx(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
 int mx_tile_n();
 int mx_tile_m();
 cudaError_t launch_gemm_mx(const MxArgs& g, const MxMaps& maps, int grid, cudaStream_t st);
-// dst rows r < min(R, offsets[G]) = MXFP8 rows src[row_map[r] / row_div].
+// dst rows r < min(R, offsets[G]) = MXFP8 rows src[row_map[r] / row_div];
+// the source scales are row-major [*][C/32], the destination's SFT
+// [C/32][R].
 cudaError_t launch_gather_mx(const uint8_t* q, const uint8_t* s, int C, const int32_t* row_map, int row_div, int R,
                              const int32_t* offsets, int G, uint8_t* dq, uint8_t* ds, cudaStream_t st);
+// Row-major scales [R][C/32] -> SFT [C/32][R].
+cudaError_t launch_sf_to_sft(const uint8_t* s, int C, int64_t R, uint8_t* d, cudaStream_t st);
 
 // W1 epilogue of the NVFP4 path: sums the S partials, y = w_row * act(g, u),
 // MXFP8 along I, and the f16 operand rows of W2.
@@ -215,15 +225,16 @@ cudaError_t launch_combine(const uint16_t* z, const int32_t* inv, const float* t
                            uint16_t* out, cudaStream_t st);
 
 // Transposed MXFP8 copy: for each group e and padded row p < pad(count_e),
-// dst[c][poff[e] + p] = MXFP8 along p (blocks of 32) of the value of row
-// offsets[e] + p (zero past count_e). Source rows: bf16 rows of src16 at
-// row_map[r] / row_div.
+// q[c][poff[e] + p] = MXFP8 along p (blocks of 32) of the value of row
+// offsets[e] + p (zero past count_e), its scale at s[(poff[e] + p) / 32 * C
+// + c] (block-major). Source rows: bf16 rows of src16 at row_map[r] /
+// row_div.
 struct ColQuantArgs {
   const uint16_t* src16; const int32_t* row_map; int row_div;
   int C;
   const int32_t* offsets; const int32_t* poff; int G;
   int64_t r_pad_max;                  // row length of dst
-  uint8_t* q; uint8_t* s;             // [C][r_pad_max], [C][r_pad_max/32]
+  uint8_t* q; uint8_t* s;             // [C][r_pad_max], [r_pad_max/32][C]
 };
 cudaError_t launch_quant_cols(const ColQuantArgs& a, cudaStream_t st);
 

@@ -79,8 +79,10 @@ __global__ void __launch_bounds__(256) k_unpack_nv(const uint8_t* __restrict__ s
 }
 
 // ---- MXFP8 ------------------------------------------------------------------
-// Codes: one thread per (group, packed row, 16-byte piece); scales: one
-// thread per (group, packed row, scale byte). Padding rows are zero.
+// Codes: one thread per (group, packed row, 16-byte piece), [G][NR][K];
+// scales: one thread per (group, packed row, scale byte), stored block-major
+// over all groups' rows, [K/32][G * NR], so the GEMM's scale loaders read
+// consecutive rows' scales as consecutive bytes. Padding rows are zero.
 __global__ void __launch_bounds__(256) k_prepack_mx(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s,
                                                     int G, int N, int K, int interleave_I, int NR,
                                                     uint8_t* __restrict__ dq, uint8_t* __restrict__ ds) {
@@ -101,7 +103,7 @@ __global__ void __launch_bounds__(256) k_prepack_mx(const uint8_t* __restrict__ 
     const int p = (int)((idx / spr) % NR);
     const int g = (int)(idx / ((int64_t)spr * NR));
     const int n = mx_pack_src_row(p, N, interleave_I);
-    ds[((int64_t)g * NR + p) * spr + b] = n >= 0 ? s[((int64_t)g * N + n) * spr + b] : (uint8_t)0;
+    ds[(int64_t)b * G * NR + (int64_t)g * NR + p] = n >= 0 ? s[((int64_t)g * N + n) * spr + b] : (uint8_t)0;
   }
 }
 
@@ -130,7 +132,7 @@ __global__ void __launch_bounds__(256) k_unpack_mx(const uint8_t* __restrict__ d
     const int b = (int)(idx % spr);
     const int n = (int)((idx / spr) % N);
     const int g = (int)(idx / ((int64_t)spr * N));
-    s[((int64_t)g * N + n) * spr + b] = ds[((int64_t)g * NR + packed_row(n)) * spr + b];
+    s[((int64_t)g * N + n) * spr + b] = ds[(int64_t)b * G * NR + (int64_t)g * NR + packed_row(n)];
   }
 }
 

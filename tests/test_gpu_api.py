@@ -252,7 +252,7 @@ def test_packed_layout_round_trip(name, which):
     if name == "tiny":
         s = inputs.workload("tiny", n_shared=1)
     else:
-        s = inputs.workload("train", T=8, E=3, H=320, I=128)
+        s = inputs.workload("train", T=8, E=5, H=320, I=128)
     cfg = m.config_from_shape(s, T_max=8)
     wts = inputs.gen_expert_weights(s, 0, device=dev)
     packed = m.moe_prepack_weights(cfg, wts, which)
