@@ -148,17 +148,17 @@ typedef struct moe_dispatch {
 
 /* Tensors the training forward saves for moe_layer_backward (device,
  * caller-owned; sizes from moe_train_sizes). Pad rows: every group's rows are
- * padded with zero rows to a multiple of 32; poff[e] is the padded offset. */
+ * padded with zero rows to a multiple of 128; poff[e] is the padded offset. */
 typedef struct moe_train_save {
     uint16_t* h;        /* [R, 2I] bf16 W1 output before the activation       */
     uint8_t* y1t_q;     /* [I, R_pad] MXFP8 of y (activation x routing weight)
                            quantised along the padded row axis               */
-    uint8_t* y1t_s;     /* [R_pad/32, I] its E8M0 scales, block-major: the
-                           scale of feature i, padded rows 32b..32b+31 at
-                           [b, i]                                             */
+    uint8_t* y1t_s;     /* [R_pad/128, I] 32-bit words of its E8M0 scales:
+                           byte j of word [w, i] is the scale of feature i,
+                           padded rows 32(4w+j) .. 32(4w+j)+31                */
     uint8_t* at_q;      /* [H, R_pad] MXFP8 of the gathered x rows, quantised
                            along the padded row axis                          */
-    uint8_t* at_s;      /* [R_pad/32, H] its scales, block-major as y1t_s     */
+    uint8_t* at_s;      /* [R_pad/128, H] words of its scales, as y1t_s       */
     int32_t* poff;      /* [G + 1] padded row offsets                         */
 } moe_train_save_t;
 
@@ -175,21 +175,31 @@ typedef struct moe_ws_view {
 /* ---- configuration, sizes ---------------------------------------------- */
 
 /* Host only. MOE_OK if the config is supported: H, I multiples of 64,
- * 1 <= k <= E, k' <= 32, G <= 2048, n_shared in {0, 1}, T_max >= 0. */
+ * 1 <= k <= E, k' <= 32, G <= 2048, n_shared in {0, 1}, T_max >= 0.
+ * Source: GC-MoE summary, Limitations (the Appendix A shape constraints:
+ * top-k plus the shared slot within 32, at most 2048 experts); the H / I
+ * multiples here follow this library's 64-wide K chunks, not the pages. */
 moe_status_t moe_config_validate(const moe_config_t* cfg);
 
-/* Host only. Bytes of workspace for calls with T <= T_max (cfg->T_max). */
+/* Host only. Bytes of workspace for calls with T <= T_max (cfg->T_max).
+ * Source: GC-MoE summary, Limitations (one workspace instance per operator;
+ * calls that share it are serialised). */
 moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* bytes);
 
 /* Host only. Carves the named buffers out of a workspace of at least
- * moe_workspace_size bytes at device address ws (no device access). */
+ * moe_workspace_size bytes at device address ws (no device access). The
+ * pages have no counterpart: an inspection aid of this library. */
 moe_status_t moe_workspace_view(const moe_config_t* cfg, void* ws, moe_ws_view_t* view);
 
-/* Host only. Bytes of the packed weight blob for `which`. */
+/* Host only. Bytes of the packed weight blob for `which`. Source: GC-MoE
+ * summary, Developer notes (weights converted once into the prepacked
+ * form). */
 moe_status_t moe_packed_weights_size(const moe_config_t* cfg, int which, size_t* bytes);
 
 /* Host only. Sizes of the training save buffers for T tokens: R_pad upper
- * bound (rows of the padded transposed copies). */
+ * bound (rows of the padded transposed copies). Source: NVIDIA blog, section
+ * on fusing MXFP8/NVFP4 quantisation (the transposed MXFP8 copies kept for
+ * the backward). */
 moe_status_t moe_train_sizes(const moe_config_t* cfg, int T, int64_t* r_pad_max);
 
 /* ---- S0 weight prepack (once, at load time) ------------------------------ */
@@ -217,7 +227,10 @@ moe_status_t moe_debug_unpack_weights(const moe_config_t* cfg, const void* packe
 /* ---- forward steps ------------------------------------------------------ */
 
 /* S1. logits [T, E] fp32 (device) = x [T, H] bf16 (device) . W_r [H, E] fp32
- * (device), fp32 accumulation. ws: the workspace (holds split partials). */
+ * (device), fp32 accumulation. ws: the workspace (holds split partials).
+ * Source: GC-MoE summary, Approach (role1 starts from the tokens' routing);
+ * the pages take the logits as given, and the router product x . W_r is the
+ * plainest step that produces them from the workloads' router weights. */
 moe_status_t moe_router_logits(const moe_config_t* cfg, const uint16_t* x, const float* W_r, int T,
                                float* logits, void* ws, void* stream);
 
@@ -247,27 +260,37 @@ moe_status_t moe_router_logits_noalloc(const moe_config_t* cfg, const uint16_t* 
  * offsets, permutation, inverse, row weights, and the MXFP8 copy of x
  * [T, H] bf16 (device). Outputs in *d (device buffers). Bit-exact and
  * deterministic: ties in the logits go to the lower expert id; rows of a
- * group keep increasing t*k' + j. T = 0 writes zero counts and offsets. */
+ * group keep increasing t*k' + j. T = 0 writes zero counts and offsets.
+ * Source: GC-MoE summary, Approach (role1 aggregates the routing counts and
+ * places the tokens into expert blocks); NVIDIA blog, section on removing
+ * host-device sync (per-group counts stay in device memory). */
 moe_status_t moe_route_dispatch(const moe_config_t* cfg, const float* logits, const uint16_t* x, int T,
                                 const moe_dispatch_t* d, void* ws, void* stream);
 
-/* S2 alone: top-k ids [T, k] and weights [T, k] from logits (device). */
+/* S2 alone: top-k ids [T, k] and weights [T, k] from logits (device).
+ * Source: GC-MoE summary, Approach (role1's top-k routing). */
 moe_status_t moe_route_topk(const moe_config_t* cfg, const float* logits, int T, int32_t* topk_ids,
                             float* topk_w, void* ws, void* stream);
 
 /* S3-S4 alone: dispatch from given top-k ids/weights (device) and x.
- * d->topk_ids / d->topk_w are read, the other fields of *d written. */
+ * d->topk_ids / d->topk_w are read, the other fields of *d written.
+ * Source: as moe_route_dispatch (device-side counts and token placement). */
 moe_status_t moe_dispatch(const moe_config_t* cfg, const uint16_t* x, int T, const moe_dispatch_t* d,
                           void* ws, void* stream);
 
 /* S5-S6. Grouped W1 over the dispatched rows with the fused epilogue
  * y1 = MXFP8(w_row * act(h[:, :I], h[:, I:])); y1_q [R, I], y1_s [R, I/32]
- * (device). save (nullable): training tensors h, y1t, at, poff. */
+ * (device). save (nullable): training tensors h, y1t, at, poff.
+ * Source: GC-MoE summary, Approach and Key contributions (W1's epilogue
+ * applies SwiGLU, the routing weight and the FP8 requantisation); NVIDIA
+ * blog, GLU epilogue section (gate and up columns of one tile meet in the
+ * epilogue) and MXFP8 section (the transposed copy). */
 moe_status_t moe_grouped_gemm_w1_swiglu_quant(const moe_config_t* cfg, const moe_dispatch_t* d, int T,
                                               const void* packed_w, uint8_t* y1_q, uint8_t* y1_s,
                                               const moe_train_save_t* save, void* ws, void* stream);
 
-/* S7. Grouped W2: z [R, H] bf16 (device) = y1 . W2_e, fp32 accumulation. */
+/* S7. Grouped W2: z [R, H] bf16 (device) = y1 . W2_e, fp32 accumulation.
+ * Source: GC-MoE summary, Approach (role2's W2 writes BF16 fragments). */
 moe_status_t moe_grouped_gemm_w2(const moe_config_t* cfg, const moe_dispatch_t* d, int T,
                                  const uint8_t* y1_q, const uint8_t* y1_s, const void* packed_w,
                                  uint16_t* z, void* ws, void* stream);
@@ -275,13 +298,17 @@ moe_status_t moe_grouped_gemm_w2(const moe_config_t* cfg, const moe_dispatch_t* 
 /* S8. out [T, H] bf16 (device): out[t] = bf16(sum_j c_j * z[inv[t*k'+j]])
  * summed in fp32 in slot order j = 0..k'-1, c_j = topk_w[t, j] for routed
  * slots and 1 for shared slots when topk_w is non-NULL, else c_j = 1 (the
- * routing weight was applied in the W1 epilogue). */
+ * routing weight was applied in the W1 epilogue). Source: GC-MoE summary,
+ * Approach (role3 combines the BF16 fragments of each token). */
 moe_status_t moe_combine(const moe_config_t* cfg, const uint16_t* z, const int32_t* inv, const float* topk_w,
                          int T, uint16_t* out, void* stream);
 
 /* Whole forward. Exactly one of W_r (router weights [H, E] fp32) and
  * logits_in ([T, E] fp32) is non-NULL. out [T, H] bf16. save nullable
- * (training). Intermediates live in ws (see moe_workspace_view). */
+ * (training). Intermediates live in ws (see moe_workspace_view). Source:
+ * GC-MoE summary, Approach (role1 dispatch, role2 W1 then W2, role3
+ * combine); NVIDIA blog, section on removing host-device sync (the whole
+ * layer captures into one CUDA graph). */
 moe_status_t moe_layer_forward(const moe_config_t* cfg, const uint16_t* x, const float* W_r,
                                const float* logits_in, int T, const void* packed_w, uint16_t* out,
                                const moe_train_save_t* save, void* ws, void* stream);
@@ -293,7 +320,9 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const uint16_t* x, const
  * the logical W1 layout (gate columns then up columns), dW2 [E, I, H] bf16,
  * dlogits [T, E] fp32. packed_w_dgrad: moe_prepack_weights(..., DGRAD, ...).
  * The router's own dense GEMM gradients (dlogits . W_r^T, x^T . dlogits) are
- * left to the caller. */
+ * left to the caller. Source: NVIDIA blog, kernel families (GroupGemm +
+ * dActivation + Quantize/Transpose) and the MXFP8 section (weight gradients
+ * from the transposed MXFP8 copies). */
 moe_status_t moe_layer_backward(const moe_config_t* cfg, const uint16_t* dout, const uint16_t* x, int T,
                                 const moe_train_save_t* save, const void* packed_w_dgrad, uint16_t* dx,
                                 uint16_t* dW1, uint16_t* dW2, float* dlogits, void* ws, void* stream);
@@ -301,16 +330,19 @@ moe_status_t moe_layer_backward(const moe_config_t* cfg, const uint16_t* dout, c
 /* ---- status --------------------------------------------------------------- */
 
 /* Synchronises `stream`, copies the workspace status word to *out (host) and
- * clears it. Not for use inside graph capture. */
+ * clears it. Not for use inside graph capture. The pages have no
+ * counterpart: device-side error reporting of this library. */
 moe_status_t moe_read_status(const moe_config_t* cfg, void* ws, int32_t* out, void* stream);
 
-/* Clears the workspace status word (enqueued on stream; capturable). */
+/* Clears the workspace status word (enqueued on stream; capturable). The
+ * pages have no counterpart. */
 moe_status_t moe_clear_status(const moe_config_t* cfg, void* ws, void* stream);
 
-/* Static description of a status code. */
+/* Static description of a status code. The pages have no counterpart. */
 const char* moe_status_string(moe_status_t s);
 
-/* Number of kernels the last host call enqueued (for launch accounting). */
+/* Number of kernels the last host call enqueued (for launch accounting).
+ * The pages have no counterpart. */
 int moe_last_launch_count(void);
 
 /* Optional phase timing for moe_layer_forward, per calling thread. With
@@ -322,7 +354,7 @@ int moe_last_launch_count(void);
  * NULL switches it off. Host only; the events must outlive the calls that
  * record them. A call made while its stream is being captured into a CUDA
  * graph records them as event-record nodes, so every replay of that graph
- * records them again. */
+ * records them again. The pages have no counterpart: a measurement aid. */
 #define MOE_N_PHASE_EVENTS 6
 moe_status_t moe_set_phase_events(void* const* events);
 

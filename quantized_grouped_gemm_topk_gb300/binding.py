@@ -349,9 +349,9 @@ def alloc_train_save(cfg, T, device="cuda"):
     bufs = {
         "h": torch.empty(max(R, 1), 2 * cfg.I, dtype=torch.int16, device=device),
         "y1t_q": torch.empty(cfg.I, rp, dtype=torch.uint8, device=device),
-        "y1t_s": torch.empty(rp // 32, cfg.I, dtype=torch.uint8, device=device),
+        "y1t_s": torch.empty(rp // 128, cfg.I, 4, dtype=torch.uint8, device=device),
         "at_q": torch.empty(cfg.H, rp, dtype=torch.uint8, device=device),
-        "at_s": torch.empty(rp // 32, cfg.H, dtype=torch.uint8, device=device),
+        "at_s": torch.empty(rp // 128, cfg.H, 4, dtype=torch.uint8, device=device),
         "poff": torch.empty(G + 1 + 3, dtype=torch.int32, device=device),
         "r_pad": rp,
     }

@@ -38,12 +38,12 @@ static Dims dims_of(const moe_config_t& c) {
   d.H = c.H; d.I = c.I; d.E = c.E; d.k = c.k; d.S = c.n_shared;
   d.kp = c.k + c.n_shared; d.G = c.E + c.n_shared; d.Tmax = c.T_max;
   d.Rmax = (int64_t)c.T_max * d.kp;
-  d.RpMax = (int64_t)align_up((size_t)(d.Rmax + 31LL * d.G), 32);
+  d.RpMax = (int64_t)align_up((size_t)(d.Rmax + (kPadRows - 1LL) * d.G), kPadRows);
   return d;
 }
 
 static int64_t r_pad_for(const Dims& d, int T) {
-  return (int64_t)align_up((size_t)((int64_t)T * d.kp + 31LL * d.G), 32);
+  return (int64_t)align_up((size_t)((int64_t)T * d.kp + (kPadRows - 1LL) * d.G), kPadRows);
 }
 
 static bool backward_capable(const moe_config_t& c) {
@@ -61,7 +61,7 @@ struct WsLayout {
   size_t status, logits, rpart, ids, wts, counts, offsets, touched, ntouch, poff, hist, base;
   size_t perm, inv, wrow, xq, xs, y1q, y1s, z;
   size_t P, a16, y16, rexp1, rexp2;                       // NVFP4 path
-  size_t xg, xgs, y1st;                                   // MXFP8 path: gathered x rows, y1 scales (SFT)
+  size_t xg, xgs, y1st;                                   // MXFP8 path: gathered x rows, y1 scales (SF4)
   size_t dzq, dzs, dzg, dzgs, dztq, dzts, dhq, dhs, dhtq, dhts, dxp, dwpart;   // backward
   size_t total;
 };
@@ -103,20 +103,20 @@ static WsLayout ws_layout(const moe_config_t& c) {
     L.rexp2 = take((size_t)R * 4);
   } else {
     L.xg = take((size_t)R * d.H);
-    L.xgs = take((size_t)R * d.H / 32);
-    L.y1st = take((size_t)R * d.I / 32);
+    L.xgs = take((size_t)sf4_bytes(d.H, R));
+    L.y1st = take((size_t)sf4_bytes(d.I, R));
   }
   if (backward_capable(c)) {
     L.dzq = take((size_t)T * d.H);
     L.dzs = take((size_t)T * d.H / 32);
     L.dzg = take((size_t)R * d.H);
-    L.dzgs = take((size_t)R * d.H / 32);
+    L.dzgs = take((size_t)sf4_bytes(d.H, R));
     L.dztq = take((size_t)d.H * d.RpMax);
-    L.dzts = take((size_t)d.H * d.RpMax / 32);
+    L.dzts = take((size_t)sf4_bytes(d.RpMax, d.H));
     L.dhq = take((size_t)R * 2 * d.I);
-    L.dhs = take((size_t)R * 2 * d.I / 32);
+    L.dhs = take((size_t)sf4_bytes(2 * d.I, R));
     L.dhtq = take((size_t)2 * d.I * d.RpMax);
-    L.dhts = take((size_t)2 * d.I * d.RpMax / 32);
+    L.dhts = take((size_t)sf4_bytes(d.RpMax, 2 * d.I));
     L.dxp = take((size_t)R * d.H * 2);
     L.dwpart = take((size_t)ceil_div(d.I, kMxTileN) * R * 4);
   }
@@ -168,9 +168,9 @@ static PackLayout pack_layout(const moe_config_t& c, int which) {
     P.rows1 = P.il1 > 0 ? ceil_div(P.il1, kMxTileN / 2) * kMxTileN : P.N1;
     P.rows2 = P.N2;
     P.off_w1 = o; o = align_up(o + (size_t)P.G * P.rows1 * P.K1, 256);
-    P.off_s1 = o; o = align_up(o + (size_t)P.G * P.rows1 * (P.K1 / 32), 256);
+    P.off_s1 = o; o = align_up(o + (size_t)sf4_bytes(P.K1, (int64_t)P.G * P.rows1), 256);
     P.off_w2 = o; o = align_up(o + (size_t)P.G * P.rows2 * P.K2, 256);
-    P.off_s2 = o; o = align_up(o + (size_t)P.G * P.rows2 * (P.K2 / 32), 256);
+    P.off_s2 = o; o = align_up(o + (size_t)sf4_bytes(P.K2, (int64_t)P.G * P.rows2), 256);
   }
   P.total = o;
   return P;
@@ -500,7 +500,7 @@ static int mx_grid(const moe_config_t& c) {
 }
 
 // Token-side block-scaled GEMM (modes kMxW1, kMxPlain, kMxDswiglu): A = the
-// MXFP8 rows aq [R][K] in group order with scales as (SFT [K/32][R]), B =
+// MXFP8 rows aq [R][K] in group order with scales as (SF4, ld R), B =
 // matrix `mat` of the packed MXFP8 blob; g carries the epilogue fields.
 static moe_status_t mx_token_gemm(const moe_config_t* c, MxArgs& g, int mode, const uint8_t* aq, const uint8_t* as,
                                   int64_t R, const void* packed, int which, int mat, const int32_t* offsets,
@@ -601,7 +601,7 @@ static moe_status_t w1_impl(const moe_config_t* c, const moe_dispatch_t* d, int 
 }
 
 // W2 on the MXFP8 path: z [R][H] bf16 straight from the block-scaled GEMM.
-// y1st: y1's scales in SFT layout ([I/32][R]); nullptr converts y1s (the
+// y1st: y1's scales in the SF4 layout (ld R); nullptr converts y1s (the
 // row-major [R][I/32] layout) into the workspace first.
 static moe_status_t w2_mx(const moe_config_t* c, const int32_t* offsets, int T, const uint8_t* y1q,
                           const uint8_t* y1s, const uint8_t* y1st, const void* packed, uint16_t* z, void* ws,
@@ -610,7 +610,7 @@ static moe_status_t w2_mx(const moe_config_t* c, const int32_t* offsets, int T, 
   const int64_t R = (int64_t)T * (c->k + c->n_shared);
   if (!y1st) {
     uint8_t* t = at<uint8_t>(ws, L.y1st);
-    MOE_CHECK_CUDA(launch_sf_to_sft(y1s, c->I, R, t, st));
+    MOE_CHECK_CUDA(launch_sf_to_sf4(y1s, c->I, R, t, st));
     y1st = t;
   }
   MxArgs g = mx_args0();

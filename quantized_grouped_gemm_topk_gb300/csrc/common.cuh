@@ -18,8 +18,8 @@ constexpr unsigned kFull = 0xffffffffu;
 // chunks.
 //   chunk: [granule g < 2][row p < 128][16 B of 32 E2M1 codes] (4096 B)
 //          then [row p][4 E4M3 scale codes, one per 16 K] (512 B).
-// MXFP8: plain K-major rows, codes [G][rows][K] and scales block-major
-//   [K/32][G * rows];
+// MXFP8: plain K-major rows, codes [G][rows][K] and scales in the SF4
+//   layout (below) over all groups' rows;
 //   W1's forward rows come in tiles of 192: 96 gate features then the same
 //   96 up features (zero rows past I), every other matrix in its own row
 //   order.
@@ -42,6 +42,20 @@ __host__ __device__ inline int mx_pack_src_row(int p, int N, int il) {
   if (f >= il) return -1;
   return pp < h ? f : il + f;
 }
+
+// Token rows of every expert group are padded to a multiple of this in the
+// transposed (token-axis) MXFP8 copies of the training path.
+constexpr int kPadRows = 128;
+
+// Scale layout of everything the block-scaled GEMM reads ("SF4"): 32-bit
+// words [ceil(K / 128)][ld rows]; byte j of the word of (w, row) is the E8M0
+// scale of K block 4 w + j of that row, so one coalesced 32-bit load per row
+// brings a whole 128-wide K stage of scales. sf4_at: byte offset of K block
+// kb of row; sf4_bytes: the array's size.
+__host__ __device__ inline int64_t sf4_at(int64_t kb, int64_t row, int64_t ld) {
+  return (((kb >> 2) * ld + row) << 2) + (kb & 3);
+}
+__host__ __device__ inline int64_t sf4_bytes(int64_t K, int64_t rows) { return (K / 32 + 3) / 4 * rows * 4; }
 
 struct PackHeader {            // first 256 bytes of a packed blob
   uint32_t magic;

@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(256) k_quant_cols(const ColQuantArgs a) {
     uint4* dst = reinterpret_cast<uint4*>(a.q + (int64_t)c * a.r_pad_max + prow);
     dst[0] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
     dst[1] = make_uint4(wds[4], wds[5], wds[6], wds[7]);
-    a.s[pb * a.C + c] = (uint8_t)(ex + 127);
+    a.s[sf4_at(pb, c, a.C)] = (uint8_t)(ex + 127);
   }
 }
 

@@ -36,11 +36,10 @@
 //                tail); commits free the stage and the scale slot; a tile's
 //                last commit hands its accumulator to the epilogue. Also
 //                allocates / frees tensor memory.
-//   warps 4-7    scale loaders: per stage, the four E8M0 scale bytes of each
-//                A and B row packed into one 32-bit word (byte j = K block
-//                j of the stage), written to an 8-slot scale ring in tensor
-//                memory. Four stages of scales are loaded ahead into
-//                registers.
+//   warps 4-7    scale loaders: per stage, one 32-bit word per A and B row
+//                (the four E8M0 scales of the stage's K blocks, SF4 layout)
+//                written to an 8-slot scale ring in tensor memory. Four
+//                stages of words are loaded ahead into registers.
 //   warps 8-15   two epilogue warpgroups; tiles alternate between them and
 //                between the two accumulator buffers, so a tile's epilogue
 //                overlaps the next tile's MMAs.
@@ -82,7 +81,7 @@ struct MxUnit {
   int a_row0, a_valid;    // first A row of the tile, rows of it that are real
   int b_row0;             // first B row of the tile
   int k0, klen;           // K range of the tile
-  int cnt, pad;           // the group's rows and their 32-padded count (token side)
+  int cnt, pad;           // the group's rows and their padded count (token side)
 };
 
 // Unit u -> (group, m-tile, n-tile) through the per-group m-tile prefix
@@ -107,7 +106,7 @@ __device__ __forceinline__ void mx_unit(const MxArgs& g, const int32_t* uoff, in
   } else {
     const int r0 = g.offsets[w.e];
     w.cnt = g.offsets[w.e + 1] - r0;
-    w.pad = (w.cnt + 31) & ~31;
+    w.pad = (w.cnt + kPadRows - 1) / kPadRows * kPadRows;
     w.a_row0 = r0 + w.mi * kMxBM;
     w.a_valid = min(kMxBM, w.cnt - w.mi * kMxBM);
     w.b_row0 = (int)((int64_t)w.e * g.b_rows_per_group) + w.ni * kMxBN;
@@ -118,16 +117,12 @@ __device__ __forceinline__ void mx_unit(const MxArgs& g, const int32_t* uoff, in
 
 __device__ __forceinline__ int mx_stages(int klen) { return (klen + kMxBK - 1) / kMxBK; }
 
-// The scale bytes of K blocks kb .. kb+kv-1 of one row of an SFT array
-// (col = the row's first byte, ld = the array's row count), packed
-// little-endian (block kb in the low byte); 0 past kv. Lanes holding
-// consecutive rows read consecutive bytes.
-__device__ __forceinline__ uint32_t load_sft4(const uint8_t* col, int64_t ld, int kb, int kv) {
-  uint32_t v = 0;
-#pragma unroll
-  for (int j = 0; j < 4; ++j)
-    if (j < kv) v |= (uint32_t)__ldg(col + (int64_t)(kb + j) * ld) << (8 * j);
-  return v;
+// The SF4 word (the scales of one 128-wide K stage) of one row: one 32-bit
+// load; lanes holding consecutive rows read consecutive words. Nothing
+// consumes the value until the stage's tensor-memory store, four stages
+// later, so the load's latency stays off the loader's path.
+__device__ __forceinline__ uint32_t load_sf4_word(const uint32_t* col, int64_t ld, int kw) {
+  return __ldg(col + (int64_t)kw * ld);
 }
 
 __device__ __forceinline__ uint32_t bf16x2_bits(float a, float b) {
@@ -155,13 +150,13 @@ __device__ __forceinline__ uint8_t quant_block32_store(const float (&v)[32], uin
 
 // Column quantiser of the transposed copies: the warp's 32 lanes are 32
 // consecutive padded rows (one MX block along the token axis) of feature f;
-// lane l writes the code of its row, lane 0 the block's scale (SFT: blocks
-// of the token axis major, nf features).
+// lane l writes the code of its row, lane 0 the block's scale (SF4, K = the
+// token axis, ld = nf features).
 __device__ __forceinline__ void quant_col_store(float v, uint8_t* tq, uint8_t* ts, int64_t f, int64_t ld, int nf,
                                                 int64_t p, int lane) {
   const int e = mx_exponent(warp_max(fabsf(v)));
   tq[f * ld + p] = (uint8_t)(f32x2_to_e4m3x2(v * pow2_neg(e), 0.f) & 0xffu);
-  if (lane == 0) ts[(p / 32) * nf + f] = (uint8_t)(e + 127);
+  if (lane == 0) ts[sf4_at(p / 32, f, nf)] = (uint8_t)(e + 127);
 }
 
 template <int MODE>
@@ -217,7 +212,7 @@ __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, ui
       if (rvalid) {
         const uint8_t sb = quant_block32_store(y, g.yq + row * g.I + f);
         g.ys[row * (g.I / 32) + f / 32] = sb;
-        if (g.yst) g.yst[(int64_t)(f / 32) * g.R + row] = sb;
+        if (g.yst) g.yst[sf4_at(f / 32, row, g.R)] = sb;
         if (g.hsave) {
           uint32_t hg[16], hu[16];
 #pragma unroll
@@ -278,8 +273,8 @@ __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, ui
           dg[i] = d.x;
           du[i] = d.y;
         }
-        g.yst[(int64_t)(f / 32) * g.R + row] = quant_block32_store(dg, g.yq + row * 2 * I + f);
-        g.yst[(int64_t)((I + f) / 32) * g.R + row] = quant_block32_store(du, g.yq + row * 2 * I + I + f);
+        g.yst[sf4_at(f / 32, row, g.R)] = quant_block32_store(dg, g.yq + row * 2 * I + f);
+        g.yst[sf4_at((I + f) / 32, row, g.R)] = quant_block32_store(du, g.yq + row * 2 * I + I + f);
       } else {
 #pragma unroll
         for (int i = 0; i < 32; ++i) dg[i] = du[i] = 0.f;
@@ -457,30 +452,32 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
       MxUnit w;
       mx_unit(g, uoff, u, w);
       const int nk = mx_stages(w.klen);
-      // first byte of each row's SFT column (nullptr: no such row)
-      const uint8_t* pa[4];
-      const uint8_t* pb[4 + kNB1];
+      // each row's SF4 column (nullptr: no such row)
+      const uint32_t* pa[4];
+      const uint32_t* pb[4 + kNB1];
+      const uint32_t* wa = reinterpret_cast<const uint32_t*>(g.a_sf);
+      const uint32_t* wb = reinterpret_cast<const uint32_t*>(g.b_sf);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int64_t ra = (int64_t)w.a_row0 + 32 * c + lane;
-        pa[c] = ra < g.a_rows ? g.a_sf + ra : nullptr;
+        pa[c] = ra < g.a_rows ? wa + ra : nullptr;
       }
 #pragma unroll
       for (int c = 0; c < 4 + kNB1; ++c) {
         const int64_t rb = (int64_t)w.b_row0 + 32 * c + lane;
-        pb[c] = rb < g.b_rows ? g.b_sf + rb : nullptr;
+        pb[c] = rb < g.b_rows ? wb + rb : nullptr;
       }
-      const int kb0 = w.k0 / 32;
+      const int kw0 = w.k0 / kMxBK;
       // four stages of scale words in flight in registers
       uint32_t va[4][4], vb[4][4 + kNB1];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
-        const int kv = j < nk ? min(4, (w.klen - j * kMxBK) / 32) : 0;
+        const bool live = j < nk;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) va[j][c] = (pa[c] && kv) ? load_sft4(pa[c], g.a_sf_ld, kb0 + 4 * j, kv) : 0u;
+        for (int c = 0; c < 4; ++c) va[j][c] = (pa[c] && live) ? load_sf4_word(pa[c], g.a_sf_ld, kw0 + j) : 0u;
 #pragma unroll
         for (int c = 0; c < 4 + kNB1; ++c)
-          vb[j][c] = (pb[c] && kv) ? load_sft4(pb[c], g.b_sf_ld, kb0 + 4 * j, kv) : 0u;
+          vb[j][c] = (pb[c] && live) ? load_sf4_word(pb[c], g.b_sf_ld, kw0 + j) : 0u;
       }
       for (int s0 = 0; s0 < nk; s0 += 4) {
 #pragma unroll
@@ -505,13 +502,13 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
               ++it;
               // refill this register slot with stage s + 4
               const int s4 = s + 4;
-              const int kv = s4 < nk ? min(4, (w.klen - s4 * kMxBK) / 32) : 0;
+              const bool live = s4 < nk;
 #pragma unroll
               for (int c = 0; c < 4; ++c)
-                va[j][c] = (pa[c] && kv) ? load_sft4(pa[c], g.a_sf_ld, kb0 + 4 * s4, kv) : 0u;
+                va[j][c] = (pa[c] && live) ? load_sf4_word(pa[c], g.a_sf_ld, kw0 + s4) : 0u;
 #pragma unroll
               for (int c = 0; c < 4 + kNB1; ++c)
-                vb[j][c] = (pb[c] && kv) ? load_sft4(pb[c], g.b_sf_ld, kb0 + 4 * s4, kv) : 0u;
+                vb[j][c] = (pb[c] && live) ? load_sf4_word(pb[c], g.b_sf_ld, kw0 + s4) : 0u;
             }
           }
         }
@@ -611,7 +608,7 @@ int mx_tile_m() { return kMxBM; }
 // ---------------------------------------------------------------------------
 // Row gather of MXFP8 rows: dst[r] = src[row_map[r] / row_div] (codes and
 // scales), r < min(R, offsets[G]). One warp per row, 16-byte copies; the
-// scales land block-major (SFT, ld R) for the GEMM's scale loaders.
+// scales land in the SF4 layout (ld R) for the GEMM's scale loaders.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_gather_mx(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int C,
                                                    const int32_t* __restrict__ row_map, int row_div, int R,
@@ -626,7 +623,12 @@ __global__ void __launch_bounds__(256) k_gather_mx(const uint8_t* __restrict__ q
     const uint4* sq = reinterpret_cast<const uint4*>(q + src * C);
     uint4* d = reinterpret_cast<uint4*>(dq + (int64_t)r * C);
     for (int i = lane; i < C / 16; i += 32) d[i] = sq[i];
-    for (int i = lane; i < C / 32; i += 32) ds[(int64_t)i * R + r] = s[src * (C / 32) + i];
+    const int nb = C / 32;
+    for (int wd = lane; wd < (nb + 3) / 4; wd += 32) {
+      uint32_t v = 0;
+      for (int j = 0; j < 4 && 4 * wd + j < nb; ++j) v |= (uint32_t)s[src * nb + 4 * wd + j] << (8 * j);
+      reinterpret_cast<uint32_t*>(ds)[(int64_t)wd * R + r] = v;
+    }
   }
 }
 
@@ -640,23 +642,26 @@ cudaError_t launch_gather_mx(const uint8_t* q, const uint8_t* s, int C, const in
   return e;
 }
 
-// Row-major scales [R][C/32] -> SFT [C/32][R]: thread per (row, block),
-// rows fastest so the stores are coalesced.
-__global__ void __launch_bounds__(256) k_sf_to_sft(const uint8_t* __restrict__ s, int nb, int64_t R,
-                                                   uint8_t* __restrict__ d) {
-  const int64_t total = R * nb;
+// Row-major scales [R][C/32] -> SF4 (ld R): thread per (row, word), rows
+// fastest so the word stores are coalesced.
+__global__ void __launch_bounds__(256) k_sf_to_sf4(const uint8_t* __restrict__ s, int nb, int64_t R,
+                                                   uint32_t* __restrict__ d) {
+  const int nw = (nb + 3) / 4;
+  const int64_t total = R * nw;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t r = i % R;
-    const int b = (int)(i / R);
-    d[(int64_t)b * R + r] = s[r * nb + b];
+    const int wd = (int)(i / R);
+    uint32_t v = 0;
+    for (int j = 0; j < 4 && 4 * wd + j < nb; ++j) v |= (uint32_t)s[r * nb + 4 * wd + j] << (8 * j);
+    d[(int64_t)wd * R + r] = v;
   }
 }
 
-cudaError_t launch_sf_to_sft(const uint8_t* s, int C, int64_t R, uint8_t* d, cudaStream_t st) {
+cudaError_t launch_sf_to_sf4(const uint8_t* s, int C, int64_t R, uint8_t* d, cudaStream_t st) {
   if (R == 0) return cudaSuccess;
-  const int64_t total = R * (C / 32);
+  const int64_t total = R * ((C / 32 + 3) / 4);
   const int blocks = (int)std::min<int64_t>((total + 255) / 256, (int64_t)device_sms() * 16);
-  k_sf_to_sft<<<blocks, 256, 0, st>>>(s, C / 32, R, d);
+  k_sf_to_sf4<<<blocks, 256, 0, st>>>(s, C / 32, R, reinterpret_cast<uint32_t*>(d));
   note_launch();
   return cudaGetLastError();
 }

@@ -151,10 +151,9 @@ cudaError_t launch_act_f16(const uint8_t* q, const uint8_t* s, int C, const int3
 // Dswiglu): group e's A rows are offsets[e] .. offsets[e+1] of the A buffer,
 // its B rows b_rows_per_group * e + n. Wgrad: A rows are the M gradient
 // rows, B rows the N gradient columns, and group e's K range is
-// poff[e] .. poff[e+1] (token axis, padded to 32 per group).
-// Every scale array the kernel reads or writes for another GEMM is stored
-// block-major ("SFT"): the scale of row r, K block b at [b * ld + r], so the
-// scales of consecutive rows are consecutive bytes.
+// poff[e] .. poff[e+1] (token axis, padded to kPadRows per group).
+// Every scale array the kernel reads, or writes for another GEMM, is in the
+// SF4 layout (common.cuh) with ld = the array's row count.
 enum { kMxW1 = 0, kMxPlain = 1, kMxDswiglu = 2, kMxWgrad = 3 };
 struct MxArgs {
   int mode;
@@ -167,19 +166,19 @@ struct MxArgs {
   int M, m_tiles;               // Wgrad: gradient rows and their 128-row tiles
   int64_t b_rows_per_group;
   const int32_t* offsets;       // [G + 1] token rows per group
-  const int32_t* poff;          // [G + 1] 32-padded token rows per group
-  const uint8_t* a_sf; int64_t a_sf_ld; int64_t a_rows;   // A scales, SFT with ld = a_sf_ld; rows < a_rows exist
-  const uint8_t* b_sf; int64_t b_sf_ld; int64_t b_rows;   // B scales, SFT
+  const int32_t* poff;          // [G + 1] padded token rows per group
+  const uint8_t* a_sf; int64_t a_sf_ld; int64_t a_rows;   // A scales, SF4 with ld = a_sf_ld; rows < a_rows exist
+  const uint8_t* b_sf; int64_t b_sf_ld; int64_t b_rows;   // B scales, SF4
   int64_t R;                    // token rows (A rows of the token-side modes)
   const float* w_row;           // [R] routing weight per row
   ActParams act;
   int I;
   uint8_t* yq;                  // W1: y1 codes [R][I]; Dswiglu: dh codes [R][2I]
   uint8_t* ys;                  // W1: y1 scales [R][I/32] (row-major)
-  uint8_t* yst;                 // W1 (nullable): y1 scales again, SFT, ld R; Dswiglu: dh scales, SFT, ld R
+  uint8_t* yst;                 // W1 (nullable): y1 scales again, SF4, ld R; Dswiglu: dh scales, SF4, ld R
   uint16_t* hsave;              // W1: h bf16 [R][2I] out (nullable); Dswiglu: h in
-  uint8_t* tq; uint8_t* ts; int64_t t_ld; int t_nf;   // transposed MXFP8 copy: codes [t_nf][t_ld], scales SFT
-                                                       // [t_ld/32][t_nf]; W1: nullable
+  uint8_t* tq; uint8_t* ts; int64_t t_ld; int t_nf;   // transposed MXFP8 copy: codes [t_nf][t_ld], scales SF4
+                                                       // (K = t_ld, ld = t_nf); W1: nullable
   uint16_t* out; int64_t out_ld;            // Plain: [R][out_ld]; Wgrad: [G][M][out_ld]
   float* dwpart;                // Dswiglu: [n_tiles][R]
   int32_t* status;
@@ -192,12 +191,11 @@ int mx_tile_n();
 int mx_tile_m();
 cudaError_t launch_gemm_mx(const MxArgs& g, const MxMaps& maps, int grid, cudaStream_t st);
 // dst rows r < min(R, offsets[G]) = MXFP8 rows src[row_map[r] / row_div];
-// the source scales are row-major [*][C/32], the destination's SFT
-// [C/32][R].
+// the source scales are row-major [*][C/32], the destination's SF4 (ld R).
 cudaError_t launch_gather_mx(const uint8_t* q, const uint8_t* s, int C, const int32_t* row_map, int row_div, int R,
                              const int32_t* offsets, int G, uint8_t* dq, uint8_t* ds, cudaStream_t st);
-// Row-major scales [R][C/32] -> SFT [C/32][R].
-cudaError_t launch_sf_to_sft(const uint8_t* s, int C, int64_t R, uint8_t* d, cudaStream_t st);
+// Row-major scales [R][C/32] -> SF4 (ld R).
+cudaError_t launch_sf_to_sf4(const uint8_t* s, int C, int64_t R, uint8_t* d, cudaStream_t st);
 
 // W1 epilogue of the NVFP4 path: sums the S partials, y = w_row * act(g, u),
 // MXFP8 along I, and the f16 operand rows of W2.
@@ -226,15 +224,15 @@ cudaError_t launch_combine(const uint16_t* z, const int32_t* inv, const float* t
 
 // Transposed MXFP8 copy: for each group e and padded row p < pad(count_e),
 // q[c][poff[e] + p] = MXFP8 along p (blocks of 32) of the value of row
-// offsets[e] + p (zero past count_e), its scale at s[(poff[e] + p) / 32 * C
-// + c] (block-major). Source rows: bf16 rows of src16 at row_map[r] /
-// row_div.
+// offsets[e] + p (zero past count_e), its scales in the SF4 layout (K =
+// the padded row axis, ld = C). Source rows: bf16 rows of src16 at
+// row_map[r] / row_div.
 struct ColQuantArgs {
   const uint16_t* src16; const int32_t* row_map; int row_div;
   int C;
   const int32_t* offsets; const int32_t* poff; int G;
   int64_t r_pad_max;                  // row length of dst
-  uint8_t* q; uint8_t* s;             // [C][r_pad_max], [r_pad_max/32][C]
+  uint8_t* q; uint8_t* s;             // [C][r_pad_max], SF4 [r_pad_max/128][C] words
 };
 cudaError_t launch_quant_cols(const ColQuantArgs& a, cudaStream_t st);
 

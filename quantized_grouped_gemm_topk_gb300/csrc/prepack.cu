@@ -80,14 +80,14 @@ __global__ void __launch_bounds__(256) k_unpack_nv(const uint8_t* __restrict__ s
 
 // ---- MXFP8 ------------------------------------------------------------------
 // Codes: one thread per (group, packed row, 16-byte piece), [G][NR][K];
-// scales: one thread per (group, packed row, scale byte), stored block-major
-// over all groups' rows, [K/32][G * NR], so the GEMM's scale loaders read
-// consecutive rows' scales as consecutive bytes. Padding rows are zero.
+// scales: one thread per (group, packed row, 4-block word), in the SF4
+// layout over all groups' rows (ld G * NR), so the GEMM's scale loaders read
+// one coalesced word per row and stage. Padding rows are zero.
 __global__ void __launch_bounds__(256) k_prepack_mx(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s,
                                                     int G, int N, int K, int interleave_I, int NR,
                                                     uint8_t* __restrict__ dq, uint8_t* __restrict__ ds) {
   const int cpr = K / 16, spr = K / 32;
-  const int64_t total_c = (int64_t)G * NR * cpr, total_s = (int64_t)G * NR * spr;
+  const int64_t total_c = (int64_t)G * NR * cpr;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total_c; idx += stride) {
     const int c = (int)(idx % cpr);
@@ -98,12 +98,18 @@ __global__ void __launch_bounds__(256) k_prepack_mx(const uint8_t* __restrict__ 
                            : make_uint4(0, 0, 0, 0);
     *reinterpret_cast<uint4*>(dq + ((int64_t)g * NR + p) * K + c * 16) = v;
   }
-  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total_s; idx += stride) {
-    const int b = (int)(idx % spr);
-    const int p = (int)((idx / spr) % NR);
-    const int g = (int)(idx / ((int64_t)spr * NR));
+  // scales: one thread per (group, packed row, 4-block word)
+  const int wpr = (spr + 3) / 4;
+  const int64_t total_w = (int64_t)G * NR * wpr;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total_w; idx += stride) {
+    const int p = (int)(idx % NR);
+    const int w = (int)((idx / NR) % wpr);
+    const int g = (int)(idx / ((int64_t)NR * wpr));
     const int n = mx_pack_src_row(p, N, interleave_I);
-    ds[(int64_t)b * G * NR + (int64_t)g * NR + p] = n >= 0 ? s[((int64_t)g * N + n) * spr + b] : (uint8_t)0;
+    uint32_t v = 0;
+    if (n >= 0)
+      for (int j = 0; j < 4 && 4 * w + j < spr; ++j) v |= (uint32_t)s[((int64_t)g * N + n) * spr + 4 * w + j] << (8 * j);
+    reinterpret_cast<uint32_t*>(ds)[(int64_t)w * G * NR + (int64_t)g * NR + p] = v;
   }
 }
 
@@ -132,7 +138,7 @@ __global__ void __launch_bounds__(256) k_unpack_mx(const uint8_t* __restrict__ d
     const int b = (int)(idx % spr);
     const int n = (int)((idx / spr) % N);
     const int g = (int)(idx / ((int64_t)spr * N));
-    s[((int64_t)g * N + n) * spr + b] = ds[(int64_t)b * G * NR + (int64_t)g * NR + packed_row(n)];
+    s[((int64_t)g * N + n) * spr + b] = ds[sf4_at(b, (int64_t)g * NR + packed_row(n), (int64_t)G * NR)];
   }
 }
 

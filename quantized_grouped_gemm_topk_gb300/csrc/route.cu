@@ -310,7 +310,7 @@ __device__ void block_excl_scan3(int32_t* a, int32_t* b, int32_t* c, int n, int3
 }
 
 // From per-block histograms: counts, offsets, per-block bases, the list of
-// groups with rows (increasing id), and 32-row padded offsets.
+// groups with rows (increasing id), and padded offsets (kPadRows rows).
 // One block of 1024 threads; smem: 3 * (G + 1) + 99 ints.
 __device__ void scan_groups(const int32_t* hist, int NB, int G, int32_t* counts, int32_t* offsets,
                             int32_t* base, int32_t* touched, int32_t* n_touched, int32_t* poff, int32_t* sm) {
@@ -324,7 +324,7 @@ __device__ void scan_groups(const int32_t* hist, int NB, int G, int32_t* counts,
     counts[e] = c;
     off[e] = c;
     flag[e] = c > 0;
-    pad[e] = (c + 31) & ~31;
+    pad[e] = (c + kPadRows - 1) / kPadRows * kPadRows;
   }
   __syncthreads();
   int tot, ntouch, ptot;
