@@ -523,7 +523,7 @@ static moe_status_t mx_token_gemm(const moe_config_t* c, MxArgs& g, int mode, co
   g.status = status;
   MxMaps maps;
   if (!make_tmap_mx(&maps.a, aq, R, K, mx_tile_m()) ||
-      !make_tmap_mx(&maps.b, b + (mat == 1 ? P.off_w1 : P.off_w2), (int64_t)P.G * rows, K, mx_tile_n()))
+      !make_tmap_mx(&maps.b, b + (mat == 1 ? P.off_w1 : P.off_w2), (int64_t)P.G * rows, K, mx_b_box_rows()))
     return MOE_ERR_CUDA;
   MOE_CHECK_CUDA(launch_gemm_mx(g, maps, mx_grid(*c), st));
   return MOE_OK;
@@ -774,7 +774,7 @@ static moe_status_t mx_wgrad(const moe_config_t* c, const uint8_t* pq, const uin
   g.out = out; g.out_ld = N;
   g.status = status;
   MxMaps maps;
-  if (!make_tmap_mx(&maps.a, pq, M, Rp, mx_tile_m()) || !make_tmap_mx(&maps.b, qq, N, Rp, mx_tile_n()))
+  if (!make_tmap_mx(&maps.a, pq, M, Rp, mx_tile_m()) || !make_tmap_mx(&maps.b, qq, N, Rp, mx_b_box_rows()))
     return MOE_ERR_CUDA;
   MOE_CHECK_CUDA(launch_gemm_mx(g, maps, mx_grid(*c), st));
   return MOE_OK;

@@ -13,10 +13,6 @@
 
 namespace moe {
 
-static int grid_for(int64_t warps, int warps_per_block) {
-  int64_t b = (warps + warps_per_block - 1) / warps_per_block;
-  return (int)std::max<int64_t>(1, std::min<int64_t>(b, device_sms() * 32));
-}
 
 // ---- W1 epilogue (NVFP4 path) --------------------------------------------------
 // One CTA per row r: a warp per 32-block of I sums the K-slice partials,
@@ -205,60 +201,74 @@ cudaError_t launch_combine(const uint16_t* z, const int32_t* inv, const float* t
 }
 
 // ---- transposed MXFP8 copies ---------------------------------------------------
-// warp per (padded 32-row block, 32 columns); lane = column.
+// One CTA per padded 32-row block (grid-stride): the block's group is found
+// once, the source row of each of its 32 rows is staged in shared memory,
+// then the warps stride over 32-column chunks, lane = column: each lane
+// gathers its column's 32 values (every row read is one coalesced 64-byte
+// segment across the warp), quantises them along the row axis and writes
+// 32 code bytes and its column's scale byte.
 __global__ void __launch_bounds__(256) k_quant_cols(const ColQuantArgs a) {
-  const int lane = threadIdx.x & 31;
+  __shared__ int64_t src_row[32];
+  __shared__ int blk_e;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   const int ncc = (a.C + 31) / 32;
   const int64_t npb = a.r_pad_max / 32;
   const int ptot = a.poff[a.G];
-  const int64_t total = npb * ncc;
-  const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
-  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); w < total; w += nw) {
-    const int64_t pb = w / ncc;
-    const int cc = (int)(w % ncc);
+  for (int64_t pb = blockIdx.x; pb < npb; pb += gridDim.x) {
     const int prow = (int)(pb * 32);
-    if (prow >= ptot) continue;
-    int lo = 0, hi = a.G - 1;          // group with poff[e] <= prow < poff[e+1]
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (a.poff[mid] <= prow) lo = mid; else hi = mid - 1;
+    if (prow >= ptot) break;                 // blocks are visited in increasing order
+    __syncthreads();                         // the previous block's staging is no longer read
+    if (threadIdx.x == 0) {
+      int lo = 0, hi = a.G - 1;              // group with poff[e] <= prow < poff[e+1]
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.poff[mid] <= prow) lo = mid; else hi = mid - 1;
+      }
+      blk_e = lo;
     }
-    const int e = lo;
+    __syncthreads();
+    const int e = blk_e;
     const int cnt = a.offsets[e + 1] - a.offsets[e];
     const int p0 = prow - a.poff[e];
-    const int c = cc * 32 + lane;
-    const bool cok = c < a.C;
-    float v[32];
-    float am = 0.f;
+    if (threadIdx.x < 32) {
+      const int i = threadIdx.x;
+      src_row[i] = p0 + i < cnt ? (int64_t)(a.row_map[a.offsets[e] + p0 + i] / a.row_div) : -1;
+    }
+    __syncthreads();
+    for (int cc = warp; cc < ncc; cc += nwarps) {
+      const int c = cc * 32 + lane;
+      const bool cok = c < a.C;
+      float v[32];
+      float am = 0.f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float x = 0.f;
-      if (cok && p0 + i < cnt) {
-        const int64_t r = a.offsets[e] + p0 + i;
-        x = bf16_bits_to_f32(a.src16[(int64_t)(a.row_map[r] / a.row_div) * a.C + c]);
+      for (int i = 0; i < 32; ++i) {
+        const int64_t sr = src_row[i];
+        const float x = (cok && sr >= 0) ? bf16_bits_to_f32(a.src16[sr * a.C + c]) : 0.f;
+        v[i] = x;
+        am = fmaxf(am, fabsf(x));
       }
-      v[i] = x;
-      am = fmaxf(am, fabsf(x));
-    }
-    if (!cok) continue;
-    const int ex = mx_exponent(am);
-    const float sc = pow2_neg(ex);
-    uint32_t wds[8];
+      if (!cok) continue;
+      const int ex = mx_exponent(am);
+      const float sc = pow2_neg(ex);
+      uint32_t wds[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      wds[q] = (uint32_t)f32x2_to_e4m3x2(v[4 * q] * sc, v[4 * q + 1] * sc) |
-               ((uint32_t)f32x2_to_e4m3x2(v[4 * q + 2] * sc, v[4 * q + 3] * sc) << 16);
+      for (int q = 0; q < 8; ++q) {
+        wds[q] = (uint32_t)f32x2_to_e4m3x2(v[4 * q] * sc, v[4 * q + 1] * sc) |
+                 ((uint32_t)f32x2_to_e4m3x2(v[4 * q + 2] * sc, v[4 * q + 3] * sc) << 16);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(a.q + (int64_t)c * a.r_pad_max + prow);
+      dst[0] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+      dst[1] = make_uint4(wds[4], wds[5], wds[6], wds[7]);
+      a.s[sf4_at(pb, c, a.C)] = (uint8_t)(ex + 127);
     }
-    uint4* dst = reinterpret_cast<uint4*>(a.q + (int64_t)c * a.r_pad_max + prow);
-    dst[0] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
-    dst[1] = make_uint4(wds[4], wds[5], wds[6], wds[7]);
-    a.s[sf4_at(pb, c, a.C)] = (uint8_t)(ex + 127);
   }
 }
 
 cudaError_t launch_quant_cols(const ColQuantArgs& a, cudaStream_t st) {
   if (a.r_pad_max == 0) return cudaSuccess;
-  k_quant_cols<<<grid_for((a.r_pad_max / 32) * ((a.C + 31) / 32), 8), 256, 0, st>>>(a);
+  const int64_t npb = a.r_pad_max / 32;
+  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(npb, (int64_t)device_sms() * 8));
+  k_quant_cols<<<blocks, 256, 0, st>>>(a);
   note_launch();
   return cudaGetLastError();
 }

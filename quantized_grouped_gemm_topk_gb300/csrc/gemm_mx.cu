@@ -29,9 +29,14 @@
 // are prepacked so a 192-column tile holds 96 gate features and the same 96
 // up features.
 //
+// With clusters (kMxCl > 1), the CTAs of a cluster take consecutive
+// 128-row tiles of the same group and the same 192-column B tile; each CTA
+// copies its part of the B tile and multicasts it into all of them, and a
+// stage slot is refilled only after the MMAs of every CTA released it.
 // Roles (one CTA per SM, persistent over the work units):
 //   warp 0       TMA producer: per stage one 2-D tensor copy of the A tile
-//                and one of the B tile (128-byte swizzle) into a 5-stage ring.
+//                and one of the B tile (or its cluster part, multicast),
+//                128-byte swizzle, into a 5-stage ring.
 //   warp 1       MMA issuer: per stage 4 block-scaled MMAs (fewer at a K
 //                tail); commits free the stage and the scale slot; a tile's
 //                last commit hands its accumulator to the epilogue. Also
@@ -60,6 +65,12 @@ constexpr int kMxBM = 128;
 constexpr int kMxBN = 192;
 constexpr int kMxBK = 128;
 constexpr int kMxStages = 5;
+// CTAs per cluster. With 2, a pair takes two m-tiles sharing one B tile and
+// multicasts it (28 KB per CTA-stage from L2 instead of 40 KB); measured on
+// the training shapes it ran 5-10% slower than 1 (the mainloop is not
+// bound by L2 read bandwidth), so 1 is the default.
+constexpr int kMxCl = 1;
+constexpr int kMxBHalf = kMxBN / kMxCl;           // B rows each CTA of the pair loads (multicast to both)
 constexpr int kMxSfSlots = 8;
 constexpr int kMxThreads = 512;
 constexpr int kMxWProd = 0, kMxWMma = 1, kMxWSf = 4, kMxWEpi = 8;
@@ -84,9 +95,10 @@ struct MxUnit {
   int cnt, pad;           // the group's rows and their padded count (token side)
 };
 
-// Unit u -> (group, m-tile, n-tile) through the per-group m-tile prefix
-// sums uoff (shared memory).
-__device__ __forceinline__ void mx_unit(const MxArgs& g, const int32_t* uoff, int u, MxUnit& w) {
+// Unit u of the cluster -> (group, m-tile pair, n-tile) through the
+// per-group prefix sums of m-tile pairs uoff (shared memory); the CTA of
+// cluster rank `rank` takes m-tile 2 * pair + rank.
+__device__ __forceinline__ void mx_unit(const MxArgs& g, const int32_t* uoff, int u, int rank, MxUnit& w) {
   const int ui = u / g.n_tiles;
   w.ni = u - ui * g.n_tiles;
   int lo = 0, hi = g.G - 1;   // last e with uoff[e] <= ui
@@ -95,7 +107,7 @@ __device__ __forceinline__ void mx_unit(const MxArgs& g, const int32_t* uoff, in
     if (uoff[mid] <= ui) lo = mid; else hi = mid - 1;
   }
   w.e = lo;
-  w.mi = ui - uoff[lo];
+  w.mi = kMxCl * (ui - uoff[lo]) + rank;
   if (g.mode == kMxWgrad) {
     w.a_row0 = w.mi * kMxBM;
     w.a_valid = min(kMxBM, g.M - w.a_row0);
@@ -148,15 +160,37 @@ __device__ __forceinline__ uint8_t quant_block32_store(const float (&v)[32], uin
   return (uint8_t)(e + 127);
 }
 
-// Column quantiser of the transposed copies: the warp's 32 lanes are 32
-// consecutive padded rows (one MX block along the token axis) of feature f;
-// lane l writes the code of its row, lane 0 the block's scale (SF4, K = the
-// token axis, ld = nf features).
-__device__ __forceinline__ void quant_col_store(float v, uint8_t* tq, uint8_t* ts, int64_t f, int64_t ld, int nf,
-                                                int64_t p, int lane) {
-  const int e = mx_exponent(warp_max(fabsf(v)));
-  tq[f * ld + p] = (uint8_t)(f32x2_to_e4m3x2(v * pow2_neg(e), 0.f) & 0xffu);
-  if (lane == 0) ts[sf4_at(p / 32, f, nf)] = (uint8_t)(e + 127);
+// Column quantiser of the transposed copies, 32 features at a time: the
+// warp's 32 lanes are 32 consecutive padded rows (one MX block along the
+// token axis), v[i] is the lane's value of feature f0 + i (0 where the row
+// is padding). A reduce-scatter butterfly (16 + 8 + 4 + 2 + 1 shuffles)
+// leaves in lane i the block maximum of feature f0 + i; its scale is
+// broadcast back one feature at a time. Lane l writes the codes of its row,
+// lane i the scale byte of feature f0 + i (SF4, K = the token axis, ld =
+// nf features).
+__device__ __forceinline__ void quant_cols32(const float (&v)[32], uint8_t* tq, uint8_t* ts, int64_t f0, int64_t ld,
+                                             int nf, int64_t p, int lane) {
+  float m[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) m[i] = fabsf(v[i]);
+#pragma unroll
+  for (int h = 16; h >= 1; h >>= 1) {
+    const bool up = (lane & h) != 0;
+#pragma unroll
+    for (int j = 0; j < h; ++j) {
+      const float send = up ? m[j] : m[j + h];
+      const float keep = up ? m[j + h] : m[j];
+      m[j] = fmaxf(keep, __shfl_xor_sync(kFull, send, h));
+    }
+  }
+  const int e = mx_exponent(m[0]);
+  const float sc_mine = pow2_neg(e);
+  ts[sf4_at(p / 32, f0 + lane, nf)] = (uint8_t)(e + 127);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float sc = __shfl_sync(kFull, sc_mine, i);
+    tq[(f0 + i) * ld + p] = (uint8_t)(f32x2_to_e4m3x2(v[i] * sc, 0.f) & 0xffu);
+  }
 }
 
 template <int MODE>
@@ -230,10 +264,11 @@ __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, ui
         }
       }
       if (tblk) {
-        const bool live = rel < w.cnt;
+        if (rel >= w.cnt) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          quant_col_store(live ? y[i] : 0.f, g.tq, g.ts, f + i, g.t_ld, g.t_nf, p, lane);
+          for (int i = 0; i < 32; ++i) y[i] = 0.f;      // padding rows of the group
+        }
+        quant_cols32(y, g.tq, g.ts, f, g.t_ld, g.t_nf, p, lane);
       }
     }
   } else {   // kMxDswiglu: columns = dY1 for features f0 + c
@@ -280,15 +315,23 @@ __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, ui
         for (int i = 0; i < 32; ++i) dg[i] = du[i] = 0.f;
       }
       if (tblk) {
+        if (!live) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          quant_col_store(live ? dg[i] : 0.f, g.tq, g.ts, f + i, g.t_ld, g.t_nf, p, lane);
-          quant_col_store(live ? du[i] : 0.f, g.tq, g.ts, (int64_t)I + f + i, g.t_ld, g.t_nf, p, lane);
+          for (int i = 0; i < 32; ++i) dg[i] = du[i] = 0.f;   // padding rows of the group
         }
+        quant_cols32(dg, g.tq, g.ts, f, g.t_ld, g.t_nf, p, lane);
+        quant_cols32(du, g.tq, g.ts, (int64_t)I + f, g.t_ld, g.t_nf, p, lane);
       }
     }
     if (rvalid) g.dwpart[(int64_t)w.ni * g.R + row] = dw;
   }
+}
+
+// m-tile pairs of group e (the cluster's unit height).
+template <int MODE>
+__device__ __forceinline__ int mx_pairs(const MxArgs& g, int e) {
+  const int mt = MODE == kMxWgrad ? g.m_tiles : (g.offsets[e + 1] - g.offsets[e] + kMxBM - 1) / kMxBM;
+  return (mt + kMxCl - 1) / kMxCl;
 }
 
 template <int MODE>
@@ -319,7 +362,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
   }
   __syncthreads();
   if (bad_pack) return;   // the blob is not the packing this GEMM reads: write nothing
-  // per-group m-tile prefix sums (a block-wide scan of ceil(rows / 128))
+  // per-group prefix sums of m-tile pairs (a block-wide scan)
   {
     __shared__ int32_t wsum[kMxThreads / 32];
     const int G = g.G;
@@ -327,7 +370,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
     const int lo = threadIdx.x * per, hi = min(G, lo + per);
     int s = 0;
     for (int e = lo; e < hi; ++e)
-      s += MODE == kMxWgrad ? g.m_tiles : (g.offsets[e + 1] - g.offsets[e] + kMxBM - 1) / kMxBM;
+      s += mx_pairs<MODE>(g, e);
     int incl = s;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -341,14 +384,14 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
     int run = base + incl - s;
     for (int e = lo; e < hi; ++e) {
       uoff[e] = run;
-      run += MODE == kMxWgrad ? g.m_tiles : (g.offsets[e + 1] - g.offsets[e] + kMxBM - 1) / kMxBM;
+      run += mx_pairs<MODE>(g, e);
     }
     if (threadIdx.x == kMxThreads - 1) uoff[G] = base + incl;
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kMxStages; ++i) {
       tc::mbar_init(&full[i], 1);
-      tc::mbar_init(&empty[i], 1);
+      tc::mbar_init(&empty[i], kMxCl);   // released by the MMAs of both CTAs of the pair
     }
     for (int i = 0; i < kMxSfSlots; ++i) {
       tc::mbar_init(&sffull[i], 4);    // one elected arrive per scale-loader warp
@@ -365,9 +408,13 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
   if (warp == kMxWMma) tc::tmem_alloc(tmem_slot, kMxTmemCols);
   tc::fence_before_sync();
   __syncthreads();
+  // the peers' barriers are initialised before any copy or commit reaches them
+  if constexpr (kMxCl > 1) tc::cluster_sync();
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
   const int U = uoff[g.G] * g.n_tiles;
+  const int rank = kMxCl > 1 ? (int)tc::cluster_rank() : 0;
+  const int cid = blockIdx.x / kMxCl, ncl = gridDim.x / kMxCl;
 
   if (warp == kMxWProd) {
     // ---------------- TMA producer ----------------
@@ -376,9 +423,9 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
       tc::prefetch_tmap(&maps.b);
       uint32_t it = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
+      for (int u = cid; ok && u < U; u += ncl) {
         MxUnit w;
-        mx_unit(g, uoff, u, w);
+        mx_unit(g, uoff, u, rank, w);
         const int nk = mx_stages(w.klen);
         for (int s = 0; s < nk; ++s, ++it) {
           const int slot = it % kMxStages;
@@ -386,7 +433,13 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
           tc::mbar_arrive_expect_tx(&full[slot], kMxStageBytes);
           const int kx = w.k0 + s * kMxBK;
           tc::tma_load_2d_plain(sa + slot * kMxAStage, &maps.a, kx, w.a_row0, &full[slot]);
-          tc::tma_load_2d_plain(sb + slot * kMxBStage, &maps.b, kx, w.b_row0, &full[slot]);
+          if constexpr (kMxCl > 1) {
+            // this CTA's part of the shared B tile, into every CTA of the cluster
+            tc::tma_load_2d_mc(sb + slot * kMxBStage + rank * (kMxBHalf * kMxBK), &maps.b, kx,
+                               w.b_row0 + rank * kMxBHalf, &full[slot], (uint16_t)((1u << kMxCl) - 1));
+          } else {
+            tc::tma_load_2d_plain(sb + slot * kMxBStage, &maps.b, kx, w.b_row0, &full[slot]);
+          }
         }
       }
       if (!ok || *abort) {
@@ -405,9 +458,9 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
     if (lane == 0) {
       uint32_t it = 0, tcount = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < U; u += gridDim.x, ++tcount) {
+      for (int u = cid; ok && u < U; u += ncl, ++tcount) {
         MxUnit w;
-        mx_unit(g, uoff, u, w);
+        mx_unit(g, uoff, u, rank, w);
         const int nk = mx_stages(w.klen);
         const int d = tcount & 1;
         if (!tc::mbar_wait(&accempty[d], ((tcount >> 1) & 1) ^ 1, abort)) { ok = false; break; }
@@ -426,7 +479,8 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
           for (int j = 0; j < kv; ++j)
             tc::mma_mx_ss(dt, ad + 2 * j, bd + 2 * j, tc::idesc_mx_e4m3(kMxBM, kMxBN, j, j), sfa, sfb,
                           (s | j) != 0 ? 1u : 0u);
-          tc::mma_commit(&empty[slot]);
+          if constexpr (kMxCl > 1) tc::mma_commit_mc(&empty[slot], (uint16_t)((1u << kMxCl) - 1));
+          else tc::mma_commit(&empty[slot]);
           tc::mma_commit(&sfempty[fs]);
         }
         if (!ok) break;
@@ -448,9 +502,9 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
     static_assert(kNB1 == 2, "B's second group holds rows 128-191");
     uint32_t it = 0;
     bool ok = true;
-    for (int u = blockIdx.x; ok && u < U; u += gridDim.x) {
+    for (int u = cid; ok && u < U; u += ncl) {
       MxUnit w;
-      mx_unit(g, uoff, u, w);
+      mx_unit(g, uoff, u, rank, w);
       const int nk = mx_stages(w.klen);
       // each row's SF4 column (nullptr: no such row)
       const uint32_t* pa[4];
@@ -521,10 +575,10 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
     const int q = warp & 3;
     const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + wg * kMxBN;
     uint32_t tcount = 0, mine = 0;
-    for (int u = blockIdx.x; u < U; u += gridDim.x, ++tcount) {
+    for (int u = cid; u < U; u += ncl, ++tcount) {
       if ((int)(tcount & 1) != wg) continue;
       MxUnit w;
-      mx_unit(g, uoff, u, w);
+      mx_unit(g, uoff, u, rank, w);
       const bool got = tc::mbar_wait(&accfull[wg], mine & 1, abort);
       if (!__all_sync(kFull, got)) break;
       tc::fence_after_sync();
@@ -538,6 +592,17 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
 
   tc::fence_before_sync();
   __syncthreads();
+  if constexpr (kMxCl > 1) {
+    if (*abort) {
+      // a CTA that gave up may have copies into its peers still in flight:
+      // give them time to land (bounded) before the cluster can leave
+      const long long t0 = clock64();
+      while (clock64() - t0 < 100000) {
+      }
+    }
+    // no CTA leaves while a peer may still multicast into it or arrive on it
+    tc::cluster_sync();
+  }
   if (threadIdx.x == 0 && *abort) set_status(g.status, MOE_DEV_TIMEOUT);
   if (warp == kMxWMma) {
     tc::fence_after_sync();
@@ -580,11 +645,40 @@ bool make_tmap_mx(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
 }
 
 template <int MODE>
-static cudaError_t launch_mx_t(const MxArgs& g, const MxMaps& maps, int grid, cudaStream_t st) {
+static cudaError_t launch_mx_t(const MxArgs& g, const MxMaps& maps, int grid_cap, cudaStream_t st) {
   static std::atomic<bool> done[kMaxDevices] = {};
+  static std::atomic<int> max_clusters[kMaxDevices] = {};
   cudaError_t e = set_smem_once((const void*)k_gemm_mx<MODE>, kMxSmemBytes, done);
   if (e != cudaSuccess) return e;
-  return launch_pdl(k_gemm_mx<MODE>, dim3(grid), dim3(kMxThreads), (size_t)kMxSmemBytes, st, g, maps);
+  int dev = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(kMxThreads);
+  cfg.dynamicSmemBytes = kMxSmemBytes;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kMxCl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  // clusters that fit on the device at once (pairs of SMs of one GPC),
+  // queried once per device
+  const bool slot = dev >= 0 && dev < kMaxDevices;
+  int nc = slot ? max_clusters[dev].load() : 0;
+  if (nc <= 0) {
+    cfg.gridDim = dim3(kMxCl * 64);
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&nc, k_gemm_mx<MODE>, &cfg) != cudaSuccess || nc <= 0)
+      nc = std::max(1, device_sms() / kMxCl);
+    if (slot) max_clusters[dev].store(nc);
+  }
+  const int ncl = std::max(1, std::min(nc, grid_cap / kMxCl));
+  cfg.gridDim = dim3(ncl * kMxCl);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, k_gemm_mx<MODE>, g, maps);
 }
 
 cudaError_t launch_gemm_mx(const MxArgs& g, const MxMaps& maps, int grid, cudaStream_t st) {
@@ -603,6 +697,7 @@ cudaError_t launch_gemm_mx(const MxArgs& g, const MxMaps& maps, int grid, cudaSt
 }
 
 int mx_tile_n() { return kMxBN; }
+int mx_b_box_rows() { return kMxBHalf; }
 int mx_tile_m() { return kMxBM; }
 
 // ---------------------------------------------------------------------------

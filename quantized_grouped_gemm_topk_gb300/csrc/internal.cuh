@@ -184,10 +184,11 @@ struct MxArgs {
   int32_t* status;
 };
 struct MxMaps {
-  CUtensorMap a, b;             // boxes of 128 K-bytes x 128 (A) / 192 (B) rows
+  CUtensorMap a, b;             // boxes of 128 K-bytes x 128 (A) / mx_b_box_rows() (B) rows
 };
 bool make_tmap_mx(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows);
 int mx_tile_n();
+int mx_b_box_rows();          // rows of B per tensor copy (each CTA of a pair copies this many)
 int mx_tile_m();
 cudaError_t launch_gemm_mx(const MxArgs& g, const MxMaps& maps, int grid, cudaStream_t st);
 // dst rows r < min(R, offsets[G]) = MXFP8 rows src[row_map[r] / row_div];
