@@ -32,6 +32,7 @@ Parity pins: tests/test_oracle_moe.py and tests/test_oracle_backward.py.
 from __future__ import annotations
 
 import dataclasses
+import math
 
 import numpy as np
 
@@ -117,14 +118,30 @@ def sigmoid(v):
     return 1.0 / (1.0 + np.exp(-v))
 
 
+def gelu_cdf(v):
+    """Phi(v), the standard normal CDF, = (1 + erf(v / sqrt 2)) / 2."""
+    v = np.asarray(v, np.float64)
+    return 0.5 * (1.0 + np.vectorize(math.erf, otypes=[np.float64])(v / math.sqrt(2.0)))
+
+
+def gelu_pdf(v):
+    """phi(v) = exp(-v^2 / 2) / sqrt(2 pi)."""
+    v = np.asarray(v, np.float64)
+    return np.exp(-0.5 * v * v) / math.sqrt(2.0 * math.pi)
+
+
 def act_fwd(g, u, act="swiglu", alpha=1.0, limit=0.0):
-    """SwiGLU with b = c = 0: Swish_beta(g) * u = g * sigmoid(beta*g) * u.
-    'swiglu' uses beta = 1; 'swiglu_clamp' clamps g and u to [-limit, limit]
-    first and uses beta = alpha."""
+    """The gated activations the blog's fused kernels support (NVIDIA blog,
+    kernel families: SwiGLU, GeGLU), with b = c = 0:
+    'swiglu'        Swish_1(g) * u = g * sigmoid(g) * u;
+    'swiglu_clamp'  g and u clamped to [-limit, limit] first, Swish_alpha;
+    'geglu'         GELU(g) * u with the exact GELU(v) = v * Phi(v)."""
     g = np.asarray(g, np.float64)
     u = np.asarray(u, np.float64)
     if act == "swiglu":
         return g * sigmoid(g) * u
+    if act == "geglu":
+        return g * gelu_cdf(g) * u
     gc = np.clip(g, -limit, limit)
     uc = np.clip(u, -limit, limit)
     return gc * sigmoid(alpha * gc) * uc
@@ -138,6 +155,9 @@ def act_bwd(g, u, d, act="swiglu", alpha=1.0, limit=0.0):
     if act == "swiglu":
         s = sigmoid(g)
         return d * (s + g * s * (1.0 - s)) * u, d * g * s
+    if act == "geglu":
+        c = gelu_cdf(g)
+        return d * (c + g * gelu_pdf(g)) * u, d * g * c
     gc = np.clip(g, -limit, limit)
     uc = np.clip(u, -limit, limit)
     s = sigmoid(alpha * gc)

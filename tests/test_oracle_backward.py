@@ -23,8 +23,9 @@ def _setup(act, S=0, rs=1.0):
     w1 = rng.normal(0, 0.6, (G, 2 * I, H))
     w2 = rng.normal(0, 0.6, (G, H, I))
     dout = rng.normal(0, 1, (T, H))
+    clamp = act == "swiglu_clamp"
     kw = dict(E=E, k=k, n_shared=S, routed_scale=rs, act=act,
-              alpha=1.702 if act != "swiglu" else 1.0, limit=1.5 if act != "swiglu" else 0.0)
+              alpha=1.702 if clamp else 1.0, limit=1.5 if clamp else 0.0)
     return x, logits, w1, w2, dout, kw
 
 
@@ -33,7 +34,8 @@ def _loss(x, logits, w1, w2, dout, kw):
     return float((f.out * dout).sum())
 
 
-@pytest.mark.parametrize("act,S,rs", [("swiglu", 0, 1.0), ("swiglu_clamp", 0, 1.0), ("swiglu", 1, 2.5)])
+@pytest.mark.parametrize("act,S,rs", [("swiglu", 0, 1.0), ("swiglu_clamp", 0, 1.0), ("swiglu", 1, 2.5),
+                                      ("geglu", 0, 1.0)])
 def test_backward_matches_finite_differences(act, S, rs):
     x, logits, w1, w2, dout, kw = _setup(act, S, rs)
     f = M.layer_forward(x, logits, {"w1_f64": w1, "w2_f64": w2}, quant=False, **kw)

@@ -40,6 +40,31 @@ def test_swiglu_clamp_closed_forms():
     assert dg[0] == 0.0 and du[1] == 0.0 and dg[1] != 0.0 and du[0] != 0.0
 
 
+def test_geglu_closed_forms():
+    """GELU(v) = v * Phi(v): Phi(0) = 1/2, Phi(1) = 0.8413447460685429 (the
+    normal table), Phi(-1) = 1 - Phi(1); GELU(g) * u -> g * u as g -> +inf
+    and -> 0 as g -> -inf."""
+    kw = dict(act="geglu")
+    assert M.act_fwd(0.0, 3.0, **kw) == 0.0
+    assert M.act_fwd(2.0, 0.0, **kw) == 0.0
+    assert M.act_fwd(1.0, 1.0, **kw) == pytest.approx(0.8413447460685429, abs=1e-15)
+    assert M.act_fwd(-1.0, 2.0, **kw) == pytest.approx(-2.0 * (1.0 - 0.8413447460685429), abs=1e-15)
+    assert M.act_fwd(2.0, 1.5, **kw) == pytest.approx(3.0 * 0.9772498680518208, rel=1e-15)   # Phi(2)
+    assert M.act_fwd(12.0, 0.5, **kw) == pytest.approx(6.0, rel=1e-15)
+    assert M.act_fwd(-12.0, 0.5, **kw) == pytest.approx(0.0, abs=1e-15)
+
+
+def test_geglu_derivative_closed_form():
+    """d/dg [g Phi(g) u] = u (Phi(g) + g phi(g)), d/du = g Phi(g); at g = 1:
+    Phi(1) + phi(1) = 0.8413447460685429 + 0.24197072451914337 (the normal
+    density at 1); at g = 0 the gate derivative is 1/2."""
+    dg, du = M.act_bwd(1.0, 2.0, 1.0, "geglu")
+    assert dg == pytest.approx(2.0 * (0.8413447460685429 + 0.24197072451914337), rel=1e-14)
+    assert du == pytest.approx(0.8413447460685429, rel=1e-14)
+    dg0, du0 = M.act_bwd(0.0, -3.0, 2.0, "geglu")
+    assert dg0 == pytest.approx(2.0 * 0.5 * -3.0, rel=1e-15) and du0 == 0.0
+
+
 def test_swiglu_derivative_closed_form():
     # d/dg [g s(g) u] = u (s + g s (1 - s)); d/du = g s(g)
     g, u = 0.7, -1.3
@@ -138,7 +163,7 @@ def _tiny_case(act="swiglu", wfmt="nvfp4", S=0, rs=1.0, T=16):
 
 
 @pytest.mark.parametrize("act,wfmt,S,rs", [("swiglu", "nvfp4", 0, 1.0), ("swiglu", "nvfp4", 1, 2.5),
-                                          ("swiglu_clamp", "mxfp8", 0, 1.0)])
+                                          ("swiglu_clamp", "mxfp8", 0, 1.0), ("geglu", "nvfp4", 0, 1.0)])
 def test_routed_equals_dense_formulation(act, wfmt, S, rs):
     s, xb, lg, wts = _tiny_case(act, wfmt, S, rs)
     kw = dict(E=s.E, k=s.k, n_shared=S, routed_scale=rs, act=s.act, alpha=s.alpha, limit=s.limit, wfmt=wfmt)
