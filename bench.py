@@ -102,11 +102,12 @@ def host_cpu():
 
 
 def kernel_source_sha():
-    """Hash of the decode GEMM kernel's sources with comments and whitespace
-    removed, so a recorded ncu traffic figure stays tied to the code that was
-    captured and a comment edit does not void it."""
+    """Hash of the decode GEMM kernel's own sources (its file, the tensor-core
+    wrappers, its argument struct) with comments and whitespace removed, so a
+    recorded ncu traffic figure stays tied to the code that was captured and
+    a comment edit does not void it."""
     h = hashlib.sha256()
-    for f in ("gemm_tc.cu", "tc.cuh", "common.cuh", "internal.cuh"):
+    for f in ("gemm_tc.cu", "tc.cuh", "internal.cuh"):
         src = open(os.path.join(ROOT, "quantized_grouped_gemm_topk_gb300", "csrc", f)).read()
         src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
         src = re.sub(r"//[^\n]*", "", src)
@@ -491,10 +492,13 @@ def bench_skewed(m, dev, K, warmup, flush, hbm, bf16):
     return res
 
 
-def bench_train(m, dev, K, warmup, bf16):
+def bench_train(m, dev, K, warmup, bf16, T=None, E=None):
     """Training forward + backward (MXFP8 x MXFP8 on the block-scaled tensor
-    cores). Weights (3.2 GB) and activations exceed L2, so no flush."""
+    cores). Weights (3.2 GB) and activations exceed L2, so no flush. T / E
+    override the workload's sizes (smaller profiling cases)."""
     s = inputs.workload("train")
+    if T or E:
+        s = inputs.workload("train", T=T or s.T, E=E or s.E)
     T = s.T
     cfg = m.config_from_shape(s, T_max=T)
     wts = inputs.gen_expert_weights(s, 0, device=dev)
@@ -555,6 +559,23 @@ def bench_train(m, dev, K, warmup, bf16):
     del packed, packed_d, ws, bufs, dW1, dW2
     torch.cuda.empty_cache()
     return res
+
+
+def run_only(args, local):
+    """One workload of the per-config block alone (profiling runs); prints
+    its block as one JSON line."""
+    m = load_lib()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    hbm, bf16, _, _ = peaks()
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    if args.only == "shared":
+        res = bench_shared_decode(m, dev, args.steps, args.warmup, flush, hbm)
+    elif args.only == "skewed":
+        res = bench_skewed(m, dev, args.steps, args.warmup, flush, hbm, bf16)
+    else:
+        res = bench_train(m, dev, args.steps, args.warmup, bf16, args.train_T, args.train_E)
+    print(json.dumps(res), flush=True)
 
 
 def run_ours(args, s, rank, world, local):
@@ -651,6 +672,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="headline workload only")
     ap.add_argument("--E", type=int, default=0, help="override the expert count (small profiling cases)")
+    ap.add_argument("--only", default="", choices=["", "shared", "skewed", "train"],
+                    help="run one workload of the per-config block alone (profiling)")
+    ap.add_argument("--train-T", type=int, default=0, help="training tokens for --only train")
+    ap.add_argument("--train-E", type=int, default=0, help="training experts for --only train")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -661,6 +686,9 @@ def main():
         s = inputs.workload(args.workload, E=args.E)
     if args.impl == "reference":
         run_reference(args, s, rank, world)
+        return
+    if args.only:
+        run_only(args, local)
         return
     if world > 1:
         torch.cuda.set_device(local)

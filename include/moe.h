@@ -89,7 +89,7 @@ typedef enum moe_status {
 #define MOE_DEV_BAD_PACK 0x4      /* packed weight blob header mismatch      */
 #define MOE_DEV_TIMEOUT 0x8       /* a kernel gave up waiting on itself      */
 
-enum { MOE_ACT_SWIGLU = 0, MOE_ACT_SWIGLU_CLAMP = 1 };
+enum { MOE_ACT_SWIGLU = 0, MOE_ACT_SWIGLU_CLAMP = 1, MOE_ACT_GEGLU = 2 };
 enum { MOE_WFMT_NVFP4 = 0, MOE_WFMT_MXFP8 = 1 };
 enum { MOE_PACK_FORWARD = 0, MOE_PACK_DGRAD = 1 };
 
@@ -98,6 +98,11 @@ enum { MOE_PACK_FORWARD = 0, MOE_PACK_DGRAD = 1 };
  * act = MOE_ACT_SWIGLU_CLAMP:  g' = clamp(g, -act_limit, act_limit),
  *                              u' = clamp(u, -act_limit, act_limit),
  *                              act = g' * sigmoid(act_alpha * g') * u'
+ * act = MOE_ACT_GEGLU:         act(g, u) = GELU(g) * u, GELU(v) = v * Phi(v)
+ *                              with Phi the standard normal CDF (exact erf
+ *                              form). The gated activations are those the
+ *                              NVIDIA blog's fused kernels list (kernel
+ *                              families: SwiGLU, GeGLU, with clamping). 
  * weight_fmt = MOE_WFMT_NVFP4: E2M1 elements, E4M3 scale per 16 along K,
  *                              fp32 scale per (group, matrix)
  * weight_fmt = MOE_WFMT_MXFP8: E4M3 elements, E8M0 scale per 32 along K */

@@ -51,7 +51,7 @@ class MoEShape:
     k: int
     n_shared: int = 0
     routed_scale: float = 1.0
-    act: str = "swiglu"          # "swiglu" | "swiglu_clamp"
+    act: str = "swiglu"          # "swiglu" | "swiglu_clamp" | "geglu"
     alpha: float = 1.0
     limit: float = 0.0
     wfmt: str = "nvfp4"          # "nvfp4" | "mxfp8"

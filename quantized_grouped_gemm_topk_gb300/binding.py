@@ -23,7 +23,8 @@ MOE_DEV_BAD_EXPERT_ID = 0x1
 MOE_DEV_NAN_LOGIT = 0x2
 MOE_DEV_BAD_PACK = 0x4
 MOE_DEV_TIMEOUT = 0x8
-MOE_ACT_SWIGLU, MOE_ACT_SWIGLU_CLAMP = 0, 1
+MOE_ACT_SWIGLU, MOE_ACT_SWIGLU_CLAMP, MOE_ACT_GEGLU = 0, 1, 2
+ACTS = {"swiglu": MOE_ACT_SWIGLU, "swiglu_clamp": MOE_ACT_SWIGLU_CLAMP, "geglu": MOE_ACT_GEGLU}
 MOE_WFMT_NVFP4, MOE_WFMT_MXFP8 = 0, 1
 MOE_PACK_FORWARD, MOE_PACK_DGRAD = 0, 1
 
@@ -146,7 +147,7 @@ def _require_cuda():
 def make_config(H, I, E, k, n_shared=0, T_max=0, act="swiglu", alpha=1.0, limit=0.0, routed_scale=1.0,
                 wfmt="nvfp4", max_sms=0) -> moe_config_t:
     return moe_config_t(H, I, E, k, n_shared, T_max,
-                        MOE_ACT_SWIGLU if act == "swiglu" else MOE_ACT_SWIGLU_CLAMP,
+                        ACTS[act],
                         float(alpha), float(limit), float(routed_scale),
                         MOE_WFMT_NVFP4 if wfmt == "nvfp4" else MOE_WFMT_MXFP8, max_sms)
 

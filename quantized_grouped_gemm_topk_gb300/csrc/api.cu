@@ -223,7 +223,8 @@ moe_status_t moe_config_validate(const moe_config_t* c) {
   if (c->n_shared < 0 || c->n_shared > 1) return MOE_ERR_INVALID_ARG;
   if (c->k + c->n_shared > 32 || c->E + c->n_shared > 2048) return MOE_ERR_INVALID_ARG;
   if (c->T_max < 0) return MOE_ERR_INVALID_ARG;
-  if (c->act != MOE_ACT_SWIGLU && c->act != MOE_ACT_SWIGLU_CLAMP) return MOE_ERR_INVALID_ARG;
+  if (c->act != MOE_ACT_SWIGLU && c->act != MOE_ACT_SWIGLU_CLAMP && c->act != MOE_ACT_GEGLU)
+    return MOE_ERR_INVALID_ARG;
   if (c->act == MOE_ACT_SWIGLU_CLAMP && !(c->act_limit > 0.f)) return MOE_ERR_INVALID_ARG;
   if (c->weight_fmt != MOE_WFMT_NVFP4 && c->weight_fmt != MOE_WFMT_MXFP8) return MOE_ERR_INVALID_ARG;
   if (!(c->routed_scale > 0.f)) return MOE_ERR_INVALID_ARG;
@@ -538,7 +539,7 @@ static MxArgs mx_args0() {
 static ActParams act_params(const moe_config_t* c) {
   ActParams p;
   p.act = c->act;
-  p.alpha = c->act == MOE_ACT_SWIGLU ? 1.f : c->act_alpha;
+  p.alpha = c->act == MOE_ACT_SWIGLU_CLAMP ? c->act_alpha : 1.f;
   p.limit = c->act_limit;
   return p;
 }

@@ -154,10 +154,19 @@ struct ActParams {
   float alpha, limit;
 };
 
-__device__ __forceinline__ float sigmoidf_(float v) { return 1.0f / (1.0f + expf(-v)); }
+// Logistic sigmoid with the fast exponential and divide intrinsics: relative
+// error ~1e-6, far inside the layer's tolerance, and several times cheaper
+// than the IEEE forms in the epilogues that evaluate it per element.
+__device__ __forceinline__ float sigmoidf_(float v) { return __fdividef(1.0f, 1.0f + __expf(-v)); }
+
+// Phi(v), the standard normal CDF, and phi(v), its density (CUDA's erff /
+// expf).
+__device__ __forceinline__ float normal_cdf(float v) { return 0.5f * (1.0f + erff(v * 0.70710678118654752f)); }
+__device__ __forceinline__ float normal_pdf(float v) { return 0.39894228040143268f * expf(-0.5f * v * v); }
 
 __device__ __forceinline__ float act_fwd(float g, float u, const ActParams& p) {
   if (p.act == MOE_ACT_SWIGLU) return g * sigmoidf_(g) * u;
+  if (p.act == MOE_ACT_GEGLU) return g * normal_cdf(g) * u;
   float gc = fminf(fmaxf(g, -p.limit), p.limit);
   float uc = fminf(fmaxf(u, -p.limit), p.limit);
   return gc * sigmoidf_(p.alpha * gc) * uc;
@@ -169,12 +178,39 @@ __device__ __forceinline__ float2 act_bwd(float g, float u, float d, const ActPa
     float s = sigmoidf_(g);
     return make_float2(d * (s + g * s * (1.0f - s)) * u, d * g * s);
   }
+  if (p.act == MOE_ACT_GEGLU) {
+    const float c = normal_cdf(g);
+    return make_float2(d * (c + g * normal_pdf(g)) * u, d * g * c);
+  }
   float gc = fminf(fmaxf(g, -p.limit), p.limit);
   float uc = fminf(fmaxf(u, -p.limit), p.limit);
   float s = sigmoidf_(p.alpha * gc);
   float dg = (g >= -p.limit && g <= p.limit) ? d * (s + p.alpha * gc * s * (1.0f - s)) * uc : 0.0f;
   float du = (u >= -p.limit && u <= p.limit) ? d * gc * s : 0.0f;
   return make_float2(dg, du);
+}
+
+// act(g, u) and the gradients (dg, du) of d * act(g, u) in one evaluation
+// (the backward epilogue needs both; the sigmoid / normal CDF is computed
+// once). Same values as act_fwd / act_bwd.
+__device__ __forceinline__ float3 act_fwd_bwd(float g, float u, float d, const ActParams& p) {
+  if (p.act == MOE_ACT_SWIGLU) {
+    const float s = sigmoidf_(g);
+    const float gs = g * s;
+    return make_float3(gs * u, d * (s + gs * (1.0f - s)) * u, d * gs);
+  }
+  if (p.act == MOE_ACT_GEGLU) {
+    const float c = normal_cdf(g);
+    const float gc = g * c;
+    return make_float3(gc * u, d * (c + g * normal_pdf(g)) * u, d * gc);
+  }
+  const float gc = fminf(fmaxf(g, -p.limit), p.limit);
+  const float uc = fminf(fmaxf(u, -p.limit), p.limit);
+  const float s = sigmoidf_(p.alpha * gc);
+  const float gs = gc * s;
+  const float dg = (g >= -p.limit && g <= p.limit) ? d * (s + p.alpha * gs * (1.0f - s)) * uc : 0.0f;
+  const float du = (u >= -p.limit && u <= p.limit) ? d * gs : 0.0f;
+  return make_float3(gs * uc, dg, du);
 }
 
 // Programmatic dependent launch. Every kernel of the forward chain first

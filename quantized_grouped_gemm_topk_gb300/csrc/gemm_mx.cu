@@ -303,10 +303,10 @@ __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, ui
           const float gg = __uint_as_float(i & 1 ? gw & 0xffff0000u : gw << 16);
           const float uu = __uint_as_float(i & 1 ? uw & 0xffff0000u : uw << 16);
           const float dy = __uint_as_float(dv[i]);
-          dw = fmaf(dy, act_fwd(gg, uu, g.act), dw);
-          const float2 d = act_bwd(gg, uu, wr * dy, g.act);
-          dg[i] = d.x;
-          du[i] = d.y;
+          const float3 a = act_fwd_bwd(gg, uu, wr * dy, g.act);
+          dw = fmaf(dy, a.x, dw);
+          dg[i] = a.y;
+          du[i] = a.z;
         }
         g.yst[sf4_at(f / 32, row, g.R)] = quant_block32_store(dg, g.yq + row * 2 * I + f);
         g.yst[sf4_at((I + f) / 32, row, g.R)] = quant_block32_store(du, g.yq + row * 2 * I + I + f);

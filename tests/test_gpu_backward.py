@@ -50,9 +50,10 @@ def _oracle_backward(s, r, f, dout, experts=None):
                             quant=True, experts=experts, w1t=w1t, w2t=w2t)
 
 
-def test_train_reduced_full_check():
+@pytest.mark.parametrize("act", ["swiglu_clamp", "geglu"])
+def test_train_reduced_full_check(act):
     dev = cuda_device()
-    s = inputs.workload("train", T=48, E=8)
+    s = inputs.workload("train", T=48, E=8, act=act)
     r = run_forward(s, s.T, dev=dev, save=True)
     f = oracle_forward(s, r)
     assert (np_(r["views"]["topk_ids"]) == f.ids).all()

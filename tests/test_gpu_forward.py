@@ -173,3 +173,21 @@ def test_route_topk_exact_ties(T, E, k):
     assert list(np_(ids)[0]) == list(range(k))
     np.testing.assert_allclose(np_(w), ref_w, rtol=1e-6, atol=0)
     assert m.moe_read_status(cfg, ws) == 0
+
+
+@pytest.mark.parametrize("name", ["tiny", "train"])
+def test_geglu_forward(name):
+    """GeGLU (GELU(gate) * up) through both GEMM paths: the NVFP4 decode GEMM
+    with its epilogue kernel, and the block-scaled MXFP8 GEMM with the fused
+    epilogue."""
+    dev = cuda_device()
+    if name == "tiny":
+        s = inputs.workload("tiny", act="geglu")
+    else:
+        s = inputs.workload("train", T=40, E=8, act="geglu")
+    r = run_forward(s, s.T, dev=dev, seed=4)
+    assert r["status"] == 0
+    f = oracle_forward(s, r)
+    _check_dispatch(s, r, f)
+    assert_mx_close(np_(r["views"]["y1_q"]), np_(r["views"]["y1_s"]), f.y1q, f.y1s, "y1")
+    assert_close_layer(np_(r["out"].float()), f.out, "out")
