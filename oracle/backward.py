@@ -133,3 +133,42 @@ def layer_backward(fwd: Forward, x_bits, dout_bits, wts: dict, *, E: int, k: int
         dsel = p * (dp - (p * dp).sum())
         dlogits[t, fwd.ids[t]] = dsel
     return Backward(dx, dW1, dW2, dlogits, dw_row, dh, dY1)
+
+
+# ---------------------------------------------------------------------------
+# NVFP4 training recipe: per-tensor amax of the activation output and of its
+# transposed Hadamard rotation (NVIDIA blog "Boosting MoE training
+# throughput with advanced fusion kernels", section on fusing MXFP8/NVFP4
+# quantisation: for NVFP4 the kernel emits the output's per-tensor amax for
+# the forward and, for the backward, the amax of the Hadamard rotation of
+# the transposed output).
+# Reading taken: the rotation is the normalised Sylvester Hadamard matrix of
+# order 16, H16 / 4, applied along the token axis in blocks of 16
+# consecutive rows of one expert, the expert's rows zero-padded to a
+# multiple of 16 (no random sign flips: the page names a Hadamard rotation).
+# ---------------------------------------------------------------------------
+def sylvester_hadamard(n: int) -> np.ndarray:
+    """Sylvester's construction: H1 = [1], H2m = [[Hm, Hm], [Hm, -Hm]]."""
+    h = np.ones((1, 1))
+    while h.shape[0] < n:
+        h = np.block([[h, h], [h, -h]])
+    return h
+
+
+def nvfp4_amax(y: np.ndarray, offsets: np.ndarray):
+    """(max |y|, max over experts e, 16-row blocks and features of
+    |(H16 / 4) @ block|) for y [R, I] in expert order, offsets [G + 1]."""
+    y = np.asarray(y, np.float64)
+    amax = float(np.abs(y).max(initial=0.0))
+    h = sylvester_hadamard(16) / 4.0
+    amax_t = 0.0
+    for e in range(len(offsets) - 1):
+        blk = y[offsets[e]:offsets[e + 1]]
+        n = blk.shape[0]
+        if n == 0:
+            continue
+        pad = np.zeros(((n + 15) // 16 * 16, y.shape[1]))
+        pad[:n] = blk
+        rot = np.einsum("ij,bjf->bif", h, pad.reshape(-1, 16, y.shape[1]))
+        amax_t = max(amax_t, float(np.abs(rot).max()))
+    return amax, amax_t

@@ -171,3 +171,31 @@ def test_backward_reads_bf16_rounded_h():
     assert bw.dh[0, I] == pytest.approx(s1, abs=1e-15)     # du = g * sigmoid(g) at g = 1
     exact = (1.0 + 2.0 ** -10) / (1.0 + np.exp(-(1.0 + 2.0 ** -10)))
     assert abs(bw.dw_row[0] - exact) > 5e-4
+
+
+def test_sylvester_hadamard_matches_the_bit_parity_formula():
+    """Two constructions of H16 agree: Sylvester's recursion and the closed
+    form H[i, j] = (-1)^popcount(i & j); H H^T = 16 I."""
+    h = B.sylvester_hadamard(16)
+    ref = np.array([[(-1) ** bin(i & j).count("1") for j in range(16)] for i in range(16)], np.float64)
+    assert np.array_equal(h, ref)
+    assert np.array_equal(h @ h.T, 16 * np.eye(16))
+
+
+def test_nvfp4_amax_closed_forms():
+    """One expert, one feature: a constant block c rotates to (4c, 0, ..., 0)
+    (amax 4|c|); a single nonzero v rotates to sixteen values of magnitude
+    |v|/4; rows of different experts never share a block (the second expert's
+    single row is zero-padded to its own block)."""
+    c = 0.75
+    y = np.full((16, 1), c)
+    assert B.nvfp4_amax(y, np.array([0, 16])) == (c, 4 * c)
+    y = np.zeros((16, 2)); y[5, 1] = -3.0
+    assert B.nvfp4_amax(y, np.array([0, 16])) == (3.0, 0.75)
+    # 15 rows of 1.0 in expert 0 and one row of 1.0 in expert 1: expert 0's
+    # padded block rotates to a first entry of 15/4, expert 1's to 1/4 each
+    y = np.ones((16, 1))
+    amax, amax_t = B.nvfp4_amax(y, np.array([0, 15, 16]))
+    assert amax == 1.0 and amax_t == 15 / 4
+    # merged into one expert the block would be constant: 16/4
+    assert B.nvfp4_amax(y, np.array([0, 16]))[1] == 4.0
