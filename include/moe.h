@@ -165,6 +165,15 @@ typedef struct moe_train_save {
                            along the padded row axis                          */
     uint8_t* at_s;      /* [R_pad/128, H] words of its scales, as y1t_s       */
     int32_t* poff;      /* [G + 1] padded row offsets                         */
+    float* amax;        /* nullable [2]: the NVFP4 training recipe's amaxes of
+                           y (activation x routing weight): [0] = max |y|,
+                           [1] = max |(H16 / 4) . block| over the Hadamard
+                           rotations of y's transpose, blocks of 16 rows of
+                           one expert (zero-padded), H16 Sylvester's Hadamard
+                           matrix. Source: NVIDIA blog, section on fusing
+                           MXFP8/NVFP4 quantisation (per-tensor amax for the
+                           forward, amax of the transposed Hadamard-rotated
+                           output for the backward).                        */
 } moe_train_save_t;
 
 /* Pointers into a workspace (all device). */

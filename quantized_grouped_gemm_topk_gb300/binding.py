@@ -65,7 +65,8 @@ class moe_dispatch_t(ctypes.Structure):
 
 class moe_train_save_t(ctypes.Structure):
     _fields_ = [("h", ctypes.c_void_p), ("y1t_q", ctypes.c_void_p), ("y1t_s", ctypes.c_void_p),
-                ("at_q", ctypes.c_void_p), ("at_s", ctypes.c_void_p), ("poff", ctypes.c_void_p)]
+                ("at_q", ctypes.c_void_p), ("at_s", ctypes.c_void_p), ("poff", ctypes.c_void_p),
+                ("amax", ctypes.c_void_p)]
 
 
 class moe_ws_view_t(ctypes.Structure):
@@ -341,8 +342,9 @@ def dispatch_struct(t: dict) -> moe_dispatch_t:
                           _ptr(t["perm_src"]), _ptr(t["inv"]), _ptr(t["w_row"]), _ptr(t["xq"]), _ptr(t["xs"]))
 
 
-def alloc_train_save(cfg, T, device="cuda"):
-    """Caller-side allocation of the training save buffers for T tokens."""
+def alloc_train_save(cfg, T, device="cuda", amax=False):
+    """Caller-side allocation of the training save buffers for T tokens
+    (amax=True adds the NVFP4-recipe amax pair)."""
     rp = moe_train_sizes(cfg, T)
     kp = cfg.k + cfg.n_shared
     R = T * kp
@@ -354,7 +356,8 @@ def alloc_train_save(cfg, T, device="cuda"):
         "at_q": torch.empty(cfg.H, rp, dtype=torch.uint8, device=device),
         "at_s": torch.empty(rp // 128, cfg.H, 4, dtype=torch.uint8, device=device),
         "poff": torch.empty(G + 1 + 3, dtype=torch.int32, device=device),
+        "amax": torch.empty(4, dtype=torch.float32, device=device) if amax else None,
         "r_pad": rp,
     }
-    st = moe_train_save_t(*(_ptr(bufs[k]) for k in ("h", "y1t_q", "y1t_s", "at_q", "at_s", "poff")))
+    st = moe_train_save_t(*(_ptr(bufs[k]) for k in ("h", "y1t_q", "y1t_s", "at_q", "at_s", "poff", "amax")))
     return st, bufs

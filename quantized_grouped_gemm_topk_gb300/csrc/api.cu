@@ -571,6 +571,10 @@ static moe_status_t w1_impl(const moe_config_t* c, const moe_dispatch_t* d, int 
     g.yst = at<uint8_t>(ws, L.y1st);
     if (save) {
       g.hsave = save->h; g.tq = save->y1t_q; g.ts = save->y1t_s; g.t_ld = r_pad_for(dims_of(*c), T); g.t_nf = c->I;
+      if (save->amax) {
+        MOE_CHECK_CUDA(cudaMemsetAsync(save->amax, 0, 2 * sizeof(float), st));
+        g.amax = save->amax;
+      }
     }
     moe_status_t s = mx_token_gemm(c, g, kMxW1, xg, xgs, R, packed, MOE_PACK_FORWARD, 1, d->offsets,
                                    at<int32_t>(ws, L.poff), status, st);
@@ -626,6 +630,7 @@ static moe_status_t check_save(const moe_config_t* c, const moe_train_save_t* sa
   if (!save) return MOE_OK;
   if (!backward_capable(*c)) return MOE_ERR_UNSUPPORTED;
   REQ(save->h); REQ(save->y1t_q); REQ(save->y1t_s); REQ(save->at_q); REQ(save->at_s); REQ(save->poff);
+  OPT(save->amax);
   return MOE_OK;
 }
 

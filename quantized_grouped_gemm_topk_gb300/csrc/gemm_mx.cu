@@ -193,6 +193,35 @@ __device__ __forceinline__ void quant_cols32(const float (&v)[32], uint8_t* tq, 
   }
 }
 
+// The NVFP4 training recipe's two amaxes over 32 features of the warp's 32
+// rows (lane = row; rows that are not the group's count as zero): max |v|,
+// and max |(H16 / 4) . block| of the transpose, the two 16-lane halves being
+// two blocks of 16 consecutive rows of one expert (the warp's rows start at
+// a multiple of 32 from the expert's first row). The Walsh-Hadamard
+// butterfly over lanes gives lane l the sum over j of (-1)^popc(l & j) v_j.
+// Both maxima go to amax[0..1] with an integer atomicMax on the float bits
+// (valid for values >= 0; the result is independent of the order).
+__device__ __forceinline__ void nvfp4_amax32(const float (&y)[32], bool live, float* amax, int lane) {
+  float am = 0.f, amt = 0.f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    float h = live ? y[i] : 0.f;
+    am = fmaxf(am, fabsf(h));
+#pragma unroll
+    for (int s = 1; s < 16; s <<= 1) {
+      const float o = __shfl_xor_sync(kFull, h, s);
+      h = (lane & s) ? o - h : h + o;
+    }
+    amt = fmaxf(amt, fabsf(h));
+  }
+  am = warp_max(am);
+  amt = warp_max(amt) * 0.25f;
+  if (lane == 0) {
+    atomicMax(reinterpret_cast<int*>(amax), __float_as_int(am));
+    atomicMax(reinterpret_cast<int*>(amax) + 1, __float_as_int(amt));
+  }
+}
+
 template <int MODE>
 __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, uint32_t acc_tmem, int q, int lane,
                                             bool has_k) {
@@ -263,6 +292,7 @@ __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, ui
           }
         }
       }
+      if (g.amax) nvfp4_amax32(y, rel < w.cnt, g.amax, lane);
       if (tblk) {
         if (rel >= w.cnt) {
 #pragma unroll

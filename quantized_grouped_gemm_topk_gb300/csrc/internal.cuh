@@ -181,6 +181,7 @@ struct MxArgs {
                                                        // (K = t_ld, ld = t_nf); W1: nullable
   uint16_t* out; int64_t out_ld;            // Plain: [R][out_ld]; Wgrad: [G][M][out_ld]
   float* dwpart;                // Dswiglu: [n_tiles][R]
+  float* amax;                  // W1 (nullable): [2] max |y|, max |H16/4 . block of y^T| (zeroed by the caller)
   int32_t* status;
 };
 struct MxMaps {

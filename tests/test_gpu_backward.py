@@ -70,6 +70,28 @@ def test_train_reduced_full_check(act):
     assert_close_layer(np_(dlog), b.dlogits, "dlogits")
 
 
+def test_nvfp4_recipe_amax():
+    """The W1 epilogue's NVFP4-recipe amaxes: max |y| and the amax of the
+    16-row Hadamard rotation of y's transpose within each expert, against the
+    oracle's on the same routing."""
+    dev = cuda_device()
+    s = inputs.workload("train", T=56, E=8)
+    T = s.T
+    r = run_forward(s, T, dev=dev, save=False)
+    cfg = r["cfg"]
+    st, bufs = m.alloc_train_save(cfg, T, dev, amax=True)
+    bufs["amax"].fill_(-1.0)
+    out = torch.empty_like(r["out"])
+    m.moe_layer_forward(cfg, r["x"], r["Wr"], None, T, r["packed"], out, st, r["ws"])
+    torch.cuda.synchronize()
+    assert m.moe_read_status(cfg, r["ws"]) == 0
+    f = oracle_forward(s, r)
+    amax, amax_t = B.nvfp4_amax(f.y, f.disp.offsets)
+    got = np_(bufs["amax"])[:2]
+    np.testing.assert_allclose(got, [amax, amax_t], rtol=1e-4)
+    assert amax_t > 0 and amax > 0
+
+
 def test_train_empty_expert_grads_are_zero():
     dev = cuda_device()
     s = inputs.workload("train", T=4, E=16)
