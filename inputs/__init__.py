@@ -36,7 +36,7 @@ import torch
 
 __all__ = [
     "MoEShape", "WORKLOADS", "workload", "gen_x", "gen_router", "gen_logits",
-    "gen_dout", "gen_expert_weights", "encode_nvfp4", "encode_mxfp8",
+    "gen_dout", "gen_expert_weights", "encode_nvfp4", "encode_mxfp8", "encode_mxfp4",
     "bf16_bits", "expected_touched",
 ]
 
@@ -54,7 +54,7 @@ class MoEShape:
     act: str = "swiglu"          # "swiglu" | "swiglu_clamp" | "geglu"
     alpha: float = 1.0
     limit: float = 0.0
-    wfmt: str = "nvfp4"          # "nvfp4" | "mxfp8"
+    wfmt: str = "nvfp4"          # "nvfp4" | "mxfp8" | "mxfp4"
     logits: str = "router"       # "router" (x @ W_r) | "zipf" (drawn directly)
 
     @property
@@ -230,6 +230,30 @@ def encode_mxfp8(w: torch.Tensor):
     return q.contiguous(), (e + 127).to(torch.uint8).contiguous()
 
 
+def _mx_exponent_fp4(amax: torch.Tensor) -> torch.Tensor:
+    """Smallest integer e with amax <= 6 * 2^e, clamped to [-127, 127];
+    amax == 0 gives -127."""
+    m, ex = torch.frexp(amax.to(torch.float32))      # amax = m * 2^ex, m in [0.5, 1)
+    # 6 * 2^e = 0.75 * 2^(e + 3): e = ex - 3 if m <= 0.75, else ex - 2
+    e = ex.to(torch.int32) - 3 + (m > 0.75).to(torch.int32)
+    e = torch.where(amax > 0, e, torch.full_like(e, -127))
+    return e.clamp(-127, 127)
+
+
+def encode_mxfp4(w: torch.Tensor):
+    """MXFP4-encode rows of w [N, K]: blocks of 32 along K, E8M0 scale 2^e
+    with e the smallest integer such that amax <= 6 * 2^e, E2M1 elements
+    RNE(w / 2^e). Returns (packed nibbles uint8 [N, K/2], element 2i in the
+    low nibble, scale codes uint8 [N, K/32])."""
+    N, K = w.shape
+    w = w.to(torch.float32)
+    blk = w.view(N, K // 32, 32)
+    e = _mx_exponent_fp4(blk.abs().amax(-1))
+    q = _e2m1_codes(blk * torch.pow(2.0, -e.to(torch.float32)).unsqueeze(-1)).view(N, K)
+    packed = (q[:, 0::2] | (q[:, 1::2] << 4)).to(torch.uint8)
+    return packed.contiguous(), (e + 127).to(torch.uint8).contiguous()
+
+
 def gen_one_expert(s: MoEShape, seed: int, e: int, device="cpu", dgrad_copies: bool = False) -> dict:
     """Weights of expert group e, drawn and encoded exactly as in
     gen_expert_weights (per-expert generators, so any expert can be drawn
@@ -243,6 +267,11 @@ def gen_one_expert(s: MoEShape, seed: int, e: int, device="cpu", dgrad_copies: b
     if s.wfmt == "nvfp4":
         out["w1_q"], out["w1_s"], out["w1_gs"] = encode_nvfp4(w1)
         out["w2_q"], out["w2_s"], out["w2_gs"] = encode_nvfp4(w2)
+    elif s.wfmt == "mxfp4":
+        out["w1_q"], out["w1_s"] = encode_mxfp4(w1)
+        out["w2_q"], out["w2_s"] = encode_mxfp4(w2)
+        out["w1_gs"] = torch.ones((), dtype=torch.float32, device=device)
+        out["w2_gs"] = torch.ones((), dtype=torch.float32, device=device)
     elif s.wfmt == "mxfp8":
         w1 = w1.to(torch.bfloat16).to(torch.float32)      # bf16 master weights
         w2 = w2.to(torch.bfloat16).to(torch.float32)

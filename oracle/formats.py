@@ -159,6 +159,17 @@ def nvfp4_dequantize(packed: np.ndarray, scales: np.ndarray, gs: float) -> np.nd
     return w.reshape(q.shape) * float(gs)
 
 
+def mxfp4_dequantize(packed: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """MXFP4 matrix [N, K/2] bytes (two E2M1 codes each, element 2i in the low
+    nibble) + E8M0 scales [N, K/32] -> fp64 [N, K] = E2M1 value * 2^(s - 127)
+    per block of 32 along K (OCP MX: the FP4 element format with the shared
+    E8M0 scale, the GC-MoE summary's "(1,1,32)" scale recipe)."""
+    q = decode_e2m1_packed(packed)
+    K = q.shape[-1]
+    s = decode_e8m0(scales)
+    return (q.reshape(q.shape[:-1] + (K // 32, 32)) * s[..., None]).reshape(q.shape)
+
+
 def bf16_to_f64(bits: np.ndarray) -> np.ndarray:
     """Raw bfloat16 bit patterns (uint16/int16) -> exact fp64 values."""
     b = np.asarray(bits).astype(np.uint16).astype(np.uint32) << 16

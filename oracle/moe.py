@@ -183,6 +183,8 @@ def expert_w1(wts: dict, e: int, wfmt: str) -> np.ndarray:
         return np.asarray(wts["w1_f64"][e], np.float64)
     if wfmt == "nvfp4":
         return F.nvfp4_dequantize(wts["w1_q"][e], wts["w1_s"][e], wts["w1_gs"][e])
+    if wfmt == "mxfp4":
+        return F.mxfp4_dequantize(wts["w1_q"][e], wts["w1_s"][e])
     return F.mx_dequantize(wts["w1_q"][e], wts["w1_s"][e])
 
 
@@ -192,6 +194,8 @@ def expert_w2(wts: dict, e: int, wfmt: str) -> np.ndarray:
         return np.asarray(wts["w2_f64"][e], np.float64)
     if wfmt == "nvfp4":
         return F.nvfp4_dequantize(wts["w2_q"][e], wts["w2_s"][e], wts["w2_gs"][e])
+    if wfmt == "mxfp4":
+        return F.mxfp4_dequantize(wts["w2_q"][e], wts["w2_s"][e])
     return F.mx_dequantize(wts["w2_q"][e], wts["w2_s"][e])
 
 

@@ -74,6 +74,18 @@ def test_nvfp4_dequantize_by_hand():
     assert w[0].tolist() == expect
 
 
+def test_mxfp4_dequantize_by_hand():
+    # one row, 64 elements (two blocks of 32): block 0 holds codes 0..15
+    # twice with scale 0x80 (2^1), block 1 the code 0x7 (6.0) everywhere
+    # with scale 0x7C (2^-3)
+    codes = np.concatenate([np.arange(16), np.arange(16), np.full(32, 7)]).astype(np.uint8)
+    packed = (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)[None]
+    w = F.mxfp4_dequantize(packed, np.array([[0x80, 0x7C]], np.uint8))
+    mag = [0, .5, 1, 1.5, 2, 3, 4, 6, -0., -.5, -1, -1.5, -2, -3, -4, -6]
+    assert w[0, :32].tolist() == [2.0 * v for v in mag * 2]
+    assert w[0, 32:].tolist() == [0.75] * 32
+
+
 def _brute_e4m3(x):
     best, bestd = None, None
     for c in range(256):

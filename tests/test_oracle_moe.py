@@ -163,7 +163,8 @@ def _tiny_case(act="swiglu", wfmt="nvfp4", S=0, rs=1.0, T=16):
 
 
 @pytest.mark.parametrize("act,wfmt,S,rs", [("swiglu", "nvfp4", 0, 1.0), ("swiglu", "nvfp4", 1, 2.5),
-                                          ("swiglu_clamp", "mxfp8", 0, 1.0), ("geglu", "nvfp4", 0, 1.0)])
+                                          ("swiglu_clamp", "mxfp8", 0, 1.0), ("geglu", "nvfp4", 0, 1.0),
+                                          ("swiglu", "mxfp4", 0, 1.0)])
 def test_routed_equals_dense_formulation(act, wfmt, S, rs):
     s, xb, lg, wts = _tiny_case(act, wfmt, S, rs)
     kw = dict(E=s.E, k=s.k, n_shared=S, routed_scale=rs, act=s.act, alpha=s.alpha, limit=s.limit, wfmt=wfmt)
@@ -324,3 +325,20 @@ def test_router_logits_hand_computed_case():
                     [1.0, 1.0, 1.0]])
     got = M.router_logits(x, W_r)
     assert got.tolist() == [[0.0, -0.5, 3.0], [-7.5, 4.0, 1.0]]
+
+
+def test_mxfp4_encoding_scale_rule():
+    """The MXFP4 weights the workloads hand the layer: every block's scale is
+    the smallest power of two with amax <= 6 * 2^e (so no element saturates,
+    and the block maximum lands in the top binade [3, 6]), and decoding
+    returns each element within half an E2M1 step of its value."""
+    g = torch.Generator().manual_seed(5)
+    w = torch.randn(8, 128, generator=g) * 0.02
+    packed, sc = inputs.encode_mxfp4(w)
+    dec = F.mxfp4_dequantize(packed.numpy(), sc.numpy())
+    e = sc.numpy().astype(np.int64) - 127
+    blk = w.numpy().astype(np.float64).reshape(8, 4, 32)
+    amax = np.abs(blk).max(-1)
+    assert (amax <= 6.0 * np.exp2(e)).all() and (amax > 3.0 * np.exp2(e)).all()
+    err = np.abs(dec.reshape(8, 4, 32) - blk) / np.exp2(e)[..., None]
+    assert err.max() <= 1.0 + 1e-12          # steps of E2M1 are at most 2 (between 4 and 6)
