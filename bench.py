@@ -65,16 +65,23 @@ SHARED_TS = (1, 16, 64)
 FLUSH_BYTES = 512 << 20
 
 
-def nvfp4_matrix_bytes(n, k):
-    return n * k // 2 + n * k // 16
+def matrix_bytes(n, k, wfmt="nvfp4"):
+    """Bytes of one n x k weight matrix with its block scales (NVFP4: E2M1
+    codes + one E4M3 scale per 16; MXFP4: E2M1 + one E8M0 per 32; MXFP8:
+    E4M3 + one E8M0 per 32)."""
+    if wfmt == "nvfp4":
+        return n * k // 2 + n * k // 16
+    if wfmt == "mxfp4":
+        return n * k // 2 + n * k // 32
+    return n * k + n * k // 32
 
 
 def w1_bytes_per_expert(s):
-    return nvfp4_matrix_bytes(2 * s.I, s.H)
+    return matrix_bytes(2 * s.I, s.H, s.wfmt)
 
 
 def w2_bytes_per_expert(s):
-    return nvfp4_matrix_bytes(s.H, s.I)
+    return matrix_bytes(s.H, s.I, s.wfmt)
 
 
 def peaks():
@@ -361,7 +368,7 @@ class DecodeBench:
 
     def weight_bytes(self, T, i):
         """Algorithmic bytes of the layer: every touched group's W1 and W2
-        (NVFP4 with scales), the router weights, x in and out."""
+        (codes with their scales), the router weights, x in and out."""
         s = self.s
         return (self.touched[(T, i)] * (w1_bytes_per_expert(s) + w2_bytes_per_expert(s)) + s.H * s.E * 4
                 + 2 * T * s.H * 2)
@@ -436,6 +443,30 @@ def bench_shared_decode(m, dev, K, warmup, flush, hbm):
         out["per_T"][str(T)] = {"us_per_layer": us, "tokens_per_s": T / us * 1e6,
                                 "layer_bytes": gb, "hbm_frac_of_measured": gb / (us * 1e-6) / 1e9 / hbm}
     out["w1_gemm_hbm_frac_of_measured"] = r["w1_bytes"] / (r["w1_us"] * 1e-6) / 1e9 / hbm
+    b.free()
+    return out
+
+
+def bench_mxfp4_decode(m, dev, K, warmup, flush, hbm):
+    """The DeepSeek-V3-shaped decode layers with MXFP4 weights (E2M1, E8M0
+    scale per 32) on the block-scaled GEMM: FP8 tokens x E2M1 weights in the
+    tensor core, no weight decode."""
+    s = inputs.workload("dsv3", wfmt="mxfp4")
+    b = DecodeBench(m, s, DECODE_TS, dev, 0)
+    r = b.run(K, warmup, flush)
+    out = {"workload": "dsv3_decode_mxfp4", "H": s.H, "I": s.I, "E": s.E, "k": s.k, "weights": "mxfp4",
+           "launch": "CUDA graph per layer", "per_T": {}}
+    for T in DECODE_TS:
+        us = statistics.median(r["layer_us"][T])
+        gb = statistics.mean(r["layer_bytes"][T])
+        out["per_T"][str(T)] = {"us_per_layer": us, "tokens_per_s": T / us * 1e6,
+                                "layer_bytes": gb, "hbm_frac_of_measured": gb / (us * 1e-6) / 1e9 / hbm}
+    out["us_per_step"] = sum(sum(v) for v in r["layer_us"].values()) / K
+    out["w1_gemm"] = {"kernel": "k_gemm_mx (E4M3 x E2M1, block-scaled)", "us_per_step": r["w1_us"] / K,
+                      "hbm_frac_of_measured": r["w1_bytes"] / (r["w1_us"] * 1e-6) / 1e9 / hbm,
+                      "algorithmic_bytes": "touched experts x MXFP4 W1 bytes (2I*H/2 + 2I*H/32) + MXFP8 rows "
+                                           "in and out"}
+    out["w2_gemm_us_per_step"] = r["w2_us"] / K
     b.free()
     return out
 
@@ -571,6 +602,8 @@ def run_only(args, local):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     if args.only == "shared":
         res = bench_shared_decode(m, dev, args.steps, args.warmup, flush, hbm)
+    elif args.only == "mxfp4":
+        res = bench_mxfp4_decode(m, dev, args.steps, args.warmup, flush, hbm)
     elif args.only == "skewed":
         res = bench_skewed(m, dev, args.steps, args.warmup, flush, hbm, bf16)
     else:
@@ -641,6 +674,7 @@ def run_ours(args, s, rank, world, local):
     if not args.no_per_config:
         pc = {}
         pc["shared_decode"] = bench_shared_decode(m, dev, min(K, 50), args.warmup, flush, hbm)
+        pc["mxfp4_decode"] = bench_mxfp4_decode(m, dev, min(K, 50), args.warmup, flush, hbm)
         pc["skewed_prefill"] = bench_skewed(m, dev, min(K, 20), args.warmup, flush, hbm, bf16)
         pc["train"] = bench_train(m, dev, min(K, 10), max(2, min(args.warmup, 3)), bf16)
         pc["peaks"] = {"hbm_gbs": hbm, "bf16_tflops_burst": bf16, "bf16_tflops_sustained": bf16_sus,
@@ -672,7 +706,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="headline workload only")
     ap.add_argument("--E", type=int, default=0, help="override the expert count (small profiling cases)")
-    ap.add_argument("--only", default="", choices=["", "shared", "skewed", "train"],
+    ap.add_argument("--only", default="", choices=["", "shared", "mxfp4", "skewed", "train"],
                     help="run one workload of the per-config block alone (profiling)")
     ap.add_argument("--train-T", type=int, default=0, help="training tokens for --only train")
     ap.add_argument("--train-E", type=int, default=0, help="training experts for --only train")

@@ -90,7 +90,7 @@ typedef enum moe_status {
 #define MOE_DEV_TIMEOUT 0x8       /* a kernel gave up waiting on itself      */
 
 enum { MOE_ACT_SWIGLU = 0, MOE_ACT_SWIGLU_CLAMP = 1, MOE_ACT_GEGLU = 2 };
-enum { MOE_WFMT_NVFP4 = 0, MOE_WFMT_MXFP8 = 1 };
+enum { MOE_WFMT_NVFP4 = 0, MOE_WFMT_MXFP8 = 1, MOE_WFMT_MXFP4 = 2 };
 enum { MOE_PACK_FORWARD = 0, MOE_PACK_DGRAD = 1 };
 
 /* Layer configuration (plain data, validated by moe_config_validate).
@@ -105,7 +105,11 @@ enum { MOE_PACK_FORWARD = 0, MOE_PACK_DGRAD = 1 };
  *                              families: SwiGLU, GeGLU, with clamping). 
  * weight_fmt = MOE_WFMT_NVFP4: E2M1 elements, E4M3 scale per 16 along K,
  *                              fp32 scale per (group, matrix)
- * weight_fmt = MOE_WFMT_MXFP8: E4M3 elements, E8M0 scale per 32 along K */
+ * weight_fmt = MOE_WFMT_MXFP8: E4M3 elements, E8M0 scale per 32 along K
+ * weight_fmt = MOE_WFMT_MXFP4: E2M1 elements, E8M0 scale per 32 along K (the
+ *                              GC-MoE summary's "(1,1,32)" recipe: Limitations;
+ *                              the block-scaled FP8 x FP4 MMA: Key
+ *                              contributions); forward only */
 typedef struct moe_config {
     int32_t H, I, E, k;
     int32_t n_shared;     /* 0 or 1                                          */
@@ -127,7 +131,9 @@ typedef struct moe_config {
  * NVFP4: w*_q [G, N, K/2] bytes, element 2i in the low nibble of byte i;
  *        w*_s [G, N, K/16] E4M3 codes; w*_gs [G] fp32.
  * MXFP8: w*_q [G, N, K] E4M3 codes; w*_s [G, N, K/32] E8M0 codes;
- *        w*_gs ignored (may be NULL). */
+ *        w*_gs ignored (may be NULL).
+ * MXFP4: w*_q [G, N, K/2] bytes, element 2i in the low nibble of byte i;
+ *        w*_s [G, N, K/32] E8M0 codes; w*_gs ignored (may be NULL). */
 typedef struct moe_weights_view {
     const uint8_t* w1_q;
     const uint8_t* w1_s;

@@ -1,5 +1,5 @@
 """GB300 (sm_103a) routed Mixture-of-Experts layer: top-k routing, on-device
-dispatch, FP8 x NVFP4/MXFP8 grouped GEMMs with a fused SwiGLU + requantise
+dispatch, FP8 x NVFP4/MXFP8/MXFP4 grouped GEMMs with a fused SwiGLU + requantise
 epilogue, combine, and the training backward. The compute lives in the CUDA
 library ``libmoe.so`` (C ABI: include/moe.h); ``binding`` marshals torch
 tensors into it."""

@@ -25,7 +25,8 @@ MOE_DEV_BAD_PACK = 0x4
 MOE_DEV_TIMEOUT = 0x8
 MOE_ACT_SWIGLU, MOE_ACT_SWIGLU_CLAMP, MOE_ACT_GEGLU = 0, 1, 2
 ACTS = {"swiglu": MOE_ACT_SWIGLU, "swiglu_clamp": MOE_ACT_SWIGLU_CLAMP, "geglu": MOE_ACT_GEGLU}
-MOE_WFMT_NVFP4, MOE_WFMT_MXFP8 = 0, 1
+MOE_WFMT_NVFP4, MOE_WFMT_MXFP8, MOE_WFMT_MXFP4 = 0, 1, 2
+WFMTS = {"nvfp4": MOE_WFMT_NVFP4, "mxfp8": MOE_WFMT_MXFP8, "mxfp4": MOE_WFMT_MXFP4}
 MOE_PACK_FORWARD, MOE_PACK_DGRAD = 0, 1
 
 # every exported symbol the header declares
@@ -150,7 +151,7 @@ def make_config(H, I, E, k, n_shared=0, T_max=0, act="swiglu", alpha=1.0, limit=
     return moe_config_t(H, I, E, k, n_shared, T_max,
                         ACTS[act],
                         float(alpha), float(limit), float(routed_scale),
-                        MOE_WFMT_NVFP4 if wfmt == "nvfp4" else MOE_WFMT_MXFP8, max_sms)
+                        WFMTS[wfmt], max_sms)
 
 
 def config_from_shape(s, T_max=None, max_sms=0) -> moe_config_t:

@@ -52,7 +52,10 @@ static bool backward_capable(const moe_config_t& c) {
 
 // MXFP8 weights run on the block-scaled tensor-core GEMM (gemm_mx.cu); NVFP4
 // weights on the decoding GEMM (gemm_tc.cu).
-static bool mx_path(const moe_config_t& c) { return c.weight_fmt == MOE_WFMT_MXFP8; }
+static bool mx_path(const moe_config_t& c) { return c.weight_fmt == MOE_WFMT_MXFP8 || c.weight_fmt == MOE_WFMT_MXFP4; }
+
+// Code bytes of one packed row of K elements.
+static int64_t row_bytes(int fmt, int K) { return fmt == MOE_WFMT_MXFP4 ? K / 2 : K; }
 
 static int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -167,9 +170,9 @@ static PackLayout pack_layout(const moe_config_t& c, int which) {
   } else {
     P.rows1 = P.il1 > 0 ? ceil_div(P.il1, kMxTileN / 2) * kMxTileN : P.N1;
     P.rows2 = P.N2;
-    P.off_w1 = o; o = align_up(o + (size_t)P.G * P.rows1 * P.K1, 256);
+    P.off_w1 = o; o = align_up(o + (size_t)P.G * P.rows1 * row_bytes(P.fmt, P.K1), 256);
     P.off_s1 = o; o = align_up(o + (size_t)sf4_bytes(P.K1, (int64_t)P.G * P.rows1), 256);
-    P.off_w2 = o; o = align_up(o + (size_t)P.G * P.rows2 * P.K2, 256);
+    P.off_w2 = o; o = align_up(o + (size_t)P.G * P.rows2 * row_bytes(P.fmt, P.K2), 256);
     P.off_s2 = o; o = align_up(o + (size_t)sf4_bytes(P.K2, (int64_t)P.G * P.rows2), 256);
   }
   P.total = o;
@@ -226,7 +229,10 @@ moe_status_t moe_config_validate(const moe_config_t* c) {
   if (c->act != MOE_ACT_SWIGLU && c->act != MOE_ACT_SWIGLU_CLAMP && c->act != MOE_ACT_GEGLU)
     return MOE_ERR_INVALID_ARG;
   if (c->act == MOE_ACT_SWIGLU_CLAMP && !(c->act_limit > 0.f)) return MOE_ERR_INVALID_ARG;
-  if (c->weight_fmt != MOE_WFMT_NVFP4 && c->weight_fmt != MOE_WFMT_MXFP8) return MOE_ERR_INVALID_ARG;
+  if (c->weight_fmt != MOE_WFMT_NVFP4 && c->weight_fmt != MOE_WFMT_MXFP8 && c->weight_fmt != MOE_WFMT_MXFP4)
+    return MOE_ERR_INVALID_ARG;
+  // the unpacking tensor copy of E2M1 rows moves whole 128-element runs
+  if (c->weight_fmt == MOE_WFMT_MXFP4 && (c->H % 128 || c->I % 128)) return MOE_ERR_INVALID_ARG;
   if (!(c->routed_scale > 0.f)) return MOE_ERR_INVALID_ARG;
   if (c->max_sms < 0) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
@@ -311,10 +317,10 @@ moe_status_t moe_prepack_weights(const moe_config_t* c, const moe_weights_view_t
     MOE_CHECK_CUDA(launch_prepack_nv(src->w2_q, src->w2_s, P.G, P.N2, P.K2, 0, P.tiles2, P.tile_bytes2,
                                      d8 + P.off_w2, st));
   } else {
-    MOE_CHECK_CUDA(launch_prepack_mx(src->w1_q, src->w1_s, P.G, P.N1, P.K1, P.il1, P.rows1, d8 + P.off_w1,
-                                     d8 + P.off_s1, st));
-    MOE_CHECK_CUDA(launch_prepack_mx(src->w2_q, src->w2_s, P.G, P.N2, P.K2, 0, P.rows2, d8 + P.off_w2,
-                                     d8 + P.off_s2, st));
+    MOE_CHECK_CUDA(launch_prepack_mx(src->w1_q, src->w1_s, P.G, P.N1, P.K1, row_bytes(P.fmt, P.K1), P.il1, P.rows1,
+                                     d8 + P.off_w1, d8 + P.off_s1, st));
+    MOE_CHECK_CUDA(launch_prepack_mx(src->w2_q, src->w2_s, P.G, P.N2, P.K2, row_bytes(P.fmt, P.K2), 0, P.rows2,
+                                     d8 + P.off_w2, d8 + P.off_s2, st));
   }
   return MOE_OK;
 }
@@ -337,7 +343,7 @@ moe_status_t moe_debug_unpack_weights(const moe_config_t* c, const void* packed,
                                     st));
   } else {
     MOE_CHECK_CUDA(launch_unpack_mx(b + (mat == 1 ? P.off_w1 : P.off_w2), b + (mat == 1 ? P.off_s1 : P.off_s2), P.G,
-                                    N, K, il, mat == 1 ? P.rows1 : P.rows2, q, sc, st));
+                                    N, K, row_bytes(P.fmt, K), il, mat == 1 ? P.rows1 : P.rows2, q, sc, st));
   }
   return MOE_OK;
 }
@@ -520,11 +526,13 @@ static moe_status_t mx_token_gemm(const moe_config_t* c, MxArgs& g, int mode, co
   g.poff = poff;
   g.a_sf = as; g.a_sf_ld = R; g.a_rows = R;
   g.b_sf = b + (mat == 1 ? P.off_s1 : P.off_s2); g.b_sf_ld = (int64_t)P.G * rows; g.b_rows = (int64_t)P.G * rows;
+  g.b_fp4 = P.fmt == MOE_WFMT_MXFP4;
   g.R = R;
   g.status = status;
   MxMaps maps;
-  if (!make_tmap_mx(&maps.a, aq, R, K, mx_tile_m()) ||
-      !make_tmap_mx(&maps.b, b + (mat == 1 ? P.off_w1 : P.off_w2), (int64_t)P.G * rows, K, mx_b_box_rows()))
+  if (!make_tmaps_mx_a(&maps, aq, R, K) ||
+      !make_tmap_mx(&maps.b, b + (mat == 1 ? P.off_w1 : P.off_w2), (int64_t)P.G * rows, K, mx_b_box_rows(),
+                    g.b_fp4 != 0))
     return MOE_ERR_CUDA;
   MOE_CHECK_CUDA(launch_gemm_mx(g, maps, mx_grid(*c), st));
   return MOE_OK;
@@ -780,7 +788,7 @@ static moe_status_t mx_wgrad(const moe_config_t* c, const uint8_t* pq, const uin
   g.out = out; g.out_ld = N;
   g.status = status;
   MxMaps maps;
-  if (!make_tmap_mx(&maps.a, pq, M, Rp, mx_tile_m()) || !make_tmap_mx(&maps.b, qq, N, Rp, mx_b_box_rows()))
+  if (!make_tmaps_mx_a(&maps, pq, M, Rp) || !make_tmap_mx(&maps.b, qq, N, Rp, mx_b_box_rows(), false))
     return MOE_ERR_CUDA;
   MOE_CHECK_CUDA(launch_gemm_mx(g, maps, mx_grid(*c), st));
   return MOE_OK;

@@ -18,8 +18,9 @@ constexpr unsigned kFull = 0xffffffffu;
 // chunks.
 //   chunk: [granule g < 2][row p < 128][16 B of 32 E2M1 codes] (4096 B)
 //          then [row p][4 E4M3 scale codes, one per 16 K] (512 B).
-// MXFP8: plain K-major rows, codes [G][rows][K] and scales in the SF4
-//   layout (below) over all groups' rows;
+// MXFP8 / MXFP4: plain K-major rows, codes [G][rows][K] (MXFP4: packed
+//   E2M1 nibbles, [G][rows][K/2]) and scales in the SF4 layout (below) over
+//   all groups' rows;
 //   W1's forward rows come in tiles of 192: 96 gate features then the same
 //   96 up features (zero rows past I), every other matrix in its own row
 //   order.

@@ -129,6 +129,15 @@ __device__ __forceinline__ void mx_unit(const MxArgs& g, const int32_t* uoff, in
 
 __device__ __forceinline__ int mx_stages(int klen) { return (klen + kMxBK - 1) / kMxBK; }
 
+// The A copy of a tile covers 16 << i rows, the fewest of 16 / 32 / 64 / 128
+// that hold its real rows (a decode tile with a handful of tokens then moves
+// 2 KB of activations a stage, not 16 KB). The MMA still reads all 128 rows:
+// the rest hold an earlier stage's bytes, and the epilogue drops those
+// accumulator rows (each output row depends on its own A row only).
+__device__ __forceinline__ int mx_a_box(int a_valid) {
+  return a_valid <= 16 ? 0 : a_valid <= 32 ? 1 : a_valid <= 64 ? 2 : 3;
+}
+
 // The SF4 word (the scales of one 128-wide K stage) of one row: one 32-bit
 // load; lanes holding consecutive rows read consecutive words. Nothing
 // consumes the value until the stage's tensor-memory store, four stages
@@ -387,7 +396,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
   __shared__ int bad_pack;
   pdl_enter();
   if (threadIdx.x == 0) {
-    bad_pack = g.hdr && !pack_header_ok(g.hdr, MOE_WFMT_MXFP8, g.which, g.G);
+    bad_pack = g.hdr && !pack_header_ok(g.hdr, g.b_fp4 ? MOE_WFMT_MXFP4 : MOE_WFMT_MXFP8, g.which, g.G);
     if (bad_pack) set_status(g.status, MOE_DEV_BAD_PACK);
   }
   __syncthreads();
@@ -449,8 +458,14 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
   if (warp == kMxWProd) {
     // ---------------- TMA producer ----------------
     if (lane == 0) {
-      tc::prefetch_tmap(&maps.a);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) tc::prefetch_tmap(&maps.a[i]);
       tc::prefetch_tmap(&maps.b);
+      // bytes a stage's B copy reports to the barrier: packed E2M1 reports
+      // its global bytes (two elements a byte) although it lands one element
+      // a byte in shared memory (8 data bytes, then an 8-byte gap the copy
+      // leaves untouched, per 16 elements)
+      const uint32_t b_tx = g.b_fp4 ? kMxBStage / 2 : kMxBStage;
       uint32_t it = 0;
       bool ok = true;
       for (int u = cid; ok && u < U; u += ncl) {
@@ -460,9 +475,10 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
         for (int s = 0; s < nk; ++s, ++it) {
           const int slot = it % kMxStages;
           if (!tc::mbar_wait(&empty[slot], ((it / kMxStages) & 1) ^ 1, abort)) { ok = false; break; }
-          tc::mbar_arrive_expect_tx(&full[slot], kMxStageBytes);
+          const int ai = mx_a_box(w.a_valid);
+          tc::mbar_arrive_expect_tx(&full[slot], (uint32_t)(kMxBK * (16 << ai)) + b_tx);
           const int kx = w.k0 + s * kMxBK;
-          tc::tma_load_2d_plain(sa + slot * kMxAStage, &maps.a, kx, w.a_row0, &full[slot]);
+          tc::tma_load_2d_plain(sa + slot * kMxAStage, &maps.a[ai], kx, w.a_row0, &full[slot]);
           if constexpr (kMxCl > 1) {
             // this CTA's part of the shared B tile, into every CTA of the cluster
             tc::tma_load_2d_mc(sb + slot * kMxBStage + rank * (kMxBHalf * kMxBK), &maps.b, kx,
@@ -488,6 +504,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
     if (lane == 0) {
       uint32_t it = 0, tcount = 0;
       bool ok = true;
+      const uint32_t btype = g.b_fp4 ? tc::kMxE2M1 : tc::kMxE4M3;
       for (int u = cid; ok && u < U; u += ncl, ++tcount) {
         MxUnit w;
         mx_unit(g, uoff, u, rank, w);
@@ -507,7 +524,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
           const uint32_t sfa = tmem + kMxSfCol0 + fs * kMxSfCols;
           const uint32_t sfb = sfa + 4;
           for (int j = 0; j < kv; ++j)
-            tc::mma_mx_ss(dt, ad + 2 * j, bd + 2 * j, tc::idesc_mx_e4m3(kMxBM, kMxBN, j, j), sfa, sfb,
+            tc::mma_mx_ss(dt, ad + 2 * j, bd + 2 * j, tc::idesc_mx(kMxBM, kMxBN, j, j, btype), sfa, sfb,
                           (s | j) != 0 ? 1u : 0u);
           if constexpr (kMxCl > 1) tc::mma_commit_mc(&empty[slot], (uint16_t)((1u << kMxCl) - 1));
           else tc::mma_commit(&empty[slot]);
@@ -659,19 +676,28 @@ static EncodeTiledFnMx encode_fn_mx() {
   return fn;
 }
 
-// Byte matrix [rows][cols] (cols = K, contiguous) as a 2-D tensor map with
-// boxes of 128 K-bytes x box_rows rows, 128-byte swizzle; reads past either
-// edge return zero.
-bool make_tmap_mx(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows) {
+// Matrix [rows][cols] (cols = K elements, contiguous) as a 2-D tensor map
+// with boxes of 128 K-elements x box_rows rows, 128-byte swizzle; reads past
+// either edge return zero. fp4: packed E2M1 pairs (cols / 2 bytes a row;
+// the unpacking copy wants cols % 128 == 0 and a 32-byte aligned base).
+bool make_tmap_mx(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows, bool fp4) {
   EncodeTiledFnMx fn = encode_fn_mx();
-  if (!fn || cols % 16 != 0 || ((uintptr_t)base & 15u)) return false;
+  if (!fn || cols % (fp4 ? 128 : 16) != 0 || ((uintptr_t)base & (fp4 ? 31u : 15u))) return false;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)std::max<int64_t>(rows, 1)};
-  cuuint64_t strides[1] = {(cuuint64_t)cols};
+  cuuint64_t strides[1] = {(cuuint64_t)(fp4 ? cols / 2 : cols)};
   cuuint32_t box[2] = {(cuuint32_t)kMxBK, (cuuint32_t)box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+  return fn(map, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The four A maps of one E4M3 matrix, boxes of 16 / 32 / 64 / 128 rows.
+bool make_tmaps_mx_a(MxMaps* maps, const void* base, int64_t rows, int64_t cols) {
+  for (int i = 0; i < 4; ++i)
+    if (!make_tmap_mx(&maps->a[i], base, rows, cols, 16 << i, false)) return false;
+  return true;
 }
 
 template <int MODE>

@@ -169,6 +169,7 @@ struct MxArgs {
   const int32_t* poff;          // [G + 1] padded token rows per group
   const uint8_t* a_sf; int64_t a_sf_ld; int64_t a_rows;   // A scales, SF4 with ld = a_sf_ld; rows < a_rows exist
   const uint8_t* b_sf; int64_t b_sf_ld; int64_t b_rows;   // B scales, SF4
+  int b_fp4;                    // B elements are E2M1 (MXFP4 weights), else E4M3
   int64_t R;                    // token rows (A rows of the token-side modes)
   const float* w_row;           // [R] routing weight per row
   ActParams act;
@@ -185,9 +186,15 @@ struct MxArgs {
   int32_t* status;
 };
 struct MxMaps {
-  CUtensorMap a, b;             // boxes of 128 K-bytes x 128 (A) / mx_b_box_rows() (B) rows
+  CUtensorMap a[4];             // A boxes of 128 K-elements x 16 << i rows (the tile's rows pick one)
+  CUtensorMap b;                // B box of 128 K-elements x mx_b_box_rows() rows
 };
-bool make_tmap_mx(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows);
+// Matrix [rows][cols elements] as a 2-D tensor map, boxes of 128 elements x
+// box_rows rows, 128-byte swizzle, zero fill past the edges. fp4: packed
+// E2M1 (two per byte in memory) unpacked to one element per byte in shared
+// memory, the layout the block-scaled MMA reads; else one byte per element.
+bool make_tmap_mx(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows, bool fp4);
+bool make_tmaps_mx_a(MxMaps* maps, const void* base, int64_t rows, int64_t cols);
 int mx_tile_n();
 int mx_b_box_rows();          // rows of B per tensor copy (each CTA of a pair copies this many)
 int mx_tile_m();
@@ -250,9 +257,10 @@ cudaError_t launch_prepack_nv(const uint8_t* q, const uint8_t* s, int G, int N, 
                               int64_t tile_bytes, uint8_t* dst, cudaStream_t st);
 cudaError_t launch_unpack_nv(const uint8_t* src, int G, int N, int K, int interleave_I, int tiles, int64_t tile_bytes,
                              uint8_t* q, uint8_t* s, cudaStream_t st);
-cudaError_t launch_prepack_mx(const uint8_t* q, const uint8_t* s, int G, int N, int K, int interleave_I, int NR,
-                              uint8_t* dq, uint8_t* ds, cudaStream_t st);
-cudaError_t launch_unpack_mx(const uint8_t* dq, const uint8_t* ds, int G, int N, int K, int interleave_I, int NR,
-                             uint8_t* q, uint8_t* s, cudaStream_t st);
+// MXFP8 / MXFP4 rows: cb = code bytes per row (K, or K/2 for packed E2M1).
+cudaError_t launch_prepack_mx(const uint8_t* q, const uint8_t* s, int G, int N, int K, int64_t cb, int interleave_I,
+                              int NR, uint8_t* dq, uint8_t* ds, cudaStream_t st);
+cudaError_t launch_unpack_mx(const uint8_t* dq, const uint8_t* ds, int G, int N, int K, int64_t cb, int interleave_I,
+                             int NR, uint8_t* q, uint8_t* s, cudaStream_t st);
 
 }  // namespace moe

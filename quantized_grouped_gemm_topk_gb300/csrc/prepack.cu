@@ -78,15 +78,16 @@ __global__ void __launch_bounds__(256) k_unpack_nv(const uint8_t* __restrict__ s
   }
 }
 
-// ---- MXFP8 ------------------------------------------------------------------
-// Codes: one thread per (group, packed row, 16-byte piece), [G][NR][K];
+// ---- MXFP8 / MXFP4 ------------------------------------------------------------
+// Codes: one thread per (group, packed row, 16-byte piece), [G][NR][cb]
+// (cb = K bytes for E4M3, K/2 for packed E2M1);
 // scales: one thread per (group, packed row, 4-block word), in the SF4
 // layout over all groups' rows (ld G * NR), so the GEMM's scale loaders read
 // one coalesced word per row and stage. Padding rows are zero.
 __global__ void __launch_bounds__(256) k_prepack_mx(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s,
-                                                    int G, int N, int K, int interleave_I, int NR,
+                                                    int G, int N, int K, int64_t cb, int interleave_I, int NR,
                                                     uint8_t* __restrict__ dq, uint8_t* __restrict__ ds) {
-  const int cpr = K / 16, spr = K / 32;
+  const int cpr = (int)(cb / 16), spr = K / 32;
   const int64_t total_c = (int64_t)G * NR * cpr;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total_c; idx += stride) {
@@ -94,9 +95,9 @@ __global__ void __launch_bounds__(256) k_prepack_mx(const uint8_t* __restrict__ 
     const int p = (int)((idx / cpr) % NR);
     const int g = (int)(idx / ((int64_t)cpr * NR));
     const int n = mx_pack_src_row(p, N, interleave_I);
-    const uint4 v = n >= 0 ? *reinterpret_cast<const uint4*>(q + ((int64_t)g * N + n) * K + c * 16)
+    const uint4 v = n >= 0 ? *reinterpret_cast<const uint4*>(q + ((int64_t)g * N + n) * cb + c * 16)
                            : make_uint4(0, 0, 0, 0);
-    *reinterpret_cast<uint4*>(dq + ((int64_t)g * NR + p) * K + c * 16) = v;
+    *reinterpret_cast<uint4*>(dq + ((int64_t)g * NR + p) * cb + c * 16) = v;
   }
   // scales: one thread per (group, packed row, 4-block word)
   const int wpr = (spr + 3) / 4;
@@ -115,9 +116,9 @@ __global__ void __launch_bounds__(256) k_prepack_mx(const uint8_t* __restrict__ 
 
 // Inverse of k_prepack_mx for the logical rows n < N.
 __global__ void __launch_bounds__(256) k_unpack_mx(const uint8_t* __restrict__ dq, const uint8_t* __restrict__ ds,
-                                                   int G, int N, int K, int interleave_I, int NR,
+                                                   int G, int N, int K, int64_t cb, int interleave_I, int NR,
                                                    uint8_t* __restrict__ q, uint8_t* __restrict__ s) {
-  const int cpr = K / 16, spr = K / 32;
+  const int cpr = (int)(cb / 16), spr = K / 32;
   const int64_t total_c = (int64_t)G * N * cpr, total_s = (int64_t)G * N * spr;
   const int64_t stride = (int64_t)gridDim.x * blockDim.x;
   const int h = kMxTileN / 2;
@@ -131,8 +132,8 @@ __global__ void __launch_bounds__(256) k_unpack_mx(const uint8_t* __restrict__ d
     const int n = (int)((idx / cpr) % N);
     const int g = (int)(idx / ((int64_t)cpr * N));
     const int p = packed_row(n);
-    *reinterpret_cast<uint4*>(q + ((int64_t)g * N + n) * K + c * 16) =
-        *reinterpret_cast<const uint4*>(dq + ((int64_t)g * NR + p) * K + c * 16);
+    *reinterpret_cast<uint4*>(q + ((int64_t)g * N + n) * cb + c * 16) =
+        *reinterpret_cast<const uint4*>(dq + ((int64_t)g * NR + p) * cb + c * 16);
   }
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total_s; idx += stride) {
     const int b = (int)(idx % spr);
@@ -164,20 +165,20 @@ cudaError_t launch_unpack_nv(const uint8_t* src, int G, int N, int K, int interl
   return cudaGetLastError();
 }
 
-cudaError_t launch_prepack_mx(const uint8_t* q, const uint8_t* s, int G, int N, int K, int interleave_I, int NR,
-                              uint8_t* dq, uint8_t* ds, cudaStream_t st) {
-  const int64_t total = (int64_t)G * NR * (K / 16);
+cudaError_t launch_prepack_mx(const uint8_t* q, const uint8_t* s, int G, int N, int K, int64_t cb, int interleave_I,
+                              int NR, uint8_t* dq, uint8_t* ds, cudaStream_t st) {
+  const int64_t total = (int64_t)G * NR * (cb / 16);
   if (total == 0) return cudaSuccess;
-  k_prepack_mx<<<grid_of(total), 256, 0, st>>>(q, s, G, N, K, interleave_I, NR, dq, ds);
+  k_prepack_mx<<<grid_of(total), 256, 0, st>>>(q, s, G, N, K, cb, interleave_I, NR, dq, ds);
   note_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_unpack_mx(const uint8_t* dq, const uint8_t* ds, int G, int N, int K, int interleave_I, int NR,
-                             uint8_t* q, uint8_t* s, cudaStream_t st) {
-  const int64_t total = (int64_t)G * N * (K / 16);
+cudaError_t launch_unpack_mx(const uint8_t* dq, const uint8_t* ds, int G, int N, int K, int64_t cb, int interleave_I,
+                             int NR, uint8_t* q, uint8_t* s, cudaStream_t st) {
+  const int64_t total = (int64_t)G * N * (cb / 16);
   if (total == 0) return cudaSuccess;
-  k_unpack_mx<<<grid_of(total), 256, 0, st>>>(dq, ds, G, N, K, interleave_I, NR, q, s);
+  k_unpack_mx<<<grid_of(total), 256, 0, st>>>(dq, ds, G, N, K, cb, interleave_I, NR, q, s);
   note_launch();
   return cudaGetLastError();
 }

@@ -277,12 +277,13 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::mxf8f6f4 block-scaled: E4M3 A and B
-// (K-major), UE8M0 scales, fp32 accumulator; sf_a / sf_b select the byte of
-// the 32-bit scale words (bits 29-30 and 4-5).
-__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int M, int N, int sf_a, int sf_b) {
+// Instruction descriptor, kind::mxf8f6f4 block-scaled: E4M3 A, B of format
+// btype (kMxE4M3 or kMxE2M1), both K-major, UE8M0 scales, fp32 accumulator;
+// sf_a / sf_b select the byte of the 32-bit scale words (bits 29-30 and 4-5).
+constexpr uint32_t kMxE4M3 = 0, kMxE2M1 = 5;
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, int sf_a, int sf_b, uint32_t btype) {
   return ((uint32_t)sf_b << 4)              // B scale-factor id
-         | (0u << 7) | (0u << 10)           // A, B format E4M3
+         | (kMxE4M3 << 7) | (btype << 10)   // A, B formats
          | ((uint32_t)(N >> 3) << 17)       // N / 8
          | (1u << 23)                       // scale format UE8M0
          | ((uint32_t)(M >> 4) << 24)       // M / 16

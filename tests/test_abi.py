@@ -49,6 +49,11 @@ def test_config_validation(lib):
     for b in bad:
         assert m.moe_config_validate(_cfg(**b)) == 1, b
     assert m.moe_config_validate(_cfg(act="swiglu_clamp", limit=7.0, alpha=1.702)) == 0
+    # MXFP4 rows move in 128-element runs: H and I multiples of 128
+    assert m.moe_config_validate(_cfg(wfmt="mxfp4")) == 0
+    assert m.moe_config_validate(_cfg(wfmt="mxfp4", H=320)) == 1
+    assert m.moe_config_validate(_cfg(wfmt="mxfp4", I=192)) == 1
+    assert m.moe_config_validate(_cfg(wfmt="mxfp8", H=320, I=192)) == 0
 
 
 def test_sizes(lib):
@@ -65,6 +70,11 @@ def test_sizes(lib):
     assert m.moe_train_sizes(c8, 16) % 32 == 0
     with pytest.raises(m.MoEError):
         m.moe_train_sizes(c8, 17)                            # T > T_max
+    c4 = _cfg(wfmt="mxfp4")
+    # codes K/2 bytes a row (as NVFP4) but E8M0 scales per 32: smaller than MXFP8
+    assert 0 < m.moe_packed_weights_size(c4) < m.moe_packed_weights_size(c8)
+    with pytest.raises(m.MoEError):
+        m.moe_packed_weights_size(c4, m.MOE_PACK_DGRAD)      # forward only
 
 
 def test_host_errors_enqueue_nothing(lib):

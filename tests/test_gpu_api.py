@@ -242,15 +242,17 @@ def test_launch_accounting_and_phases():
     assert all(b >= a for a, b in zip(ts, ts[1:]))
 
 
-@pytest.mark.parametrize("name,which", [("tiny", 0), ("train_small", 0), ("train_small", 1)])
+@pytest.mark.parametrize("name,which", [("tiny", 0), ("mxfp4", 0), ("train_small", 0), ("train_small", 1)])
 def test_packed_layout_round_trip(name, which):
     """moe_prepack_weights followed by moe_debug_unpack_weights gives back the
     source bytes of both matrices exactly (NVFP4 tiles with gate/up
-    interleave; MXFP8 rows with the 96 + 96 gate/up tiles, and the dgrad
-    copies)."""
+    interleave; MXFP8 and MXFP4 rows with the 96 + 96 gate/up tiles, and the
+    MXFP8 dgrad copies)."""
     dev = cuda_device()
     if name == "tiny":
         s = inputs.workload("tiny", n_shared=1)
+    elif name == "mxfp4":
+        s = inputs.workload("tiny", H=384, I=384, E=5, k=2, n_shared=1, wfmt="mxfp4")
     else:
         s = inputs.workload("train", T=8, E=5, H=320, I=128)
     cfg = m.config_from_shape(s, T_max=8)

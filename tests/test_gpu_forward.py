@@ -191,3 +191,40 @@ def test_geglu_forward(name):
     _check_dispatch(s, r, f)
     assert_mx_close(np_(r["views"]["y1_q"]), np_(r["views"]["y1_s"]), f.y1q, f.y1s, "y1")
     assert_close_layer(np_(r["out"].float()), f.out, "out")
+
+
+@pytest.mark.parametrize("T", [16, 1, 33])
+def test_mxfp4_tiny_forward(T):
+    """MXFP4 weights (E2M1 elements, E8M0 scale per 32 along K) through the
+    block-scaled GEMM with E2M1 as the weight operand: every output against
+    the oracle, ragged token counts included."""
+    dev = cuda_device()
+    s = inputs.workload("tiny", T=T, wfmt="mxfp4")
+    r = run_forward(s, T, dev=dev, seed=5)
+    assert r["status"] == 0
+    f = oracle_forward(s, r)
+    _check_dispatch(s, r, f)
+    assert_mx_close(np_(r["views"]["y1_q"]), np_(r["views"]["y1_s"]), f.y1q, f.y1s, "y1")
+    assert_close_layer(np_(r["views"]["z"].view(torch.bfloat16).float()), f.z, "z")
+    assert_close_layer(np_(r["out"].float()), f.out, "out")
+
+
+def test_mxfp4_shared_expert():
+    """MXFP4 with one always-on shared expert and routed weights x2.5 (a
+    multi-tile expert axis: H=512, I=256, E=16)."""
+    dev = cuda_device()
+    s = inputs.workload("tiny", T=48, H=512, I=256, E=16, k=4, n_shared=1, routed_scale=2.5, wfmt="mxfp4")
+    r = run_forward(s, s.T, dev=dev, seed=6)
+    assert r["status"] == 0
+    f = oracle_forward(s, r)
+    _check_dispatch(s, r, f)
+    assert_close_layer(np_(r["out"].float()), f.out, "out")
+
+
+@pytest.mark.parametrize("T", [1, 32, 128])
+def test_mxfp4_dsv3_decode(T):
+    """DeepSeek-V3-shaped decode (H=7168, I=2048, E=256, top-8) with MXFP4
+    weights at full size; dispatch in full, the expert path on up to 16
+    sampled tokens."""
+    s = inputs.workload("dsv3", T=T, wfmt="mxfp4")
+    _full_size_sampled(s, T, 1)
