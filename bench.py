@@ -6,9 +6,12 @@ T = 1, 8, 32 and 128 tokens, every layer on a fresh batch of synthetic tokens
 (so routing touches a different set of experts), with the L2 cache flushed
 (512 MiB write) before each layer and the flush kept out of the timing.
 Each layer call replays a CUDA graph holding one captured moe_layer_forward
-(the decode layer is launch-bound without one). The metric is microseconds
-per step (lower is better), the sum of the layers' device times; the per-T
-layer times are listed in ``config.per_T_us``.
+(the decode layer is launch-bound without one), timed by CUDA events
+recorded on the stream around the replay. The metric is microseconds per
+step (lower is better), the sum of the layers' device times; the per-T
+layer times are listed in ``config.per_T_us``. A twin graph of each layer
+with the library's phase events inside (replayed in the same loop, not part
+of the metric) gives the W1 and W2 GEMM kernels' own durations.
 
 ``e2e`` is the same step measured on the host clock through the public C ABI
 (no graph): per layer, perf_counter around the copy of the tokens from
@@ -18,6 +21,8 @@ and a synchronize.
 ``per_config`` adds the other workloads, each on its own inputs:
   * shared_decode  H=6144, I=1536, E=160 + 1 shared expert, top-8, x2.5,
                    T = 1, 16, 64 (graph-replayed layers, as the headline);
+  * mxfp4_decode   the headline's layers with MXFP4 weights (E2M1, E8M0
+                   scale per 32) on the block-scaled E4M3 x E2M1 GEMM;
   * skewed_prefill T=4096, H=4096, I=1536, E=128, top-8, Zipf(1.2) routing
                    with 30% of the experts empty, NVFP4 weights;
   * train          T=16384, H=I=2880, E=128, top-4, MXFP8 weights, clamped
@@ -301,7 +306,9 @@ def config_block(s, per_T):
          "T": list(DECODE_TS), "weights": s.wfmt, "activations": "mxfp8",
          "l2": "flushed by a 512 MiB write before every layer; flush not timed",
          "inputs": "fresh seeded batch per layer call; weights resident in HBM", "parallelism": "replica per GPU",
-         "launch": "each layer call is a CUDA graph of one moe_layer_forward; e2e calls the C ABI directly"}
+         "launch": "each layer call is a CUDA graph of one moe_layer_forward, timed by events recorded on the "
+                   "stream around its replay; GEMM kernel times come from a twin graph with phase events inside, "
+                   "replayed in the same loop; e2e calls the C ABI directly"}
     if per_T is not None:
         c["per_T_us"] = per_T
     return c
@@ -337,6 +344,7 @@ class DecodeBench:
         self.xs = {T: [inputs.gen_x(s, 100 + 1000 * T + i + 7919 * rank, device=dev, T=T) for i in range(nx)]
                    for T in Ts}
         self.outs = {T: torch.empty(T, s.H, dtype=torch.bfloat16, device=dev) for T in Ts}
+        self.fused = {T: m.moe_layer_fused(self.cfg, T) for T in Ts}
         # routing is deterministic: learn each batch's touched-group count once
         self.touched = {}
         for T in Ts:
@@ -347,23 +355,36 @@ class DecodeBench:
                 self.touched[(T, i)] = int((v["counts"] > 0).sum())
         torch.cuda.synchronize()
         assert m.moe_read_status(self.cfg, self.ws) == 0
-        # one CUDA graph per (T, batch): the whole layer forward captured
-        # once, with its phase events as event-record nodes
-        self.graphs, self.gev, self.glaunch = {}, {}, {}
+        # two CUDA graphs per (T, batch), each the whole layer forward:
+        # - plain: what a caller captures; timed from events recorded on the
+        #   stream right before and after its replay. Event-record nodes
+        #   inside a graph cut the programmatic-dependent-launch chaining of
+        #   the kernels around them (measured: ~20 us more per layer), so
+        #   the layer time never comes from an instrumented graph.
+        # - phased: the same forward with its phase events as event-record
+        #   nodes, replayed in the same timed loop; it gives the GEMM
+        #   kernels' own durations for the roofline.
+        self.graphs, self.pgraphs, self.gev, self.glaunch = {}, {}, {}, {}
         for T in Ts:
             for i in range(nx):
-                evs = [torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_N_PHASE_EVENTS)]
-                for e in evs:
-                    e.record()      # creates the event's handle
-                torch.cuda.synchronize()
                 g = torch.cuda.CUDAGraph()
-                m.moe_set_phase_events(evs)
                 with torch.cuda.graph(g):
                     m.moe_layer_forward(self.cfg, self.xs[T][i], self.Wr, None, T, self.packed, self.outs[T], None,
                                         self.ws)
                     self.glaunch[(T, i)] = m.moe_last_launch_count()
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(m.MOE_N_PHASE_EVENTS)]
+                for e in evs:
+                    e.record()      # creates the event's handle
+                torch.cuda.synchronize()
+                pg = torch.cuda.CUDAGraph()
+                m.moe_set_phase_events(evs)
+                with torch.cuda.graph(pg):
+                    m.moe_layer_forward(self.cfg, self.xs[T][i], self.Wr, None, T, self.packed, self.outs[T], None,
+                                        self.ws)
                 m.moe_set_phase_events(None)
-                self.graphs[(T, i)], self.gev[(T, i)] = g, evs
+                self.graphs[(T, i)], self.pgraphs[(T, i)], self.gev[(T, i)] = g, pg, evs
+        self.ev_a = {T: [torch.cuda.Event(enable_timing=True) for _ in range(nx)] for T in Ts}
+        self.ev_b = {T: [torch.cuda.Event(enable_timing=True) for _ in range(nx)] for T in Ts}
         torch.cuda.synchronize()
 
     def weight_bytes(self, T, i):
@@ -378,31 +399,57 @@ class DecodeBench:
         R = T * s.kp
         return self.touched[(T, i)] * w1_bytes_per_expert(s) + R * (s.H + s.H // 32) + R * (s.I + s.I // 32)
 
+    def gemm_bytes(self, T, i):
+        """Algorithmic bytes of the grouped-GEMM span (W1, its epilogue, W2):
+        every touched group's W1 and W2 with scales, the MXFP8 rows of x in,
+        the bf16 rows of z out."""
+        s = self.s
+        R = T * s.kp
+        return (self.touched[(T, i)] * (w1_bytes_per_expert(s) + w2_bytes_per_expert(s)) + R * (s.H + s.H // 32)
+                + R * s.H * 2)
+
     def run(self, K, warmup, flush):
         m = self.m
         for w in range(warmup):
             for T in self.Ts:
                 flush.zero_()
                 self.graphs[(T, w % self.nx)].replay()
+                flush.zero_()
+                self.pgraphs[(T, w % self.nx)].replay()
         torch.cuda.synchronize()
         res = {"layer_us": {T: [] for T in self.Ts}, "w1_us": 0.0, "w1_bytes": 0, "w2_us": 0.0, "launches": 0,
-               "layer_bytes": {T: [] for T in self.Ts}}
+               "gemm_us": 0.0, "gemm_bytes": 0, "gemm_launches": 0,
+               "layer_bytes": {T: [] for T in self.Ts}, "phased_layer_us": {T: [] for T in self.Ts}}
         for step in range(K):
             i = step % self.nx
             for T in self.Ts:
                 flush.zero_()
+                self.ev_a[T][i].record()
                 self.graphs[(T, i)].replay()
-                res["launches"] += self.glaunch[(T, i)]
+                self.ev_b[T][i].record()
+                flush.zero_()
+                self.pgraphs[(T, i)].replay()
+                res["launches"] += 2 * self.glaunch[(T, i)]
             # the graphs of this step are replayed again nx steps later: read
             # their events now (host-side wait, outside every device interval)
             torch.cuda.synchronize()
             for T in self.Ts:
                 e = self.gev[(T, i)]
-                res["layer_us"][T].append(e[0].elapsed_time(e[5]) * 1e3)
+                res["layer_us"][T].append(self.ev_a[T][i].elapsed_time(self.ev_b[T][i]) * 1e3)
+                res["phased_layer_us"][T].append(e[0].elapsed_time(e[5]) * 1e3)
                 res["layer_bytes"][T].append(self.weight_bytes(T, i))
                 res["w1_us"] += e[1].elapsed_time(e[2]) * 1e3
                 res["w2_us"] += e[3].elapsed_time(e[4]) * 1e3
                 res["w1_bytes"] += self.w1_bytes(T, i)
+                # the grouped-GEMM kernels: one fused W1 -> W2 launch, or the
+                # W1 and W2 launches around the separate epilogue kernel
+                if self.fused[T]:
+                    res["gemm_us"] += e[1].elapsed_time(e[2]) * 1e3
+                    res["gemm_launches"] += 1
+                else:
+                    res["gemm_us"] += (e[1].elapsed_time(e[2]) + e[3].elapsed_time(e[4])) * 1e3
+                    res["gemm_launches"] += 2
+                res["gemm_bytes"] += self.gemm_bytes(T, i)
         assert m.moe_read_status(self.cfg, self.ws) == 0
         return res
 
@@ -427,7 +474,7 @@ class DecodeBench:
         return total / K * 1e6, sum(T * s.H * 2 for T in self.Ts)
 
     def free(self):
-        del self.graphs, self.packed, self.ws, self.xs
+        del self.graphs, self.pgraphs, self.packed, self.ws, self.xs
         torch.cuda.empty_cache()
 
 
@@ -618,6 +665,7 @@ def run_ours(args, s, rank, world, local):
     hbm, bf16, bf16_sus, peak_kind = peaks()
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     bench = DecodeBench(m, s, DECODE_TS, dev, rank)
+    bench_fused = dict(bench.fused)
 
     if world > 1:
         torch.distributed.barrier()
@@ -637,25 +685,36 @@ def run_ours(args, s, rank, world, local):
     if world > 1:
         e2e_us = max_over_ranks(e2e_us, dev)
 
-    achieved = r["w1_bytes"] / (r["w1_us"] * 1e-6) / 1e9
+    # the dominant kernel, k_gemm_tc: at T <= 32 W1, its epilogue and W2 run
+    # as one persistent launch, at T = 128 as the W1 and W2 launches; each
+    # launch timed between the phase events around it
+    achieved = r["gemm_bytes"] / (r["gemm_us"] * 1e-6) / 1e9
     sha = kernel_source_sha()
     tr = traffic_per_launch(sha)
     roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-            "traffic": None, "kernel": "W1 grouped GEMM (k_gemm_tc)", "peak_source": f"{peak_kind} hbm_gbs",
-            "algorithmic_bytes": "touched experts x NVFP4 W1 bytes (2I*H/2 + 2I*H/16) + MXFP8 rows in and out",
-            "kernel_us_per_step": r["w1_us"] / K, "w2_gemm_us_per_step": r["w2_us"] / K}
+            "traffic": None,
+            "kernel": "grouped GEMM k_gemm_tc: one fused W1 -> W2 launch per layer where moe_layer_fused (T = 1, 8, "
+                      "32 here), else W1 and W2 launches (T = 128); the separate W1 epilogue kernel is not counted",
+            "fused_T": [T for T in DECODE_TS if bench_fused[T]],
+            "peak_source": f"{peak_kind} hbm_gbs",
+            "algorithmic_bytes": "per layer: touched experts x NVFP4 W1 + W2 bytes (2I*H*9/16 + H*I*9/16) + MXFP8 "
+                                 "rows of x in + bf16 rows of z out",
+            "kernel_us_per_step": r["gemm_us"] / K,
+            "algorithmic_bytes_per_launch": r["gemm_bytes"] / r["gemm_launches"],
+            "launch_us": r["gemm_us"] / r["gemm_launches"]}
     if tr is not None:
-        # DRAM bytes of one captured W1 launch over its algorithmic bytes,
-        # applied to this run's average algorithmic bytes per W1 launch
-        roof["traffic"] = tr["dram_over_algorithmic"] * r["w1_bytes"] / (K * len(DECODE_TS))
-        roof["traffic_note"] = (f"ncu dram__bytes_read+write of one W1 launch ({tr['captured']}) = "
+        # DRAM bytes of one captured launch over its algorithmic bytes,
+        # applied to this run's average algorithmic bytes per launch
+        roof["traffic"] = tr["dram_over_algorithmic"] * r["gemm_bytes"] / r["gemm_launches"]
+        roof["traffic_note"] = (f"ncu dram__bytes_read+write of one launch ({tr['captured']}) = "
                                 f"{tr['dram_over_algorithmic']:.4f} x its algorithmic bytes, scaled to this "
-                                f"run's average W1 launch")
+                                f"run's average launch")
     per_T_us = {str(T): statistics.median(v) for T, v in r["layer_us"].items()}
     layer_frac = {str(T): statistics.mean(r["layer_bytes"][T]) / (statistics.median(r["layer_us"][T]) * 1e-6) / 1e9
                   / hbm for T in DECODE_TS}
     clocks = clk.summary()
     cfgb = config_block(s, per_T_us)
+    cfgb["per_T_us_phased_twin"] = {str(T): statistics.median(v) for T, v in r["phased_layer_us"].items()}
     cfgb["per_T_layer_hbm_frac_of_measured"] = layer_frac
     line = {
         "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,

@@ -333,6 +333,19 @@ moe_status_t moe_layer_forward(const moe_config_t* cfg, const uint16_t* x, const
                                const float* logits_in, int T, const void* packed_w, uint16_t* out,
                                const moe_train_save_t* save, void* ws, void* stream);
 
+/* *fused (host) = 1 when moe_layer_forward with this config and T (and no
+ * training save) runs W1, its epilogue and W2 as one persistent kernel:
+ * NVFP4 weights, I <= 2048, at most 2 token rows per group on average. The
+ * last W1 tile of each group to finish converts the group's y1 rows into
+ * W2's operand and sets a flag that the group's W2 tiles wait for (bounded:
+ * MOE_DEV_TIMEOUT). Otherwise 0: W1, the epilogue kernel and W2 run as
+ * separate launches. Both give the same bits; the step-wise calls split K
+ * the same way at these sizes. Source: GC-MoE summary, Key contributions
+ * (the per-block W1-completion tracking that lets W2 start without a
+ * separate launch); FlashDMoE abstract (one persistent kernel for the
+ * layer). */
+moe_status_t moe_layer_fused(const moe_config_t* cfg, int T, int32_t* fused);
+
 /* ---- backward (MXFP8 weights, n_shared = 0) ------------------------------ */
 
 /* Gradients of L = sum(dout * out) for the forward that filled ws and save
@@ -371,6 +384,8 @@ int moe_last_launch_count(void);
  * stream: [0] at entry, [1] after routing, dispatch and the gather of the
  * W1 operand rows, [2] after the W1 grouped-GEMM kernel, [3] after the W1
  * epilogue, [4] after the W2 grouped-GEMM kernel, [5] after the combine.
+ * In the fused layer (moe_layer_fused) [2], [3] and [4] are recorded one
+ * after the other behind the one W1 -> W2 kernel.
  * NULL switches it off. Host only; the events must outlive the calls that
  * record them. A call made while its stream is being captured into a CUDA
  * graph records them as event-record nodes, so every replay of that graph

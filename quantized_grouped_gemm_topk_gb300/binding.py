@@ -36,6 +36,7 @@ EXPORTS = (
     "moe_dispatch", "moe_grouped_gemm_w1_swiglu_quant", "moe_grouped_gemm_w2", "moe_combine",
     "moe_layer_forward", "moe_layer_backward", "moe_read_status", "moe_clear_status", "moe_status_string",
     "moe_last_launch_count", "moe_set_phase_events", "moe_router_logits_noalloc", "moe_debug_unpack_weights",
+    "moe_layer_fused",
 )
 MOE_N_PHASE_EVENTS = 6
 
@@ -111,6 +112,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "moe_status_string": [ctypes.c_int],
         "moe_last_launch_count": [],
         "moe_set_phase_events": [ctypes.POINTER(ctypes.c_void_p)],
+        "moe_layer_fused": [cfgp, ctypes.c_int, ctypes.POINTER(ctypes.c_int32)],
         "moe_router_logits_noalloc": [cfgp, P, P, ctypes.c_int, P, P],
         "moe_debug_unpack_weights": [cfgp, P, ctypes.c_int, ctypes.c_int, P, P, P],
     }
@@ -195,6 +197,13 @@ def moe_status_string(code) -> str:
 
 def moe_last_launch_count() -> int:
     return load().moe_last_launch_count()
+
+
+def moe_layer_fused(cfg, T) -> bool:
+    """Whether moe_layer_forward runs W1 -> W2 as one persistent kernel at T."""
+    v = ctypes.c_int32(0)
+    _check("moe_layer_fused", load().moe_layer_fused(ctypes.byref(cfg), int(T), ctypes.byref(v)))
+    return bool(v.value)
 
 
 def moe_set_phase_events(events):

@@ -63,7 +63,7 @@ static int ceil_div(int a, int b) { return (a + b - 1) / b; }
 struct WsLayout {
   size_t status, logits, rpart, ids, wts, counts, offsets, touched, ntouch, poff, hist, base;
   size_t perm, inv, wrow, xq, xs, y1q, y1s, z;
-  size_t P, a16, y16, rexp1, rexp2;                       // NVFP4 path
+  size_t P, a16, y16, rexp1, rexp2, P2, fcnt;            // NVFP4 path (P2, fcnt: the fused layer)
   size_t xg, xgs, y1st;                                   // MXFP8 path: gathered x rows, y1 scales (SF4)
   size_t dzq, dzs, dzg, dzgs, dztq, dzts, dhq, dhs, dhtq, dhts, dxp, dwpart;   // backward
   size_t total;
@@ -104,6 +104,8 @@ static WsLayout ws_layout(const moe_config_t& c) {
     L.y16 = take((size_t)R * d.I * 2);
     L.rexp1 = take((size_t)R * 4);
     L.rexp2 = take((size_t)R * 4);
+    L.P2 = take((size_t)R * d.H * 4);
+    L.fcnt = take((size_t)tc_fused_counters(d.G) * 4);
   } else {
     L.xg = take((size_t)R * d.H);
     L.xgs = take((size_t)sf4_bytes(d.H, R));
@@ -461,6 +463,62 @@ struct TcRun {
   int S;
 };
 
+// The fused layer (NVFP4 weights, small decode batches: at most 2 rows per
+// group on average): W1, its epilogue and W2 in one persistent launch. It
+// removes the W1 epilogue kernel and the W1 -> W2 launch boundary, which
+// dominate at a few tokens; with more rows per group the per-tile epilogue
+// work inside the kernel (each W1 tile's activation and requant, each
+// group's conversion to the W2 operand) costs more than the boundary it
+// saves (measured on the DeepSeek-V3 shape: -7 us at T = 1, even at T = 8
+// and 32, +13 us at T = 128), and the separate kernels run instead.
+static bool fused_layer(const moe_config_t& c, int T) {
+  const int64_t R = (int64_t)T * (c.k + c.n_shared);
+  return !mx_path(c) && T > 0 && R <= 2LL * (c.E + c.n_shared) && c.I <= kFusedMaxI;
+}
+
+// The decoding GEMM's fields shared by its matrices.
+static void tc_common(TcArgs& g, const moe_config_t* c, const PackLayout& P, const void* packed, void* ws,
+                      const WsLayout& L, const int32_t* offsets) {
+  std::memset(&g, 0, sizeof(g));
+  g.hdr = reinterpret_cast<const PackHeader*>(packed);
+  g.which = MOE_PACK_FORWARD;
+  g.G = P.G;
+  g.offsets = offsets;
+  g.touched = at<int32_t>(ws, L.touched);
+  g.n_touched = at<int32_t>(ws, L.ntouch);
+  int sms = device_sms();
+  if (c->max_sms > 0) sms = std::min(sms, c->max_sms);
+  g.max_ctas = sms;
+  g.status = at<int32_t>(ws, L.status);
+}
+
+// Packed matrix `mat` (1 or 2) of `packed` as one matrix of the decoding
+// GEMM: B operand rows with exponents rexp, fp32 K-slice partials into out.
+static TcMat tc_mat(const moe_config_t* c, const PackLayout& P, int mat, const void* packed, int T,
+                    const int32_t* rexp, float* out, int sms) {
+  TcMat m;
+  std::memset(&m, 0, sizeof(m));
+  const uint8_t* b = reinterpret_cast<const uint8_t*>(packed);
+  if (mat == 1) {
+    m.w = b + P.off_w1; m.gs = reinterpret_cast<const float*>(b + P.off_gs1);
+    m.tile_bytes = P.tile_bytes1; m.tiles = P.tiles1; m.N = P.N1; m.K = P.K1; m.interleave_I = P.il1;
+  } else {
+    m.w = b + P.off_w2; m.gs = reinterpret_cast<const float*>(b + P.off_gs2);
+    m.tile_bytes = P.tile_bytes2; m.tiles = P.tiles2; m.N = P.N2; m.K = P.K2; m.interleave_I = 0;
+  }
+  m.act_rowexp = rexp;
+  m.out = out;
+  const int64_t R = (int64_t)T * (c->k + c->n_shared);
+  m.split_stride = R * m.N;
+  // The fused layer runs both matrices unsplit: W1's tiles then need no
+  // other CTA's partials, W2's units balance the load of W1's last round,
+  // and W2's units stay long enough to hide the per-unit check of their
+  // group's flag. The separate calls at those sizes split the same way, so
+  // the layer and its steps give the same bits.
+  m.S = fused_layer(*c, T) ? 1 : tc_splits(*c, T, m.tiles, m.K, sms);
+  return m;
+}
+
 // One grouped GEMM over packed matrix `mat` (1 or 2) of `packed`, B operand
 // the f16 rows a16 [T*k', K] with exponents rexp; fp32 K-slice partials into
 // the workspace buffer P.
@@ -468,35 +526,17 @@ static moe_status_t tc_gemm(const moe_config_t* c, const PackLayout& P, int mat,
                             const WsLayout& L, const int32_t* offsets, int T, const uint16_t* a16,
                             const int32_t* rexp, cudaStream_t st, TcRun* run) {
   TcArgs g;
-  const uint8_t* b = reinterpret_cast<const uint8_t*>(packed);
-  g.hdr = reinterpret_cast<const PackHeader*>(b);
-  g.which = MOE_PACK_FORWARD;
-  g.G = P.G;
-  if (mat == 1) {
-    g.w = b + P.off_w1; g.gs = reinterpret_cast<const float*>(b + P.off_gs1);
-    g.tile_bytes = P.tile_bytes1; g.tiles = P.tiles1; g.N = P.N1; g.K = P.K1; g.interleave_I = P.il1;
-  } else {
-    g.w = b + P.off_w2; g.gs = reinterpret_cast<const float*>(b + P.off_gs2);
-    g.tile_bytes = P.tile_bytes2; g.tiles = P.tiles2; g.N = P.N2; g.K = P.K2; g.interleave_I = 0;
-  }
-  g.offsets = offsets;
-  g.touched = at<int32_t>(ws, L.touched);
-  g.n_touched = at<int32_t>(ws, L.ntouch);
-  g.act_rowexp = rexp;
-  g.out = at<float>(ws, L.P);
+  tc_common(g, c, P, packed, ws, L, offsets);
+  g.nmat = 1;
+  g.m[0] = tc_mat(c, P, mat, packed, T, rexp, at<float>(ws, L.P), g.max_ctas);
   const int64_t R = (int64_t)T * (c->k + c->n_shared);
-  g.split_stride = R * g.N;
-  int sms = device_sms();
-  if (c->max_sms > 0) sms = std::min(sms, c->max_sms);
-  g.max_ctas = sms;
-  g.S = tc_splits(*c, T, g.tiles, g.K, sms);
-  g.status = at<int32_t>(ws, L.status);
   TcMaps maps;
-  if (!make_tmaps_b(&maps, a16, R, g.K)) return MOE_ERR_CUDA;
+  if (!make_tmaps_b(maps.m[0], a16, R, g.m[0].K)) return MOE_ERR_CUDA;
+  std::memcpy(&maps.m[1], &maps.m[0], sizeof(maps.m[0]));
   MOE_CHECK_CUDA(launch_gemm_tc(g, maps, tc_token_tile(T, c->k + c->n_shared, c->E + c->n_shared), st));
-  run->out = g.out;
-  run->split_stride = g.split_stride;
-  run->S = g.S;
+  run->out = g.m[0].out;
+  run->split_stride = g.m[0].split_stride;
+  run->S = g.m[0].S;
   return MOE_OK;
 }
 
@@ -550,6 +590,41 @@ static ActParams act_params(const moe_config_t* c) {
   p.alpha = c->act == MOE_ACT_SWIGLU_CLAMP ? c->act_alpha : 1.f;
   p.limit = c->act_limit;
   return p;
+}
+
+// W1 -> W2 in one launch of the decoding GEMM (the counters in the workspace
+// must be zero: the operand gather clears them). y1 (MXFP8) lands in y1q /
+// y1s; W2's fp32 K-slice partials in run2.
+static moe_status_t tc_fused(const moe_config_t* c, const moe_dispatch_t* d, int T, const void* packed, uint8_t* y1q,
+                             uint8_t* y1s, void* ws, cudaStream_t st, TcRun* run2) {
+  const WsLayout L = ws_layout(*c);
+  const PackLayout P = pack_layout(*c, MOE_PACK_FORWARD);
+  TcArgs g;
+  tc_common(g, c, P, packed, ws, L, d->offsets);
+  g.nmat = 2;
+  g.m[0] = tc_mat(c, P, 1, packed, T, at<int32_t>(ws, L.rexp1), at<float>(ws, L.P), g.max_ctas);
+  g.m[1] = tc_mat(c, P, 2, packed, T, at<int32_t>(ws, L.rexp2), at<float>(ws, L.P2), g.max_ctas);
+  // the kernel's fused W1 epilogue reads one K slice, in 16-token tiles
+  const int nt = tc_token_tile(T, c->k + c->n_shared, c->E + c->n_shared);
+  if (g.m[0].S != 1 || nt != 16) return MOE_ERR_UNSUPPORTED;
+  g.f.w_row = d->w_row;
+  g.f.act = act_params(c);
+  g.f.I = c->I;
+  g.f.y1q = y1q;
+  g.f.y1s = y1s;
+  g.f.y16 = at<uint16_t>(ws, L.y16);
+  g.f.y_rowexp = at<int32_t>(ws, L.rexp2);
+  g.f.cnt = at<int32_t>(ws, L.fcnt);
+  const int64_t R = (int64_t)T * (c->k + c->n_shared);
+  TcMaps maps;
+  if (!make_tmaps_b(maps.m[0], at<uint16_t>(ws, L.a16), R, g.m[0].K) ||
+      !make_tmaps_b(maps.m[1], g.f.y16, R, g.m[1].K))
+    return MOE_ERR_CUDA;
+  MOE_CHECK_CUDA(launch_gemm_tc(g, maps, nt, st));
+  run2->out = g.m[1].out;
+  run2->split_stride = g.m[1].split_stride;
+  run2->S = g.m[1].S;
+  return MOE_OK;
 }
 
 // W1 with its fused epilogue. NVFP4: f16 operand rows (unless a_ready),
@@ -733,6 +808,10 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
     if (mx_path(*c))
       MOE_CHECK_CUDA(launch_gather_mx(v.d.xq, v.d.xs, c->H, v.d.perm_src, kp, T * kp, v.d.offsets, G,
                                       at<uint8_t>(ws, L.xg), at<uint8_t>(ws, L.xgs), st));
+    else if (fused_layer(*c, T) && !save)
+      MOE_CHECK_CUDA(launch_act_f16(v.d.xq, v.d.xs, c->H, v.d.perm_src, kp, T * kp, v.d.offsets, G,
+                                    at<uint16_t>(ws, L.a16), at<int32_t>(ws, L.rexp1), st, at<int32_t>(ws, L.fcnt),
+                                    tc_fused_counters(G)));
     else
       MOE_CHECK_CUDA(launch_act_f16(v.d.xq, v.d.xs, c->H, v.d.perm_src, kp, T * kp, v.d.offsets, G,
                                     at<uint16_t>(ws, L.a16), at<int32_t>(ws, L.rexp1), st));
@@ -749,6 +828,16 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
     q.C = c->H; q.offsets = v.d.offsets; q.poff = at<int32_t>(ws, L.poff); q.G = G;
     q.r_pad_max = r_pad_for(dims_of(*c), T); q.q = save->at_q; q.s = save->at_s;
     MOE_CHECK_CUDA(launch_quant_cols(q, st));
+  }
+  if (fused_layer(*c, T) && !save) {
+    TcRun run;
+    if ((s = tc_fused(c, &v.d, T, packed_w, v.y1_q, v.y1_s, ws, st, &run)) != MOE_OK) return s;
+    phase(2, st);
+    phase(3, st);
+    phase(4, st);
+    MOE_CHECK_CUDA(launch_finalize_combine(run.out, run.S, run.split_stride, c->H, v.d.inv, T, kp, v.z, out, st));
+    phase(5, st);
+    return MOE_OK;
   }
   if ((s = w1_impl(c, &v.d, T, packed_w, v.y1_q, v.y1_s, save, ws, st, true)) != MOE_OK) return s;
   if (mx_path(*c)) {
@@ -905,6 +994,14 @@ const char* moe_status_string(moe_status_t s) {
 }
 
 int moe_last_launch_count(void) { return launch_count(); }
+
+moe_status_t moe_layer_fused(const moe_config_t* c, int T, int32_t* fused) {
+  moe_status_t s = check_T(c, T);
+  if (s != MOE_OK) return s;
+  if (!fused) return MOE_ERR_INVALID_ARG;
+  *fused = fused_layer(*c, T) ? 1 : 0;
+  return MOE_OK;
+}
 
 moe_status_t moe_set_phase_events(void* const* events) {
   if (!events) {

@@ -226,6 +226,30 @@ __device__ __forceinline__ void pdl_enter() {
   pdl_trigger();
 }
 
+// gpu-scope acquire load / release store of a flag another CTA sets or reads.
+__device__ __forceinline__ int ld_acquire_gpu(const int32_t* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_gpu(int32_t* p, int v) {
+  asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// gpu-scope atomic add with acquire and release semantics; returns the old
+// value. After a CTA barrier, one thread's release publishes the writes of
+// every thread that reached the barrier; after its acquire and a barrier,
+// every thread sees what the releasing CTAs published.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int32_t* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+// Orders this thread's generic-proxy global accesses with its async-proxy
+// (tensor copy) ones.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 __device__ __forceinline__ void set_status(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
 }

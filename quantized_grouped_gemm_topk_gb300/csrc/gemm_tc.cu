@@ -71,6 +71,9 @@ struct TcCfg {
   // holds all of them and the epilogue adds them.
   static constexpr int P = NT <= 32 ? 4 : 2;                         // MMA issuers
   static constexpr int DStride = P * NT;                             // TMEM columns per D buffer
+  // D buffers: three where they fit next to the A buffers (16-token tiles),
+  // so the epilogue may fall two units behind the MMAs when units are short
+  static constexpr int ND = kDCol0 + 3 * DStride <= kTmemCols ? 3 : 2;
   static constexpr int CB = 4608;                                    // NVFP4 chunk bytes
   // A stage is one pair of chunks, so every stage feeds exactly one decoder
   // group and one MMA issuer: weight slot s always belongs to group
@@ -100,29 +103,26 @@ constexpr int kUnitTab = 512;
 constexpr int kMaxSplits = 64;
 struct UnitTab {
   int e[kUnitTab], r0[kUnitTab], r1[kUnitTab];
-  int cb[kMaxSplits + 1];   // K-slice s covers chunks [cb[s], cb[s + 1])
+  int cb[2][kMaxSplits + 1];   // matrix m's K slice s covers chunks [cb[m][s], cb[m][s + 1])
 };
 
-// Work unit u = (ti * tiles + j) * S + s, visited as u = blockIdx.x,
-// blockIdx.x + gridDim.x, ...; the mixed-radix digits are advanced by the
-// precomputed digits of gridDim.x, with no division per step.
+// Work unit u = (ti * tiles + j) * S + s of one matrix; the mixed-radix
+// digits are advanced by the precomputed digits of gridDim.x, with no
+// division per step.
 struct UnitIt {
-  uint32_t ti, j, s;
+  uint32_t ti, j, s, mat;
 };
 struct UnitStep {
   uint32_t dti, dj, ds, tiles, S;
-  __device__ UnitStep(const TcArgs& g) {
-    tiles = (uint32_t)g.tiles;
-    S = (uint32_t)g.S;
+  __device__ void init(int tiles_, int S_) {
+    tiles = (uint32_t)tiles_;
+    S = (uint32_t)S_;
     const uint32_t step = gridDim.x;
     ds = step % S;
     dj = (step / S) % tiles;
     dti = step / (S * tiles);
   }
-  __device__ UnitIt first() const {
-    const uint32_t b = blockIdx.x;
-    return UnitIt{b / (S * tiles), (b / S) % tiles, b % S};
-  }
+  __device__ UnitIt at(uint32_t u, uint32_t mat) const { return UnitIt{u / (S * tiles), (u / S) % tiles, u % S, mat}; }
   __device__ void next(UnitIt& it) const {
     it.s += ds;
     uint32_t cj = 0;
@@ -131,6 +131,45 @@ struct UnitStep {
     uint32_t ct = 0;
     if (it.j >= tiles) { it.j -= tiles; ct = 1; }
     it.ti += dti + ct;
+  }
+};
+
+// A CTA's walk over the units: u = blockIdx.x, blockIdx.x + gridDim.x, ...
+// through matrix 0's n_groups * tiles * S units and, in the fused layer, on
+// through matrix 1's; every role visits the same sequence. Kept in shared
+// memory (set once per CTA): the role loops then hold only their iterator
+// in registers.
+struct UnitWalk {
+  UnitStep st0, st1;
+  uint32_t n_groups, u0;   // u0: units of matrix 0
+  int nmat;
+  __device__ void init(const TcArgs& g, uint32_t ng) {
+    st0.init(g.m[0].tiles, g.m[0].S);
+    st1.init(g.m[g.nmat - 1].tiles, g.m[g.nmat - 1].S);
+    n_groups = ng;
+    u0 = ng * (uint32_t)g.m[0].tiles * (uint32_t)g.m[0].S;
+    nmat = g.nmat;
+  }
+  __device__ UnitIt first() const {
+    UnitIt it = st0.at(blockIdx.x, 0);
+    if (it.ti >= n_groups) to_second(it);
+    return it;
+  }
+  __device__ bool more(const UnitIt& it) const { return it.ti < n_groups; }
+  __device__ void next(UnitIt& it) const {
+    if (it.mat == 0) {
+      st0.next(it);
+      if (it.ti >= n_groups) to_second(it);
+    } else {
+      st1.next(it);
+    }
+  }
+  // the first unit of matrix 1 on this CTA's stride: the smallest u >= u0
+  // with u = blockIdx.x (mod gridDim.x), as an index into matrix 1's units
+  __device__ void to_second(UnitIt& it) const {
+    if (nmat < 2) return;
+    const uint32_t G = gridDim.x;
+    it = st1.at((blockIdx.x + G - u0 % G) % G, 1);
   }
 };
 
@@ -146,9 +185,125 @@ __device__ __forceinline__ bool tc_unit(const TcArgs& g, const UnitTab& tab, con
     w.r0 = g.offsets[w.e];
     w.r1 = g.offsets[w.e + 1];
   }
-  w.c0 = tab.cb[it.s];
-  w.c1 = tab.cb[it.s + 1];
+  w.c0 = tab.cb[it.mat][it.s];
+  w.c1 = tab.cb[it.mat][it.s + 1];
   return w.c1 > w.c0 && w.r1 > w.r0;
+}
+
+// Waits (bounded, as the mbarrier waits) for a flag another CTA sets with a
+// release store; acquire on success.
+__device__ __forceinline__ bool wait_flag(const int32_t* flag, volatile int* abort) {
+  const long long t0 = clock64();
+  for (uint32_t it = 0;; ++it) {
+    if (ld_acquire_gpu(flag) != 0) return true;
+    if ((it & 15) == 15) {
+      if (*abort) return false;
+      if (clock64() - t0 > 4000000000ll) {
+        *abort = 1;
+        return false;
+      }
+    }
+    __nanosleep(128);
+  }
+}
+
+// The four epilogue warps' own barrier, and the same barrier returning
+// whether v held in every one of its threads.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ bool epi_all(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.and.pred q, 1, 128, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"((uint32_t)v)
+      : "memory");
+  return r != 0;
+}
+
+// Fused layer, W1 tile (group w.e, features 64 j .. 64 j + 63 of gate and
+// up), its partials just written by this CTA's epilogue: y = w_row *
+// act(gate, up) and the MXFP8 requant per 32 features, the same arithmetic
+// as the separate epilogue kernel (which sums K slices; here there is one).
+// Warp q takes feature block q & 1 of the rows r0 + (q >> 1),
+// r0 + (q >> 1) + 2, ...
+__device__ __noinline__ void fused_w1_tile(const TcArgs& g, const TcUnit& w, int q, int lane) {
+  const TcFused& f = g.f;
+  const TcMat& M = g.m[0];
+  const int I = f.I, nb = I / 32;
+  const int b = q & 1;
+  const int fi = 64 * w.j + 32 * b + lane;
+  for (int r = w.r0 + (q >> 1); r < w.r1; r += 2) {
+    const float* P = M.out + (int64_t)r * 2 * I;
+    float gg = 0.f, uu = 0.f;
+#pragma unroll 4
+    for (int s = 0; s < M.S; ++s) {
+      gg += __ldcg(P + (int64_t)s * M.split_stride + fi);
+      uu += __ldcg(P + (int64_t)s * M.split_stride + I + fi);
+    }
+    const float y = f.w_row[r] * act_fwd(gg, uu, f.act);
+    const int e = mx_exponent(warp_max(fabsf(y)));
+    f.y1q[(int64_t)r * I + fi] = (uint8_t)(f32x2_to_e4m3x2(y * pow2_neg(e), 0.f) & 0xffu);
+    if (lane == 0) f.y1s[(int64_t)r * nb + 2 * w.j + b] = (uint8_t)(e + 127);
+  }
+}
+
+// Fused layer, after the group's last W1 tile: its rows as the W2 operand,
+// y16[r][i] = E4M3 value * 2^(block exponent - row exponent) with
+// y_rowexp[r] the row's largest block exponent (as the separate epilogue
+// kernel and k_act_f16 compute them). Warp q takes rows r0 + q, r0 + q + 4,
+// ...; a row's loads are issued four code words a lane at a time ahead of
+// the conversions (each is an L2 round trip: the rows were written by other
+// CTAs), the scale bytes shared across the warp by shuffles.
+__device__ __noinline__ void fused_w2_rows(const TcArgs& g, const TcUnit& w, int q, int lane) {
+  const TcFused& f = g.f;
+  const int I = f.I, nb = I / 32, nw = (I + 255) / 256;   // column words of 8 a lane (the last one partial)
+  constexpr int kB = 4;   // code words in flight per lane
+  for (int r = w.r0 + q; r < w.r1; r += 4) {
+    const uint8_t* ss = f.y1s + (int64_t)r * nb;
+    const uint8_t* qs = f.y1q + (int64_t)r * I;
+    uint2 codes[kB];
+#pragma unroll
+    for (int k = 0; k < kB; ++k)
+      codes[k] = lane * 8 + 256 * k < I ? __ldcg(reinterpret_cast<const uint2*>(qs + lane * 8 + 256 * k))
+                                        : make_uint2(0u, 0u);
+    // scale bytes of blocks lane and lane + 32
+    const int sb0 = lane < nb ? (int)__ldcg(ss + lane) : 0;
+    const int sb1 = lane + 32 < nb ? (int)__ldcg(ss + lane + 32) : 0;
+    int mx = max(sb0, sb1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(kFull, mx, o));
+    if (lane == 0) f.y_rowexp[r] = mx - 127;
+    for (int k0 = 0; k0 < nw; k0 += kB) {
+      if (k0 > 0) {
+#pragma unroll
+        for (int k = 0; k < kB; ++k)
+          codes[k] = lane * 8 + 256 * (k0 + k) < I
+                         ? __ldcg(reinterpret_cast<const uint2*>(qs + lane * 8 + 256 * (k0 + k)))
+                         : make_uint2(0u, 0u);
+      }
+#pragma unroll
+      for (int k = 0; k < kB; ++k) {
+        if (k0 + k >= nw) break;   // uniform across the warp
+        const int b = lane / 4 + 8 * (k0 + k);                 // block of columns lane * 8 + 256 (k0 + k)
+        const int v0 = __shfl_sync(kFull, sb0, b & 31), v1 = __shfl_sync(kFull, sb1, b & 31);
+        const float fs = ldexpf(1.0f, (b < 32 ? v0 : v1) - mx);
+        uint32_t outw[4];
+        const uint32_t cw[2] = {codes[k].x, codes[k].y};
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float2 lo = e4m3x2_to_f32x2((uint16_t)(cw[h] & 0xffffu));
+          const float2 hi = e4m3x2_to_f32x2((uint16_t)(cw[h] >> 16));
+          const __half2 h0 = __floats2half2_rn(lo.x * fs, lo.y * fs);
+          const __half2 h1 = __floats2half2_rn(hi.x * fs, hi.y * fs);
+          outw[2 * h] = *reinterpret_cast<const uint32_t*>(&h0);
+          outw[2 * h + 1] = *reinterpret_cast<const uint32_t*>(&h1);
+        }
+        if (lane * 8 + 256 * (k0 + k) < I)
+          *reinterpret_cast<uint4*>(f.y16 + (int64_t)r * I + lane * 8 + 256 * (k0 + k)) =
+              make_uint4(outw[0], outw[1], outw[2], outw[3]);
+      }
+    }
+  }
 }
 
 __device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
@@ -220,13 +375,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
   uint64_t* afull = bempty + C::BS;
   uint64_t* afree = afull + kTcNA;
   uint64_t* dfull = afree + kTcNA;
-  uint64_t* dfree = dfull + 2;
-  uint64_t* drain = dfree + 2;
+  uint64_t* dfree = dfull + C::ND;
+  uint64_t* drain = dfree + C::ND;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   __shared__ UnitTab tab;
+  __shared__ UnitWalk walk;
   __shared__ int bad_pack;
+  __shared__ int epi_last;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_enter();
   if (threadIdx.x == 0) {
@@ -243,8 +400,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       tab.r0[i] = g.offsets[e];
       tab.r1[i] = g.offsets[e + 1];
     }
-    const int nchunks = g.K / kChunkK;
-    for (int i = threadIdx.x; i <= g.S; i += blockDim.x) tab.cb[i] = (int)((int64_t)i * nchunks / g.S);
+    for (int m = 0; m < g.nmat; ++m) {
+      const int nchunks = g.m[m].K / kChunkK, S = g.m[m].S;
+      for (int i = threadIdx.x; i <= S; i += blockDim.x) tab.cb[m][i] = (int)((int64_t)i * nchunks / S);
+    }
   }
   if (threadIdx.x == 0) {
     for (int i = 0; i < C::WS; ++i) {
@@ -259,11 +418,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       tc::mbar_init(&afull[i], 4);     // one elected arrive per decoder warp
       tc::mbar_init(&afree[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::ND; ++i) {
       tc::mbar_init(&dfull[i], C::P);
       tc::mbar_init(&dfree[i], 4);     // one elected arrive per epilogue warp
     }
     tc::mbar_init(drain, C::P);     // one commit from each MMA issuer
+    walk.init(g, (uint32_t)*g.n_touched);   // groups with rows
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -273,8 +433,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
   tc::fence_after_sync();
   const uint32_t tmem = *tmem_slot;
 
-  const uint32_t n_groups = (uint32_t)*g.n_touched;   // groups with rows
-  const UnitStep ustep(g);
+
 
   // Every role walks the same sequence: units -> token tiles -> chunk pairs;
   // `ait` counts pairs (= weight stages).
@@ -285,10 +444,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       const uint64_t pol_w = tc::policy_evict_first();
       uint32_t wit = 0, issued = 0;   // issued: one past the last stage this thread issued
       bool ok = true;
-      for (UnitIt it = ustep.first(); ok && it.ti < n_groups; ustep.next(it)) {
+      for (UnitIt it = walk.first(); ok && walk.more(it); walk.next(it)) {
         TcUnit w;
         if (!tc_unit(g, tab, it, w)) continue;
-        const uint8_t* tile = g.w + ((int64_t)w.e * g.tiles + w.j) * g.tile_bytes;
+        const TcMat& M = g.m[it.mat];
+        const uint8_t* tile = M.w + ((int64_t)w.e * M.tiles + w.j) * M.tile_bytes;
         const uint32_t npt = (uint32_t)(w.c1 - w.c0 + 1) >> 1;   // chunk pairs per token tile
         for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT, wit += npt) {
           for (uint32_t i = first_own(wit, pid, 2); i < wit + npt; i += 2) {
@@ -316,13 +476,23 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
   } else if (warp == kWBProd) {
     // ---------------- activation producer ----------------
     if (lane == 0) {
-      for (int i = 0; i < 4; ++i) tc::prefetch_tmap(&maps.m[i]);
+      for (int m = 0; m < g.nmat; ++m)
+        for (int i = 0; i < 4; ++i) tc::prefetch_tmap(&maps.m[m][i]);
       const uint64_t pol_a = tc::policy_evict_last();
+      const int32_t* ready = g.f.cnt + g.G;
       uint32_t ait = 0;
+      int ready_e = -1;
       bool ok = true;
-      for (UnitIt it = ustep.first(); ok && it.ti < n_groups; ustep.next(it)) {
+      for (UnitIt it = walk.first(); ok && walk.more(it); walk.next(it)) {
         TcUnit w;
         if (!tc_unit(g, tab, it, w)) continue;
+        if (it.mat == 1 && w.e != ready_e) {
+          // fused layer: the group's W2 operand rows are written by the CTA
+          // that finished its last W1 tile; the copies below read them
+          if (!wait_flag(ready + w.e, abort)) { ok = false; break; }
+          fence_proxy_async_global();
+          ready_e = w.e;
+        }
         for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT) {
           const int bi = box_index(min(NT, w.r1 - t0));
           const uint32_t b_bytes = 2u * (8u << bi) * 128u;
@@ -331,7 +501,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
             if (!tc::mbar_wait(&bempty[bs], ((ait / C::BS) & 1) ^ 1, abort)) { ok = false; break; }
             tc::mbar_arrive_expect_tx(&bfull[bs], b_bytes);
             // 2 chunks x (8 << bi) rows; a chunk past K reads as zero
-            tc::tma_load_3d(bring + bs * C::BSlot, &maps.m[bi], 0, t0, c, &bfull[bs], pol_a);
+            tc::tma_load_3d(bring + bs * C::BSlot, &maps.m[it.mat][bi], 0, t0, c, &bfull[bs], pol_a);
           }
         }
       }
@@ -350,7 +520,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
     if (lane == 0 && mine < (uint32_t)C::P) {
       uint32_t ait = 0, dit = 0;
       bool ok = true;
-      for (UnitIt it = ustep.first(); ok && it.ti < n_groups; ustep.next(it)) {
+      for (UnitIt it = walk.first(); ok && walk.more(it); walk.next(it)) {
         TcUnit w;
         if (!tc_unit(g, tab, it, w)) continue;
         for (int t0 = w.r0; ok && t0 < w.r1; t0 += NT) {
@@ -358,8 +528,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
           const int nmma = ((nv + 15) >> 4) << 4;
           const uint32_t b_chunk = (8u << box_index(nv)) * 128u;   // bytes per chunk in an activation slot
           const uint32_t idesc = tc::idesc_f16_f32(128, nmma);
-          const int d = dit & 1;
-          if (!tc::mbar_wait(&dfree[d], ((dit >> 1) & 1) ^ 1, abort)) { ok = false; break; }
+          const int d = dit % C::ND;
+          if (!tc::mbar_wait(&dfree[d], ((dit / C::ND) & 1) ^ 1, abort)) { ok = false; break; }
           tc::fence_after_sync();
           const uint32_t dt = tmem + kDCol0 + d * C::DStride + mine * NT;
           const uint32_t npt = (uint32_t)(w.c1 - w.c0 + 1) >> 1;   // chunk pairs per token tile
@@ -405,7 +575,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     uint32_t ait = 0;
     bool ok = true;
-    for (UnitIt it = ustep.first(); ok && it.ti < n_groups; ustep.next(it)) {
+    for (UnitIt it = walk.first(); ok && walk.more(it); walk.next(it)) {
       TcUnit w;
       if (!tc_unit(g, tab, it, w)) continue;
       const uint32_t npt = (uint32_t)(w.c1 - w.c0 + 1) >> 1;   // chunk pairs per token tile
@@ -441,52 +611,93 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
     const int q = warp & 3;
     const int p = q * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
+    const int32_t* ready = g.f.cnt + g.G;
+    int ready_e = -1;
     uint32_t dit = 0, ait = 0;
     bool ok = true;
-    for (UnitIt it = ustep.first(); ok && it.ti < n_groups; ustep.next(it)) {
+    for (UnitIt it = walk.first(); ok && walk.more(it); walk.next(it)) {
       TcUnit w;
       if (!tc_unit(g, tab, it, w)) continue;
+      const TcMat& M = g.m[it.mat];
+      if (it.mat == 1 && w.e != ready_e) {
+        // fused layer: the row exponents of the group's W2 operand come from
+        // another CTA (already published: the MMAs consumed those rows)
+        if (!wait_flag(ready + w.e, abort)) { ok = false; break; }
+        ready_e = w.e;
+      }
       // chunk pairs per token tile (the sequence the issuers walk)
       const int pairs = (w.c1 - w.c0 + 1) >> 1;
       int n;
-      if (g.interleave_I > 0) n = p < 64 ? 64 * w.j + p : g.interleave_I + 64 * w.j + (p - 64);
+      if (M.interleave_I > 0) n = p < 64 ? 64 * w.j + p : M.interleave_I + 64 * w.j + (p - 64);
       else n = kTileN * w.j + p;
-      const bool nvalid = n < g.N;
-      const float rowf = g.gs[w.e];
-      float* outp = g.out + (int64_t)w.s * g.split_stride + n;
+      const bool nvalid = n < M.N;
+      const float rowf = M.gs[w.e];
+      float* outp = M.out + (int64_t)w.s * M.split_stride + n;
       for (int t0 = w.r0; t0 < w.r1; t0 += NT) {
         const int nt = min(NT, w.r1 - t0);
-        // issuer m wrote its tile iff one of this tile's pairs had index = m (mod P)
+        // the tile's token exponents, one per lane, shuffled out per token
+        // below (W2's in the fused layer come from another CTA: every lane
+        // did its own acquire of the group's flag before these loads)
+        const int rx0 = lane < nt ? M.act_rowexp[t0 + lane] : 0;
+        const int rx1 = NT > 32 && lane + 32 < nt ? M.act_rowexp[t0 + 32 + lane] : 0;
         const uint32_t a_first = ait;
         ait += pairs;
-        const int d = dit & 1;
-        if (!tc::mbar_wait(&dfull[d], (dit >> 1) & 1, abort)) { ok = false; break; }
+        const int d = dit % C::ND;
+        if (!tc::mbar_wait(&dfull[d], (dit / C::ND) & 1, abort)) { ok = false; break; }
         tc::fence_after_sync();
         for (int cb = 0; cb < nt; cb += 16) {
           float acc[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+          // issuer tiles in the order of the tile's own pair residues (pair
+          // k of the tile went to issuer (a_first + k) % P), so the sum does
+          // not depend on how many pairs this CTA ran before
 #pragma unroll
-          for (int ac = 0; ac < C::P; ++ac) {
-            if (pairs < C::P && (uint32_t)((ac - (int)(a_first % C::P) + C::P) % C::P) >= (uint32_t)pairs) continue;
+          for (int k = 0; k < C::P; ++k) {
+            if (k >= pairs) continue;
+            const int ac = (int)((a_first + (uint32_t)k) % C::P);
             uint32_t v[16];
             tc::tmem_ld16(lane_base + kDCol0 + d * C::DStride + ac * NT + cb, v);
             tc::tmem_wait_ld();
 #pragma unroll
             for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(v[i]);
           }
-          if (nvalid) {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int t = t0 + cb + i;
-              if (cb + i < nt) outp[(int64_t)t * g.N] = acc[i] * rowf * ldexpf(1.0f, g.act_rowexp[t]);
-            }
+          for (int i = 0; i < 16; ++i) {
+            const int rx = __shfl_sync(kFull, cb + i < 32 ? rx0 : rx1, (cb + i) & 31);   // every lane
+            if (nvalid && cb + i < nt) outp[(int64_t)(t0 + cb + i) * M.N] = acc[i] * rowf * ldexpf(1.0f, rx);
           }
         }
         tc::fence_before_sync();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&dfree[d]);
         ++dit;
+      }
+      if constexpr (NT == 16) if (it.mat == 0 && g.nmat > 1) {
+        // Fused layer (W1 unsplit along K; 16-token tiles only, the host
+        // runs it at a few rows per group): this unit wrote its tile's whole
+        // partials. The four warps agree first on whether all of them got
+        // here (a warp whose wait gave up arrives with ok = false), so none
+        // is left alone at the barriers below. Hand-offs between CTAs are
+        // the barrier, then one thread's gpu-scope release / acquire atomic
+        // (no full fence, which would wait out this SM's copies in flight).
+        if (!epi_all(ok)) { ok = false; break; }
+        int32_t* cnt = g.f.cnt;
+        const int tiles1 = g.m[0].tiles;
+        // act * w and the requant of the tile's features
+        fused_w1_tile(g, w, q, lane);
+        epi_sync();
+        if (warp == kWEpi && lane == 0) epi_last = atom_add_acq_rel_gpu(cnt + w.e, 1) == tiles1 - 1;
+        epi_sync();
+        if (epi_last) {
+          // the group's last tile: its rows as the W2 operand, then the
+          // flag its W2 units wait for (the tensor copies of other CTAs
+          // read y16: generic writes, the proxy fence, then the release)
+          fused_w2_rows(g, w, q, lane);
+          fence_proxy_async_global();
+          epi_sync();
+          if (warp == kWEpi && lane == 0) st_release_gpu(cnt + g.G + w.e, 1);
+        }
       }
     }
   }
@@ -524,7 +735,7 @@ static EncodeTiledFn encode_fn() {
 // f16 matrix [rows][cols] viewed as (64 columns, rows, cols / 64 chunks),
 // strides (2 B, cols * 2 B, 128 B); boxes of 64 x (8 << i) x 2 chunks,
 // 128-byte swizzle; rows past the end and chunks past the last read as zero.
-bool make_tmaps_b(TcMaps* maps, const void* base, int64_t rows, int64_t cols) {
+bool make_tmaps_b(CUtensorMap (&m)[4], const void* base, int64_t rows, int64_t cols) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || cols % kChunkK != 0) return false;
   cuuint64_t dims[3] = {(cuuint64_t)kChunkK, (cuuint64_t)std::max<int64_t>(rows, 1), (cuuint64_t)(cols / kChunkK)};
@@ -532,7 +743,7 @@ bool make_tmaps_b(TcMaps* maps, const void* base, int64_t rows, int64_t cols) {
   cuuint32_t estr[3] = {1, 1, 1};
   for (int i = 0; i < 4; ++i) {
     cuuint32_t box[3] = {(cuuint32_t)kChunkK, 8u << i, 2u};
-    if (fn(&maps->m[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+    if (fn(&m[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return false;
@@ -576,8 +787,11 @@ cudaError_t launch_gemm_tc(const TcArgs& g, const TcMaps& maps, int nt, cudaStre
 __global__ void __launch_bounds__(256) k_act_f16(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int C,
                                                  const int32_t* __restrict__ row_map, int row_div, int R,
                                                  const int32_t* __restrict__ offsets, int G, uint16_t* __restrict__ a16,
-                                                 int32_t* __restrict__ rowexp) {
+                                                 int32_t* __restrict__ rowexp, int32_t* __restrict__ zero,
+                                                 int64_t nzero) {
   pdl_enter();
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < nzero; i += (int64_t)gridDim.x * blockDim.x)
+    zero[i] = 0;
   const int lane = threadIdx.x & 31;
   const int Rv = min(R, offsets[G]);
   const int nsl = (C + 255) / 256;
@@ -615,12 +829,15 @@ __global__ void __launch_bounds__(256) k_act_f16(const uint8_t* __restrict__ q, 
 }
 
 cudaError_t launch_act_f16(const uint8_t* q, const uint8_t* s, int C, const int32_t* row_map, int row_div, int R,
-                           const int32_t* offsets, int G, uint16_t* a16, int32_t* rowexp, cudaStream_t st) {
+                           const int32_t* offsets, int G, uint16_t* a16, int32_t* rowexp, cudaStream_t st,
+                           int32_t* zero, int64_t nzero) {
   if (R == 0) return cudaSuccess;
+  if (!zero) nzero = 0;
   const int64_t warps = (int64_t)R * ((C + 255) / 256);
-  const int blocks = (int)std::min<int64_t>((warps + 7) / 8, (int64_t)device_sms() * 16);
+  const int64_t work = std::max<int64_t>((warps + 7) / 8, (nzero + 255) / 256);
+  const int blocks = (int)std::min<int64_t>(work, (int64_t)device_sms() * 16);
   cudaError_t e = launch_pdl(k_act_f16, dim3(blocks), dim3(256), 0, st, q, s, C, row_map, row_div, R, offsets, G,
-                             a16, rowexp);
+                             a16, rowexp, zero, nzero);
   note_launch();
   return e;
 }

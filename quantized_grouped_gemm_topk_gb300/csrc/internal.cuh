@@ -108,42 +108,70 @@ cudaError_t launch_quant_rows(const uint16_t* src, int rows, int C, uint8_t* q, 
 // out[s][r][n] = gs[e] * 2^act_rowexp[r] * sum_k W_e[n][k] * a16[r][k] over
 // K slice s; the f16 activation rows a16 [R][K] come in through a TMA
 // descriptor.
-struct TcArgs {
+// One matrix of the decoding GEMM.
+struct TcMat {
   const uint8_t* w;
   const float* gs;            // [G]
-  const PackHeader* hdr;      // the packed blob's header (checked on entry)
-  int which;                  // MOE_PACK_FORWARD / MOE_PACK_DGRAD expected in hdr
-  int G;
   int64_t tile_bytes;
   int tiles;
   int N, K;
   int interleave_I;
+  const int32_t* act_rowexp;  // [R]
+  float* out;                 // fp32 K-slice partials [S][R][N]
+  int64_t split_stride;
+  int S;
+};
+// The fused layer's W1 epilogue and hand-off (nmat == 2, W1 unsplit along
+// K): each W1 tile's unit applies act * w and the MXFP8 requant to the
+// tile's features; the last W1 tile of a group to finish converts the
+// group's y1 rows to the f16 W2 operand (y16, y_rowexp) and sets the
+// group's ready flag, which the W2 units of that group wait for.
+struct TcFused {
+  const float* w_row;         // [R]
+  ActParams act;
+  int I;
+  uint8_t* y1q; uint8_t* y1s; // [R][I], [R][I / 32]
+  uint16_t* y16;              // [R][I]
+  int32_t* y_rowexp;          // [R]
+  int32_t* cnt;               // [G] W1 tiles done, [G] ready flags; zero on entry
+};
+struct TcArgs {
+  TcMat m[2];                 // m[0]: the (first) matrix; m[1]: W2 of the fused layer
+  int nmat;                   // 1: one grouped GEMM over m[0]; 2: W1 -> W2 fused layer
+  const PackHeader* hdr;      // the packed blob's header (checked on entry)
+  int which;                  // MOE_PACK_FORWARD / MOE_PACK_DGRAD expected in hdr
+  int G;
   const int32_t* offsets;
   const int32_t* touched;
   const int32_t* n_touched;
-  const int32_t* act_rowexp;  // [R]
-  float* out;
-  int64_t split_stride;
-  int S;
   int max_ctas;
   int32_t* status;
+  TcFused f;
 };
+// Largest I the fused layer takes (a lane of the group conversion holds
+// I / 256 code words of a row in registers).
+constexpr int kFusedMaxI = 2048;
+// Ints of the fused layer's counters for G groups.
+inline int64_t tc_fused_counters(int G) { return 2LL * G; }
 // Tensor maps of the f16 operand rows a16 [rows, cols], viewed as
 // (64 columns, rows, cols / 64 chunks): m[i] loads a box of 8 << i rows of
 // two consecutive 64-column chunks in one copy (128-byte swizzle), stored
 // chunk after chunk.
 struct TcMaps {
-  CUtensorMap m[4];
+  CUtensorMap m[2][4];        // per matrix (the fused layer's W2 reads y16)
 };
-bool make_tmaps_b(TcMaps* maps, const void* base, int64_t rows, int64_t cols);
+bool make_tmaps_b(CUtensorMap (&m)[4], const void* base, int64_t rows, int64_t cols);
 // nt: tokens per MMA tile (16, 32 or 64); tc_token_tile picks it from the
 // average rows per group.
 int tc_token_tile(int T, int kp, int G);
 cudaError_t launch_gemm_tc(const TcArgs& g, const TcMaps& maps, int nt, cudaStream_t st);
 // a16[r] = f16 rows of the MXFP8 rows q/s [*, C] at row_map[r] / row_div
 // (or r), rowexp[r] = the row's largest block exponent.
+// zero / nzero (nullable): ints the kernel also sets to zero (the fused
+// layer's counters, cleared by the launch just before it).
 cudaError_t launch_act_f16(const uint8_t* q, const uint8_t* s, int C, const int32_t* row_map, int row_div, int R,
-                           const int32_t* offsets, int G, uint16_t* a16, int32_t* rowexp, cudaStream_t st);
+                           const int32_t* offsets, int G, uint16_t* a16, int32_t* rowexp, cudaStream_t st,
+                           int32_t* zero = nullptr, int64_t nzero = 0);
 
 // ---- block-scaled MXFP8 grouped GEMM (gemm_mx.cu) ----------------------------
 // D_e[m][n] = sum_k A[m][k] * B[n][k], both operands MXFP8 (E4M3 bytes,

@@ -125,3 +125,18 @@ def test_more_host_errors(lib):
     # status strings exist for every code
     for code in range(6):
         assert m.moe_status_string(code) not in ("", "unknown status")
+
+
+def test_layer_fused_rule(lib):
+    """The fused W1 -> W2 layer runs for NVFP4 weights, I <= 2048 and at most
+    2 token rows per group on average; otherwise the separate kernels."""
+    from quantized_grouped_gemm_topk_gb300 import binding as m
+    c = m.make_config(H=7168, I=2048, E=256, k=8, T_max=128)
+    assert [m.moe_layer_fused(c, T) for T in (0, 1, 8, 32, 64, 65, 128)] == [False, True, True, True, True, False,
+                                                                              False]
+    assert not m.moe_layer_fused(m.make_config(H=7168, I=2048, E=256, k=8, T_max=128, wfmt="mxfp8"), 8)
+    assert not m.moe_layer_fused(m.make_config(H=7168, I=2560, E=256, k=8, T_max=128), 8)
+    s = m.make_config(H=6144, I=1536, E=160, k=8, n_shared=1, T_max=64)   # 9 rows a token over 161 groups
+    assert m.moe_layer_fused(s, 35) and not m.moe_layer_fused(s, 36)
+    with pytest.raises(m.MoEError):
+        m.moe_layer_fused(c, 129)                                          # T > T_max

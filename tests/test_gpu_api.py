@@ -61,10 +61,22 @@ def _check_guards(t):
         assert _guards_intact(whole, n, fill), f"write outside {name}"
 
 
-@pytest.mark.parametrize("name,S", [("tiny", 0), ("tiny", 1)])
+@pytest.mark.parametrize("name,S", [("tiny", 0), ("tiny", 1), ("dsv3", 0), ("tiny_small", 0)])
 def test_stepwise_equals_layer_forward(name, S):
+    """The step-wise calls (router, top-k, dispatch, W1 + epilogue, W2,
+    combine: one kernel chain each) give bit for bit what moe_layer_forward
+    gives. With at most 2 rows per expert on average the layer runs W1, its
+    epilogue and W2 as one persistent launch (DeepSeek-V3 shapes with E=32,
+    T=8: 64 token rows over 32 experts; tiny with T=4); tiny at T=16
+    (4 rows per expert, with and without a shared expert) takes the
+    separate kernels."""
     dev = cuda_device()
-    s = inputs.workload(name, n_shared=S, routed_scale=2.5 if S else 1.0)
+    if name == "dsv3":
+        s = inputs.workload("dsv3", T=8, E=32)
+    elif name == "tiny_small":
+        s = inputs.workload("tiny", T=4)
+    else:
+        s = inputs.workload(name, n_shared=S, routed_scale=2.5 if S else 1.0)
     T = s.T
     r = run_forward(s, T, dev=dev)
     cfg, ws = r["cfg"], r["ws"]
