@@ -489,7 +489,10 @@ def bench_shared_decode(m, dev, K, warmup, flush, hbm):
         gb = statistics.mean(r["layer_bytes"][T])
         out["per_T"][str(T)] = {"us_per_layer": us, "tokens_per_s": T / us * 1e6,
                                 "layer_bytes": gb, "hbm_frac_of_measured": gb / (us * 1e-6) / 1e9 / hbm}
-    out["w1_gemm_hbm_frac_of_measured"] = r["w1_bytes"] / (r["w1_us"] * 1e-6) / 1e9 / hbm
+    out["gemm_hbm_frac_of_measured"] = r["gemm_bytes"] / (r["gemm_us"] * 1e-6) / 1e9 / hbm
+    out["gemm_note"] = ("k_gemm_tc launches (the fused W1 -> W2 kernel where moe_layer_fused, else W1 and W2): "
+                        "touched groups' NVFP4 W1 + W2 bytes and the rows over their device time")
+    out["fused_T"] = [T for T in SHARED_TS if b.fused[T]]
     b.free()
     return out
 
