@@ -418,7 +418,7 @@ class DecodeBench:
                 self.pgraphs[(T, w % self.nx)].replay()
         torch.cuda.synchronize()
         res = {"layer_us": {T: [] for T in self.Ts}, "w1_us": 0.0, "w1_bytes": 0, "w2_us": 0.0, "launches": 0,
-               "gemm_us": 0.0, "gemm_bytes": 0, "gemm_launches": 0,
+               "gemm_us": 0.0, "gemm_bytes": 0, "gemm_bytes_fused": 0, "gemm_launches": 0,
                "layer_bytes": {T: [] for T in self.Ts}, "phased_layer_us": {T: [] for T in self.Ts}}
         for step in range(K):
             i = step % self.nx
@@ -446,6 +446,7 @@ class DecodeBench:
                 if self.fused[T]:
                     res["gemm_us"] += e[1].elapsed_time(e[2]) * 1e3
                     res["gemm_launches"] += 1
+                    res["gemm_bytes_fused"] += self.gemm_bytes(T, i)
                 else:
                     res["gemm_us"] += (e[1].elapsed_time(e[2]) + e[3].elapsed_time(e[4])) * 1e3
                     res["gemm_launches"] += 2
@@ -706,18 +707,26 @@ def run_ours(args, s, rank, world, local):
             "algorithmic_bytes_per_launch": r["gemm_bytes"] / r["gemm_launches"],
             "launch_us": r["gemm_us"] / r["gemm_launches"]}
     if tr is not None:
-        # DRAM bytes of one captured launch over its algorithmic bytes,
-        # applied to this run's average algorithmic bytes per launch
-        roof["traffic"] = tr["dram_over_algorithmic"] * r["gemm_bytes"] / r["gemm_launches"]
-        roof["traffic_note"] = (f"ncu dram__bytes_read+write of one launch ({tr['captured']}) = "
-                                f"{tr['dram_over_algorithmic']:.4f} x its algorithmic bytes, scaled to this "
-                                f"run's average launch")
+        # DRAM bytes over algorithmic bytes of a captured fused launch and a
+        # captured separate W1 launch, applied to this run's bytes of each
+        # kind, per launch
+        sep = r["gemm_bytes"] - r["gemm_bytes_fused"]
+        roof["traffic"] = (tr["dram_over_algorithmic_fused"] * r["gemm_bytes_fused"]
+                           + tr["dram_over_algorithmic_separate"] * sep) / r["gemm_launches"]
+        roof["traffic_note"] = (f"ncu dram__bytes_read+write ({tr['captured']}): "
+                                f"{tr['dram_over_algorithmic_fused']:.4f} (fused) and "
+                                f"{tr['dram_over_algorithmic_separate']:.4f} (separate) x the algorithmic bytes, "
+                                f"applied to this run's bytes, per launch")
     per_T_us = {str(T): statistics.median(v) for T, v in r["layer_us"].items()}
     layer_frac = {str(T): statistics.mean(r["layer_bytes"][T]) / (statistics.median(r["layer_us"][T]) * 1e-6) / 1e9
                   / hbm for T in DECODE_TS}
     clocks = clk.summary()
     cfgb = config_block(s, per_T_us)
     cfgb["per_T_us_phased_twin"] = {str(T): statistics.median(v) for T, v in r["phased_layer_us"].items()}
+    # groups touched by each T's first batch and its grouped-GEMM bytes (the
+    # layers an ncu capture of the first eager calls sees)
+    cfgb["batch0"] = {str(T): {"touched": bench.touched[(T, 0)], "gemm_bytes": bench.gemm_bytes(T, 0),
+                               "w1_bytes": bench.w1_bytes(T, 0), "fused": bench.fused[T]} for T in DECODE_TS}
     cfgb["per_T_layer_hbm_frac_of_measured"] = layer_frac
     line = {
         "metric": METRIC, "value": us_step, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
