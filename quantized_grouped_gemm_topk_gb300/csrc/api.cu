@@ -530,10 +530,14 @@ static moe_status_t tc_gemm(const moe_config_t* c, const PackLayout& P, int mat,
   g.nmat = 1;
   g.m[0] = tc_mat(c, P, mat, packed, T, rexp, at<float>(ws, L.P), g.max_ctas);
   const int64_t R = (int64_t)T * (c->k + c->n_shared);
+  const int nt = tc_token_tile(T, c->k + c->n_shared, c->E + c->n_shared);
+  // prefill-sized groups: units of at most 8 token tiles, so a hot group's
+  // rows spread over many CTAs
+  g.split_rows = nt >= 32 ? 8 * nt : 0;
   TcMaps maps;
   if (!make_tmaps_b(maps.m[0], a16, R, g.m[0].K)) return MOE_ERR_CUDA;
   std::memcpy(&maps.m[1], &maps.m[0], sizeof(maps.m[0]));
-  MOE_CHECK_CUDA(launch_gemm_tc(g, maps, tc_token_tile(T, c->k + c->n_shared, c->E + c->n_shared), st));
+  MOE_CHECK_CUDA(launch_gemm_tc(g, maps, nt, st));
   run->out = g.m[0].out;
   run->split_stride = g.m[0].split_stride;
   run->S = g.m[0].S;

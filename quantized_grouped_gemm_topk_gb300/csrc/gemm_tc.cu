@@ -81,7 +81,7 @@ struct TcCfg {
   // every phase of its slots in order.
   static constexpr int WSlot = (2 * CB + 1023) / 1024 * 1024;
   static constexpr int BSlot = 2 * NT * 128;                         // two chunks x NT rows x 64 f16
-  static constexpr int BS = NT == 16 ? 16 : NT == 32 ? 8 : 4;        // activation slots
+  static constexpr int BS = NT == 16 ? 16 : 8;                       // activation slots
   static constexpr int WSraw = (kSmemBudget - BS * BSlot) / WSlot / kTcNG * kTcNG;
   static constexpr int WS = WSraw > 24 ? 24 : WSraw;                 // weight stages
   static constexpr int SmemBytes = WS * WSlot + BS * BSlot + 1024 /*align*/ + 1024 /*barriers*/;
@@ -392,13 +392,65 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
   }
   __syncthreads();
   if (bad_pack) return;   // the blob is not the packing this GEMM reads: write nothing
+  __shared__ int vgroups;   // entries of the walk's group axis
   {
-    const int nt = min(*g.n_touched, kUnitTab);
-    for (int i = threadIdx.x; i < nt; i += blockDim.x) {
-      const int e = g.touched[i];
-      tab.e[i] = e;
-      tab.r0[i] = g.offsets[e];
-      tab.r1[i] = g.offsets[e + 1];
+    // The walk's groups: each touched group or, with split_rows > 0, each
+    // block of at most split_rows of its rows (a multiple of NT, so the
+    // token tiles are the same). A unit then covers at most split_rows / NT
+    // token tiles and the round-robin spreads a hot group over many CTAs;
+    // the weights are streamed once per token tile either way. When the
+    // blocks do not fit the table, whole groups.
+    __shared__ int scan_w[kTcThreads / 32 + 1];
+    const int ntouch = *g.n_touched;
+    const int RB = g.split_rows;
+    const bool split = RB > 0 && ntouch <= (int)blockDim.x;
+    const int i = threadIdx.x;
+    int nb = 0, e = 0, r0 = 0, r1 = 0;
+    if (split && i < ntouch) {
+      e = g.touched[i];
+      r0 = g.offsets[e];
+      r1 = g.offsets[e + 1];
+      nb = (r1 - r0 + RB - 1) / RB;
+    }
+    int incl = nb;   // block-wide exclusive scan of nb
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(kFull, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) scan_w[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      constexpr int nw = kTcThreads / 32;
+      const int v = lane < nw ? scan_w[lane] : 0;
+      int x = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+      }
+      if (lane < nw) scan_w[lane] = x - v;
+      if (lane == 31) scan_w[nw] = x;
+    }
+    __syncthreads();
+    const int total = scan_w[kTcThreads / 32];
+    if (split && total <= kUnitTab) {
+      const int base = scan_w[warp] + incl - nb;
+      for (int k = 0; k < nb; ++k) {
+        tab.e[base + k] = e;
+        tab.r0[base + k] = r0 + k * RB;
+        tab.r1[base + k] = min(r1, r0 + (k + 1) * RB);
+      }
+      if (i == 0) vgroups = total;
+    } else {
+      const int nt = min(ntouch, kUnitTab);
+      for (int j = i; j < nt; j += blockDim.x) {
+        const int ej = g.touched[j];
+        tab.e[j] = ej;
+        tab.r0[j] = g.offsets[ej];
+        tab.r1[j] = g.offsets[ej + 1];
+      }
+      if (i == 0) vgroups = ntouch;
     }
     for (int m = 0; m < g.nmat; ++m) {
       const int nchunks = g.m[m].K / kChunkK, S = g.m[m].S;
@@ -423,7 +475,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       tc::mbar_init(&dfree[i], 4);     // one elected arrive per epilogue warp
     }
     tc::mbar_init(drain, C::P);     // one commit from each MMA issuer
-    walk.init(g, (uint32_t)*g.n_touched);   // groups with rows
+    walk.init(g, (uint32_t)vgroups);   // groups with rows (or their row blocks)
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -635,11 +687,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       float* outp = M.out + (int64_t)w.s * M.split_stride + n;
       for (int t0 = w.r0; t0 < w.r1; t0 += NT) {
         const int nt = min(NT, w.r1 - t0);
-        // the tile's token exponents, one per lane, shuffled out per token
-        // below (W2's in the fused layer come from another CTA: every lane
-        // did its own acquire of the group's flag before these loads)
-        const int rx0 = lane < nt ? M.act_rowexp[t0 + lane] : 0;
-        const int rx1 = NT > 32 && lane + 32 < nt ? M.act_rowexp[t0 + 32 + lane] : 0;
+        // the tile's token scales 2^exponent, one per lane, shuffled out per
+        // token below (W2's exponents in the fused layer come from another
+        // CTA: every lane did its own acquire of the group's flag first)
+        const float px0 = ldexpf(1.0f, lane < nt ? M.act_rowexp[t0 + lane] : 0);
+        const float px1 = ldexpf(1.0f, NT > 32 && lane + 32 < nt ? M.act_rowexp[t0 + 32 + lane] : 0);
         const uint32_t a_first = ait;
         ait += pairs;
         const int d = dit % C::ND;
@@ -652,20 +704,35 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
           // issuer tiles in the order of the tile's own pair residues (pair
           // k of the tile went to issuer (a_first + k) % P), so the sum does
           // not depend on how many pairs this CTA ran before
-#pragma unroll
-          for (int k = 0; k < C::P; ++k) {
-            if (k >= pairs) continue;
-            const int ac = (int)((a_first + (uint32_t)k) % C::P);
-            uint32_t v[16];
-            tc::tmem_ld16(lane_base + kDCol0 + d * C::DStride + ac * NT + cb, v);
+          if constexpr (C::P == 2) {
+            // both issuers' tiles in flight behind one wait
+            uint32_t v0[16], v1[16];
+            const uint32_t base = lane_base + kDCol0 + d * C::DStride + cb;
+            tc::tmem_ld16(base + (a_first % 2) * NT, v0);
+            if (pairs > 1) tc::tmem_ld16(base + ((a_first + 1) % 2) * NT, v1);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(v[i]);
+            for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(v0[i]);
+            if (pairs > 1) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(v1[i]);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < C::P; ++k) {
+              if (k >= pairs) continue;
+              const int ac = (int)((a_first + (uint32_t)k) % C::P);
+              uint32_t v[16];
+              tc::tmem_ld16(lane_base + kDCol0 + d * C::DStride + ac * NT + cb, v);
+              tc::tmem_wait_ld();
+#pragma unroll
+              for (int i = 0; i < 16; ++i) acc[i] += __uint_as_float(v[i]);
+            }
           }
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int rx = __shfl_sync(kFull, cb + i < 32 ? rx0 : rx1, (cb + i) & 31);   // every lane
-            if (nvalid && cb + i < nt) outp[(int64_t)(t0 + cb + i) * M.N] = acc[i] * rowf * ldexpf(1.0f, rx);
+            const float px = __shfl_sync(kFull, cb + i < 32 ? px0 : px1, (cb + i) & 31);   // every lane
+            if (nvalid && cb + i < nt) outp[(int64_t)(t0 + cb + i) * M.N] = acc[i] * rowf * px;
           }
         }
         tc::fence_before_sync();

@@ -146,6 +146,7 @@ struct TcArgs {
   const int32_t* n_touched;
   int max_ctas;
   int32_t* status;
+  int split_rows;             // > 0: the walk takes groups in blocks of this many rows (a multiple of the token tile)
   TcFused f;
 };
 // Largest I the fused layer takes (a lane of the group conversion holds
