@@ -244,6 +244,15 @@ moe_status_t moe_prepack_weights(const moe_config_t* cfg, const moe_weights_view
 moe_status_t moe_debug_unpack_weights(const moe_config_t* cfg, const void* packed, int which, int mat,
                                       uint8_t* q, uint8_t* s, void* stream);
 
+/* Runs, in one thread, the bounded wait the fused layer's W2 tiles use on
+ * their group's ready flag (flag: device int32, waited on until non-zero),
+ * giving up after limit_cycles SM clock cycles (> 0) and then setting
+ * MOE_DEV_TIMEOUT in the workspace status word. For tests of the timeout
+ * path: a flag that nothing sets must end in MOE_DEV_TIMEOUT with the
+ * context still usable. The pages have no counterpart. */
+moe_status_t moe_debug_flag_wait(const moe_config_t* cfg, const int32_t* flag, int64_t limit_cycles, void* ws,
+                                 void* stream);
+
 /* ---- forward steps ------------------------------------------------------ */
 
 /* S1. logits [T, E] fp32 (device) = x [T, H] bf16 (device) . W_r [H, E] fp32

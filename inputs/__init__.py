@@ -55,6 +55,7 @@ class MoEShape:
     alpha: float = 1.0
     limit: float = 0.0
     wfmt: str = "nvfp4"          # "nvfp4" | "mxfp8" | "mxfp4"
+    bias: bool = False           # W1 carries a per-expert fp32 bias [2I] (gate b, up c)
     logits: str = "router"       # "router" (x @ W_r) | "zipf" (drawn directly)
 
     @property
@@ -284,6 +285,10 @@ def gen_one_expert(s: MoEShape, seed: int, e: int, device="cpu", dgrad_copies: b
             out["w2t_q"], out["w2t_s"] = encode_mxfp8(w2.t().contiguous())
     else:
         raise ValueError(s.wfmt)
+    if s.bias:
+        # its own generator: the weights' draws do not depend on the bias
+        out["b1"] = torch.randn(2 * I, generator=_gen((seed + 6) * 65536 + e, device), device=device,
+                                dtype=torch.float32) * 0.1
     return out
 
 
@@ -297,6 +302,7 @@ def gen_expert_weights(s: MoEShape, seed: int = 0, device="cpu", dgrad_copies: b
     w*_gs fp32 per (group, matrix). MXFP8 (bf16 master weights): w*_q E4M3
     [N, K], w*_s E8M0 [N, K/32], w*_gs = 1; the dgrad copies w1t_* [H, 2I] and
     w2t_* [I, H] are quantised along the other axis from the same draws.
+    With s.bias, b1 [G, 2I] fp32 ~N(0, 0.1) (gate then up).
     """
     G = s.groups
     if dgrad_copies is None:

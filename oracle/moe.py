@@ -21,7 +21,10 @@ Readings taken where the pages are silent (each listed in the design notes):
     ties in the logit order go to the lower expert id;
   * shared experts: every token, weight 1.0, slot k (after the routed slots);
   * rows of an expert are ordered by flat assignment index t*k' + j;
-  * W1 holds gate columns [0, I) then up columns [I, 2I); b = c = 0, beta = 1;
+  * W1 holds gate columns [0, I) then up columns [I, 2I); beta = 1; the
+    blog's b and c are an optional per-expert fp32 bias vector of W1's 2I
+    outputs (b for gate, c for up; the blog's fused epilogues add a "bias
+    vector", kernel families section), zero when the weights carry none;
   * the clamped variant is g' = clamp(g, -L, L), u' = clamp(u, -L, L),
     act = g' * sigmoid(alpha * g') * u';
   * the routing weight multiplies the SwiGLU output before requantisation;
@@ -188,6 +191,13 @@ def expert_w1(wts: dict, e: int, wfmt: str) -> np.ndarray:
     return F.mx_dequantize(wts["w1_q"][e], wts["w1_s"][e])
 
 
+def expert_b1(wts: dict, e: int, n: int) -> np.ndarray:
+    """W1's bias of group e, [2I] (gate b then up c), zeros if none."""
+    if "b1" not in wts:
+        return np.zeros(n)
+    return np.asarray(wts["b1"][e], np.float64).reshape(n)
+
+
 def expert_w2(wts: dict, e: int, wfmt: str) -> np.ndarray:
     """Decoded W2 of group e as stored: [H, I]."""
     if "w2_f64" in wts:
@@ -260,7 +270,7 @@ def layer_forward(x_bits, logits, wts: dict, *, E: int, k: int, n_shared: int = 
         toks = d.perm_src[rs] // kp
         A = a_tok[toks]                              # gathered rows [n, H]
         W1 = expert_w1(wts, e, wfmt)                 # [2I, H]
-        he = A @ W1.T                                # [n, 2I]
+        he = A @ W1.T + expert_b1(wts, e, 2 * I)     # [n, 2I]: xW + b | xV + c
         ye = d.w_row[rs, None] * act_fwd(he[:, :I], he[:, I:], act, alpha, limit)
         if quant:
             q, s = F.mx_quantize(ye)
@@ -315,7 +325,7 @@ def dense_forward(x_bits, logits, wts: dict, *, E: int, k: int, n_shared: int = 
     for e in range(G):
         W1 = expert_w1(wts, e, wfmt)
         W2 = expert_w2(wts, e, wfmt)
-        hh = a @ W1.T
+        hh = a @ W1.T + expert_b1(wts, e, 2 * I)
         yy = gate[:, e:e + 1] * act_fwd(hh[:, :I], hh[:, I:], act, alpha, limit)
         q, s = F.mx_quantize(yy)
         zz = F.mx_dequantize(q, s) @ W2.T

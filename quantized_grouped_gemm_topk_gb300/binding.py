@@ -36,7 +36,7 @@ EXPORTS = (
     "moe_dispatch", "moe_grouped_gemm_w1_swiglu_quant", "moe_grouped_gemm_w2", "moe_combine",
     "moe_layer_forward", "moe_layer_backward", "moe_read_status", "moe_clear_status", "moe_status_string",
     "moe_last_launch_count", "moe_set_phase_events", "moe_router_logits_noalloc", "moe_debug_unpack_weights",
-    "moe_layer_fused",
+    "moe_layer_fused", "moe_debug_flag_wait",
 )
 MOE_N_PHASE_EVENTS = 6
 
@@ -113,6 +113,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         "moe_last_launch_count": [],
         "moe_set_phase_events": [ctypes.POINTER(ctypes.c_void_p)],
         "moe_layer_fused": [cfgp, ctypes.c_int, ctypes.POINTER(ctypes.c_int32)],
+        "moe_debug_flag_wait": [cfgp, P, ctypes.c_int64, P, P],
         "moe_router_logits_noalloc": [cfgp, P, P, ctypes.c_int, P, P],
         "moe_debug_unpack_weights": [cfgp, P, ctypes.c_int, ctypes.c_int, P, P, P],
     }
@@ -197,6 +198,12 @@ def moe_status_string(code) -> str:
 
 def moe_last_launch_count() -> int:
     return load().moe_last_launch_count()
+
+
+def moe_debug_flag_wait(cfg, flag, limit_cycles, ws, stream=None):
+    """The fused layer's bounded flag wait on its own (flag: int32 device tensor)."""
+    _check("moe_debug_flag_wait", load().moe_debug_flag_wait(ctypes.byref(cfg), _ptr(flag), int(limit_cycles),
+                                                              _ptr(ws), _stream(stream)))
 
 
 def moe_layer_fused(cfg, T) -> bool:

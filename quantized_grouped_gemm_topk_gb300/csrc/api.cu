@@ -999,6 +999,19 @@ const char* moe_status_string(moe_status_t s) {
 
 int moe_last_launch_count(void) { return launch_count(); }
 
+moe_status_t moe_debug_flag_wait(const moe_config_t* c, const int32_t* flag, int64_t limit_cycles, void* ws,
+                                 void* stream) {
+  moe_status_t s = moe_config_validate(c);
+  if (s != MOE_OK) return s;
+  if (!flag || ((uintptr_t)flag & 3u) || limit_cycles <= 0) return MOE_ERR_INVALID_ARG;
+  REQ(ws);
+  reset_launch_count();
+  const WsLayout L = ws_layout(*c);
+  MOE_CHECK_CUDA(launch_debug_flag_wait(flag, (long long)limit_cycles, at<int32_t>(ws, L.status),
+                                        (cudaStream_t)stream));
+  return MOE_OK;
+}
+
 moe_status_t moe_layer_fused(const moe_config_t* c, int T, int32_t* fused) {
   moe_status_t s = check_T(c, T);
   if (s != MOE_OK) return s;

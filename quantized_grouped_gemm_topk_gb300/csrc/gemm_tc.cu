@@ -192,13 +192,14 @@ __device__ __forceinline__ bool tc_unit(const TcArgs& g, const UnitTab& tab, con
 
 // Waits (bounded, as the mbarrier waits) for a flag another CTA sets with a
 // release store; acquire on success.
-__device__ __forceinline__ bool wait_flag(const int32_t* flag, volatile int* abort) {
+__device__ __forceinline__ bool wait_flag(const int32_t* flag, volatile int* abort,
+                                          long long limit_cycles = 4000000000ll) {
   const long long t0 = clock64();
   for (uint32_t it = 0;; ++it) {
     if (ld_acquire_gpu(flag) != 0) return true;
     if ((it & 15) == 15) {
       if (*abort) return false;
-      if (clock64() - t0 > 4000000000ll) {
+      if (clock64() - t0 > limit_cycles) {
         *abort = 1;
         return false;
       }
@@ -893,6 +894,21 @@ __global__ void __launch_bounds__(256) k_act_f16(const uint8_t* __restrict__ q, 
       *reinterpret_cast<uint4*>(a16 + r * C + c0) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
     }
   }
+}
+
+// The fused layer's flag wait on its own: one thread waits (bounded by
+// limit_cycles) for *flag != 0 and sets MOE_DEV_TIMEOUT when it gives up.
+__global__ void k_debug_flag_wait(const int32_t* flag, long long limit_cycles, int32_t* status) {
+  __shared__ volatile int abort_;
+  if (threadIdx.x != 0) return;
+  abort_ = 0;
+  if (!wait_flag(flag, &abort_, limit_cycles)) set_status(status, MOE_DEV_TIMEOUT);
+}
+
+cudaError_t launch_debug_flag_wait(const int32_t* flag, long long limit_cycles, int32_t* status, cudaStream_t st) {
+  k_debug_flag_wait<<<1, 32, 0, st>>>(flag, limit_cycles, status);
+  note_launch();
+  return cudaGetLastError();
 }
 
 cudaError_t launch_act_f16(const uint8_t* q, const uint8_t* s, int C, const int32_t* row_map, int row_div, int R,

@@ -168,6 +168,7 @@ int tc_token_tile(int T, int kp, int G);
 cudaError_t launch_gemm_tc(const TcArgs& g, const TcMaps& maps, int nt, cudaStream_t st);
 // a16[r] = f16 rows of the MXFP8 rows q/s [*, C] at row_map[r] / row_div
 // (or r), rowexp[r] = the row's largest block exponent.
+cudaError_t launch_debug_flag_wait(const int32_t* flag, long long limit_cycles, int32_t* status, cudaStream_t st);
 // zero / nzero (nullable): ints the kernel also sets to zero (the fused
 // layer's counters, cleared by the launch just before it).
 cudaError_t launch_act_f16(const uint8_t* q, const uint8_t* s, int C, const int32_t* row_map, int row_div, int R,

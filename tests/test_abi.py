@@ -140,3 +140,17 @@ def test_layer_fused_rule(lib):
     assert m.moe_layer_fused(s, 35) and not m.moe_layer_fused(s, 36)
     with pytest.raises(m.MoEError):
         m.moe_layer_fused(c, 129)                                          # T > T_max
+
+
+def test_flag_wait_host_errors(lib):
+    """moe_debug_flag_wait checks its arguments on the host and enqueues
+    nothing on an error."""
+    import ctypes
+    from quantized_grouped_gemm_topk_gb300 import binding as m
+    c = _cfg()
+    L = m.load()
+    fake = ctypes.c_void_p(4096)
+    assert L.moe_debug_flag_wait(ctypes.byref(c), None, 100, fake, None) == 1
+    assert L.moe_debug_flag_wait(ctypes.byref(c), fake, 0, fake, None) == 1
+    assert L.moe_debug_flag_wait(ctypes.byref(c), ctypes.c_void_p(4098), 100, fake, None) == 1
+    assert L.moe_last_launch_count() == 0

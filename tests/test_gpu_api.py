@@ -297,3 +297,25 @@ def test_wrong_pack_sets_status_and_writes_nothing():
     st = m.moe_read_status(cfg, ws)
     assert st & m.MOE_DEV_BAD_PACK
     assert (v["y1_q"] == 0x33).all()
+
+
+def test_flag_wait_times_out_and_context_survives():
+    """The fused layer's cross-CTA wait is bounded: waiting on a flag that
+    nothing sets gives up after the limit and sets MOE_DEV_TIMEOUT; a set
+    flag passes; the context stays usable (a layer forward afterwards matches
+    one before)."""
+    dev = cuda_device()
+    s = inputs.workload("tiny", T=4)
+    r = run_forward(s, s.T, dev=dev)
+    cfg, ws = r["cfg"], r["ws"]
+    flag = torch.zeros(4, dtype=torch.int32, device=dev)
+    m.moe_debug_flag_wait(cfg, flag, 20_000_000, ws)          # ~10 ms at the top clock
+    assert m.moe_read_status(cfg, ws) == m.MOE_DEV_TIMEOUT
+    flag.fill_(1)
+    m.moe_debug_flag_wait(cfg, flag, 20_000_000, ws)
+    assert m.moe_read_status(cfg, ws) == 0
+    out2 = torch.empty_like(r["out"])
+    m.moe_layer_forward(cfg, r["x"], r["Wr"], None, s.T, r["packed"], out2, None, ws)
+    torch.cuda.synchronize()
+    assert m.moe_read_status(cfg, ws) == 0
+    assert torch.equal(out2, r["out"])

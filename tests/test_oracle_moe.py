@@ -174,6 +174,29 @@ def test_routed_equals_dense_formulation(act, wfmt, S, rs):
     assert np.isfinite(f.out).all()
 
 
+def test_w1_bias_is_added_to_gate_and_up_before_the_activation():
+    """With W1 = 0 every row's W1 output is exactly its expert's bias (gate
+    part b first, up part c second); with W1 as drawn, adding the bias
+    shifts each row's W1 output by exactly that vector (up to fp64
+    rounding), and the layer equals its dense formulation."""
+    s, xb, lg, wts = _tiny_case(T=8)
+    G, I, H = s.groups, s.I, s.H
+    rng = np.random.default_rng(11)
+    b1 = rng.normal(0, 0.5, (G, 2 * I))
+    f0 = M.layer_forward(xb, lg, dict(wts, w1_f64=np.zeros((G, 2 * I, H)), b1=b1), E=s.E, k=s.k)
+    e_row = f0.disp.expert[f0.disp.perm_src]
+    assert (f0.h == b1[e_row]).all()
+    # gate from b, up from c: a swapped pair would change y
+    g, u = b1[e_row, :I], b1[e_row, I:]
+    expect = f0.disp.w_row[:, None] * (g / (1.0 + np.exp(-g))) * u
+    assert np.allclose(f0.y, expect, rtol=1e-14, atol=0)
+    fa = M.layer_forward(xb, lg, wts, E=s.E, k=s.k)
+    fb = M.layer_forward(xb, lg, dict(wts, b1=b1), E=s.E, k=s.k)
+    assert np.allclose(fb.h - fa.h, b1[e_row], rtol=0, atol=1e-15)
+    dense = M.dense_forward(xb, lg, dict(wts, b1=b1), E=s.E, k=s.k)
+    assert np.allclose(fb.out, dense, rtol=1e-12, atol=1e-12)
+
+
 def test_gemm_brute_force_triple_loop():
     s, xb, lg, wts = _tiny_case(T=3)
     f = M.layer_forward(xb, lg, wts, E=s.E, k=s.k, wfmt="nvfp4")
