@@ -120,6 +120,10 @@ typedef struct moe_config {
     float routed_scale;   /* multiplies the renormalised routing weights     */
     int32_t weight_fmt;
     int32_t max_sms;      /* 0: use every SM; else cap the GEMM grids        */
+    int32_t w1_bias;      /* 1: W1 carries a per-group fp32 bias [2I] (gate b,
+                           * up c) added before the activation, forward only
+                           * (the NVIDIA blog's SwiGLU(xW + b, xV + c) and its
+                           * fused bias-vector epilogue, kernel families) */
 } moe_config_t;
 
 /* Unpacked expert weights (device pointers), one entry per group e < G, in
@@ -141,6 +145,8 @@ typedef struct moe_weights_view {
     const uint8_t* w2_q;
     const uint8_t* w2_s;
     const float* w2_gs;
+    const float* b1;      /* [G, 2I] fp32 (gate then up); required when
+                           * cfg->w1_bias, else ignored (may be NULL)        */
 } moe_weights_view_t;
 
 /* Dispatch results (device pointers, caller-owned; see moe_workspace_view

@@ -51,12 +51,13 @@ class moe_config_t(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("n_shared", ctypes.c_int32), ("T_max", ctypes.c_int32), ("act", ctypes.c_int32),
                 ("act_alpha", ctypes.c_float), ("act_limit", ctypes.c_float), ("routed_scale", ctypes.c_float),
-                ("weight_fmt", ctypes.c_int32), ("max_sms", ctypes.c_int32)]
+                ("weight_fmt", ctypes.c_int32), ("max_sms", ctypes.c_int32), ("w1_bias", ctypes.c_int32)]
 
 
 class moe_weights_view_t(ctypes.Structure):
     _fields_ = [("w1_q", ctypes.c_void_p), ("w1_s", ctypes.c_void_p), ("w1_gs", ctypes.c_void_p),
-                ("w2_q", ctypes.c_void_p), ("w2_s", ctypes.c_void_p), ("w2_gs", ctypes.c_void_p)]
+                ("w2_q", ctypes.c_void_p), ("w2_s", ctypes.c_void_p), ("w2_gs", ctypes.c_void_p),
+                ("b1", ctypes.c_void_p)]
 
 
 class moe_dispatch_t(ctypes.Structure):
@@ -150,17 +151,17 @@ def _require_cuda():
 
 
 def make_config(H, I, E, k, n_shared=0, T_max=0, act="swiglu", alpha=1.0, limit=0.0, routed_scale=1.0,
-                wfmt="nvfp4", max_sms=0) -> moe_config_t:
+                wfmt="nvfp4", max_sms=0, bias=False) -> moe_config_t:
     return moe_config_t(H, I, E, k, n_shared, T_max,
                         ACTS[act],
                         float(alpha), float(limit), float(routed_scale),
-                        WFMTS[wfmt], max_sms)
+                        WFMTS[wfmt], max_sms, 1 if bias else 0)
 
 
 def config_from_shape(s, T_max=None, max_sms=0) -> moe_config_t:
     """moe_config_t from an object with the fields of inputs.MoEShape."""
     return make_config(s.H, s.I, s.E, s.k, s.n_shared, s.T if T_max is None else T_max, s.act, s.alpha,
-                       s.limit, s.routed_scale, s.wfmt, max_sms)
+                       s.limit, s.routed_scale, s.wfmt, max_sms, getattr(s, "bias", False))
 
 
 # ---- sizes / views (host only) -----------------------------------------------
@@ -236,7 +237,8 @@ def moe_prepack_weights(cfg, wts: dict, which=MOE_PACK_FORWARD, dst=None, stream
         dst = torch.empty(n, dtype=torch.uint8, device="cuda")
     p = "" if which == MOE_PACK_FORWARD else "t"
     view = moe_weights_view_t(_ptr(wts[f"w1{p}_q"]), _ptr(wts[f"w1{p}_s"]), _ptr(wts.get("w1_gs")),
-                              _ptr(wts[f"w2{p}_q"]), _ptr(wts[f"w2{p}_s"]), _ptr(wts.get("w2_gs")))
+                              _ptr(wts[f"w2{p}_q"]), _ptr(wts[f"w2{p}_s"]), _ptr(wts.get("w2_gs")),
+                              _ptr(wts.get("b1")))
     _check("moe_prepack_weights", load().moe_prepack_weights(ctypes.byref(cfg), ctypes.byref(view), which,
                                                              _ptr(dst), dst.numel(), _stream(stream)))
     return dst

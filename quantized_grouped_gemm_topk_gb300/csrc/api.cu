@@ -47,7 +47,7 @@ static int64_t r_pad_for(const Dims& d, int T) {
 }
 
 static bool backward_capable(const moe_config_t& c) {
-  return c.weight_fmt == MOE_WFMT_MXFP8 && c.n_shared == 0;
+  return c.weight_fmt == MOE_WFMT_MXFP8 && c.n_shared == 0 && !c.w1_bias;
 }
 
 // MXFP8 weights run on the block-scaled tensor-core GEMM (gemm_mx.cu); NVFP4
@@ -144,6 +144,7 @@ struct PackLayout {
   int rows1, rows2;
   size_t off_s1, off_s2;
   size_t off_w1, off_w2, total;
+  size_t off_b1;   // W1 bias [G][2I] fp32 (forward packs of configs with w1_bias), 0 for none
 };
 
 static PackLayout pack_layout(const moe_config_t& c, int which) {
@@ -176,6 +177,9 @@ static PackLayout pack_layout(const moe_config_t& c, int which) {
     P.off_s1 = o; o = align_up(o + (size_t)sf4_bytes(P.K1, (int64_t)P.G * P.rows1), 256);
     P.off_w2 = o; o = align_up(o + (size_t)P.G * P.rows2 * row_bytes(P.fmt, P.K2), 256);
     P.off_s2 = o; o = align_up(o + (size_t)sf4_bytes(P.K2, (int64_t)P.G * P.rows2), 256);
+  }
+  if (c.w1_bias && which == MOE_PACK_FORWARD) {
+    P.off_b1 = o; o = align_up(o + (size_t)P.G * 2 * c.I * 4, 256);
   }
   P.total = o;
   return P;
@@ -237,6 +241,7 @@ moe_status_t moe_config_validate(const moe_config_t* c) {
   if (c->weight_fmt == MOE_WFMT_MXFP4 && (c->H % 128 || c->I % 128)) return MOE_ERR_INVALID_ARG;
   if (!(c->routed_scale > 0.f)) return MOE_ERR_INVALID_ARG;
   if (c->max_sms < 0) return MOE_ERR_INVALID_ARG;
+  if (c->w1_bias != 0 && c->w1_bias != 1) return MOE_ERR_INVALID_ARG;
   return MOE_OK;
 }
 
@@ -296,6 +301,7 @@ moe_status_t moe_prepack_weights(const moe_config_t* c, const moe_weights_view_t
   if (which == MOE_PACK_DGRAD && c->weight_fmt != MOE_WFMT_MXFP8) return MOE_ERR_UNSUPPORTED;
   REQ(dst); REQ(src->w1_q); REQ(src->w1_s); REQ(src->w2_q); REQ(src->w2_s);
   if (c->weight_fmt == MOE_WFMT_NVFP4) { REQ(src->w1_gs); REQ(src->w2_gs); }
+  if (c->w1_bias && which == MOE_PACK_FORWARD) REQ(src->b1);
   const PackLayout P = pack_layout(*c, which);
   if (dst_bytes < P.total) return MOE_ERR_WORKSPACE;
   cudaStream_t st = (cudaStream_t)stream;
@@ -308,6 +314,7 @@ moe_status_t moe_prepack_weights(const moe_config_t* c, const moe_weights_view_t
   h.off_gs1 = P.off_gs1; h.off_gs2 = P.off_gs2; h.off_w1 = P.off_w1; h.off_w2 = P.off_w2;
   h.tile_bytes1 = P.tile_bytes1; h.tile_bytes2 = P.tile_bytes2; h.tiles1 = P.tiles1; h.tiles2 = P.tiles2;
   h.off_s1 = P.off_s1; h.off_s2 = P.off_s2; h.rows1 = P.rows1; h.rows2 = P.rows2;
+  h.off_b1 = (int64_t)P.off_b1;
   k_write_header<<<1, 1, 0, st>>>(h, d8);
   note_launch();
   MOE_CHECK_CUDA(cudaGetLastError());
@@ -324,6 +331,9 @@ moe_status_t moe_prepack_weights(const moe_config_t* c, const moe_weights_view_t
     MOE_CHECK_CUDA(launch_prepack_mx(src->w2_q, src->w2_s, P.G, P.N2, P.K2, row_bytes(P.fmt, P.K2), 0, P.rows2,
                                      d8 + P.off_w2, d8 + P.off_s2, st));
   }
+  if (P.off_b1)
+    MOE_CHECK_CUDA(cudaMemcpyAsync(d8 + P.off_b1, src->b1, (size_t)P.G * 2 * c->I * 4, cudaMemcpyDeviceToDevice,
+                                   st));
   return MOE_OK;
 }
 
@@ -490,6 +500,7 @@ static void tc_common(TcArgs& g, const moe_config_t* c, const PackLayout& P, con
   if (c->max_sms > 0) sms = std::min(sms, c->max_sms);
   g.max_ctas = sms;
   g.status = at<int32_t>(ws, L.status);
+  g.bias = c->w1_bias;
 }
 
 // Packed matrix `mat` (1 or 2) of `packed` as one matrix of the decoding
@@ -571,6 +582,7 @@ static moe_status_t mx_token_gemm(const moe_config_t* c, MxArgs& g, int mode, co
   g.a_sf = as; g.a_sf_ld = R; g.a_rows = R;
   g.b_sf = b + (mat == 1 ? P.off_s1 : P.off_s2); g.b_sf_ld = (int64_t)P.G * rows; g.b_rows = (int64_t)P.G * rows;
   g.b_fp4 = P.fmt == MOE_WFMT_MXFP4;
+  g.bias = which == MOE_PACK_FORWARD && c->w1_bias;
   g.R = R;
   g.status = status;
   MxMaps maps;
@@ -619,6 +631,7 @@ static moe_status_t tc_fused(const moe_config_t* c, const moe_dispatch_t* d, int
   g.f.y16 = at<uint16_t>(ws, L.y16);
   g.f.y_rowexp = at<int32_t>(ws, L.rexp2);
   g.f.cnt = at<int32_t>(ws, L.fcnt);
+  g.f.b1 = P.off_b1 ? reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(packed) + P.off_b1) : nullptr;
   const int64_t R = (int64_t)T * (c->k + c->n_shared);
   TcMaps maps;
   if (!make_tmaps_b(maps.m[0], at<uint16_t>(ws, L.a16), R, g.m[0].K) ||
@@ -652,6 +665,7 @@ static moe_status_t w1_impl(const moe_config_t* c, const moe_dispatch_t* d, int 
     MxArgs g = mx_args0();
     g.n_tiles = P.rows1 / kMxTileN;
     g.I = c->I;
+    g.b1 = P.off_b1 ? reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(packed) + P.off_b1) : nullptr;
     g.w_row = d->w_row;
     g.act = act_params(c);
     g.yq = y1q; g.ys = y1s;
@@ -687,6 +701,7 @@ static moe_status_t w1_impl(const moe_config_t* c, const moe_dispatch_t* d, int 
   f.y1q = y1q; f.y1s = y1s;
   f.y16 = at<uint16_t>(ws, L.y16);
   f.y_rowexp = at<int32_t>(ws, L.rexp2);
+  f.b1 = P.off_b1 ? reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(packed) + P.off_b1) : nullptr;
   MOE_CHECK_CUDA(launch_w1_finalize(f, st));
   phase(3, st);
   return MOE_OK;

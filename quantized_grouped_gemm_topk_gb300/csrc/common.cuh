@@ -28,7 +28,7 @@ constexpr int kTileN = 128;
 constexpr int kChunkK = 64;
 constexpr int kMxTileN = 192;
 constexpr uint32_t kPackMagic = 0x4d4f4557u;  // 'MOEW'
-constexpr int kPackVersion = 2;
+constexpr int kPackVersion = 3;
 
 __host__ __device__ inline int chunk_bytes(int fmt) {
   return fmt == MOE_WFMT_NVFP4 ? (4096 + 512) : (8192 + 256);
@@ -68,12 +68,14 @@ struct PackHeader {            // first 256 bytes of a packed blob
   int32_t tiles1, tiles2;                     // NVFP4: tiles per group
   int64_t off_s1, off_s2;                     // MXFP8: scale arrays
   int32_t rows1, rows2;                       // MXFP8: packed rows per group
+  int64_t off_b1;                             // W1 bias [G][2I] fp32, 0 for none
 };
 static_assert(sizeof(PackHeader) <= 256, "pack header fits its 256 bytes");
 
 // True when the blob's header describes the packing a GEMM expects.
-__device__ __forceinline__ bool pack_header_ok(const PackHeader* h, int fmt, int which, int G) {
-  return h->magic == kPackMagic && h->version == kPackVersion && h->fmt == fmt && h->which == which && h->G == G;
+__device__ __forceinline__ bool pack_header_ok(const PackHeader* h, int fmt, int which, int G, bool bias = false) {
+  return h->magic == kPackMagic && h->version == kPackVersion && h->fmt == fmt && h->which == which && h->G == G &&
+         (h->off_b1 != 0) == bias;
 }
 
 // ---- conversions ------------------------------------------------------------

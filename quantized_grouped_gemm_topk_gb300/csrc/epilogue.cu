@@ -36,6 +36,15 @@ __global__ void __launch_bounds__(1024) k_w1_finalize_rows(const W1FinArgs a) {
   if (r >= Rv) return;
   const float* P = a.P + r * 2 * a.I;
   const float wr = a.w_row[r];
+  const float* bg = nullptr;   // W1 bias of the row's group (the last e with offsets[e] <= r owns row r)
+  if (a.b1) {
+    int lo = 0, hi = a.G - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (a.offsets[mid] <= r) lo = mid; else hi = mid - 1;
+    }
+    bg = a.b1 + (int64_t)lo * 2 * a.I;
+  }
   int mx = 0;
   for (int b = warp; b < nb; b += nwarps) {
     const int i = b * 32 + lane;
@@ -44,6 +53,10 @@ __global__ void __launch_bounds__(1024) k_w1_finalize_rows(const W1FinArgs a) {
     for (int s = 0; s < a.S; ++s) {
       g += P[(int64_t)s * a.split_stride + i];
       u += P[(int64_t)s * a.split_stride + a.I + i];
+    }
+    if (bg) {
+      g += bg[i];
+      u += bg[a.I + i];
     }
     const float y = wr * act_fwd(g, u, a.act);
     const int e = mx_exponent(warp_max(fabsf(y)));

@@ -278,6 +278,16 @@ __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, ui
       tc::tmem_ld32(acc_tmem + 32 * b, gv);
       tc::tmem_ld32(acc_tmem + kMxBN / 2 + 32 * b, uv);
       tc::tmem_wait_ld();
+      if (g.b1) {
+        // W1 bias of the group: gate b, up c, before the activation (the
+        // same value in every lane: one broadcast load each)
+        const float* bb = g.b1 + (int64_t)w.e * 2 * g.I + f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          gv[i] = __float_as_uint(__uint_as_float(gv[i]) + __ldg(bb + i));
+          uv[i] = __float_as_uint(__uint_as_float(uv[i]) + __ldg(bb + g.I + i));
+        }
+      }
       float y[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) y[i] = wr * act_fwd(__uint_as_float(gv[i]), __uint_as_float(uv[i]), g.act);
@@ -396,7 +406,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
   __shared__ int bad_pack;
   pdl_enter();
   if (threadIdx.x == 0) {
-    bad_pack = g.hdr && !pack_header_ok(g.hdr, g.b_fp4 ? MOE_WFMT_MXFP4 : MOE_WFMT_MXFP8, g.which, g.G);
+    bad_pack = g.hdr && !pack_header_ok(g.hdr, g.b_fp4 ? MOE_WFMT_MXFP4 : MOE_WFMT_MXFP8, g.which, g.G, g.bias != 0);
     if (bad_pack) set_status(g.status, MOE_DEV_BAD_PACK);
   }
   __syncthreads();

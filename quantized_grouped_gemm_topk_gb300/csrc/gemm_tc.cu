@@ -241,6 +241,10 @@ __device__ __noinline__ void fused_w1_tile(const TcArgs& g, const TcUnit& w, int
       gg += __ldcg(P + (int64_t)s * M.split_stride + fi);
       uu += __ldcg(P + (int64_t)s * M.split_stride + I + fi);
     }
+    if (f.b1) {   // W1 bias of the group: gate b, up c
+      gg += f.b1[(int64_t)w.e * 2 * I + fi];
+      uu += f.b1[(int64_t)w.e * 2 * I + I + fi];
+    }
     const float y = f.w_row[r] * act_fwd(gg, uu, f.act);
     const int e = mx_exponent(warp_max(fabsf(y)));
     f.y1q[(int64_t)r * I + fi] = (uint8_t)(f32x2_to_e4m3x2(y * pow2_neg(e), 0.f) & 0xffu);
@@ -388,7 +392,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   pdl_enter();
   if (threadIdx.x == 0) {
-    bad_pack = !pack_header_ok(g.hdr, MOE_WFMT_NVFP4, g.which, g.G);
+    bad_pack = !pack_header_ok(g.hdr, MOE_WFMT_NVFP4, g.which, g.G, g.bias != 0);
     if (bad_pack) set_status(g.status, MOE_DEV_BAD_PACK);
   }
   __syncthreads();

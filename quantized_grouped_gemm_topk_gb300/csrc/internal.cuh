@@ -134,6 +134,7 @@ struct TcFused {
   uint16_t* y16;              // [R][I]
   int32_t* y_rowexp;          // [R]
   int32_t* cnt;               // [G] W1 tiles done, [G] ready flags; zero on entry
+  const float* b1;            // [G][2I] W1 bias (gate then up), nullable
 };
 struct TcArgs {
   TcMat m[2];                 // m[0]: the (first) matrix; m[1]: W2 of the fused layer
@@ -147,6 +148,7 @@ struct TcArgs {
   int max_ctas;
   int32_t* status;
   int split_rows;             // > 0: the walk takes groups in blocks of this many rows (a multiple of the token tile)
+  int bias;                   // the blob carries a W1 bias (checked against its header)
   TcFused f;
 };
 // Largest I the fused layer takes (a lane of the group conversion holds
@@ -200,6 +202,8 @@ struct MxArgs {
   const uint8_t* a_sf; int64_t a_sf_ld; int64_t a_rows;   // A scales, SF4 with ld = a_sf_ld; rows < a_rows exist
   const uint8_t* b_sf; int64_t b_sf_ld; int64_t b_rows;   // B scales, SF4
   int b_fp4;                    // B elements are E2M1 (MXFP4 weights), else E4M3
+  int bias;                     // the blob carries a W1 bias (checked against its header)
+  const float* b1;              // W1 mode (nullable): [G][2I] bias, gate then up
   int64_t R;                    // token rows (A rows of the token-side modes)
   const float* w_row;           // [R] routing weight per row
   ActParams act;
@@ -247,6 +251,7 @@ struct W1FinArgs {
   uint8_t* y1q; uint8_t* y1s;
   uint16_t* y16;                      // [R][I] f16 rows for the W2 B operand
   int32_t* y_rowexp;                  // [R] row exponent of y16
+  const float* b1;                    // [G][2I] W1 bias (gate then up), nullable
 };
 cudaError_t launch_w1_finalize(const W1FinArgs& a, cudaStream_t st);
 

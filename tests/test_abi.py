@@ -154,3 +154,23 @@ def test_flag_wait_host_errors(lib):
     assert L.moe_debug_flag_wait(ctypes.byref(c), fake, 0, fake, None) == 1
     assert L.moe_debug_flag_wait(ctypes.byref(c), ctypes.c_void_p(4098), 100, fake, None) == 1
     assert L.moe_last_launch_count() == 0
+
+
+def test_w1_bias_host_rules(lib):
+    """w1_bias is 0 or 1; it enlarges the forward pack by G * 2I fp32 and
+    leaves the dgrad pack alone; the backward refuses a biased config
+    (forward only) before touching any pointer."""
+    import ctypes
+    from quantized_grouped_gemm_topk_gb300 import binding as m
+    c0 = _cfg(wfmt="mxfp8")
+    c1 = _cfg(wfmt="mxfp8", bias=True)
+    assert m.moe_config_validate(c1) == 0
+    bad = _cfg()
+    bad.w1_bias = 2
+    assert m.moe_config_validate(bad) == 1
+    assert m.moe_packed_weights_size(c1) - m.moe_packed_weights_size(c0) >= 8 * 2 * 128 * 4
+    assert m.moe_packed_weights_size(c1, m.MOE_PACK_DGRAD) == m.moe_packed_weights_size(c0, m.MOE_PACK_DGRAD)
+    fake = ctypes.c_void_p(4096)
+    L = m.load()
+    assert L.moe_layer_backward(ctypes.byref(c1), fake, fake, 16, None, fake, fake, fake, fake, fake, fake,
+                                None) == 2

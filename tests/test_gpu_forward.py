@@ -228,3 +228,28 @@ def test_mxfp4_dsv3_decode(T):
     sampled tokens."""
     s = inputs.workload("dsv3", T=T, wfmt="mxfp4")
     _full_size_sampled(s, T, 1)
+
+
+@pytest.mark.parametrize("case", ["nvfp4_fused", "nvfp4_separate", "mxfp8", "mxfp4"])
+def test_w1_bias_forward(case):
+    """A per-expert W1 bias (gate b, up c, added before the activation) on
+    every W1 epilogue: the fused layer's tile epilogue (tiny, T = 4), the
+    separate NVFP4 epilogue kernel (tiny, T = 16), and the block-scaled
+    GEMM's epilogue with MXFP8 (training shape, reduced) and MXFP4 weights."""
+    dev = cuda_device()
+    if case == "nvfp4_fused":
+        s = inputs.workload("tiny", T=4, bias=True)
+    elif case == "nvfp4_separate":
+        s = inputs.workload("tiny", T=16, bias=True)
+    elif case == "mxfp8":
+        s = inputs.workload("train", T=40, E=8, bias=True)
+    else:
+        s = inputs.workload("tiny", T=16, wfmt="mxfp4", bias=True)
+    r = run_forward(s, s.T, dev=dev, seed=7)
+    assert r["status"] == 0
+    import quantized_grouped_gemm_topk_gb300 as m
+    assert m.moe_layer_fused(r["cfg"], s.T) == (case == "nvfp4_fused")
+    f = oracle_forward(s, r)
+    _check_dispatch(s, r, f)
+    assert_mx_close(np_(r["views"]["y1_q"]), np_(r["views"]["y1_s"]), f.y1q, f.y1s, "y1")
+    assert_close_layer(np_(r["out"].float()), f.out, "out")
