@@ -51,7 +51,7 @@ class MoEShape:
     k: int
     n_shared: int = 0
     routed_scale: float = 1.0
-    act: str = "swiglu"          # "swiglu" | "swiglu_clamp" | "geglu"
+    act: str = "swiglu"          # "swiglu" | "swiglu_clamp" | "geglu" | "srelu"
     alpha: float = 1.0
     limit: float = 0.0
     wfmt: str = "nvfp4"          # "nvfp4" | "mxfp8" | "mxfp4"
@@ -260,7 +260,8 @@ def gen_one_expert(s: MoEShape, seed: int, e: int, device="cpu", dgrad_copies: b
     gen_expert_weights (per-expert generators, so any expert can be drawn
     alone)."""
     H, I = s.H, s.I
-    w1 = torch.randn(2 * I, H, generator=_gen((seed + 2) * 65536 + e, device), device=device,
+    n1 = I if s.act == "srelu" else 2 * I     # sReLU: a non-gated W1 of I outputs
+    w1 = torch.randn(n1, H, generator=_gen((seed + 2) * 65536 + e, device), device=device,
                      dtype=torch.float32) * 0.02
     w2 = torch.randn(H, I, generator=_gen((seed + 3) * 65536 + e, device), device=device,
                      dtype=torch.float32) * 0.02
@@ -287,7 +288,7 @@ def gen_one_expert(s: MoEShape, seed: int, e: int, device="cpu", dgrad_copies: b
         raise ValueError(s.wfmt)
     if s.bias:
         # its own generator: the weights' draws do not depend on the bias
-        out["b1"] = torch.randn(2 * I, generator=_gen((seed + 6) * 65536 + e, device), device=device,
+        out["b1"] = torch.randn(n1, generator=_gen((seed + 6) * 65536 + e, device), device=device,
                                 dtype=torch.float32) * 0.1
     return out
 

@@ -25,6 +25,8 @@ Readings taken where the pages are silent (each listed in the design notes):
     blog's b and c are an optional per-expert fp32 bias vector of W1's 2I
     outputs (b for gate, c for up; the blog's fused epilogues add a "bias
     vector", kernel families section), zero when the weights carry none;
+  * sReLU (the blog's non-gated activation) is max(h, 0)^2 of a W1 with I
+    outputs, then the routing weight;
   * the clamped variant is g' = clamp(g, -L, L), u' = clamp(u, -L, L),
     act = g' * sigmoid(alpha * g') * u';
   * the routing weight multiplies the SwiGLU output before requantisation;
@@ -133,6 +135,19 @@ def gelu_pdf(v):
     return np.exp(-0.5 * v * v) / math.sqrt(2.0 * math.pi)
 
 
+def gated(act: str) -> bool:
+    """Whether W1 has gate and up halves (2I outputs) or I outputs."""
+    return act != "srelu"
+
+
+def act_plain(h, act="srelu"):
+    """The non-gated activation the blog's fused kernels list (kernel
+    families: sReLU): the squared ReLU, max(h, 0)^2, of W1's I outputs."""
+    h = np.asarray(h, np.float64)
+    assert act == "srelu", act
+    return np.square(np.maximum(h, 0.0))
+
+
 def act_fwd(g, u, act="swiglu", alpha=1.0, limit=0.0):
     """The gated activations the blog's fused kernels support (NVIDIA blog,
     kernel families: SwiGLU, GeGLU), with b = c = 0:
@@ -219,7 +234,7 @@ class Forward:
     disp: Dispatch
     xq: np.ndarray        # uint8 [T, H]   E4M3 codes of x
     xs: np.ndarray        # uint8 [T, H/32] E8M0 scales of x
-    h: np.ndarray         # fp64 [R, 2I]  W1 output (gate | up)
+    h: np.ndarray         # fp64 [R, 2I]  W1 output (gate | up); sReLU: [R, I]
     y: np.ndarray         # fp64 [R, I]   routing weight * act(g, u)
     y1q: np.ndarray       # uint8 [R, I]
     y1s: np.ndarray       # uint8 [R, I/32]
@@ -256,7 +271,8 @@ def layer_forward(x_bits, logits, wts: dict, *, E: int, k: int, n_shared: int = 
     else:
         want[np.asarray(list(rows), np.int64)] = True
     I = expert_w2(wts, 0, wfmt).shape[1]
-    h = np.full((R, 2 * I), np.nan)
+    N1 = 2 * I if gated(act) else I
+    h = np.full((R, N1), np.nan)
     y = np.full((R, I), np.nan)
     y1q = np.zeros((R, I), np.uint8)
     y1s = np.zeros((R, max(I // 32, 1)), np.uint8)
@@ -269,9 +285,12 @@ def layer_forward(x_bits, logits, wts: dict, *, E: int, k: int, n_shared: int = 
         rs = np.asarray(rs)
         toks = d.perm_src[rs] // kp
         A = a_tok[toks]                              # gathered rows [n, H]
-        W1 = expert_w1(wts, e, wfmt)                 # [2I, H]
-        he = A @ W1.T + expert_b1(wts, e, 2 * I)     # [n, 2I]: xW + b | xV + c
-        ye = d.w_row[rs, None] * act_fwd(he[:, :I], he[:, I:], act, alpha, limit)
+        W1 = expert_w1(wts, e, wfmt)                 # [2I, H] (sReLU: [I, H])
+        he = A @ W1.T + expert_b1(wts, e, N1)        # [n, 2I]: xW + b | xV + c
+        if gated(act):
+            ye = d.w_row[rs, None] * act_fwd(he[:, :I], he[:, I:], act, alpha, limit)
+        else:
+            ye = d.w_row[rs, None] * act_plain(he, act)
         if quant:
             q, s = F.mx_quantize(ye)
             y_in = F.mx_dequantize(q, s)
@@ -325,8 +344,12 @@ def dense_forward(x_bits, logits, wts: dict, *, E: int, k: int, n_shared: int = 
     for e in range(G):
         W1 = expert_w1(wts, e, wfmt)
         W2 = expert_w2(wts, e, wfmt)
-        hh = a @ W1.T + expert_b1(wts, e, 2 * I)
-        yy = gate[:, e:e + 1] * act_fwd(hh[:, :I], hh[:, I:], act, alpha, limit)
+        N1 = 2 * I if gated(act) else I
+        hh = a @ W1.T + expert_b1(wts, e, N1)
+        if gated(act):
+            yy = gate[:, e:e + 1] * act_fwd(hh[:, :I], hh[:, I:], act, alpha, limit)
+        else:
+            yy = gate[:, e:e + 1] * act_plain(hh, act)
         q, s = F.mx_quantize(yy)
         zz = F.mx_dequantize(q, s) @ W2.T
         out += np.where(gate[:, e:e + 1] != 0, zz, 0.0)

@@ -164,7 +164,8 @@ def _tiny_case(act="swiglu", wfmt="nvfp4", S=0, rs=1.0, T=16):
 
 @pytest.mark.parametrize("act,wfmt,S,rs", [("swiglu", "nvfp4", 0, 1.0), ("swiglu", "nvfp4", 1, 2.5),
                                           ("swiglu_clamp", "mxfp8", 0, 1.0), ("geglu", "nvfp4", 0, 1.0),
-                                          ("swiglu", "mxfp4", 0, 1.0)])
+                                          ("swiglu", "mxfp4", 0, 1.0), ("srelu", "nvfp4", 0, 1.0),
+                                          ("srelu", "mxfp8", 1, 2.5)])
 def test_routed_equals_dense_formulation(act, wfmt, S, rs):
     s, xb, lg, wts = _tiny_case(act, wfmt, S, rs)
     kw = dict(E=s.E, k=s.k, n_shared=S, routed_scale=rs, act=s.act, alpha=s.alpha, limit=s.limit, wfmt=wfmt)
@@ -195,6 +196,32 @@ def test_w1_bias_is_added_to_gate_and_up_before_the_activation():
     assert np.allclose(fb.h - fa.h, b1[e_row], rtol=0, atol=1e-15)
     dense = M.dense_forward(xb, lg, dict(wts, b1=b1), E=s.E, k=s.k)
     assert np.allclose(fb.out, dense, rtol=1e-12, atol=1e-12)
+
+
+def test_srelu_is_the_squared_relu_of_a_non_gated_w1():
+    """sReLU: W1 has I outputs (no up half); with one-hot W1 rows each output
+    is an exact scaled activation, and y = w_row * max(h, 0)^2 exactly:
+    negative outputs give 0 (not |h|^2), positive ones their square (not h)."""
+    s, xb, lg, wts = _tiny_case(act="srelu", T=8)
+    G, I, H = s.groups, s.I, s.H
+    assert wts["w1_q"].shape[1] == I
+    w1 = np.zeros((G, I, H))
+    for n in range(I):
+        w1[:, n, (5 * n) % H] = 2.0 ** ((n % 3) - 1)
+    f = M.layer_forward(xb, lg, dict(wts, w1_f64=w1), E=s.E, k=s.k, act="srelu")
+    a = F.mx_dequantize(f.xq, f.xs)
+    t = f.disp.perm_src // s.kp
+    assert f.h.shape == (s.T * s.kp, I)
+    neg = pos = 0
+    for r in range(s.T * s.kp):
+        for n in range(0, I, 7):
+            v = a[t[r], (5 * n) % H] * 2.0 ** ((n % 3) - 1)
+            assert f.h[r, n] == v
+            want = f.disp.w_row[r] * (v * v if v > 0 else 0.0)
+            assert f.y[r, n] == want
+            neg += v < 0
+            pos += v > 0
+    assert neg > 10 and pos > 10
 
 
 def test_gemm_brute_force_triple_loop():
