@@ -89,7 +89,7 @@ typedef enum moe_status {
 #define MOE_DEV_BAD_PACK 0x4      /* packed weight blob header mismatch      */
 #define MOE_DEV_TIMEOUT 0x8       /* a kernel gave up waiting on itself      */
 
-enum { MOE_ACT_SWIGLU = 0, MOE_ACT_SWIGLU_CLAMP = 1, MOE_ACT_GEGLU = 2 };
+enum { MOE_ACT_SWIGLU = 0, MOE_ACT_SWIGLU_CLAMP = 1, MOE_ACT_GEGLU = 2, MOE_ACT_SRELU = 3 };
 enum { MOE_WFMT_NVFP4 = 0, MOE_WFMT_MXFP8 = 1, MOE_WFMT_MXFP4 = 2 };
 enum { MOE_PACK_FORWARD = 0, MOE_PACK_DGRAD = 1 };
 
@@ -102,7 +102,11 @@ enum { MOE_PACK_FORWARD = 0, MOE_PACK_DGRAD = 1 };
  *                              with Phi the standard normal CDF (exact erf
  *                              form). The gated activations are those the
  *                              NVIDIA blog's fused kernels list (kernel
- *                              families: SwiGLU, GeGLU, with clamping). 
+ *                              families: SwiGLU, GeGLU, with clamping).
+ * act = MOE_ACT_SRELU:         the non-gated squared ReLU the blog also lists
+ *                              (sReLU): W1 has I outputs h (no up half) and
+ *                              act = max(h, 0)^2. Forward only, without
+ *                              w1_bias, not in the fused W1 -> W2 layer. 
  * weight_fmt = MOE_WFMT_NVFP4: E2M1 elements, E4M3 scale per 16 along K,
  *                              fp32 scale per (group, matrix)
  * weight_fmt = MOE_WFMT_MXFP8: E4M3 elements, E8M0 scale per 32 along K
@@ -129,7 +133,7 @@ typedef struct moe_config {
 /* Unpacked expert weights (device pointers), one entry per group e < G, in
  * the layout "one row per output feature, reduction axis contiguous":
  *   which = MOE_PACK_FORWARD: W1 rows n < 2I (gate features then up
- *     features), K = H; W2 rows n < H, K = I.
+ *     features; MOE_ACT_SRELU: rows n < I), K = H; W2 rows n < H, K = I.
  *   which = MOE_PACK_DGRAD (MXFP8 only, training): W1 copy with rows h < H,
  *     K = 2I; W2 copy with rows i < I, K = H (quantised along that K).
  * NVFP4: w*_q [G, N, K/2] bytes, element 2i in the low nibble of byte i;

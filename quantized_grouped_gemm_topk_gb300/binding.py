@@ -23,8 +23,9 @@ MOE_DEV_BAD_EXPERT_ID = 0x1
 MOE_DEV_NAN_LOGIT = 0x2
 MOE_DEV_BAD_PACK = 0x4
 MOE_DEV_TIMEOUT = 0x8
-MOE_ACT_SWIGLU, MOE_ACT_SWIGLU_CLAMP, MOE_ACT_GEGLU = 0, 1, 2
-ACTS = {"swiglu": MOE_ACT_SWIGLU, "swiglu_clamp": MOE_ACT_SWIGLU_CLAMP, "geglu": MOE_ACT_GEGLU}
+MOE_ACT_SWIGLU, MOE_ACT_SWIGLU_CLAMP, MOE_ACT_GEGLU, MOE_ACT_SRELU = 0, 1, 2, 3
+ACTS = {"swiglu": MOE_ACT_SWIGLU, "swiglu_clamp": MOE_ACT_SWIGLU_CLAMP, "geglu": MOE_ACT_GEGLU,
+        "srelu": MOE_ACT_SRELU}
 MOE_WFMT_NVFP4, MOE_WFMT_MXFP8, MOE_WFMT_MXFP4 = 0, 1, 2
 WFMTS = {"nvfp4": MOE_WFMT_NVFP4, "mxfp8": MOE_WFMT_MXFP8, "mxfp4": MOE_WFMT_MXFP4}
 MOE_PACK_FORWARD, MOE_PACK_DGRAD = 0, 1

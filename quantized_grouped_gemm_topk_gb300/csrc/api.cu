@@ -46,8 +46,11 @@ static int64_t r_pad_for(const Dims& d, int T) {
   return (int64_t)align_up((size_t)((int64_t)T * d.kp + (kPadRows - 1LL) * d.G), kPadRows);
 }
 
+// W1 with gate and up halves (2I outputs); sReLU's W1 has I outputs.
+static bool gated(const moe_config_t& c) { return c.act != MOE_ACT_SRELU; }
+
 static bool backward_capable(const moe_config_t& c) {
-  return c.weight_fmt == MOE_WFMT_MXFP8 && c.n_shared == 0 && !c.w1_bias;
+  return c.weight_fmt == MOE_WFMT_MXFP8 && c.n_shared == 0 && !c.w1_bias && gated(c);
 }
 
 // MXFP8 weights run on the block-scaled tensor-core GEMM (gemm_mx.cu); NVFP4
@@ -153,7 +156,7 @@ static PackLayout pack_layout(const moe_config_t& c, int which) {
   P.fmt = c.weight_fmt;
   P.G = c.E + c.n_shared;
   if (which == MOE_PACK_FORWARD) {
-    P.N1 = 2 * c.I; P.K1 = c.H; P.il1 = c.I;
+    P.N1 = gated(c) ? 2 * c.I : c.I; P.K1 = c.H; P.il1 = gated(c) ? c.I : 0;
     P.N2 = c.H; P.K2 = c.I;
   } else {
     P.N1 = c.H; P.K1 = 2 * c.I; P.il1 = 0;
@@ -232,7 +235,8 @@ moe_status_t moe_config_validate(const moe_config_t* c) {
   if (c->n_shared < 0 || c->n_shared > 1) return MOE_ERR_INVALID_ARG;
   if (c->k + c->n_shared > 32 || c->E + c->n_shared > 2048) return MOE_ERR_INVALID_ARG;
   if (c->T_max < 0) return MOE_ERR_INVALID_ARG;
-  if (c->act != MOE_ACT_SWIGLU && c->act != MOE_ACT_SWIGLU_CLAMP && c->act != MOE_ACT_GEGLU)
+  if (c->act != MOE_ACT_SWIGLU && c->act != MOE_ACT_SWIGLU_CLAMP && c->act != MOE_ACT_GEGLU &&
+      c->act != MOE_ACT_SRELU)
     return MOE_ERR_INVALID_ARG;
   if (c->act == MOE_ACT_SWIGLU_CLAMP && !(c->act_limit > 0.f)) return MOE_ERR_INVALID_ARG;
   if (c->weight_fmt != MOE_WFMT_NVFP4 && c->weight_fmt != MOE_WFMT_MXFP8 && c->weight_fmt != MOE_WFMT_MXFP4)
@@ -242,6 +246,7 @@ moe_status_t moe_config_validate(const moe_config_t* c) {
   if (!(c->routed_scale > 0.f)) return MOE_ERR_INVALID_ARG;
   if (c->max_sms < 0) return MOE_ERR_INVALID_ARG;
   if (c->w1_bias != 0 && c->w1_bias != 1) return MOE_ERR_INVALID_ARG;
+  if (c->w1_bias && c->act == MOE_ACT_SRELU) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -280,7 +285,7 @@ moe_status_t moe_packed_weights_size(const moe_config_t* c, int which, size_t* b
   moe_status_t s = moe_config_validate(c);
   if (s != MOE_OK) return s;
   if (!bytes || (which != MOE_PACK_FORWARD && which != MOE_PACK_DGRAD)) return MOE_ERR_INVALID_ARG;
-  if (which == MOE_PACK_DGRAD && c->weight_fmt != MOE_WFMT_MXFP8) return MOE_ERR_UNSUPPORTED;
+  if (which == MOE_PACK_DGRAD && (c->weight_fmt != MOE_WFMT_MXFP8 || !gated(*c))) return MOE_ERR_UNSUPPORTED;
   *bytes = pack_layout(*c, which).total;
   return MOE_OK;
 }
@@ -298,7 +303,7 @@ moe_status_t moe_prepack_weights(const moe_config_t* c, const moe_weights_view_t
   moe_status_t s = moe_config_validate(c);
   if (s != MOE_OK) return s;
   if (!src || (which != MOE_PACK_FORWARD && which != MOE_PACK_DGRAD)) return MOE_ERR_INVALID_ARG;
-  if (which == MOE_PACK_DGRAD && c->weight_fmt != MOE_WFMT_MXFP8) return MOE_ERR_UNSUPPORTED;
+  if (which == MOE_PACK_DGRAD && (c->weight_fmt != MOE_WFMT_MXFP8 || !gated(*c))) return MOE_ERR_UNSUPPORTED;
   REQ(dst); REQ(src->w1_q); REQ(src->w1_s); REQ(src->w2_q); REQ(src->w2_s);
   if (c->weight_fmt == MOE_WFMT_NVFP4) { REQ(src->w1_gs); REQ(src->w2_gs); }
   if (c->w1_bias && which == MOE_PACK_FORWARD) REQ(src->b1);
@@ -342,7 +347,7 @@ moe_status_t moe_debug_unpack_weights(const moe_config_t* c, const void* packed,
   moe_status_t s = moe_config_validate(c);
   if (s != MOE_OK) return s;
   if ((which != MOE_PACK_FORWARD && which != MOE_PACK_DGRAD) || (mat != 1 && mat != 2)) return MOE_ERR_INVALID_ARG;
-  if (which == MOE_PACK_DGRAD && c->weight_fmt != MOE_WFMT_MXFP8) return MOE_ERR_UNSUPPORTED;
+  if (which == MOE_PACK_DGRAD && (c->weight_fmt != MOE_WFMT_MXFP8 || !gated(*c))) return MOE_ERR_UNSUPPORTED;
   REQ(packed); REQ(q); REQ(sc);
   const PackLayout P = pack_layout(*c, which);
   cudaStream_t st = (cudaStream_t)stream;
@@ -483,7 +488,7 @@ struct TcRun {
 // and 32, +13 us at T = 128), and the separate kernels run instead.
 static bool fused_layer(const moe_config_t& c, int T) {
   const int64_t R = (int64_t)T * (c.k + c.n_shared);
-  return !mx_path(c) && T > 0 && R <= 2LL * (c.E + c.n_shared) && c.I <= kFusedMaxI;
+  return !mx_path(c) && gated(c) && T > 0 && R <= 2LL * (c.E + c.n_shared) && c.I <= kFusedMaxI;
 }
 
 // The decoding GEMM's fields shared by its matrices.
@@ -663,8 +668,9 @@ static moe_status_t w1_impl(const moe_config_t* c, const moe_dispatch_t* d, int 
     uint8_t* xgs = at<uint8_t>(ws, L.xgs);
     if (!a_ready) MOE_CHECK_CUDA(launch_gather_mx(d->xq, d->xs, c->H, d->perm_src, kp, R, d->offsets, G, xg, xgs, st));
     MxArgs g = mx_args0();
-    g.n_tiles = P.rows1 / kMxTileN;
+    g.n_tiles = ceil_div(P.rows1, kMxTileN);
     g.I = c->I;
+    g.gated = gated(*c);
     g.b1 = P.off_b1 ? reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(packed) + P.off_b1) : nullptr;
     g.w_row = d->w_row;
     g.act = act_params(c);
@@ -698,7 +704,7 @@ static moe_status_t w1_impl(const moe_config_t* c, const moe_dispatch_t* d, int 
   W1FinArgs f;
   f.P = run.out; f.S = run.S; f.split_stride = run.split_stride; f.R = R; f.I = c->I;
   f.offsets = d->offsets; f.G = G; f.w_row = d->w_row; f.act = act_params(c);
-  f.y1q = y1q; f.y1s = y1s;
+  f.y1q = y1q; f.y1s = y1s; f.gated = gated(*c);
   f.y16 = at<uint16_t>(ws, L.y16);
   f.y_rowexp = at<int32_t>(ws, L.rexp2);
   f.b1 = P.off_b1 ? reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(packed) + P.off_b1) : nullptr;

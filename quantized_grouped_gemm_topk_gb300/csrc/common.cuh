@@ -157,6 +157,12 @@ struct ActParams {
   float alpha, limit;
 };
 
+// The non-gated activation: sReLU, max(h, 0)^2 of W1's I outputs.
+__device__ __forceinline__ float act_plain(float h) {
+  const float r = fmaxf(h, 0.f);
+  return r * r;
+}
+
 // Logistic sigmoid with the fast exponential and divide intrinsics: relative
 // error ~1e-6, far inside the layer's tolerance, and several times cheaper
 // than the IEEE forms in the epilogues that evaluate it per element.

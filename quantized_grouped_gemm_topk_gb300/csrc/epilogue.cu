@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(1024) k_w1_finalize_rows(const W1FinArgs a) {
   const int Rv = min(a.R, a.offsets[a.G]);
   const int64_t r = blockIdx.x;
   if (r >= Rv) return;
-  const float* P = a.P + r * 2 * a.I;
+  const float* P = a.P + r * (a.gated ? 2 : 1) * a.I;   // W1's outputs of row r (sReLU: I, no up half)
   const float wr = a.w_row[r];
   const float* bg = nullptr;   // W1 bias of the row's group (the last e with offsets[e] <= r owns row r)
   if (a.b1) {
@@ -49,16 +49,23 @@ __global__ void __launch_bounds__(1024) k_w1_finalize_rows(const W1FinArgs a) {
   for (int b = warp; b < nb; b += nwarps) {
     const int i = b * 32 + lane;
     float g = 0.f, u = 0.f;
+    float y;
+    if (a.gated) {
 #pragma unroll 4
-    for (int s = 0; s < a.S; ++s) {
-      g += P[(int64_t)s * a.split_stride + i];
-      u += P[(int64_t)s * a.split_stride + a.I + i];
+      for (int s = 0; s < a.S; ++s) {
+        g += P[(int64_t)s * a.split_stride + i];
+        u += P[(int64_t)s * a.split_stride + a.I + i];
+      }
+      if (bg) {
+        g += bg[i];
+        u += bg[a.I + i];
+      }
+      y = wr * act_fwd(g, u, a.act);
+    } else {
+#pragma unroll 4
+      for (int s = 0; s < a.S; ++s) g += P[(int64_t)s * a.split_stride + i];
+      y = wr * act_plain(g);
     }
-    if (bg) {
-      g += bg[i];
-      u += bg[a.I + i];
-    }
-    const float y = wr * act_fwd(g, u, a.act);
     const int e = mx_exponent(warp_max(fabsf(y)));
     const uint8_t c = (uint8_t)(f32x2_to_e4m3x2(y * pow2_neg(e), 0.f) & 0xffu);
     a.y1q[r * a.I + i] = c;

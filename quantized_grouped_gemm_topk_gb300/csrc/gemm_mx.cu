@@ -264,6 +264,25 @@ __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, ui
           orow[n0 + i] = (uint16_t)(i & 1 ? pk[i >> 1] >> 16 : pk[i >> 1] & 0xffffu);
       }
     }
+  } else if (MODE == kMxW1 && !g.gated) {
+    // sReLU: column c is feature ni * 192 + c of a W1 with I outputs
+    const int f0 = w.ni * kMxBN;
+    const float wr = rvalid ? g.w_row[row] : 0.f;
+    for (int b = 0; b < kMxBN / 32; ++b) {
+      const int f = f0 + 32 * b;
+      if (f >= g.I) break;
+      uint32_t v[32];
+      tc::tmem_ld32(acc_tmem + 32 * b, v);
+      tc::tmem_wait_ld();
+      float y[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) y[i] = wr * act_plain(__uint_as_float(v[i]));
+      if (rvalid) {
+        const uint8_t sb = quant_block32_store(y, g.yq + row * g.I + f);
+        g.ys[row * (g.I / 32) + f / 32] = sb;
+        if (g.yst) g.yst[sf4_at(f / 32, row, g.R)] = sb;
+      }
+    }
   } else if (MODE == kMxW1) {
     // columns [0, 96): gate features f0 + c, [96, 192): the same up features
     const int f0 = w.ni * (kMxBN / 2);

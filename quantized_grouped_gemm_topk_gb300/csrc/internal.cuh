@@ -204,6 +204,7 @@ struct MxArgs {
   int b_fp4;                    // B elements are E2M1 (MXFP4 weights), else E4M3
   int bias;                     // the blob carries a W1 bias (checked against its header)
   const float* b1;              // W1 mode (nullable): [G][2I] bias, gate then up
+  int gated;                    // W1 mode: 1 = gate / up halves in each tile, 0 = sReLU (192 plain features a tile)
   int64_t R;                    // token rows (A rows of the token-side modes)
   const float* w_row;           // [R] routing weight per row
   ActParams act;
@@ -252,6 +253,7 @@ struct W1FinArgs {
   uint16_t* y16;                      // [R][I] f16 rows for the W2 B operand
   int32_t* y_rowexp;                  // [R] row exponent of y16
   const float* b1;                    // [G][2I] W1 bias (gate then up), nullable
+  int gated;                          // 0: sReLU, P holds I columns a row (no up half)
 };
 cudaError_t launch_w1_finalize(const W1FinArgs& a, cudaStream_t st);
 

@@ -174,3 +174,17 @@ def test_w1_bias_host_rules(lib):
     L = m.load()
     assert L.moe_layer_backward(ctypes.byref(c1), fake, fake, 16, None, fake, fake, fake, fake, fake, fake,
                                 None) == 2
+
+
+def test_srelu_host_rules(lib):
+    """sReLU: valid; its W1 pack holds I rows (a smaller blob than the gated
+    W1's 2I); no dgrad pack, no bias, no fused layer."""
+    from quantized_grouped_gemm_topk_gb300 import binding as m
+    g = _cfg(wfmt="mxfp8")
+    c = _cfg(wfmt="mxfp8", act="srelu")
+    assert m.moe_config_validate(c) == 0
+    assert m.moe_packed_weights_size(c) < m.moe_packed_weights_size(g)
+    with pytest.raises(m.MoEError):
+        m.moe_packed_weights_size(c, m.MOE_PACK_DGRAD)
+    assert m.moe_config_validate(_cfg(act="srelu", bias=True)) == 2
+    assert not m.moe_layer_fused(_cfg(act="srelu"), 1)

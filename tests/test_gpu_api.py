@@ -254,7 +254,8 @@ def test_launch_accounting_and_phases():
     assert all(b >= a for a, b in zip(ts, ts[1:]))
 
 
-@pytest.mark.parametrize("name,which", [("tiny", 0), ("mxfp4", 0), ("train_small", 0), ("train_small", 1)])
+@pytest.mark.parametrize("name,which", [("tiny", 0), ("mxfp4", 0), ("srelu", 0), ("srelu_mx", 0), ("train_small", 0),
+                                        ("train_small", 1)])
 def test_packed_layout_round_trip(name, which):
     """moe_prepack_weights followed by moe_debug_unpack_weights gives back the
     source bytes of both matrices exactly (NVFP4 tiles with gate/up
@@ -265,6 +266,10 @@ def test_packed_layout_round_trip(name, which):
         s = inputs.workload("tiny", n_shared=1)
     elif name == "mxfp4":
         s = inputs.workload("tiny", H=384, I=384, E=5, k=2, n_shared=1, wfmt="mxfp4")
+    elif name == "srelu":
+        s = inputs.workload("tiny", I=192, act="srelu")                   # NVFP4 tiles of a non-gated W1
+    elif name == "srelu_mx":
+        s = inputs.workload("train", T=8, E=5, H=320, I=256, act="srelu")  # MXFP8 rows, no gate / up interleave
     else:
         s = inputs.workload("train", T=8, E=5, H=320, I=128)
     cfg = m.config_from_shape(s, T_max=8)

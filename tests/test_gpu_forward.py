@@ -253,3 +253,28 @@ def test_w1_bias_forward(case):
     _check_dispatch(s, r, f)
     assert_mx_close(np_(r["views"]["y1_q"]), np_(r["views"]["y1_s"]), f.y1q, f.y1s, "y1")
     assert_close_layer(np_(r["out"].float()), f.out, "out")
+
+
+@pytest.mark.parametrize("case", ["nvfp4", "nvfp4_decode", "mxfp8", "mxfp4"])
+def test_srelu_forward(case):
+    """sReLU (max(h, 0)^2 of a non-gated W1 with I outputs): the NVFP4
+    decoding GEMM with its epilogue kernel (tiny T = 16; a decode size,
+    where the fused layer declines it) and the block-scaled GEMM's epilogue
+    with MXFP8 (training shape, reduced) and MXFP4 weights."""
+    dev = cuda_device()
+    import quantized_grouped_gemm_topk_gb300 as m
+    if case == "nvfp4":
+        s = inputs.workload("tiny", T=16, act="srelu")
+    elif case == "nvfp4_decode":
+        s = inputs.workload("dsv3", T=8, E=32, act="srelu")
+    elif case == "mxfp8":
+        s = inputs.workload("train", T=40, E=8, act="srelu")
+    else:
+        s = inputs.workload("tiny", T=16, wfmt="mxfp4", act="srelu")
+    r = run_forward(s, s.T, dev=dev, seed=8)
+    assert r["status"] == 0
+    assert not m.moe_layer_fused(r["cfg"], s.T)
+    f = oracle_forward(s, r)
+    _check_dispatch(s, r, f)
+    assert_mx_close(np_(r["views"]["y1_q"]), np_(r["views"]["y1_s"]), f.y1q, f.y1s, "y1")
+    assert_close_layer(np_(r["out"].float()), f.out, "out")
