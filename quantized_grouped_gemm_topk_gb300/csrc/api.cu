@@ -546,10 +546,15 @@ static moe_status_t tc_gemm(const moe_config_t* c, const PackLayout& P, int mat,
   g.nmat = 1;
   g.m[0] = tc_mat(c, P, mat, packed, T, rexp, at<float>(ws, L.P), g.max_ctas);
   const int64_t R = (int64_t)T * (c->k + c->n_shared);
-  const int nt = tc_token_tile(T, c->k + c->n_shared, c->E + c->n_shared);
+  int nt = tc_token_tile(T, c->k + c->n_shared, c->E + c->n_shared);
+  // 128-token tiles halve the weight decoding per FLOP, but with one MMA
+  // issuer and two accumulators they pay off only on long K (measured on
+  // the skewed prefill: W1, K = 4096, 1180 -> 1044 us; W2, K = 1536,
+  // 668 -> 826 us)
+  if (nt == 128 && g.m[0].K < 4096) nt = 64;
   // prefill-sized groups: units of at most 8 token tiles, so a hot group's
   // rows spread over many CTAs
-  g.split_rows = nt >= 32 ? 8 * nt : 0;
+  g.split_rows = nt >= 128 ? 4 * nt : nt >= 32 ? 8 * nt : 0;
   TcMaps maps;
   if (!make_tmaps_b(maps.m[0], a16, R, g.m[0].K)) return MOE_ERR_CUDA;
   std::memcpy(&maps.m[1], &maps.m[0], sizeof(maps.m[0]));

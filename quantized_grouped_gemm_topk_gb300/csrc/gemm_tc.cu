@@ -69,7 +69,7 @@ template <int NT>
 struct TcCfg {
   // Each MMA issuer accumulates into its own NT-column tile; a D buffer
   // holds all of them and the epilogue adds them.
-  static constexpr int P = NT <= 32 ? 4 : 2;                         // MMA issuers
+  static constexpr int P = NT <= 32 ? 4 : NT <= 64 ? 2 : 1;          // MMA issuers
   static constexpr int DStride = P * NT;                             // TMEM columns per D buffer
   // D buffers: three where they fit next to the A buffers (16-token tiles),
   // so the epilogue may fall two units behind the MMAs when units are short
@@ -81,7 +81,7 @@ struct TcCfg {
   // every phase of its slots in order.
   static constexpr int WSlot = (2 * CB + 1023) / 1024 * 1024;
   static constexpr int BSlot = 2 * NT * 128;                         // two chunks x NT rows x 64 f16
-  static constexpr int BS = NT == 16 ? 16 : 8;                       // activation slots
+  static constexpr int BS = NT == 16 ? 16 : NT == 128 ? 4 : 8;       // activation slots
   static constexpr int WSraw = (kSmemBudget - BS * BSlot) / WSlot / kTcNG * kTcNG;
   static constexpr int WS = WSraw > 24 ? 24 : WSraw;                 // weight stages
   static constexpr int SmemBytes = WS * WSlot + BS * BSlot + 1024 /*align*/ + 1024 /*barriers*/;
@@ -362,7 +362,9 @@ __device__ __forceinline__ uint32_t first_own(uint32_t base, uint32_t r, uint32_
 // rows; the MMA still spans round_up(nv, 16) rows, and rows past the box
 // (other chunks' data or stale shared memory) only reach accumulator columns
 // of tokens past nv, which the epilogue never reads.
-__device__ __forceinline__ int box_index(int nv) { return nv <= 8 ? 0 : nv <= 16 ? 1 : nv <= 32 ? 2 : 3; }
+__device__ __forceinline__ int box_index(int nv) {
+  return nv <= 8 ? 0 : nv <= 16 ? 1 : nv <= 32 ? 2 : nv <= 64 ? 3 : 4;
+}
 
 template <int NT>
 __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant__ TcArgs g,
@@ -534,7 +536,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
     // ---------------- activation producer ----------------
     if (lane == 0) {
       for (int m = 0; m < g.nmat; ++m)
-        for (int i = 0; i < 4; ++i) tc::prefetch_tmap(&maps.m[m][i]);
+        for (int i = 0; i < kTcBoxes; ++i) tc::prefetch_tmap(&maps.m[m][i]);
       const uint64_t pol_a = tc::policy_evict_last();
       const int32_t* ready = g.f.cnt + g.G;
       uint32_t ait = 0;
@@ -697,6 +699,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
         // CTA: every lane did its own acquire of the group's flag first)
         const float px0 = ldexpf(1.0f, lane < nt ? M.act_rowexp[t0 + lane] : 0);
         const float px1 = ldexpf(1.0f, NT > 32 && lane + 32 < nt ? M.act_rowexp[t0 + 32 + lane] : 0);
+        const float px2 = ldexpf(1.0f, NT > 64 && lane + 64 < nt ? M.act_rowexp[t0 + 64 + lane] : 0);
+        const float px3 = ldexpf(1.0f, NT > 64 && lane + 96 < nt ? M.act_rowexp[t0 + 96 + lane] : 0);
         const uint32_t a_first = ait;
         ait += pairs;
         const int d = dit % C::ND;
@@ -736,7 +740,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
           }
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float px = __shfl_sync(kFull, cb + i < 32 ? px0 : px1, (cb + i) & 31);   // every lane
+            const int kk = (cb + i) >> 5;
+            const float px = __shfl_sync(kFull, kk == 0 ? px0 : kk == 1 ? px1 : kk == 2 ? px2 : px3,
+                                         (cb + i) & 31);   // every lane
             if (nvalid && cb + i < nt) outp[(int64_t)(t0 + cb + i) * M.N] = acc[i] * rowf * px;
           }
         }
@@ -807,13 +813,13 @@ static EncodeTiledFn encode_fn() {
 // f16 matrix [rows][cols] viewed as (64 columns, rows, cols / 64 chunks),
 // strides (2 B, cols * 2 B, 128 B); boxes of 64 x (8 << i) x 2 chunks,
 // 128-byte swizzle; rows past the end and chunks past the last read as zero.
-bool make_tmaps_b(CUtensorMap (&m)[4], const void* base, int64_t rows, int64_t cols) {
+bool make_tmaps_b(CUtensorMap (&m)[kTcBoxes], const void* base, int64_t rows, int64_t cols) {
   EncodeTiledFn fn = encode_fn();
   if (!fn || cols % kChunkK != 0) return false;
   cuuint64_t dims[3] = {(cuuint64_t)kChunkK, (cuuint64_t)std::max<int64_t>(rows, 1), (cuuint64_t)(cols / kChunkK)};
   cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)kChunkK * 2};
   cuuint32_t estr[3] = {1, 1, 1};
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < kTcBoxes; ++i) {
     cuuint32_t box[3] = {(cuuint32_t)kChunkK, 8u << i, 2u};
     if (fn(&m[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -835,14 +841,16 @@ int tc_token_tile(int T, int kp, int G) {
   const double avg = (double)T * kp / std::max(G, 1);
   if (avg <= 12.0) return 16;
   if (avg <= 24.0) return 32;
-  return 64;
+  if (avg <= 96.0) return 64;
+  return 128;   // prefill-sized groups: each decoded weight pair feeds 128 tokens
 }
 
 cudaError_t launch_gemm_tc(const TcArgs& g, const TcMaps& maps, int nt, cudaStream_t st) {
   const int grid = std::max(1, g.max_ctas);
   const cudaError_t e = nt <= 16 ? launch_tc_t<16>(g, maps, grid, st)
                         : nt <= 32 ? launch_tc_t<32>(g, maps, grid, st)
-                                   : launch_tc_t<64>(g, maps, grid, st);
+                        : nt <= 64 ? launch_tc_t<64>(g, maps, grid, st)
+                                   : launch_tc_t<128>(g, maps, grid, st);
   note_launch();
   return e;
 }

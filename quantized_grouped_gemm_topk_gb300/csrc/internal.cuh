@@ -156,15 +156,16 @@ struct TcArgs {
 constexpr int kFusedMaxI = 2048;
 // Ints of the fused layer's counters for G groups.
 inline int64_t tc_fused_counters(int G) { return 2LL * G; }
+constexpr int kTcBoxes = 5;   // activation boxes of 8, 16, 32, 64, 128 rows
 // Tensor maps of the f16 operand rows a16 [rows, cols], viewed as
 // (64 columns, rows, cols / 64 chunks): m[i] loads a box of 8 << i rows of
 // two consecutive 64-column chunks in one copy (128-byte swizzle), stored
 // chunk after chunk.
 struct TcMaps {
-  CUtensorMap m[2][4];        // per matrix (the fused layer's W2 reads y16)
+  CUtensorMap m[2][kTcBoxes]; // per matrix (the fused layer's W2 reads y16)
 };
-bool make_tmaps_b(CUtensorMap (&m)[4], const void* base, int64_t rows, int64_t cols);
-// nt: tokens per MMA tile (16, 32 or 64); tc_token_tile picks it from the
+bool make_tmaps_b(CUtensorMap (&m)[kTcBoxes], const void* base, int64_t rows, int64_t cols);
+// nt: tokens per MMA tile (16, 32, 64 or 128); tc_token_tile picks it from the
 // average rows per group.
 int tc_token_tile(int T, int kp, int G);
 cudaError_t launch_gemm_tc(const TcArgs& g, const TcMaps& maps, int nt, cudaStream_t st);
