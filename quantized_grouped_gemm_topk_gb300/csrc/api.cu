@@ -819,14 +819,10 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
     const int64_t n = (int64_t)T * c->E;
     if (KS > 1 && n * KS > kRouteStage) {
       // too many partials for the routing kernel's single block to sum: a
-      // grid-wide pass (same ks order, same result) writes the logits, then
-      // the warp-per-token top-k kernel routes all tokens in parallel and
-      // the dispatch kernel takes the ids as given
-      MOE_CHECK_CUDA(launch_pdl(k_reduce_partials, dim3((unsigned)std::min<int64_t>((n + 255) / 256, 4096)), dim3(256),
-                                0, st, (const float*)part, KS, n, v.logits));
-      note_launch();
-      MOE_CHECK_CUDA(launch_topk_only(v.logits, T, c->E, c->k, c->routed_scale, v.d.topk_ids, v.d.topk_w,
-                                      at<int32_t>(ws, L.status), st));
+      // block per token sums its partials (in ks order) into the logits and
+      // routes it; the dispatch kernel takes the ids as given
+      MOE_CHECK_CUDA(launch_sum_topk(part, KS, T, c->E, c->k, c->routed_scale, v.logits, v.d.topk_ids, v.d.topk_w,
+                                     at<int32_t>(ws, L.status), st));
       a.part = v.logits; a.KS = 1; a.route = false;
     }
   } else {

@@ -102,6 +102,10 @@ cudaError_t launch_router(const uint16_t* x, const float* Wr, int T, int H, int 
 cudaError_t launch_route_dispatch(const RouteArgs& a, cudaStream_t st);
 cudaError_t launch_topk_only(const float* logits, int T, int E, int k, float rs, int32_t* ids, float* w,
                              int32_t* status, cudaStream_t st);
+// Sums the router's KS split-K partials [KS][T][E] into logits (ks order)
+// and routes each token: one block per token.
+cudaError_t launch_sum_topk(const float* part, int KS, int T, int E, int k, float rs, float* logits, int32_t* ids,
+                            float* w, int32_t* status, cudaStream_t st);
 cudaError_t launch_quant_rows(const uint16_t* src, int rows, int C, uint8_t* q, uint8_t* s, cudaStream_t st);
 
 // ---- NVFP4 grouped GEMM on tcgen05 (gemm_tc.cu) ---------------------------------

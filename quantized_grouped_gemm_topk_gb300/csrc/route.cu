@@ -624,6 +624,33 @@ cudaError_t launch_route_dispatch(const RouteArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// Router split-K partials -> logits -> top-k, one block per token: its
+// threads sum the partials of the token's experts in ks order (each a
+// handful of independent loads), then its first warp routes the token.
+template <int VPL>
+__global__ void __launch_bounds__(256) k_sum_topk(const float* __restrict__ part, int KS, int T, int E, int k,
+                                                  float rs, float* __restrict__ logits, int32_t* __restrict__ ids,
+                                                  float* __restrict__ wts, int32_t* status) {
+  pdl_enter();
+  const int t = blockIdx.x;
+  const int64_t n = (int64_t)T * E;
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    logits[(int64_t)t * E + e] = sum_partials(part, KS, n, (int64_t)t * E + e);
+  __syncthreads();
+  if (threadIdx.x < 32) route_token<VPL>(t, threadIdx.x, logits, 1, T, E, k, rs, logits, ids, wts, status);
+}
+
+cudaError_t launch_sum_topk(const float* part, int KS, int T, int E, int k, float rs, float* logits, int32_t* ids,
+                            float* w, int32_t* status, cudaStream_t st) {
+  if (T == 0) return cudaSuccess;
+  cudaError_t e = E <= 256 ? launch_pdl(k_sum_topk<8>, dim3(T), dim3(256), 0, st, part, KS, T, E, k, rs, logits,
+                                        ids, w, status)
+                           : launch_pdl(k_sum_topk<64>, dim3(T), dim3(256), 0, st, part, KS, T, E, k, rs, logits,
+                                        ids, w, status);
+  note_launch();
+  return e;
+}
+
 cudaError_t launch_topk_only(const float* logits, int T, int E, int k, float rs, int32_t* ids, float* w,
                              int32_t* status, cudaStream_t st) {
   if (T == 0) return cudaSuccess;
