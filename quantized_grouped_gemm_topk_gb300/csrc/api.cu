@@ -598,7 +598,8 @@ static moe_status_t mx_token_gemm(const moe_config_t* c, MxArgs& g, int mode, co
   MxMaps maps;
   if (!make_tmaps_mx_a(&maps, aq, R, K) ||
       !make_tmap_mx(&maps.b, b + (mat == 1 ? P.off_w1 : P.off_w2), (int64_t)P.G * rows, K, mx_b_box_rows(),
-                    g.b_fp4 != 0))
+                    g.b_fp4 != 0) ||
+      !make_tmap_mx_sf(&maps.sfb, g.b_sf, g.b_rows, ceil_div(K, 128), g.b_sf_ld))
     return MOE_ERR_CUDA;
   MOE_CHECK_CUDA(launch_gemm_mx(g, maps, mx_grid(*c), st));
   return MOE_OK;
@@ -903,7 +904,8 @@ static moe_status_t mx_wgrad(const moe_config_t* c, const uint8_t* pq, const uin
   g.out = out; g.out_ld = N;
   g.status = status;
   MxMaps maps;
-  if (!make_tmaps_mx_a(&maps, pq, M, Rp) || !make_tmap_mx(&maps.b, qq, N, Rp, mx_b_box_rows(), false))
+  if (!make_tmaps_mx_a(&maps, pq, M, Rp) || !make_tmap_mx(&maps.b, qq, N, Rp, mx_b_box_rows(), false) ||
+      !make_tmap_mx_sf(&maps.sfb, qs, N, Rp / 128, N))
     return MOE_ERR_CUDA;
   MOE_CHECK_CUDA(launch_gemm_mx(g, maps, mx_grid(*c), st));
   return MOE_OK;

@@ -82,7 +82,13 @@ constexpr uint32_t kMxSfCol0 = 2 * kMxBN;         // 384
 constexpr uint32_t kMxSfCols = 12;
 constexpr int kMxMaxGroups = 2048;
 constexpr int kMxBarBytes = 1024;
-constexpr int kMxSmemBytes = 1024 /*align*/ + kMxStages * kMxStageBytes + kMxBarBytes + 4 * (kMxMaxGroups + 1);
+// B's scale words of a stage (one SF4 word per B row) come with the stage's
+// tensor copies into shared memory: they are weight scales streamed from
+// HBM, whose latency a register prefetch a few short stages deep (decode)
+// does not cover.
+constexpr int kMxSfbBytes = kMxBN * 4;
+constexpr int kMxSmemBytes =
+    1024 /*align*/ + kMxStages * (kMxStageBytes + kMxSfbBytes) + kMxBarBytes + 4 * (kMxMaxGroups + 1);
 static_assert(kMxSfCol0 + kMxSfSlots * kMxSfCols <= kMxTmemCols, "tensor memory budget");
 static_assert(kMxSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kMxSfSlots % 4 == 0, "scale prefetch depth divides the slot count");
@@ -409,7 +415,8 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* sa = smem;
   uint8_t* sb = smem + kMxStages * kMxAStage;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kMxStages * kMxStageBytes);
+  uint8_t* sfb = smem + kMxStages * kMxStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sfb + kMxStages * kMxSfbBytes);
   uint64_t* full = bars;
   uint64_t* empty = full + kMxStages;
   uint64_t* sffull = empty + kMxStages;
@@ -490,6 +497,7 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
 #pragma unroll
       for (int i = 0; i < 4; ++i) tc::prefetch_tmap(&maps.a[i]);
       tc::prefetch_tmap(&maps.b);
+      tc::prefetch_tmap(&maps.sfb);
       // bytes a stage's B copy reports to the barrier: packed E2M1 reports
       // its global bytes (two elements a byte) although it lands one element
       // a byte in shared memory (8 data bytes, then an 8-byte gap the copy
@@ -505,8 +513,9 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
           const int slot = it % kMxStages;
           if (!tc::mbar_wait(&empty[slot], ((it / kMxStages) & 1) ^ 1, abort)) { ok = false; break; }
           const int ai = mx_a_box(w.a_valid);
-          tc::mbar_arrive_expect_tx(&full[slot], (uint32_t)(kMxBK * (16 << ai)) + b_tx);
+          tc::mbar_arrive_expect_tx(&full[slot], (uint32_t)(kMxBK * (16 << ai)) + b_tx + kMxSfbBytes);
           const int kx = w.k0 + s * kMxBK;
+          tc::tma_load_2d_plain(sfb + slot * kMxSfbBytes, &maps.sfb, w.b_row0, kx / kMxBK, &full[slot]);
           tc::tma_load_2d_plain(sa + slot * kMxAStage, &maps.a[ai], kx, w.a_row0, &full[slot]);
           if constexpr (kMxCl > 1) {
             // this CTA's part of the shared B tile, into every CTA of the cluster
@@ -582,49 +591,45 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
       MxUnit w;
       mx_unit(g, uoff, u, rank, w);
       const int nk = mx_stages(w.klen);
-      // each row's SF4 column (nullptr: no such row)
+      // each A row's SF4 column (nullptr: no such row); B's words come with
+      // the stage into shared memory (sfb)
       const uint32_t* pa[4];
-      const uint32_t* pb[4 + kNB1];
       const uint32_t* wa = reinterpret_cast<const uint32_t*>(g.a_sf);
-      const uint32_t* wb = reinterpret_cast<const uint32_t*>(g.b_sf);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const int64_t ra = (int64_t)w.a_row0 + 32 * c + lane;
         pa[c] = ra < g.a_rows ? wa + ra : nullptr;
       }
-#pragma unroll
-      for (int c = 0; c < 4 + kNB1; ++c) {
-        const int64_t rb = (int64_t)w.b_row0 + 32 * c + lane;
-        pb[c] = rb < g.b_rows ? wb + rb : nullptr;
-      }
       const int kw0 = w.k0 / kMxBK;
-      // four stages of scale words in flight in registers
-      uint32_t va[4][4], vb[4][4 + kNB1];
+      // four stages of A's scale words in flight in registers
+      uint32_t va[4][4];
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const bool live = j < nk;
 #pragma unroll
         for (int c = 0; c < 4; ++c) va[j][c] = (pa[c] && live) ? load_sf4_word(pa[c], g.a_sf_ld, kw0 + j) : 0u;
-#pragma unroll
-        for (int c = 0; c < 4 + kNB1; ++c)
-          vb[j][c] = (pb[c] && live) ? load_sf4_word(pb[c], g.b_sf_ld, kw0 + j) : 0u;
       }
       for (int s0 = 0; s0 < nk; s0 += 4) {
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int s = s0 + j;
           if (s < nk && ok) {
-            const int fs = it % kMxSfSlots;
+            const int fs = it % kMxSfSlots, slot = it % kMxStages;
             // the warp's collective tensor-memory stores need one decision
-            const bool got = tc::mbar_wait(&sfempty[fs], ((it / kMxSfSlots) & 1) ^ 1, abort);
+            bool got = tc::mbar_wait(&sfempty[fs], ((it / kMxSfSlots) & 1) ^ 1, abort);
+            got = got && tc::mbar_wait(&full[slot], (it / kMxStages) & 1, abort);
             if (!__all_sync(kFull, got)) {
               ok = false;
             } else {
               tc::fence_after_sync();
+              const uint32_t* sw = reinterpret_cast<const uint32_t*>(sfb + slot * kMxSfbBytes);
+              uint32_t vb[4 + kNB1];
+#pragma unroll
+              for (int c = 0; c < 4 + kNB1; ++c) vb[c] = sw[32 * c + lane];
               const uint32_t col = kMxSfCol0 + fs * kMxSfCols;
               tc::tmem_st4(lane_base + col, va[j][0], va[j][1], va[j][2], va[j][3]);
-              tc::tmem_st4(lane_base + col + 4, vb[j][0], vb[j][1], vb[j][2], vb[j][3]);
-              tc::tmem_st4(lane_base + col + 8, vb[j][4], vb[j][5], 0u, 0u);
+              tc::tmem_st4(lane_base + col + 4, vb[0], vb[1], vb[2], vb[3]);
+              tc::tmem_st4(lane_base + col + 8, vb[4], vb[5], 0u, 0u);
               tc::tmem_wait_st();
               tc::fence_before_sync();
               __syncwarp();
@@ -636,9 +641,6 @@ __global__ void __launch_bounds__(kMxThreads, 1) k_gemm_mx(const __grid_constant
 #pragma unroll
               for (int c = 0; c < 4; ++c)
                 va[j][c] = (pa[c] && live) ? load_sf4_word(pa[c], g.a_sf_ld, kw0 + s4) : 0u;
-#pragma unroll
-              for (int c = 0; c < 4 + kNB1; ++c)
-                vb[j][c] = (pb[c] && live) ? load_sf4_word(pb[c], g.b_sf_ld, kw0 + s4) : 0u;
             }
           }
         }
@@ -719,6 +721,18 @@ bool make_tmap_mx(CUtensorMap* map, const void* base, int64_t rows, int64_t cols
   return fn(map, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tmap_mx_sf(CUtensorMap* map, const void* sf, int64_t rows, int64_t words, int64_t ld) {
+  EncodeTiledFnMx fn = encode_fn_mx();
+  if (!fn || ld % 4 != 0 || ((uintptr_t)sf & 15u) || rows > ld) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)std::max<int64_t>(rows, 1), (cuuint64_t)std::max<int64_t>(words, 1)};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
+  cuuint32_t box[2] = {(cuuint32_t)kMxBN, 1u};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<void*>(sf), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

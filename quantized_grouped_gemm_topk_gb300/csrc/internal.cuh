@@ -228,6 +228,7 @@ struct MxArgs {
 struct MxMaps {
   CUtensorMap a[4];             // A boxes of 128 K-elements x 16 << i rows (the tile's rows pick one)
   CUtensorMap b;                // B box of 128 K-elements x mx_b_box_rows() rows
+  CUtensorMap sfb;              // B's SF4 scale words: boxes of one word x 192 rows
 };
 // Matrix [rows][cols elements] as a 2-D tensor map, boxes of 128 elements x
 // box_rows rows, 128-byte swizzle, zero fill past the edges. fp4: packed
@@ -235,6 +236,9 @@ struct MxMaps {
 // memory, the layout the block-scaled MMA reads; else one byte per element.
 bool make_tmap_mx(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_rows, bool fp4);
 bool make_tmaps_mx_a(MxMaps* maps, const void* base, int64_t rows, int64_t cols);
+// SF4 scale words [words][ld] (uint32) of `rows` rows as a 2-D tensor map,
+// boxes of one word x 192 rows; ld must be a multiple of 4.
+bool make_tmap_mx_sf(CUtensorMap* map, const void* sf, int64_t rows, int64_t words, int64_t ld);
 int mx_tile_n();
 int mx_b_box_rows();          // rows of B per tensor copy (each CTA of a pair copies this many)
 int mx_tile_m();
