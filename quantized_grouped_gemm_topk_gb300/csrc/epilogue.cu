@@ -221,74 +221,185 @@ cudaError_t launch_combine(const uint16_t* z, const int32_t* inv, const float* t
 }
 
 // ---- transposed MXFP8 copies ---------------------------------------------------
-// One CTA per padded 32-row block (grid-stride): the block's group is found
-// once, the source row of each of its 32 rows is staged in shared memory,
-// then the warps stride over 32-column chunks, lane = column: each lane
-// gathers its column's 32 values (every row read is one coalesced 64-byte
-// segment across the warp), quantises them along the row axis and writes
-// 32 code bytes and its column's scale byte.
-__global__ void __launch_bounds__(256) k_quant_cols(const ColQuantArgs a) {
-  __shared__ int64_t src_row[32];
-  __shared__ int blk_e;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const int ncc = (a.C + 31) / 32;
-  const int64_t npb = a.r_pad_max / 32;
-  const int ptot = a.poff[a.G];
-  for (int64_t pb = blockIdx.x; pb < npb; pb += gridDim.x) {
-    const int prow = (int)(pb * 32);
-    if (prow >= ptot) break;                 // blocks are visited in increasing order
-    __syncthreads();                         // the previous block's staging is no longer read
-    if (threadIdx.x == 0) {
-      int lo = 0, hi = a.G - 1;              // group with poff[e] <= prow < poff[e+1]
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (a.poff[mid] <= prow) lo = mid; else hi = mid - 1;
-      }
-      blk_e = lo;
-    }
-    __syncthreads();
-    const int e = blk_e;
-    const int cnt = a.offsets[e + 1] - a.offsets[e];
-    const int p0 = prow - a.poff[e];
-    if (threadIdx.x < 32) {
-      const int i = threadIdx.x;
-      src_row[i] = p0 + i < cnt ? (int64_t)(a.row_map[a.offsets[e] + p0 + i] / a.row_div) : -1;
-    }
-    __syncthreads();
-    for (int cc = warp; cc < ncc; cc += nwarps) {
-      const int c = cc * 32 + lane;
-      const bool cok = c < a.C;
-      float v[32];
-      float am = 0.f;
+// Work items are (128-row block, 128-column tile) pairs, row-block major.
+// Groups are padded to multiples of 128 rows, so a row block lies in one
+// group. A persistent CTA takes an even share of the items: it first finds,
+// for each row block its share touches (at most kQcMaxRb; one warp per block),
+// the block's group (the lanes count the groups whose padded start is <= the
+// block's first row) and the source row of each of its 128 rows. It then
+// streams its tiles through a three-stage cp.async ring in shared memory
+// without a break at row-block boundaries (a warp copies two 256-byte row
+// segments per request; pad rows and columns past C are zero-filled). In the
+// ring, the 16-byte chunk k of row r sits at chunk k ^ 2(r / 32), so that the
+// reads below are free of bank conflicts. Lane l of warp w owns the column
+// pair 2(8w + l/4) and the 32-row block l % 4: it reads 32 words (both
+// columns' values of its 32 rows), quantises each column along the row axis
+// and writes its 2 x 32 code bytes; the four lanes of a pair fill whole
+// 128-byte lines, and the first of them writes the pair's two scale words
+// (one byte per 32-row block).
+constexpr int kQcRows = 128, kQcCols = 128, kQcStages = 3, kQcMaxRb = 8;
+constexpr int kQcRowBytes = kQcCols * 2;
+constexpr int kQcTileBytes = kQcRows * kQcRowBytes;
+constexpr int kQcSmem = kQcStages * kQcTileBytes + kQcMaxRb * kQcRows * 4;
+
+__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, bool ok) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(ok ? 16 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+
+// Elementwise max of |a| and |b| over the two bf16 halves; the result's sign
+// bits are those of a xor b (callers mask them off). A NaN half yields the
+// other input's half.
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// 32 bytes to a 32-byte aligned global address in one store.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* v) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(v[0]), "r"(v[1]),
+               "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+
+__device__ __forceinline__ void st_codes32(uint8_t* p, const uint32_t* v, bool a32) {
+  if (a32) {
+    st_global_v8(p, v);
+  } else {
+    uint4* d = reinterpret_cast<uint4*>(p);
+    d[0] = make_uint4(v[0], v[1], v[2], v[3]);
+    d[1] = make_uint4(v[4], v[5], v[6], v[7]);
+  }
+}
+
+__global__ void __launch_bounds__(256, 2) k_quant_cols(const ColQuantArgs a) {
+  extern __shared__ __align__(128) uint8_t qsm[];
+  int* src_row = reinterpret_cast<int*>(qsm + kQcStages * kQcTileBytes);   // [kQcMaxRb][kQcRows]
+  const int nct = (a.C + kQcCols - 1) / kQcCols;
+  const int64_t nitem = (int64_t)(__ldg(&a.poff[a.G]) / kQcRows) * nct;
+  const int64_t i0 = (int64_t)blockIdx.x * nitem / gridDim.x;
+  const int njob = (int)((int64_t)(blockIdx.x + 1) * nitem / gridDim.x - i0);
+  if (njob <= 0) return;
+  const int rb0 = (int)(i0 / nct);
+  const int ct_first = (int)(i0 - (int64_t)rb0 * nct);
+  // row blocks of the share; the launch sizes the grid so that this is at
+  // most kQcMaxRb (items beyond that are left out rather than misread)
+  const int nrb = min((ct_first + njob - 1) / nct + 1, kQcMaxRb);
+  const int njob_ok = min(njob, nrb * nct - ct_first);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp < nrb) {
+    const int prow = (rb0 + warp) * kQcRows;
+    int n = 0;                               // groups e < G with poff[e] <= prow
+    for (int j = lane; j < a.G; j += 32) n += __ldg(&a.poff[j]) <= prow;
 #pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        const int64_t sr = src_row[i];
-        const float x = (cok && sr >= 0) ? bf16_bits_to_f32(a.src16[sr * a.C + c]) : 0.f;
-        v[i] = x;
-        am = fmaxf(am, fabsf(x));
-      }
-      if (!cok) continue;
-      const int ex = mx_exponent(am);
-      const float sc = pow2_neg(ex);
-      uint32_t wds[8];
+    for (int o = 16; o > 0; o >>= 1) n += __shfl_xor_sync(0xffffffffu, n, o);
+    const int e = n - 1;
+    const int off = __ldg(&a.offsets[e]);
+    const int cnt = __ldg(&a.offsets[e + 1]) - off;
+    const int p0 = prow - __ldg(&a.poff[e]);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        wds[q] = (uint32_t)f32x2_to_e4m3x2(v[4 * q] * sc, v[4 * q + 1] * sc) |
-                 ((uint32_t)f32x2_to_e4m3x2(v[4 * q + 2] * sc, v[4 * q + 3] * sc) << 16);
-      }
-      uint4* dst = reinterpret_cast<uint4*>(a.q + (int64_t)c * a.r_pad_max + prow);
-      dst[0] = make_uint4(wds[0], wds[1], wds[2], wds[3]);
-      dst[1] = make_uint4(wds[4], wds[5], wds[6], wds[7]);
-      a.s[sf4_at(pb, c, a.C)] = (uint8_t)(ex + 127);
+    for (int i = lane; i < kQcRows; i += 32)
+      src_row[warp * kQcRows + i] = p0 + i < cnt ? __ldg(&a.row_map[off + p0 + i]) / a.row_div : -1;
+  }
+  __syncthreads();
+  // Copies: thread t takes chunk t % 16 of rows t / 16 + 16k, k < 8; row r's
+  // chunk lands at chunk ^ 2(r / 32) = chunk ^ (k & 6). The copy cursor
+  // (row block, column tile, stage) runs two tiles ahead of the compute one.
+  const int ch = threadIdx.x & 15;
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(qsm) + (uint32_t)((threadIdx.x >> 4) * kQcRowBytes);
+  int cp_rb = 0, cp_ct = ct_first, cp_st = 0;
+  auto issue_next = [&]() {
+    const int c = cp_ct * kQcCols + ch * 8;
+    const bool cok = c < a.C;
+    const int* rows = src_row + cp_rb * kQcRows + (threadIdx.x >> 4);
+    const uint32_t st = sbase + (uint32_t)(cp_st * kQcTileBytes);
+#pragma unroll
+    for (int k = 0; k < kQcRows / 16; ++k) {
+      const int sr = rows[16 * k];
+      const bool ok = cok && sr >= 0;
+      cp_async16_zfill(st + (uint32_t)(16 * k * kQcRowBytes + ((ch ^ (k & 6)) << 4)),
+                       ok ? a.src16 + (int64_t)sr * a.C + c : a.src16, ok);
     }
+    if (++cp_ct == nct) { cp_ct = 0; ++cp_rb; }
+    if (++cp_st == kQcStages) cp_st = 0;
+  };
+  const int rb = lane & 3;                   // 32-row block within the 128 rows
+  const int cl = (warp * 8 + (lane >> 2)) * 2;  // even tile-local column
+  const uint32_t roff = (uint32_t)(rb * 32 * kQcRowBytes + ((((cl >> 3) ^ (rb * 2))) << 4) + (cl & 7) * 2);
+  const bool a32 = (reinterpret_cast<uintptr_t>(a.q) & 31) == 0;
+  int q_rb = 0, q_ct = ct_first, q_st = 0;
+  issue_next();
+  cp_async_commit();
+  if (njob_ok > 1) issue_next();
+  cp_async_commit();
+  for (int j = 0; j < njob_ok; ++j) {
+    if (j + 2 < njob_ok) issue_next();       // into the stage read two tiles ago
+    cp_async_commit();
+    cp_async_wait<2>();                      // this thread's copies of tile j have landed
+    __syncthreads();                         // ... and every other thread's
+    const uint8_t* src = qsm + q_st * kQcTileBytes + roff;
+    uint32_t w[32];                          // bf16 pairs: column cl (low half), cl + 1 (high half)
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = *reinterpret_cast<const uint32_t*>(src + i * kQcRowBytes);
+    // |max| of each half over the 32 rows, four chains; signs of the result are dropped
+    uint32_t m[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 32; ++i) m[i & 3] = bf16x2_absmax(m[i & 3], w[i]);
+    const uint32_t mm = bf16x2_absmax(bf16x2_absmax(m[0], m[1]), bf16x2_absmax(m[2], m[3]));
+    const int ex0 = mx_exponent(__uint_as_float((mm << 16) & 0x7fffffffu));
+    const int ex1 = mx_exponent(__uint_as_float(mm & 0x7fff0000u));
+    uint32_t s0 = 0, s1 = 0;                 // the pair's scale words, bytes in 32-row block order
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      s0 |= (uint32_t)(__shfl_sync(0xffffffffu, ex0, (lane & ~3) + r) + 127) << (8 * r);
+      s1 |= (uint32_t)(__shfl_sync(0xffffffffu, ex1, (lane & ~3) + r) + 127) << (8 * r);
+    }
+    const int prow = (rb0 + q_rb) * kQcRows;
+    const int c = q_ct * kQcCols + cl;
+    if (c < a.C) {                           // C is a multiple of 8: c + 1 < C too
+      const float2 sc = make_float2(pow2_neg(ex0), pow2_neg(ex1));
+      uint32_t q0[8], q1[8];                 // codes of column cl, cl + 1: four rows per word
+#pragma unroll
+      for (int i = 0; i < 32; i += 2) {
+        const float2 ya = __fmul2_rn(make_float2(__uint_as_float(w[i] << 16), __uint_as_float(w[i] & 0xffff0000u)), sc);
+        const float2 yb =
+            __fmul2_rn(make_float2(__uint_as_float(w[i + 1] << 16), __uint_as_float(w[i + 1] & 0xffff0000u)), sc);
+        const uint32_t p0 = f32x2_to_e4m3x2(ya.x, yb.x), p1 = f32x2_to_e4m3x2(ya.y, yb.y);
+        if (i & 2) {
+          q0[i >> 2] |= p0 << 16;
+          q1[i >> 2] |= p1 << 16;
+        } else {
+          q0[i >> 2] = p0;
+          q1[i >> 2] = p1;
+        }
+      }
+      uint8_t* d0 = a.q + (int64_t)c * a.r_pad_max + prow + rb * 32;
+      st_codes32(d0, q0, a32);
+      st_codes32(d0 + a.r_pad_max, q1, a32);
+      if (rb == 0)
+        *reinterpret_cast<uint2*>(reinterpret_cast<uint32_t*>(a.s) + (int64_t)(prow / kQcRows) * a.C + c) =
+            make_uint2(s0, s1);
+    }
+    if (++q_ct == nct) { q_ct = 0; ++q_rb; }
+    if (++q_st == kQcStages) q_st = 0;
+    __syncthreads();                         // the stage is refilled two iterations on
   }
 }
 
 cudaError_t launch_quant_cols(const ColQuantArgs& a, cudaStream_t st) {
   if (a.r_pad_max == 0) return cudaSuccess;
-  const int64_t npb = a.r_pad_max / 32;
-  const int blocks = (int)std::max<int64_t>(1, std::min<int64_t>(npb, (int64_t)device_sms() * 8));
-  k_quant_cols<<<blocks, 256, 0, st>>>(a);
+  if (a.C % 8 || a.r_pad_max % kQcRows) return cudaErrorInvalidValue;
+  // Two CTAs per SM, or more when a share would span more than kQcMaxRb row
+  // blocks: a share of ceil(nrb * nct / grid) <= (kQcMaxRb - 1) * nct items
+  // touches at most kQcMaxRb row blocks.
+  const int64_t nrb = a.r_pad_max / kQcRows;
+  const int64_t grid = std::max<int64_t>(2 * device_sms(), (nrb + kQcMaxRb - 2) / (kQcMaxRb - 1));
+  cudaError_t e = cudaFuncSetAttribute(k_quant_cols, cudaFuncAttributeMaxDynamicSharedMemorySize, kQcSmem);
+  if (e != cudaSuccess) return e;
+  k_quant_cols<<<(unsigned)grid, 256, kQcSmem, st>>>(a);
   note_launch();
   return cudaGetLastError();
 }

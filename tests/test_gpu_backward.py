@@ -12,6 +12,7 @@ import torch
 import inputs
 import quantized_grouped_gemm_topk_gb300 as m
 from oracle import backward as B
+from oracle import formats as F
 from oracle import moe as M
 
 from gpu_harness import LazyExperts, oracle_forward, oracle_weights, run_forward
@@ -125,3 +126,36 @@ def test_train_full_size_sampled():
     for e in experts:
         assert_close_layer(np_(dW1[e].float()), b.dW1[e], f"dW1[{e}]")
         assert_close_layer(np_(dW2[e].float()), b.dW2[e], f"dW2[{e}]")
+
+
+@pytest.mark.parametrize("T,E", [(300, 8), (4, 16)])
+def test_train_saved_transposed_x_bit_exact(T, E):
+    """The transposed MXFP8 copy of the gathered x rows that the training
+    forward saves (at_q, at_s) against the oracle's MXFP8 quantisation of
+    each expert's rows, zero-padded to a multiple of 128 rows, along the row
+    axis: codes and scales byte for byte. H = 2880 spans eleven full
+    256-column tiles and a 64-column tail; T = 300 gives experts of several
+    32-row blocks with ragged ends, T = 4 empty experts."""
+    dev = cuda_device()
+    s = inputs.workload("train", T=T, E=E)
+    r = run_forward(s, T, dev=dev, save=True)
+    assert r["status"] == 0
+    f = oracle_forward(s, r)
+    offs = f.disp.offsets
+    cnt = np.diff(offs)
+    poff = np.concatenate([[0], np.cumsum((cnt + 127) // 128 * 128)])
+    bufs = r["save_bufs"]
+    assert np.array_equal(np_(bufs["poff"])[: len(poff)], poff)
+    xv = F.bf16_to_f64(inputs.bf16_bits(r["x"]).cpu().numpy())
+    at_q = np_(bufs["at_q"])
+    rp = bufs["r_pad"]
+    at_s = np_(bufs["at_s"]).reshape(rp // 128, s.H, 4).transpose(1, 0, 2).reshape(s.H, rp // 32)
+    for e in range(len(cnt)):
+        n = poff[e + 1] - poff[e]
+        if n == 0:
+            continue
+        rows = np.zeros((n, s.H))
+        rows[: cnt[e]] = xv[f.disp.perm_src[offs[e]: offs[e + 1]] // s.kp]
+        q, sc = F.mx_quantize(rows.T)
+        assert np.array_equal(at_q[:, poff[e]: poff[e + 1]], q), f"at_q of expert {e}"
+        assert np.array_equal(at_s[:, poff[e] // 32: poff[e + 1] // 32], sc), f"at_s of expert {e}"
