@@ -120,6 +120,99 @@ __global__ void __launch_bounds__(256) k_router_partial(const uint16_t* __restri
   }
 }
 
+// S1 at large T (the tiles alone fill the SMs; no split of H): one CTA per
+// 64 tokens x 128 experts, thread (tx = tid % 16, ty = tid / 16) owns tokens
+// 4ty..4ty+3 and experts 4tx..4tx+3 and 64+4tx..64+4tx+3, so three 16-byte
+// shared loads feed 32 FMAs. Both operands are staged per 16 rows of H in a
+// double-buffered shared tile (x converted to fp32 and transposed to
+// [h][token]); the next stage's global loads are in registers while the
+// current one is multiplied. Each logit is the fmaf chain over h in
+// increasing order, the same chain k_router_partial forms with one slice.
+constexpr int kRbTT = 64, kRbTE = 128, kRbKH = 16;
+
+static bool router_big(int T, int H, int E) {
+  return H % kRbKH == 0 && E % 4 == 0 &&
+         (int64_t)((T + kRbTT - 1) / kRbTT) * ((E + kRbTE - 1) / kRbTE) >= device_sms();
+}
+
+__global__ void __launch_bounds__(256) k_router_big(const uint16_t* __restrict__ x, const float* __restrict__ Wr,
+                                                    int T, int H, int E, float* __restrict__ logits) {
+  pdl_enter();
+  __shared__ __align__(16) float xs[2][kRbKH][kRbTT];
+  __shared__ __align__(16) float ws[2][kRbKH][kRbTE];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int t0 = blockIdx.x * kRbTT, e0 = blockIdx.y * kRbTE;
+  // x stage: 64 tokens x 16 h, one 8-value chunk per thread < 128 (token
+  // tid % 64, h half tid / 64); W stage: 16 h x 128 experts, two float4 per
+  // thread (rows tid / 32 and 8 + tid / 32, experts 4 (tid % 32)..)
+  const int xt = tid & 63, xh = (tid >> 6) & 1;
+  const bool xok = tid < 128 && t0 + xt < T;
+  const uint16_t* xp = x + (int64_t)(xok ? t0 + xt : 0) * H + xh * 8;
+  const int we = e0 + (tid & 31) * 4;
+  const bool wok = we < E;
+  const float* wp = Wr + (int64_t)(tid >> 5) * E + (wok ? we : 0);
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  uint4 xr = make_uint4(0u, 0u, 0u, 0u);
+  float4 wr0 = z4, wr1 = z4;
+  auto gload = [&](int hb) {
+    if (xok) xr = __ldg(reinterpret_cast<const uint4*>(xp + hb));
+    if (wok) {
+      wr0 = __ldg(reinterpret_cast<const float4*>(wp + (int64_t)hb * E));
+      wr1 = __ldg(reinterpret_cast<const float4*>(wp + (int64_t)(hb + 8) * E));
+    }
+  };
+  auto sstore = [&](int b) {
+    if (tid < 128) {
+      float* d = &xs[b][xh * 8][xt];
+      const uint32_t v[4] = {xr.x, xr.y, xr.z, xr.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        d[(2 * q) * kRbTT] = __uint_as_float(v[q] << 16);
+        d[(2 * q + 1) * kRbTT] = __uint_as_float(v[q] & 0xffff0000u);
+      }
+    }
+    *reinterpret_cast<float4*>(&ws[b][tid >> 5][(tid & 31) * 4]) = wr0;
+    *reinterpret_cast<float4*>(&ws[b][8 + (tid >> 5)][(tid & 31) * 4]) = wr1;
+  };
+  float acc[4][8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  gload(0);
+  sstore(0);
+  __syncthreads();
+  const int nk = H / kRbKH;
+  for (int kb = 0; kb < nk; ++kb) {
+    const int b = kb & 1;
+    if (kb + 1 < nk) gload((kb + 1) * kRbKH);
+#pragma unroll
+    for (int hh = 0; hh < kRbKH; ++hh) {
+      const float4 a = *reinterpret_cast<const float4*>(&xs[b][hh][ty * 4]);
+      const float4 w0 = *reinterpret_cast<const float4*>(&ws[b][hh][tx * 4]);
+      const float4 w1 = *reinterpret_cast<const float4*>(&ws[b][hh][64 + tx * 4]);
+      const float av[4] = {a.x, a.y, a.z, a.w};
+      const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], wv[j], acc[i][j]);
+    }
+    if (kb + 1 < nk) sstore(b ^ 1);          // the buffer read one stage ago
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+    float* row = logits + (int64_t)t * E;
+    if (e0 + tx * 4 < E)
+      *reinterpret_cast<float4*>(row + e0 + tx * 4) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    if (e0 + 64 + tx * 4 < E)
+      *reinterpret_cast<float4*>(row + e0 + 64 + tx * 4) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+  }
+}
+
 // Sum over ks of part[ks * n + i], in ks order, with 8 loads in flight.
 __device__ __forceinline__ float sum_partials(const float* __restrict__ part, int KS, int64_t n, int64_t i) {
   float v = 0.f;
@@ -557,6 +650,7 @@ static int router_tile(int T) { return T <= 16 ? 16 : 32; }
 // H slices: about two CTAs per SM, each slice >= 128 rows (two W tiles), and
 // at most 4096 partial rows (KS * T) to sum afterwards.
 int router_splits(int T, int H, int E) {
+  if (router_big(T, H, E)) return 1;
   const int tiles = ((T + router_tile(T) - 1) / router_tile(T)) * ((E + 63) / 64);
   int ks = (2 * device_sms() + tiles - 1) / std::max(tiles, 1);
   ks = std::max(1, std::min(ks, std::max(1, H / 128)));
@@ -567,6 +661,12 @@ int router_splits(int T, int H, int E) {
 cudaError_t launch_router(const uint16_t* x, const float* Wr, int T, int H, int E, int KS, float* part,
                           cudaStream_t st) {
   if (T == 0) return cudaSuccess;
+  if (KS == 1 && router_big(T, H, E)) {
+    cudaError_t e = launch_pdl(k_router_big, dim3((T + kRbTT - 1) / kRbTT, (E + kRbTE - 1) / kRbTE), dim3(256), 0,
+                               st, x, Wr, T, H, E, part);
+    note_launch();
+    return e;
+  }
   const int tt = router_tile(T);
   dim3 grid((T + tt - 1) / tt, (E + 63) / 64, KS);
   cudaError_t e = tt == 16 ? launch_pdl(k_router_partial<16>, grid, dim3(256), 0, st, x, Wr, T, H, E, KS, part)

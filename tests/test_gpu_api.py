@@ -6,6 +6,7 @@ import torch
 
 import inputs
 import quantized_grouped_gemm_topk_gb300 as m
+from oracle import moe as M
 
 from gpu_harness import oracle_forward, run_forward, weights_for
 from util import assert_close_layer, cuda_device, np_
@@ -324,3 +325,22 @@ def test_flag_wait_times_out_and_context_survives():
     torch.cuda.synchronize()
     assert m.moe_read_status(cfg, ws) == 0
     assert torch.equal(out2, r["out"])
+
+
+def test_router_logits_large_batch():
+    """Router logits at a batch whose 64-token x 128-expert tiles fill the
+    SMs (the large-batch logits kernel, no split of H), ragged in tokens
+    (T % 64 = 36) and in experts (E = 200: the second expert tile is partly
+    empty), against the fp64 product of the same bf16 x and fp32 W_r."""
+    dev = cuda_device()
+    s = inputs.workload("tiny", T=4900, H=512, E=200)
+    T = s.T
+    cfg = m.make_config(s.H, s.I, s.E, s.k, T_max=T)
+    x = inputs.gen_x(s, 5, device=dev)
+    Wr = inputs.gen_router(s, 5, device=dev)
+    ws = torch.zeros(m.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    logits = torch.full((T, s.E), float("nan"), dtype=torch.float32, device=dev)
+    m.moe_router_logits(cfg, x, Wr, T, logits, ws)
+    torch.cuda.synchronize()
+    ref = M.router_logits(np_(x.float()), np_(Wr))
+    np.testing.assert_allclose(np_(logits), ref, rtol=1e-4, atol=1e-5)
