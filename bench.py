@@ -479,6 +479,52 @@ class DecodeBench:
         torch.cuda.empty_cache()
 
 
+PARTITION_SMS = (0, 4, 8, 16, 20)
+
+
+def partition_ablation(m, b, K, warmup, flush, nds=PARTITION_SMS):
+    """The partitioned fused layer against the unpartitioned one, on the
+    headline's weights and batches: per T where the layer is fused, the
+    median plain-graph layer time with the W1 operand gather as a launch of
+    its own (0) or done by nd ring CTAs of the fused W1 -> W2 kernel, which
+    raise per-group ring flags the GEMM CTAs acquire."""
+    Ts = [T for T in b.Ts if b.fused[T]]
+    per = {str(T): [] for T in Ts}
+    for nd in nds:
+        cfg = m.config_from_shape(b.s, T_max=max(b.Ts), dispatch_sms=nd)
+        graphs = {}
+        for T in Ts:
+            for i in range(b.nx):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    m.moe_layer_forward(cfg, b.xs[T][i], b.Wr, None, T, b.packed, b.outs[T], None, b.ws)
+                graphs[(T, i)] = g
+        for w in range(warmup):
+            for T in Ts:
+                flush.zero_()
+                graphs[(T, w % b.nx)].replay()
+        torch.cuda.synchronize()
+        us = {T: [] for T in Ts}
+        for step in range(K):
+            i = step % b.nx
+            for T in Ts:
+                flush.zero_()
+                b.ev_a[T][i].record()
+                graphs[(T, i)].replay()
+                b.ev_b[T][i].record()
+            torch.cuda.synchronize()
+            for T in Ts:
+                us[T].append(b.ev_a[T][i].elapsed_time(b.ev_b[T][i]) * 1e3)
+        assert m.moe_read_status(cfg, b.ws) == 0
+        for T in Ts:
+            per[str(T)].append(statistics.median(us[T]))
+        del graphs
+    return {"workload": b.s.name, "dispatch_sms": list(nds), "per_T_layer_us": per,
+            "note": "0: the W1 operand rows are gathered by a launch of their own before the fused W1 -> W2 "
+                    "kernel; nd > 0: nd of the kernel's CTAs (one per SM) gather them group by group and raise "
+                    "per-group ring flags that the other CTAs acquire before reading a group's rows"}
+
+
 def bench_shared_decode(m, dev, K, warmup, flush, hbm):
     s = inputs.workload("shared")
     b = DecodeBench(m, s, SHARED_TS, dev, 0)
@@ -657,6 +703,10 @@ def run_only(args, local):
         res = bench_mxfp4_decode(m, dev, args.steps, args.warmup, flush, hbm)
     elif args.only == "skewed":
         res = bench_skewed(m, dev, args.steps, args.warmup, flush, hbm, bf16)
+    elif args.only == "partition":
+        b = DecodeBench(m, inputs.workload("dsv3"), [T for T in DECODE_TS if T <= 32], dev, 0)
+        res = partition_ablation(m, b, args.steps, args.warmup, flush)
+        b.free()
     else:
         res = bench_train(m, dev, args.steps, args.warmup, bf16, args.train_T, args.train_E)
     print(json.dumps(res), flush=True)
@@ -740,10 +790,12 @@ def run_ours(args, s, rank, world, local):
         "clocks": clocks,
         "wall_ms_per_step": wall_ms,
     }
+    ablation = None if args.no_per_config else partition_ablation(m, bench, min(K, 50), args.warmup, flush)
     bench.free()
     del bench
     if not args.no_per_config:
         pc = {}
+        pc["partition_ablation"] = ablation
         pc["shared_decode"] = bench_shared_decode(m, dev, min(K, 50), args.warmup, flush, hbm)
         pc["mxfp4_decode"] = bench_mxfp4_decode(m, dev, min(K, 50), args.warmup, flush, hbm)
         pc["skewed_prefill"] = bench_skewed(m, dev, min(K, 20), args.warmup, flush, hbm, bf16)
@@ -777,7 +829,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="headline workload only")
     ap.add_argument("--E", type=int, default=0, help="override the expert count (small profiling cases)")
-    ap.add_argument("--only", default="", choices=["", "shared", "mxfp4", "skewed", "train"],
+    ap.add_argument("--only", default="", choices=["", "shared", "mxfp4", "skewed", "train", "partition"],
                     help="run one workload of the per-config block alone (profiling)")
     ap.add_argument("--train-T", type=int, default=0, help="training tokens for --only train")
     ap.add_argument("--train-E", type=int, default=0, help="training experts for --only train")

@@ -128,6 +128,22 @@ typedef struct moe_config {
                            * up c) added before the activation, forward only
                            * (the NVIDIA blog's SwiGLU(xW + b, xV + c) and its
                            * fused bias-vector epilogue, kernel families) */
+    int32_t dispatch_sms; /* 0..64. Where moe_layer_fused holds and > 0 (it
+                           * must be below the kernel's CTA count), the
+                           * layer runs partitioned: that many CTAs (one per
+                           * SM) of the fused W1 -> W2 kernel fill the token
+                           * ring (the gathered W1 operand rows) group by
+                           * group and raise a per-group ring flag; the
+                           * other CTAs run W1 -> W2, each waiting (bounded;
+                           * MOE_DEV_TIMEOUT) for a group's flag before it
+                           * reads the group's rows. 0: the rows are
+                           * gathered by a launch of their own first.
+                           * Results are the same bits either way. Source:
+                           * GC-MoE summary, Approach (a small dispatch
+                           * partition fills the token ring and publishes
+                           * its counter, the compute partition acquires
+                           * ring blocks) and Limitations (the partition
+                           * size was not ablated). */
 } moe_config_t;
 
 /* Unpacked expert weights (device pointers), one entry per group e < G, in

@@ -52,7 +52,8 @@ class moe_config_t(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("n_shared", ctypes.c_int32), ("T_max", ctypes.c_int32), ("act", ctypes.c_int32),
                 ("act_alpha", ctypes.c_float), ("act_limit", ctypes.c_float), ("routed_scale", ctypes.c_float),
-                ("weight_fmt", ctypes.c_int32), ("max_sms", ctypes.c_int32), ("w1_bias", ctypes.c_int32)]
+                ("weight_fmt", ctypes.c_int32), ("max_sms", ctypes.c_int32), ("w1_bias", ctypes.c_int32),
+                ("dispatch_sms", ctypes.c_int32)]
 
 
 class moe_weights_view_t(ctypes.Structure):
@@ -152,17 +153,17 @@ def _require_cuda():
 
 
 def make_config(H, I, E, k, n_shared=0, T_max=0, act="swiglu", alpha=1.0, limit=0.0, routed_scale=1.0,
-                wfmt="nvfp4", max_sms=0, bias=False) -> moe_config_t:
+                wfmt="nvfp4", max_sms=0, bias=False, dispatch_sms=0) -> moe_config_t:
     return moe_config_t(H, I, E, k, n_shared, T_max,
                         ACTS[act],
                         float(alpha), float(limit), float(routed_scale),
-                        WFMTS[wfmt], max_sms, 1 if bias else 0)
+                        WFMTS[wfmt], max_sms, 1 if bias else 0, dispatch_sms)
 
 
-def config_from_shape(s, T_max=None, max_sms=0) -> moe_config_t:
+def config_from_shape(s, T_max=None, max_sms=0, dispatch_sms=0) -> moe_config_t:
     """moe_config_t from an object with the fields of inputs.MoEShape."""
     return make_config(s.H, s.I, s.E, s.k, s.n_shared, s.T if T_max is None else T_max, s.act, s.alpha,
-                       s.limit, s.routed_scale, s.wfmt, max_sms, getattr(s, "bias", False))
+                       s.limit, s.routed_scale, s.wfmt, max_sms, getattr(s, "bias", False), dispatch_sms)
 
 
 # ---- sizes / views (host only) -----------------------------------------------

@@ -246,6 +246,7 @@ moe_status_t moe_config_validate(const moe_config_t* c) {
   if (!(c->routed_scale > 0.f)) return MOE_ERR_INVALID_ARG;
   if (c->max_sms < 0) return MOE_ERR_INVALID_ARG;
   if (c->w1_bias != 0 && c->w1_bias != 1) return MOE_ERR_INVALID_ARG;
+  if (c->dispatch_sms < 0 || c->dispatch_sms > 64) return MOE_ERR_INVALID_ARG;
   if (c->w1_bias && c->act == MOE_ACT_SRELU) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
@@ -406,6 +407,7 @@ static RouteArgs route_args(const moe_config_t* c, int T, const moe_dispatch_t* 
   a.perm = d->perm_src; a.inv = d->inv; a.w_row = d->w_row;
   a.x = nullptr; a.xq = d->xq; a.xs = d->xs;
   a.status = at<int32_t>(ws, L.status);
+  a.zero = nullptr; a.nzero = 0;
   return a;
 }
 
@@ -623,7 +625,7 @@ static ActParams act_params(const moe_config_t* c) {
 // must be zero: the operand gather clears them). y1 (MXFP8) lands in y1q /
 // y1s; W2's fp32 K-slice partials in run2.
 static moe_status_t tc_fused(const moe_config_t* c, const moe_dispatch_t* d, int T, const void* packed, uint8_t* y1q,
-                             uint8_t* y1s, void* ws, cudaStream_t st, TcRun* run2) {
+                             uint8_t* y1s, void* ws, cudaStream_t st, TcRun* run2, int n_disp) {
   const WsLayout L = ws_layout(*c);
   const PackLayout P = pack_layout(*c, MOE_PACK_FORWARD);
   TcArgs g;
@@ -643,6 +645,12 @@ static moe_status_t tc_fused(const moe_config_t* c, const moe_dispatch_t* d, int
   g.f.y_rowexp = at<int32_t>(ws, L.rexp2);
   g.f.cnt = at<int32_t>(ws, L.fcnt);
   g.f.b1 = P.off_b1 ? reinterpret_cast<const float*>(reinterpret_cast<const uint8_t*>(packed) + P.off_b1) : nullptr;
+  // partitioned layer: the first n_disp CTAs gather the W1 operand rows
+  if (n_disp >= g.max_ctas) return MOE_ERR_INVALID_ARG;
+  g.f.n_disp = n_disp;
+  g.f.xq = d->xq; g.f.xs = d->xs;
+  g.f.row_map = d->perm_src; g.f.row_div = c->k + c->n_shared;
+  g.f.a16 = at<uint16_t>(ws, L.a16); g.f.a_rowexp = at<int32_t>(ws, L.rexp1);
   const int64_t R = (int64_t)T * (c->k + c->n_shared);
   TcMaps maps;
   if (!make_tmaps_b(maps.m[0], at<uint16_t>(ws, L.a16), R, g.m[0].K) ||
@@ -811,6 +819,14 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
   RouteArgs a = route_args(c, T, &v.d, ws, L);
   a.x = x;
   a.logits = v.logits;
+  // partitioned fused layer: the routing kernel clears the hand-off
+  // counters and ring flags; the fused kernel gathers the W1 operand rows
+  const int n_disp = T > 0 && fused_layer(*c, T) && !save ? c->dispatch_sms : 0;
+  if (n_disp > 0 && n_disp >= mx_grid(*c)) return MOE_ERR_INVALID_ARG;   // no GEMM CTA would be left
+  if (n_disp > 0) {
+    a.zero = at<int32_t>(ws, L.fcnt);
+    a.nzero = tc_fused_counters(G);
+  }
   phase(0, st);
   if (W_r) {
     const int KS = router_splits(T, c->H, c->E);
@@ -835,7 +851,9 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
     if (mx_path(*c))
       MOE_CHECK_CUDA(launch_gather_mx(v.d.xq, v.d.xs, c->H, v.d.perm_src, kp, T * kp, v.d.offsets, G,
                                       at<uint8_t>(ws, L.xg), at<uint8_t>(ws, L.xgs), st));
-    else if (fused_layer(*c, T) && !save)
+    else if (n_disp > 0) {
+      // the fused kernel's ring CTAs gather the rows
+    } else if (fused_layer(*c, T) && !save)
       MOE_CHECK_CUDA(launch_act_f16(v.d.xq, v.d.xs, c->H, v.d.perm_src, kp, T * kp, v.d.offsets, G,
                                     at<uint16_t>(ws, L.a16), at<int32_t>(ws, L.rexp1), st, at<int32_t>(ws, L.fcnt),
                                     tc_fused_counters(G)));
@@ -858,7 +876,7 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
   }
   if (fused_layer(*c, T) && !save) {
     TcRun run;
-    if ((s = tc_fused(c, &v.d, T, packed_w, v.y1_q, v.y1_s, ws, st, &run)) != MOE_OK) return s;
+    if ((s = tc_fused(c, &v.d, T, packed_w, v.y1_q, v.y1_s, ws, st, &run, n_disp)) != MOE_OK) return s;
     phase(2, st);
     phase(3, st);
     phase(4, st);

@@ -114,10 +114,9 @@ struct UnitIt {
 };
 struct UnitStep {
   uint32_t dti, dj, ds, tiles, S;
-  __device__ void init(int tiles_, int S_) {
+  __device__ void init(int tiles_, int S_, uint32_t step) {
     tiles = (uint32_t)tiles_;
     S = (uint32_t)S_;
-    const uint32_t step = gridDim.x;
     ds = step % S;
     dj = (step / S) % tiles;
     dti = step / (S * tiles);
@@ -134,24 +133,27 @@ struct UnitStep {
   }
 };
 
-// A CTA's walk over the units: u = blockIdx.x, blockIdx.x + gridDim.x, ...
-// through matrix 0's n_groups * tiles * S units and, in the fused layer, on
-// through matrix 1's; every role visits the same sequence. Kept in shared
-// memory (set once per CTA): the role loops then hold only their iterator
-// in registers.
+// A CTA's walk over the units: u = cta, cta + ncta, ... (cta: the CTA's
+// index among the ncta GEMM CTAs) through matrix 0's n_groups * tiles * S
+// units and, in the fused layer, on through matrix 1's; every role visits
+// the same sequence. Kept in shared memory (set once per CTA): the role loops
+// then hold only their iterator in registers.
 struct UnitWalk {
   UnitStep st0, st1;
   uint32_t n_groups, u0;   // u0: units of matrix 0
+  uint32_t cta, ncta;
   int nmat;
-  __device__ void init(const TcArgs& g, uint32_t ng) {
-    st0.init(g.m[0].tiles, g.m[0].S);
-    st1.init(g.m[g.nmat - 1].tiles, g.m[g.nmat - 1].S);
+  __device__ void init(const TcArgs& g, uint32_t ng, uint32_t cta_, uint32_t ncta_) {
+    cta = cta_;
+    ncta = ncta_;
+    st0.init(g.m[0].tiles, g.m[0].S, ncta);
+    st1.init(g.m[g.nmat - 1].tiles, g.m[g.nmat - 1].S, ncta);
     n_groups = ng;
     u0 = ng * (uint32_t)g.m[0].tiles * (uint32_t)g.m[0].S;
     nmat = g.nmat;
   }
   __device__ UnitIt first() const {
-    UnitIt it = st0.at(blockIdx.x, 0);
+    UnitIt it = st0.at(cta, 0);
     if (it.ti >= n_groups) to_second(it);
     return it;
   }
@@ -165,11 +167,10 @@ struct UnitWalk {
     }
   }
   // the first unit of matrix 1 on this CTA's stride: the smallest u >= u0
-  // with u = blockIdx.x (mod gridDim.x), as an index into matrix 1's units
+  // with u = cta (mod ncta), as an index into matrix 1's units
   __device__ void to_second(UnitIt& it) const {
     if (nmat < 2) return;
-    const uint32_t G = gridDim.x;
-    it = st1.at((blockIdx.x + G - u0 % G) % G, 1);
+    it = st1.at((cta + ncta - u0 % ncta) % ncta, 1);
   }
 };
 
@@ -366,6 +367,67 @@ __device__ __forceinline__ int box_index(int nv) {
   return nv <= 8 ? 0 : nv <= 16 ? 1 : nv <= 32 ? 2 : nv <= 64 ? 3 : 4;
 }
 
+// ---------------------------------------------------------------------------
+// f16 activation rows for the B operand.
+// a16[r][k] = E4M3 value * 2^(block exponent - row exponent), rowexp[r] =
+// the largest block exponent of the row (unbiased), so the product of the
+// two is the MXFP8 value exactly unless a block sits more than 15 binades
+// below the row's largest block (then bits below 2^-24 of the row scale are
+// rounded away). One warp per (row, 256-column slice); every warp derives the
+// row exponent from the row's scale bytes itself.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void act_f16_item(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int C,
+                                             const int32_t* __restrict__ row_map, int row_div, int64_t r, int sl,
+                                             uint16_t* __restrict__ a16, int32_t* __restrict__ rowexp, int lane) {
+  const int nb = C / 32;
+  const int64_t src = row_map ? (int64_t)(row_map[r] / row_div) : r;
+  const uint8_t* sr = s + src * nb;
+  int mx = 0;
+  for (int b = lane; b < nb; b += 32) mx = max(mx, (int)sr[b]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(kFull, mx, o));
+  if (sl == 0 && lane == 0) rowexp[r] = mx - 127;
+  const int c0 = sl * 256 + lane * 8;
+  if (c0 < C) {
+    const uint2 codes = *reinterpret_cast<const uint2*>(q + src * C + c0);
+    const float f = ldexpf(1.0f, (int)sr[c0 / 32] - mx);
+    uint32_t outw[4];
+    const uint32_t cw[2] = {codes.x, codes.y};
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const float2 lo = e4m3x2_to_f32x2((uint16_t)(cw[i] & 0xffffu));
+      const float2 hi = e4m3x2_to_f32x2((uint16_t)(cw[i] >> 16));
+      const __half2 h0 = __floats2half2_rn(lo.x * f, lo.y * f);
+      const __half2 h1 = __floats2half2_rn(hi.x * f, hi.y * f);
+      outw[2 * i] = *reinterpret_cast<const uint32_t*>(&h0);
+      outw[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&h1);
+    }
+    *reinterpret_cast<uint4*>(a16 + r * C + c0) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+  }
+}
+
+// The partitioned layer's ring CTAs (n_disp of them): CTA d fills the W1
+// operand rows of the touched groups d, d + n_disp, ... (the order the GEMM
+// CTAs' walk needs them), all its warps on one group at a time, then raises
+// the group's ring flag with a release store behind the CTA barrier.
+__device__ void fill_ring(const TcArgs& g) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int C = g.m[0].K;
+  const int nsl = (C + 255) / 256;
+  const int ntouch = *g.n_touched;
+  int32_t* ring = g.f.cnt + 2 * g.G;
+  for (int ti = blockIdx.x; ti < ntouch; ti += g.f.n_disp) {
+    const int e = g.touched[ti];
+    const int r0 = g.offsets[e];
+    const int64_t items = (int64_t)(g.offsets[e + 1] - r0) * nsl;
+    for (int64_t wi = warp; wi < items; wi += nw)
+      act_f16_item(g.f.xq, g.f.xs, C, g.f.row_map, g.f.row_div, r0 + wi / nsl, (int)(wi % nsl), g.f.a16,
+                   g.f.a_rowexp, lane);
+    __syncthreads();
+    if (threadIdx.x == 0) st_release_gpu(ring + e, 1);
+  }
+}
+
 template <int NT>
 __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant__ TcArgs g,
                                                            const __grid_constant__ TcMaps maps) {
@@ -399,6 +461,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
   }
   __syncthreads();
   if (bad_pack) return;   // the blob is not the packing this GEMM reads: write nothing
+  // partitioned layer: the first n_disp CTAs fill the token ring and leave
+  int n_disp = 0;
+  if constexpr (NT == 16) {
+    if (g.nmat == 2) n_disp = g.f.n_disp;
+    if ((int)blockIdx.x < n_disp) {
+      fill_ring(g);
+      return;
+    }
+  }
   __shared__ int vgroups;   // entries of the walk's group axis
   {
     // The walk's groups: each touched group or, with split_rows > 0, each
@@ -482,7 +553,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
       tc::mbar_init(&dfree[i], 4);     // one elected arrive per epilogue warp
     }
     tc::mbar_init(drain, C::P);     // one commit from each MMA issuer
-    walk.init(g, (uint32_t)vgroups);   // groups with rows (or their row blocks)
+    // groups with rows (or their row blocks), over the GEMM CTAs
+    walk.init(g, (uint32_t)vgroups, blockIdx.x - (uint32_t)n_disp, gridDim.x - (uint32_t)n_disp);
     *abort = 0;
     tc::fence_mbar_init();
   }
@@ -539,12 +611,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
         for (int i = 0; i < kTcBoxes; ++i) tc::prefetch_tmap(&maps.m[m][i]);
       const uint64_t pol_a = tc::policy_evict_last();
       const int32_t* ready = g.f.cnt + g.G;
+      const int32_t* ring = g.f.cnt + 2 * g.G;
       uint32_t ait = 0;
-      int ready_e = -1;
+      int ready_e = -1, ring_e = -1;
       bool ok = true;
       for (UnitIt it = walk.first(); ok && walk.more(it); walk.next(it)) {
         TcUnit w;
         if (!tc_unit(g, tab, it, w)) continue;
+        if (it.mat == 0 && n_disp > 0 && w.e != ring_e) {
+          // partitioned layer: the group's W1 operand rows come from a ring CTA
+          if (!wait_flag(ring + w.e, abort)) { ok = false; break; }
+          fence_proxy_async_global();
+          ring_e = w.e;
+        }
         if (it.mat == 1 && w.e != ready_e) {
           // fused layer: the group's W2 operand rows are written by the CTA
           // that finished its last W1 tile; the copies below read them
@@ -671,13 +750,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
     const int p = q * 32 + lane;
     const uint32_t lane_base = tmem + ((uint32_t)(q * 32) << 16);
     const int32_t* ready = g.f.cnt + g.G;
-    int ready_e = -1;
+    const int32_t* ring = g.f.cnt + 2 * g.G;
+    int ready_e = -1, ring_e = -1;
     uint32_t dit = 0, ait = 0;
     bool ok = true;
     for (UnitIt it = walk.first(); ok && walk.more(it); walk.next(it)) {
       TcUnit w;
       if (!tc_unit(g, tab, it, w)) continue;
       const TcMat& M = g.m[it.mat];
+      if (it.mat == 0 && n_disp > 0 && w.e != ring_e) {
+        // partitioned layer: the row exponents of the group's W1 operand
+        // rows come from a ring CTA
+        if (!wait_flag(ring + w.e, abort)) { ok = false; break; }
+        ring_e = w.e;
+      }
       if (it.mat == 1 && w.e != ready_e) {
         // fused layer: the row exponents of the group's W2 operand come from
         // another CTA (already published: the MMAs consumed those rows)
@@ -855,15 +941,6 @@ cudaError_t launch_gemm_tc(const TcArgs& g, const TcMaps& maps, int nt, cudaStre
   return e;
 }
 
-// ---------------------------------------------------------------------------
-// f16 activation rows for the B operand.
-// a16[r][k] = E4M3 value * 2^(block exponent - row exponent), rowexp[r] =
-// the largest block exponent of the row (unbiased), so the product of the
-// two is the MXFP8 value exactly unless a block sits more than 15 binades
-// below the row's largest block (then bits below 2^-24 of the row scale are
-// rounded away). One warp per (row, 256-column slice); every warp derives the
-// row exponent from the row's scale bytes itself.
-// ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_act_f16(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int C,
                                                  const int32_t* __restrict__ row_map, int row_div, int R,
                                                  const int32_t* __restrict__ offsets, int G, uint16_t* __restrict__ a16,
@@ -875,37 +952,10 @@ __global__ void __launch_bounds__(256) k_act_f16(const uint8_t* __restrict__ q, 
   const int lane = threadIdx.x & 31;
   const int Rv = min(R, offsets[G]);
   const int nsl = (C + 255) / 256;
-  const int nb = C / 32;
   const int64_t total = (int64_t)Rv * nsl;
   const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
-  for (int64_t wi = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); wi < total; wi += nw) {
-    const int64_t r = wi / nsl;
-    const int sl = (int)(wi % nsl);
-    const int64_t src = row_map ? (int64_t)(row_map[r] / row_div) : r;
-    const uint8_t* sr = s + src * nb;
-    int mx = 0;
-    for (int b = lane; b < nb; b += 32) mx = max(mx, (int)sr[b]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(kFull, mx, o));
-    if (sl == 0 && lane == 0) rowexp[r] = mx - 127;
-    const int c0 = sl * 256 + lane * 8;
-    if (c0 < C) {
-      const uint2 codes = *reinterpret_cast<const uint2*>(q + src * C + c0);
-      const float f = ldexpf(1.0f, (int)sr[c0 / 32] - mx);
-      uint32_t outw[4];
-      const uint32_t cw[2] = {codes.x, codes.y};
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const float2 lo = e4m3x2_to_f32x2((uint16_t)(cw[i] & 0xffffu));
-        const float2 hi = e4m3x2_to_f32x2((uint16_t)(cw[i] >> 16));
-        const __half2 h0 = __floats2half2_rn(lo.x * f, lo.y * f);
-        const __half2 h1 = __floats2half2_rn(hi.x * f, hi.y * f);
-        outw[2 * i] = *reinterpret_cast<const uint32_t*>(&h0);
-        outw[2 * i + 1] = *reinterpret_cast<const uint32_t*>(&h1);
-      }
-      *reinterpret_cast<uint4*>(a16 + r * C + c0) = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-    }
-  }
+  for (int64_t wi = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); wi < total; wi += nw)
+    act_f16_item(q, s, C, row_map, row_div, wi / nsl, (int)(wi % nsl), a16, rowexp, lane);
 }
 
 // The fused layer's flag wait on its own: one thread waits (bounded by

@@ -89,6 +89,8 @@ struct RouteArgs {
   const uint16_t* x;          // nullable: skip quantisation
   uint8_t *xq, *xs;
   int32_t* status;
+  int32_t* zero;              // nullable: [nzero] ints cleared by the routing kernel
+  int64_t nzero;              // (the partitioned layer's hand-off counters)
 };
 
 int router_splits(int T, int H, int E);
@@ -137,8 +139,17 @@ struct TcFused {
   uint8_t* y1q; uint8_t* y1s; // [R][I], [R][I / 32]
   uint16_t* y16;              // [R][I]
   int32_t* y_rowexp;          // [R]
-  int32_t* cnt;               // [G] W1 tiles done, [G] ready flags; zero on entry
+  int32_t* cnt;               // [G] W1 tiles done, [G] ready flags, [G] ring flags; zero on entry
   const float* b1;            // [G][2I] W1 bias (gate then up), nullable
+  // Partitioned layer: CTAs [0, n_disp) fill the token ring (the f16 W1
+  // operand rows a16 and their exponents, gathered from the dispatched MXFP8
+  // rows xq / xs by row_map / row_div) group by group and raise the group's
+  // ring flag; the other CTAs run W1 -> W2. n_disp = 0: a16 is filled before
+  // the launch.
+  int n_disp;
+  const uint8_t* xq; const uint8_t* xs;
+  const int32_t* row_map; int row_div;
+  uint16_t* a16; int32_t* a_rowexp;
 };
 struct TcArgs {
   TcMat m[2];                 // m[0]: the (first) matrix; m[1]: W2 of the fused layer
@@ -159,7 +170,7 @@ struct TcArgs {
 // I / 256 code words of a row in registers).
 constexpr int kFusedMaxI = 2048;
 // Ints of the fused layer's counters for G groups.
-inline int64_t tc_fused_counters(int G) { return 2LL * G; }
+inline int64_t tc_fused_counters(int G) { return 3LL * G; }
 constexpr int kTcBoxes = 5;   // activation boxes of 8, 16, 32, 64, 128 rows
 // Tensor maps of the f16 operand rows a16 [rows, cols], viewed as
 // (64 columns, rows, cols / 64 chunks): m[i] loads a box of 8 << i rows of

@@ -444,8 +444,10 @@ __device__ void scan_groups(const int32_t* hist, int NB, int G, int32_t* counts,
 
 __global__ void __launch_bounds__(1024) k_scan(const int32_t* __restrict__ hist, int NB, int G,
                                                int32_t* counts, int32_t* offsets, int32_t* base,
-                                               int32_t* touched, int32_t* n_touched, int32_t* poff) {
+                                               int32_t* touched, int32_t* n_touched, int32_t* poff,
+                                               int32_t* zero, int64_t nzero) {
   extern __shared__ int32_t sm[];
+  for (int64_t i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
   scan_groups(hist, NB, G, counts, offsets, base, touched, n_touched, poff, sm);
 }
 
@@ -561,9 +563,12 @@ __global__ void __launch_bounds__(1024) k_route_small(const float* __restrict__ 
                                                       int32_t* touched, int32_t* n_touched, int32_t* poff,
                                                       int32_t* perm, int32_t* inv, float* w_row,
                                                       const uint16_t* __restrict__ x, int H, uint8_t* xq,
-                                                      uint8_t* xs, int32_t* status) {
+                                                      uint8_t* xs, int32_t* status, int32_t* zero,
+                                                      int64_t nzero) {
   extern __shared__ int32_t sm[];
   pdl_enter();
+  if (blockIdx.x == 0)
+    for (int64_t i = threadIdx.x; i < nzero; i += blockDim.x) zero[i] = 0;
   if (blockIdx.x > 0) {
     const int lane = threadIdx.x & 31;
     const int groups = (H + 255) / 256;
@@ -687,7 +692,7 @@ static void launch_small(const RouteArgs& a, int kp, int G, int nq, cudaStream_t
   set_smem_once((const void*)k_route_small<VPL>, 200 * 1024, done);
   launch_pdl(k_route_small<VPL>, dim3(1 + nq), dim3(1024), smem, st, a.part, a.KS, a.T, a.E, a.k, kp, G, a.rs,
              a.route ? 1 : 0, a.logits, a.ids, a.wts, a.counts, a.offsets, a.touched, a.n_touched, a.poff, a.perm,
-             a.inv, a.w_row, a.x, a.H, a.xq, a.xs, a.status);
+             a.inv, a.w_row, a.x, a.H, a.xq, a.xs, a.status, a.zero, a.zero ? a.nzero : 0);
 }
 
 cudaError_t launch_route_dispatch(const RouteArgs& a, cudaStream_t st) {
@@ -710,7 +715,8 @@ cudaError_t launch_route_dispatch(const RouteArgs& a, cudaStream_t st) {
   note_launch();
   size_t smem = (size_t)(3 * (G + 1) + 99) * 4;
   if (smem > 48 * 1024) cudaFuncSetAttribute(k_scan, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  k_scan<<<1, 1024, smem, st>>>(a.hist, NB, G, a.counts, a.offsets, a.base, a.touched, a.n_touched, a.poff);
+  k_scan<<<1, 1024, smem, st>>>(a.hist, NB, G, a.counts, a.offsets, a.base, a.touched, a.n_touched, a.poff,
+                                a.zero, a.zero ? a.nzero : 0);
   note_launch();
   k_scatter<<<NB, 32, G * 4, st>>>(a.ids, a.wts, T, a.k, kp, a.E, G, a.base, a.perm, a.inv, a.w_row);
   note_launch();

@@ -188,3 +188,12 @@ def test_srelu_host_rules(lib):
         m.moe_packed_weights_size(c, m.MOE_PACK_DGRAD)
     assert m.moe_config_validate(_cfg(act="srelu", bias=True)) == 2
     assert not m.moe_layer_fused(_cfg(act="srelu"), 1)
+
+
+def test_dispatch_sms_host_rules(lib):
+    """dispatch_sms (the partitioned fused layer's ring CTAs) is 0..64."""
+    from quantized_grouped_gemm_topk_gb300 import binding as m
+    for nd, want in ((0, 0), (8, 0), (64, 0), (-1, 1), (65, 1)):
+        c = _cfg()
+        c.dispatch_sms = nd
+        assert m.moe_config_validate(c) == want, nd

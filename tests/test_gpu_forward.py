@@ -278,3 +278,32 @@ def test_srelu_forward(case):
     _check_dispatch(s, r, f)
     assert_mx_close(np_(r["views"]["y1_q"]), np_(r["views"]["y1_s"]), f.y1q, f.y1s, "y1")
     assert_close_layer(np_(r["out"].float()), f.out, "out")
+
+
+@pytest.mark.parametrize("name,T,E,nd", [("dsv3", 8, 32, 1), ("dsv3", 8, 32, 12), ("dsv3", 1, 256, 8),
+                                          ("dsv3", 32, 256, 20), ("shared", 16, 160, 8)])
+def test_partitioned_fused_layer(name, T, E, nd):
+    """The partitioned fused layer: nd CTAs of the W1 -> W2 kernel gather the
+    W1 operand rows group by group and raise ring flags that the other CTAs
+    acquire. Its output has the bits of the unpartitioned fused layer (the
+    gather as a launch of its own), on two calls in a row through one
+    workspace (the routing kernel clears the flags and counters each call),
+    and the reduced case matches the oracle."""
+    import quantized_grouped_gemm_topk_gb300 as m
+    dev = cuda_device()
+    s = inputs.workload(name, T=T, E=E)
+    r = run_forward(s, T, dev=dev)
+    assert r["status"] == 0
+    assert m.moe_layer_fused(r["cfg"], T)
+    cfg = m.config_from_shape(s, T_max=T, dispatch_sms=nd)
+    ws = torch.zeros(m.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(r["out"])
+    for _ in range(2):
+        out.fill_(float("nan"))
+        m.moe_layer_forward(cfg, r["x"], r["Wr"], r["logits_in"], T, r["packed"], out, None, ws)
+        torch.cuda.synchronize()
+        assert m.moe_read_status(cfg, ws) == 0
+        assert torch.equal(out, r["out"])
+    if E <= 32:
+        f = oracle_forward(s, r)
+        assert_close_layer(np_(out.float()), f.out, "out")
