@@ -30,7 +30,7 @@ import dataclasses
 import numpy as np
 
 from . import formats as F
-from .moe import Forward, act_bwd, act_fwd, values
+from .moe import Forward, act_bwd, act_fwd, act_plain, act_plain_bwd, gated, values
 
 
 def _q_rows(v, quant):
@@ -58,11 +58,11 @@ def _q_cols(v, quant):
 @dataclasses.dataclass
 class Backward:
     dx: np.ndarray       # fp64 [T, H]
-    dW1: np.ndarray      # fp64 [G, H, 2I]   (logical W1 layout: H x (gate|up))
+    dW1: np.ndarray      # fp64 [G, H, 2I]   (logical W1 layout: H x (gate|up); sReLU: [G, H, I])
     dW2: np.ndarray      # fp64 [G, I, H]
     dlogits: np.ndarray  # fp64 [T, E]
     dw_row: np.ndarray   # fp64 [R]
-    dh: np.ndarray       # fp64 [R, 2I]
+    dh: np.ndarray       # fp64 [R, 2I] (sReLU: [R, I])
     dY1: np.ndarray      # fp64 [R, I]
 
 
@@ -72,9 +72,12 @@ def layer_backward(fwd: Forward, x_bits, dout_bits, wts: dict, *, E: int, k: int
                    w1t=None, w2t=None) -> Backward:
     """Gradients of L = sum(dOut * out) for the layer computed by ``fwd``.
 
-    Weights for the dgrad GEMMs come from ``w1t(e)`` -> [H, 2I] and
-    ``w2t(e)`` -> [I, H] (decoded fp64). ``experts`` restricts the work to a
-    subset of expert groups (others leave zeros / NaN rows).
+    Weights for the dgrad GEMMs come from ``w1t(e)`` -> [H, 2I] ([H, I] for
+    the non-gated sReLU) and ``w2t(e)`` -> [I, H] (decoded fp64).
+    ``experts`` restricts the work to a subset of expert groups (others
+    leave zeros / NaN rows). The backward kernel family of the NVIDIA fusion
+    blog (GroupGemm + dActivation + Quantize/Transpose) covers SwiGLU, GeGLU
+    and sReLU; for sReLU dh = w_row * dY1 * 2 max(h, 0) over W1's I outputs.
     """
     x = values(x_bits)
     dout = values(dout_bits)
@@ -84,13 +87,14 @@ def layer_backward(fwd: Forward, x_bits, dout_bits, wts: dict, *, E: int, k: int
     kp = len(d.inv) // max(T, 1) if T else k
     R = len(d.perm_src)
     I = fwd.y.shape[1]
+    N1 = 2 * I if gated(act) else I                    # W1 outputs
     want = np.zeros(G, bool)
     want[list(range(G)) if experts is None else list(experts)] = True
     dY1 = np.full((R, I), np.nan)
-    dh = np.full((R, 2 * I), np.nan)
+    dh = np.full((R, N1), np.nan)
     dXp = np.full((R, H), np.nan)
     dw_row = np.full(R, np.nan)
-    dW1 = np.zeros((G, H, 2 * I))
+    dW1 = np.zeros((G, H, N1))
     dW2 = np.zeros((G, I, H))
     for e in range(G):
         lo, hi = d.offsets[e], d.offsets[e + 1]
@@ -104,16 +108,21 @@ def layer_backward(fwd: Forward, x_bits, dout_bits, wts: dict, *, E: int, k: int
         hb = fwd.h[rs]
         if quant:                                      # saved h is bf16
             hb = F.bf16_to_f64(F.f64_to_bf16(hb))
-        g, u = hb[:, :I], hb[:, I:]
-        a_val = act_fwd(g, u, act, alpha, limit)
-        dw_row[rs] = (dy * a_val).sum(axis=1)
-        dg, du = act_bwd(g, u, d.w_row[rs, None] * dy, act, alpha, limit)
-        dhe = np.concatenate([dg, du], axis=1)         # [n, 2I]
-        # dXp = dh . W1^T (contraction over 2I; W1 copy quantised along 2I)
+        if gated(act):
+            g, u = hb[:, :I], hb[:, I:]
+            a_val = act_fwd(g, u, act, alpha, limit)
+            dw_row[rs] = (dy * a_val).sum(axis=1)
+            dg, du = act_bwd(g, u, d.w_row[rs, None] * dy, act, alpha, limit)
+            dhe = np.concatenate([dg, du], axis=1)     # [n, 2I]
+        else:
+            a_val = act_plain(hb, act)
+            dw_row[rs] = (dy * a_val).sum(axis=1)
+            dhe = act_plain_bwd(hb, d.w_row[rs, None] * dy, act)   # [n, I]
+        # dXp = dh . W1^T (contraction over N1; W1 copy quantised along N1)
         dXp[rs] = _q_rows(dhe, quant) @ w1t(e).T       # [n, H]
         # wgrads: contraction over the expert's rows
         a_cols = _q_cols(x[toks], quant)               # [n, H]
-        dW1[e] = a_cols.T @ _q_cols(dhe, quant)        # [H, 2I]
+        dW1[e] = a_cols.T @ _q_cols(dhe, quant)        # [H, N1]
         dW2[e] = _q_cols(fwd.y[rs], quant).T @ _q_cols(dz, quant)   # [I, H]
         dY1[rs], dh[rs] = dy, dhe
     dx = np.full((T, H), np.nan)

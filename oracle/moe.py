@@ -148,6 +148,15 @@ def act_plain(h, act="srelu"):
     return np.square(np.maximum(h, 0.0))
 
 
+def act_plain_bwd(h, d, act="srelu"):
+    """Gradient of sum(d * act_plain(h)) with respect to h: the derivative
+    of max(h, 0)^2 is 2 max(h, 0) (the dActivation kernel family of the same
+    blog lists sReLU among its activations)."""
+    h = np.asarray(h, np.float64)
+    assert act == "srelu", act
+    return d * 2.0 * np.maximum(h, 0.0)
+
+
 def act_fwd(g, u, act="swiglu", alpha=1.0, limit=0.0):
     """The gated activations the blog's fused kernels support (NVIDIA blog,
     kernel families: SwiGLU, GeGLU), with b = c = 0:

@@ -20,7 +20,7 @@ def _setup(act, S=0, rs=1.0):
     G = E + S
     x = rng.normal(0, 1, (T, H))
     logits = rng.normal(0, 1, (T, E))
-    w1 = rng.normal(0, 0.6, (G, 2 * I, H))
+    w1 = rng.normal(0, 0.6, (G, I if act == "srelu" else 2 * I, H))
     w2 = rng.normal(0, 0.6, (G, H, I))
     dout = rng.normal(0, 1, (T, H))
     clamp = act == "swiglu_clamp"
@@ -35,7 +35,7 @@ def _loss(x, logits, w1, w2, dout, kw):
 
 
 @pytest.mark.parametrize("act,S,rs", [("swiglu", 0, 1.0), ("swiglu_clamp", 0, 1.0), ("swiglu", 1, 2.5),
-                                      ("geglu", 0, 1.0)])
+                                      ("geglu", 0, 1.0), ("srelu", 0, 1.0)])
 def test_backward_matches_finite_differences(act, S, rs):
     x, logits, w1, w2, dout, kw = _setup(act, S, rs)
     f = M.layer_forward(x, logits, {"w1_f64": w1, "w2_f64": w2}, quant=False, **kw)
@@ -60,13 +60,14 @@ def test_backward_matches_finite_differences(act, S, rs):
     for t in range(x.shape[0]):
         for e in range(kw["E"]):
             assert bw.dlogits[t, e] == pytest.approx(fd(logits, (t, e)), rel=1e-5, abs=1e-6)
-    G, I2, H = w1.shape
+    G, N1, H = w1.shape
+    I = w2.shape[2]
     for e in range(G):
-        for n in range(0, I2, 3):
+        for n in range(0, N1, 3):
             for h in range(0, H, 5):
                 assert bw.dW1[e, h, n] == pytest.approx(fd(w1, (e, n, h)), rel=1e-5, abs=1e-6)
         for h in range(0, H, 4):
-            for i in range(0, I2 // 2, 3):
+            for i in range(0, I, 3):
                 assert bw.dW2[e, i, h] == pytest.approx(fd(w2, (e, h, i)), rel=1e-5, abs=1e-6)
 
 
