@@ -64,6 +64,7 @@ class Backward:
     dw_row: np.ndarray   # fp64 [R]
     dh: np.ndarray       # fp64 [R, 2I] (sReLU: [R, I])
     dY1: np.ndarray      # fp64 [R, I]
+    db1: np.ndarray      # fp64 [G, 2I]: gradient of W1's bias (gate b then up c)
 
 
 def layer_backward(fwd: Forward, x_bits, dout_bits, wts: dict, *, E: int, k: int,
@@ -75,7 +76,9 @@ def layer_backward(fwd: Forward, x_bits, dout_bits, wts: dict, *, E: int, k: int
     Weights for the dgrad GEMMs come from ``w1t(e)`` -> [H, 2I] ([H, I] for
     the non-gated sReLU) and ``w2t(e)`` -> [I, H] (decoded fp64).
     ``experts`` restricts the work to a subset of expert groups (others
-    leave zeros / NaN rows). The backward kernel family of the NVIDIA fusion
+    leave zeros / NaN rows). With a W1 bias (h = xW + b | xV + c) the
+    backward is unchanged but for the bias gradient db1[e] = the sum of dh
+    over the group's rows. The backward kernel family of the NVIDIA fusion
     blog (GroupGemm + dActivation + Quantize/Transpose) covers SwiGLU, GeGLU
     and sReLU; for sReLU dh = w_row * dY1 * 2 max(h, 0) over W1's I outputs.
     """
@@ -95,6 +98,7 @@ def layer_backward(fwd: Forward, x_bits, dout_bits, wts: dict, *, E: int, k: int
     dXp = np.full((R, H), np.nan)
     dw_row = np.full(R, np.nan)
     dW1 = np.zeros((G, H, N1))
+    db1 = np.zeros((G, N1))
     dW2 = np.zeros((G, I, H))
     for e in range(G):
         lo, hi = d.offsets[e], d.offsets[e + 1]
@@ -125,6 +129,7 @@ def layer_backward(fwd: Forward, x_bits, dout_bits, wts: dict, *, E: int, k: int
         dW1[e] = a_cols.T @ _q_cols(dhe, quant)        # [H, N1]
         dW2[e] = _q_cols(fwd.y[rs], quant).T @ _q_cols(dz, quant)   # [I, H]
         dY1[rs], dh[rs] = dy, dhe
+        db1[e] = dhe.sum(axis=0)
     dx = np.full((T, H), np.nan)
     dlogits = np.zeros((T, E))
     for t in range(T):
@@ -141,7 +146,7 @@ def layer_backward(fwd: Forward, x_bits, dout_bits, wts: dict, *, E: int, k: int
         dp = routed_scale * dw_row[rr[:k]]
         dsel = p * (dp - (p * dp).sum())
         dlogits[t, fwd.ids[t]] = dsel
-    return Backward(dx, dW1, dW2, dlogits, dw_row, dh, dY1)
+    return Backward(dx, dW1, dW2, dlogits, dw_row, dh, dY1, db1)
 
 
 # ---------------------------------------------------------------------------

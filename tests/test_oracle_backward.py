@@ -71,6 +71,43 @@ def test_backward_matches_finite_differences(act, S, rs):
                 assert bw.dW2[e, i, h] == pytest.approx(fd(w2, (e, h, i)), rel=1e-5, abs=1e-6)
 
 
+@pytest.mark.parametrize("act", ["swiglu", "geglu"])
+def test_bias_gradient_matches_finite_differences(act):
+    """With a W1 bias (gate b, up c) the oracle's db1 is the finite-difference
+    gradient of the loss in the bias, and the other gradients still are."""
+    x, logits, w1, w2, dout, kw = _setup(act)
+    rng = np.random.default_rng(5)
+    b1 = rng.normal(0, 0.5, (w1.shape[0], w1.shape[1]))
+    wts = {"w1_f64": w1, "w2_f64": w2, "b1": b1}
+
+    def loss():
+        f = M.layer_forward(x, logits, wts, quant=False, **kw)
+        return float((f.out * dout).sum())
+
+    f = M.layer_forward(x, logits, wts, quant=False, **kw)
+    bw = B.layer_backward(f, x, dout, wts, E=kw["E"], k=kw["k"], act=act, quant=False,
+                          w1t=lambda e: w1[e].T, w2t=lambda e: w2[e].T)
+    eps = 1e-6
+
+    def fd(arr, idx):
+        old = arr[idx]
+        arr[idx] = old + eps
+        lp = loss()
+        arr[idx] = old - eps
+        lm = loss()
+        arr[idx] = old
+        return (lp - lm) / (2 * eps)
+
+    for e in range(b1.shape[0]):
+        for n in range(b1.shape[1]):
+            assert bw.db1[e, n] == pytest.approx(fd(b1, (e, n)), rel=1e-5, abs=1e-6)
+    for t in range(0, x.shape[0], 2):
+        for h in range(0, x.shape[1], 4):
+            assert bw.dx[t, h] == pytest.approx(fd(x, (t, h)), rel=1e-5, abs=1e-6)
+    for h in range(0, x.shape[1], 5):
+        assert bw.dW1[0, h, 1] == pytest.approx(fd(w1, (0, 1, h)), rel=1e-5, abs=1e-6)
+
+
 def test_quantised_backward_close_to_unquantised():
     """With quantisers on, gradients stay within MXFP8 error of the exact ones
     (sanity: the quantised path is the same algebra)."""
