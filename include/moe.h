@@ -105,8 +105,9 @@ enum { MOE_PACK_FORWARD = 0, MOE_PACK_DGRAD = 1 };
  *                              families: SwiGLU, GeGLU, with clamping).
  * act = MOE_ACT_SRELU:         the non-gated squared ReLU the blog also lists
  *                              (sReLU): W1 has I outputs h (no up half) and
- *                              act = max(h, 0)^2. Forward only, without
- *                              w1_bias, not in the fused W1 -> W2 layer. 
+ *                              act = max(h, 0)^2; its backward (MXFP8) takes
+ *                              dh = w_row * dY1 * 2 max(h, 0). Without
+ *                              w1_bias, not in the fused W1 -> W2 layer.
  * weight_fmt = MOE_WFMT_NVFP4: E2M1 elements, E4M3 scale per 16 along K,
  *                              fp32 scale per (group, matrix)
  * weight_fmt = MOE_WFMT_MXFP8: E4M3 elements, E8M0 scale per 32 along K
@@ -125,7 +126,8 @@ typedef struct moe_config {
     int32_t weight_fmt;
     int32_t max_sms;      /* 0: use every SM; else cap the GEMM grids        */
     int32_t w1_bias;      /* 1: W1 carries a per-group fp32 bias [2I] (gate b,
-                           * up c) added before the activation, forward only
+                           * up c) added before the activation; the
+                           * backward returns its gradient db1
                            * (the NVIDIA blog's SwiGLU(xW + b, xV + c) and its
                            * fused bias-vector epilogue, kernel families) */
     int32_t dispatch_sms; /* 0..64. Where moe_layer_fused holds and > 0 (it
@@ -151,7 +153,8 @@ typedef struct moe_config {
  *   which = MOE_PACK_FORWARD: W1 rows n < 2I (gate features then up
  *     features; MOE_ACT_SRELU: rows n < I), K = H; W2 rows n < H, K = I.
  *   which = MOE_PACK_DGRAD (MXFP8 only, training): W1 copy with rows h < H,
- *     K = 2I; W2 copy with rows i < I, K = H (quantised along that K).
+ *     K = 2I (MOE_ACT_SRELU: K = I); W2 copy with rows i < I, K = H
+ *     (quantised along that K).
  * NVFP4: w*_q [G, N, K/2] bytes, element 2i in the low nibble of byte i;
  *        w*_s [G, N, K/16] E4M3 codes; w*_gs [G] fp32.
  * MXFP8: w*_q [G, N, K] E4M3 codes; w*_s [G, N, K/32] E8M0 codes;
@@ -187,7 +190,8 @@ typedef struct moe_dispatch {
  * caller-owned; sizes from moe_train_sizes). Pad rows: every group's rows are
  * padded with zero rows to a multiple of 128; poff[e] is the padded offset. */
 typedef struct moe_train_save {
-    uint16_t* h;        /* [R, 2I] bf16 W1 output before the activation       */
+    uint16_t* h;        /* [R, 2I] bf16 W1 output before the activation
+                           ([R, I] for MOE_ACT_SRELU)                         */
     uint8_t* y1t_q;     /* [I, R_pad] MXFP8 of y (activation x routing weight)
                            quantised along the padded row axis               */
     uint8_t* y1t_s;     /* [R_pad/128, I] 32-bit words of its E8M0 scales:
@@ -385,15 +389,19 @@ moe_status_t moe_layer_fused(const moe_config_t* cfg, int T, int32_t* fused);
 
 /* Gradients of L = sum(dout * out) for the forward that filled ws and save
  * with the same T: dx [T, H] bf16 (expert path only), dW1 [E, H, 2I] bf16 in
- * the logical W1 layout (gate columns then up columns), dW2 [E, I, H] bf16,
- * dlogits [T, E] fp32. packed_w_dgrad: moe_prepack_weights(..., DGRAD, ...).
+ * the logical W1 layout (gate columns then up columns; [E, H, I] for
+ * MOE_ACT_SRELU), dW2 [E, I, H] bf16,
+ * dlogits [T, E] fp32; with cfg->w1_bias, db1 [E, 2I] fp32 (gate b then up
+ * c: the sum of dh over each group's rows; NULL otherwise, else
+ * MOE_ERR_INVALID_ARG). packed_w_dgrad: moe_prepack_weights(..., DGRAD, ...).
  * The router's own dense GEMM gradients (dlogits . W_r^T, x^T . dlogits) are
  * left to the caller. Source: NVIDIA blog, kernel families (GroupGemm +
  * dActivation + Quantize/Transpose) and the MXFP8 section (weight gradients
  * from the transposed MXFP8 copies). */
 moe_status_t moe_layer_backward(const moe_config_t* cfg, const uint16_t* dout, const uint16_t* x, int T,
                                 const moe_train_save_t* save, const void* packed_w_dgrad, uint16_t* dx,
-                                uint16_t* dW1, uint16_t* dW2, float* dlogits, void* ws, void* stream);
+                                uint16_t* dW1, uint16_t* dW2, float* dlogits, float* db1, void* ws,
+                                void* stream);
 
 /* ---- status --------------------------------------------------------------- */
 

@@ -304,11 +304,12 @@ def moe_layer_forward(cfg, x, W_r, logits, T, packed, out, save, ws, stream=None
                                     ctypes.byref(save) if save is not None else None, _ptr(ws), _stream(stream)))
 
 
-def moe_layer_backward(cfg, dout, x, T, save, packed_dgrad, dx, dW1, dW2, dlogits, ws, stream=None):
+def moe_layer_backward(cfg, dout, x, T, save, packed_dgrad, dx, dW1, dW2, dlogits, ws, stream=None, db1=None):
+    """db1: [E, 2I] fp32 W1 bias gradient, required when cfg.w1_bias."""
     _check("moe_layer_backward",
            load().moe_layer_backward(ctypes.byref(cfg), _ptr(dout), _ptr(x), T, ctypes.byref(save),
-                                     _ptr(packed_dgrad), _ptr(dx), _ptr(dW1), _ptr(dW2), _ptr(dlogits), _ptr(ws),
-                                     _stream(stream)))
+                                     _ptr(packed_dgrad), _ptr(dx), _ptr(dW1), _ptr(dW2), _ptr(dlogits), _ptr(db1),
+                                     _ptr(ws), _stream(stream)))
 
 
 def moe_read_status(cfg, ws, stream=None) -> int:
@@ -371,7 +372,8 @@ def alloc_train_save(cfg, T, device="cuda", amax=False):
     R = T * kp
     G = cfg.E + cfg.n_shared
     bufs = {
-        "h": torch.empty(max(R, 1), 2 * cfg.I, dtype=torch.int16, device=device),
+        "h": torch.empty(max(R, 1), (cfg.I if cfg.act == MOE_ACT_SRELU else 2 * cfg.I), dtype=torch.int16,
+                         device=device),
         "y1t_q": torch.empty(cfg.I, rp, dtype=torch.uint8, device=device),
         "y1t_s": torch.empty(rp // 128, cfg.I, 4, dtype=torch.uint8, device=device),
         "at_q": torch.empty(cfg.H, rp, dtype=torch.uint8, device=device),

@@ -50,7 +50,7 @@ static int64_t r_pad_for(const Dims& d, int T) {
 static bool gated(const moe_config_t& c) { return c.act != MOE_ACT_SRELU; }
 
 static bool backward_capable(const moe_config_t& c) {
-  return c.weight_fmt == MOE_WFMT_MXFP8 && c.n_shared == 0 && !c.w1_bias && gated(c);
+  return c.weight_fmt == MOE_WFMT_MXFP8 && c.n_shared == 0;
 }
 
 // MXFP8 weights run on the block-scaled tensor-core GEMM (gemm_mx.cu); NVFP4
@@ -69,6 +69,7 @@ struct WsLayout {
   size_t P, a16, y16, rexp1, rexp2, P2, fcnt;            // NVFP4 path (P2, fcnt: the fused layer)
   size_t xg, xgs, y1st;                                   // MXFP8 path: gathered x rows, y1 scales (SF4)
   size_t dzq, dzs, dzg, dzgs, dztq, dzts, dhq, dhs, dhtq, dhts, dxp, dwpart;   // backward
+  size_t dbpart;                                          // backward with a W1 bias
   size_t total;
 };
 
@@ -127,6 +128,7 @@ static WsLayout ws_layout(const moe_config_t& c) {
     L.dhts = take((size_t)sf4_bytes(d.RpMax, 2 * d.I));
     L.dxp = take((size_t)R * d.H * 2);
     L.dwpart = take((size_t)ceil_div(d.I, kMxTileN) * R * 4);
+    if (c.w1_bias) L.dbpart = take((size_t)(d.RpMax / 32) * 2 * d.I * 4);   // bias gradient partials
   }
   L.total = o;
   return L;
@@ -159,7 +161,7 @@ static PackLayout pack_layout(const moe_config_t& c, int which) {
     P.N1 = gated(c) ? 2 * c.I : c.I; P.K1 = c.H; P.il1 = gated(c) ? c.I : 0;
     P.N2 = c.H; P.K2 = c.I;
   } else {
-    P.N1 = c.H; P.K1 = 2 * c.I; P.il1 = 0;
+    P.N1 = c.H; P.K1 = gated(c) ? 2 * c.I : c.I; P.il1 = 0;
     P.N2 = c.I; P.K2 = c.H;
   }
   size_t o = 256;
@@ -286,7 +288,7 @@ moe_status_t moe_packed_weights_size(const moe_config_t* c, int which, size_t* b
   moe_status_t s = moe_config_validate(c);
   if (s != MOE_OK) return s;
   if (!bytes || (which != MOE_PACK_FORWARD && which != MOE_PACK_DGRAD)) return MOE_ERR_INVALID_ARG;
-  if (which == MOE_PACK_DGRAD && (c->weight_fmt != MOE_WFMT_MXFP8 || !gated(*c))) return MOE_ERR_UNSUPPORTED;
+  if (which == MOE_PACK_DGRAD && c->weight_fmt != MOE_WFMT_MXFP8) return MOE_ERR_UNSUPPORTED;
   *bytes = pack_layout(*c, which).total;
   return MOE_OK;
 }
@@ -304,7 +306,7 @@ moe_status_t moe_prepack_weights(const moe_config_t* c, const moe_weights_view_t
   moe_status_t s = moe_config_validate(c);
   if (s != MOE_OK) return s;
   if (!src || (which != MOE_PACK_FORWARD && which != MOE_PACK_DGRAD)) return MOE_ERR_INVALID_ARG;
-  if (which == MOE_PACK_DGRAD && (c->weight_fmt != MOE_WFMT_MXFP8 || !gated(*c))) return MOE_ERR_UNSUPPORTED;
+  if (which == MOE_PACK_DGRAD && c->weight_fmt != MOE_WFMT_MXFP8) return MOE_ERR_UNSUPPORTED;
   REQ(dst); REQ(src->w1_q); REQ(src->w1_s); REQ(src->w2_q); REQ(src->w2_s);
   if (c->weight_fmt == MOE_WFMT_NVFP4) { REQ(src->w1_gs); REQ(src->w2_gs); }
   if (c->w1_bias && which == MOE_PACK_FORWARD) REQ(src->b1);
@@ -348,7 +350,7 @@ moe_status_t moe_debug_unpack_weights(const moe_config_t* c, const void* packed,
   moe_status_t s = moe_config_validate(c);
   if (s != MOE_OK) return s;
   if ((which != MOE_PACK_FORWARD && which != MOE_PACK_DGRAD) || (mat != 1 && mat != 2)) return MOE_ERR_INVALID_ARG;
-  if (which == MOE_PACK_DGRAD && (c->weight_fmt != MOE_WFMT_MXFP8 || !gated(*c))) return MOE_ERR_UNSUPPORTED;
+  if (which == MOE_PACK_DGRAD && c->weight_fmt != MOE_WFMT_MXFP8) return MOE_ERR_UNSUPPORTED;
   REQ(packed); REQ(q); REQ(sc);
   const PackLayout P = pack_layout(*c, which);
   cudaStream_t st = (cudaStream_t)stream;
@@ -931,13 +933,14 @@ static moe_status_t mx_wgrad(const moe_config_t* c, const uint8_t* pq, const uin
 
 moe_status_t moe_layer_backward(const moe_config_t* c, const uint16_t* dout, const uint16_t* x, int T,
                                 const moe_train_save_t* save, const void* packed_w_dgrad, uint16_t* dx, uint16_t* dW1,
-                                uint16_t* dW2, float* dlogits, void* ws, void* stream) {
+                                uint16_t* dW2, float* dlogits, float* db1, void* ws, void* stream) {
   moe_status_t s = check_T(c, T);
   if (s != MOE_OK) return s;
   if (!backward_capable(*c)) return MOE_ERR_UNSUPPORTED;
   if (!save) return MOE_ERR_INVALID_ARG;
   if ((s = check_save(c, save)) != MOE_OK) return s;
   REQ_T(dout); REQ_T(x); REQ(packed_w_dgrad); REQ_T(dx); REQ(dW1); REQ(dW2); REQ_T(dlogits); REQ(ws);
+  if (c->w1_bias) { REQ(db1); } else if (db1) return MOE_ERR_INVALID_ARG;
   reset_launch_count();
   cudaStream_t st = (cudaStream_t)stream;
   const WsLayout L = ws_layout(*c);
@@ -945,6 +948,7 @@ moe_status_t moe_layer_backward(const moe_config_t* c, const uint16_t* dout, con
   moe_workspace_view(c, ws, &v);
   const Dims dm = dims_of(*c);
   const int kp = dm.kp, G = dm.G, I = c->I, H = c->H;
+  const int N1 = gated(*c) ? 2 * I : I;   // W1 outputs: h and dh columns
   const int R = T * kp;
   const int64_t Rp = r_pad_for(dm, T);
   int32_t* status = at<int32_t>(ws, L.status);
@@ -976,12 +980,14 @@ moe_status_t moe_layer_backward(const moe_config_t* c, const uint16_t* dout, con
     MxArgs g = mx_args0();
     g.n_tiles = nparts;
     g.I = I;
+    g.gated = gated(*c);
     g.w_row = v.d.w_row;
     g.act = act_params(c);
     g.hsave = save->h;
     g.yq = dhq; g.yst = dhs;
-    g.tq = dhtq; g.ts = dhts; g.t_ld = Rp; g.t_nf = 2 * I;
+    g.tq = dhtq; g.ts = dhts; g.t_ld = Rp; g.t_nf = N1;
     g.dwpart = dwpart;
+    if (c->w1_bias) { g.dbpart = at<float>(ws, L.dbpart); g.db_ld = N1; }
     if ((s = mx_token_gemm(c, g, kMxDswiglu, dzg, dzgs, R, packed_w_dgrad, MOE_PACK_DGRAD, 2, v.d.offsets, poff,
                            status, st)) != MOE_OK)
       return s;
@@ -996,9 +1002,11 @@ moe_status_t moe_layer_backward(const moe_config_t* c, const uint16_t* dout, con
     MOE_CHECK_CUDA(launch_combine(dxp, v.d.inv, nullptr, T, c->k, kp, H, dx, st));
   }
   // 4. wgrads over each group's padded rows (groups without rows: zeros)
-  if ((s = mx_wgrad(c, save->at_q, save->at_s, H, dhtq, dhts, 2 * I, Rp, poff, dW1, status, st)) != MOE_OK) return s;
+  if ((s = mx_wgrad(c, save->at_q, save->at_s, H, dhtq, dhts, N1, Rp, poff, dW1, status, st)) != MOE_OK) return s;
   if ((s = mx_wgrad(c, save->y1t_q, save->y1t_s, I, dztq, dzts, H, Rp, poff, dW2, status, st)) != MOE_OK) return s;
-  // 5. router
+  // 5. W1 bias: each group's padded 32-row block partials summed in order
+  if (c->w1_bias) MOE_CHECK_CUDA(launch_bias_grad(at<float>(ws, L.dbpart), N1, poff, G, db1, st));
+  // 6. router
   MOE_CHECK_CUDA(launch_router_bwd(v.d.topk_w, v.d.topk_ids, dwpart, nparts, R, v.d.inv, T, c->E, c->k, kp,
                                    c->routed_scale, dlogits, st));
   return MOE_OK;

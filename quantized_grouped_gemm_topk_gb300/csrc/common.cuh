@@ -162,6 +162,8 @@ __device__ __forceinline__ float act_plain(float h) {
   const float r = fmaxf(h, 0.f);
   return r * r;
 }
+// Its gradient: d * 2 max(h, 0).
+__device__ __forceinline__ float act_plain_bwd(float h, float d) { return d * (2.f * fmaxf(h, 0.f)); }
 
 // Logistic sigmoid with the fast exponential and divide intrinsics: relative
 // error ~1e-6, far inside the layer's tolerance, and several times cheaper

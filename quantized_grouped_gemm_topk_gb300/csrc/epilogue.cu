@@ -404,6 +404,30 @@ cudaError_t launch_quant_cols(const ColQuantArgs& a, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// ---- W1 bias gradient ----------------------------------------------------------
+// db[e][c] = sum over group e's padded 32-row blocks b, in block order, of
+// part[b][c] (the dActivation epilogue's per-warp column sums of dh; pad
+// rows hold zeros). Grid (column slices, G); a group without rows gets 0.
+__global__ void __launch_bounds__(256) k_bias_grad(const float* __restrict__ part, int N,
+                                                   const int32_t* __restrict__ poff, float* __restrict__ db) {
+  pdl_enter();
+  const int e = blockIdx.y;
+  const int b0 = poff[e] / 32, b1 = poff[e + 1] / 32;
+  for (int c = blockIdx.x * blockDim.x + threadIdx.x; c < N; c += gridDim.x * blockDim.x) {
+    float acc = 0.f;
+    for (int b = b0; b < b1; ++b) acc += part[(int64_t)b * N + c];
+    db[(int64_t)e * N + c] = acc;
+  }
+}
+
+cudaError_t launch_bias_grad(const float* part, int N, const int32_t* poff, int G, float* db, cudaStream_t st) {
+  if (G == 0 || N == 0) return cudaSuccess;
+  cudaError_t e = launch_pdl(k_bias_grad, dim3((unsigned)((N + 255) / 256), (unsigned)G), dim3(256), 0, st, part, N,
+                             poff, db);
+  note_launch();
+  return e;
+}
+
 // ---- router backward: softmax-over-selected Jacobian ---------------------------
 __global__ void __launch_bounds__(256) k_router_bwd(const float* __restrict__ topk_w, const int32_t* __restrict__ ids,
                                                     const float* __restrict__ dwpart, int nparts, int64_t R,

@@ -20,7 +20,8 @@
 //   kMxPlain    D -> bf16 rows (W2 forward; W1 dgrad).
 //   kMxDswiglu  dY1 = dz_e . W2_e^T; dh = dact(h; w_row * dY1) -> MXFP8 rows
 //               and the transposed MXFP8 copy; per-tile routing-weight
-//               gradient partials sum(dY1 * act(h)).
+//               gradient partials sum(dY1 * act(h)). Gated: h and dh hold
+//               2I a row (gate then up); sReLU: I a row.
 //   kMxWgrad    dW_e = P_e^T . Q_e over the group's padded token rows
 //               (variable K per group) -> bf16; a group with no rows writes
 //               zeros.
@@ -237,6 +238,23 @@ __device__ __forceinline__ void nvfp4_amax32(const float (&y)[32], bool live, fl
   }
 }
 
+// Column sums over a warp's 32 rows: v[c] is the lane's row's value of
+// column c; on return v[0] of lane l is the sum over the 32 lanes of column l
+// (a butterfly that halves the columns a lane holds at each of 5 steps).
+__device__ __forceinline__ float warp_colsum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int s = 16; s >= 1; s >>= 1) {
+    const bool up = (lane & s) != 0;           // this lane keeps columns with bit s set
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      const float send = up ? v[i] : v[i + s];
+      const float keep = up ? v[i + s] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  return v[0];
+}
+
 template <int MODE>
 __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, uint32_t acc_tmem, int q, int lane,
                                             bool has_k) {
@@ -271,9 +289,13 @@ __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, ui
       }
     }
   } else if (MODE == kMxW1 && !g.gated) {
-    // sReLU: column c is feature ni * 192 + c of a W1 with I outputs
+    // sReLU: column c is feature ni * 192 + c of a W1 with I outputs; the
+    // training saves are h (bf16, I a row) and the transposed copy of y
     const int f0 = w.ni * kMxBN;
     const float wr = rvalid ? g.w_row[row] : 0.f;
+    const int rel = w.mi * kMxBM + m;
+    const bool tblk = g.tq && (w.mi * kMxBM + q * 32) < w.pad;
+    const int64_t p = g.tq ? (int64_t)g.poff[w.e] + rel : 0;
     for (int b = 0; b < kMxBN / 32; ++b) {
       const int f = f0 + 32 * b;
       if (f >= g.I) break;
@@ -287,6 +309,22 @@ __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, ui
         const uint8_t sb = quant_block32_store(y, g.yq + row * g.I + f);
         g.ys[row * (g.I / 32) + f / 32] = sb;
         if (g.yst) g.yst[sf4_at(f / 32, row, g.R)] = sb;
+        if (g.hsave) {
+          uint32_t hv[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) hv[i] = bf16x2_bits(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+          uint4* dh = reinterpret_cast<uint4*>(g.hsave + row * g.I + f);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) dh[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+        }
+      }
+      if (g.amax) nvfp4_amax32(y, rel < w.cnt, g.amax, lane);
+      if (tblk) {
+        if (rel >= w.cnt) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) y[i] = 0.f;      // padding rows of the group
+        }
+        quant_cols32(y, g.tq, g.ts, f, g.t_ld, g.t_nf, p, lane);
       }
     }
   } else if (MODE == kMxW1) {
@@ -345,6 +383,52 @@ __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, ui
         quant_cols32(y, g.tq, g.ts, f, g.t_ld, g.t_nf, p, lane);
       }
     }
+  } else if (!g.gated) {   // kMxDswiglu for sReLU: dh = w_row * dY1 * 2 max(h, 0), I features a row
+    const int f0 = w.ni * kMxBN;
+    const float wr = rvalid ? g.w_row[row] : 0.f;
+    const int rel = w.mi * kMxBM + m;
+    const bool tblk = (w.mi * kMxBM + q * 32) < w.pad;
+    const bool live = rel < w.cnt;
+    const int64_t p = (int64_t)g.poff[w.e] + rel;
+    const int I = g.I;
+    float dw = 0.f;
+    for (int c0 = 0; c0 < kMxBN; c0 += 32) {
+      const int f = f0 + c0;
+      if (f >= I) break;
+      uint32_t dv[32];
+      tc::tmem_ld32(acc_tmem + c0, dv);
+      tc::tmem_wait_ld();
+      float dh[32];
+      if (rvalid) {
+        const uint4* h4 = reinterpret_cast<const uint4*>(g.hsave + row * I + f);
+        uint32_t hw[16];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint4 a = h4[i];
+          hw[4 * i] = a.x; hw[4 * i + 1] = a.y; hw[4 * i + 2] = a.z; hw[4 * i + 3] = a.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const uint32_t x = hw[i >> 1];
+          const float hh = __uint_as_float(i & 1 ? x & 0xffff0000u : x << 16);
+          const float dy = __uint_as_float(dv[i]);
+          dw = fmaf(dy, act_plain(hh), dw);
+          dh[i] = act_plain_bwd(hh, wr * dy);
+        }
+        g.yst[sf4_at(f / 32, row, g.R)] = quant_block32_store(dh, g.yq + row * I + f);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) dh[i] = 0.f;
+      }
+      if (tblk) {
+        if (!live) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) dh[i] = 0.f;   // padding rows of the group
+        }
+        quant_cols32(dh, g.tq, g.ts, f, g.t_ld, g.t_nf, p, lane);
+      }
+    }
+    if (rvalid) g.dwpart[(int64_t)w.ni * g.R + row] = dw;
   } else {   // kMxDswiglu: columns = dY1 for features f0 + c
     const int f0 = w.ni * kMxBN;
     const float wr = rvalid ? g.w_row[row] : 0.f;
@@ -395,6 +479,15 @@ __device__ __forceinline__ void mx_epilogue(const MxArgs& g, const MxUnit& w, ui
         }
         quant_cols32(dg, g.tq, g.ts, f, g.t_ld, g.t_nf, p, lane);
         quant_cols32(du, g.tq, g.ts, (int64_t)I + f, g.t_ld, g.t_nf, p, lane);
+      }
+      if (g.dbpart && tblk) {
+        // W1 bias gradient partials: this warp's 32 rows summed per column
+        // (rows past the group's count hold zeros)
+        float* dst = g.dbpart + (p - lane) / 32 * g.db_ld;
+        const float sg = warp_colsum32(dg, lane);
+        const float su = warp_colsum32(du, lane);
+        dst[f + lane] = sg;
+        dst[I + f + lane] = su;
       }
     }
     if (rvalid) g.dwpart[(int64_t)w.ni * g.R + row] = dw;

@@ -220,7 +220,8 @@ struct MxArgs {
   int b_fp4;                    // B elements are E2M1 (MXFP4 weights), else E4M3
   int bias;                     // the blob carries a W1 bias (checked against its header)
   const float* b1;              // W1 mode (nullable): [G][2I] bias, gate then up
-  int gated;                    // W1 mode: 1 = gate / up halves in each tile, 0 = sReLU (192 plain features a tile)
+  int gated;                    // 1 = gate / up halves (W1: in each tile; dSwiGLU: h and dh of 2I a row),
+                                // 0 = sReLU (W1: 192 plain features a tile; dActivation: h and dh of I a row)
   int64_t R;                    // token rows (A rows of the token-side modes)
   const float* w_row;           // [R] routing weight per row
   ActParams act;
@@ -233,6 +234,8 @@ struct MxArgs {
                                                        // (K = t_ld, ld = t_nf); W1: nullable
   uint16_t* out; int64_t out_ld;            // Plain: [R][out_ld]; Wgrad: [G][M][out_ld]
   float* dwpart;                // Dswiglu: [n_tiles][R]
+  float* dbpart;                // Dswiglu (nullable): [R_pad / 32][db_ld] column sums of dh over each
+  int db_ld;                    //   padded 32-row block (the W1 bias gradient's partials)
   float* amax;                  // W1 (nullable): [2] max |y|, max |H16/4 . block of y^T| (zeroed by the caller)
   int32_t* status;
 };
@@ -305,6 +308,10 @@ cudaError_t launch_quant_cols(const ColQuantArgs& a, cudaStream_t st);
 // ---- backward pieces ----------------------------------------------------------
 // dlogits from the routing-weight gradients dw_row[r] = sum over p < nparts of
 // dwpart[p * R + r] (added in p order).
+// W1 bias gradient: db[e][c] = sum over group e's padded 32-row blocks b (in
+// block order) of part[b][c], c < N; groups without rows get zeros.
+cudaError_t launch_bias_grad(const float* part, int N, const int32_t* poff, int G, float* db, cudaStream_t st);
+
 cudaError_t launch_router_bwd(const float* topk_w, const int32_t* ids, const float* dwpart, int nparts, int64_t R,
                               const int32_t* inv, int T, int E, int k, int kp, float rs, float* dlogits,
                               cudaStream_t st);

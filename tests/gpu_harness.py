@@ -27,7 +27,7 @@ _WCACHE = {}
 
 
 def weights_for(s, seed, dev):
-    key = (s.name, s.H, s.I, s.E, s.n_shared, s.wfmt, seed)
+    key = (s.name, s.H, s.I, s.E, s.n_shared, s.wfmt, s.act == "srelu", getattr(s, "bias", False), seed)
     if key not in _WCACHE:
         _WCACHE.clear()
         torch.cuda.empty_cache()

@@ -90,8 +90,8 @@ def test_host_errors_enqueue_nothing(lib):
     assert lib.moe_layer_forward(ctypes.byref(c), 0x1000, 0x1000, None, 17, 0x3000, 0x4000, None, 0x5000,
                                  None) == 1               # T > T_max
     assert lib.moe_combine(ctypes.byref(c), None, P(0x1000), None, 4, P(0x2000), None) == 1
-    assert lib.moe_layer_backward(ctypes.byref(c), 0x10, 0x10, 4, None, 0x10, 0x10, 0x10, 0x10, 0x10, 0x10,
-                                  None) == 2              # NVFP4 config: backward unsupported
+    assert lib.moe_layer_backward(ctypes.byref(c), 0x10, 0x10, 4, None, 0x10, 0x10, 0x10, 0x10, 0x10, None,
+                                  0x10, None) == 2        # NVFP4 config: backward unsupported
     assert m.moe_status_string(0) == "ok"
 
 
@@ -158,8 +158,8 @@ def test_flag_wait_host_errors(lib):
 
 def test_w1_bias_host_rules(lib):
     """w1_bias is 0 or 1; it enlarges the forward pack by G * 2I fp32 and
-    leaves the dgrad pack alone; the backward refuses a biased config
-    (forward only) before touching any pointer."""
+    leaves the dgrad pack alone; the backward of a biased config requires
+    the db1 output, and an unbiased one refuses it, before any device work."""
     import ctypes
     from quantized_grouped_gemm_topk_gb300 import binding as m
     c0 = _cfg(wfmt="mxfp8")
@@ -172,20 +172,26 @@ def test_w1_bias_host_rules(lib):
     assert m.moe_packed_weights_size(c1, m.MOE_PACK_DGRAD) == m.moe_packed_weights_size(c0, m.MOE_PACK_DGRAD)
     fake = ctypes.c_void_p(4096)
     L = m.load()
-    assert L.moe_layer_backward(ctypes.byref(c1), fake, fake, 16, None, fake, fake, fake, fake, fake, fake,
-                                None) == 2
+    save = m.moe_train_save_t(4096, 4096, 4096, 4096, 4096, 4096, None)
+    by = ctypes.byref
+    assert L.moe_layer_backward(by(c1), fake, fake, 16, by(save), fake, fake, fake, fake, fake, None, fake,
+                                None) == 1                 # bias: db1 required
+    assert L.moe_layer_backward(by(c0), fake, fake, 16, by(save), fake, fake, fake, fake, fake, fake, fake,
+                                None) == 1                 # no bias: no db1
 
 
 def test_srelu_host_rules(lib):
     """sReLU: valid; its W1 pack holds I rows (a smaller blob than the gated
-    W1's 2I); no dgrad pack, no bias, no fused layer."""
+    W1's 2I), and so does its dgrad pack's W1 copy (K = I); no bias, no
+    fused layer."""
     from quantized_grouped_gemm_topk_gb300 import binding as m
     g = _cfg(wfmt="mxfp8")
     c = _cfg(wfmt="mxfp8", act="srelu")
     assert m.moe_config_validate(c) == 0
     assert m.moe_packed_weights_size(c) < m.moe_packed_weights_size(g)
+    assert 0 < m.moe_packed_weights_size(c, m.MOE_PACK_DGRAD) < m.moe_packed_weights_size(g, m.MOE_PACK_DGRAD)
     with pytest.raises(m.MoEError):
-        m.moe_packed_weights_size(c, m.MOE_PACK_DGRAD)
+        m.moe_packed_weights_size(_cfg(act="srelu"), m.MOE_PACK_DGRAD)   # NVFP4: no dgrad copy
     assert m.moe_config_validate(_cfg(act="srelu", bias=True)) == 2
     assert not m.moe_layer_fused(_cfg(act="srelu"), 1)
 

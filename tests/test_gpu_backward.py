@@ -21,16 +21,16 @@ from util import assert_close_layer, assert_mx_close, cuda_device, np_
 pytestmark = pytest.mark.gpu
 
 
-def _run_backward(s, r, T, seed=0):
+def _run_backward(s, r, T, seed=0, db1=None):
     dev = r["x"].device
     cfg = r["cfg"]
     dout = inputs.gen_dout(s, seed, device=dev, T=T)
     packed_d = m.moe_prepack_weights(cfg, r["wts"], m.MOE_PACK_DGRAD)
     dx = torch.empty(T, s.H, dtype=torch.bfloat16, device=dev)
-    dW1 = torch.empty(s.E, s.H, 2 * s.I, dtype=torch.bfloat16, device=dev)
+    dW1 = torch.empty(s.E, s.H, s.I if s.act == "srelu" else 2 * s.I, dtype=torch.bfloat16, device=dev)
     dW2 = torch.empty(s.E, s.I, s.H, dtype=torch.bfloat16, device=dev)
     dlog = torch.empty(T, s.E, dtype=torch.float32, device=dev)
-    m.moe_layer_backward(cfg, dout, r["x"], T, r["save"], packed_d, dx, dW1, dW2, dlog, r["ws"])
+    m.moe_layer_backward(cfg, dout, r["x"], T, r["save"], packed_d, dx, dW1, dW2, dlog, r["ws"], db1=db1)
     torch.cuda.synchronize()
     assert m.moe_read_status(cfg, r["ws"]) == 0
     return dout, dx, dW1, dW2, dlog
@@ -52,7 +52,7 @@ def _oracle_backward(s, r, f, dout, experts=None):
                             quant=True, experts=experts, w1t=w1t, w2t=w2t)
 
 
-@pytest.mark.parametrize("act", ["swiglu_clamp", "geglu"])
+@pytest.mark.parametrize("act", ["swiglu_clamp", "geglu", "srelu"])
 def test_train_reduced_full_check(act):
     dev = cuda_device()
     s = inputs.workload("train", T=48, E=8, act=act)
@@ -159,3 +159,26 @@ def test_train_saved_transposed_x_bit_exact(T, E):
         q, sc = F.mx_quantize(rows.T)
         assert np.array_equal(at_q[:, poff[e]: poff[e + 1]], q), f"at_q of expert {e}"
         assert np.array_equal(at_s[:, poff[e] // 32: poff[e + 1] // 32], sc), f"at_s of expert {e}"
+
+
+@pytest.mark.parametrize("act,T", [("swiglu_clamp", 48), ("geglu", 300)])
+def test_train_w1_bias(act, T):
+    """Training with a W1 bias (gate b, up c): the forward adds it before the
+    activation (saved h includes it), the backward's gradients match the
+    oracle's, and db1 (the sum of dh over each group's rows, from the
+    dActivation epilogue's per-32-row column sums) matches the oracle's db1.
+    T = 300 over 8 experts spans several 128-row tiles per group."""
+    dev = cuda_device()
+    s = inputs.workload("train", T=T, E=8, act=act, bias=True)
+    r = run_forward(s, s.T, dev=dev, save=True)
+    assert r["status"] == 0
+    f = oracle_forward(s, r)
+    assert_close_layer(np_(r["out"].float()), f.out, "out")
+    db1 = torch.full((s.E, 2 * s.I), float("nan"), dtype=torch.float32, device=dev)
+    dout, dx, dW1, dW2, dlog = _run_backward(s, r, s.T, db1=db1)
+    b = _oracle_backward(s, r, f, dout)
+    assert_close_layer(np_(dx.float()), b.dx, "dx")
+    assert_close_layer(np_(dW1.float()), b.dW1, "dW1")
+    assert_close_layer(np_(dW2.float()), b.dW2, "dW2")
+    assert_close_layer(np_(dlog), b.dlogits, "dlogits")
+    assert_close_layer(np_(db1), b.db1, "db1")
