@@ -829,6 +829,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-config", action="store_true", help="headline workload only")
     ap.add_argument("--E", type=int, default=0, help="override the expert count (small profiling cases)")
+    ap.add_argument("--wfmt", default="", choices=["", "nvfp4", "mxfp8", "mxfp4"],
+                    help="override the weight format of the headline loop (profiling cases)")
     ap.add_argument("--only", default="", choices=["", "shared", "mxfp4", "skewed", "train", "partition"],
                     help="run one workload of the per-config block alone (profiling)")
     ap.add_argument("--train-T", type=int, default=0, help="training tokens for --only train")
@@ -838,9 +840,12 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    s = inputs.workload(args.workload)
+    over = {}
     if args.E:
-        s = inputs.workload(args.workload, E=args.E)
+        over["E"] = args.E
+    if args.wfmt:
+        over["wfmt"] = args.wfmt
+    s = inputs.workload(args.workload, **over)
     if args.impl == "reference":
         run_reference(args, s, rank, world)
         return

@@ -193,13 +193,15 @@ def test_geglu_forward(name):
     assert_close_layer(np_(r["out"].float()), f.out, "out")
 
 
-@pytest.mark.parametrize("T", [16, 1, 33])
-def test_mxfp4_tiny_forward(T):
+@pytest.mark.parametrize("T,logits", [(16, "router"), (1, "router"), (33, "router"), (64, "zipf"),
+                                      (400, "router")])
+def test_mxfp4_tiny_forward(T, logits):
     """MXFP4 weights (E2M1 elements, E8M0 scale per 32 along K) through the
     block-scaled GEMM with E2M1 as the weight operand: every output against
-    the oracle, ragged token counts included."""
+    the oracle, ragged token counts included; the Zipf-skewed T = 64 gives
+    uneven groups, T = 400 groups of about 100 rows."""
     dev = cuda_device()
-    s = inputs.workload("tiny", T=T, wfmt="mxfp4")
+    s = inputs.workload("tiny", T=T, wfmt="mxfp4", logits=logits)
     r = run_forward(s, T, dev=dev, seed=5)
     assert r["status"] == 0
     f = oracle_forward(s, r)
