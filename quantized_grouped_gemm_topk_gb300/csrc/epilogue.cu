@@ -242,13 +242,6 @@ constexpr int kQcRowBytes = kQcCols * 2;
 constexpr int kQcTileBytes = kQcRows * kQcRowBytes;
 constexpr int kQcSmem = kQcStages * kQcTileBytes + kQcMaxRb * kQcRows * 4;
 
-__device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, bool ok) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(ok ? 16 : 0) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
-
 // Elementwise max of |a| and |b| over the two bf16 halves; the result's sign
 // bits are those of a xor b (callers mask them off). A NaN half yields the
 // other input's half.

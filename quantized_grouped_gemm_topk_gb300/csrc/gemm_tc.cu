@@ -373,26 +373,54 @@ __device__ __forceinline__ int box_index(int nv) {
 // the largest block exponent of the row (unbiased), so the product of the
 // two is the MXFP8 value exactly unless a block sits more than 15 binades
 // below the row's largest block (then bits below 2^-24 of the row scale are
-// rounded away). One warp per (row, 256-column slice); every warp derives the
-// row exponent from the row's scale bytes itself.
+// rounded away). One warp per (row, kActSlice-column slice); every warp
+// derives the row exponent from the row's scale bytes itself. After the
+// row index, every load of an item (the slice's codes, their block scales
+// and the row's scale bytes) is issued before any is used, so an item costs
+// two memory round trips.
 // ---------------------------------------------------------------------------
+constexpr int kActSlice = 2048;            // 8 chunks of 8 columns per lane
+
 __device__ __forceinline__ void act_f16_item(const uint8_t* __restrict__ q, const uint8_t* __restrict__ s, int C,
                                              const int32_t* __restrict__ row_map, int row_div, int64_t r, int sl,
                                              uint16_t* __restrict__ a16, int32_t* __restrict__ rowexp, int lane) {
   const int nb = C / 32;
   const int64_t src = row_map ? (int64_t)(row_map[r] / row_div) : r;
   const uint8_t* sr = s + src * nb;
+  const uint8_t* qr = q + src * C;
+  uint2 codes[8];
+  int bs[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int c0 = sl * kActSlice + j * 256 + lane * 8;
+    codes[j] = make_uint2(0u, 0u);
+    bs[j] = 0;
+    if (c0 < C) {
+      codes[j] = *reinterpret_cast<const uint2*>(qr + c0);
+      bs[j] = sr[c0 / 32];
+    }
+  }
   int mx = 0;
-  for (int b = lane; b < nb; b += 32) mx = max(mx, (int)sr[b]);
+  for (int b0 = 0; b0 < nb; b0 += 256) {
+    int sv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int b = b0 + lane + 32 * i;
+      sv[i] = b < nb ? (int)sr[b] : 0;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) mx = max(mx, sv[i]);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(kFull, mx, o));
   if (sl == 0 && lane == 0) rowexp[r] = mx - 127;
-  const int c0 = sl * 256 + lane * 8;
-  if (c0 < C) {
-    const uint2 codes = *reinterpret_cast<const uint2*>(q + src * C + c0);
-    const float f = ldexpf(1.0f, (int)sr[c0 / 32] - mx);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int c0 = sl * kActSlice + j * 256 + lane * 8;
+    if (c0 >= C) break;
+    const float f = ldexpf(1.0f, bs[j] - mx);
     uint32_t outw[4];
-    const uint32_t cw[2] = {codes.x, codes.y};
+    const uint32_t cw[2] = {codes[j].x, codes[j].y};
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
       const float2 lo = e4m3x2_to_f32x2((uint16_t)(cw[i] & 0xffffu));
@@ -413,7 +441,7 @@ __device__ __forceinline__ void act_f16_item(const uint8_t* __restrict__ q, cons
 __device__ void fill_ring(const TcArgs& g) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
   const int C = g.m[0].K;
-  const int nsl = (C + 255) / 256;
+  const int nsl = (C + kActSlice - 1) / kActSlice;
   const int ntouch = *g.n_touched;
   int32_t* ring = g.f.cnt + 2 * g.G;
   for (int ti = blockIdx.x; ti < ntouch; ti += g.f.n_disp) {
@@ -951,7 +979,7 @@ __global__ void __launch_bounds__(256) k_act_f16(const uint8_t* __restrict__ q, 
     zero[i] = 0;
   const int lane = threadIdx.x & 31;
   const int Rv = min(R, offsets[G]);
-  const int nsl = (C + 255) / 256;
+  const int nsl = (C + kActSlice - 1) / kActSlice;
   const int64_t total = (int64_t)Rv * nsl;
   const int64_t nw = (int64_t)gridDim.x * (blockDim.x / 32);
   for (int64_t wi = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5); wi < total; wi += nw)
@@ -978,9 +1006,9 @@ cudaError_t launch_act_f16(const uint8_t* q, const uint8_t* s, int C, const int3
                            int32_t* zero, int64_t nzero) {
   if (R == 0) return cudaSuccess;
   if (!zero) nzero = 0;
-  const int64_t warps = (int64_t)R * ((C + 255) / 256);
+  const int64_t warps = (int64_t)R * ((C + kActSlice - 1) / kActSlice);
   const int64_t work = std::max<int64_t>((warps + 7) / 8, (nzero + 255) / 256);
-  const int blocks = (int)std::min<int64_t>(work, (int64_t)device_sms() * 16);
+  const int blocks = (int)std::min<int64_t>(work, (int64_t)device_sms() * 8);   // one wave
   cudaError_t e = launch_pdl(k_act_f16, dim3(blocks), dim3(256), 0, st, q, s, C, row_map, row_div, R, offsets, G,
                              a16, rowexp, zero, nzero);
   note_launch();

@@ -21,84 +21,96 @@ namespace moe {
 // S1: logits partials, a register-tiled fp32 GEMM over one slice of H.
 // grid (ceil(T/TT), ceil(E/64), KS), block 256: thread (tx = tid % 16,
 // ty = tid / 16) owns experts 4tx..4tx+3 and tokens ty*TT/16.. of the
-// CTA's 64-expert x TT-token tile. Per 64-row step of H both operands are
-// staged in shared memory (x transposed to [h][token]), so each pair of
-// shared loads feeds 4 * TT/16 FMAs. Every thread accumulates its h in
-// increasing order. part[ks][t][e] = sum over the ks-th slice of H of
-// x[t][h] * W_r[h][e].
+// CTA's 64-expert x TT-token tile. The slice [h0, h1) (multiples of 8 rows)
+// moves through shared memory in 128-row chunks by cp.async, two chunks in
+// flight: a chunk's W rows (fp32) and x columns (bf16, as stored) are all
+// requested at once, so a decode-sized slice of one chunk costs one memory
+// round trip instead of one per load wave (W_r is streamed once; at decode
+// the latency of the copies, not the FLOPs, sets the time). Every thread
+// accumulates its h in increasing order: part[ks][t][e] = sum over the
+// ks-th slice of H of x[t][h] * W_r[h][e].
 // ---------------------------------------------------------------------------
-constexpr int kRtKH = 64;
+constexpr int kRtKH = 128;                 // rows of H per chunk
+constexpr int kRtXLd = kRtKH + 8;          // x row stride in shared memory (bf16; keeps 16-byte pieces aligned)
 
-// Loads one 64-row x 64-expert W tile (4 float4 per thread) into registers;
-// rows past hn and experts past E read as zero.
-__device__ __forceinline__ void router_load_w(const float* __restrict__ Wr, int hb, int hn, int e0, int E,
-                                              float4 (&w)[4]) {
-#pragma unroll
-  for (int r = 0; r < 4; ++r) {
-    const int i = threadIdx.x + r * 256;
-    const int hh = i >> 4, c = (i & 15) * 4;
-    w[r] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (hh < hn) {
-      const float* src = Wr + (int64_t)(hb + hh) * E + e0 + c;
-      if (e0 + c + 3 < E && (E & 3) == 0) {
-        w[r] = __ldg(reinterpret_cast<const float4*>(src));
-      } else {
-        if (e0 + c + 0 < E) w[r].x = __ldg(src + 0);
-        if (e0 + c + 1 < E) w[r].y = __ldg(src + 1);
-        if (e0 + c + 2 < E) w[r].z = __ldg(src + 2);
-        if (e0 + c + 3 < E) w[r].w = __ldg(src + 3);
-      }
-    }
-  }
+template <int TT>
+constexpr int router_stage_bytes() { return kRtKH * 64 * 4 + TT * kRtXLd * 2; }
+template <int TT>
+constexpr int router_smem() { return 2 * router_stage_bytes<TT>(); }
+
+// Slice ks of KS over H, in units of 8 rows (H is a multiple of 64).
+__host__ __device__ __forceinline__ int router_slice_begin(int ks, int KS, int H) {
+  return 8 * (int)((int64_t)ks * (H / 8) / KS);
 }
 
-// One CTA: TT tokens x 64 experts over the H slice [h0, h1). The next 64-row
-// W tile is loaded into registers while the current one is multiplied, so a
-// CTA keeps its loads in flight instead of paying one DRAM round trip per
-// tile (W_r is streamed once; at decode the CTA count, not the FLOPs, sets
-// the time).
+// Requests chunk [hb, hb + hn) of the CTA's W columns e0..e0+63 and token
+// rows t0..t0+TT-1 of x into stage buffers ws / xs (zero-filled outside the
+// chunk, the experts and the tokens) and commits them as one group.
+template <int TT>
+__device__ __forceinline__ void router_issue(const uint16_t* __restrict__ x, const float* __restrict__ Wr, int T,
+                                             int H, int E, int t0, int e0, int hb, int hn, float* ws,
+                                             uint16_t* xs) {
+  const uint32_t wsb = (uint32_t)__cvta_generic_to_shared(ws);
+  const uint32_t xsb = (uint32_t)__cvta_generic_to_shared(xs);
+  if ((E & 3) == 0) {
+    for (int i = threadIdx.x; i < kRtKH * 16; i += 256) {       // 16 pieces of 4 experts a row
+      const int r = i >> 4, c = (i & 15) * 4;
+      const bool ok = r < hn && e0 + c < E;
+      cp_async16_zfill(wsb + (uint32_t)(r * 64 + c) * 4u, ok ? Wr + (int64_t)(hb + r) * E + e0 + c : Wr, ok);
+    }
+  } else {
+    for (int i = threadIdx.x; i < kRtKH * 64; i += 256) {       // rows not 16-byte aligned: one float at a time
+      const int r = i >> 6, c = i & 63;
+      const bool ok = r < hn && e0 + c < E;
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(wsb + (uint32_t)(r * 64 + c) * 4u),
+                   "l"(ok ? Wr + (int64_t)(hb + r) * E + e0 + c : Wr), "r"(ok ? 4 : 0)
+                   : "memory");
+    }
+  }
+  for (int i = threadIdx.x; i < TT * (kRtKH / 8); i += 256) {  // 8 bf16 of one token a piece
+    const int tt = i / (kRtKH / 8), c = (i % (kRtKH / 8)) * 8;
+    const bool ok = t0 + tt < T && c < hn;
+    cp_async16_zfill(xsb + (uint32_t)(tt * kRtXLd + c) * 2u, ok ? x + (int64_t)(t0 + tt) * H + hb + c : x, ok);
+  }
+  cp_async_commit();
+}
+
 template <int TT>
 __global__ void __launch_bounds__(256) k_router_partial(const uint16_t* __restrict__ x,
                                                         const float* __restrict__ Wr, int T, int H, int E,
                                                         int KS, float* __restrict__ part) {
+  extern __shared__ __align__(16) uint8_t rsm[];
   pdl_enter();
   constexpr int TPT = TT / 16;                     // tokens per thread
-  __shared__ __align__(16) float ws_[kRtKH][64];
-  __shared__ __align__(16) float xs_[kRtKH][TT + 1];   // +1: conflict-free transposed stores
   const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
   const int t0 = blockIdx.x * TT;
   const int e0 = blockIdx.y * 64;
   const int ks = blockIdx.z;
-  const int h0 = (int)((int64_t)ks * H / KS), h1 = (int)((int64_t)(ks + 1) * H / KS);
+  const int h0 = router_slice_begin(ks, KS, H), h1 = router_slice_begin(ks + 1, KS, H);
+  const int nch = (h1 - h0 + kRtKH - 1) / kRtKH;
+  auto wbuf = [&](int b) { return reinterpret_cast<float*>(rsm + b * router_stage_bytes<TT>()); };
+  auto xbuf = [&](int b) {
+    return reinterpret_cast<uint16_t*>(rsm + b * router_stage_bytes<TT>() + kRtKH * 64 * 4);
+  };
   float acc[TPT][4];
 #pragma unroll
   for (int i = 0; i < TPT; ++i)
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-  float4 wn[4];
-  router_load_w(Wr, h0, min(kRtKH, h1 - h0), e0, E, wn);
-  for (int hb = h0; hb < h1; hb += kRtKH) {
-    const int hn = min(kRtKH, h1 - hb);
-    __syncthreads();
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      const int i = threadIdx.x + r * 256;
-      *reinterpret_cast<float4*>(&ws_[i >> 4][(i & 15) * 4]) = wn[r];
-    }
-    for (int i = threadIdx.x; i < TT * kRtKH; i += 256) {       // x tile, transposed
-      const int tt = i / kRtKH, hh = i % kRtKH;
-      float v = 0.f;
-      if (t0 + tt < T && hh < hn) v = bf16_bits_to_f32(x[(int64_t)(t0 + tt) * H + hb + hh]);
-      xs_[hh][tt] = v;
-    }
-    __syncthreads();
-    if (hb + kRtKH < h1) router_load_w(Wr, hb + kRtKH, min(kRtKH, h1 - hb - kRtKH), e0, E, wn);
+  for (int c = 0; c < min(nch, 2); ++c)
+    router_issue<TT>(x, Wr, T, H, E, t0, e0, h0 + c * kRtKH, min(kRtKH, h1 - h0 - c * kRtKH), wbuf(c), xbuf(c));
+  for (int c = 0; c < nch; ++c) {
+    if (c + 1 < nch) cp_async_wait<1>();
+    else cp_async_wait<0>();
+    __syncthreads();                               // chunk c has landed for every thread
+    const float* ws = wbuf(c & 1);
+    const uint16_t* xs = xbuf(c & 1);
 #pragma unroll 8
     for (int hh = 0; hh < kRtKH; ++hh) {
-      const float4 w = *reinterpret_cast<const float4*>(&ws_[hh][tx * 4]);
+      const float4 w = *reinterpret_cast<const float4*>(&ws[hh * 64 + tx * 4]);
       float a[TPT];
 #pragma unroll
-      for (int i = 0; i < TPT; ++i) a[i] = xs_[hh][ty * TPT + i];
+      for (int i = 0; i < TPT; ++i) a[i] = bf16_bits_to_f32(xs[(ty * TPT + i) * kRtXLd + hh]);
 #pragma unroll
       for (int i = 0; i < TPT; ++i) {
         acc[i][0] = fmaf(a[i], w.x, acc[i][0]);
@@ -107,6 +119,10 @@ __global__ void __launch_bounds__(256) k_router_partial(const uint16_t* __restri
         acc[i][3] = fmaf(a[i], w.w, acc[i][3]);
       }
     }
+    __syncthreads();                               // every thread is done with stage c & 1
+    if (c + 2 < nch)
+      router_issue<TT>(x, Wr, T, H, E, t0, e0, h0 + (c + 2) * kRtKH, min(kRtKH, h1 - h0 - (c + 2) * kRtKH),
+                       wbuf(c & 1), xbuf(c & 1));
   }
 #pragma unroll
   for (int i = 0; i < TPT; ++i) {
@@ -117,6 +133,106 @@ __global__ void __launch_bounds__(256) k_router_partial(const uint16_t* __restri
       const int e = e0 + tx * 4 + j;
       if (e < E) part[((int64_t)ks * T + t) * E + e] = acc[i][j];
     }
+  }
+}
+
+// S1 at decode sizes (T <= 32, E a multiple of 4): one CTA per 64 experts x
+// one slice of H, about one CTA per SM. The CTA's W rows go straight into
+// registers, thread (tx = tid % 16, ty = tid / 16) holding experts
+// 4tx..4tx+3 of rows ty, ty + 16, ..., ty + 176 of a 192-row chunk, every
+// load of the chunk in flight at once; x comes in transposed to [h][token]
+// through shared memory. Each W element is read from memory once and feeds
+// all TT tokens from registers, so at T = 1 the kernel costs one memory
+// round trip and at T = 32 it stays FMA-bound rather than bound by shared
+// memory. Per logit: each thread's fmaf chain over its rows (increasing h),
+// the two row groups of a warp added (lane l and l ^ 16), then the 8 warps'
+// sums added in warp order; a fixed order, so the result is deterministic.
+constexpr int kRrRPT = 12;                 // rows of a chunk per thread
+constexpr int kRrRows = 16 * kRrRPT;       // 192 rows of H per chunk
+
+static bool router_rows(int T, int E) { return T <= 32 && E % 4 == 0; }
+
+template <int TT>
+constexpr int router_rows_smem() { return kRrRows * TT * 2 + 8 * TT * 64 * 4; }
+
+template <int TT>
+__global__ void __launch_bounds__(256, 1) k_router_rows(const uint16_t* __restrict__ x, const float* __restrict__ Wr,
+                                                        int T, int H, int E, int KS, float* __restrict__ part) {
+  extern __shared__ __align__(16) uint8_t rsm[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(rsm);                     // [kRrRows][TT] bf16
+  float* red = reinterpret_cast<float*>(rsm + kRrRows * TT * 2);       // [8][TT][64]
+  pdl_enter();
+  const int tx = threadIdx.x & 15, ty = threadIdx.x >> 4;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int e0 = blockIdx.x * 64, ks = blockIdx.y;
+  const int h0 = router_slice_begin(ks, KS, H), h1 = router_slice_begin(ks + 1, KS, H);
+  const bool ecol = e0 + tx * 4 < E;
+  float acc[TT][4];
+#pragma unroll
+  for (int t = 0; t < TT; ++t)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[t][j] = 0.f;
+  for (int hb = h0; hb < h1; hb += kRrRows) {
+    const int hn = min(kRrRows, h1 - hb);
+    float4 w[kRrRPT];
+#pragma unroll
+    for (int r = 0; r < kRrRPT; ++r) {
+      const int row = ty + 16 * r;
+      w[r] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (row < hn && ecol) w[r] = __ldg(reinterpret_cast<const float4*>(Wr + (int64_t)(hb + row) * E + e0 + tx * 4));
+    }
+    if (hb != h0) __syncthreads();                 // every thread is done with the previous chunk's x
+    for (int i = threadIdx.x; i < TT * (kRrRows / 8); i += 256) {
+      const int t = i / (kRrRows / 8), c = (i % (kRrRows / 8)) * 8;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);        // tokens past T and rows past the slice read as zero
+      if (t < T && c < hn) v = __ldg(reinterpret_cast<const uint4*>(x + (int64_t)t * H + hb + c));
+      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        xs[(c + 2 * j) * TT + t] = (uint16_t)(wd[j] & 0xffffu);
+        xs[(c + 2 * j + 1) * TT + t] = (uint16_t)(wd[j] >> 16);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int r = 0; r < kRrRPT; ++r) {
+      const uint4* xr = reinterpret_cast<const uint4*>(xs + (ty + 16 * r) * TT);
+#pragma unroll
+      for (int q = 0; q < TT / 8; ++q) {
+        const uint4 xv = xr[q];
+        const uint32_t wd[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          const float a0 = __uint_as_float(wd[p] << 16), a1 = __uint_as_float(wd[p] & 0xffff0000u);
+          float* c0 = acc[q * 8 + 2 * p];
+          float* c1 = acc[q * 8 + 2 * p + 1];
+          c0[0] = fmaf(a0, w[r].x, c0[0]); c0[1] = fmaf(a0, w[r].y, c0[1]);
+          c0[2] = fmaf(a0, w[r].z, c0[2]); c0[3] = fmaf(a0, w[r].w, c0[3]);
+          c1[0] = fmaf(a1, w[r].x, c1[0]); c1[1] = fmaf(a1, w[r].y, c1[1]);
+          c1[2] = fmaf(a1, w[r].z, c1[2]); c1[3] = fmaf(a1, w[r].w, c1[3]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < TT; ++t)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[t][j] += __shfl_xor_sync(kFull, acc[t][j], 16);
+  if (lane < 16) {
+#pragma unroll
+    for (int t = 0; t < TT; ++t)
+      if (t < T)
+        *reinterpret_cast<float4*>(&red[(warp * TT + t) * 64 + tx * 4]) =
+            make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
+  }
+  __syncthreads();
+  for (int o = threadIdx.x; o < T * 64; o += 256) {
+    const int t = o >> 6, e = o & 63;
+    if (e0 + e >= E) continue;
+    float v = red[t * 64 + e];
+#pragma unroll
+    for (int q = 1; q < 8; ++q) v += red[(q * TT + t) * 64 + e];
+    part[((int64_t)ks * T + t) * E + e0 + e] = v;
   }
 }
 
@@ -213,73 +329,174 @@ __global__ void __launch_bounds__(256) k_router_big(const uint16_t* __restrict__
   }
 }
 
-// Sum over ks of part[ks * n + i], in ks order, with 8 loads in flight.
+// ---------------------------------------------------------------------------
+// S2: one warp routes one token. Logits are first summed over the KS
+// partials in ks order and written out (or taken as given from row_src);
+// then k rounds of a warp arg-max on (value desc, id asc). NaN logits rank
+// below every number and raise MOE_DEV_NAN_LOGIT. Weights: softmax over the
+// selected logits x scale.
+//
+// The arg-max runs on order-preserving integer keys: a larger logit has a
+// larger key, -0 and +0 share one (they compare equal), and -inf (NaN) is
+// above 0, the key of an expert that is taken or out of range. Each lane
+// keeps its best untaken expert (the lowest id among equal keys: its ids
+// grow with i), the warp's largest key comes from one redux.sync max, and
+// the lowest id holding it from one redux.sync min, so a round costs two
+// warp reductions instead of five shuffle-and-compare steps.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  const uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+// S1 between the two (T > 32, E a multiple of 4, too few 64 x 128 tiles to
+// fill the SMs): the same tile and thread layout as k_router_big, split
+// along H into KS slices of whole 16-row stages (part[ks][t][e]), with both
+// operands moving through a kRmStages-deep cp.async ring so that several
+// stages of W are in flight while one is multiplied (one stage ahead, the
+// tile waited on memory every stage). x stays bf16 in shared memory,
+// [token][h] with a 48-byte row; a thread reads two h of each of its 4
+// tokens in one 32-bit load. Each logit is its fmaf chain over the slice in
+// increasing h.
+constexpr int kRmStages = 6;
+constexpr int kRmXLd = 24;                                   // bf16 per x row in shared memory
+constexpr int kRmWBytes = kRbKH * kRbTE * 4;                 // 8 KB
+constexpr int kRmStage = kRmWBytes + kRbTT * kRmXLd * 2;     // + 3 KB of x
+constexpr int kRmSmem = kRmStages * kRmStage;
+
+static bool router_mid(int T, int H, int E) { return T > 32 && E % 4 == 0 && H % kRbKH == 0 && !router_big(T, H, E); }
+
+__global__ void __launch_bounds__(256) k_router_mid(const uint16_t* __restrict__ x, const float* __restrict__ Wr,
+                                                    int T, int H, int E, int KS, float* __restrict__ part) {
+  extern __shared__ __align__(16) uint8_t rsm[];
+  pdl_enter();
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int t0 = blockIdx.x * kRbTT, e0 = blockIdx.y * kRbTE, ks = blockIdx.z;
+  const int u0 = (int)((int64_t)ks * (H / kRbKH) / KS), u1 = (int)((int64_t)(ks + 1) * (H / kRbKH) / KS);
+  const int nk = u1 - u0;                                    // 16-row stages of this slice
+  const uint32_t sbase = (uint32_t)__cvta_generic_to_shared(rsm);
+  auto issue = [&](int kb) {
+    if (kb < nk) {
+      const int hb = (u0 + kb) * kRbKH;
+      const uint32_t st = sbase + (uint32_t)((kb % kRmStages) * kRmStage);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {                          // W: 16 rows x 32 pieces of 4 experts
+        const int i = tid + 256 * j, r = i >> 5, c = (i & 31) * 4;
+        const bool ok = e0 + c < E;
+        cp_async16_zfill(st + (uint32_t)(r * kRbTE + c) * 4u, ok ? Wr + (int64_t)(hb + r) * E + e0 + c : Wr, ok);
+      }
+      if (tid < 2 * kRbTT) {                                 // x: 64 tokens x 2 pieces of 8 h
+        const int tt = tid >> 1, c = (tid & 1) * 8;
+        const bool ok = t0 + tt < T;
+        cp_async16_zfill(st + kRmWBytes + (uint32_t)(tt * kRmXLd + c) * 2u, ok ? x + (int64_t)(t0 + tt) * H + hb + c : x,
+                         ok);
+      }
+    }
+    cp_async_commit();                                       // an empty group past the end keeps the count uniform
+  };
+  float acc[4][8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+#pragma unroll
+  for (int kb = 0; kb < kRmStages - 1; ++kb) issue(kb);
+  for (int kb = 0; kb < nk; ++kb) {
+    cp_async_wait<kRmStages - 2>();
+    __syncthreads();                                         // stage kb landed; stage kb - 1 is free
+    issue(kb + kRmStages - 1);
+    const float* ws = reinterpret_cast<const float*>(rsm + (kb % kRmStages) * kRmStage);
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(rsm + (kb % kRmStages) * kRmStage + kRmWBytes);
+#pragma unroll
+    for (int hh = 0; hh < kRbKH; hh += 2) {
+      float a[2][4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(&xs[(ty * 4 + i) * kRmXLd + hh]);
+        a[0][i] = __uint_as_float(v << 16);
+        a[1][i] = __uint_as_float(v & 0xffff0000u);
+      }
+#pragma unroll
+      for (int d = 0; d < 2; ++d) {
+        const float4 w0 = *reinterpret_cast<const float4*>(&ws[(hh + d) * kRbTE + tx * 4]);
+        const float4 w1 = *reinterpret_cast<const float4*>(&ws[(hh + d) * kRbTE + 64 + tx * 4]);
+        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[d][i], wv[j], acc[i][j]);
+      }
+    }
+  }
+  cp_async_wait<0>();
+  float* out = part + (int64_t)ks * T * E;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = t0 + ty * 4 + i;
+    if (t >= T) continue;
+    float* row = out + (int64_t)t * E;
+    if (e0 + tx * 4 < E)
+      *reinterpret_cast<float4*>(row + e0 + tx * 4) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+    if (e0 + 64 + tx * 4 < E)
+      *reinterpret_cast<float4*>(row + e0 + 64 + tx * 4) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+  }
+}
+
+// Sum over ks of part[ks * n + i], in ks order, 16 loads in flight at a
+// time (the tail's loads predicated, not serialised).
 __device__ __forceinline__ float sum_partials(const float* __restrict__ part, int KS, int64_t n, int64_t i) {
   float v = 0.f;
-  int ks = 0;
-  for (; ks + 8 <= KS; ks += 8) {
-    float t[8];
+  for (int ks = 0; ks < KS; ks += 16) {
+    float t[16];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) t[j] = part[(int64_t)(ks + j) * n + i];
+    for (int j = 0; j < 16; ++j) t[j] = ks + j < KS ? part[(int64_t)(ks + j) * n + i] : 0.f;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) v += t[j];
+    for (int j = 0; j < 16; ++j)
+      if (ks + j < KS) v += t[j];
   }
-  for (; ks < KS; ++ks) v += part[(int64_t)ks * n + i];
   return v;
 }
 
-// ---------------------------------------------------------------------------
-// S2: one warp routes one token. Logits are first summed over the KS
-// partials in ks order and written out; then k rounds of a warp arg-max on
-// (value desc, id asc). NaN logits rank below every number and raise
-// MOE_DEV_NAN_LOGIT. Weights: softmax over the selected logits x scale.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ bool better(float va, int ia, float vb, int ib) {
-  return va > vb || (va == vb && ia < ib);
-}
-
-// VPL: logits per lane kept in registers (E <= 32 * VPL).
+// VPL: logits per lane kept in registers (E <= 32 * VPL). With row_src the
+// token's E logits are read from there (any memory) and not written again.
 template <int VPL>
 __device__ void route_token(int t, int lane, const float* __restrict__ part, int KS, int T, int E, int k,
                             float rs, float* __restrict__ logits, int32_t* __restrict__ ids,
-                            float* __restrict__ wts, int32_t* status) {
+                            float* __restrict__ wts, int32_t* status, const float* row_src = nullptr) {
   bool nan_seen = false;
-  const float* row_in = part + (int64_t)t * E;
+  const float* row_in = row_src ? row_src : part + (int64_t)t * E;
   float* row = logits + (int64_t)t * E;
-  float vals[VPL];
+  uint32_t keys[VPL];
 #pragma unroll (VPL <= 8 ? VPL : 1)
   for (int i = 0; i < VPL; ++i) {
     const int e = lane + 32 * i;
-    float v = -INFINITY;
+    uint32_t key = 0;
     if (e < E) {
-      v = KS == 1 ? row_in[e] : sum_partials(part, KS, (int64_t)T * E, (int64_t)t * E + e);
+      float v = (KS == 1 || row_src) ? row_in[e] : sum_partials(part, KS, (int64_t)T * E, (int64_t)t * E + e);
       if (v != v) nan_seen = true;
-      if (row != row_in) row[e] = v;
+      if (!row_src && row != row_in) row[e] = v;
       if (v != v) v = -INFINITY;
+      key = logit_key(v);
     }
-    vals[i] = v;
+    keys[i] = key;
   }
   if (__any_sync(kFull, nan_seen) && lane == 0) set_status(status, MOE_DEV_NAN_LOGIT);
   uint64_t taken = 0;
   float sel_v = 0.f;    // lane j keeps the j-th selected logit
   int sel_i = 0;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
+    uint32_t bk = 0;
     int bi = 0x7fffffff;
 #pragma unroll (VPL <= 8 ? VPL : 1)
-    for (int i = 0; i < VPL; ++i) {
-      const int e = lane + 32 * i;
-      if (e >= E || (taken >> i & 1ull)) continue;
-      if (better(vals[i], e, bv, bi)) { bv = vals[i]; bi = e; }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      float ov = __shfl_xor_sync(kFull, bv, o);
-      int oi = __shfl_xor_sync(kFull, bi, o);
-      if (better(ov, oi, bv, bi)) { bv = ov; bi = oi; }
-    }
-    if (bi < E && (bi & 31) == lane) taken |= 1ull << (bi >> 5);
-    if (lane == j) { sel_v = bv; sel_i = bi; }
+    for (int i = 0; i < VPL; ++i)
+      if (!(taken >> i & 1ull) && keys[i] > bk) { bk = keys[i]; bi = lane + 32 * i; }
+    const uint32_t mk = __reduce_max_sync(kFull, bk);
+    const int win = (int)__reduce_min_sync(kFull, bk == mk ? (uint32_t)bi : 0xffffffffu);
+    if (win >= 0 && (win & 31) == lane) taken |= 1ull << (win >> 5);
+    if (lane == j) { sel_v = key_logit(mk); sel_i = win; }
   }
   // softmax over the selected logits (lane j holds selection j); the first
   // selection is the maximum.
@@ -557,7 +774,7 @@ __global__ void __launch_bounds__(256) k_quant_rows_bf16(const uint16_t* __restr
 // then the staged router partials when KS > 1.
 // ---------------------------------------------------------------------------
 template <int VPL>
-__global__ void __launch_bounds__(1024) k_route_small(const float* __restrict__ part, int KS, int T, int E, int k,
+__global__ void __launch_bounds__(1024, 1) k_route_small(const float* __restrict__ part, int KS, int T, int E, int k,
                                                       int kp, int G, float rs, int route, float* __restrict__ logits,
                                                       int32_t* ids, float* wts, int32_t* counts, int32_t* offsets,
                                                       int32_t* touched, int32_t* n_touched, int32_t* poff,
@@ -607,13 +824,24 @@ __global__ void __launch_bounds__(1024) k_route_small(const float* __restrict__ 
       __syncthreads();
       for (int i = threadIdx.x; i < n; i += blockDim.x) {
         float v = stg[i];
-        for (int ks = 1; ks < KS; ++ks) v += stg[ks * n + i];
+        int ks = 1;
+        for (; ks + 8 <= KS; ks += 8) {
+          float t8[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) t8[j] = stg[(ks + j) * n + i];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) v += t8[j];
+        }
+        for (; ks < KS; ++ks) v += stg[ks * n + i];
         logits[i] = v;
+        stg[i] = v;                     // the routing below reads the sums from here
       }
       __syncthreads();
-      src = logits;
+      for (int t = warp; t < T; t += 32)
+        route_token<VPL>(t, lane, nullptr, 1, T, E, k, rs, logits, ids, wts, status, stg + (int64_t)t * E);
+    } else {
+      for (int t = warp; t < T; t += 32) route_token<VPL>(t, lane, src, 1, T, E, k, rs, logits, ids, wts, status);
     }
-    for (int t = warp; t < T; t += 32) route_token<VPL>(t, lane, src, 1, T, E, k, rs, logits, ids, wts, status);
   }
   __syncthreads();   // ids / wts written by this block are visible block-wide
   // per-warp segment counts (atomic-free, see warp_count); the histogram is
@@ -656,6 +884,18 @@ static int router_tile(int T) { return T <= 16 ? 16 : 32; }
 // at most 4096 partial rows (KS * T) to sum afterwards.
 int router_splits(int T, int H, int E) {
   if (router_big(T, H, E)) return 1;
+  if (router_mid(T, H, E)) {
+    // at most one CTA per SM, slices of at least 64 rows, KS * T <= 4096
+    const int tiles = ((T + kRbTT - 1) / kRbTT) * ((E + kRbTE - 1) / kRbTE);
+    int ks = std::max(1, std::min(device_sms() / tiles, H / 64));
+    return std::max(1, std::min(ks, 4096 / std::max(T, 1)));
+  }
+  if (router_rows(T, E)) {
+    // about one CTA per SM, slices of at least 64 rows, KS * T <= 4096
+    const int et = (E + 63) / 64;
+    int ks = std::max(1, std::min(device_sms() / et, H / 64));
+    return std::max(1, std::min(ks, 4096 / std::max(T, 1)));
+  }
   const int tiles = ((T + router_tile(T) - 1) / router_tile(T)) * ((E + 63) / 64);
   int ks = (2 * device_sms() + tiles - 1) / std::max(tiles, 1);
   ks = std::max(1, std::min(ks, std::max(1, H / 128)));
@@ -672,10 +912,48 @@ cudaError_t launch_router(const uint16_t* x, const float* Wr, int T, int H, int 
     note_launch();
     return e;
   }
+  if (router_mid(T, H, E)) {
+    static std::atomic<bool> dm[kMaxDevices] = {};
+    cudaError_t e = set_smem_once((const void*)k_router_mid, kRmSmem, dm);
+    if (e == cudaSuccess)
+      e = launch_pdl(k_router_mid, dim3((T + kRbTT - 1) / kRbTT, (E + kRbTE - 1) / kRbTE, KS), dim3(256), kRmSmem, st,
+                     x, Wr, T, H, E, KS, part);
+    note_launch();
+    return e;
+  }
+  if (router_rows(T, E)) {
+    static std::atomic<bool> dr8[kMaxDevices] = {}, dr16[kMaxDevices] = {}, dr32[kMaxDevices] = {};
+    dim3 grid((E + 63) / 64, KS);
+    cudaError_t e;
+    if (T <= 8) {
+      e = set_smem_once((const void*)k_router_rows<8>, router_rows_smem<8>(), dr8);
+      if (e == cudaSuccess)
+        e = launch_pdl(k_router_rows<8>, grid, dim3(256), router_rows_smem<8>(), st, x, Wr, T, H, E, KS, part);
+    } else if (T <= 16) {
+      e = set_smem_once((const void*)k_router_rows<16>, router_rows_smem<16>(), dr16);
+      if (e == cudaSuccess)
+        e = launch_pdl(k_router_rows<16>, grid, dim3(256), router_rows_smem<16>(), st, x, Wr, T, H, E, KS, part);
+    } else {
+      e = set_smem_once((const void*)k_router_rows<32>, router_rows_smem<32>(), dr32);
+      if (e == cudaSuccess)
+        e = launch_pdl(k_router_rows<32>, grid, dim3(256), router_rows_smem<32>(), st, x, Wr, T, H, E, KS, part);
+    }
+    note_launch();
+    return e;
+  }
   const int tt = router_tile(T);
   dim3 grid((T + tt - 1) / tt, (E + 63) / 64, KS);
-  cudaError_t e = tt == 16 ? launch_pdl(k_router_partial<16>, grid, dim3(256), 0, st, x, Wr, T, H, E, KS, part)
-                           : launch_pdl(k_router_partial<32>, grid, dim3(256), 0, st, x, Wr, T, H, E, KS, part);
+  static std::atomic<bool> done16[kMaxDevices] = {}, done32[kMaxDevices] = {};
+  cudaError_t e;
+  if (tt == 16) {
+    e = set_smem_once((const void*)k_router_partial<16>, router_smem<16>(), done16);
+    if (e == cudaSuccess)
+      e = launch_pdl(k_router_partial<16>, grid, dim3(256), router_smem<16>(), st, x, Wr, T, H, E, KS, part);
+  } else {
+    e = set_smem_once((const void*)k_router_partial<32>, router_smem<32>(), done32);
+    if (e == cudaSuccess)
+      e = launch_pdl(k_router_partial<32>, grid, dim3(256), router_smem<32>(), st, x, Wr, T, H, E, KS, part);
+  }
   note_launch();
   return e;
 }
@@ -732,18 +1010,25 @@ cudaError_t launch_route_dispatch(const RouteArgs& a, cudaStream_t st) {
 
 // Router split-K partials -> logits -> top-k, one block per token: its
 // threads sum the partials of the token's experts in ks order (each a
-// handful of independent loads), then its first warp routes the token.
+// handful of independent loads), write the logits out and keep them in
+// shared memory, where its first warp routes the token. (Staging the
+// partials through shared memory with 1024-thread blocks measured slower:
+// 7.7 against 5.4 us a launch for 38 partials x 256 experts.)
 template <int VPL>
 __global__ void __launch_bounds__(256) k_sum_topk(const float* __restrict__ part, int KS, int T, int E, int k,
                                                   float rs, float* __restrict__ logits, int32_t* __restrict__ ids,
                                                   float* __restrict__ wts, int32_t* status) {
+  __shared__ float lg[32 * VPL];
   pdl_enter();
   const int t = blockIdx.x;
   const int64_t n = (int64_t)T * E;
-  for (int e = threadIdx.x; e < E; e += blockDim.x)
-    logits[(int64_t)t * E + e] = sum_partials(part, KS, n, (int64_t)t * E + e);
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    const float v = sum_partials(part, KS, n, (int64_t)t * E + e);
+    logits[(int64_t)t * E + e] = v;
+    lg[e] = v;
+  }
   __syncthreads();
-  if (threadIdx.x < 32) route_token<VPL>(t, threadIdx.x, logits, 1, T, E, k, rs, logits, ids, wts, status);
+  if (threadIdx.x < 32) route_token<VPL>(t, threadIdx.x, nullptr, 1, T, E, k, rs, logits, ids, wts, status, lg);
 }
 
 cudaError_t launch_sum_topk(const float* part, int KS, int T, int E, int k, float rs, float* logits, int32_t* ids,
