@@ -196,6 +196,12 @@ __global__ void __launch_bounds__(256, 1) k_router_rows(const uint16_t* __restri
     __syncthreads();
 #pragma unroll
     for (int r = 0; r < kRrRPT; ++r) {
+      if constexpr (TT == 1) {                     // one token: one x value a row
+        const float a0 = bf16_bits_to_f32(xs[ty + 16 * r]);
+        acc[0][0] = fmaf(a0, w[r].x, acc[0][0]); acc[0][1] = fmaf(a0, w[r].y, acc[0][1]);
+        acc[0][2] = fmaf(a0, w[r].z, acc[0][2]); acc[0][3] = fmaf(a0, w[r].w, acc[0][3]);
+        continue;
+      }
       const uint4* xr = reinterpret_cast<const uint4*>(xs + (ty + 16 * r) * TT);
 #pragma unroll
       for (int q = 0; q < TT / 8; ++q) {
@@ -922,10 +928,14 @@ cudaError_t launch_router(const uint16_t* x, const float* Wr, int T, int H, int 
     return e;
   }
   if (router_rows(T, E)) {
-    static std::atomic<bool> dr8[kMaxDevices] = {}, dr16[kMaxDevices] = {}, dr32[kMaxDevices] = {};
+    static std::atomic<bool> dr1[kMaxDevices] = {}, dr8[kMaxDevices] = {}, dr16[kMaxDevices] = {}, dr32[kMaxDevices] = {};
     dim3 grid((E + 63) / 64, KS);
     cudaError_t e;
-    if (T <= 8) {
+    if (T == 1) {
+      e = set_smem_once((const void*)k_router_rows<1>, router_rows_smem<1>(), dr1);
+      if (e == cudaSuccess)
+        e = launch_pdl(k_router_rows<1>, grid, dim3(256), router_rows_smem<1>(), st, x, Wr, T, H, E, KS, part);
+    } else if (T <= 8) {
       e = set_smem_once((const void*)k_router_rows<8>, router_rows_smem<8>(), dr8);
       if (e == cudaSuccess)
         e = launch_pdl(k_router_rows<8>, grid, dim3(256), router_rows_smem<8>(), st, x, Wr, T, H, E, KS, part);
