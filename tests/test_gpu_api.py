@@ -332,6 +332,32 @@ def test_flag_wait_times_out_and_context_survives():
     assert torch.equal(out2, r["out"])
 
 
+@pytest.mark.parametrize("E", [200, 202])
+@pytest.mark.parametrize("T", [1, 5, 16, 17, 32, 33, 100])
+def test_router_logits_every_kernel(T, E):
+    """Router logits through each kernel the split-K router picks by batch
+    size: the register-resident kernel for one token, for T <= 8, <= 16 and
+    <= 32, and the staged 64-token x 128-expert tile kernel above that.
+    E = 200 leaves the last 64- and 128-expert tiles ragged; E = 202 (rows
+    not a multiple of 16 bytes) takes the scalar-load kernel. Against the
+    fp64 product of the same bf16 x and fp32 W_r, and the allocation-free
+    entry point bit for bit."""
+    dev = cuda_device()
+    s = inputs.workload("tiny", T=T, H=1024, E=E)
+    cfg = m.make_config(s.H, s.I, s.E, s.k, T_max=128)
+    x = inputs.gen_x(s, 40 + T, device=dev)
+    Wr = inputs.gen_router(s, 40 + T, device=dev)
+    ws = torch.zeros(m.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    logits = torch.full((T, s.E), float("nan"), dtype=torch.float32, device=dev)
+    m.moe_router_logits(cfg, x, Wr, T, logits, ws)
+    got = torch.full((T, s.E), float("nan"), dtype=torch.float32, device=dev)
+    m.moe_router_logits_noalloc(cfg, x, Wr, T, got)
+    torch.cuda.synchronize()
+    ref = M.router_logits(np_(x.float()), np_(Wr))
+    np.testing.assert_allclose(np_(logits), ref, rtol=1e-4, atol=1e-5)
+    assert torch.equal(got, logits)
+
+
 def test_router_logits_large_batch():
     """Router logits at a batch whose 64-token x 128-expert tiles fill the
     SMs (the large-batch logits kernel, no split of H), ragged in tokens

@@ -175,6 +175,44 @@ def test_route_topk_exact_ties(T, E, k):
     assert m.moe_read_status(cfg, ws) == 0
 
 
+@pytest.mark.parametrize("E", [40, 300])
+def test_route_topk_special_values(E):
+    """Logits with signed zeros, infinities, the largest finite values and
+    subnormals (E = 300 keeps 10 logits a lane): -0 and +0 tie (the lower id
+    first), -inf ranks below every number, and ids and weights match the
+    oracle's rule."""
+    dev = cuda_device()
+    import quantized_grouped_gemm_topk_gb300 as m
+    T, k = 24, 8
+    s = inputs.workload("tiny", E=E, k=k)
+    cfg = m.config_from_shape(s, T_max=T)
+    ws = torch.zeros(m.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
+    g = torch.Generator(device="cpu")
+    g.manual_seed(23)
+    pool = torch.tensor([0.0, -0.0, float("-inf"), 3.4e38, -3.4e38, 1e-40, -1e-40, 1.0, -1.0, 2.5],
+                        dtype=torch.float32)
+    logits = pool[torch.randint(0, len(pool), (T, E), generator=g)]
+    logits[0] = -0.0                     # all tie: ids 0..k-1
+    logits[0, 5] = 0.0
+    logits[1] = float("-inf")            # all -inf: ids 0..k-1 as well
+    logits[2] = -0.0
+    logits[2, E - 1] = 1e-40             # one subnormal above the zeros
+    ids = torch.empty(T, k, dtype=torch.int32, device=dev)
+    w = torch.empty(T, k, dtype=torch.float32, device=dev)
+    m.moe_route_topk(cfg, logits.to(dev), T, ids, w, ws)
+    torch.cuda.synchronize()
+    with np.errstate(invalid="ignore"):          # the all--inf token's weights are 0/0
+        ref_ids, ref_w = M.topk_route(logits.numpy().astype(np.float64), k, 1.0)
+    got = np_(ids)
+    assert (got == ref_ids).all()
+    assert list(got[0]) == list(range(k))
+    assert list(got[1]) == list(range(k))
+    assert got[2][0] == E - 1 and list(got[2][1:]) == list(range(k - 1))
+    fin = np.isfinite(ref_w)
+    np.testing.assert_allclose(np_(w)[fin], ref_w[fin], rtol=1e-6, atol=0)
+    assert m.moe_read_status(cfg, ws) == 0
+
+
 @pytest.mark.parametrize("name", ["tiny", "train"])
 def test_geglu_forward(name):
     """GeGLU (GELU(gate) * up) through both GEMM paths: the NVFP4 decode GEMM
