@@ -109,7 +109,7 @@ static WsLayout ws_layout(const moe_config_t& c) {
     L.rexp1 = take((size_t)R * 4);
     L.rexp2 = take((size_t)R * 4);
     L.P2 = take((size_t)R * d.H * 4);
-    L.fcnt = take((size_t)tc_fused_counters(d.G, d.H) * 4);
+    L.fcnt = take((size_t)tc_fused_counters(d.G) * 4);
   } else {
     L.xg = take((size_t)R * d.H);
     L.xgs = take((size_t)sf4_bytes(d.H, R));
@@ -476,13 +476,10 @@ static int tc_splits(const moe_config_t& c, int T, int tiles, int K, int grid) {
   return std::max(1, std::min(S, 64));   // the GEMM stages at most 64 K-slice boundaries
 }
 
-constexpr int kFusedCombineMaxT = 4;   // 4 tokens x 32 column quads = the 128 epilogue threads
-
 struct TcRun {
   float* out;
   int64_t split_stride;
   int S;
-  bool combined = false;   // the fused layer's kernel wrote out (and z) itself
 };
 
 // The fused layer (NVFP4 weights, small decode batches: at most 2 rows per
@@ -630,8 +627,7 @@ static ActParams act_params(const moe_config_t* c) {
 // must be zero: the operand gather clears them). y1 (MXFP8) lands in y1q /
 // y1s; W2's fp32 K-slice partials in run2.
 static moe_status_t tc_fused(const moe_config_t* c, const moe_dispatch_t* d, int T, const void* packed, uint8_t* y1q,
-                             uint8_t* y1s, void* ws, cudaStream_t st, TcRun* run2, int n_disp, uint16_t* z,
-                             uint16_t* out) {
+                             uint8_t* y1s, void* ws, cudaStream_t st, TcRun* run2, int n_disp) {
   const WsLayout L = ws_layout(*c);
   const PackLayout P = pack_layout(*c, MOE_PACK_FORWARD);
   TcArgs g;
@@ -657,13 +653,6 @@ static moe_status_t tc_fused(const moe_config_t* c, const moe_dispatch_t* d, int
   g.f.xq = d->xq; g.f.xs = d->xs;
   g.f.row_map = d->perm_src; g.f.row_div = c->k + c->n_shared;
   g.f.a16 = at<uint16_t>(ws, L.a16); g.f.a_rowexp = at<int32_t>(ws, L.rexp1);
-  // the combine runs in the kernel when W2 is unsplit (each output tile then
-  // has one unit per group) and the tile's last unit has at most one
-  // (token, 4 columns) item per epilogue thread: with more, the work at the
-  // end of the kernel costs more than the combine launch it saves
-  g.f.combine = g.m[1].S == 1 && T <= kFusedCombineMaxT ? 1 : 0;
-  g.f.inv = d->inv; g.f.T = T; g.f.kp = c->k + c->n_shared;
-  g.f.out = out; g.f.z = z;
   const int64_t R = (int64_t)T * (c->k + c->n_shared);
   TcMaps maps;
   if (!make_tmaps_b(maps.m[0], at<uint16_t>(ws, L.a16), R, g.m[0].K) ||
@@ -673,7 +662,6 @@ static moe_status_t tc_fused(const moe_config_t* c, const moe_dispatch_t* d, int
   run2->out = g.m[1].out;
   run2->split_stride = g.m[1].split_stride;
   run2->S = g.m[1].S;
-  run2->combined = g.f.combine != 0;
   return MOE_OK;
 }
 
@@ -839,7 +827,7 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
   if (n_disp > 0 && n_disp >= mx_grid(*c)) return MOE_ERR_INVALID_ARG;   // no GEMM CTA would be left
   if (n_disp > 0) {
     a.zero = at<int32_t>(ws, L.fcnt);
-    a.nzero = tc_fused_counters(G, c->H);
+    a.nzero = tc_fused_counters(G);
   }
   phase(0, st);
   if (W_r) {
@@ -870,7 +858,7 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
     } else if (fused_layer(*c, T) && !save)
       MOE_CHECK_CUDA(launch_act_f16(v.d.xq, v.d.xs, c->H, v.d.perm_src, kp, T * kp, v.d.offsets, G,
                                     at<uint16_t>(ws, L.a16), at<int32_t>(ws, L.rexp1), st, at<int32_t>(ws, L.fcnt),
-                                    tc_fused_counters(G, c->H)));
+                                    tc_fused_counters(G)));
     else
       MOE_CHECK_CUDA(launch_act_f16(v.d.xq, v.d.xs, c->H, v.d.perm_src, kp, T * kp, v.d.offsets, G,
                                     at<uint16_t>(ws, L.a16), at<int32_t>(ws, L.rexp1), st));
@@ -890,12 +878,11 @@ moe_status_t moe_layer_forward(const moe_config_t* c, const uint16_t* x, const f
   }
   if (fused_layer(*c, T) && !save) {
     TcRun run;
-    if ((s = tc_fused(c, &v.d, T, packed_w, v.y1_q, v.y1_s, ws, st, &run, n_disp, v.z, out)) != MOE_OK) return s;
+    if ((s = tc_fused(c, &v.d, T, packed_w, v.y1_q, v.y1_s, ws, st, &run, n_disp)) != MOE_OK) return s;
     phase(2, st);
     phase(3, st);
     phase(4, st);
-    if (!run.combined)
-      MOE_CHECK_CUDA(launch_finalize_combine(run.out, run.S, run.split_stride, c->H, v.d.inv, T, kp, v.z, out, st));
+    MOE_CHECK_CUDA(launch_finalize_combine(run.out, run.S, run.split_stride, c->H, v.d.inv, T, kp, v.z, out, st));
     phase(5, st);
     return MOE_OK;
   }

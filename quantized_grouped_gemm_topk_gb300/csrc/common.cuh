@@ -260,42 +260,6 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// S8 for four adjacent columns n..n+3 of token t: each of the token's k'
-// slots (row r = inv[t k' + slot], skipped when negative) contributes its
-// row's sum over the S split-K slices of P (slice order), rounded to bf16
-// (written to z[r] when z is given); the slot terms are added in slot order
-// in fp32 and the sum rounded to bf16 into out[t]. kL2: read P through L2
-// only (rows written by other CTAs of the running kernel).
-template <bool kL2>
-__device__ __forceinline__ void combine_quad(const float* P, int S, int64_t ss, int N, const int32_t* inv,
-                                             int64_t t, int kp, uint16_t* z, uint16_t* out, int n) {
-  auto ld4 = [&](const float* a) {
-    if constexpr (kL2) return __ldcg(reinterpret_cast<const float4*>(a));
-    else return *reinterpret_cast<const float4*>(a);
-  };
-  auto bf2 = [](float a, float b) {
-    return (uint32_t)f32_to_bf16_bits(a) | ((uint32_t)f32_to_bf16_bits(b) << 16);
-  };
-  float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-  for (int j = 0; j < kp; ++j) {
-    const int r = inv[t * kp + j];
-    if (r < 0) continue;
-    const int64_t off = (int64_t)r * N + n;
-    float4 v = ld4(P + off);
-    for (int s = 1; s < S; ++s) {
-      const float4 w = ld4(P + (int64_t)s * ss + off);
-      v.x += w.x; v.y += w.y; v.z += w.z; v.w += w.w;
-    }
-    const uint32_t lo = bf2(v.x, v.y), hi = bf2(v.z, v.w);
-    if (z) *reinterpret_cast<uint2*>(z + off) = make_uint2(lo, hi);
-    o0 += __uint_as_float(lo << 16);
-    o1 += __uint_as_float(lo & 0xffff0000u);
-    o2 += __uint_as_float(hi << 16);
-    o3 += __uint_as_float(hi & 0xffff0000u);
-  }
-  *reinterpret_cast<uint2*>(out + t * N + n) = make_uint2(bf2(o0, o1), bf2(o2, o3));
-}
-
 // 16-byte cp.async into shared memory (L2 only); with ok false the
 // destination is zero-filled and nothing is read.
 __device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, bool ok) {

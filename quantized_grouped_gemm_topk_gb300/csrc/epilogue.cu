@@ -135,8 +135,23 @@ __global__ void __launch_bounds__(256) k_finalize_combine(const float* __restric
   const int nq = N / 4;
   const int64_t total = (int64_t)T * nq;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
-       idx += (int64_t)gridDim.x * blockDim.x)
-    combine_quad<false>(P, S, ss, N, inv, idx / nq, kp, z, out, (int)(idx % nq) * 4);
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t t = idx / nq;
+    const int n = (int)(idx % nq) * 4;
+    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+    for (int j = 0; j < kp; ++j) {
+      const int r = inv[t * kp + j];
+      if (r < 0) continue;
+      const float4 v = sum_splits4(P, S, ss, (int64_t)r * N + n);
+      const uint32_t lo = pack_bf16x2(v.x, v.y), hi = pack_bf16x2(v.z, v.w);
+      if (z) *reinterpret_cast<uint2*>(z + (int64_t)r * N + n) = make_uint2(lo, hi);
+      o0 += __uint_as_float(lo << 16);
+      o1 += __uint_as_float(lo & 0xffff0000u);
+      o2 += __uint_as_float(hi << 16);
+      o3 += __uint_as_float(hi & 0xffff0000u);
+    }
+    *reinterpret_cast<uint2*>(out + t * N + n) = make_uint2(pack_bf16x2(o0, o1), pack_bf16x2(o2, o3));
+  }
 }
 
 cudaError_t launch_finalize_combine(const float* P, int S, int64_t ss, int N, const int32_t* inv, int T, int kp,

@@ -312,49 +312,6 @@ __device__ __noinline__ void fused_w2_rows(const TcArgs& g, const TcUnit& w, int
   }
 }
 
-// Fused combine of output tile j (columns 128 j .. 128 j + 127 of H) over
-// every token, by the four epilogue warps of the CTA whose W2 unit finished
-// the tile last (the other units' rows were published by their release). A
-// thread takes four columns of a token and requests all of its slots' rows
-// before adding any, so an item costs two memory round trips (the slot's
-// row, then its values); the sums are those of combine_quad with one split.
-__device__ __noinline__ void fused_combine_tile(const TcArgs& g, int j, int q, int lane) {
-  const TcFused& f = g.f;
-  const TcMat& M = g.m[1];
-  const int N = M.N;
-  const int n0 = kTileN * j;
-  const int nq = min(kTileN, N - n0) / 4;
-  for (int idx = q * 32 + lane; idx < f.T * nq; idx += 128) {
-    const int64_t t = idx / nq;
-    const int n = n0 + (idx % nq) * 4;
-    float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-    for (int j0 = 0; j0 < f.kp; j0 += 8) {
-      int r[8];
-      float4 v[8];
-#pragma unroll
-      for (int b = 0; b < 8; ++b) r[b] = j0 + b < f.kp ? f.inv[t * f.kp + j0 + b] : -1;
-#pragma unroll
-      for (int b = 0; b < 8; ++b)
-        v[b] = r[b] >= 0 ? __ldcg(reinterpret_cast<const float4*>(M.out + (int64_t)r[b] * N + n))
-                         : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        if (r[b] < 0) continue;
-        const uint32_t lo = (uint32_t)f32_to_bf16_bits(v[b].x) | ((uint32_t)f32_to_bf16_bits(v[b].y) << 16);
-        const uint32_t hi = (uint32_t)f32_to_bf16_bits(v[b].z) | ((uint32_t)f32_to_bf16_bits(v[b].w) << 16);
-        if (f.z) *reinterpret_cast<uint2*>(f.z + (int64_t)r[b] * N + n) = make_uint2(lo, hi);
-        o0 += __uint_as_float(lo << 16);
-        o1 += __uint_as_float(lo & 0xffff0000u);
-        o2 += __uint_as_float(hi << 16);
-        o3 += __uint_as_float(hi & 0xffff0000u);
-      }
-    }
-    const uint32_t a = (uint32_t)f32_to_bf16_bits(o0) | ((uint32_t)f32_to_bf16_bits(o1) << 16);
-    const uint32_t b = (uint32_t)f32_to_bf16_bits(o2) | ((uint32_t)f32_to_bf16_bits(o3) << 16);
-    *reinterpret_cast<uint2*>(f.out + t * N + n) = make_uint2(a, b);
-  }
-}
-
 __device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -933,18 +890,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) k_gemm_tc(const __grid_constant
           epi_sync();
           if (warp == kWEpi && lane == 0) st_release_gpu(cnt + g.G + w.e, 1);
         }
-      }
-      if constexpr (NT == 16) if (it.mat == 1 && g.f.combine) {
-        // Fused combine (W2 unsplit, so every unit of the walk is one of
-        // the vgroups that write output tile w.j): the same barrier and
-        // release / acquire hand-off as above; the tile's last unit sums
-        // its columns over all tokens.
-        if (!epi_all(ok)) { ok = false; break; }
-        epi_sync();
-        if (warp == kWEpi && lane == 0)
-          epi_last = atom_add_acq_rel_gpu(g.f.cnt + 3 * g.G + w.j, 1) == vgroups - 1;
-        epi_sync();
-        if (epi_last) fused_combine_tile(g, w.j, q, lane);
       }
     }
   }

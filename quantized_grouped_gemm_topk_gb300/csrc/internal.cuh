@@ -139,8 +139,7 @@ struct TcFused {
   uint8_t* y1q; uint8_t* y1s; // [R][I], [R][I / 32]
   uint16_t* y16;              // [R][I]
   int32_t* y_rowexp;          // [R]
-  int32_t* cnt;               // [G] W1 tiles done, [G] ready flags, [G] ring flags, [ceil(H / 128)] W2
-                              // units done per output tile; zero on entry
+  int32_t* cnt;               // [G] W1 tiles done, [G] ready flags, [G] ring flags; zero on entry
   const float* b1;            // [G][2I] W1 bias (gate then up), nullable
   // Partitioned layer: CTAs [0, n_disp) fill the token ring (the f16 W1
   // operand rows a16 and their exponents, gathered from the dispatched MXFP8
@@ -151,14 +150,6 @@ struct TcFused {
   const uint8_t* xq; const uint8_t* xs;
   const int32_t* row_map; int row_div;
   uint16_t* a16; int32_t* a_rowexp;
-  // Fused combine (W2 unsplit, S = 1): the last W2 unit to finish an output
-  // tile of 128 columns sums every token's rows of that tile into out
-  // [T][H] (and the rows' bf16 values into z [R][H], nullable), as the
-  // combine kernel would; combine = 0 leaves the fp32 W2 rows to that
-  // kernel.
-  int combine;
-  const int32_t* inv; int T; int kp;
-  uint16_t* out; uint16_t* z;
 };
 struct TcArgs {
   TcMat m[2];                 // m[0]: the (first) matrix; m[1]: W2 of the fused layer
@@ -179,7 +170,7 @@ struct TcArgs {
 // I / 256 code words of a row in registers).
 constexpr int kFusedMaxI = 2048;
 // Ints of the fused layer's counters for G groups.
-inline int64_t tc_fused_counters(int G, int H) { return 3LL * G + (H + 127) / 128; }
+inline int64_t tc_fused_counters(int G) { return 3LL * G; }
 constexpr int kTcBoxes = 5;   // activation boxes of 8, 16, 32, 64, 128 rows
 // Tensor maps of the f16 operand rows a16 [rows, cols], viewed as
 // (64 columns, rows, cols / 64 chunks): m[i] loads a box of 8 << i rows of
