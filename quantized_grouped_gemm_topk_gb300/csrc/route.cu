@@ -768,6 +768,68 @@ __global__ void __launch_bounds__(256) k_quant_rows_bf16(const uint16_t* __restr
   for (int64_t i = wid; i < total; i += nw) quant_group_bf16(src, i / groups, C, (int)(i % groups), q, s, lane);
 }
 
+// S3-S4 for at most 32 assignments (a one-token batch, or T * k' <= 32),
+// without histograms or scans: warp 0 holds one assignment a lane (its
+// group, weight, how many assignments share the group, whether it is the
+// group's first), and every thread of the block derives its groups' count,
+// offset, padded offset and place in the touched list by one pass over
+// those <= 32 entries. The rank of an assignment in its group is the number
+// of lower lanes holding the same group, so the row order is the stable
+// flat order the general path produces; every output equals that path's.
+__device__ void route_tiny(int n, const int32_t* ids, const float* wts, int k, int kp, int E, int G,
+                           int32_t* counts, int32_t* offsets, int32_t* touched, int32_t* n_touched, int32_t* poff,
+                           int32_t* perm, int32_t* inv, float* w_row, int32_t* status) {
+  __shared__ int32_t te[kWarp], tcnt[kWarp], tfirst[kWarp];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int e = -2;
+  float wt = 0.f;
+  unsigned m = 0;
+  if (warp == 0) {
+    if (lane < n) {
+      const int t = lane / kp, j = lane % kp;
+      e = assignment_expert(ids, t, j, k, E);
+      wt = j < k ? wts[(int64_t)t * k + j] : 1.0f;
+    }
+    if (__any_sync(kFull, e == -1) && lane == 0) set_status(status, MOE_DEV_BAD_EXPERT_ID);
+    m = __match_any_sync(kFull, e);
+    te[lane] = e;
+    tcnt[lane] = __popc(m);
+    tfirst[lane] = e >= 0 && (m & ((1u << lane) - 1u)) == 0;
+  }
+  __syncthreads();
+  for (int g = threadIdx.x; g <= G; g += blockDim.x) {
+    int cnt = 0, off = 0, pof = 0, tix = 0;
+    for (int b = 0; b < n; ++b) {
+      const int eb = te[b];
+      if (eb < 0) continue;
+      if (eb == g) ++cnt;
+      if (eb < g) {
+        ++off;
+        if (tfirst[b]) { pof += (tcnt[b] + kPadRows - 1) / kPadRows * kPadRows; ++tix; }
+      }
+    }
+    offsets[g] = off;
+    if (poff) poff[g] = pof;
+    if (g < G) {
+      counts[g] = cnt;
+      if (cnt > 0) touched[tix] = g;
+    } else {
+      *n_touched = tix;
+    }
+  }
+  if (warp == 0 && lane < n) {
+    if (e >= 0) {
+      int r = __popc(m & ((1u << lane) - 1u));
+      for (int b = 0; b < n; ++b) r += te[b] >= 0 && te[b] < e;
+      perm[r] = lane;
+      inv[lane] = r;
+      w_row[r] = wt;
+    } else {
+      inv[lane] = -1;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Small-T fused path: block 0 sums the router partials (all threads), routes
 // every token (warp per token), histograms, scans and scatters; blocks 1..
@@ -850,9 +912,13 @@ __global__ void __launch_bounds__(1024, 1) k_route_small(const float* __restrict
     }
   }
   __syncthreads();   // ids / wts written by this block are visible block-wide
+  const int n = T * kp;
+  if (n <= kWarp) {
+    route_tiny(n, ids, wts, k, kp, E, G, counts, offsets, touched, n_touched, poff, perm, inv, w_row, status);
+    return;
+  }
   // per-warp segment counts (atomic-free, see warp_count); the histogram is
   // their sum in warp order
-  const int n = T * kp;
   const int seg = ((n + 31) / 32 + 31) / 32 * 32;
   const int a0 = min(n, warp * seg), a1 = min(n, a0 + seg);
   int32_t* wcw = wc + warp * G;
