@@ -161,13 +161,15 @@ def test_cuda_graph_replay_matches_eager(nd):
         assert torch.equal(out_static, ref)
 
 
-def test_bad_expert_ids_flag_status():
+@pytest.mark.parametrize("T", [8, 40])
+def test_bad_expert_ids_flag_status(T):
     """Out-of-range expert ids set MOE_DEV_BAD_EXPERT_ID, their slots are
     skipped (inv = -1), nothing is written past the valid rows, and every
-    output buffer's canary bands are untouched."""
+    output buffer's canary bands are untouched. T = 8 (16 assignments) takes
+    the routing kernel's direct path for at most 32 assignments, T = 40 its
+    histogram and scan path."""
     dev = cuda_device()
     s = inputs.workload("tiny")
-    T = 8
     cfg = m.config_from_shape(s, T_max=T)
     ws = torch.zeros(m.moe_workspace_size(cfg), dtype=torch.uint8, device=dev)
     x = inputs.gen_x(s, 0, device=dev, T=T)
