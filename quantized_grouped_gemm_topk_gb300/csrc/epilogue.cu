@@ -128,6 +128,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   return (uint32_t)f32_to_bf16_bits(a) | ((uint32_t)f32_to_bf16_bits(b) << 16);
 }
 
+// One thread per (token, 4 columns): its slots' row indices, then every
+// slot's row values, are requested eight slots at a time before any is used
+// (two memory round trips a batch instead of two a slot); the sums are the
+// ones below in the same order: each row's splits in s order, the slots'
+// bf16-rounded rows in slot order.
 __global__ void __launch_bounds__(256) k_finalize_combine(const float* __restrict__ P, int S, int64_t ss, int N,
                                                           const int32_t* __restrict__ inv, int T, int kp,
                                                           uint16_t* __restrict__ z, uint16_t* __restrict__ out) {
@@ -139,16 +144,32 @@ __global__ void __launch_bounds__(256) k_finalize_combine(const float* __restric
     const int64_t t = idx / nq;
     const int n = (int)(idx % nq) * 4;
     float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
-    for (int j = 0; j < kp; ++j) {
-      const int r = inv[t * kp + j];
-      if (r < 0) continue;
-      const float4 v = sum_splits4(P, S, ss, (int64_t)r * N + n);
-      const uint32_t lo = pack_bf16x2(v.x, v.y), hi = pack_bf16x2(v.z, v.w);
-      if (z) *reinterpret_cast<uint2*>(z + (int64_t)r * N + n) = make_uint2(lo, hi);
-      o0 += __uint_as_float(lo << 16);
-      o1 += __uint_as_float(lo & 0xffff0000u);
-      o2 += __uint_as_float(hi << 16);
-      o3 += __uint_as_float(hi & 0xffff0000u);
+    for (int j0 = 0; j0 < kp; j0 += 8) {
+      int r[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) r[b] = j0 + b < kp ? inv[t * kp + j0 + b] : -1;
+      float4 v[8];
+#pragma unroll
+      for (int b = 0; b < 8; ++b)
+        v[b] = r[b] >= 0 ? *reinterpret_cast<const float4*>(P + (int64_t)r[b] * N + n) : make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int sp = 1; sp < S; ++sp) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+          if (r[b] < 0) continue;
+          const float4 w = *reinterpret_cast<const float4*>(P + (int64_t)sp * ss + (int64_t)r[b] * N + n);
+          v[b].x += w.x; v[b].y += w.y; v[b].z += w.z; v[b].w += w.w;
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        if (r[b] < 0) continue;
+        const uint32_t lo = pack_bf16x2(v[b].x, v[b].y), hi = pack_bf16x2(v[b].z, v[b].w);
+        if (z) *reinterpret_cast<uint2*>(z + (int64_t)r[b] * N + n) = make_uint2(lo, hi);
+        o0 += __uint_as_float(lo << 16);
+        o1 += __uint_as_float(lo & 0xffff0000u);
+        o2 += __uint_as_float(hi << 16);
+        o3 += __uint_as_float(hi & 0xffff0000u);
+      }
     }
     *reinterpret_cast<uint2*>(out + t * N + n) = make_uint2(pack_bf16x2(o0, o1), pack_bf16x2(o2, o3));
   }
