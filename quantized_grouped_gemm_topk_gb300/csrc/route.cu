@@ -18,7 +18,9 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// S1: logits partials, a register-tiled fp32 GEMM over one slice of H.
+// S1: logits partials, a register-tiled fp32 GEMM over one slice of H
+// (the general kernel; the decode-size and mid-batch kernels below take
+// every shape whose expert count is a multiple of 4).
 // grid (ceil(T/TT), ceil(E/64), KS), block 256: thread (tx = tid % 16,
 // ty = tid / 16) owns experts 4tx..4tx+3 and tokens ty*TT/16.. of the
 // CTA's 64-expert x TT-token tile. The slice [h0, h1) (multiples of 8 rows)
@@ -335,29 +337,6 @@ __global__ void __launch_bounds__(256) k_router_big(const uint16_t* __restrict__
   }
 }
 
-// ---------------------------------------------------------------------------
-// S2: one warp routes one token. Logits are first summed over the KS
-// partials in ks order and written out (or taken as given from row_src);
-// then k rounds of a warp arg-max on (value desc, id asc). NaN logits rank
-// below every number and raise MOE_DEV_NAN_LOGIT. Weights: softmax over the
-// selected logits x scale.
-//
-// The arg-max runs on order-preserving integer keys: a larger logit has a
-// larger key, -0 and +0 share one (they compare equal), and -inf (NaN) is
-// above 0, the key of an expert that is taken or out of range. Each lane
-// keeps its best untaken expert (the lowest id among equal keys: its ids
-// grow with i), the warp's largest key comes from one redux.sync max, and
-// the lowest id holding it from one redux.sync min, so a round costs two
-// warp reductions instead of five shuffle-and-compare steps.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t logit_key(float v) {
-  const uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_logit(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
 // S1 between the two (T > 32, E a multiple of 4, too few 64 x 128 tiles to
 // fill the SMs): the same tile and thread layout as k_router_big, split
 // along H into KS slices of whole 16-row stages (part[ks][t][e]), with both
@@ -449,6 +428,29 @@ __global__ void __launch_bounds__(256) k_router_mid(const uint16_t* __restrict__
     if (e0 + 64 + tx * 4 < E)
       *reinterpret_cast<float4*>(row + e0 + 64 + tx * 4) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
   }
+}
+
+// ---------------------------------------------------------------------------
+// S2: one warp routes one token. Logits are first summed over the KS
+// partials in ks order and written out (or taken as given from row_src);
+// then k rounds of a warp arg-max on (value desc, id asc). NaN logits rank
+// below every number and raise MOE_DEV_NAN_LOGIT. Weights: softmax over the
+// selected logits x scale.
+//
+// The arg-max runs on order-preserving integer keys: a larger logit has a
+// larger key, -0 and +0 share one (they compare equal), and -inf (NaN) is
+// above 0, the key of an expert that is taken or out of range. Each lane
+// keeps its best untaken expert (the lowest id among equal keys: its ids
+// grow with i), the warp's largest key comes from one redux.sync max, and
+// the lowest id holding it from one redux.sync min, so a round costs two
+// warp reductions instead of five shuffle-and-compare steps.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t logit_key(float v) {
+  const uint32_t u = __float_as_uint(v == 0.f ? 0.f : v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_logit(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 // Sum over ks of part[ks * n + i], in ks order, 16 loads in flight at a
