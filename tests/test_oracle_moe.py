@@ -111,6 +111,33 @@ def test_topk_brute_force_subsets_and_ties():
         assert [e for _, e in best] == list(ids[0])
 
 
+def test_topk_special_values_brute_force():
+    """Signed zeros, infinities and subnormals: -0 and +0 compare equal (the
+    lower id wins the tie), -inf ranks below every finite number, and the
+    selection is the brute-force best (value desc, id asc) subset; a token
+    whose selected logits are all -inf has undefined (NaN) weights, every
+    other token's weights sum to the routed scale."""
+    rng = np.random.default_rng(5)
+    pool = np.array([0.0, -0.0, -np.inf, 3.4e38, -3.4e38, 1e-310, -1e-310, 1.0, -1.0])
+    for trial in range(300):
+        E = int(rng.integers(2, 7))
+        k = int(rng.integers(1, E + 1))
+        lg = pool[rng.integers(0, len(pool), size=(1, E))]
+        with np.errstate(invalid="ignore"):
+            ids, w = M.topk_route(lg, k, 2.0)
+        best = None
+        for sub in itertools.combinations(range(E), k):
+            key = sorted(((-lg[0, e], e) for e in sub))
+            if best is None or key < best:
+                best = key
+        assert [e for _, e in best] == list(ids[0])
+        if np.isfinite(lg[0, ids[0]]).any():
+            assert abs(w[0].sum() - 2.0) < 1e-12
+    # all zeros of either sign: ids in order
+    ids, _ = M.topk_route(np.array([[-0.0, 0.0, -0.0, 0.0]]), 3)
+    assert list(ids[0]) == [0, 1, 2]
+
+
 # ---- dispatch --------------------------------------------------------------
 @pytest.mark.parametrize("T,E,k,S", [(0, 4, 2, 0), (1, 8, 2, 0), (37, 8, 3, 0), (64, 33, 8, 1), (200, 5, 5, 0)])
 def test_dispatch_invariants(T, E, k, S):
